@@ -1,0 +1,386 @@
+"""Float64 oracle of one Epoch MoE-layer refinement iteration (test infrastructure).
+
+Only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline/reference legs
+may import this module. It shares no code with the CUDA library.
+
+Source pages (cited by title and section; the walk-through is the method source):
+  [W] "Epoch 完全拆解:把扩散块编译成稀疏 MoE 服务单元" (pinghaoyang.com.cn walk-through)
+  [A] "Epoch: Compiling Diffusion Blocks for Sparse MoE Serving" (abstract page)
+
+What one iteration computes, in the pages' notation:
+  * MoE layer:  y_t = sum_{e in TopK(g(x_t))} w_{t,e} E_e(x_t)
+        [W] section "MoE 路径为什么成为瓶颈" (why the MoE path is the bottleneck), layer equation.
+  * Router logits G in R^{N x E} for every position, recomputed every iteration
+        [W] section "Expert Atlas", definition of G; [A] abstract ("recomputing gate logits every iteration").
+  * Top-k restricted to the block's active expert support S_l (a mask over
+    experts; ids, order and weights of a token's selection may change each
+    iteration)
+        [W] section "Expert Atlas", third step (hot path reuses the support mask), Figure 7.
+  * Fresh set: with D_i the decoded set, Z_i = D_i ∩ D_{i-1} (stable),
+    N_i = D_i \\ D_{i-1} (newly decoded); F_i = all positions on a cache miss or
+    refresh, otherwise the complement of Z_i; a newly decoded position is fresh once
+        [W] section "Liveness-Shard Parallelism", equations for Z_i, N_i and F_i.
+  * B_i = Compact(H, F_i); Y_F = SparseMoE(B_i, S_l); Y[F_i] = Y_F; Y[not F_i] = C_l[not F_i]
+    where C_l caches the routed-expert output (not the layer output, not hidden)
+        [W] section "Liveness-Shard Parallelism", the four merge equations.
+  * Cached rows have bounded age; refresh period 1 makes the decoded branch exact
+        [W] section "decoded-cache 的刷新周期为什么默认取 5" (refresh period), age bound.
+  * Any cache miss, version/shape mismatch or liveness-transition anomaly falls
+    back to the full fresh path
+        [W] sections "Two Clocks" and "cold、hot-update、hot-skip" (lifecycle).
+  * The worklist of (token, expert) pairs is grouped by expert and each expert
+    runs once over its rows ("light-traffic expert kernel"); the combine returns
+    rows by compact offset and the scatter/merge restores the dense shard
+        [W] section "FreshLane Dispatch", steps 1-6.
+  * The shared expert is untouched by the liveness split and runs on all positions
+        [W] section "Liveness-Shard Parallelism" (closing paragraph).
+
+Readings taken where the pages are silent:
+  * support: experts ranked by block-start dense top-k hit count (count desc,
+    id asc); the support is the smallest prefix whose counts reach
+    T = ceil(tau * N * k), at least k experts; tau >= 1 means every expert;
+  * selection uses raw logits (bias included); ties go to the lower expert id;
+    weights are a softmax over the k selected logits (they sum to 1);
+  * refresh: a decoded position is stale when i - stamp >= R (R = None: never);
+  * the expert is SwiGLU: E(x) = W_down (silu(W_gate x) * (W_up x)), silu(z) = z / (1 + e^-z);
+  * a position flagged both live and decoded, or neither, is treated as live;
+    a decoded -> live transition is an anomaly that makes the whole iteration
+    full-fresh with every expert eligible;
+  * optional residual: y = x + routed + shared (used to chain a layer stack).
+
+Parity pins (tests/test_oracle_pins.py): brute-force top-k over all k-subsets,
+minimal-cardinality support by brute force over expert subsets, hand-worked
+fresh-set schedules (tests/golden/), closed-form silu values, the dense-MoE
+special case (tau = 1, R = 1) against an all-experts masked formulation, and the
+cache/staleness invariants. Outputs after many iterations with reused rows are
+pinned only through those invariants.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Callable, List, Optional, Sequence, Tuple
+
+import numpy as np
+
+ExpertWeights = Tuple[np.ndarray, np.ndarray, np.ndarray]   # (W_gate [I,H], W_up [I,H], W_down [H,I])
+
+
+# ------------------------------------------------------------------ expert math
+
+def silu(z: np.ndarray) -> np.ndarray:
+    """silu(z) = z * sigmoid(z) = z / (1 + exp(-z))."""
+    return z / (1.0 + np.exp(-z))
+
+
+def swiglu_expert(X: np.ndarray, w: ExpertWeights) -> np.ndarray:
+    """E(x) = W_down (silu(W_gate x) * (W_up x)) for every row x of X."""
+    wg, wu, wd = w
+    return (silu(X @ wg.T) * (X @ wu.T)) @ wd.T
+
+
+# ------------------------------------------------------------------ routing
+
+def gate_logits(x: np.ndarray, w_router: np.ndarray, b_router: np.ndarray) -> np.ndarray:
+    """G = x W_r^T + b, one row per position ([W] "Expert Atlas", G in R^{N x E})."""
+    return x @ w_router.T + b_router[None, :]
+
+
+def rank_eligible(g_row: np.ndarray, eligible: np.ndarray) -> np.ndarray:
+    """Eligible expert ids ordered by logit descending, lower id first on equal logits."""
+    ids = np.nonzero(eligible)[0]
+    order = np.lexsort((ids, -g_row[ids]))
+    return ids[order]
+
+
+def topk_select(g_row: np.ndarray, eligible: np.ndarray, k: int) -> np.ndarray:
+    """The k experts a token selects among the eligible ones, in selection order."""
+    return rank_eligible(g_row, eligible)[:k]
+
+
+def renorm_softmax(g_sel: np.ndarray) -> np.ndarray:
+    """w_j = exp(g_j) / sum_m exp(g_m) over the selected logits only."""
+    m = np.max(g_sel)
+    ex = np.exp(g_sel - m)
+    return ex / np.sum(ex)
+
+
+def near_tie(g_row: np.ndarray, eligible: np.ndarray, k: int, eps: float = 1e-5) -> bool:
+    """True when two of the k+1 best eligible logits are within eps of each other,
+    so that a rounding difference could change the selection or its order."""
+    ranked = rank_eligible(g_row, eligible)[: k + 1]
+    vals = g_row[ranked]
+    return bool(np.any(np.abs(np.diff(vals)) <= eps))
+
+
+# ------------------------------------------------------------------ block plan
+
+def hit_counts(G: np.ndarray, k: int) -> np.ndarray:
+    """cnt[e] = number of positions whose dense top-k (all experts eligible) contains e."""
+    N, E = G.shape
+    everyone = np.ones(E, dtype=bool)
+    cnt = np.zeros(E, dtype=np.int64)
+    for t in range(N):
+        for e in topk_select(G[t], everyone, k):
+            cnt[e] += 1
+    return cnt
+
+
+def coverage_threshold(tau: float, n_pos: int, k: int) -> int:
+    """T = ceil(tau * N * k) edges, evaluated in float64."""
+    return int(math.ceil(tau * float(n_pos * k)))
+
+
+def plan_support(cnt: np.ndarray, k: int, tau: float, n_pos: int) -> Tuple[np.ndarray, int]:
+    """Experts ranked by (count desc, id asc) and the support length |S|.
+
+    |S| is the smallest prefix length whose counts reach T = ceil(tau N k),
+    raised to at least k (so every token can still pick k experts); tau >= 1
+    keeps every expert, zero-count ones included.
+    """
+    E = cnt.shape[0]
+    ranked = np.array(sorted(range(E), key=lambda e: (-int(cnt[e]), e)), dtype=np.int64)
+    if tau >= 1.0:
+        return ranked, E
+    T = coverage_threshold(tau, n_pos, k)
+    covered, j = 0, 0
+    while j < E and covered < T:
+        covered += int(cnt[ranked[j]])
+        j += 1
+    return ranked, min(max(j, k), E)
+
+
+# ------------------------------------------------------------------ liveness
+
+@dataclasses.dataclass
+class Classified:
+    fresh: np.ndarray        # bool [N]
+    is_live: np.ndarray      # bool [N] (both/neither flags count as live)
+    anomaly: bool            # a decoded -> live transition was seen
+    bad_flags: int           # positions flagged both live and decoded, or neither
+    n_live: int
+    n_new: int
+    n_miss: int
+    n_stale: int
+    n_forced: int            # would have been reused, made fresh by a fallback
+    n_reuse: int
+
+
+def classify_positions(live: np.ndarray, decoded: np.ndarray, prev_decoded: np.ndarray,
+                       stamp: np.ndarray, i: int, refresh_R: Optional[int],
+                       force_all: bool) -> Classified:
+    """Fresh set of iteration i ([W] "Liveness-Shard Parallelism", F_i).
+
+    live: still Mask; new: in D_i but not D_{i-1}; miss: decoded without a cached
+    row; stale: cached row at least R iterations old. Every other decoded
+    position is in Z_i and reuses its cached row, unless the iteration falls back
+    to full fresh (a host-side mismatch, or a decoded -> live transition).
+    """
+    N = live.shape[0]
+    lv = np.asarray(live, dtype=bool)
+    dc = np.asarray(decoded, dtype=bool)
+    is_live = lv | ~dc
+    bad = int(np.sum(lv == dc))
+    anomaly = bool(np.any(prev_decoded[:N].astype(bool) & is_live))
+    force = force_all or anomaly
+    fresh = np.zeros(N, dtype=bool)
+    n = dict(live=0, new=0, miss=0, stale=0, forced=0, reuse=0)
+    for t in range(N):
+        if is_live[t]:
+            cat = "live"
+        elif not prev_decoded[t]:
+            cat = "new"
+        elif stamp[t] < 0:
+            cat = "miss"
+        elif refresh_R is not None and i - int(stamp[t]) >= refresh_R:
+            cat = "stale"
+        else:
+            cat = "forced" if force else "reuse"
+        n[cat] += 1
+        fresh[t] = cat != "reuse"
+    return Classified(fresh, is_live, anomaly, bad, n["live"], n["new"], n["miss"],
+                      n["stale"], n["forced"], n["reuse"])
+
+
+# ------------------------------------------------------------------ results
+
+@dataclasses.dataclass
+class PlanResult:
+    G: np.ndarray
+    counts: np.ndarray
+    ranked: np.ndarray
+    support_len: int
+    threshold: int
+
+    @property
+    def support(self) -> np.ndarray:
+        return self.ranked[: self.support_len]
+
+
+@dataclasses.dataclass
+class IterResult:
+    y: np.ndarray                 # [N, H]
+    G: np.ndarray                 # [N, E]
+    fresh_pos: np.ndarray         # ascending positions in F_i
+    sel: np.ndarray               # [|F|, k] selected experts, selection order
+    w: np.ndarray                 # [|F|, k] weights
+    wl_expert: np.ndarray         # worklist edges sorted by (expert, position)
+    wl_pos: np.ndarray
+    wl_j: np.ndarray              # which of the token's k selections the edge is
+    offsets: np.ndarray           # [E+1] edge offsets per expert
+    routed: np.ndarray            # [N, H] routed-expert output (fresh or cached)
+    fallback: bool
+    host_fallback: bool
+    classified: Classified
+
+    @property
+    def n_edges(self) -> int:
+        return int(self.wl_pos.shape[0])
+
+
+# ------------------------------------------------------------------ the layer
+
+class LayerOracle:
+    """One MoE layer with its block plan, per-position cache and stamps.
+
+    ``expert(e)`` returns routed expert e's float64 weights; ``shared`` lists the
+    always-on shared experts. State arrays are sized ``max_positions``.
+    """
+
+    def __init__(self, *, n_experts: int, top_k: int, tau: float, refresh_R: Optional[int],
+                 w_router: np.ndarray, b_router: np.ndarray,
+                 expert: Callable[[int], ExpertWeights],
+                 shared: Sequence[ExpertWeights] = (), residual: bool = False,
+                 max_positions: int):
+        self.E = n_experts
+        self.k = top_k
+        self.tau = tau
+        self.R = refresh_R
+        self.w_router = w_router
+        self.b_router = b_router
+        self.expert = expert
+        self.shared = list(shared)
+        self.residual = residual
+        self.H = w_router.shape[1]
+        self.max_positions = max_positions
+        self.stamp = -np.ones(max_positions, dtype=np.int64)
+        self.prev_decoded = np.zeros(max_positions, dtype=bool)
+        self.cache = np.zeros((max_positions, self.H))
+        self.planned = False
+        self.n_pos = 0
+        self.last_iter = -1
+        self.support_mask = np.ones(self.E, dtype=bool)
+        self.plan: Optional[PlanResult] = None
+
+    # cold path ([W] "cold、hot-update、hot-skip": clear the per-block cache,
+    # initialise the live set, build the support of each layer)
+    def plan_block(self, x: np.ndarray) -> PlanResult:
+        N = x.shape[0]
+        G = gate_logits(x, self.w_router, self.b_router)
+        cnt = hit_counts(G, self.k)
+        ranked, slen = plan_support(cnt, self.k, self.tau, N)
+        self.plan = PlanResult(G, cnt, ranked, slen, coverage_threshold(self.tau, N, self.k))
+        self.support_mask = np.zeros(self.E, dtype=bool)
+        self.support_mask[ranked[:slen]] = True
+        self.stamp[:] = -1
+        self.prev_decoded[:] = False
+        self.cache[:] = 0.0
+        self.planned = True
+        self.n_pos = N
+        self.last_iter = -1
+        return self.plan
+
+    def adopt_support(self, ranked: np.ndarray, slen: int) -> None:
+        """Replace the plan's support (used after a logged near-tie at plan time)."""
+        self.support_mask = np.zeros(self.E, dtype=bool)
+        self.support_mask[np.asarray(ranked[:slen], dtype=np.int64)] = True
+
+    def block_end(self) -> None:
+        self.planned = False
+
+    def iterate(self, x: np.ndarray, live: np.ndarray, decoded: np.ndarray, i: int,
+                adopt: Optional[Callable[[int, np.ndarray], Optional[np.ndarray]]] = None
+                ) -> IterResult:
+        """One refinement iteration. ``adopt(t, sel)`` may return a replacement
+        selection for position t (the parity harness uses it after a logged near-tie)."""
+        N = x.shape[0]
+        host_fallback = (not self.planned) or (i != self.last_iter + 1) or (N != self.n_pos)
+        G = gate_logits(x, self.w_router, self.b_router)
+        cl = classify_positions(live, decoded, self.prev_decoded, self.stamp, i, self.R, host_fallback)
+        fallback = host_fallback or cl.anomaly
+        eligible = np.ones(self.E, dtype=bool) if fallback else self.support_mask
+
+        fresh_pos = np.nonzero(cl.fresh)[0]
+        F = fresh_pos.shape[0]
+        sel = np.zeros((F, self.k), dtype=np.int64)
+        w = np.zeros((F, self.k))
+        for f, t in enumerate(fresh_pos):
+            s = topk_select(G[t], eligible, self.k)
+            if adopt is not None:
+                repl = adopt(int(t), s)
+                if repl is not None:
+                    s = np.asarray(repl, dtype=np.int64)
+            sel[f] = s
+            w[f] = renorm_softmax(G[t, s])
+
+        # worklist: every (position, selection) edge, grouped by expert, positions ascending
+        edges = sorted(((int(sel[f, j]), int(fresh_pos[f]), j, f)
+                        for f in range(F) for j in range(self.k)))
+        wl_expert = np.array([e for e, _, _, _ in edges], dtype=np.int64)
+        wl_pos = np.array([t for _, t, _, _ in edges], dtype=np.int64)
+        wl_j = np.array([j for _, _, j, _ in edges], dtype=np.int64)
+        wl_f = np.array([f for _, _, _, f in edges], dtype=np.int64)
+        offsets = np.zeros(self.E + 1, dtype=np.int64)
+        for e in wl_expert:
+            offsets[e + 1] += 1
+        offsets = np.cumsum(offsets)
+
+        # each expert runs once over its rows
+        out = np.zeros((len(edges), self.H))
+        for e in range(self.E):
+            lo, hi = offsets[e], offsets[e + 1]
+            if hi > lo:
+                out[lo:hi] = swiglu_expert(x[wl_pos[lo:hi]], self.expert(e))
+        slot = np.zeros((F, self.k), dtype=np.int64)
+        slot[wl_f, wl_j] = np.arange(len(edges))
+
+        # combine (selection order) + cache fill for fresh rows; cached rows elsewhere
+        routed = np.zeros((N, self.H))
+        for f, t in enumerate(fresh_pos):
+            acc = np.zeros(self.H)
+            for j in range(self.k):
+                acc = acc + w[f, j] * out[slot[f, j]]
+            routed[t] = acc
+            self.cache[t] = acc
+            self.stamp[t] = i
+        reuse = ~cl.fresh
+        routed[reuse] = self.cache[:N][reuse]
+
+        y = routed.copy()
+        for sw in self.shared:
+            y = y + swiglu_expert(x, sw)
+        if self.residual:
+            y = y + x
+
+        self.prev_decoded[:N] = ~cl.is_live
+        self.last_iter = i
+        return IterResult(y, G, fresh_pos, sel, w, wl_expert, wl_pos, wl_j, offsets, routed,
+                          fallback, host_fallback, cl)
+
+
+def dense_moe(x: np.ndarray, w_router: np.ndarray, b_router: np.ndarray,
+              expert: Callable[[int], ExpertWeights], n_experts: int, k: int,
+              shared: Sequence[ExpertWeights] = ()) -> np.ndarray:
+    """y_t = sum over the dense top-k of g(x_t) of w_{t,e} E_e(x_t), plus shared experts
+    ([W] "MoE 路径为什么成为瓶颈", layer equation), one position at a time."""
+    G = gate_logits(x, w_router, b_router)
+    everyone = np.ones(n_experts, dtype=bool)
+    y = np.zeros_like(x)
+    for t in range(x.shape[0]):
+        s = topk_select(G[t], everyone, k)
+        wt = renorm_softmax(G[t, s])
+        for j, e in enumerate(s):
+            y[t] += wt[j] * swiglu_expert(x[t:t + 1], expert(int(e)))[0]
+    for sw in shared:
+        y = y + swiglu_expert(x, sw)
+    return y

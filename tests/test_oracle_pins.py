@@ -1,0 +1,494 @@
+"""Pins of the float64 oracle against things other than itself.
+
+Each pin is a hand-worked fixture (tests/golden/, derived from the Epoch
+walk-through's definitions), a closed form, a brute-force search on tiny inputs,
+or a special case that reduces to the plain dense MoE formula computed in a
+different arrangement. The mutation tests at the end plant plausible mistakes
+in the oracle and check that some pin catches each one.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import epoch_moe as om
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ------------------------------------------------------------------ fixtures
+
+def _floats(s):
+    return np.array([float(v) for v in s.split(",")])
+
+
+def _ints(s):
+    return [] if s == "-" else [int(v) for v in s.split(",")]
+
+
+def load_schedules():
+    scheds, cur = [], None
+    with open(os.path.join(GOLDEN, "fresh_schedules.txt"), encoding="utf-8") as fh:
+        for line in fh:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            tok = line.split()
+            if tok[0] == "schedule":
+                cur = dict(name=tok[1], R=None if tok[3] == "inf" else int(tok[3]), steps=[])
+                scheds.append(cur)
+            else:
+                kv = dict(zip(tok[0::2], tok[1::2]))
+                cur["steps"].append(dict(i=int(kv["i"]), decoded=[int(c) for c in kv["decoded"]],
+                                         fresh=_ints(kv["fresh"]), fallback=int(kv["fallback"])))
+    return scheds
+
+
+def load_routing():
+    cases = {"gate": [], "topk": [], "plan": []}
+    with open(os.path.join(GOLDEN, "routing_cases.txt"), encoding="utf-8") as fh:
+        for line in fh:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            tok = line.split()
+            kv = dict(zip(tok[1::2], tok[2::2]))
+            cases[tok[0]].append(kv)
+    return cases
+
+
+def tiny_layer(E=6, H=5, I=4, k=2, tau=1.0, R=None, n_shared=0, seed=0, max_positions=16,
+               residual=False):
+    rng = np.random.default_rng(seed)
+    wr = rng.normal(size=(E, H))
+    b = rng.normal(size=E)
+    experts = [(rng.normal(size=(I, H)), rng.normal(size=(I, H)), rng.normal(size=(H, I)))
+               for _ in range(E)]
+    shared = [(rng.normal(size=(I, H)), rng.normal(size=(I, H)), rng.normal(size=(H, I)))
+              for _ in range(n_shared)]
+    lay = oracle.LayerOracle(n_experts=E, top_k=k, tau=tau, refresh_R=R, w_router=wr, b_router=b,
+                             expert=lambda e: experts[e], shared=shared, residual=residual,
+                             max_positions=max_positions)
+    return lay, wr, b, experts, shared
+
+
+# ------------------------------------------------------------------ closed forms
+
+def test_gate_golden():
+    for c in load_routing()["gate"]:
+        x = _floats(c["x"])[None, :]
+        wr = np.array([[float(v) for v in r.split(",")] for r in c["wr"].split(";")])
+        G = oracle.gate_logits(x, wr, _floats(c["b"]))
+        np.testing.assert_allclose(G[0], _floats(c["G"]), rtol=0, atol=1e-15)
+
+
+def test_silu_closed_forms():
+    ln3 = math.log(3.0)
+    assert oracle.silu(np.array(0.0)) == 0.0
+    assert abs(oracle.silu(np.array(ln3)) - 0.75 * ln3) < 1e-15
+    assert abs(oracle.silu(np.array(-ln3)) + 0.25 * ln3) < 1e-15
+    z = np.linspace(-30, 30, 241)
+    # silu(z) - silu(-z) = z because sigmoid(-z) = 1 - sigmoid(z)
+    np.testing.assert_allclose(oracle.silu(z) - oracle.silu(-z), z, atol=1e-12)
+    # silu(z) -> z for large z and -> 0 for very negative z
+    assert abs(oracle.silu(np.array(40.0)) - 40.0) < 1e-12
+    assert abs(oracle.silu(np.array(-40.0))) < 1e-15
+
+
+def test_swiglu_golden():
+    ln3 = math.log(3.0)
+    x = np.array([[1.0, 0.0]])
+    wg = np.array([[0, 0], [ln3, 0], [0, 0]], dtype=float)
+    wu = np.array([[1, 0], [2, 0], [5, 7]], dtype=float)
+    wd = np.array([[1, 1, 4], [0, 1, 9]], dtype=float)
+    y = oracle.swiglu_expert(x, (wg, wu, wd))
+    np.testing.assert_allclose(y[0], [1.5 * ln3, 1.5 * ln3], rtol=0, atol=1e-15)
+
+
+def test_softmax_closed_form():
+    w = oracle.renorm_softmax(np.array([2.0, 2.0, 0.5]))
+    d = 2.0 + math.exp(-1.5)
+    np.testing.assert_allclose(w, [1 / d, 1 / d, math.exp(-1.5) / d], rtol=1e-15)
+    assert oracle.renorm_softmax(np.array([7.25]))[0] == 1.0
+    # ratios are exp of logit differences, whatever the shift
+    g = np.array([1000.0, 999.0, 997.5])
+    w = oracle.renorm_softmax(g)
+    np.testing.assert_allclose([w[0] / w[1], w[1] / w[2]], [math.e, math.exp(1.5)], rtol=1e-12)
+    assert abs(w.sum() - 1.0) < 1e-15
+
+
+# ------------------------------------------------------------------ routing
+
+def test_topk_golden():
+    for c in load_routing()["topk"]:
+        elig = np.array([ch == "1" for ch in c["elig"]])
+        sel = oracle.topk_select(_floats(c["g"]), elig, int(c["k"]))
+        assert list(sel) == _ints(c["sel"]), c
+
+
+def brute_topk(g, elig, k):
+    """Max-sum k-subset of the eligible experts; among equal sums, the
+    lexicographically smallest sorted id tuple (= ties to the lower id)."""
+    ids = [e for e in range(len(g)) if elig[e]]
+    best = None
+    for comb in itertools.combinations(ids, k):
+        key = (-sum(g[e] for e in comb), comb)
+        if best is None or key < best:
+            best = key
+    return set(best[1])
+
+
+def test_topk_bruteforce():
+    rng = np.random.default_rng(11)
+    for trial in range(400):
+        E = int(rng.integers(2, 9))
+        # few distinct values, so exact ties are common
+        g = rng.integers(-3, 4, size=E).astype(float) * 0.5
+        elig = rng.random(E) < 0.8
+        if elig.sum() == 0:
+            elig[rng.integers(E)] = True
+        k = int(rng.integers(1, elig.sum() + 1))
+        sel = oracle.topk_select(g, elig, k)
+        assert set(sel.tolist()) == brute_topk(g, elig, k)
+        # selection order: logit descending, lower id first among equal logits
+        keys = [(-g[e], e) for e in sel]
+        assert keys == sorted(keys)
+        assert all(elig[e] for e in sel)
+
+
+def test_hit_counts_bruteforce():
+    rng = np.random.default_rng(12)
+    for _ in range(30):
+        N, E = int(rng.integers(1, 9)), int(rng.integers(2, 7))
+        k = int(rng.integers(1, E + 1))
+        G = rng.integers(-2, 3, size=(N, E)).astype(float)
+        cnt = oracle.hit_counts(G, k)
+        assert cnt.sum() == N * k
+        ref = np.zeros(E, dtype=int)
+        for t in range(N):
+            for e in brute_topk(G[t], np.ones(E, bool), k):
+                ref[e] += 1
+        assert (cnt == ref).all()
+
+
+def test_plan_golden():
+    for c in load_routing()["plan"]:
+        cnt = np.array(_ints(c["cnt"]))
+        k, n, tau = int(c["k"]), int(c["n"]), float(c["tau"])
+        assert oracle.coverage_threshold(tau, n, k) == int(c["T"])
+        ranked, slen = oracle.plan_support(cnt, k, tau, n)
+        assert list(ranked) == _ints(c["ranked"])
+        assert slen == int(c["len"])
+
+
+def test_plan_minimal_support_bruteforce():
+    """|S| = max(k, fewest experts whose counts reach T), and S holds the largest
+    counts, ties to the lower id: checked over every subset of up to 9 experts."""
+    rng = np.random.default_rng(13)
+    for _ in range(150):
+        E = int(rng.integers(2, 10))
+        k = int(rng.integers(1, min(E, 4) + 1))
+        n = int(rng.integers(1, 7))
+        # counts summing to n*k, each at most n (a position picks an expert once)
+        cnt = np.zeros(E, dtype=int)
+        for _t in range(n):
+            cnt[rng.choice(E, size=k, replace=False)] += 1
+        tau = float(rng.choice([0.3, 0.5, 0.75, 0.9, 0.95, 0.99, 1.0]))
+        ranked, slen = oracle.plan_support(cnt, k, tau, n)
+        if tau >= 1.0:
+            assert slen == E
+            continue
+        T = math.ceil(tau * n * k)
+        best = None
+        for m in range(0, E + 1):
+            for comb in itertools.combinations(range(E), m):
+                if sum(cnt[e] for e in comb) >= T:
+                    key = (m, -sum(cnt[e] for e in comb), comb)
+                    if best is None or key < best:
+                        best = key
+        m_star = best[0]
+        assert slen == min(max(m_star, k), E)
+        S = set(ranked[:slen].tolist())
+        if slen == m_star:
+            assert S == set(best[2])
+        # the support is closed upward in (count desc, id asc)
+        for a in S:
+            for b in set(range(E)) - S:
+                assert (cnt[a], -a) > (cnt[b], -b)
+
+
+def test_near_tie_detects_close_logits():
+    g = np.array([1.0, 0.5, 0.5 + 5e-6, -1.0])
+    assert oracle.near_tie(g, np.ones(4, bool), 2)
+    assert not oracle.near_tie(np.array([3.0, 2.0, 1.0, 0.0]), np.ones(4, bool), 2)
+
+
+# ------------------------------------------------------------------ liveness schedules
+
+@pytest.mark.parametrize("sched", load_schedules(), ids=lambda s: s["name"])
+def test_fresh_schedules_golden(sched):
+    N = len(sched["steps"][0]["decoded"])
+    lay, *_ = tiny_layer(E=5, H=4, I=3, k=2, tau=1.0, R=sched["R"], max_positions=N)
+    rng = np.random.default_rng(5)
+    x = rng.normal(size=(N, 4))
+    lay.plan_block(x)
+    for st in sched["steps"]:
+        dec = np.array(st["decoded"], dtype=np.uint8)
+        res = lay.iterate(x + 0.01 * st["i"], 1 - dec, dec, st["i"])
+        assert list(res.fresh_pos) == st["fresh"], (sched["name"], st)
+        assert int(res.fallback) == st["fallback"], (sched["name"], st)
+
+
+# ------------------------------------------------------------------ dense special case
+
+def masked_dense(x, wr, b, experts, k, shared=()):
+    """Every expert on every token, combined with a [N, E] weight matrix that is
+    zero outside each token's brute-force top-k."""
+    G = x @ wr.T + b
+    N, E = G.shape
+    Wt = np.zeros((N, E))
+    for t in range(N):
+        s = sorted(brute_topk(G[t], np.ones(E, bool), k))
+        ex = np.exp(G[t, s] - G[t, s].max())
+        Wt[t, s] = ex / ex.sum()
+    y = np.zeros_like(x)
+    for e in range(E):
+        wg, wu, wd = experts[e]
+        h = x @ wg.T
+        y += Wt[:, e:e + 1] * (((h / (1 + np.exp(-h))) * (x @ wu.T)) @ wd.T)
+    for wg, wu, wd in shared:
+        h = x @ wg.T
+        y += ((h / (1 + np.exp(-h))) * (x @ wu.T)) @ wd.T
+    return y
+
+
+@pytest.mark.parametrize("n_shared", [0, 1])
+def test_tau1_R1_equals_dense_moe(n_shared):
+    """tau = 1 and refresh period 1: every position fresh, every expert eligible,
+    so each iteration equals the dense MoE layer."""
+    N, H, E, I, k = 12, 6, 7, 5, 3
+    lay, wr, b, experts, shared = tiny_layer(E=E, H=H, I=I, k=k, tau=1.0, R=1,
+                                             n_shared=n_shared, seed=3, max_positions=N)
+    rng = np.random.default_rng(4)
+    x = rng.normal(size=(N, H))
+    lay.plan_block(x)
+    dec = np.zeros(N, np.uint8)
+    for i in range(6):
+        dec[rng.choice(N, size=2, replace=False)] = 1
+        xi = x + 0.05 * rng.normal(size=(N, H))
+        res = lay.iterate(xi, 1 - dec, dec, i)
+        assert res.fresh_pos.size == N
+        np.testing.assert_allclose(res.y, masked_dense(xi, wr, b, experts, k, shared),
+                                   rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(
+            res.y, oracle.dense_moe(xi, wr, b, lambda e: experts[e], E, k, shared),
+            rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------------ invariants
+
+def run_random_block(E=8, H=6, I=5, k=2, tau=0.7, R=3, N=24, iters=10, seed=7, n_shared=1):
+    lay, wr, b, experts, shared = tiny_layer(E=E, H=H, I=I, k=k, tau=tau, R=R, n_shared=n_shared,
+                                             seed=seed, max_positions=N)
+    rng = np.random.default_rng(seed + 100)
+    x = rng.normal(size=(N, H))
+    plan = lay.plan_block(x)
+    dec = np.zeros(N, np.uint8)
+    history = []
+    for i in range(iters):
+        res = lay.iterate(x, 1 - dec, dec, i)
+        history.append((i, dec.copy(), x.copy(), res, lay.stamp.copy()))
+        live = np.nonzero(dec == 0)[0]
+        if live.size:
+            dec[rng.choice(live, size=min(3, live.size), replace=False)] = 1
+        x = x + 0.05 * rng.normal(size=(N, H))
+    return lay, plan, history, (wr, b, experts, shared)
+
+
+def test_iteration_invariants():
+    k, R = 2, 3
+    lay, plan, hist, (wr, b, experts, shared) = run_random_block(k=k, R=R)
+    S = set(plan.support.tolist())
+    prev_dec = np.zeros_like(hist[0][1])
+    last_fresh = {}
+    for i, dec, x, res, stamp in hist:
+        fresh = set(res.fresh_pos.tolist())
+        live = set(np.nonzero(dec == 0)[0].tolist())
+        new = set(np.nonzero((dec == 1) & (prev_dec == 0))[0].tolist())
+        assert live <= fresh                      # a live position never reads the cache
+        assert new <= fresh                       # newly decoded rows are fresh once
+        assert res.n_edges == k * len(fresh)      # worklist length = k |F|
+        assert res.offsets[-1] == res.n_edges
+        assert not res.fallback
+        assert set(res.wl_expert.tolist()) <= S   # only support experts are eligible
+        pairs = list(zip(res.wl_expert.tolist(), res.wl_pos.tolist()))
+        assert all(a < b_ for a, b_ in zip(pairs, pairs[1:]))  # (expert, position) strictly ordered
+        np.testing.assert_allclose(res.w.sum(axis=1), 1.0, rtol=1e-14)
+        for t in range(len(dec)):
+            if t in fresh:
+                last_fresh[t] = (i, res.routed[t].copy())
+            else:
+                j, row = last_fresh[t]
+                assert 1 <= i - j <= R - 1        # bounded age of reused rows
+                assert np.array_equal(res.routed[t], row)  # the cached routed output, unchanged
+        prev_dec = dec
+
+
+def test_support_equal_k_selects_whole_support():
+    lay, wr, b, experts, shared = tiny_layer(E=9, H=5, I=4, k=3, tau=0.05, R=2, seed=21,
+                                             max_positions=10)
+    rng = np.random.default_rng(22)
+    x = rng.normal(size=(10, 5))
+    plan = lay.plan_block(x)
+    assert plan.support_len == 3
+    res = lay.iterate(x, np.ones(10, np.uint8), np.zeros(10, np.uint8), 0)
+    for row in res.sel:
+        assert set(row.tolist()) == set(plan.support.tolist())
+
+
+def test_never_refresh_all_decoded_is_pure_cache():
+    N = 8
+    lay, wr, b, experts, shared = tiny_layer(E=6, H=5, I=4, k=2, tau=0.8, R=None, n_shared=1,
+                                             seed=31, max_positions=N)
+    rng = np.random.default_rng(32)
+    x = rng.normal(size=(N, 5))
+    lay.plan_block(x)
+    dec = np.zeros(N, np.uint8)
+    lay.iterate(x, 1 - dec, dec, 0)
+    dec[:] = 1
+    r1 = lay.iterate(x, 1 - dec, dec, 1)        # all newly decoded: fresh
+    cached = r1.routed.copy()
+    for i in range(2, 5):
+        xi = x + 0.1 * i
+        res = lay.iterate(xi, 1 - dec, dec, i)
+        assert res.n_edges == 0
+        sh = sum(oracle.swiglu_expert(xi, s) for s in shared)
+        np.testing.assert_allclose(res.y, cached + sh, rtol=1e-13, atol=1e-13)
+
+
+def test_residual_adds_input():
+    N = 6
+    a, *_ = tiny_layer(seed=41, max_positions=N, residual=False, n_shared=1)
+    c, *_ = tiny_layer(seed=41, max_positions=N, residual=True, n_shared=1)
+    x = np.random.default_rng(42).normal(size=(N, 5))
+    a.plan_block(x)
+    c.plan_block(x)
+    live, dec = np.ones(N, np.uint8), np.zeros(N, np.uint8)
+    np.testing.assert_allclose(c.iterate(x, live, dec, 0).y, a.iterate(x, live, dec, 0).y + x,
+                               rtol=1e-14, atol=1e-14)
+
+
+def test_no_plan_or_skip_is_full_fresh_with_all_experts():
+    N = 10
+    lay, *_ = tiny_layer(E=8, k=2, tau=0.3, R=4, seed=51, max_positions=N)
+    rng = np.random.default_rng(52)
+    x = rng.normal(size=(N, 5))
+    dec = np.zeros(N, np.uint8)
+    dec[:6] = 1
+    res = lay.iterate(x, 1 - dec, dec, 0)       # no plan yet
+    assert res.host_fallback and res.fresh_pos.size == N
+    lay.plan_block(x)
+    assert lay.plan.support_len < 8
+    res = lay.iterate(x, 1 - dec, dec, 0)
+    assert not res.fallback
+    res = lay.iterate(x, 1 - dec, dec, 1)
+    assert res.fresh_pos.size == N - 6
+    res = lay.iterate(x, 1 - dec, dec, 5)       # skipped iterations
+    assert res.host_fallback and res.fresh_pos.size == N
+    # in a fallback every expert is eligible: the selection equals the dense top-k
+    G = res.G
+    for f, t in enumerate(res.fresh_pos):
+        assert set(res.sel[f].tolist()) == brute_topk(G[t], np.ones(8, bool), 2)
+
+
+def test_both_or_neither_flag_is_treated_live():
+    N = 4
+    lay, *_ = tiny_layer(E=5, k=2, tau=1.0, R=None, seed=61, max_positions=N)
+    x = np.random.default_rng(62).normal(size=(N, 5))
+    lay.plan_block(x)
+    lay.iterate(x, np.ones(N, np.uint8), np.zeros(N, np.uint8), 0)
+    dec = np.array([1, 1, 1, 1], np.uint8)
+    lay.iterate(x, 1 - dec, dec, 1)
+    live = np.array([1, 0, 0, 0], np.uint8)      # position 0 both flags -> live -> anomaly
+    res = lay.iterate(x, live, dec, 2)
+    assert res.classified.bad_flags == 1 and res.fallback
+    live = np.array([0, 0, 0, 0], np.uint8)
+    dec2 = np.array([1, 1, 0, 1], np.uint8)      # position 2 neither -> live
+    res = lay.iterate(x, live, dec2, 3)
+    assert res.classified.bad_flags == 1 and 2 in res.fresh_pos.tolist()
+
+
+# ------------------------------------------------------------------ mutations
+
+def _pins_pass():
+    """Run the pins that do not depend on fixtures' parametrisation."""
+    checks = [test_gate_golden, test_silu_closed_forms, test_swiglu_golden, test_softmax_closed_form,
+              test_topk_golden, test_topk_bruteforce, test_plan_golden,
+              test_plan_minimal_support_bruteforce, test_iteration_invariants,
+              lambda: test_tau1_R1_equals_dense_moe(1),
+              lambda: [test_fresh_schedules_golden(s) for s in load_schedules()]]
+    for c in checks:
+        try:
+            c()
+        except AssertionError:
+            return False
+    return True
+
+
+def _mut_rank_desc_ids(g_row, eligible):
+    ids = np.nonzero(eligible)[0]
+    return ids[np.lexsort((-ids, -g_row[ids]))]
+
+
+def _mut_gate_no_bias(x, w, b):
+    return x @ w.T
+
+
+def _mut_silu_sign(z):
+    return z / (1.0 + np.exp(z))
+
+
+def _mut_swiglu_swapped(X, w):
+    wg, wu, wd = w
+    return (silu_orig(X @ wu.T) * (X @ wg.T)) @ wd.T
+
+
+silu_orig = om.silu
+
+
+def _mut_softmax_unnormalised(g):
+    return np.exp(g - np.max(g))
+
+
+def _mut_plan_off_by_one(cnt, k, tau, n_pos):
+    ranked, slen = PLAN_ORIG(cnt, k, tau, n_pos)
+    return ranked, min(slen + 1, len(cnt)) if tau < 1.0 else slen
+
+
+PLAN_ORIG = om.plan_support
+
+
+def _mut_stale_strict(live, decoded, prev, stamp, i, R, force):
+    return CLASSIFY_ORIG(live, decoded, prev, stamp, i, None if R is None else R + 1, force)
+
+
+CLASSIFY_ORIG = om.classify_positions
+
+
+@pytest.mark.parametrize("name,attr,mutant", [
+    ("tie to higher id", "rank_eligible", _mut_rank_desc_ids),
+    ("dropped router bias", "gate_logits", _mut_gate_no_bias),
+    ("wrong sign in silu", "silu", _mut_silu_sign),
+    ("gate/up swapped", "swiglu_expert", _mut_swiglu_swapped),
+    ("weights not renormalised", "renorm_softmax", _mut_softmax_unnormalised),
+    ("support one too long", "plan_support", _mut_plan_off_by_one),
+    ("refresh one iteration late", "classify_positions", _mut_stale_strict),
+])
+def test_planted_mistakes_are_caught(monkeypatch, name, attr, mutant):
+    assert _pins_pass()
+    monkeypatch.setattr(om, attr, mutant)
+    monkeypatch.setattr(oracle, attr, mutant)
+    assert not _pins_pass(), f"no pin caught: {name}"
