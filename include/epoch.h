@@ -1,0 +1,247 @@
+/*
+ * epoch.h -- C ABI of the Epoch routed-expert MoE layer iteration on GB300 (sm_103a).
+ *
+ * Source pages, cited by title and section:
+ *   [W] "Epoch 完全拆解:把扩散块编译成稀疏 MoE 服务单元" (pinghaoyang.com.cn walk-through of Epoch)
+ *   [A] "Epoch: Compiling Diffusion Blocks for Sparse MoE Serving" (abstract)
+ *
+ * One layer object holds one MoE layer's block plan (expert support), its
+ * per-position routed-output cache with stamps, and the scratch of one
+ * iteration. A caller runs, per diffusion block:
+ *     epoch_plan_block  (cold path, once)  ->  epoch_moe_iter (i = 0, 1, ...)  ->  epoch_block_end
+ *
+ * Conventions for every entry point:
+ *  - Pointers named *_dev or documented as "device" are CUDA device pointers in
+ *    the current context; all others are host pointers. Device pointers must be
+ *    16-byte aligned.
+ *  - Matrices are row-major, contiguous. "dtype" is the layer's epoch_dtype:
+ *    EPOCH_F32 (float) or EPOCH_BF16 (bfloat16 bit patterns, 2 bytes).
+ *  - The caller owns every buffer it passes (weights, x, masks, y, workspace);
+ *    the library keeps the weight and workspace pointers until
+ *    epoch_layer_destroy and never frees them. It allocates no device memory.
+ *  - Work is enqueued on the given stream (NULL = legacy default stream) and
+ *    returns without synchronising, except where a function says it syncs.
+ *  - Errors come in three tiers: invalid arguments return EPOCH_EINVAL before
+ *    anything is enqueued; state anomalies (no plan, skipped iteration, n_pos
+ *    differing from the plan, a decoded->live transition seen on the device)
+ *    turn the iteration into a counted full-fresh fallback and still return
+ *    EPOCH_OK; device-detected errors set a sticky device error word that
+ *    epoch_get_status reports.
+ */
+#ifndef EPOCH_H
+#define EPOCH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *epoch_stream; /* a cudaStream_t */
+typedef struct epoch_layer epoch_layer;   /* opaque layer object */
+
+typedef enum {
+  EPOCH_OK = 0,
+  EPOCH_EINVAL = 1,   /* bad argument; nothing enqueued */
+  EPOCH_ESTATE = 2,   /* call not valid in the layer's state (e.g. destroyed workspace too small) */
+  EPOCH_ECUDA = 3,    /* a CUDA runtime call failed (launch, copy, driver entry point) */
+  EPOCH_ETIMEOUT = 4, /* a bounded device wait gave up (device error word bit 1) */
+  EPOCH_EDEVICE = 5   /* other device-detected error (device error word bits 0, 2) */
+} epoch_status;
+
+typedef enum { EPOCH_F32 = 0, EPOCH_BF16 = 1 } epoch_dtype;
+
+#define EPOCH_REFRESH_NEVER INT32_MAX
+
+/* Device error word bits (sticky until epoch_clear_status). */
+#define EPOCH_DEVERR_FLAGS 1u    /* a position flagged both live and decoded, or neither (treated live) */
+#define EPOCH_DEVERR_TIMEOUT 2u  /* a bounded mbarrier wait expired; the kernel returned early */
+#define EPOCH_DEVERR_BOUNDS 4u   /* an index failed its range check; the access was skipped */
+
+/* Layer shape and policy.
+ *  hidden (H), n_experts (E), inter (I), top_k (k): y_t = sum over the k selected
+ *    experts e of w_{t,e} E_e(x_t) ([W] section "MoE 路径为什么成为瓶颈", layer equation),
+ *    E_e(x) = W_down,e (silu(W_gate,e x) * (W_up,e x)) (SwiGLU).
+ *  n_shared, shared_inter: always-on shared experts added to every position,
+ *    untouched by the liveness split ([W] section "Liveness-Shard Parallelism").
+ *  max_positions: the largest n_pos any call passes (sizes the workspace).
+ *  dtype: element type of weights, x, y and the row cache (router bias is float).
+ *  tau in (0, 1]: support coverage fraction; the support is the smallest prefix
+ *    of experts ranked by block-start top-k hit count (count desc, id asc) whose
+ *    counts reach ceil(tau * n_pos * k) edges, at least k experts; tau = 1 keeps
+ *    every expert (the coverage-driven support of [W] section "Expert Atlas").
+ *  refresh_R >= 1: a decoded position whose cached routed output is at least R
+ *    iterations old is recomputed (EPOCH_REFRESH_NEVER: never) -- the bounded
+ *    age of [W] section "decoded-cache 的刷新周期为什么默认取 5".
+ *  residual: nonzero makes y = x + routed + shared (chains a stack of layers).
+ * Constraints (else EPOCH_EINVAL): 1 <= top_k <= n_experts <= 1024, top_k <= 16;
+ *  bf16: H, I and shared_inter multiples of 128; f32: multiples of 4;
+ *  1 <= max_positions <= 16384. */
+typedef struct {
+  int32_t hidden;
+  int32_t n_experts;
+  int32_t inter;
+  int32_t top_k;
+  int32_t n_shared;
+  int32_t shared_inter;
+  int32_t max_positions;
+  int32_t dtype;
+  double tau;
+  int32_t refresh_R;
+  int32_t residual;
+} epoch_layer_config;
+
+/* Weights, all device pointers of the layer dtype unless noted.
+ *  w_router [E][H], b_router [E] (float); w_gate, w_up [E][I][H]; w_down [E][H][I];
+ *  ws_gate, ws_up [n_shared][shared_inter][H], ws_down [n_shared][H][shared_inter]
+ *  (NULL when n_shared = 0). */
+typedef struct {
+  const void *w_router;
+  const float *b_router;
+  const void *w_gate;
+  const void *w_up;
+  const void *w_down;
+  const void *ws_gate;
+  const void *ws_up;
+  const void *ws_down;
+} epoch_layer_weights;
+
+/* Per-iteration statistics, written by the device at the end of each
+ * epoch_moe_iter (the block plan's path counters, [W] section "Two Clocks").
+ * Categories partition the positions: live + new + miss + stale + forced + reuse = n_pos. */
+typedef struct {
+  int32_t iteration;
+  int32_t n_pos;
+  int32_t n_live;      /* still Mask */
+  int32_t n_new;       /* decoded now, not at the previous iteration */
+  int32_t n_miss;      /* decoded, no cached row */
+  int32_t n_stale;     /* decoded, cached row at least R iterations old */
+  int32_t n_forced;    /* would have reused its row; made fresh by a fallback */
+  int32_t n_reuse;     /* stable decoded, cached row reused */
+  int32_t n_fresh;     /* |F_i| */
+  int32_t n_edges;     /* worklist length L = k |F_i| */
+  int32_t n_hit_experts;
+  int32_t support_len; /* experts eligible this iteration (E on a fallback) */
+  int32_t fallback;    /* bit 0: host-detected mismatch; bit 1: decoded->live anomaly */
+  int32_t bad_flags;   /* positions flagged both live and decoded, or neither */
+  int32_t tiles_up;    /* grouped-GEMM tiles launched */
+  int32_t tiles_down;
+} epoch_iter_stats;
+
+/* Device pointers into the workspace for inspection (valid after the stream
+ * that ran the last call has been synchronised; read-only for the caller). */
+typedef struct {
+  const int32_t *support_ids;  /* [E] experts in rank order; first *support_len valid */
+  const int32_t *support_len;  /* [1] */
+  const int32_t *plan_counts;  /* [E] block-start top-k hit counts */
+  const float *logit_parts;    /* [n_logit_parts][max_positions][E] partial sums of x W_r^T over
+                                  disjoint slices of H (no bias); G = their sum + b_router */
+  int32_t n_logit_parts;
+  const int32_t *fresh_pos;    /* [n_fresh] ascending fresh positions */
+  const int32_t *sel;          /* [n_fresh][k] selected experts, selection order */
+  const float *sel_w;          /* [n_fresh][k] routing weights */
+  const int32_t *offsets;      /* [E+1] worklist offsets per expert */
+  const int32_t *wl_pos;       /* [n_edges] positions of the expert-sorted worklist */
+  const int32_t *slot;         /* [n_fresh][k] worklist row of each selection */
+  const int32_t *stamp;        /* [max_positions] iteration of each row's last fresh compute, -1 none */
+  const void *cache;           /* [max_positions][H] routed-output cache, layer dtype */
+  const epoch_iter_stats *stats;
+  const uint32_t *error_word;
+} epoch_debug_view;
+
+/* Per-kernel timing, accumulated while profiling is on. */
+#define EPOCH_PROF_KINDS 12
+typedef struct {
+  const char *name[EPOCH_PROF_KINDS];
+  int64_t launches[EPOCH_PROF_KINDS];
+  double total_ms[EPOCH_PROF_KINDS];
+  int64_t kernels_launched; /* every kernel this layer enqueued since creation */
+} epoch_profile;
+
+/* Bytes of device workspace a layer with this config needs (0 on an invalid config). */
+size_t epoch_workspace_bytes(const epoch_layer_config *cfg);
+
+/* Validates cfg and weights, carves the caller's device workspace (>= epoch_workspace_bytes,
+ * 256-byte aligned) and encodes the TMA descriptors of the weights. Clears the
+ * row cache state synchronously (cudaMemset on the legacy stream).
+ * Returns EPOCH_EINVAL on a bad config or pointer, EPOCH_ECUDA if the CUDA
+ * driver entry point cannot be found. *out is set only on EPOCH_OK. */
+epoch_status epoch_layer_create(const epoch_layer_config *cfg, const epoch_layer_weights *w,
+                                void *workspace_dev, size_t workspace_bytes, epoch_layer **out);
+
+/* Cold path of a block ([W] section "cold、hot-update、hot-skip"): gate logits
+ * G = x W_r^T + b for the n_pos positions of x [n_pos][H] (device, dtype), dense
+ * top-k hit counts, the coverage support (see tau), and clears the stamps and
+ * previous-decoded flags so that the block starts with an empty cache. The
+ * support is readable through epoch_debug_pointers after a sync.
+ * EPOCH_EINVAL if n_pos is not in [1, max_positions] or x is NULL/misaligned. */
+epoch_status epoch_plan_block(epoch_layer *layer, const void *x_dev, int32_t n_pos, epoch_stream stream);
+
+/* One refinement iteration ([W] sections "Expert Atlas" step three,
+ * "Liveness-Shard Parallelism", "FreshLane Dispatch"):
+ *  x_dev [n_pos][H] hidden states; live_dev, decoded_dev [n_pos] uint8 flags
+ *  (exactly one nonzero per position); iteration i; y_dev [n_pos][H] output.
+ *  Recomputes G for every position; classifies positions (live, newly decoded,
+ *  stale or missing row -> fresh; stable decoded -> reuse); takes the top-k of
+ *  each fresh position over the support, softmax-weighted; builds the
+ *  expert-sorted worklist; runs the SwiGLU experts over it; and writes
+ *  y = routed (+ shared) (+ x if residual), routed being the fresh result or the
+ *  cached row. Fresh rows refill the cache and get stamp i.
+ *  A full-fresh fallback with every expert eligible happens when no plan is
+ *  active, i != previous iteration + 1, n_pos differs from the plan, or a
+ *  decoded position becomes live. EPOCH_EINVAL on bad sizes or pointers. */
+epoch_status epoch_moe_iter(epoch_layer *layer, const void *x_dev, const uint8_t *live_dev,
+                            const uint8_t *decoded_dev, int32_t n_pos, int32_t iteration, void *y_dev,
+                            epoch_stream stream);
+
+/* Ends the block: the plan, cache and stamps become invalid; the next
+ * epoch_moe_iter without a new plan runs as a fallback. Host-only, no sync. */
+epoch_status epoch_block_end(epoch_layer *layer);
+
+/* Reads the sticky device error word (synchronises the stream). *word_out may be NULL.
+ * EPOCH_OK when clear, EPOCH_ETIMEOUT if the timeout bit is set, else EPOCH_EDEVICE. */
+epoch_status epoch_get_status(epoch_layer *layer, epoch_stream stream, uint32_t *word_out);
+
+/* Clears the device error word (enqueued on the stream). */
+epoch_status epoch_clear_status(epoch_layer *layer, epoch_stream stream);
+
+/* Copies the last iteration's statistics to host memory (synchronises the stream). */
+epoch_status epoch_read_stats(epoch_layer *layer, epoch_iter_stats *out, epoch_stream stream);
+
+/* Device pointers of the layer's internal arrays (no copy, no sync). */
+epoch_status epoch_debug_pointers(epoch_layer *layer, epoch_debug_view *out);
+
+/* Copies bytes from a device pointer (such as one from epoch_debug_pointers)
+ * into host memory; synchronises the stream. */
+epoch_status epoch_debug_copy(void *host_dst, const void *dev_src, size_t bytes, epoch_stream stream);
+
+/* Host-side counters of the lifecycle paths: plans (cold), normal iterations
+ * (hot-skip), host-detected fallbacks. Any pointer may be NULL. */
+epoch_status epoch_path_counters(epoch_layer *layer, int64_t *cold, int64_t *hot, int64_t *fallback);
+
+/* Bounded device waits: a wait that makes no progress for timeout_ns gives up,
+ * sets EPOCH_DEVERR_TIMEOUT and lets the kernel return (default 2e9 ns). */
+epoch_status epoch_set_wait_timeout(epoch_layer *layer, int64_t timeout_ns);
+
+/* Per-kernel CUDA-event timing on the launching stream (adds an event pair per launch). */
+epoch_status epoch_set_profiling(epoch_layer *layer, int32_t enable);
+/* Synchronises pending events, accumulates their times, and copies the totals. */
+epoch_status epoch_read_profile(epoch_layer *layer, epoch_profile *out);
+epoch_status epoch_reset_profile(epoch_layer *layer);
+
+/* Test hook: launches one kernel whose only work is a bounded wait on an
+ * mbarrier that nothing completes, with the given timeout; it must set
+ * EPOCH_DEVERR_TIMEOUT and return. Exercises the timeout path without a hang. */
+epoch_status epoch_test_wait_timeout(epoch_layer *layer, int64_t timeout_ns, epoch_stream stream);
+
+/* Releases host state only (the caller frees the workspace and weights). NULL is ignored. */
+void epoch_layer_destroy(epoch_layer *layer);
+
+const char *epoch_status_str(epoch_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EPOCH_H */

@@ -299,10 +299,12 @@ class LayerOracle:
         self.planned = False
 
     def iterate(self, x: np.ndarray, live: np.ndarray, decoded: np.ndarray, i: int,
-                adopt: Optional[Callable[[int, np.ndarray], Optional[np.ndarray]]] = None
+                adopt: Optional[Callable[[int, np.ndarray, np.ndarray, np.ndarray],
+                                         Optional[np.ndarray]]] = None
                 ) -> IterResult:
-        """One refinement iteration. ``adopt(t, sel)`` may return a replacement
-        selection for position t (the parity harness uses it after a logged near-tie)."""
+        """One refinement iteration. ``adopt(t, sel, g_row, eligible)`` may return a
+        replacement selection for position t (the parity harness uses it after a
+        logged near-tie)."""
         N = x.shape[0]
         host_fallback = (not self.planned) or (i != self.last_iter + 1) or (N != self.n_pos)
         G = gate_logits(x, self.w_router, self.b_router)
@@ -317,7 +319,7 @@ class LayerOracle:
         for f, t in enumerate(fresh_pos):
             s = topk_select(G[t], eligible, self.k)
             if adopt is not None:
-                repl = adopt(int(t), s)
+                repl = adopt(int(t), s, G[t], eligible)
                 if repl is not None:
                     s = np.asarray(repl, dtype=np.int64)
             sel[f] = s

@@ -1,0 +1,460 @@
+// C ABI of the Epoch MoE-layer iteration: argument checks, workspace carve-up,
+// the block-plan state machine (cold path, hot iterations, full-fresh
+// fallback), the per-iteration launch sequence, and per-kernel profiling.
+//
+// Lifecycle ([W] = walk-through page "Epoch 完全拆解:把扩散块编译成稀疏 MoE 服务单元",
+// section "cold、hot-update、hot-skip"): the cold path runs once per block
+// (epoch_plan_block); hot iterations reuse the support mask and recompute
+// logits, weights and fresh expert outputs; a missing plan, a skipped
+// iteration, a shape mismatch or a liveness anomaly fall back to full fresh
+// ([W] section "Two Clocks": the plan can always return to the dense path).
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+#include "layer.h"
+
+using namespace epoch;
+
+struct epoch_layer {
+  epoch_layer_config cfg;
+  Dims dims;  // static part (n_pos, iter, host_fallback, SK filled per call)
+  Weights w;
+  Work ws;
+  Maps maps;
+  bool bf16;
+  int sk_max;
+  int last_sk;
+  // block-plan state
+  bool planned;
+  int32_t n_pos_plan;
+  int32_t last_iter;
+  int64_t n_cold, n_hot, n_fallback, n_launch;
+  // profiling
+  bool prof;
+  struct Pending {
+    int kind;
+    cudaEvent_t a, b;
+  };
+  std::vector<Pending> pending;
+  std::vector<cudaEvent_t> pool;
+  double total_ms[K_NUM];
+  int64_t launches[K_NUM];
+};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_config(const epoch_layer_config *c) {
+  if (c == nullptr) return false;
+  if (c->hidden <= 0 || c->inter <= 0 || c->n_experts < 1 || c->n_experts > 1024) return false;
+  if (c->top_k < 1 || c->top_k > 16 || c->top_k > c->n_experts) return false;
+  if (c->n_shared < 0 || c->n_shared > 8) return false;
+  if (c->n_shared > 0 && c->shared_inter <= 0) return false;
+  if (c->max_positions < 1 || c->max_positions > 16384) return false;
+  if (c->dtype != EPOCH_F32 && c->dtype != EPOCH_BF16) return false;
+  if (!(c->tau > 0.0 && c->tau <= 1.0)) return false;
+  if (c->refresh_R < 1) return false;
+  const int q = c->dtype == EPOCH_BF16 ? 128 : 4;
+  if (c->hidden % q || c->inter % q) return false;
+  if (c->n_shared > 0 && c->shared_inter % q) return false;
+  return true;
+}
+
+int sk_max_for(const epoch_layer_config &c) {
+  if (c.dtype != EPOCH_BF16) return 1;
+  const int kb = c.hidden / 64;
+  return kb < 16 ? kb : 16;
+}
+
+// Lays the workspace out (base == nullptr: only measures). Returns total bytes.
+size_t carve(const epoch_layer_config &c, char *base, Work *w) {
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> void * {
+    off = (off + kAlign - 1) & ~(kAlign - 1);
+    void *p = base ? base + off : nullptr;
+    off += bytes;
+    return p;
+  };
+  const size_t N = c.max_positions, E = c.n_experts, H = c.hidden, I = c.inter, k = c.top_k;
+  const size_t nsh = c.n_shared, Is = c.n_shared ? c.shared_inter : 0;
+  const size_t act = c.dtype == EPOCH_BF16 ? 2 : 4;
+  const size_t G = E + nsh;
+  const size_t chunks = (N + 31) / 32;
+  Work t;
+  t.stamp = static_cast<int32_t *>(take(N * 4));
+  t.prev_dec = static_cast<uint8_t *>(take(N));
+  t.support_mask = static_cast<uint8_t *>(take(E));
+  t.support_ids = static_cast<int32_t *>(take(E * 4));
+  t.plan_counts = static_cast<int32_t *>(take(E * 4));
+  t.cache = take(N * H * act);
+  t.gparts = static_cast<float *>(take(static_cast<size_t>(sk_max_for(c)) * N * E * 4));
+  t.fidx = static_cast<int32_t *>(take(N * 4));
+  t.fresh_pos = static_cast<int32_t *>(take(N * 4));
+  t.sel = static_cast<int32_t *>(take(N * k * 4));
+  t.selw = static_cast<float *>(take(N * k * 4));
+  t.chunk_mask = static_cast<uint32_t *>(take(chunks * E * 4));
+  t.offsets = static_cast<int32_t *>(take((E + 1) * 4));
+  t.grp_rows = static_cast<int32_t *>(take(G * 4));
+  t.grp_row0 = static_cast<int32_t *>(take(G * 4));
+  t.tile_off_up = static_cast<int32_t *>(take((G + 1) * 4));
+  t.tile_off_dn = static_cast<int32_t *>(take((G + 1) * 4));
+  t.wl_pos = static_cast<int32_t *>(take(N * k * 4));
+  t.slot = static_cast<int32_t *>(take(N * k * 4));
+  t.xp = take(N * k * H * act);
+  t.a_int = take(N * k * I * act);
+  t.a_sh = take(nsh * N * Is * act + 16);
+  t.o_int = static_cast<float *>(take(N * k * H * 4));
+  t.o_sh = static_cast<float *>(take(nsh * N * H * 4 + 16));
+  t.ctrl = static_cast<Ctrl *>(take(sizeof(Ctrl)));
+  t.stats = static_cast<epoch_iter_stats *>(take(sizeof(epoch_iter_stats)));
+  t.err = static_cast<uint32_t *>(take(16));
+  if (w) *w = t;
+  return (off + kAlign - 1) & ~(kAlign - 1);
+}
+
+cudaStream_t S(epoch_stream s) { return reinterpret_cast<cudaStream_t>(s); }
+
+cudaEvent_t get_event(epoch_layer *L) {
+  if (!L->pool.empty()) {
+    cudaEvent_t e = L->pool.back();
+    L->pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Enqueues one kernel (bracketed by events while profiling) and counts it.
+template <typename F>
+epoch_status run(epoch_layer *L, Kind kind, cudaStream_t s, F &&launch) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (L->prof) {
+    a = get_event(L);
+    cudaEventRecord(a, s);
+  }
+  const cudaError_t e = launch();
+  if (L->prof) {
+    b = get_event(L);
+    cudaEventRecord(b, s);
+    L->pending.push_back({kind, a, b});
+  }
+  ++L->n_launch;
+  return e == cudaSuccess ? EPOCH_OK : EPOCH_ECUDA;
+}
+
+#define EPOCH_TRY(expr)                       \
+  do {                                        \
+    const epoch_status st_ = (expr);          \
+    if (st_ != EPOCH_OK) return st_;          \
+  } while (0)
+
+Dims call_dims(const epoch_layer *L, int32_t n_pos, int32_t iter, int host_fallback) {
+  Dims d = L->dims;
+  d.n_pos = n_pos;
+  d.iter = iter;
+  d.host_fallback = host_fallback;
+  return d;
+}
+
+// G for every position: tcgen05 split-K for bf16 layers, FFMA for fp32 layers.
+epoch_status run_gate(epoch_layer *L, Dims &d, const void *x, CUtensorMap *x_map, cudaStream_t s) {
+  if (L->bf16) {
+    d.SK = tc_gate_splits(d);
+    if (d.SK > L->sk_max) d.SK = L->sk_max;
+    while ((d.H / 64) % d.SK) --d.SK;
+    if (!encode_kmajor_bf16(x_map, x, d.H, d.n_pos, 128)) return EPOCH_ECUDA;
+    L->last_sk = d.SK;
+    return run(L, K_GATE, s, [&] { return launch_gate_tc(d, L->maps, L->ws, *x_map, s); });
+  }
+  d.SK = 1;
+  L->last_sk = 1;
+  return run(L, K_GATE, s, [&] { return launch_gate_simt(d, L->w, L->ws, x, 0, s); });
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t epoch_workspace_bytes(const epoch_layer_config *cfg) {
+  if (!valid_config(cfg)) return 0;
+  return carve(*cfg, nullptr, nullptr);
+}
+
+epoch_status epoch_layer_create(const epoch_layer_config *cfg, const epoch_layer_weights *w, void *workspace,
+                                size_t bytes, epoch_layer **out) {
+  if (out == nullptr || w == nullptr || !valid_config(cfg)) return EPOCH_EINVAL;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1))) return EPOCH_EINVAL;
+  if (bytes < carve(*cfg, nullptr, nullptr)) return EPOCH_EINVAL;
+  if (!aligned16(w->w_router) || !aligned16(w->b_router) || !aligned16(w->w_gate) || !aligned16(w->w_up) ||
+      !aligned16(w->w_down))
+    return EPOCH_EINVAL;
+  if (cfg->n_shared > 0 && (!aligned16(w->ws_gate) || !aligned16(w->ws_up) || !aligned16(w->ws_down)))
+    return EPOCH_EINVAL;
+  epoch_layer *L = new (std::nothrow) epoch_layer();
+  if (L == nullptr) return EPOCH_ECUDA;
+  L->cfg = *cfg;
+  L->bf16 = cfg->dtype == EPOCH_BF16;
+  L->sk_max = sk_max_for(*cfg);
+  L->last_sk = 1;
+  carve(*cfg, static_cast<char *>(workspace), &L->ws);
+  L->w = Weights{w->w_router, w->b_router, w->w_gate, w->w_up, w->w_down, w->ws_gate, w->ws_up, w->ws_down};
+  Dims &d = L->dims;
+  memset(&d, 0, sizeof(d));
+  d.H = cfg->hidden;
+  d.E = cfg->n_experts;
+  d.I = cfg->inter;
+  d.k = cfg->top_k;
+  d.n_sh = cfg->n_shared;
+  d.I_s = cfg->n_shared ? cfg->shared_inter : 128;
+  d.Nmax = cfg->max_positions;
+  d.SK = 1;
+  d.R = cfg->refresh_R;
+  d.residual = cfg->residual ? 1 : 0;
+  d.tn_up = L->bf16 ? 128 : 0;
+  d.tn_dn = L->bf16 ? 128 : 0;
+  d.timeout_ns = 2000000000ll;
+  memset(&L->maps, 0, sizeof(L->maps));
+  if (L->bf16) {
+    if (!tma_encode_init()) {
+      delete L;
+      return EPOCH_ECUDA;
+    }
+    const uint64_t H = d.H, E = d.E, I = d.I, N = d.Nmax, k = d.k, nsh = d.n_sh, Is = d.I_s;
+    bool ok = encode_kmajor_bf16(&L->maps.w_router, w->w_router, H, E, 128) &&
+              encode_kmajor_bf16(&L->maps.w_gate, w->w_gate, H, E * I, 128) &&
+              encode_kmajor_bf16(&L->maps.w_up, w->w_up, H, E * I, 128) &&
+              encode_kmajor_bf16(&L->maps.w_down, w->w_down, I, E * H, 128) &&
+              encode_kmajor_bf16(&L->maps.xp, L->ws.xp, H, N * k, d.tn_up) &&
+              encode_kmajor_bf16(&L->maps.a_int, L->ws.a_int, I, N * k, d.tn_dn);
+    if (ok && nsh > 0) {
+      ok = encode_kmajor_bf16(&L->maps.ws_gate, w->ws_gate, H, nsh * Is, 128) &&
+           encode_kmajor_bf16(&L->maps.ws_up, w->ws_up, H, nsh * Is, 128) &&
+           encode_kmajor_bf16(&L->maps.ws_down, w->ws_down, Is, nsh * H, 128) &&
+           encode_kmajor_bf16(&L->maps.a_sh, L->ws.a_sh, Is, nsh * N, d.tn_dn);
+    }
+    if (!ok) {
+      delete L;
+      return EPOCH_EINVAL;
+    }
+  }
+  // empty cache, no plan: zero the workspace, stamps = -1, support = every expert
+  if (cudaMemset(workspace, 0, bytes) != cudaSuccess ||
+      cudaMemset(L->ws.stamp, 0xFF, sizeof(int32_t) * d.Nmax) != cudaSuccess ||
+      cudaMemset(L->ws.support_mask, 1, d.E) != cudaSuccess) {
+    delete L;
+    return EPOCH_ECUDA;
+  }
+  Ctrl c0;
+  memset(&c0, 0, sizeof(c0));
+  c0.support_len = d.E;
+  if (cudaMemcpy(L->ws.ctrl, &c0, sizeof(c0), cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    delete L;
+    return EPOCH_ECUDA;
+  }
+  L->planned = false;
+  L->n_pos_plan = 0;
+  L->last_iter = -1;
+  L->prof = false;
+  for (int i = 0; i < K_NUM; ++i) {
+    L->total_ms[i] = 0.0;
+    L->launches[i] = 0;
+  }
+  *out = L;
+  return EPOCH_OK;
+}
+
+epoch_status epoch_plan_block(epoch_layer *L, const void *x, int32_t n_pos, epoch_stream stream) {
+  if (L == nullptr || !aligned16(x) || n_pos < 1 || n_pos > L->cfg.max_positions) return EPOCH_EINVAL;
+  cudaStream_t s = S(stream);
+  Dims d = call_dims(L, n_pos, 0, 0);
+  CUtensorMap x_map;
+  EPOCH_TRY(run_gate(L, d, x, &x_map, s));
+  if (cudaMemsetAsync(L->ws.plan_counts, 0, sizeof(int32_t) * d.E, s) != cudaSuccess) return EPOCH_ECUDA;
+  EPOCH_TRY(run(L, K_PLAN_TOPK, s, [&] { return launch_plan_topk(d, L->w, L->ws, s); }));
+  const double tau = L->cfg.tau;
+  const int all = tau >= 1.0;
+  const int32_t T = static_cast<int32_t>(std::ceil(tau * static_cast<double>(n_pos * L->cfg.top_k)));
+  EPOCH_TRY(run(L, K_PLAN_SUPPORT, s, [&] { return launch_plan_support(d, L->ws, T, all, s); }));
+  L->planned = true;
+  L->n_pos_plan = n_pos;
+  L->last_iter = -1;
+  ++L->n_cold;
+  return EPOCH_OK;
+}
+
+epoch_status epoch_moe_iter(epoch_layer *L, const void *x, const uint8_t *live, const uint8_t *decoded,
+                            int32_t n_pos, int32_t iteration, void *y, epoch_stream stream) {
+  if (L == nullptr || !aligned16(x) || !aligned16(y) || live == nullptr || decoded == nullptr) return EPOCH_EINVAL;
+  if (n_pos < 1 || n_pos > L->cfg.max_positions || iteration < 0) return EPOCH_EINVAL;
+  cudaStream_t s = S(stream);
+  const int host_fallback = !L->planned || iteration != L->last_iter + 1 || n_pos != L->n_pos_plan;
+  Dims d = call_dims(L, n_pos, iteration, host_fallback);
+  CUtensorMap x_map;
+  EPOCH_TRY(run_gate(L, d, x, &x_map, s));
+  EPOCH_TRY(run(L, K_CLASSIFY, s, [&] { return launch_classify(d, L->ws, live, decoded, s); }));
+  EPOCH_TRY(run(L, K_ROUTE, s, [&] { return launch_route(d, L->w, L->ws, s); }));
+  EPOCH_TRY(run(L, K_WORKLIST, s, [&] { return launch_worklist(d, L->ws, s); }));
+  EPOCH_TRY(run(L, K_PERMUTE, s, [&] { return launch_permute(d, L->ws, x, L->bf16, s); }));
+  if (L->bf16) {
+    EPOCH_TRY(run(L, K_UP, s, [&] { return launch_up_tc(d, L->maps, L->ws, x_map, s); }));
+    EPOCH_TRY(run(L, K_DOWN, s, [&] { return launch_down_tc(d, L->maps, L->ws, s); }));
+  } else {
+    EPOCH_TRY(run(L, K_UP, s, [&] { return launch_up_simt(d, L->w, L->ws, x, s); }));
+    EPOCH_TRY(run(L, K_DOWN, s, [&] { return launch_down_simt(d, L->w, L->ws, s); }));
+  }
+  EPOCH_TRY(run(L, K_COMBINE, s, [&] { return launch_combine(d, L->ws, x, y, L->bf16, s); }));
+  L->last_iter = iteration;
+  if (host_fallback) ++L->n_fallback;
+  else ++L->n_hot;
+  return EPOCH_OK;
+}
+
+epoch_status epoch_block_end(epoch_layer *L) {
+  if (L == nullptr) return EPOCH_EINVAL;
+  L->planned = false;
+  return EPOCH_OK;
+}
+
+epoch_status epoch_get_status(epoch_layer *L, epoch_stream stream, uint32_t *word_out) {
+  if (L == nullptr) return EPOCH_EINVAL;
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, L->ws.err, sizeof(word), cudaMemcpyDeviceToHost, S(stream)) != cudaSuccess ||
+      cudaStreamSynchronize(S(stream)) != cudaSuccess)
+    return EPOCH_ECUDA;
+  if (word_out) *word_out = word;
+  if (word & EPOCH_DEVERR_TIMEOUT) return EPOCH_ETIMEOUT;
+  return word ? EPOCH_EDEVICE : EPOCH_OK;
+}
+
+epoch_status epoch_clear_status(epoch_layer *L, epoch_stream stream) {
+  if (L == nullptr) return EPOCH_EINVAL;
+  return cudaMemsetAsync(L->ws.err, 0, sizeof(uint32_t), S(stream)) == cudaSuccess ? EPOCH_OK : EPOCH_ECUDA;
+}
+
+epoch_status epoch_read_stats(epoch_layer *L, epoch_iter_stats *out, epoch_stream stream) {
+  if (L == nullptr || out == nullptr) return EPOCH_EINVAL;
+  if (cudaMemcpyAsync(out, L->ws.stats, sizeof(*out), cudaMemcpyDeviceToHost, S(stream)) != cudaSuccess ||
+      cudaStreamSynchronize(S(stream)) != cudaSuccess)
+    return EPOCH_ECUDA;
+  return EPOCH_OK;
+}
+
+epoch_status epoch_debug_pointers(epoch_layer *L, epoch_debug_view *v) {
+  if (L == nullptr || v == nullptr) return EPOCH_EINVAL;
+  v->support_ids = L->ws.support_ids;
+  v->support_len = &L->ws.ctrl->support_len;
+  v->plan_counts = L->ws.plan_counts;
+  v->logit_parts = L->ws.gparts;
+  v->n_logit_parts = L->last_sk;
+  v->fresh_pos = L->ws.fresh_pos;
+  v->sel = L->ws.sel;
+  v->sel_w = L->ws.selw;
+  v->offsets = L->ws.offsets;
+  v->wl_pos = L->ws.wl_pos;
+  v->slot = L->ws.slot;
+  v->stamp = L->ws.stamp;
+  v->cache = L->ws.cache;
+  v->stats = L->ws.stats;
+  v->error_word = L->ws.err;
+  return EPOCH_OK;
+}
+
+epoch_status epoch_debug_copy(void *host_dst, const void *dev_src, size_t bytes, epoch_stream stream) {
+  if (host_dst == nullptr || dev_src == nullptr) return EPOCH_EINVAL;
+  if (bytes == 0) return EPOCH_OK;
+  if (cudaMemcpyAsync(host_dst, dev_src, bytes, cudaMemcpyDeviceToHost, S(stream)) != cudaSuccess ||
+      cudaStreamSynchronize(S(stream)) != cudaSuccess)
+    return EPOCH_ECUDA;
+  return EPOCH_OK;
+}
+
+epoch_status epoch_path_counters(epoch_layer *L, int64_t *cold, int64_t *hot, int64_t *fallback) {
+  if (L == nullptr) return EPOCH_EINVAL;
+  if (cold) *cold = L->n_cold;
+  if (hot) *hot = L->n_hot;
+  if (fallback) *fallback = L->n_fallback;
+  return EPOCH_OK;
+}
+
+epoch_status epoch_set_wait_timeout(epoch_layer *L, int64_t timeout_ns) {
+  if (L == nullptr || timeout_ns < 1000) return EPOCH_EINVAL;
+  L->dims.timeout_ns = timeout_ns;
+  return EPOCH_OK;
+}
+
+epoch_status epoch_set_profiling(epoch_layer *L, int32_t enable) {
+  if (L == nullptr) return EPOCH_EINVAL;
+  L->prof = enable != 0;
+  return EPOCH_OK;
+}
+
+epoch_status epoch_read_profile(epoch_layer *L, epoch_profile *out) {
+  if (L == nullptr || out == nullptr) return EPOCH_EINVAL;
+  for (auto &p : L->pending) {
+    if (cudaEventSynchronize(p.b) != cudaSuccess) return EPOCH_ECUDA;
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, p.a, p.b);
+    L->total_ms[p.kind] += ms;
+    L->launches[p.kind] += 1;
+    L->pool.push_back(p.a);
+    L->pool.push_back(p.b);
+  }
+  L->pending.clear();
+  for (int i = 0; i < EPOCH_PROF_KINDS; ++i) {
+    out->name[i] = i < K_NUM ? kKindName[i] : "";
+    out->launches[i] = i < K_NUM ? L->launches[i] : 0;
+    out->total_ms[i] = i < K_NUM ? L->total_ms[i] : 0.0;
+  }
+  out->kernels_launched = L->n_launch;
+  return EPOCH_OK;
+}
+
+epoch_status epoch_reset_profile(epoch_layer *L) {
+  if (L == nullptr) return EPOCH_EINVAL;
+  epoch_profile tmp;
+  const epoch_status st = epoch_read_profile(L, &tmp);
+  for (int i = 0; i < K_NUM; ++i) {
+    L->total_ms[i] = 0.0;
+    L->launches[i] = 0;
+  }
+  return st;
+}
+
+epoch_status epoch_test_wait_timeout(epoch_layer *L, int64_t timeout_ns, epoch_stream stream) {
+  if (L == nullptr || timeout_ns < 1000 || timeout_ns > 5000000000ll) return EPOCH_EINVAL;
+  return run(L, K_TEST, S(stream), [&] { return launch_wait_test(L->ws.err, timeout_ns, S(stream)); });
+}
+
+void epoch_layer_destroy(epoch_layer *L) {
+  if (L == nullptr) return;
+  for (auto &p : L->pending) {
+    cudaEventDestroy(p.a);
+    cudaEventDestroy(p.b);
+  }
+  for (auto e : L->pool) cudaEventDestroy(e);
+  delete L;
+}
+
+const char *epoch_status_str(epoch_status s) {
+  switch (s) {
+    case EPOCH_OK: return "ok";
+    case EPOCH_EINVAL: return "invalid argument";
+    case EPOCH_ESTATE: return "invalid state";
+    case EPOCH_ECUDA: return "CUDA runtime error";
+    case EPOCH_ETIMEOUT: return "device wait timed out";
+    case EPOCH_EDEVICE: return "device-detected error";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,439 @@
+// tcgen05 + TMA grouped GEMMs of the Epoch MoE layer (bf16 in, fp32 accumulate).
+//
+// Three contractions share one persistent, warp-specialised kernel:
+//   GATE  G^T = W_r x^T, split along H (the route kernel sums the splits in a
+//         fixed order and adds the bias) -- router logits for every position
+//         ([W] section "Expert Atlas": G in R^{N x E}, recomputed every iteration);
+//   UP    per group g: A_g = silu(X_g W_gate,g^T) * (X_g W_up,g^T) -> bf16;
+//   DOWN  per group g: O_g = A_g W_down,g^T -> fp32.
+// Groups are the routed experts with at least one worklist row, then the
+// shared experts over every position; each routed expert runs once over its
+// compact rows (the "light-traffic expert kernel" of [W] section
+// "FreshLane Dispatch"); experts with no row produce no tile, so their weights
+// are never read ("invalid slots load no expert weights", same section).
+// [W] = walk-through page "Epoch 完全拆解:把扩散块编译成稀疏 MoE 服务单元".
+//
+// Swap-AB: weight rows are the MMA M dimension (128) and tokens the N
+// dimension (16..TN, rounded up to 16 per tile), because an expert may hold
+// from one to a thousand rows. Roles per CTA (192 threads): warp 0 issues TMA
+// loads into a STAGES-deep shared-memory ring (128-byte swizzle, K-major),
+// warp 1 issues tcgen05.mma into TMEM accumulators (double-buffered when they
+// fit, so the epilogue of one tile overlaps the next tile's main loop), warps
+// 2-5 read TMEM with tcgen05.ld and store. One CTA per SM, persistent over a
+// device-resident tile count: no host synchronisation.
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
+#include "common.cuh"
+#include "layer.h"
+
+namespace epoch {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+
+enum Mode { M_GATE = 0, M_UP = 1, M_DOWN = 2 };
+
+struct __align__(128) TcParams {
+  CUtensorMap a0;   // GATE: W_r; UP: W_gate (routed); DOWN: W_down (routed)
+  CUtensorMap a1;   // UP: W_up (routed)
+  CUtensorMap a0s;  // UP: W_gate (shared); DOWN: W_down (shared)
+  CUtensorMap a1s;  // UP: W_up (shared)
+  CUtensorMap b;    // GATE: x; UP: Xp; DOWN: A (routed)
+  CUtensorMap bs;   // UP: x; DOWN: A (shared)
+  Dims d;
+  Work ws;
+  int32_t gate_tiles;
+};
+
+template <int MODE, int TN, int STAGES>
+struct Cfg {
+  static constexpr int NA = MODE == M_UP ? 2 : 1;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = TN * BK * 2;
+  static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES;
+  static constexpr int ACC_COLS = NA * TN;
+  static constexpr int NBUF = 2 * ACC_COLS <= 512 ? 2 : 1;
+  static constexpr int USED_COLS = NBUF * ACC_COLS;
+  static constexpr int TMEM_COLS = USED_COLS <= 32 ? 32 : USED_COLS <= 64 ? 64 : USED_COLS <= 128 ? 128
+                                   : USED_COLS <= 256 ? 256 : 512;
+  static constexpr int NBARS = 2 * STAGES + 2 * NBUF + 1;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + NBARS * 8 + 16;
+  static_assert(TN % 16 == 0 && TN >= 16 && TN <= 256, "MMA N");
+  static_assert(USED_COLS <= 512, "TMEM");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+struct Tile {
+  int a_row, b_row;   // rows in the A (weights) and B (tokens) tensor maps
+  int shared;         // group is a shared expert (selects the *s maps)
+  int k0, nk;         // first K element, number of BK blocks
+  int n_valid;        // valid token columns
+  int out_row0;       // output row of column 0
+  int out_rows;       // rows in the output buffer (bounds check)
+  int ld;             // output leading dimension
+  int col0;           // output column of MMA row 0
+  int m_limit;        // valid MMA rows
+  void *out;
+};
+
+__device__ __forceinline__ int group_of(const int32_t *__restrict__ off, int G, int tile) {
+  int lo = 0, hi = G;  // off[lo] <= tile < off[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (off[mid] <= tile) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
+template <int MODE, int TN>
+__device__ __forceinline__ Tile decode(const TcParams &p, int tile) {
+  const Dims &d = p.d;
+  const Work &ws = p.ws;
+  Tile t;
+  if (MODE == M_GATE) {
+    const int mt = (d.E + BM - 1) / BM, nt = (d.n_pos + TN - 1) / TN;
+    const int ks = tile / (mt * nt), rem = tile % (mt * nt);
+    const int m = rem / nt, tt = rem % nt;
+    const int kspan = d.H / d.SK;
+    t.a_row = m * BM;
+    t.b_row = tt * TN;
+    t.shared = 0;
+    t.k0 = ks * kspan;
+    t.nk = kspan / BK;
+    t.n_valid = min(TN, d.n_pos - tt * TN);
+    t.out_row0 = tt * TN;
+    t.out_rows = d.Nmax;
+    t.ld = d.E;
+    t.col0 = m * BM;
+    t.m_limit = min(BM, d.E - m * BM);
+    t.out = ws.gparts + static_cast<size_t>(ks) * d.Nmax * d.E;
+    return t;
+  }
+  const int G = d.E + d.n_sh;
+  const int32_t *off = MODE == M_UP ? ws.tile_off_up : ws.tile_off_dn;
+  const int g = group_of(off, G, tile);
+  const int rows = ws.grp_rows[g], row0 = ws.grp_row0[g];
+  const int nt = (rows + TN - 1) / TN;
+  const int local = tile - off[g];
+  const int m = local / nt, tt = local % nt;
+  t.shared = g >= d.E;
+  const int s = g - d.E;
+  t.n_valid = min(TN, rows - tt * TN);
+  t.col0 = m * BM;
+  t.m_limit = BM;
+  t.k0 = 0;
+  t.out_row0 = row0 + tt * TN;
+  if (MODE == M_UP) {
+    t.a_row = t.shared ? s * d.I_s + m * BM : g * d.I + m * BM;
+    t.b_row = t.shared ? tt * TN : row0 + tt * TN;
+    t.nk = d.H / BK;
+    t.ld = t.shared ? d.I_s : d.I;
+    t.out = t.shared ? ws.a_sh : ws.a_int;
+    t.out_rows = t.shared ? d.n_sh * d.Nmax : d.Nmax * d.k;
+  } else {
+    t.a_row = t.shared ? s * d.H + m * BM : g * d.H + m * BM;
+    t.b_row = row0 + tt * TN;
+    t.nk = (t.shared ? d.I_s : d.I) / BK;
+    t.ld = d.H;
+    t.out = t.shared ? static_cast<void *>(ws.o_sh) : static_cast<void *>(ws.o_int);
+    t.out_rows = t.shared ? d.n_sh * d.Nmax : d.Nmax * d.k;
+  }
+  return t;
+}
+
+// Waits for a phase without the abort check (teardown after an abort: lets
+// copies and MMAs already issued land before the CTA exits).
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint64_t ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > ns) return;
+  }
+}
+
+template <int MODE, int TN, int STAGES>
+__global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcParams p) {
+  using C = Cfg<MODE, TN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sA = sbase;                                   // [STAGES][NA] A tiles
+  const uint32_t sB = sbase + STAGES * C::NA * C::A_BYTES;     // [STAGES] B tiles
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * C::STAGE_BYTES);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + C::NBUF + b); };
+  const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 2 * C::NBUF);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::NBARS);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const Dims &d = p.d;
+  const Work &ws = p.ws;
+  const int total = MODE == M_GATE ? p.gate_tiles : (MODE == M_UP ? ws.ctrl->tiles_up : ws.ctrl->tiles_dn);
+  if (static_cast<int>(blockIdx.x) >= total) return;
+  const int wid = warp_id(), lane = lane_id();
+  const uint64_t tmo = static_cast<uint64_t>(d.timeout_ns);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < C::NBUF; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 128);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (wid == 0) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (wid == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      tma_prefetch_desc(&p.a0);
+      tma_prefetch_desc(&p.b);
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_b = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const Tile t = decode<MODE, TN>(p, tile);
+        const CUtensorMap *ma0 = t.shared ? &p.a0s : &p.a0;
+        const CUtensorMap *ma1 = t.shared ? &p.a1s : &p.a1;
+        const CUtensorMap *mb = t.shared ? &p.bs : &p.b;
+        for (int kb = 0; kb < t.nk; ++kb) {
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, ws.err, tmo)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar(stage), C::STAGE_BYTES);
+          const int kc = t.k0 + kb * BK;
+          const uint32_t a_dst = sA + stage * C::NA * C::A_BYTES;
+          tma_load_2d(a_dst, ma0, kc, t.a_row, full_bar(stage), pol_w);
+          if (C::NA == 2) tma_load_2d(a_dst + C::A_BYTES, ma1, kc, t.a_row, full_bar(stage), pol_w);
+          tma_load_2d(sB + stage * C::B_BYTES, mb, kc, t.b_row, full_bar(stage), pol_b);
+          armed |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < STAGES; ++s)
+          if (armed & (1u << s)) mbar_drain(full_bar(s), (armed_par >> s) & 1u, 50000000ull);
+      }
+    }
+  } else if (wid == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      int stage = 0, buf = 0;
+      uint32_t phase = 0, bphase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const Tile t = decode<MODE, TN>(p, tile);
+        const int n_mma = ((t.n_valid + 15) / 16) * 16;
+        const uint32_t idesc = idesc_bf16_f32(BM, n_mma);
+        if (!mbar_wait_bounded(tempty_bar(buf), bphase ^ 1u, abort_flag, ws.err, tmo)) break;
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + static_cast<uint32_t>(buf * C::ACC_COLS);
+        for (int kb = 0; kb < t.nk; ++kb) {
+          if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, ws.err, tmo)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_src = sA + stage * C::NA * C::A_BYTES;
+          const uint64_t ad0 = sw128_kmajor_desc(a_src);
+          const uint64_t ad1 = sw128_kmajor_desc(a_src + C::A_BYTES);
+          const uint64_t bd = sw128_kmajor_desc(sB + stage * C::B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint32_t acc = (kb | kk) != 0;
+            tc_mma_bf16(d0, ad0 + 2u * kk, bd + 2u * kk, idesc, acc);
+            if (C::NA == 2) tc_mma_bf16(d0 + TN, ad1 + 2u * kk, bd + 2u * kk, idesc, acc);
+          }
+          tc_commit(empty_bar(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(tfull_bar(buf));
+        if (++buf == C::NBUF) {
+          buf = 0;
+          bphase ^= 1u;
+        }
+      }
+      tc_commit(done_bar);
+      mbar_drain(done_bar, 0, 50000000ull);
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5; warp w reads TMEM lanes 32*(w%4)..)
+    const int q = wid & 3;
+    const int row = q * 32 + lane;
+    int buf = 0;
+    uint32_t bphase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const Tile t = decode<MODE, TN>(p, tile);
+      if (!mbar_wait_bounded(tfull_bar(buf), bphase, abort_flag, ws.err, tmo)) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * C::ACC_COLS);
+      for (int c0 = 0; c0 < t.n_valid; c0 += 16) {
+        float v0[16], v1[16];
+        tmem_ld16(tb + c0, v0);
+        if (C::NA == 2) tmem_ld16(tb + TN + c0, v1);
+        tmem_ld_wait();
+        if (row < t.m_limit) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int orow = t.out_row0 + c0 + c;
+            if (c0 + c < t.n_valid) {
+              if (orow < 0 || orow >= t.out_rows) {
+                set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+                continue;
+              }
+              const size_t o = static_cast<size_t>(orow) * t.ld + t.col0 + row;
+              if (MODE == M_UP) {
+                static_cast<__nv_bfloat16 *>(t.out)[o] = __float2bfloat16_rn(silu(v0[c]) * v1[c]);
+              } else {
+                static_cast<float *>(t.out)[o] = v0[c];
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty_bar(buf));
+      if (++buf == C::NBUF) {
+        buf = 0;
+        bphase ^= 1u;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (wid == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool tma_encode_init() {
+  if (g_encode) return true;
+  void *fn = nullptr;
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return false;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+
+// Row-major [rows][k_elems] bf16 matrix, boxes of 64 (K) x box_rows, 128-byte swizzle.
+bool encode_kmajor_bf16(CUtensorMap *map, const void *base, uint64_t k_elems, uint64_t rows, uint32_t box_rows) {
+  if (!g_encode || base == nullptr || rows == 0) return false;
+  cuuint64_t dims[2] = {k_elems, rows};
+  cuuint64_t strides[1] = {k_elems * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+constexpr int kTnGate = 128, kStGate = 6;
+constexpr int kTnUp = 128, kStUp = 4;
+constexpr int kTnDn = 128, kStDn = 6;
+
+// Split count of the gate along H: enough (m, n, split) tiles to cover the SMs,
+// each split a whole number of 64-wide K blocks.
+int tc_gate_splits(const Dims &d) {
+  const int tiles_mn = ((d.E + BM - 1) / BM) * ((d.n_pos + kTnGate - 1) / kTnGate);
+  const int kb = d.H / BK;
+  int target = num_sms() / (tiles_mn > 0 ? tiles_mn : 1);
+  if (target < 1) target = 1;
+  if (target > 16) target = 16;
+  int sk = 1;
+  for (int c = 1; c <= target; ++c)
+    if (kb % c == 0) sk = c;
+  return sk;
+}
+
+template <int MODE, int TN, int STAGES>
+static cudaError_t launch_tc(const TcParams &p, int grid, cudaStream_t s) {
+  using C = Cfg<MODE, TN, STAGES>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(k_tc_gemm<MODE, TN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  k_tc_gemm<MODE, TN, STAGES><<<grid, 192, C::SMEM, s>>>(p);
+  return cudaGetLastError();
+}
+
+static void base_params(TcParams &p, const Dims &d, const Work &ws) {
+  memset(&p, 0, sizeof(p));
+  p.d = d;
+  p.ws = ws;
+}
+
+cudaError_t launch_gate_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map,
+                           cudaStream_t s) {
+  TcParams p;
+  base_params(p, d, ws);
+  p.a0 = m.w_router;
+  p.b = x_map;
+  const int tiles = ((d.E + BM - 1) / BM) * ((d.n_pos + kTnGate - 1) / kTnGate) * d.SK;
+  p.gate_tiles = tiles;
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  return launch_tc<M_GATE, kTnGate, kStGate>(p, grid, s);
+}
+
+cudaError_t launch_up_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map,
+                         cudaStream_t s) {
+  TcParams p;
+  base_params(p, d, ws);
+  p.a0 = m.w_gate;
+  p.a1 = m.w_up;
+  p.a0s = m.ws_gate;
+  p.a1s = m.ws_up;
+  p.b = m.xp;
+  p.bs = x_map;
+  return launch_tc<M_UP, kTnUp, kStUp>(p, num_sms(), s);
+}
+
+cudaError_t launch_down_tc(const Dims &d, const Maps &m, const Work &ws, cudaStream_t s) {
+  TcParams p;
+  base_params(p, d, ws);
+  p.a0 = m.w_down;
+  p.a0s = m.ws_down;
+  p.b = m.a_int;
+  p.bs = m.a_sh;
+  return launch_tc<M_DOWN, kTnDn, kStDn>(p, num_sms(), s);
+}
+
+}  // namespace epoch

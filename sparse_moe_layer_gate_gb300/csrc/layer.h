@@ -1,0 +1,130 @@
+// Internal layout of an Epoch MoE layer: workspace carve-up, per-call
+// arguments passed to the kernels, and the launchers each .cu file exports.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "epoch.h"
+
+namespace epoch {
+
+// Device-resident control values of one iteration (no host sync inside a call).
+struct Ctrl {
+  int32_t n_fresh;      // |F_i|
+  int32_t fallback;     // bit 0 host mismatch, bit 1 device-detected anomaly
+  int32_t n_edges;      // L = k |F_i|
+  int32_t n_hit;        // experts with at least one edge
+  int32_t tiles_up;     // grouped-GEMM tiles (routed + shared)
+  int32_t tiles_dn;
+  int32_t support_len;  // |S| of the current plan
+  int32_t pad;
+};
+
+// Device pointers carved from the caller's workspace.
+struct Work {
+  // block-lifetime state
+  int32_t *stamp;         // [Nmax] iteration of the row's last fresh compute, -1 none
+  uint8_t *prev_dec;      // [Nmax] decoded at the previous iteration
+  uint8_t *support_mask;  // [E]
+  int32_t *support_ids;   // [E] ranked experts
+  int32_t *plan_counts;   // [E] block-start hit counts
+  void *cache;            // [Nmax][H] routed-output cache, layer dtype
+  // one iteration
+  float *gparts;          // [SK][Nmax][E] split-K partial logits (no bias)
+  int32_t *fidx;          // [Nmax] fresh index of a position, -1 if reused
+  int32_t *fresh_pos;     // [Nmax] ascending fresh positions
+  int32_t *sel;           // [Nmax][k]
+  float *selw;            // [Nmax][k]
+  uint32_t *chunk_mask;   // [Nmax/32][E] bit p: fresh position p of the chunk selected e
+  int32_t *offsets;       // [E+1]
+  int32_t *grp_rows;      // [G] rows of each grouped-GEMM group (routed experts, then shared)
+  int32_t *grp_row0;      // [G] first row of the group in the compact buffers
+  int32_t *tile_off_up;   // [G+1]
+  int32_t *tile_off_dn;   // [G+1]
+  int32_t *wl_pos;        // [Nmax*k] expert-sorted worklist positions
+  int32_t *slot;          // [Nmax][k] worklist row of selection (f, j)
+  void *xp;               // [Nmax*k][H] permuted fresh rows
+  void *a_int;            // [Nmax*k][I] SwiGLU activations of routed edges
+  void *a_sh;             // [n_sh*Nmax][I_s] SwiGLU activations of shared experts
+  float *o_int;           // [Nmax*k][H] routed expert outputs
+  float *o_sh;            // [n_sh*Nmax][H] shared expert outputs
+  Ctrl *ctrl;
+  epoch_iter_stats *stats;
+  uint32_t *err;
+};
+
+// Shapes and per-call values handed to every kernel by value.
+struct Dims {
+  int32_t H, E, I, k, n_sh, I_s, Nmax, SK;
+  int32_t R;         // refresh period (INT32_MAX = never)
+  int32_t residual;
+  int32_t n_pos;
+  int32_t iter;
+  int32_t host_fallback;
+  int32_t tn_up, tn_dn;  // token-tile width of the tcgen05 grouped GEMMs (0 on the SIMT path)
+  int64_t timeout_ns;
+};
+
+struct Weights {
+  const void *w_router;
+  const float *b_router;
+  const void *w_gate, *w_up, *w_down;
+  const void *ws_gate, *ws_up, *ws_down;
+};
+
+// TMA descriptors that stay valid for the layer's lifetime.
+struct Maps {
+  CUtensorMap w_router;   // [E][H], box 64 x 128
+  CUtensorMap w_gate;     // [E*I][H]
+  CUtensorMap w_up;       // [E*I][H]
+  CUtensorMap w_down;     // [E*H][I]
+  CUtensorMap ws_gate;    // [n_sh*I_s][H]
+  CUtensorMap ws_up;
+  CUtensorMap ws_down;    // [n_sh*H][I_s]
+  CUtensorMap xp;         // [Nmax*k][H], box 64 x tn_up
+  CUtensorMap a_int;      // [Nmax*k][I], box 64 x tn_dn
+  CUtensorMap a_sh;       // [n_sh*Nmax][I_s], box 64 x tn_dn
+};
+
+// Kernel kinds, for profiling and launch counting.
+enum Kind {
+  K_GATE = 0, K_PLAN_TOPK, K_PLAN_SUPPORT, K_CLASSIFY, K_ROUTE, K_WORKLIST, K_PERMUTE,
+  K_UP, K_DOWN, K_COMBINE, K_TEST, K_MEMSET, K_NUM
+};
+extern const char *const kKindName[K_NUM];
+
+// ------------------------------------------------------------ launchers
+// route.cu
+cudaError_t launch_gate_simt(const Dims &d, const Weights &w, const Work &ws, const void *x, int bf16,
+                             cudaStream_t s);
+cudaError_t launch_plan_topk(const Dims &d, const Weights &w, const Work &ws, cudaStream_t s);
+cudaError_t launch_plan_support(const Dims &d, const Work &ws, int32_t threshold, int all_experts,
+                                cudaStream_t s);
+cudaError_t launch_classify(const Dims &d, const Work &ws, const uint8_t *live, const uint8_t *decoded,
+                            cudaStream_t s);
+cudaError_t launch_route(const Dims &d, const Weights &w, const Work &ws, cudaStream_t s);
+cudaError_t launch_worklist(const Dims &d, const Work &ws, cudaStream_t s);
+cudaError_t launch_permute(const Dims &d, const Work &ws, const void *x, int bf16, cudaStream_t s);
+cudaError_t launch_combine(const Dims &d, const Work &ws, const void *x, void *y, int bf16, cudaStream_t s);
+cudaError_t launch_wait_test(uint32_t *err, int64_t timeout_ns, cudaStream_t s);
+
+// gemm_simt.cu (fp32 layers)
+cudaError_t launch_up_simt(const Dims &d, const Weights &w, const Work &ws, const void *x, cudaStream_t s);
+cudaError_t launch_down_simt(const Dims &d, const Weights &w, const Work &ws, cudaStream_t s);
+
+// gemm_tc.cu (bf16 layers, tcgen05 + TMA)
+bool tma_encode_init();
+bool encode_kmajor_bf16(CUtensorMap *map, const void *base, uint64_t k_elems, uint64_t rows, uint32_t box_rows);
+int tc_gate_splits(const Dims &d);
+cudaError_t launch_gate_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map,
+                           cudaStream_t s);
+cudaError_t launch_up_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map,
+                         cudaStream_t s);
+cudaError_t launch_down_tc(const Dims &d, const Maps &m, const Work &ws, cudaStream_t s);
+
+int num_sms();
+
+}  // namespace epoch

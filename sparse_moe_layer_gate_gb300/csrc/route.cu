@@ -1,0 +1,655 @@
+// Routing side of the Epoch MoE-layer iteration (sm_103a): block plan,
+// liveness classification and compaction, support-restricted top-k, the
+// expert-sorted worklist, the permute into compact rows, and the weighted
+// combine with the routed-output cache.
+//
+// Source: walk-through page "Epoch 完全拆解:把扩散块编译成稀疏 MoE 服务单元" ([W]):
+//   section "Expert Atlas" (G in R^{N x E}; the hot path keeps the support as a
+//   mask and re-runs the top-k rule over it every iteration), section
+//   "Liveness-Shard Parallelism" (Z_i, N_i, F_i; B_i = Compact(H, F_i);
+//   Y[F_i] = Y_F, Y[not F_i] = C_l[not F_i]), section "FreshLane Dispatch"
+//   (pack, count exchange -> offsets, light-traffic expert kernel, combine by
+//   compact offset, scatter/merge), section "cold、hot-update、hot-skip"
+//   (cold path clears the per-block cache and builds the support).
+#include <cfloat>
+#include <climits>
+
+#include "common.cuh"
+#include "layer.h"
+
+namespace epoch {
+
+const char *const kKindName[K_NUM] = {"gate",     "plan_topk", "plan_support", "classify",
+                                      "route",    "worklist",  "permute",      "expert_up",
+                                      "expert_down", "combine", "wait_test",   "memset"};
+
+// ---------------------------------------------------------------- helpers
+
+// (value desc, id asc) order used for every top-k: true if (va, ia) ranks first.
+__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+// Warp-wide arg-best of (v, id) pairs; every lane returns the winner.
+__device__ __forceinline__ void warp_best(float &v, int &id) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, id, o);
+    if (ranks_before(ov, oi, v, id)) {
+      v = ov;
+      id = oi;
+    }
+  }
+}
+
+// Logit of expert e at position t: split-K partial sums in fixed order, then the bias.
+__device__ __forceinline__ float logit(const float *__restrict__ gparts, int SK, int Nmax, int E, int t, int e,
+                                       const float *__restrict__ bias) {
+  float g = gparts[static_cast<size_t>(t) * E + e];
+  for (int s = 1; s < SK; ++s) g += gparts[(static_cast<size_t>(s) * Nmax + t) * E + e];
+  return g + bias[e];
+}
+
+// Top-k of one position by one warp. Lane l owns experts l, l+32, ... Ineligible
+// experts never win. Writes sel/val (selection order) on every lane.
+template <int EPL>
+__device__ __forceinline__ void warp_topk(const float (&v)[EPL], const bool (&ok)[EPL], int k, int *sel,
+                                          float *val) {
+  bool taken[EPL];
+#pragma unroll
+  for (int c = 0; c < EPL; ++c) taken[c] = !ok[c];
+  const int lane = lane_id();
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+#pragma unroll
+    for (int c = 0; c < EPL; ++c) {
+      const int e = lane + 32 * c;
+      if (!taken[c] && ranks_before(v[c], e, bv, bi)) {
+        bv = v[c];
+        bi = e;
+      }
+    }
+    warp_best(bv, bi);
+    sel[j] = bi;
+    val[j] = bv;
+#pragma unroll
+    for (int c = 0; c < EPL; ++c)
+      if (lane + 32 * c == bi) taken[c] = true;
+  }
+}
+
+// ---------------------------------------------------------------- gate (SIMT)
+// G part 0 = x W_r^T for fp32 layers: one warp per (position, expert), lanes
+// split H, fixed-order reduction (deterministic).
+template <typename T>
+__global__ void k_gate_simt(Dims d, const T *__restrict__ x, const T *__restrict__ wr, float *__restrict__ g) {
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int lane = lane_id();
+  for (int o = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; o < d.n_pos * d.E; o += warps) {
+    const int t = o / d.E, e = o % d.E;
+    const T *xr = x + static_cast<size_t>(t) * d.H;
+    const T *wrow = wr + static_cast<size_t>(e) * d.H;
+    float acc = 0.f;
+    for (int h = lane; h < d.H; h += 32) acc = fmaf(to_f32(xr[h]), to_f32(wrow[h]), acc);
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (lane == 0) g[static_cast<size_t>(t) * d.E + e] = acc;
+  }
+}
+
+// ---------------------------------------------------------------- block plan
+// Dense top-k of every position over all experts -> hit counts (integer atomics).
+template <int EPL>
+__global__ void k_plan_topk(Dims d, const float *__restrict__ gparts, const float *__restrict__ bias,
+                            int32_t *__restrict__ counts) {
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int lane = lane_id();
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < d.n_pos; t += warps) {
+    float v[EPL];
+    bool ok[EPL];
+#pragma unroll
+    for (int c = 0; c < EPL; ++c) {
+      const int e = lane + 32 * c;
+      ok[c] = e < d.E;
+      v[c] = ok[c] ? logit(gparts, d.SK, d.Nmax, d.E, t, e, bias) : -INFINITY;
+    }
+    int sel[16];
+    float val[16];
+    warp_topk<EPL>(v, ok, d.k, sel, val);
+    if (lane < d.k) {
+      int mine = 0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (j == lane) mine = sel[j];
+      atomicAdd(&counts[mine], 1);
+    }
+  }
+}
+
+// One CTA: rank experts by (count desc, id asc), take the smallest prefix whose
+// counts reach `threshold` (at least k; every expert when all_experts), and
+// clear the block's stamps and previous-decoded flags (cold path).
+__global__ void __launch_bounds__(1024) k_plan_support(Dims d, Work ws, int32_t threshold, int all_experts) {
+  __shared__ int32_t cnt[1024];
+  __shared__ int32_t sorted_cnt[1024];
+  __shared__ int32_t len_s;
+  const int tid = threadIdx.x;
+  const int E = d.E;
+  if (tid < E) cnt[tid] = ws.plan_counts[tid];
+  if (tid == 0) len_s = E;
+  __syncthreads();
+  if (tid < E) {
+    const int c = cnt[tid];
+    int rank = 0;
+    for (int e = 0; e < E; ++e) {
+      const int ce = cnt[e];
+      rank += (ce > c) || (ce == c && e < tid);
+    }
+    ws.support_ids[rank] = tid;
+    sorted_cnt[rank] = c;
+  }
+  __syncthreads();
+  // inclusive prefix of the ranked counts (E <= 1024, simple Hillis-Steele)
+  for (int off = 1; off < E; off <<= 1) {
+    int add = 0;
+    if (tid < E && tid >= off) add = sorted_cnt[tid - off];
+    __syncthreads();
+    if (tid < E) sorted_cnt[tid] += add;
+    __syncthreads();
+  }
+  if (!all_experts && tid < E) {
+    const bool reach = sorted_cnt[tid] >= threshold;
+    const bool before = tid > 0 && sorted_cnt[tid - 1] >= threshold;
+    if (reach && !before) len_s = tid + 1;
+  }
+  __syncthreads();
+  int len = len_s;
+  if (len < d.k) len = d.k;
+  if (len > E) len = E;
+  if (tid < E) {
+    int rank = 0;
+    const int c = cnt[tid];
+    for (int e = 0; e < E; ++e) {
+      const int ce = cnt[e];
+      rank += (ce > c) || (ce == c && e < tid);
+    }
+    ws.support_mask[tid] = rank < len ? 1 : 0;
+  }
+  if (tid == 0) ws.ctrl->support_len = len;
+  for (int t = tid; t < d.Nmax; t += blockDim.x) {
+    ws.stamp[t] = -1;
+    ws.prev_dec[t] = 0;
+  }
+}
+
+// ---------------------------------------------------------------- classify + compact
+// One CTA of 1024 threads; thread j owns the consecutive positions
+// [j*c, (j+1)*c), so a block-wide exclusive scan keeps the fresh list ascending.
+__global__ void __launch_bounds__(1024) k_classify(Dims d, Work ws, const uint8_t *__restrict__ live,
+                                                   const uint8_t *__restrict__ decoded) {
+  constexpr int kThreads = 1024;
+  __shared__ int32_t warp_sum[32];
+  __shared__ int32_t cat[8];
+  const int tid = threadIdx.x;
+  if (tid < 8) cat[tid] = 0;
+  const int n = d.n_pos;
+  const int per = (n + kThreads - 1) / kThreads;
+  const int lo = min(tid * per, n), hi = min(lo + per, n);
+
+  // pass 1: liveness anomalies (decoded -> live) and malformed flags
+  int anomaly = 0, bad = 0;
+  for (int t = lo; t < hi; ++t) {
+    const bool lv = live[t] != 0, dc = decoded[t] != 0;
+    const bool is_live = lv || !dc;
+    bad += (lv == dc);
+    anomaly |= (is_live && ws.prev_dec[t]);
+  }
+  const int any_anomaly = __syncthreads_or(anomaly);
+  const bool force = d.host_fallback || any_anomaly;
+
+  // pass 2: categories and fresh flags
+  int nf = 0;
+  int c_live = 0, c_new = 0, c_miss = 0, c_stale = 0, c_forced = 0, c_reuse = 0;
+  for (int t = lo; t < hi; ++t) {
+    const bool lv = live[t] != 0, dc = decoded[t] != 0;
+    const bool is_live = lv || !dc;
+    const int st = ws.stamp[t];
+    bool fresh = true;
+    if (is_live) {
+      ++c_live;
+    } else if (!ws.prev_dec[t]) {
+      ++c_new;
+    } else if (st < 0) {
+      ++c_miss;
+    } else if (d.R != INT_MAX && d.iter - st >= d.R) {
+      ++c_stale;
+    } else if (force) {
+      ++c_forced;
+    } else {
+      ++c_reuse;
+      fresh = false;
+    }
+    nf += fresh;
+  }
+  // block exclusive scan of nf
+  const int lane = lane_id(), wid = warp_id();
+  int incl = nf;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sum[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int ws_v = warp_sum[lane];
+    int wi = ws_v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += v;
+    }
+    warp_sum[lane] = wi - ws_v;  // exclusive warp offsets
+  }
+  __syncthreads();
+  int f = warp_sum[wid] + incl - nf;
+
+  // pass 3: write the compact list, stamps and the new previous-decoded flags
+  for (int t = lo; t < hi; ++t) {
+    const bool lv = live[t] != 0, dc = decoded[t] != 0;
+    const bool is_live = lv || !dc;
+    const int st = ws.stamp[t];
+    const bool reuse = !is_live && ws.prev_dec[t] && st >= 0 && !(d.R != INT_MAX && d.iter - st >= d.R) && !force;
+    if (!reuse) {
+      ws.fresh_pos[f] = t;
+      ws.fidx[t] = f;
+      ws.stamp[t] = d.iter;
+      ++f;
+    } else {
+      ws.fidx[t] = -1;
+    }
+    ws.prev_dec[t] = is_live ? 0 : 1;
+  }
+  atomicAdd(&cat[0], c_live);
+  atomicAdd(&cat[1], c_new);
+  atomicAdd(&cat[2], c_miss);
+  atomicAdd(&cat[3], c_stale);
+  atomicAdd(&cat[4], c_forced);
+  atomicAdd(&cat[5], c_reuse);
+  atomicAdd(&cat[6], bad);
+  __syncthreads();
+  if (tid == 0) {
+    const int n_fresh = n - cat[5];
+    const int fb = (d.host_fallback ? 1 : 0) | (any_anomaly ? 2 : 0);
+    ws.ctrl->n_fresh = n_fresh;
+    ws.ctrl->fallback = fb;
+    ws.ctrl->n_edges = n_fresh * d.k;
+    epoch_iter_stats *st = ws.stats;
+    st->iteration = d.iter;
+    st->n_pos = n;
+    st->n_live = cat[0];
+    st->n_new = cat[1];
+    st->n_miss = cat[2];
+    st->n_stale = cat[3];
+    st->n_forced = cat[4];
+    st->n_reuse = cat[5];
+    st->n_fresh = n_fresh;
+    st->n_edges = n_fresh * d.k;
+    st->support_len = fb ? d.E : ws.ctrl->support_len;
+    st->fallback = fb;
+    st->bad_flags = cat[6];
+    if (cat[6]) set_error(ws.err, EPOCH_DEVERR_FLAGS);
+  }
+}
+
+// ---------------------------------------------------------------- restricted top-k
+// One CTA per chunk of 32 fresh positions (8 warps x 4 positions). Each fresh
+// position takes its top-k over the support (every expert on a fallback),
+// softmax weights over the selected logits, and marks bit p of the chunk's
+// per-expert mask; the masks give the worklist its offsets without sorting.
+template <int EPL>
+__global__ void __launch_bounds__(256) k_route(Dims d, Work ws, const float *__restrict__ bias) {
+  __shared__ uint32_t mask[1024];
+  const int chunk = blockIdx.x;
+  const int n_fresh = ws.ctrl->n_fresh;
+  if (chunk * 32 >= n_fresh) return;
+  for (int e = threadIdx.x; e < d.E; e += blockDim.x) mask[e] = 0;
+  __syncthreads();
+  const bool all = ws.ctrl->fallback != 0;
+  const int lane = lane_id(), wid = warp_id();
+  bool elig[EPL];
+#pragma unroll
+  for (int c = 0; c < EPL; ++c) {
+    const int e = lane + 32 * c;
+    elig[c] = e < d.E && (all || ws.support_mask[e]);
+  }
+  for (int p = wid * 4; p < wid * 4 + 4; ++p) {
+    const int f = chunk * 32 + p;
+    if (f >= n_fresh) break;
+    const int t = ws.fresh_pos[f];
+    float v[EPL];
+#pragma unroll
+    for (int c = 0; c < EPL; ++c) {
+      const int e = lane + 32 * c;
+      v[c] = elig[c] ? logit(ws.gparts, d.SK, d.Nmax, d.E, t, e, bias) : -INFINITY;
+    }
+    int sel[16];
+    float val[16];
+    warp_topk<EPL>(v, elig, d.k, sel, val);
+    float denom = 0.f;
+    for (int j = 0; j < d.k; ++j) denom += expf(val[j] - val[0]);
+    if (lane < d.k) {
+      int e = 0;
+      float g = 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (j == lane) {
+          e = sel[j];
+          g = val[j];
+        }
+      ws.sel[f * d.k + lane] = e;
+      ws.selw[f * d.k + lane] = expf(g - val[0]) / denom;
+      if (e >= 0 && e < d.E) atomicOr(&mask[e], 1u << p);
+      else set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < d.E; e += blockDim.x) ws.chunk_mask[static_cast<size_t>(chunk) * d.E + e] = mask[e];
+}
+
+// ---------------------------------------------------------------- worklist
+// One CTA per chunk: offsets[e] = exclusive scan over experts of their edge
+// counts (popcounts of every chunk mask), this chunk's base inside expert e =
+// popcounts of earlier chunks; an edge (p, e) lands at
+// offsets[e] + base_e + popc(mask[e] & bits below p): expert-major, positions
+// ascending, with no atomics. CTA 0 also writes the grouped-GEMM tile tables.
+__global__ void __launch_bounds__(256) k_worklist(Dims d, Work ws) {
+  __shared__ int32_t base[1024];
+  __shared__ uint32_t mymask[1024];
+  __shared__ int32_t tot[1024];
+  __shared__ int32_t scan_tmp[256];
+  const int n_fresh = ws.ctrl->n_fresh;
+  const int n_chunks = (n_fresh + 31) / 32;
+  const int chunk = blockIdx.x;
+  if (chunk >= (n_chunks > 0 ? n_chunks : 1)) return;
+  const int E = d.E;
+  const int tid = threadIdx.x;
+  for (int e = tid; e < E; e += blockDim.x) {
+    int before = 0, total = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+      const int pc = __popc(ws.chunk_mask[static_cast<size_t>(c) * E + e]);
+      total += pc;
+      before += (c < chunk) ? pc : 0;
+    }
+    tot[e] = total;
+    base[e] = before;
+    mymask[e] = chunk < n_chunks ? ws.chunk_mask[static_cast<size_t>(chunk) * E + e] : 0u;
+  }
+  __syncthreads();
+  // exclusive scan of tot over experts: thread tid owns experts [tid*per, tid*per + per)
+  const int per = (E + 255) / 256;
+  int local = 0;
+  for (int q = 0; q < per; ++q) {
+    const int e = tid * per + q;
+    if (e < E) local += tot[e];
+  }
+  scan_tmp[tid] = local;
+  __syncthreads();
+  for (int off = 1; off < 256; off <<= 1) {
+    int add = tid >= off ? scan_tmp[tid - off] : 0;
+    __syncthreads();
+    scan_tmp[tid] += add;
+    __syncthreads();
+  }
+  int run = scan_tmp[tid] - local;
+  for (int q = 0; q < per; ++q) {
+    const int e = tid * per + q;
+    if (e < E) {
+      const int o = run;
+      run += tot[e];
+      if (chunk == 0) ws.offsets[e] = o;
+      base[e] += o;
+    }
+  }
+  if (chunk == 0 && tid == 255) ws.offsets[E] = run;
+  __syncthreads();
+  // scatter this chunk's edges
+  const int k = d.k;
+  for (int q = tid; q < 32 * k; q += blockDim.x) {
+    const int p = q / k, j = q % k;
+    const int f = chunk * 32 + p;
+    if (f >= n_fresh) continue;
+    const int e = ws.sel[f * k + j];
+    if (e < 0 || e >= E) {
+      set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+      continue;
+    }
+    const int dst = base[e] + __popc(mymask[e] & ((1u << p) - 1u));
+    if (dst < 0 || dst >= d.Nmax * k) {
+      set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+      continue;
+    }
+    ws.wl_pos[dst] = ws.fresh_pos[f];
+    ws.slot[f * k + j] = dst;
+  }
+  if (chunk != 0) return;
+  // tile tables (groups: routed experts, then shared experts over all positions)
+  __syncthreads();
+  const int G = E + d.n_sh;
+  if (tid == 0) {
+    int hit = 0, up = 0, dn = 0;
+    const int mt_up = d.I / 128, mt_sh = d.I_s / 128, mt_dn = d.H / 128;
+    for (int g = 0; g < G; ++g) {
+      const bool routed = g < E;
+      const int rows = routed ? tot[g] : d.n_pos;
+      const int row0 = routed ? ws.offsets[g] : (g - E) * d.Nmax;
+      ws.grp_rows[g] = rows;
+      ws.grp_row0[g] = row0;
+      ws.tile_off_up[g] = up;
+      ws.tile_off_dn[g] = dn;
+      if (routed) hit += rows > 0;
+      if (d.tn_up > 0) up += ((rows + d.tn_up - 1) / d.tn_up) * (routed ? mt_up : mt_sh);
+      if (d.tn_dn > 0) dn += ((rows + d.tn_dn - 1) / d.tn_dn) * mt_dn;
+    }
+    ws.tile_off_up[G] = up;
+    ws.tile_off_dn[G] = dn;
+    ws.ctrl->n_hit = hit;
+    ws.ctrl->tiles_up = up;
+    ws.ctrl->tiles_dn = dn;
+    ws.stats->n_hit_experts = hit;
+    ws.stats->tiles_up = up;
+    ws.stats->tiles_down = dn;
+  }
+}
+
+// ---------------------------------------------------------------- permute
+// Xp[l] = x[wl_pos[l]]: one warp per worklist row, 16-byte vectors.
+__global__ void k_permute(Dims d, Work ws, const uint4 *__restrict__ x, int vec_per_row) {
+  const int n = ws.ctrl->n_edges;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  uint4 *xp = reinterpret_cast<uint4 *>(ws.xp);
+  for (int l = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; l < n; l += warps) {
+    const int t = ws.wl_pos[l];
+    if (t < 0 || t >= d.n_pos) {
+      if (lane_id() == 0) set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+      continue;
+    }
+    const uint4 *src = x + static_cast<size_t>(t) * vec_per_row;
+    uint4 *dst = xp + static_cast<size_t>(l) * vec_per_row;
+    for (int v = lane_id(); v < vec_per_row; v += 32) dst[v] = src[v];
+  }
+}
+
+// ---------------------------------------------------------------- combine + cache
+// One CTA per position. Fresh t: r = sum_j w_j O[slot(t, j)] (j ascending,
+// fp32) and the cache row is refilled; reused t: r = cached row. Then
+// y = r + shared outputs (+ x when residual), rounded once.
+template <typename T>
+__global__ void __launch_bounds__(128) k_combine(Dims d, Work ws, const T *__restrict__ x, T *__restrict__ y) {
+  const int t = blockIdx.x;
+  if (t >= d.n_pos) return;
+  const int f = ws.fidx[t];
+  const int H = d.H, k = d.k;
+  T *cache = reinterpret_cast<T *>(ws.cache) + static_cast<size_t>(t) * H;
+  __shared__ int32_t slot_s[16];
+  __shared__ float w_s[16];
+  if (f >= 0 && threadIdx.x < k) {
+    int sl = ws.slot[f * k + threadIdx.x];
+    if (sl < 0 || sl >= d.Nmax * k) {
+      set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+      sl = 0;
+    }
+    slot_s[threadIdx.x] = sl;
+    w_s[threadIdx.x] = ws.selw[f * k + threadIdx.x];
+  }
+  __syncthreads();
+  for (int h0 = threadIdx.x * 4; h0 < H; h0 += blockDim.x * 4) {
+    float r[4];
+    if (f >= 0) {
+      r[0] = r[1] = r[2] = r[3] = 0.f;
+      for (int j = 0; j < k; ++j) {
+        const float4 o = *reinterpret_cast<const float4 *>(ws.o_int + static_cast<size_t>(slot_s[j]) * H + h0);
+        const float wj = w_s[j];
+        r[0] = fmaf(wj, o.x, r[0]);
+        r[1] = fmaf(wj, o.y, r[1]);
+        r[2] = fmaf(wj, o.z, r[2]);
+        r[3] = fmaf(wj, o.w, r[3]);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) cache[h0 + q] = from_f32<T>(r[q]);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) r[q] = to_f32(cache[h0 + q]);
+    }
+    for (int s = 0; s < d.n_sh; ++s) {
+      const float4 o =
+          *reinterpret_cast<const float4 *>(ws.o_sh + (static_cast<size_t>(s) * d.Nmax + t) * H + h0);
+      r[0] += o.x;
+      r[1] += o.y;
+      r[2] += o.z;
+      r[3] += o.w;
+    }
+    if (d.residual) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) r[q] += to_f32(x[static_cast<size_t>(t) * H + h0 + q]);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) y[static_cast<size_t>(t) * H + h0 + q] = from_f32<T>(r[q]);
+  }
+}
+
+// ---------------------------------------------------------------- bounded-wait test
+// Waits on an mbarrier that nothing ever completes; the bounded wait must give
+// up after timeout_ns, set the timeout bit and return.
+__global__ void k_wait_test(uint32_t *err, int64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    (void)mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, err, static_cast<uint64_t>(timeout_ns));
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------- launchers
+
+static int epl_for(int E) {
+  const int epl = (E + 31) / 32;
+  return epl <= 1 ? 1 : epl <= 2 ? 2 : epl <= 4 ? 4 : epl <= 8 ? 8 : epl <= 16 ? 16 : 32;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+cudaError_t launch_gate_simt(const Dims &d, const Weights &w, const Work &ws, const void *x, int bf16,
+                             cudaStream_t s) {
+  const int outputs = d.n_pos * d.E;
+  int blocks = (outputs + 7) / 8;
+  if (blocks > 8 * num_sms()) blocks = 8 * num_sms();
+  if (bf16)
+    k_gate_simt<__nv_bfloat16><<<blocks, 256, 0, s>>>(d, static_cast<const __nv_bfloat16 *>(x),
+                                                      static_cast<const __nv_bfloat16 *>(w.w_router), ws.gparts);
+  else
+    k_gate_simt<float><<<blocks, 256, 0, s>>>(d, static_cast<const float *>(x),
+                                              static_cast<const float *>(w.w_router), ws.gparts);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_plan_topk(const Dims &d, const Weights &w, const Work &ws, cudaStream_t s) {
+  int blocks = (d.n_pos + 7) / 8;
+  switch (epl_for(d.E)) {
+#define EPOCH_CASE(N) \
+  case N: k_plan_topk<N><<<blocks, 256, 0, s>>>(d, ws.gparts, w.b_router, ws.plan_counts); break;
+    EPOCH_CASE(1) EPOCH_CASE(2) EPOCH_CASE(4) EPOCH_CASE(8) EPOCH_CASE(16) EPOCH_CASE(32)
+#undef EPOCH_CASE
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_plan_support(const Dims &d, const Work &ws, int32_t threshold, int all_experts,
+                                cudaStream_t s) {
+  k_plan_support<<<1, 1024, 0, s>>>(d, ws, threshold, all_experts);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_classify(const Dims &d, const Work &ws, const uint8_t *live, const uint8_t *decoded,
+                            cudaStream_t s) {
+  k_classify<<<1, 1024, 0, s>>>(d, ws, live, decoded);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route(const Dims &d, const Weights &w, const Work &ws, cudaStream_t s) {
+  const int chunks = (d.Nmax + 31) / 32;
+  switch (epl_for(d.E)) {
+#define EPOCH_CASE(N) \
+  case N: k_route<N><<<chunks, 256, 0, s>>>(d, ws, w.b_router); break;
+    EPOCH_CASE(1) EPOCH_CASE(2) EPOCH_CASE(4) EPOCH_CASE(8) EPOCH_CASE(16) EPOCH_CASE(32)
+#undef EPOCH_CASE
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_worklist(const Dims &d, const Work &ws, cudaStream_t s) {
+  const int chunks = (d.Nmax + 31) / 32;
+  k_worklist<<<chunks, 256, 0, s>>>(d, ws);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const Dims &d, const Work &ws, const void *x, int bf16, cudaStream_t s) {
+  const int vec = d.H * (bf16 ? 2 : 4) / 16;
+  int blocks = (d.Nmax * d.k + 7) / 8;
+  if (blocks > 4 * num_sms()) blocks = 4 * num_sms();
+  k_permute<<<blocks, 256, 0, s>>>(d, ws, static_cast<const uint4 *>(x), vec);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const Dims &d, const Work &ws, const void *x, void *y, int bf16, cudaStream_t s) {
+  if (bf16)
+    k_combine<__nv_bfloat16><<<d.n_pos, 128, 0, s>>>(d, ws, static_cast<const __nv_bfloat16 *>(x),
+                                                     static_cast<__nv_bfloat16 *>(y));
+  else
+    k_combine<float><<<d.n_pos, 128, 0, s>>>(d, ws, static_cast<const float *>(x), static_cast<float *>(y));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_test(uint32_t *err, int64_t timeout_ns, cudaStream_t s) {
+  k_wait_test<<<1, 32, 0, s>>>(err, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace epoch

@@ -1,0 +1,226 @@
+"""Torch-facing wrapper of one Epoch MoE layer (marshalling only).
+
+PyTorch provides device memory and streams; every step of the layer runs in
+the sm_103a library through the C ABI in ``binding``.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from typing import Dict, Optional
+
+import numpy as np
+import torch
+
+from . import binding as B
+
+_TORCH_DT = {"bf16": torch.bfloat16, "f32": torch.float32}
+_ABI_DT = {"bf16": B.EPOCH_BF16, "f32": B.EPOCH_F32}
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+class EpochLayer:
+    """One routed-expert MoE layer with its block plan and routed-output cache.
+
+    weights: dict of CUDA tensors -- w_router [E,H], b_router [E] float32,
+    w_gate/w_up [E,I,H], w_down [E,H,I], and when n_shared > 0 ws_gate/ws_up
+    [n_sh,I_s,H], ws_down [n_sh,H,I_s]; all contiguous, in the layer dtype.
+    """
+
+    def __init__(self, *, hidden: int, n_experts: int, inter: int, top_k: int, max_positions: int,
+                 dtype: str, tau: float, refresh_R: Optional[int], weights: Dict[str, torch.Tensor],
+                 n_shared: int = 0, shared_inter: Optional[int] = None, residual: bool = False):
+        self.dtype = dtype
+        self.hidden, self.n_experts, self.inter, self.top_k = hidden, n_experts, inter, top_k
+        self.n_shared = n_shared
+        self.max_positions = max_positions
+        self.cfg = B.epoch_layer_config(
+            hidden=hidden, n_experts=n_experts, inter=inter, top_k=top_k, n_shared=n_shared,
+            shared_inter=(shared_inter or inter) if n_shared else 0, max_positions=max_positions,
+            dtype=_ABI_DT[dtype], tau=float(tau),
+            refresh_R=B.EPOCH_REFRESH_NEVER if refresh_R is None else int(refresh_R),
+            residual=1 if residual else 0)
+        tdt = _TORCH_DT[dtype]
+        for name, t in weights.items():
+            if not (t.is_cuda and t.is_contiguous()):
+                raise ValueError(f"weight {name} must be a contiguous CUDA tensor")
+            want = torch.float32 if name == "b_router" else tdt
+            if t.dtype != want:
+                raise ValueError(f"weight {name} has dtype {t.dtype}, expected {want}")
+        self._weights = weights  # keep alive: the library holds raw pointers
+        self.wstruct = B.epoch_layer_weights(
+            w_router=_ptr(weights["w_router"]), b_router=_ptr(weights["b_router"]),
+            w_gate=_ptr(weights["w_gate"]), w_up=_ptr(weights["w_up"]), w_down=_ptr(weights["w_down"]),
+            ws_gate=_ptr(weights.get("ws_gate")), ws_up=_ptr(weights.get("ws_up")),
+            ws_down=_ptr(weights.get("ws_down")))
+        self.workspace_bytes = B.epoch_workspace_bytes(self.cfg)
+        if self.workspace_bytes == 0:
+            raise ValueError("invalid layer configuration")
+        dev = weights["w_router"].device
+        self._ws = torch.empty(self.workspace_bytes + 256, dtype=torch.uint8, device=dev)
+        base = self._ws.data_ptr()
+        self._ws_ptr = (base + 255) // 256 * 256
+        self.handle = B.epoch_layer_create(self.cfg, self.wstruct, self._ws_ptr, self.workspace_bytes)
+        self.device = dev
+
+    # ------------------------------------------------------------------ entry points
+    def plan_block(self, x: torch.Tensor, stream=None) -> None:
+        self._check_x(x)
+        B.check(B.epoch_plan_block(self.handle, x.data_ptr(), x.shape[0], _stream(stream)),
+                "epoch_plan_block")
+
+    def moe_iter(self, x: torch.Tensor, live: torch.Tensor, decoded: torch.Tensor, iteration: int,
+                 y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        self._check_x(x)
+        n = x.shape[0]
+        for m in (live, decoded):
+            if not (m.is_cuda and m.dtype == torch.uint8 and m.is_contiguous() and m.numel() >= n):
+                raise ValueError("live/decoded must be contiguous uint8 CUDA tensors of n_pos flags")
+        if y is None:
+            y = torch.empty_like(x)
+        B.check(B.epoch_moe_iter(self.handle, x.data_ptr(), live.data_ptr(), decoded.data_ptr(), n,
+                                 int(iteration), y.data_ptr(), _stream(stream)), "epoch_moe_iter")
+        return y
+
+    def block_end(self) -> None:
+        B.check(B.epoch_block_end(self.handle), "epoch_block_end")
+
+    # ------------------------------------------------------------------ inspection
+    def stats(self, stream=None) -> dict:
+        st = B.epoch_iter_stats()
+        B.check(B.lib().epoch_read_stats(self.handle, C.byref(st), _stream(stream)), "epoch_read_stats")
+        return st.as_dict()
+
+    def status(self, stream=None):
+        word = C.c_uint32(0)
+        code = B.lib().epoch_get_status(self.handle, _stream(stream), C.byref(word))
+        return code, word.value
+
+    def clear_status(self, stream=None) -> None:
+        B.check(B.lib().epoch_clear_status(self.handle, _stream(stream)), "epoch_clear_status")
+
+    def path_counters(self):
+        c, h, f = C.c_int64(), C.c_int64(), C.c_int64()
+        B.check(B.lib().epoch_path_counters(self.handle, C.byref(c), C.byref(h), C.byref(f)),
+                "epoch_path_counters")
+        return {"cold": c.value, "hot": h.value, "fallback": f.value}
+
+    def set_wait_timeout(self, ns: int) -> None:
+        B.check(B.lib().epoch_set_wait_timeout(self.handle, int(ns)), "epoch_set_wait_timeout")
+
+    def test_wait_timeout(self, ns: int, stream=None) -> None:
+        B.check(B.lib().epoch_test_wait_timeout(self.handle, int(ns), _stream(stream)),
+                "epoch_test_wait_timeout")
+
+    def set_profiling(self, on: bool) -> None:
+        B.check(B.lib().epoch_set_profiling(self.handle, 1 if on else 0), "epoch_set_profiling")
+
+    def read_profile(self) -> dict:
+        p = B.epoch_profile()
+        B.check(B.lib().epoch_read_profile(self.handle, C.byref(p)), "epoch_read_profile")
+        out = {}
+        for i in range(B.EPOCH_PROF_KINDS):
+            name = p.name[i].decode() if p.name[i] else ""
+            if name and p.launches[i]:
+                out[name] = {"launches": int(p.launches[i]), "total_ms": float(p.total_ms[i])}
+        out["_kernels_launched"] = int(p.kernels_launched)
+        return out
+
+    def reset_profile(self) -> None:
+        B.check(B.lib().epoch_reset_profile(self.handle), "epoch_reset_profile")
+
+    def _copy(self, ptr: int, count: int, dtype, stream=None) -> np.ndarray:
+        out = np.empty(count, dtype=dtype)
+        if count:
+            B.check(B.lib().epoch_debug_copy(out.ctypes.data, ptr, out.nbytes, _stream(stream)),
+                    "epoch_debug_copy")
+        return out
+
+    def debug(self, n_pos: int, parts=("plan", "iter"), stream=None) -> dict:
+        """Host copies of internal arrays. parts: "plan" (support, hit counts),
+        "iter" (fresh list, selections, weights, worklist, stamps), "logits"
+        (split partial logits), "cache" (routed-output cache rows)."""
+        v = B.epoch_debug_view()
+        B.check(B.lib().epoch_debug_pointers(self.handle, C.byref(v)), "epoch_debug_pointers")
+        st = self.stats(stream)
+        E, k, N = self.n_experts, self.top_k, self.max_positions
+        nf, ne = st["n_fresh"], st["n_edges"]
+        d = dict(stats=st)
+        d["error_word"] = int(self._copy(v.error_word, 1, np.uint32, stream)[0])
+        if "plan" in parts:
+            d["support_len"] = int(self._copy(v.support_len, 1, np.int32, stream)[0])
+            d["support_ids"] = self._copy(v.support_ids, E, np.int32, stream)
+            d["plan_counts"] = self._copy(v.plan_counts, E, np.int32, stream)
+        if "iter" in parts:
+            d["fresh_pos"] = self._copy(v.fresh_pos, nf, np.int32, stream)
+            d["sel"] = self._copy(v.sel, nf * k, np.int32, stream).reshape(nf, k)
+            d["sel_w"] = self._copy(v.sel_w, nf * k, np.float32, stream).reshape(nf, k)
+            d["offsets"] = self._copy(v.offsets, E + 1, np.int32, stream)
+            d["wl_pos"] = self._copy(v.wl_pos, ne, np.int32, stream)
+            d["slot"] = self._copy(v.slot, nf * k, np.int32, stream).reshape(nf, k)
+            d["stamp"] = self._copy(v.stamp, n_pos, np.int32, stream)
+        if "logits" in parts:
+            raw = self._copy(v.logit_parts, v.n_logit_parts * N * E, np.float32, stream)
+            d["logit_parts"] = raw.reshape(v.n_logit_parts, N, E)[:, :n_pos]
+        if "cache" in parts:
+            cdt = np.uint16 if self.dtype == "bf16" else np.float32
+            d["cache"] = self._copy(v.cache, n_pos * self.hidden, cdt, stream).reshape(n_pos, self.hidden)
+        return d
+
+    def _check_x(self, x: torch.Tensor) -> None:
+        if not (x.is_cuda and x.is_contiguous() and x.dtype == _TORCH_DT[self.dtype] and x.dim() == 2
+                and x.shape[1] == self.hidden):
+            raise ValueError(f"x must be a contiguous CUDA {self.dtype} tensor [n_pos, {self.hidden}]")
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            B.epoch_layer_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def payload_to_torch(payload: np.ndarray, dtype: str, device) -> torch.Tensor:
+    """Uploads a synth payload (bf16 bit patterns as uint16, or float32) as a CUDA tensor."""
+    if dtype == "bf16":
+        t = torch.from_numpy(np.ascontiguousarray(payload).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(payload, dtype=np.float32))
+    return t.to(device)
+
+
+def layer_for_workload(wl, layer_index: int = 0, device="cuda", threads: Optional[int] = None,
+                       max_positions: Optional[int] = None) -> EpochLayer:
+    """Builds the device layer of a synth workload (weights generated by synth, uploaded)."""
+    import synth
+    wr, b = synth.router_payload(wl, layer_index)
+    wg, wu, wd = synth.experts_payload(wl, layer_index, threads)
+    weights = {
+        "w_router": payload_to_torch(wr, wl.dtype, device),
+        "b_router": torch.from_numpy(b).to(device),
+        "w_gate": payload_to_torch(wg, wl.dtype, device),
+        "w_up": payload_to_torch(wu, wl.dtype, device),
+        "w_down": payload_to_torch(wd, wl.dtype, device),
+    }
+    del wg, wu, wd
+    if wl.n_shared:
+        sg, su, sd = synth.shared_experts_payload(wl, layer_index, threads)
+        weights.update(ws_gate=payload_to_torch(sg, wl.dtype, device),
+                       ws_up=payload_to_torch(su, wl.dtype, device),
+                       ws_down=payload_to_torch(sd, wl.dtype, device))
+    return EpochLayer(hidden=wl.hidden, n_experts=wl.n_experts, inter=wl.inter, top_k=wl.top_k,
+                      max_positions=max_positions or wl.n_pos, dtype=wl.dtype, tau=wl.tau, refresh_R=wl.refresh_R,
+                      weights=weights, n_shared=wl.n_shared, shared_inter=wl.shared_inter,
+                      residual=wl.residual)

@@ -1,0 +1,208 @@
+"""GPU parity: the sm_103a library against the float64 oracle, through the C ABI.
+
+Every workload shape of the synthetic suite, full blocks where the oracle
+finishes in seconds, plus edge cases: ragged position counts, an empty
+worklist, every fallback path, malformed flags, determinism and the bounded
+device wait.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity_harness import block_parity, layer_for_workload, oracle_layer, payload_to_torch, scenario_parity
+
+pytestmark = pytest.mark.gpu
+
+TINY_BF16 = synth.WORKLOADS["tiny_fp32"].replace(
+    name="tiny_bf16", wid=6, iid=6, dtype="bf16", n_shared=1, batch=3, iters=10, refresh_R=3,
+    description="tiny bf16 layer with a shared expert: H256 E16 I128 top2, 3x32 positions")
+
+
+@pytest.fixture(scope="session", autouse=True)
+def built_library():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_moe_layer_gate_gb300 import builder
+    if builder.is_stale():
+        builder.build()
+
+
+def assert_clean(rep):
+    assert not rep.mismatches, "\n".join(rep.mismatches[:20])
+    if rep.near_ties:
+        print(f"{len(rep.near_ties)} near-tie(s) logged: " + "; ".join(rep.near_ties[:5]))
+    print(f"iterations {rep.iterations}, edges {rep.edges}, max rel err {rep.max_rel_err:.3g}")
+
+
+def test_tiny_fp32_block():
+    assert_clean(block_parity(synth.WORKLOADS["tiny_fp32"]))
+
+
+def test_tiny_bf16_block_tcgen05():
+    assert_clean(block_parity(TINY_BF16))
+
+
+def test_llada_moe_7b_block():
+    assert_clean(block_parity(synth.WORKLOADS["llada_moe_7b"]))
+
+
+def test_llada2_mini_block():
+    rep = block_parity(synth.WORKLOADS["llada2_mini"])
+    assert_clean(rep)
+    assert rep.iterations == 32
+
+
+def test_llada2_flash_stack_of_four():
+    # ten iterations: cold, new commits every iteration and the first R=8 refreshes
+    rep = block_parity(synth.WORKLOADS["llada2_flash_x4"], n_iters=10)
+    assert_clean(rep)
+    assert rep.iterations == 40
+
+
+@pytest.mark.parametrize("batch,tau,R", [(1, 0.9, 4), (1, 1.0, 1), (4, 0.95, None), (4, 0.99, 4),
+                                         (16, 1.0, 4), (1, 0.9, None)])
+def test_sweep_points(batch, tau, R):
+    assert_clean(block_parity(synth.sweep_workload(batch, tau, R), n_iters=12))
+
+
+def test_sweep_largest_batch_first_iterations():
+    assert_clean(block_parity(synth.sweep_workload(64, 0.95, 4), n_iters=3))
+
+
+def test_tau1_R1_is_dense_moe():
+    """tau = 1 and R = 1: every position fresh with every expert eligible, so the
+    layer equals the dense MoE formula at every iteration."""
+    wl = synth.sweep_workload(1, 1.0, 1)
+    lay = layer_for_workload(wl)
+    xs = synth.hidden_states(wl, 6)
+    live, dec = synth.block_masks(wl, 6)
+    wr, b = synth.router_payload(wl)
+    orc = oracle_layer(wl)
+    shared = orc.shared
+    lay.plan_block(payload_to_torch(xs[0], wl.dtype, lay.device))
+    for i in range(6):
+        x = payload_to_torch(xs[i], wl.dtype, lay.device)
+        y = lay.moe_iter(x, torch.from_numpy(live[i]).cuda(), torch.from_numpy(dec[i]).cuda(), i)
+        st = lay.stats()
+        assert st["n_fresh"] == wl.n_pos and st["support_len"] == wl.n_experts
+        x64 = synth.to_f64(xs[i], wl.dtype)
+        dense = oracle.dense_moe(x64, synth.to_f64(wr, wl.dtype), b.astype(np.float64), orc.expert,
+                                 wl.n_experts, wl.top_k, shared)
+        yg = y.float().cpu().numpy().astype(np.float64)
+        assert np.max(np.abs(yg - dense)) <= 1e-2 * np.max(np.abs(dense))
+    lay.close()
+
+
+def _steps_from(wl, n_iters, n_pos=None, block=0):
+    xs = synth.hidden_states(wl, n_iters, block)
+    live, dec = synth.block_masks(wl, n_iters, block)
+    n = n_pos or wl.n_pos
+    return xs[:, :n], live[:, :n], dec[:, :n]
+
+
+def test_ragged_position_count():
+    """45 positions: a partial chunk of 32, partial MMA token tiles and a partial block."""
+    wl = TINY_BF16
+    xs, live, dec = _steps_from(wl, 6, n_pos=45)
+    steps = [dict(op="plan", x=xs[0])] + [dict(op="iter", x=xs[i], live=live[i], dec=dec[i], i=i)
+                                          for i in range(6)]
+    assert_clean(scenario_parity(wl, steps, max_positions=64))
+
+
+def test_single_position():
+    wl = TINY_BF16
+    xs, live, dec = _steps_from(wl, 3, n_pos=1)
+    steps = [dict(op="plan", x=xs[0])] + [dict(op="iter", x=xs[i], live=live[i], dec=dec[i], i=i)
+                                          for i in range(3)]
+    assert_clean(scenario_parity(wl, steps, max_positions=96))
+
+
+def test_empty_worklist_reuses_cache():
+    """Never refresh, everything decoded and stable: L = 0, y = cached rows + shared."""
+    wl = TINY_BF16.replace(refresh_R=None)
+    xs, _, _ = _steps_from(wl, 5)
+    N = wl.n_pos
+    live0, dec0 = np.ones(N, np.uint8), np.zeros(N, np.uint8)
+    live1, dec1 = np.zeros(N, np.uint8), np.ones(N, np.uint8)
+    steps = [dict(op="plan", x=xs[0]), dict(op="iter", x=xs[0], live=live0, dec=dec0, i=0),
+             dict(op="iter", x=xs[1], live=live1, dec=dec1, i=1)]
+    steps += [dict(op="iter", x=xs[i], live=live1, dec=dec1, i=i) for i in range(2, 5)]
+    lay = layer_for_workload(wl)
+    rep = scenario_parity(wl, steps, layer=lay)
+    assert_clean(rep)
+    st = lay.stats()
+    assert st["n_edges"] == 0 and st["n_fresh"] == 0 and st["n_reuse"] == N
+    lay.close()
+
+
+def test_fallback_paths():
+    """No plan, a skipped iteration, a different position count, a decoded->live
+    transition and malformed flags: each iteration is full fresh with every
+    expert eligible (or, for the flags, treated live) and matches the oracle."""
+    wl = TINY_BF16.replace(tau=0.5)
+    xs, live, dec = _steps_from(wl, 8)
+    N = wl.n_pos
+    steps = [dict(op="iter", x=xs[0], live=live[0], dec=dec[0], i=0),        # no plan yet
+             dict(op="plan", x=xs[0]),
+             dict(op="iter", x=xs[0], live=live[0], dec=dec[0], i=0),
+             dict(op="iter", x=xs[1], live=live[1], dec=dec[1], i=1),
+             dict(op="iter", x=xs[3], live=live[3], dec=dec[3], i=3),        # skipped 2
+             dict(op="iter", x=xs[4], live=live[4], dec=dec[4], i=4)]
+    anomalous_live = live[5].copy()
+    anomalous_dec = dec[5].copy()
+    d_idx = np.nonzero(dec[4])[0]
+    anomalous_live[d_idx[0]] = 1
+    anomalous_dec[d_idx[0]] = 0                                              # decoded -> live
+    steps += [dict(op="iter", x=xs[5], live=anomalous_live, dec=anomalous_dec, i=5)]
+    both = live[6].copy()
+    both[d_idx[1]] = 1                                                       # both flags set
+    steps += [dict(op="iter", x=xs[6], live=both, dec=dec[6], i=6)]
+    steps += [dict(op="iter", x=xs[7][:N - 5], live=live[7][:N - 5], dec=dec[7][:N - 5], i=7)]  # n_pos differs
+    steps += [dict(op="end"), dict(op="iter", x=xs[7], live=live[7], dec=dec[7], i=8)]         # after block end
+    lay = layer_for_workload(wl)
+    rep = scenario_parity(wl, steps, layer=lay)
+    assert_clean(rep)
+    counters = lay.path_counters()
+    assert counters["cold"] == 1
+    assert counters["fallback"] == 4  # no plan, skip, n_pos mismatch, after block end
+    code, word = lay.status()
+    assert word & 1  # malformed flags were reported
+    lay.clear_status()
+    assert lay.status() == (0, 0)
+    lay.close()
+
+
+def test_determinism_bitwise():
+    wl = synth.WORKLOADS["llada2_mini"]
+    xs = synth.hidden_states(wl, 3)
+    live, dec = synth.block_masks(wl, 3)
+    outs = []
+    for _ in range(2):
+        lay = layer_for_workload(wl)
+        x0 = payload_to_torch(xs[0], wl.dtype, lay.device)
+        lay.plan_block(x0)
+        ys, wls = [], []
+        for i in range(3):
+            x = payload_to_torch(xs[i], wl.dtype, lay.device)
+            y = lay.moe_iter(x, torch.from_numpy(live[i]).cuda(), torch.from_numpy(dec[i]).cuda(), i)
+            ys.append(y.view(torch.int16).cpu().numpy())
+            wls.append(lay.debug(wl.n_pos)["wl_pos"])
+        outs.append((ys, wls))
+        lay.close()
+    for a, b in zip(outs[0][0], outs[1][0]):
+        assert np.array_equal(a, b)
+    for a, b in zip(outs[0][1], outs[1][1]):
+        assert np.array_equal(a, b)
+
+
+def test_bounded_wait_times_out_and_reports():
+    lay = layer_for_workload(TINY_BF16)
+    lay.test_wait_timeout(2_000_000)  # 2 ms on a barrier nothing completes
+    code, word = lay.status()
+    assert code == 4 and word & 2
+    lay.clear_status()
+    # the context is still usable
+    assert_clean(block_parity(TINY_BF16, n_iters=2))
+    lay.close()
