@@ -1,0 +1,448 @@
+#!/usr/bin/env python3
+"""Benchmark of the Epoch MoE-layer iteration on GB300.
+
+A step is one diffusion block of the LLaDA2.0-mini-shaped layer (H 2048, 256
+routed SwiGLU experts of inter 512, top-8, one shared expert, 32 requests x 32
+positions = 1024 positions): the block plan plus 32 refinement iterations, on
+seeded synthetic inputs already resident in HBM. Before every iteration a
+256 MiB buffer is written to flush L2 (outside the timed region); each
+iteration is timed with CUDA events on the launching stream.
+
+value: fresh token-expert edges per second over the whole job (all ranks),
+edges = sum over iterations of k |F_i|. Also reported: MoE-layer us per
+iteration, the path's roofline fraction (sum of per-iteration rooflines
+max(FLOPs / tensor peak, bytes / HBM peak) over the measured time), the
+dominant kernel's roofline, the oracle timed on the host cores (cpu_baseline),
+and the same metric end to end through host buffers (e2e).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+N > 1 runs under torchrun: one independent replica per GPU (no collective on
+the data path), timings reduced with a max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer µs/refinement iter; fresh token-expert edges/s; % of HBM/TC roofline"
+WORKLOAD = "llada2_mini"
+L2_FLUSH_BYTES = 256 << 20
+
+# DRAM traffic of one expert_up launch from an ncu capture, tied to the kernel
+# source it was measured on (null once that source changes).
+TRAFFIC = {"expert_up": None}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="epoch", choices=["epoch", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def workload_config(wl, n_gpus):
+    return {"workload": f"{wl.name}: {wl.description}", "positions": wl.n_pos, "hidden": wl.hidden,
+            "routed_experts": wl.n_experts, "inter": wl.inter, "top_k": wl.top_k, "shared_experts": wl.n_shared,
+            "iters_per_block": wl.iters, "tau": wl.tau, "refresh_R": wl.refresh_R,
+            "global_batch": wl.batch * n_gpus, "seq_len": 32, "parallelism": f"dp{n_gpus} (independent replicas)",
+            "l2": "flushed (256 MiB write) before every iteration, outside the timed region"}
+
+
+# ---------------------------------------------------------------- data parallelism (replicas only)
+
+def replica_workload(rank: int):
+    """Rank r serves its own requests: same layer weights, inputs seeded per rank."""
+    import synth
+    wl = synth.WORKLOADS[WORKLOAD]
+    return wl.replace(iid=wl.iid + 100 * rank)
+
+
+def reduce_max_over_ranks(values, device=None):
+    """Element-wise max of per-rank values (timings) over the default process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+# ---------------------------------------------------------------- algorithmic work (per iteration)
+
+def iteration_work(wl, st):
+    """(FLOPs, bytes) one iteration must do: gate for every position, SwiGLU over
+    the worklist and the shared expert, the weights of hit experts read once,
+    activations in and out, cache rows written (fresh) or read (reused)."""
+    H, E, I, Is, N, nsh = wl.hidden, wl.n_experts, wl.inter, wl.shared_inter, wl.n_pos, wl.n_shared
+    s = 2 if wl.dtype == "bf16" else 4
+    L = st["n_edges"]
+    flops = 2 * N * H * E + 6 * H * I * L + 6 * H * Is * N * nsh
+    nbytes = (st["n_hit_experts"] * 3 * H * I * s + nsh * 3 * H * Is * s + E * H * s + 4 * E
+              + 2 * N * H * s + st["n_fresh"] * H * s + st["n_reuse"] * H * s + 2 * N)
+    return flops, nbytes
+
+
+def up_kernel_bytes(wl, st):
+    """Algorithmic bytes of one expert_up launch: W_gate and W_up of every hit
+    routed expert and of the shared experts, read once."""
+    return 2 * wl.hidden * 2 * (st["n_hit_experts"] * wl.inter + wl.n_shared * wl.shared_inter)
+
+
+def source_sha():
+    h = hashlib.sha256()
+    with open(os.path.join(ROOT, "sparse_moe_layer_gate_gb300", "csrc", "gemm_tc.cu"), "rb") as fh:
+        h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
+        mx = max((float(r[2]) for r in rows if r[2].replace(".", "").isdigit()), default=None)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[j] for r in rows for j in range(4) if r[5 + j].lower() == "active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def cpu_oracle_sample(wl, n_iters, budget_s=25.0, payload=None):
+    """Times the float64 oracle (as it stands) on plan + the first iterations of
+    the block, stopping once budget_s is spent. Returns (edges/s, cores, sample)."""
+    import numpy as np
+    import oracle
+    import synth
+    wr, b = synth.router_payload(wl)
+    if payload is None:
+        payload = synth.experts_payload(wl)
+    wg, wu, wd = payload
+    sg, su, sd = synth.shared_experts_payload(wl)
+    conv = {}
+
+    def expert(e):
+        if e not in conv:
+            conv[e] = (synth.to_f64(wg[e], wl.dtype), synth.to_f64(wu[e], wl.dtype), synth.to_f64(wd[e], wl.dtype))
+        return conv[e]
+
+    shared = [(synth.to_f64(sg[s], wl.dtype), synth.to_f64(su[s], wl.dtype), synth.to_f64(sd[s], wl.dtype))
+              for s in range(wl.n_shared)]
+    xs = synth.hidden_states(wl, n_iters)
+    live, dec = synth.block_masks(wl, n_iters)
+    orc = oracle.LayerOracle(n_experts=wl.n_experts, top_k=wl.top_k, tau=wl.tau, refresh_R=wl.refresh_R,
+                             w_router=synth.to_f64(wr, wl.dtype), b_router=b.astype(np.float64), expert=expert,
+                             shared=shared, residual=wl.residual, max_positions=wl.n_pos)
+    x64 = [synth.to_f64(xs[i], wl.dtype) for i in range(n_iters)]
+    t0 = time.perf_counter()
+    plan = orc.plan_block(x64[0])
+    t_plan = time.perf_counter() - t0
+    for e in plan.support:  # weight conversion to float64 is input handling, not timed
+        expert(int(e))
+    edges, t_iter, done = 0, 0.0, 0
+    for i in range(n_iters):
+        t0 = time.perf_counter()
+        res = orc.iterate(x64[i], live[i], dec[i], i)
+        t_iter += time.perf_counter() - t0
+        edges += res.n_edges
+        done += 1
+        if t_plan + t_iter > budget_s:
+            break
+    threads = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS") or str(os.cpu_count())
+    sample = (f"block plan + iterations 0..{done - 1} of one {wl.name} block (float64 numpy oracle; "
+              f"plan {t_plan:.2f} s amortised over the sampled iterations)")
+    return edges / (t_plan * done / wl.iters + t_iter), int(threads), sample, done
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_epoch(args, rank, world):
+    import numpy as np
+    import torch
+    import synth
+    from sparse_moe_layer_gate_gb300 import builder
+    from sparse_moe_layer_gate_gb300.layer import layer_for_workload, payload_to_torch
+
+    if builder.is_stale():
+        if rank == 0:
+            builder.build()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+    torch.cuda.set_device(rank % torch.cuda.device_count())
+    dev = torch.device("cuda", torch.cuda.current_device())
+    wl = replica_workload(rank)
+    payload = synth.experts_payload(wl)
+    lay = layer_for_workload(wl, device=dev)
+    xs_host = synth.hidden_states(wl)
+    live_h, dec_h = synth.block_masks(wl)
+    xs = [payload_to_torch(xs_host[i], wl.dtype, dev) for i in range(wl.iters)]
+    lv = [torch.from_numpy(live_h[i]).to(dev) for i in range(wl.iters)]
+    dc = [torch.from_numpy(dec_h[i]).to(dev) for i in range(wl.iters)]
+    ys = [torch.empty_like(xs[0]) for _ in range(wl.iters)]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    # per-iteration work accounting (inputs are identical every block)
+    lay.plan_block(xs[0])
+    stats = []
+    for i in range(wl.iters):
+        lay.moe_iter(xs[i], lv[i], dc[i], i, ys[i])
+        stats.append(lay.stats())
+    lay.block_end()
+    work = [iteration_work(wl, st) for st in stats]
+    edges_per_block = sum(st["n_edges"] for st in stats)
+
+    def one_block(ev_plan, ev_iters, preroll=True):
+        if preroll:
+            torch.cuda._sleep(10_000_000)  # lets the host queue the whole block ahead of the GPU
+        ev_plan[0].record(stream)
+        lay.plan_block(xs[0])
+        ev_plan[1].record(stream)
+        for i in range(wl.iters):
+            flush.fill_(i & 0xFF)
+            ev_iters[i][0].record(stream)
+            lay.moe_iter(xs[i], lv[i], dc[i], i, ys[i])
+            ev_iters[i][1].record(stream)
+        lay.block_end()
+
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    for _ in range(args.warmup):
+        one_block((mk(), mk()), [(mk(), mk()) for _ in range(wl.iters)])
+    torch.cuda.synchronize()
+
+    import torch.distributed as dist
+    dist_on = world > 1 and dist.is_initialized()
+    if dist_on:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    launched0 = lay.read_profile()["_kernels_launched"]
+    lay.reset_profile()
+    lay.set_profiling(True)
+    t_wall0 = time.perf_counter()
+    records = []
+    for _ in range(args.steps):
+        evp = (mk(), mk())
+        evi = [(mk(), mk()) for _ in range(wl.iters)]
+        one_block(evp, evi)
+        records.append((evp, evi))
+    torch.cuda.synchronize()
+    if dist_on:
+        dist.barrier()
+    wall = time.perf_counter() - t_wall0
+    lay.set_profiling(False)
+    prof = lay.read_profile()
+    clk = clocks.stop()
+    gpu_launches = prof["_kernels_launched"] - launched0
+
+    plan_ms = [r[0][0].elapsed_time(r[0][1]) for r in records]
+    iter_ms = np.array([[r[1][i][0].elapsed_time(r[1][i][1]) for i in range(wl.iters)] for r in records])
+    step_ms = np.array(plan_ms) + iter_ms.sum(axis=1)
+    dev_time_s = float(step_ms.sum()) / 1e3
+    dev_time_s, wall = reduce_max_over_ranks([dev_time_s, wall], device=dev)
+    total_edges = edges_per_block * args.steps * world
+    value = total_edges / dev_time_s
+
+    hbm, tc, tc_sus, src = peaks()
+    iter_mean_ms = iter_ms.mean(axis=0)  # per iteration index
+    t_roof = [max(f / (tc * 1e12), b / (hbm * 1e9)) for f, b in work]
+    path_frac = sum(t_roof) / (float(iter_mean_ms.sum()) / 1e3)
+    bound_iters = sum(1 for f, b in work if b / (hbm * 1e9) >= f / (tc * 1e12))
+
+    up = prof.get("expert_up", {"launches": 0, "total_ms": 0.0})
+    up_bytes = sum(up_kernel_bytes(wl, st) for st in stats) / wl.iters
+    up_ms = up["total_ms"] / max(up["launches"], 1)
+    up_gbs = up_bytes / (up_ms / 1e3) / 1e9 if up_ms > 0 else None
+    tr = TRAFFIC.get("expert_up")
+    traffic = tr["bytes_per_launch"] if tr and tr.get("source_sha") == source_sha() else None
+    kernels = {k: {"launches": v["launches"], "avg_us": 1e3 * v["total_ms"] / max(v["launches"], 1),
+                   "share": v["total_ms"] / max(sum(x["total_ms"] for kk, x in prof.items()
+                                                    if not kk.startswith("_")), 1e-9)}
+               for k, v in prof.items() if not k.startswith("_")}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(lay, wl, xs_host, live_h, dec_h, edges_per_block, max(1, min(args.steps, 3)), flush, dev,
+                      world, dist_on)
+
+    out = {
+        "metric": METRIC, "value": value, "unit": "edges/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": float(step_ms.mean()), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(wl, world),
+        "us_per_iter": 1e3 * float(iter_ms.mean()),
+        "us_per_iter_by_index": [round(1e3 * v, 2) for v in iter_mean_ms.tolist()],
+        "plan_us_per_block": 1e3 * float(np.mean(plan_ms)),
+        "edges_per_block": edges_per_block,
+        "wall_s_timed_region": wall,
+        "path_roofline": {"frac": path_frac, "hbm_bound_iters": bound_iters, "iters": wl.iters,
+                          "roofline_us_per_iter": 1e6 * sum(t_roof) / wl.iters,
+                          "peak_hbm_gbs": hbm, "peak_bf16_tflops": tc, "peaks": f"of {src}"},
+        "roofline": {"kernel": "expert_up", "bound": "hbm", "achieved": up_gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": (up_gbs / hbm) if up_gbs else None, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": up_bytes, "avg_launch_us": 1e3 * up_ms,
+                     "peak_source": f"of {src} (STREAM copy, burst)"},
+        "kernels": kernels,
+        "gpu_launches": gpu_launches,
+        "clocks": clk,
+    }
+    if e2e:
+        out["e2e"] = e2e
+    return out, wl, payload
+
+
+def run_e2e(lay, wl, xs_host, live_h, dec_h, edges_per_block, steps, flush, dev, world, dist_on):
+    """Same metric through the public call with host buffers: every iteration
+    copies x and the masks from pinned host memory and reads y back, inside the
+    timed region."""
+    import torch
+    xs_pin = [torch.from_numpy(xs_host[i].view("int16")).view(torch.bfloat16).pin_memory()
+              for i in range(wl.iters)]
+    lv_pin = [torch.from_numpy(live_h[i]).pin_memory() for i in range(wl.iters)]
+    dc_pin = [torch.from_numpy(dec_h[i]).pin_memory() for i in range(wl.iters)]
+    y_pin = torch.empty((wl.n_pos, wl.hidden), dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty((wl.n_pos, wl.hidden), dtype=torch.bfloat16, device=dev)
+    ld = torch.empty(wl.n_pos, dtype=torch.uint8, device=dev)
+    dd = torch.empty(wl.n_pos, dtype=torch.uint8, device=dev)
+    yd = torch.empty_like(xd)
+    stream = torch.cuda.current_stream()
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    total_ms = 0.0
+    for step in range(steps + 1):
+        evs = []
+        for i in range(wl.iters):
+            flush.fill_(i & 0xFF)
+            a, b = mk(), mk()
+            a.record(stream)
+            xd.copy_(xs_pin[i], non_blocking=True)
+            ld.copy_(lv_pin[i], non_blocking=True)
+            dd.copy_(dc_pin[i], non_blocking=True)
+            if i == 0:
+                lay.plan_block(xd)
+            lay.moe_iter(xd, ld, dd, i, yd)
+            y_pin.copy_(yd, non_blocking=True)
+            b.record(stream)
+            evs.append((a, b))
+        lay.block_end()
+        torch.cuda.synchronize()
+        if step > 0:  # the first block is a warm-up
+            total_ms += sum(a.elapsed_time(b) for a, b in evs)
+    t = reduce_max_over_ranks([total_ms / 1e3], device=dev)[0]
+    bi = wl.iters * (wl.n_pos * wl.hidden * 2 + 2 * wl.n_pos)
+    bo = wl.iters * wl.n_pos * wl.hidden * 2
+    return {"value": edges_per_block * steps * world / t, "unit": "edges/s", "h2d_bytes_per_step": bi,
+            "d2h_bytes_per_step": bo, "us_per_iter": 1e6 * t / (steps * wl.iters),
+            "note": "x and masks copied from pinned host memory and y read back every iteration, inside the "
+                    "event-timed region; no pre-roll, so host launch time is included"}
+
+
+# ---------------------------------------------------------------- reference arm (the oracle)
+
+def run_reference(args):
+    import synth
+    wl = synth.WORKLOADS[WORKLOAD]
+    payload = synth.experts_payload(wl)
+    steps = []
+    sample = ""
+    cores = 0
+    for _ in range(args.warmup + args.steps):
+        v, cores, sample, done = cpu_oracle_sample(wl, 3, budget_s=20.0, payload=payload)
+        steps.append(v)
+    vals = steps[args.warmup:] or steps
+    value = sum(vals) / len(vals)
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "edges/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": workload_config(wl, 1),
+            "cpu_baseline": {"value": value, "unit": "edges/s", "cores": cores, "kind": "oracle",
+                             "sample": "each step: " + sample},
+            "e2e": {"value": value, "unit": "edges/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)))
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", rank)))
+        dist.init_process_group("nccl")
+    out, wl, payload = run_epoch(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            v, cores, sample, _ = cpu_oracle_sample(wl, wl.iters, budget_s=20.0, payload=payload)
+            out["cpu_baseline"] = {"value": v, "unit": "edges/s", "cores": cores, "kind": "oracle",
+                                   "sample": sample}
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

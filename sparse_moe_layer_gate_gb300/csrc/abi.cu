@@ -56,7 +56,7 @@ bool valid_config(const epoch_layer_config *c) {
   if (c == nullptr) return false;
   if (c->hidden <= 0 || c->inter <= 0 || c->n_experts < 1 || c->n_experts > 1024) return false;
   if (c->top_k < 1 || c->top_k > 16 || c->top_k > c->n_experts) return false;
-  if (c->n_shared < 0 || c->n_shared > 8) return false;
+  if (c->n_shared < 0 || c->n_shared > 8 || c->n_experts + c->n_shared > 1024) return false;
   if (c->n_shared > 0 && c->shared_inter <= 0) return false;
   if (c->max_positions < 1 || c->max_positions > 16384) return false;
   if (c->dtype != EPOCH_F32 && c->dtype != EPOCH_BF16) return false;
@@ -74,6 +74,17 @@ int sk_max_for(const epoch_layer_config &c) {
   return kb < 16 ? kb : 16;
 }
 
+// Capacity of the grouped-GEMM tile lists: every group splits into token tiles
+// of tn rows (at most rows/tn + 1 each) times its M tiles of 128.
+void tile_caps(const epoch_layer_config &c, int tn, int *up, int *dn) {
+  const long N = c.max_positions, k = c.top_k, E = c.n_experts, nsh = c.n_shared;
+  const long Is = c.n_shared ? c.shared_inter : 0;
+  const long routed_t = (N * k + tn - 1) / tn + E;
+  const long shared_t = nsh * ((N + tn - 1) / tn);
+  *up = static_cast<int>(routed_t * (c.inter / 128) + shared_t * (Is / 128));
+  *dn = static_cast<int>((routed_t + shared_t) * (c.hidden / 128));
+}
+
 // Lays the workspace out (base == nullptr: only measures). Returns total bytes.
 size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   size_t off = 0;
@@ -86,7 +97,6 @@ size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   const size_t N = c.max_positions, E = c.n_experts, H = c.hidden, I = c.inter, k = c.top_k;
   const size_t nsh = c.n_shared, Is = c.n_shared ? c.shared_inter : 0;
   const size_t act = c.dtype == EPOCH_BF16 ? 2 : 4;
-  const size_t G = E + nsh;
   const size_t chunks = (N + 31) / 32;
   Work t;
   t.stamp = static_cast<int32_t *>(take(N * 4));
@@ -101,11 +111,12 @@ size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   t.sel = static_cast<int32_t *>(take(N * k * 4));
   t.selw = static_cast<float *>(take(N * k * 4));
   t.chunk_mask = static_cast<uint32_t *>(take(chunks * E * 4));
+  t.expert_cnt = static_cast<int32_t *>(take(E * 4));
   t.offsets = static_cast<int32_t *>(take((E + 1) * 4));
-  t.grp_rows = static_cast<int32_t *>(take(G * 4));
-  t.grp_row0 = static_cast<int32_t *>(take(G * 4));
-  t.tile_off_up = static_cast<int32_t *>(take((G + 1) * 4));
-  t.tile_off_dn = static_cast<int32_t *>(take((G + 1) * 4));
+  int cap_up = 0, cap_dn = 0;
+  if (c.dtype == EPOCH_BF16) tile_caps(c, kTnUp, &cap_up, &cap_dn);
+  t.tiles_up = static_cast<int4 *>(take(static_cast<size_t>(cap_up) * 16 + 16));
+  t.tiles_dn = static_cast<int4 *>(take(static_cast<size_t>(cap_dn) * 16 + 16));
   t.wl_pos = static_cast<int32_t *>(take(N * k * 4));
   t.slot = static_cast<int32_t *>(take(N * k * 4));
   t.xp = take(N * k * H * act);
@@ -166,14 +177,18 @@ Dims call_dims(const epoch_layer *L, int32_t n_pos, int32_t iter, int host_fallb
 }
 
 // G for every position: tcgen05 split-K for bf16 layers, FFMA for fp32 layers.
-epoch_status run_gate(epoch_layer *L, Dims &d, const void *x, CUtensorMap *x_map, cudaStream_t s) {
+// x_maps[0] (box kTnGate rows) feeds the gate, x_maps[1] (box kTnUp rows) the
+// shared experts' up-projection.
+epoch_status run_gate(epoch_layer *L, Dims &d, const void *x, CUtensorMap *x_maps, cudaStream_t s) {
   if (L->bf16) {
     d.SK = tc_gate_splits(d);
     if (d.SK > L->sk_max) d.SK = L->sk_max;
     while ((d.H / 64) % d.SK) --d.SK;
-    if (!encode_kmajor_bf16(x_map, x, d.H, d.n_pos, 128)) return EPOCH_ECUDA;
+    if (!encode_kmajor_bf16(&x_maps[0], x, d.H, d.n_pos, kTnGate) ||
+        !encode_kmajor_bf16(&x_maps[1], x, d.H, d.n_pos, kTnUp))
+      return EPOCH_ECUDA;
     L->last_sk = d.SK;
-    return run(L, K_GATE, s, [&] { return launch_gate_tc(d, L->maps, L->ws, *x_map, s); });
+    return run(L, K_GATE, s, [&] { return launch_gate_tc(d, L->maps, L->ws, x_maps[0], s); });
   }
   d.SK = 1;
   L->last_sk = 1;
@@ -219,8 +234,10 @@ epoch_status epoch_layer_create(const epoch_layer_config *cfg, const epoch_layer
   d.SK = 1;
   d.R = cfg->refresh_R;
   d.residual = cfg->residual ? 1 : 0;
-  d.tn_up = L->bf16 ? 128 : 0;
-  d.tn_dn = L->bf16 ? 128 : 0;
+  d.tn_up = L->bf16 ? kTnUp : 0;
+  d.tn_dn = L->bf16 ? kTnDn : 0;
+  d.cmax = (cfg->max_positions + 31) / 32;
+  if (L->bf16) tile_caps(*cfg, kTnUp, &d.max_tiles_up, &d.max_tiles_dn);
   d.timeout_ns = 2000000000ll;
   memset(&L->maps, 0, sizeof(L->maps));
   if (L->bf16) {
@@ -232,14 +249,15 @@ epoch_status epoch_layer_create(const epoch_layer_config *cfg, const epoch_layer
     bool ok = encode_kmajor_bf16(&L->maps.w_router, w->w_router, H, E, 128) &&
               encode_kmajor_bf16(&L->maps.w_gate, w->w_gate, H, E * I, 128) &&
               encode_kmajor_bf16(&L->maps.w_up, w->w_up, H, E * I, 128) &&
-              encode_kmajor_bf16(&L->maps.w_down, w->w_down, I, E * H, 128) &&
-              encode_kmajor_bf16(&L->maps.xp, L->ws.xp, H, N * k, d.tn_up) &&
-              encode_kmajor_bf16(&L->maps.a_int, L->ws.a_int, I, N * k, d.tn_dn);
+              encode_kmajor_bf16(&L->maps.w_down, w->w_down, I, E * H, 128);
+    for (int b = 0; ok && b < 4; ++b)
+      ok = encode_kmajor_bf16(&L->maps.xp[b], L->ws.xp, H, N * k, kBoxRows[b]) &&
+           encode_kmajor_bf16(&L->maps.a_int[b], L->ws.a_int, I, N * k, kBoxRows[b]);
     if (ok && nsh > 0) {
       ok = encode_kmajor_bf16(&L->maps.ws_gate, w->ws_gate, H, nsh * Is, 128) &&
            encode_kmajor_bf16(&L->maps.ws_up, w->ws_up, H, nsh * Is, 128) &&
            encode_kmajor_bf16(&L->maps.ws_down, w->ws_down, Is, nsh * H, 128) &&
-           encode_kmajor_bf16(&L->maps.a_sh, L->ws.a_sh, Is, nsh * N, d.tn_dn);
+           encode_kmajor_bf16(&L->maps.a_sh, L->ws.a_sh, Is, nsh * N, kTnDn);
     }
     if (!ok) {
       delete L;
@@ -277,8 +295,8 @@ epoch_status epoch_plan_block(epoch_layer *L, const void *x, int32_t n_pos, epoc
   if (L == nullptr || !aligned16(x) || n_pos < 1 || n_pos > L->cfg.max_positions) return EPOCH_EINVAL;
   cudaStream_t s = S(stream);
   Dims d = call_dims(L, n_pos, 0, 0);
-  CUtensorMap x_map;
-  EPOCH_TRY(run_gate(L, d, x, &x_map, s));
+  CUtensorMap x_maps[2];
+  EPOCH_TRY(run_gate(L, d, x, x_maps, s));
   if (cudaMemsetAsync(L->ws.plan_counts, 0, sizeof(int32_t) * d.E, s) != cudaSuccess) return EPOCH_ECUDA;
   EPOCH_TRY(run(L, K_PLAN_TOPK, s, [&] { return launch_plan_topk(d, L->w, L->ws, s); }));
   const double tau = L->cfg.tau;
@@ -299,14 +317,14 @@ epoch_status epoch_moe_iter(epoch_layer *L, const void *x, const uint8_t *live, 
   cudaStream_t s = S(stream);
   const int host_fallback = !L->planned || iteration != L->last_iter + 1 || n_pos != L->n_pos_plan;
   Dims d = call_dims(L, n_pos, iteration, host_fallback);
-  CUtensorMap x_map;
-  EPOCH_TRY(run_gate(L, d, x, &x_map, s));
+  CUtensorMap x_maps[2];
+  EPOCH_TRY(run_gate(L, d, x, x_maps, s));
   EPOCH_TRY(run(L, K_CLASSIFY, s, [&] { return launch_classify(d, L->ws, live, decoded, s); }));
   EPOCH_TRY(run(L, K_ROUTE, s, [&] { return launch_route(d, L->w, L->ws, s); }));
   EPOCH_TRY(run(L, K_WORKLIST, s, [&] { return launch_worklist(d, L->ws, s); }));
   EPOCH_TRY(run(L, K_PERMUTE, s, [&] { return launch_permute(d, L->ws, x, L->bf16, s); }));
   if (L->bf16) {
-    EPOCH_TRY(run(L, K_UP, s, [&] { return launch_up_tc(d, L->maps, L->ws, x_map, s); }));
+    EPOCH_TRY(run(L, K_UP, s, [&] { return launch_up_tc(d, L->maps, L->ws, x_maps[1], s); }));
     EPOCH_TRY(run(L, K_DOWN, s, [&] { return launch_down_tc(d, L->maps, L->ws, s); }));
   } else {
     EPOCH_TRY(run(L, K_UP, s, [&] { return launch_up_simt(d, L->w, L->ws, x, s); }));

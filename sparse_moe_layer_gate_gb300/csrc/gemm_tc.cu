@@ -36,12 +36,12 @@ constexpr int BK = 64;
 enum Mode { M_GATE = 0, M_UP = 1, M_DOWN = 2 };
 
 struct __align__(128) TcParams {
-  CUtensorMap a0;   // GATE: W_r; UP: W_gate (routed); DOWN: W_down (routed)
-  CUtensorMap a1;   // UP: W_up (routed)
-  CUtensorMap a0s;  // UP: W_gate (shared); DOWN: W_down (shared)
-  CUtensorMap a1s;  // UP: W_up (shared)
-  CUtensorMap b;    // GATE: x; UP: Xp; DOWN: A (routed)
-  CUtensorMap bs;   // UP: x; DOWN: A (shared)
+  CUtensorMap a0;    // GATE: W_r; UP: W_gate (routed); DOWN: W_down (routed)
+  CUtensorMap a1;    // UP: W_up (routed)
+  CUtensorMap a0s;   // UP: W_gate (shared); DOWN: W_down (shared)
+  CUtensorMap a1s;   // UP: W_up (shared)
+  CUtensorMap b[4];  // GATE: b[0] = x; UP: Xp; DOWN: A (routed) -- boxes of 32/64/128/256 rows
+  CUtensorMap bs;    // UP: x; DOWN: A (shared) -- box of TN rows
   Dims d;
   Work ws;
   int32_t gate_tiles;
@@ -66,27 +66,19 @@ struct Cfg {
 };
 
 struct Tile {
-  int a_row, b_row;   // rows in the A (weights) and B (tokens) tensor maps
-  int shared;         // group is a shared expert (selects the *s maps)
-  int k0, nk;         // first K element, number of BK blocks
-  int n_valid;        // valid token columns
-  int out_row0;       // output row of column 0
-  int out_rows;       // rows in the output buffer (bounds check)
-  int ld;             // output leading dimension
-  int col0;           // output column of MMA row 0
-  int m_limit;        // valid MMA rows
+  const CUtensorMap *mb;  // B-operand map (box chosen for the tile)
+  int a_row, b_row;       // rows in the A (weights) and B (tokens) tensor maps
+  int shared;             // group is a shared expert (selects the *s maps)
+  int k0, nk;             // first K element, number of BK blocks
+  int n_valid;            // valid token columns
+  int b_bytes;            // bytes of one B box
+  int out_row0;           // output row of column 0
+  int out_rows;           // rows in the output buffer (bounds check)
+  int ld;                 // output leading dimension
+  int col0;               // output column of MMA row 0
+  int m_limit;            // valid MMA rows
   void *out;
 };
-
-__device__ __forceinline__ int group_of(const int32_t *__restrict__ off, int G, int tile) {
-  int lo = 0, hi = G;  // off[lo] <= tile < off[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (off[mid] <= tile) lo = mid;
-    else hi = mid;
-  }
-  return lo;
-}
 
 template <int MODE, int TN>
 __device__ __forceinline__ Tile decode(const TcParams &p, int tile) {
@@ -98,12 +90,14 @@ __device__ __forceinline__ Tile decode(const TcParams &p, int tile) {
     const int ks = tile / (mt * nt), rem = tile % (mt * nt);
     const int m = rem / nt, tt = rem % nt;
     const int kspan = d.H / d.SK;
+    t.mb = &p.b[0];
     t.a_row = m * BM;
     t.b_row = tt * TN;
     t.shared = 0;
     t.k0 = ks * kspan;
     t.nk = kspan / BK;
     t.n_valid = min(TN, d.n_pos - tt * TN);
+    t.b_bytes = TN * BK * 2;
     t.out_row0 = tt * TN;
     t.out_rows = d.Nmax;
     t.ld = d.E;
@@ -112,30 +106,34 @@ __device__ __forceinline__ Tile decode(const TcParams &p, int tile) {
     t.out = ws.gparts + static_cast<size_t>(ks) * d.Nmax * d.E;
     return t;
   }
-  const int G = d.E + d.n_sh;
-  const int32_t *off = MODE == M_UP ? ws.tile_off_up : ws.tile_off_dn;
-  const int g = group_of(off, G, tile);
-  const int rows = ws.grp_rows[g], row0 = ws.grp_row0[g];
-  const int nt = (rows + TN - 1) / TN;
-  const int local = tile - off[g];
-  const int m = local / nt, tt = local % nt;
+  const int4 td = MODE == M_UP ? ws.tiles_up[tile] : ws.tiles_dn[tile];
+  const int g = td.x, m = td.y, r0 = td.z;
+  t.n_valid = td.w;
   t.shared = g >= d.E;
   const int s = g - d.E;
-  t.n_valid = min(TN, rows - tt * TN);
+  if (t.shared) {
+    t.mb = &p.bs;
+    t.b_bytes = TN * BK * 2;
+  } else {
+    const int bi = t.n_valid <= 32 ? 0 : t.n_valid <= 64 ? 1 : t.n_valid <= 128 ? 2 : 3;
+    t.mb = &p.b[bi];
+    t.b_bytes = (32 << bi) * BK * 2;  // box rows 32, 64, 128, 256
+  }
   t.col0 = m * BM;
   t.m_limit = BM;
   t.k0 = 0;
-  t.out_row0 = row0 + tt * TN;
   if (MODE == M_UP) {
     t.a_row = t.shared ? s * d.I_s + m * BM : g * d.I + m * BM;
-    t.b_row = t.shared ? tt * TN : row0 + tt * TN;
+    t.b_row = r0;
+    t.out_row0 = t.shared ? s * d.Nmax + r0 : r0;
     t.nk = d.H / BK;
     t.ld = t.shared ? d.I_s : d.I;
     t.out = t.shared ? ws.a_sh : ws.a_int;
     t.out_rows = t.shared ? d.n_sh * d.Nmax : d.Nmax * d.k;
   } else {
     t.a_row = t.shared ? s * d.H + m * BM : g * d.H + m * BM;
-    t.b_row = row0 + tt * TN;
+    t.b_row = t.shared ? s * d.Nmax + r0 : r0;
+    t.out_row0 = t.b_row;
     t.nk = (t.shared ? d.I_s : d.I) / BK;
     t.ld = d.H;
     t.out = t.shared ? static_cast<void *>(ws.o_sh) : static_cast<void *>(ws.o_int);
@@ -204,7 +202,7 @@ __global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcPa
     if (lane == 0) {
       // ---------------- TMA producer
       tma_prefetch_desc(&p.a0);
-      tma_prefetch_desc(&p.b);
+      tma_prefetch_desc(&p.b[0]);
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_b = policy_evict_last();
       int stage = 0;
@@ -214,13 +212,14 @@ __global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcPa
         const Tile t = decode<MODE, TN>(p, tile);
         const CUtensorMap *ma0 = t.shared ? &p.a0s : &p.a0;
         const CUtensorMap *ma1 = t.shared ? &p.a1s : &p.a1;
-        const CUtensorMap *mb = t.shared ? &p.bs : &p.b;
+        const CUtensorMap *mb = t.mb;
+        const uint32_t tx = C::NA * C::A_BYTES + t.b_bytes;
         for (int kb = 0; kb < t.nk; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, ws.err, tmo)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(stage), C::STAGE_BYTES);
+          mbar_arrive_expect_tx(full_bar(stage), tx);
           const int kc = t.k0 + kb * BK;
           const uint32_t a_dst = sA + stage * C::NA * C::A_BYTES;
           tma_load_2d(a_dst, ma0, kc, t.a_row, full_bar(stage), pol_w);
@@ -363,9 +362,9 @@ bool encode_kmajor_bf16(CUtensorMap *map, const void *base, uint64_t k_elems, ui
   return r == CUDA_SUCCESS;
 }
 
-constexpr int kTnGate = 128, kStGate = 6;
-constexpr int kTnUp = 128, kStUp = 4;
-constexpr int kTnDn = 128, kStDn = 6;
+constexpr int kStGate = 6;
+constexpr int kStUp = 3;  // 64 KB stages (W_gate + W_up + 256 token rows)
+constexpr int kStDn = 4;  // 48 KB stages
 
 // Split count of the gate along H: enough (m, n, split) tiles to cover the SMs,
 // each split a whole number of 64-wide K blocks.
@@ -406,14 +405,14 @@ cudaError_t launch_gate_tc(const Dims &d, const Maps &m, const Work &ws, const C
   TcParams p;
   base_params(p, d, ws);
   p.a0 = m.w_router;
-  p.b = x_map;
+  p.b[0] = x_map;
   const int tiles = ((d.E + BM - 1) / BM) * ((d.n_pos + kTnGate - 1) / kTnGate) * d.SK;
   p.gate_tiles = tiles;
   const int grid = tiles < num_sms() ? tiles : num_sms();
   return launch_tc<M_GATE, kTnGate, kStGate>(p, grid, s);
 }
 
-cudaError_t launch_up_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map,
+cudaError_t launch_up_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map256,
                          cudaStream_t s) {
   TcParams p;
   base_params(p, d, ws);
@@ -421,8 +420,8 @@ cudaError_t launch_up_tc(const Dims &d, const Maps &m, const Work &ws, const CUt
   p.a1 = m.w_up;
   p.a0s = m.ws_gate;
   p.a1s = m.ws_up;
-  p.b = m.xp;
-  p.bs = x_map;
+  for (int i = 0; i < 4; ++i) p.b[i] = m.xp[i];
+  p.bs = x_map256;
   return launch_tc<M_UP, kTnUp, kStUp>(p, num_sms(), s);
 }
 
@@ -431,7 +430,7 @@ cudaError_t launch_down_tc(const Dims &d, const Maps &m, const Work &ws, cudaStr
   base_params(p, d, ws);
   p.a0 = m.w_down;
   p.a0s = m.ws_down;
-  p.b = m.a_int;
+  for (int i = 0; i < 4; ++i) p.b[i] = m.a_int[i];
   p.bs = m.a_sh;
   return launch_tc<M_DOWN, kTnDn, kStDn>(p, num_sms(), s);
 }

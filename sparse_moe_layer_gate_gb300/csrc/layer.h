@@ -38,12 +38,11 @@ struct Work {
   int32_t *fresh_pos;     // [Nmax] ascending fresh positions
   int32_t *sel;           // [Nmax][k]
   float *selw;            // [Nmax][k]
-  uint32_t *chunk_mask;   // [Nmax/32][E] bit p: fresh position p of the chunk selected e
+  uint32_t *chunk_mask;   // [E][cmax] bit p of word c: fresh position 32c + p selected expert e
+  int32_t *expert_cnt;    // [E] worklist rows of each expert
   int32_t *offsets;       // [E+1]
-  int32_t *grp_rows;      // [G] rows of each grouped-GEMM group (routed experts, then shared)
-  int32_t *grp_row0;      // [G] first row of the group in the compact buffers
-  int32_t *tile_off_up;   // [G+1]
-  int32_t *tile_off_dn;   // [G+1]
+  int4 *tiles_up;         // [max_tiles_up] {group, m tile, first row, valid rows}
+  int4 *tiles_dn;         // [max_tiles_dn]
   int32_t *wl_pos;        // [Nmax*k] expert-sorted worklist positions
   int32_t *slot;          // [Nmax][k] worklist row of selection (f, j)
   void *xp;               // [Nmax*k][H] permuted fresh rows
@@ -65,6 +64,8 @@ struct Dims {
   int32_t iter;
   int32_t host_fallback;
   int32_t tn_up, tn_dn;  // token-tile width of the tcgen05 grouped GEMMs (0 on the SIMT path)
+  int32_t cmax;          // chunk capacity: ceil(Nmax / 32)
+  int32_t max_tiles_up, max_tiles_dn;
   int64_t timeout_ns;
 };
 
@@ -84,10 +85,14 @@ struct Maps {
   CUtensorMap ws_gate;    // [n_sh*I_s][H]
   CUtensorMap ws_up;
   CUtensorMap ws_down;    // [n_sh*H][I_s]
-  CUtensorMap xp;         // [Nmax*k][H], box 64 x tn_up
-  CUtensorMap a_int;      // [Nmax*k][I], box 64 x tn_dn
-  CUtensorMap a_sh;       // [n_sh*Nmax][I_s], box 64 x tn_dn
+  CUtensorMap xp[4];      // [Nmax*k][H], boxes 64 x {32, 64, 128, 256}
+  CUtensorMap a_int[4];   // [Nmax*k][I], boxes 64 x {32, 64, 128, 256}
+  CUtensorMap a_sh;       // [n_sh*Nmax][I_s], box 64 x 256
 };
+
+// Token-box heights of the routed B operands; a tile loads the smallest box
+// that holds its valid rows.
+constexpr int kBoxRows[4] = {32, 64, 128, 256};
 
 // Kernel kinds, for profiling and launch counting.
 enum Kind {
@@ -119,9 +124,12 @@ cudaError_t launch_down_simt(const Dims &d, const Weights &w, const Work &ws, cu
 bool tma_encode_init();
 bool encode_kmajor_bf16(CUtensorMap *map, const void *base, uint64_t k_elems, uint64_t rows, uint32_t box_rows);
 int tc_gate_splits(const Dims &d);
+constexpr int kTnGate = 128;  // gate token tile (x box rows)
+constexpr int kTnUp = 256;    // grouped-GEMM token tiles
+constexpr int kTnDn = 256;
 cudaError_t launch_gate_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map,
                            cudaStream_t s);
-cudaError_t launch_up_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map,
+cudaError_t launch_up_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map256,
                          cudaStream_t s);
 cudaError_t launch_down_tc(const Dims &d, const Maps &m, const Work &ws, cudaStream_t s);
 

@@ -43,41 +43,113 @@ __device__ __forceinline__ void warp_best(float &v, int &id) {
   }
 }
 
-// Logit of expert e at position t: split-K partial sums in fixed order, then the bias.
-__device__ __forceinline__ float logit(const float *__restrict__ gparts, int SK, int Nmax, int E, int t, int e,
-                                       const float *__restrict__ bias) {
-  float g = gparts[static_cast<size_t>(t) * E + e];
-  for (int s = 1; s < SK; ++s) g += gparts[(static_cast<size_t>(s) * Nmax + t) * E + e];
-  return g + bias[e];
+// Logits of the EPL consecutive experts [lane*EPL, lane*EPL + EPL) of position
+// t: split-K partial sums in a fixed order, then the bias. Experts >= E get
+// -inf. Vector loads when the row is 16-byte aligned.
+template <int EPL>
+__device__ __forceinline__ void lane_logits(const float *__restrict__ gparts, int SK, int Nmax, int E, int t,
+                                            const float *__restrict__ bias, float (&v)[EPL]) {
+  const int e0 = lane_id() * EPL;
+#pragma unroll
+  for (int c = 0; c < EPL; ++c) v[c] = 0.f;
+  if constexpr (EPL % 4 == 0) {
+    if ((E & 3) == 0 && e0 + EPL <= E) {
+#pragma unroll 4
+      for (int s = 0; s < SK; ++s) {
+        const float4 *src = reinterpret_cast<const float4 *>(gparts + (static_cast<size_t>(s) * Nmax + t) * E + e0);
+#pragma unroll
+        for (int q = 0; q < EPL / 4; ++q) {
+          const float4 a = __ldg(src + q);
+          v[4 * q] += a.x;
+          v[4 * q + 1] += a.y;
+          v[4 * q + 2] += a.z;
+          v[4 * q + 3] += a.w;
+        }
+      }
+      const float4 *bs = reinterpret_cast<const float4 *>(bias + e0);
+#pragma unroll
+      for (int q = 0; q < EPL / 4; ++q) {
+        const float4 b = __ldg(bs + q);
+        v[4 * q] += b.x;
+        v[4 * q + 1] += b.y;
+        v[4 * q + 2] += b.z;
+        v[4 * q + 3] += b.w;
+      }
+      return;
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < EPL; ++c) {
+    const int e = e0 + c;
+    if (e < E) {
+      float g = 0.f;
+      for (int s = 0; s < SK; ++s) g += __ldg(gparts + (static_cast<size_t>(s) * Nmax + t) * E + e);
+      v[c] = g + __ldg(bias + e);
+    } else {
+      v[c] = -INFINITY;
+    }
+  }
 }
 
-// Top-k of one position by one warp. Lane l owns experts l, l+32, ... Ineligible
-// experts never win. Writes sel/val (selection order) on every lane.
+// Top-k of one position by one warp over lane-owned experts lane*EPL + c;
+// ineligible experts never win. Every lane gets the selection (order: value
+// desc, id asc) in sel/val.
 template <int EPL>
-__device__ __forceinline__ void warp_topk(const float (&v)[EPL], const bool (&ok)[EPL], int k, int *sel,
-                                          float *val) {
+__device__ __forceinline__ void warp_topk(const float (&v)[EPL], const bool (&ok)[EPL], int k, int (&sel)[16],
+                                          float (&val)[16]) {
   bool taken[EPL];
 #pragma unroll
   for (int c = 0; c < EPL; ++c) taken[c] = !ok[c];
-  const int lane = lane_id();
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = INT_MAX;
+  const int e0 = lane_id() * EPL;
 #pragma unroll
-    for (int c = 0; c < EPL; ++c) {
-      const int e = lane + 32 * c;
-      if (!taken[c] && ranks_before(v[c], e, bv, bi)) {
-        bv = v[c];
-        bi = e;
+  for (int j = 0; j < 16; ++j) {
+    if (j < k) {
+      float bv = -INFINITY;
+      int bi = INT_MAX;
+#pragma unroll
+      for (int c = 0; c < EPL; ++c) {
+        if (!taken[c] && ranks_before(v[c], e0 + c, bv, bi)) {
+          bv = v[c];
+          bi = e0 + c;
+        }
       }
-    }
-    warp_best(bv, bi);
-    sel[j] = bi;
-    val[j] = bv;
+      warp_best(bv, bi);
+      sel[j] = bi;
+      val[j] = bv;
 #pragma unroll
-    for (int c = 0; c < EPL; ++c)
-      if (lane + 32 * c == bi) taken[c] = true;
+      for (int c = 0; c < EPL; ++c)
+        if (e0 + c == bi) taken[c] = true;
+    }
   }
+}
+
+// Exclusive scan over a CTA of up to 1024 threads; *total gets the sum.
+__device__ __forceinline__ int block_excl_scan(int v, int *warp_tmp, int *total) {
+  const int lane = lane_id(), wid = warp_id(), nw = (blockDim.x + 31) >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) warp_tmp[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int x = lane < nw ? warp_tmp[lane] : 0;
+    int xi = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, xi, o);
+      if (lane >= o) xi += u;
+    }
+    warp_tmp[lane] = xi - x;
+    if (lane == 31) warp_tmp[32] = xi;
+  }
+  __syncthreads();
+  const int r = warp_tmp[wid] + incl - v;
+  *total = warp_tmp[32];
+  __syncthreads();
+  return r;
 }
 
 // ---------------------------------------------------------------- gate (SIMT)
@@ -109,22 +181,15 @@ __global__ void k_plan_topk(Dims d, const float *__restrict__ gparts, const floa
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < d.n_pos; t += warps) {
     float v[EPL];
     bool ok[EPL];
+    lane_logits<EPL>(gparts, d.SK, d.Nmax, d.E, t, bias, v);
 #pragma unroll
-    for (int c = 0; c < EPL; ++c) {
-      const int e = lane + 32 * c;
-      ok[c] = e < d.E;
-      v[c] = ok[c] ? logit(gparts, d.SK, d.Nmax, d.E, t, e, bias) : -INFINITY;
-    }
+    for (int c = 0; c < EPL; ++c) ok[c] = lane * EPL + c < d.E;
     int sel[16];
     float val[16];
     warp_topk<EPL>(v, ok, d.k, sel, val);
-    if (lane < d.k) {
-      int mine = 0;
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (j == lane) mine = sel[j];
-      atomicAdd(&counts[mine], 1);
-    }
+    for (int j = 0; j < 16; ++j)
+      if (j < d.k && j == lane) atomicAdd(&counts[sel[j]], 1);
   }
 }
 
@@ -194,6 +259,7 @@ __global__ void __launch_bounds__(1024) k_classify(Dims d, Work ws, const uint8_
   __shared__ int32_t cat[8];
   const int tid = threadIdx.x;
   if (tid < 8) cat[tid] = 0;
+  if (tid < d.E) ws.expert_cnt[tid] = 0;  // the route kernel counts each expert's rows
   const int n = d.n_pos;
   const int per = (n + kThreads - 1) / kThreads;
   const int lo = min(tid * per, n), hi = min(lo + per, n);
@@ -305,160 +371,165 @@ __global__ void __launch_bounds__(1024) k_classify(Dims d, Work ws, const uint8_
 }
 
 // ---------------------------------------------------------------- restricted top-k
-// One CTA per chunk of 32 fresh positions (8 warps x 4 positions). Each fresh
-// position takes its top-k over the support (every expert on a fallback),
-// softmax weights over the selected logits, and marks bit p of the chunk's
-// per-expert mask; the masks give the worklist its offsets without sorting.
+// One CTA of 32 warps per chunk of 32 fresh positions, one warp per position.
+// Each fresh position takes its top-k over the support (every expert on a
+// fallback) and softmax weights over the selected logits, and sets bit p of the
+// chunk's per-expert mask; mask popcounts give the worklist its offsets with
+// no sort ("count exchange" of [W] section "FreshLane Dispatch", on chip).
 template <int EPL>
-__global__ void __launch_bounds__(256) k_route(Dims d, Work ws, const float *__restrict__ bias) {
+__global__ void __launch_bounds__(1024) k_route(Dims d, Work ws, const float *__restrict__ bias) {
   __shared__ uint32_t mask[1024];
   const int chunk = blockIdx.x;
   const int n_fresh = ws.ctrl->n_fresh;
   if (chunk * 32 >= n_fresh) return;
   for (int e = threadIdx.x; e < d.E; e += blockDim.x) mask[e] = 0;
   __syncthreads();
-  const bool all = ws.ctrl->fallback != 0;
-  const int lane = lane_id(), wid = warp_id();
-  bool elig[EPL];
-#pragma unroll
-  for (int c = 0; c < EPL; ++c) {
-    const int e = lane + 32 * c;
-    elig[c] = e < d.E && (all || ws.support_mask[e]);
-  }
-  for (int p = wid * 4; p < wid * 4 + 4; ++p) {
-    const int f = chunk * 32 + p;
-    if (f >= n_fresh) break;
+  const int lane = lane_id(), p = warp_id();
+  const int f = chunk * 32 + p;
+  if (f < n_fresh) {
     const int t = ws.fresh_pos[f];
+    const bool all = ws.ctrl->fallback != 0;
     float v[EPL];
+    bool ok[EPL];
+    lane_logits<EPL>(ws.gparts, d.SK, d.Nmax, d.E, t, bias, v);
 #pragma unroll
     for (int c = 0; c < EPL; ++c) {
-      const int e = lane + 32 * c;
-      v[c] = elig[c] ? logit(ws.gparts, d.SK, d.Nmax, d.E, t, e, bias) : -INFINITY;
+      const int e = lane * EPL + c;
+      ok[c] = e < d.E && (all || ws.support_mask[e]);
     }
     int sel[16];
     float val[16];
-    warp_topk<EPL>(v, elig, d.k, sel, val);
+    warp_topk<EPL>(v, ok, d.k, sel, val);
     float denom = 0.f;
-    for (int j = 0; j < d.k; ++j) denom += expf(val[j] - val[0]);
-    if (lane < d.k) {
-      int e = 0;
-      float g = 0.f;
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (j == lane) {
-          e = sel[j];
-          g = val[j];
-        }
-      ws.sel[f * d.k + lane] = e;
-      ws.selw[f * d.k + lane] = expf(g - val[0]) / denom;
-      if (e >= 0 && e < d.E) atomicOr(&mask[e], 1u << p);
-      else set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+    for (int j = 0; j < 16; ++j)
+      if (j < d.k) denom += expf(val[j] - val[0]);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (j < d.k && j == lane) {
+        const int e = sel[j];
+        ws.sel[f * d.k + j] = e;
+        ws.selw[f * d.k + j] = expf(val[j] - val[0]) / denom;
+        if (e >= 0 && e < d.E) atomicOr(&mask[e], 1u << p);
+        else set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+      }
     }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < d.E; e += blockDim.x) ws.chunk_mask[static_cast<size_t>(chunk) * d.E + e] = mask[e];
+  for (int e = threadIdx.x; e < d.E; e += blockDim.x) {
+    const uint32_t m = mask[e];
+    ws.chunk_mask[static_cast<size_t>(e) * d.cmax + chunk] = m;
+    if (m) atomicAdd(&ws.expert_cnt[e], __popc(m));
+  }
 }
 
 // ---------------------------------------------------------------- worklist
-// One CTA per chunk: offsets[e] = exclusive scan over experts of their edge
-// counts (popcounts of every chunk mask), this chunk's base inside expert e =
-// popcounts of earlier chunks; an edge (p, e) lands at
-// offsets[e] + base_e + popc(mask[e] & bits below p): expert-major, positions
-// ascending, with no atomics. CTA 0 also writes the grouped-GEMM tile tables.
-__global__ void __launch_bounds__(256) k_worklist(Dims d, Work ws) {
-  __shared__ int32_t base[1024];
-  __shared__ uint32_t mymask[1024];
-  __shared__ int32_t tot[1024];
-  __shared__ int32_t scan_tmp[256];
+// CTA e < E places expert e's rows: row offsets[e] + (rows of expert e in
+// earlier chunks) + (bits of its chunk mask below p), so rows are grouped by
+// expert with positions ascending, with no sort and no atomics; warp w of the
+// CTA takes chunk w of each 32-chunk pass. The last CTA writes the expert
+// offsets and the grouped-GEMM tile lists: routed experts with at least one
+// row, then the shared experts over every position; experts with no rows get
+// no tile, so their weights are never read ([W] section "FreshLane Dispatch":
+// invalid slots load no expert weights).
+__global__ void __launch_bounds__(1024) k_worklist(Dims d, Work ws) {
+  __shared__ int32_t tmp[33];
+  __shared__ int32_t wsum[32];
+  const int E = d.E, k = d.k;
+  const int tid = threadIdx.x, lane = lane_id(), wid = warp_id();
   const int n_fresh = ws.ctrl->n_fresh;
   const int n_chunks = (n_fresh + 31) / 32;
-  const int chunk = blockIdx.x;
-  if (chunk >= (n_chunks > 0 ? n_chunks : 1)) return;
-  const int E = d.E;
-  const int tid = threadIdx.x;
-  for (int e = tid; e < E; e += blockDim.x) {
-    int before = 0, total = 0;
-    for (int c = 0; c < n_chunks; ++c) {
-      const int pc = __popc(ws.chunk_mask[static_cast<size_t>(c) * E + e]);
-      total += pc;
-      before += (c < chunk) ? pc : 0;
+  if (static_cast<int>(blockIdx.x) < E) {
+    const int e = blockIdx.x;
+    if (ws.expert_cnt[e] == 0) return;
+    int part = 0;
+    for (int q = tid; q < e; q += blockDim.x) part += ws.expert_cnt[q];
+    int off;
+    (void)block_excl_scan(part, tmp, &off);
+    int run = 0;
+    for (int c0 = 0; c0 < n_chunks; c0 += 32) {
+      const int c = c0 + wid;
+      const uint32_t m = c < n_chunks ? ws.chunk_mask[static_cast<size_t>(e) * d.cmax + c] : 0u;
+      if (lane == 0) wsum[wid] = __popc(m);
+      __syncthreads();
+      if (wid == 0) {
+        const int x = wsum[lane];
+        int xi = x;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int u = __shfl_up_sync(0xffffffffu, xi, o);
+          if (lane >= o) xi += u;
+        }
+        wsum[lane] = xi - x;
+        if (lane == 31) tmp[32] = xi;
+      }
+      __syncthreads();
+      if ((m >> lane) & 1u) {
+        const int f = c * 32 + lane;
+        const int dst = off + run + wsum[wid] + __popc(m & ((1u << lane) - 1u));
+        if (dst < 0 || dst >= d.Nmax * k || f >= n_fresh) {
+          set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+        } else {
+          ws.wl_pos[dst] = ws.fresh_pos[f];
+          for (int j = 0; j < k; ++j)
+            if (ws.sel[f * k + j] == e) ws.slot[f * k + j] = dst;
+        }
+      }
+      run += tmp[32];
+      __syncthreads();
     }
-    tot[e] = total;
-    base[e] = before;
-    mymask[e] = chunk < n_chunks ? ws.chunk_mask[static_cast<size_t>(chunk) * E + e] : 0u;
+    return;
   }
-  __syncthreads();
-  // exclusive scan of tot over experts: thread tid owns experts [tid*per, tid*per + per)
-  const int per = (E + 255) / 256;
-  int local = 0;
-  for (int q = 0; q < per; ++q) {
-    const int e = tid * per + q;
-    if (e < E) local += tot[e];
-  }
-  scan_tmp[tid] = local;
-  __syncthreads();
-  for (int off = 1; off < 256; off <<= 1) {
-    int add = tid >= off ? scan_tmp[tid - off] : 0;
-    __syncthreads();
-    scan_tmp[tid] += add;
-    __syncthreads();
-  }
-  int run = scan_tmp[tid] - local;
-  for (int q = 0; q < per; ++q) {
-    const int e = tid * per + q;
-    if (e < E) {
-      const int o = run;
-      run += tot[e];
-      if (chunk == 0) ws.offsets[e] = o;
-      base[e] += o;
-    }
-  }
-  if (chunk == 0 && tid == 255) ws.offsets[E] = run;
-  __syncthreads();
-  // scatter this chunk's edges
-  const int k = d.k;
-  for (int q = tid; q < 32 * k; q += blockDim.x) {
-    const int p = q / k, j = q % k;
-    const int f = chunk * 32 + p;
-    if (f >= n_fresh) continue;
-    const int e = ws.sel[f * k + j];
-    if (e < 0 || e >= E) {
-      set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-      continue;
-    }
-    const int dst = base[e] + __popc(mymask[e] & ((1u << p) - 1u));
-    if (dst < 0 || dst >= d.Nmax * k) {
-      set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-      continue;
-    }
-    ws.wl_pos[dst] = ws.fresh_pos[f];
-    ws.slot[f * k + j] = dst;
-  }
-  if (chunk != 0) return;
-  // tile tables (groups: routed experts, then shared experts over all positions)
-  __syncthreads();
+  // ---- last CTA: offsets and tile lists
+  const int cnt = tid < E ? ws.expert_cnt[tid] : 0;
+  int total;
+  const int off = block_excl_scan(cnt, tmp, &total);
+  if (tid < E) ws.offsets[tid] = off;
+  if (tid == 0) ws.offsets[E] = total;
   const int G = E + d.n_sh;
-  if (tid == 0) {
-    int hit = 0, up = 0, dn = 0;
-    const int mt_up = d.I / 128, mt_sh = d.I_s / 128, mt_dn = d.H / 128;
-    for (int g = 0; g < G; ++g) {
-      const bool routed = g < E;
-      const int rows = routed ? tot[g] : d.n_pos;
-      const int row0 = routed ? ws.offsets[g] : (g - E) * d.Nmax;
-      ws.grp_rows[g] = rows;
-      ws.grp_row0[g] = row0;
-      ws.tile_off_up[g] = up;
-      ws.tile_off_dn[g] = dn;
-      if (routed) hit += rows > 0;
-      if (d.tn_up > 0) up += ((rows + d.tn_up - 1) / d.tn_up) * (routed ? mt_up : mt_sh);
-      if (d.tn_dn > 0) dn += ((rows + d.tn_dn - 1) / d.tn_dn) * mt_dn;
+  const bool routed = tid < E;
+  const bool grp = tid < G;
+  const int rows = routed ? cnt : (grp ? d.n_pos : 0);
+  const int r0 = routed ? off : 0;
+  int tu = 0, td = 0;
+  if (grp && rows > 0 && d.tn_up > 0) {
+    tu = ((rows + d.tn_up - 1) / d.tn_up) * ((routed ? d.I : d.I_s) / 128);
+    td = ((rows + d.tn_dn - 1) / d.tn_dn) * (d.H / 128);
+  }
+  int n_up, n_dn, n_hit;
+  const int bu = block_excl_scan(tu, tmp, &n_up);
+  const int bd = block_excl_scan(td, tmp, &n_dn);
+  (void)block_excl_scan(routed && cnt > 0 ? 1 : 0, tmp, &n_hit);
+  if (tu > 0) {
+    const int nt = (rows + d.tn_up - 1) / d.tn_up;
+    const int mt = (routed ? d.I : d.I_s) / 128;
+    for (int q = 0; q < tu; ++q) {
+      const int m = q / nt, tt = q % nt;
+      const int slot = bu + q;
+      if (slot < d.max_tiles_up)
+        ws.tiles_up[slot] = make_int4(tid, m, r0 + tt * d.tn_up, min(d.tn_up, rows - tt * d.tn_up));
+      else
+        set_error(ws.err, EPOCH_DEVERR_BOUNDS);
     }
-    ws.tile_off_up[G] = up;
-    ws.tile_off_dn[G] = dn;
-    ws.ctrl->n_hit = hit;
+    (void)mt;
+  }
+  if (td > 0) {
+    const int nt = (rows + d.tn_dn - 1) / d.tn_dn;
+    for (int q = 0; q < td; ++q) {
+      const int m = q / nt, tt = q % nt;
+      const int slot = bd + q;
+      if (slot < d.max_tiles_dn)
+        ws.tiles_dn[slot] = make_int4(tid, m, r0 + tt * d.tn_dn, min(d.tn_dn, rows - tt * d.tn_dn));
+      else
+        set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+    }
+  }
+  if (tid == 0) {
+    const int up = min(n_up, d.max_tiles_up), dn = min(n_dn, d.max_tiles_dn);
+    ws.ctrl->n_hit = n_hit;
     ws.ctrl->tiles_up = up;
     ws.ctrl->tiles_dn = dn;
-    ws.stats->n_hit_experts = hit;
+    ws.stats->n_hit_experts = n_hit;
     ws.stats->tiles_up = up;
     ws.stats->tiles_down = dn;
   }
@@ -483,9 +554,38 @@ __global__ void k_permute(Dims d, Work ws, const uint4 *__restrict__ x, int vec_
 }
 
 // ---------------------------------------------------------------- combine + cache
-// One CTA per position. Fresh t: r = sum_j w_j O[slot(t, j)] (j ascending,
-// fp32) and the cache row is refilled; reused t: r = cached row. Then
-// y = r + shared outputs (+ x when residual), rounded once.
+// Eight consecutive elements of a row, loaded/stored as one or two 16-byte vectors.
+__device__ __forceinline__ void load8(const float *p, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4 *>(p), b = *reinterpret_cast<const float4 *>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&v)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4 *>(p);
+  const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 f = __bfloat1622float2(h[q]);
+    v[2 * q] = f.x;
+    v[2 * q + 1] = f.y;
+  }
+}
+__device__ __forceinline__ void store8(float *p, const float (&v)[8]) {
+  *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  *reinterpret_cast<float4 *>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+__device__ __forceinline__ void store8(__nv_bfloat16 *p, const float (&v)[8]) {
+  uint4 u;
+  __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&u);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) h[q] = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+  *reinterpret_cast<uint4 *>(p) = u;
+}
+
+// One CTA per position, 8 elements per thread per pass. Fresh t:
+// r = sum_j w_j O[slot(t, j)] (j ascending, fp32) and the cache row is refilled
+// ([W] section "Liveness-Shard Parallelism": Y[F_i] = Y_F); reused t: r = the
+// cached row (Y[not F_i] = C_l[not F_i]). Then y = r + shared outputs (+ x when
+// residual), rounded once: the dense shard is restored at the layer boundary.
 template <typename T>
 __global__ void __launch_bounds__(128) k_combine(Dims d, Work ws, const T *__restrict__ x, T *__restrict__ y) {
   const int t = blockIdx.x;
@@ -505,38 +605,35 @@ __global__ void __launch_bounds__(128) k_combine(Dims d, Work ws, const T *__res
     w_s[threadIdx.x] = ws.selw[f * k + threadIdx.x];
   }
   __syncthreads();
-  for (int h0 = threadIdx.x * 4; h0 < H; h0 += blockDim.x * 4) {
-    float r[4];
+  for (int h0 = threadIdx.x * 8; h0 < H; h0 += blockDim.x * 8) {
+    float r[8];
     if (f >= 0) {
-      r[0] = r[1] = r[2] = r[3] = 0.f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) r[q] = 0.f;
       for (int j = 0; j < k; ++j) {
-        const float4 o = *reinterpret_cast<const float4 *>(ws.o_int + static_cast<size_t>(slot_s[j]) * H + h0);
+        float o[8];
+        load8(ws.o_int + static_cast<size_t>(slot_s[j]) * H + h0, o);
         const float wj = w_s[j];
-        r[0] = fmaf(wj, o.x, r[0]);
-        r[1] = fmaf(wj, o.y, r[1]);
-        r[2] = fmaf(wj, o.z, r[2]);
-        r[3] = fmaf(wj, o.w, r[3]);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) r[q] = fmaf(wj, o[q], r[q]);
       }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) cache[h0 + q] = from_f32<T>(r[q]);
+      store8(cache + h0, r);
     } else {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) r[q] = to_f32(cache[h0 + q]);
+      load8(cache + h0, r);
     }
     for (int s = 0; s < d.n_sh; ++s) {
-      const float4 o =
-          *reinterpret_cast<const float4 *>(ws.o_sh + (static_cast<size_t>(s) * d.Nmax + t) * H + h0);
-      r[0] += o.x;
-      r[1] += o.y;
-      r[2] += o.z;
-      r[3] += o.w;
+      float o[8];
+      load8(ws.o_sh + (static_cast<size_t>(s) * d.Nmax + t) * H + h0, o);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) r[q] += o[q];
     }
     if (d.residual) {
+      float xv[8];
+      load8(x + static_cast<size_t>(t) * H + h0, xv);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) r[q] += to_f32(x[static_cast<size_t>(t) * H + h0 + q]);
+      for (int q = 0; q < 8; ++q) r[q] += xv[q];
     }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) y[static_cast<size_t>(t) * H + h0 + q] = from_f32<T>(r[q]);
+    store8(y + static_cast<size_t>(t) * H + h0, r);
   }
 }
 
@@ -617,7 +714,7 @@ cudaError_t launch_route(const Dims &d, const Weights &w, const Work &ws, cudaSt
   const int chunks = (d.Nmax + 31) / 32;
   switch (epl_for(d.E)) {
 #define EPOCH_CASE(N) \
-  case N: k_route<N><<<chunks, 256, 0, s>>>(d, ws, w.b_router); break;
+  case N: k_route<N><<<chunks, 1024, 0, s>>>(d, ws, w.b_router); break;
     EPOCH_CASE(1) EPOCH_CASE(2) EPOCH_CASE(4) EPOCH_CASE(8) EPOCH_CASE(16) EPOCH_CASE(32)
 #undef EPOCH_CASE
   }
@@ -625,8 +722,7 @@ cudaError_t launch_route(const Dims &d, const Weights &w, const Work &ws, cudaSt
 }
 
 cudaError_t launch_worklist(const Dims &d, const Work &ws, cudaStream_t s) {
-  const int chunks = (d.Nmax + 31) / 32;
-  k_worklist<<<chunks, 256, 0, s>>>(d, ws);
+  k_worklist<<<d.E + 1, 1024, 0, s>>>(d, ws);
   return cudaGetLastError();
 }
 
