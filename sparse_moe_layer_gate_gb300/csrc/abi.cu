@@ -124,6 +124,14 @@ size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   t.a_sh = take(nsh * N * Is * act + 16);
   t.o_int = static_cast<float *>(take(N * k * H * 4));
   t.o_sh = static_cast<float *>(take(nsh * N * H * 4 + 16));
+  if (c.dtype == EPOCH_BF16) {
+    t.pk_gu = static_cast<uint8_t *>(take(E * I * H * 2 * 2));
+    t.pk_d = static_cast<uint8_t *>(take(E * H * I * 2));
+    t.pk_sgu = static_cast<uint8_t *>(take(nsh * Is * H * 2 * 2 + 16));
+    t.pk_sd = static_cast<uint8_t *>(take(nsh * H * Is * 2 + 16));
+  } else {
+    t.pk_gu = t.pk_d = t.pk_sgu = t.pk_sd = nullptr;
+  }
   t.ctrl = static_cast<Ctrl *>(take(sizeof(Ctrl)));
   t.stats = static_cast<epoch_iter_stats *>(take(sizeof(epoch_iter_stats)));
   t.err = static_cast<uint32_t *>(take(16));
@@ -246,18 +254,12 @@ epoch_status epoch_layer_create(const epoch_layer_config *cfg, const epoch_layer
       return EPOCH_ECUDA;
     }
     const uint64_t H = d.H, E = d.E, I = d.I, N = d.Nmax, k = d.k, nsh = d.n_sh, Is = d.I_s;
-    bool ok = encode_kmajor_bf16(&L->maps.w_router, w->w_router, H, E, 128) &&
-              encode_kmajor_bf16(&L->maps.w_gate, w->w_gate, H, E * I, 128) &&
-              encode_kmajor_bf16(&L->maps.w_up, w->w_up, H, E * I, 128) &&
-              encode_kmajor_bf16(&L->maps.w_down, w->w_down, I, E * H, 128);
+    bool ok = encode_kmajor_bf16(&L->maps.w_router, w->w_router, H, E, 128);
     for (int b = 0; ok && b < 4; ++b)
       ok = encode_kmajor_bf16(&L->maps.xp[b], L->ws.xp, H, N * k, kBoxRows[b]) &&
            encode_kmajor_bf16(&L->maps.a_int[b], L->ws.a_int, I, N * k, kBoxRows[b]);
     if (ok && nsh > 0) {
-      ok = encode_kmajor_bf16(&L->maps.ws_gate, w->ws_gate, H, nsh * Is, 128) &&
-           encode_kmajor_bf16(&L->maps.ws_up, w->ws_up, H, nsh * Is, 128) &&
-           encode_kmajor_bf16(&L->maps.ws_down, w->ws_down, Is, nsh * H, 128) &&
-           encode_kmajor_bf16(&L->maps.a_sh, L->ws.a_sh, Is, nsh * N, kTnDn);
+      ok = encode_kmajor_bf16(&L->maps.a_sh, L->ws.a_sh, Is, nsh * N, kTnDn);
     }
     if (!ok) {
       delete L;
@@ -270,6 +272,22 @@ epoch_status epoch_layer_create(const epoch_layer_config *cfg, const epoch_layer
       cudaMemset(L->ws.support_mask, 1, d.E) != cudaSuccess) {
     delete L;
     return EPOCH_ECUDA;
+  }
+  if (L->bf16) {
+    // expert weights -> packed swizzled tiles (gate and up tiles interleaved)
+    const int64_t H = d.H, E = d.E, I = d.I, nsh = d.n_sh, Is = d.I_s, T = kTileBytes;
+    cudaError_t e = launch_pack_tiles(w->w_gate, E * I, H, L->ws.pk_gu, 2 * T, 0, nullptr);
+    if (e == cudaSuccess) e = launch_pack_tiles(w->w_up, E * I, H, L->ws.pk_gu, 2 * T, T, nullptr);
+    if (e == cudaSuccess) e = launch_pack_tiles(w->w_down, E * H, I, L->ws.pk_d, T, 0, nullptr);
+    if (e == cudaSuccess && nsh > 0) {
+      e = launch_pack_tiles(w->ws_gate, nsh * Is, H, L->ws.pk_sgu, 2 * T, 0, nullptr);
+      if (e == cudaSuccess) e = launch_pack_tiles(w->ws_up, nsh * Is, H, L->ws.pk_sgu, 2 * T, T, nullptr);
+      if (e == cudaSuccess) e = launch_pack_tiles(w->ws_down, nsh * H, Is, L->ws.pk_sd, T, 0, nullptr);
+    }
+    if (e != cudaSuccess) {
+      delete L;
+      return EPOCH_ECUDA;
+    }
   }
   Ctrl c0;
   memset(&c0, 0, sizeof(c0));

@@ -111,6 +111,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+// Contiguous global -> shared bulk copy (no tensor map); both addresses 16-byte
+// aligned, size a multiple of 16; completion counted in bytes on the mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 // L2 eviction policies for TMA loads: streamed expert weights are read once
 // per tile and should not push reused activations out of L2.
 __device__ __forceinline__ uint64_t policy_evict_first() {

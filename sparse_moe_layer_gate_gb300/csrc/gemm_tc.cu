@@ -36,10 +36,7 @@ constexpr int BK = 64;
 enum Mode { M_GATE = 0, M_UP = 1, M_DOWN = 2 };
 
 struct __align__(128) TcParams {
-  CUtensorMap a0;    // GATE: W_r; UP: W_gate (routed); DOWN: W_down (routed)
-  CUtensorMap a1;    // UP: W_up (routed)
-  CUtensorMap a0s;   // UP: W_gate (shared); DOWN: W_down (shared)
-  CUtensorMap a1s;   // UP: W_up (shared)
+  CUtensorMap a0;    // GATE: W_r (UP and DOWN stream packed weight tiles instead)
   CUtensorMap b[4];  // GATE: b[0] = x; UP: Xp; DOWN: A (routed) -- boxes of 32/64/128/256 rows
   CUtensorMap bs;    // UP: x; DOWN: A (shared) -- box of TN rows
   Dims d;
@@ -66,6 +63,8 @@ struct Cfg {
 };
 
 struct Tile {
+  const uint8_t *a_src;   // UP/DOWN: first packed weight tile of the (group, m) row block
+  int a_stride;           // bytes between consecutive K blocks of packed weights
   const CUtensorMap *mb;  // B-operand map (box chosen for the tile)
   int a_row, b_row;       // rows in the A (weights) and B (tokens) tensor maps
   int shared;             // group is a shared expert (selects the *s maps)
@@ -123,6 +122,10 @@ __device__ __forceinline__ Tile decode(const TcParams &p, int tile) {
   t.m_limit = BM;
   t.k0 = 0;
   if (MODE == M_UP) {
+    const int nkb = d.H / BK;
+    const size_t rb = t.shared ? static_cast<size_t>(s) * (d.I_s / BM) + m : static_cast<size_t>(g) * (d.I / BM) + m;
+    t.a_src = (t.shared ? ws.pk_sgu : ws.pk_gu) + rb * nkb * (2 * kTileBytes);
+    t.a_stride = 2 * kTileBytes;
     t.a_row = t.shared ? s * d.I_s + m * BM : g * d.I + m * BM;
     t.b_row = r0;
     t.out_row0 = t.shared ? s * d.Nmax + r0 : r0;
@@ -131,6 +134,10 @@ __device__ __forceinline__ Tile decode(const TcParams &p, int tile) {
     t.out = t.shared ? ws.a_sh : ws.a_int;
     t.out_rows = t.shared ? d.n_sh * d.Nmax : d.Nmax * d.k;
   } else {
+    const int nkb = (t.shared ? d.I_s : d.I) / BK;
+    const size_t rb = t.shared ? static_cast<size_t>(s) * (d.H / BM) + m : static_cast<size_t>(g) * (d.H / BM) + m;
+    t.a_src = (t.shared ? ws.pk_sd : ws.pk_d) + rb * nkb * kTileBytes;
+    t.a_stride = kTileBytes;
     t.a_row = t.shared ? s * d.H + m * BM : g * d.H + m * BM;
     t.b_row = t.shared ? s * d.Nmax + r0 : r0;
     t.out_row0 = t.b_row;
@@ -201,7 +208,7 @@ __global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcPa
   if (wid == 0) {
     if (lane == 0) {
       // ---------------- TMA producer
-      tma_prefetch_desc(&p.a0);
+      if (MODE == M_GATE) tma_prefetch_desc(&p.a0);
       tma_prefetch_desc(&p.b[0]);
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_b = policy_evict_last();
@@ -210,8 +217,7 @@ __global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcPa
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         const Tile t = decode<MODE, TN>(p, tile);
-        const CUtensorMap *ma0 = t.shared ? &p.a0s : &p.a0;
-        const CUtensorMap *ma1 = t.shared ? &p.a1s : &p.a1;
+        const CUtensorMap *ma0 = &p.a0;
         const CUtensorMap *mb = t.mb;
         const uint32_t tx = C::NA * C::A_BYTES + t.b_bytes;
         for (int kb = 0; kb < t.nk; ++kb) {
@@ -222,8 +228,13 @@ __global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcPa
           mbar_arrive_expect_tx(full_bar(stage), tx);
           const int kc = t.k0 + kb * BK;
           const uint32_t a_dst = sA + stage * C::NA * C::A_BYTES;
-          tma_load_2d(a_dst, ma0, kc, t.a_row, full_bar(stage), pol_w);
-          if (C::NA == 2) tma_load_2d(a_dst + C::A_BYTES, ma1, kc, t.a_row, full_bar(stage), pol_w);
+          if (MODE == M_GATE) {
+            tma_load_2d(a_dst, ma0, kc, t.a_row, full_bar(stage), pol_w);
+          } else {
+            // packed weights: the stage's A tiles are one contiguous run
+            bulk_load(a_dst, t.a_src + static_cast<size_t>(kb) * t.a_stride, C::NA * C::A_BYTES, full_bar(stage),
+                      pol_w);
+          }
           tma_load_2d(sB + stage * C::B_BYTES, mb, kc, t.b_row, full_bar(stage), pol_b);
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
@@ -334,6 +345,40 @@ __global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcPa
   }
 }
 
+// ---------------------------------------------------------------- weight packing
+// One 16-byte chunk per thread: output tile t = rb * (k / 64) + kb holds rows
+// [128 rb, 128 rb + 128) x columns [64 kb, 64 kb + 64); row r of the tile sits
+// at byte 128 r and its 16-byte chunk c at position c ^ (r % 8) (the 128-byte
+// swizzle a TMA load with SWIZZLE_128B would produce in shared memory).
+__global__ void k_pack_tiles(const uint4 *__restrict__ src, int64_t rows, int64_t k, uint8_t *__restrict__ dst,
+                             int64_t tile_stride, int64_t tile_off) {
+  const int64_t nkb = k / BK;
+  const int64_t chunks = rows * k / 8;
+  for (int64_t q = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; q < chunks;
+       q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = q >> 10;
+    const int w = static_cast<int>(q & 1023);
+    const int r = w >> 3, pchunk = w & 7;
+    const int c8 = pchunk ^ (r & 7);
+    const int64_t rb = t / nkb, kb = t % nkb;
+    const int64_t row = rb * BM + r;
+    const int64_t col = kb * BK + c8 * 8;
+    const uint4 v = src[(row * k + col) >> 3];
+    *reinterpret_cast<uint4 *>(dst + t * tile_stride + tile_off + static_cast<int64_t>(w) * 16) = v;
+  }
+}
+
+cudaError_t launch_pack_tiles(const void *src, int64_t rows, int64_t k, uint8_t *dst, int64_t tile_stride,
+                              int64_t tile_off, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  const int64_t chunks = rows * k / 8;
+  int64_t blocks = (chunks + 255) / 256;
+  if (blocks > 16 * num_sms()) blocks = 16 * num_sms();
+  k_pack_tiles<<<static_cast<int>(blocks), 256, 0, s>>>(static_cast<const uint4 *>(src), rows, k, dst, tile_stride,
+                                                        tile_off);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- host side
 
 static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -416,10 +461,6 @@ cudaError_t launch_up_tc(const Dims &d, const Maps &m, const Work &ws, const CUt
                          cudaStream_t s) {
   TcParams p;
   base_params(p, d, ws);
-  p.a0 = m.w_gate;
-  p.a1 = m.w_up;
-  p.a0s = m.ws_gate;
-  p.a1s = m.ws_up;
   for (int i = 0; i < 4; ++i) p.b[i] = m.xp[i];
   p.bs = x_map256;
   return launch_tc<M_UP, kTnUp, kStUp>(p, num_sms(), s);
@@ -428,8 +469,6 @@ cudaError_t launch_up_tc(const Dims &d, const Maps &m, const Work &ws, const CUt
 cudaError_t launch_down_tc(const Dims &d, const Maps &m, const Work &ws, cudaStream_t s) {
   TcParams p;
   base_params(p, d, ws);
-  p.a0 = m.w_down;
-  p.a0s = m.ws_down;
   for (int i = 0; i < 4; ++i) p.b[i] = m.a_int[i];
   p.bs = m.a_sh;
   return launch_tc<M_DOWN, kTnDn, kStDn>(p, num_sms(), s);

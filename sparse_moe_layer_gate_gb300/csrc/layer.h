@@ -50,10 +50,19 @@ struct Work {
   void *a_sh;             // [n_sh*Nmax][I_s] SwiGLU activations of shared experts
   float *o_int;           // [Nmax*k][H] routed expert outputs
   float *o_sh;            // [n_sh*Nmax][H] shared expert outputs
+  // expert weights of bf16 layers, packed once at creation into 16 KB tiles of
+  // 128 rows x 64 columns in the 128-byte-swizzled K-major layout the tensor
+  // cores read, tile (row block rb, K block kb) at index rb * (K / 64) + kb:
+  uint8_t *pk_gu;         // routed W_gate/W_up: [E*I/128][H/64] x (gate tile, up tile) = 32 KB
+  uint8_t *pk_d;          // routed W_down: [E*H/128][I/64] x 16 KB
+  uint8_t *pk_sgu;        // shared W_gate/W_up: [n_sh*I_s/128][H/64] x 32 KB
+  uint8_t *pk_sd;         // shared W_down: [n_sh*H/128][I_s/64] x 16 KB
   Ctrl *ctrl;
   epoch_iter_stats *stats;
   uint32_t *err;
 };
+
+constexpr int kTileBytes = 128 * 64 * 2;  // one packed 128 x 64 bf16 tile
 
 // Shapes and per-call values handed to every kernel by value.
 struct Dims {
@@ -79,12 +88,6 @@ struct Weights {
 // TMA descriptors that stay valid for the layer's lifetime.
 struct Maps {
   CUtensorMap w_router;   // [E][H], box 64 x 128
-  CUtensorMap w_gate;     // [E*I][H]
-  CUtensorMap w_up;       // [E*I][H]
-  CUtensorMap w_down;     // [E*H][I]
-  CUtensorMap ws_gate;    // [n_sh*I_s][H]
-  CUtensorMap ws_up;
-  CUtensorMap ws_down;    // [n_sh*H][I_s]
   CUtensorMap xp[4];      // [Nmax*k][H], boxes 64 x {32, 64, 128, 256}
   CUtensorMap a_int[4];   // [Nmax*k][I], boxes 64 x {32, 64, 128, 256}
   CUtensorMap a_sh;       // [n_sh*Nmax][I_s], box 64 x 256
@@ -121,6 +124,9 @@ cudaError_t launch_up_simt(const Dims &d, const Weights &w, const Work &ws, cons
 cudaError_t launch_down_simt(const Dims &d, const Weights &w, const Work &ws, cudaStream_t s);
 
 // gemm_tc.cu (bf16 layers, tcgen05 + TMA)
+// Packs row-major [rows][k] bf16 into swizzled tiles at dst + t * tile_stride + tile_off.
+cudaError_t launch_pack_tiles(const void *src, int64_t rows, int64_t k, uint8_t *dst, int64_t tile_stride,
+                              int64_t tile_off, cudaStream_t s);
 bool tma_encode_init();
 bool encode_kmajor_bf16(CUtensorMap *map, const void *base, uint64_t k_elems, uint64_t rows, uint32_t box_rows);
 int tc_gate_splits(const Dims &d);
