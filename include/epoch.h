@@ -148,6 +148,15 @@ typedef struct {
   const void *cache;           /* [max_positions][H] routed-output cache, layer dtype */
   const epoch_iter_stats *stats;
   const uint32_t *error_word;
+  /* [3][1024][8] int64 per-CTA timelines of the last gate (0), expert-up (1)
+   * and expert-down (2) launches while tracing is on: globaltimer ns at entry,
+   * setup done, first operand stage landed, last MMA committed, epilogue done;
+   * tiles processed, valid token columns, SM id. */
+  const int64_t *trace;
+  /* [2][EPOCH_PROF_KINDS] while tracing: first CTA entry and last CTA exit
+   * (globaltimer ns) of each kernel kind in the last iteration, in the order
+   * of epoch_profile.name. */
+  const int64_t *timeline;
 } epoch_debug_view;
 
 /* Per-kernel timing, accumulated while profiling is on. */
@@ -223,6 +232,9 @@ epoch_status epoch_path_counters(epoch_layer *layer, int64_t *cold, int64_t *hot
 /* Bounded device waits: a wait that makes no progress for timeout_ns gives up,
  * sets EPOCH_DEVERR_TIMEOUT and lets the kernel return (default 2e9 ns). */
 epoch_status epoch_set_wait_timeout(epoch_layer *layer, int64_t timeout_ns);
+
+/* Per-CTA timeline recording in the tcgen05 kernels (see epoch_debug_view.trace). */
+epoch_status epoch_set_tracing(epoch_layer *layer, int32_t enable);
 
 /* Per-kernel CUDA-event timing on the launching stream (adds an event pair per launch). */
 epoch_status epoch_set_profiling(epoch_layer *layer, int32_t enable);

@@ -48,7 +48,8 @@ class epoch_debug_view(C.Structure):
                 ("logit_parts", C.c_void_p), ("n_logit_parts", C.c_int32), ("fresh_pos", C.c_void_p),
                 ("sel", C.c_void_p), ("sel_w", C.c_void_p), ("offsets", C.c_void_p),
                 ("wl_pos", C.c_void_p), ("slot", C.c_void_p), ("stamp", C.c_void_p),
-                ("cache", C.c_void_p), ("stats", C.c_void_p), ("error_word", C.c_void_p)]
+                ("cache", C.c_void_p), ("stats", C.c_void_p), ("error_word", C.c_void_p),
+                ("trace", C.c_void_p), ("timeline", C.c_void_p)]
 
 
 class epoch_profile(C.Structure):
@@ -74,6 +75,7 @@ _SIGS = {
     "epoch_path_counters": (C.c_int, [C.c_void_p, C.POINTER(C.c_int64), C.POINTER(C.c_int64),
                                       C.POINTER(C.c_int64)]),
     "epoch_set_wait_timeout": (C.c_int, [C.c_void_p, C.c_int64]),
+    "epoch_set_tracing": (C.c_int, [C.c_void_p, C.c_int32]),
     "epoch_set_profiling": (C.c_int, [C.c_void_p, C.c_int32]),
     "epoch_read_profile": (C.c_int, [C.c_void_p, C.POINTER(epoch_profile)]),
     "epoch_reset_profile": (C.c_int, [C.c_void_p]),

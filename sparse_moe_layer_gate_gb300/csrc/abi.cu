@@ -132,6 +132,8 @@ size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   } else {
     t.pk_gu = t.pk_d = t.pk_sgu = t.pk_sd = nullptr;
   }
+  t.trace = static_cast<int64_t *>(take(3ull * kTraceCtas * kTraceFields * 8));
+  t.timeline = static_cast<unsigned long long *>(take(2ull * K_NUM * 8));
   t.ctrl = static_cast<Ctrl *>(take(sizeof(Ctrl)));
   t.stats = static_cast<epoch_iter_stats *>(take(sizeof(epoch_iter_stats)));
   t.err = static_cast<uint32_t *>(take(16));
@@ -335,6 +337,11 @@ epoch_status epoch_moe_iter(epoch_layer *L, const void *x, const uint8_t *live, 
   cudaStream_t s = S(stream);
   const int host_fallback = !L->planned || iteration != L->last_iter + 1 || n_pos != L->n_pos_plan;
   Dims d = call_dims(L, n_pos, iteration, host_fallback);
+  if (d.trace) {
+    if (cudaMemsetAsync(L->ws.timeline, 0xFF, K_NUM * 8, s) != cudaSuccess ||
+        cudaMemsetAsync(L->ws.timeline + K_NUM, 0, K_NUM * 8, s) != cudaSuccess)
+      return EPOCH_ECUDA;
+  }
   CUtensorMap x_maps[2];
   EPOCH_TRY(run_gate(L, d, x, x_maps, s));
   EPOCH_TRY(run(L, K_CLASSIFY, s, [&] { return launch_classify(d, L->ws, live, decoded, s); }));
@@ -400,6 +407,8 @@ epoch_status epoch_debug_pointers(epoch_layer *L, epoch_debug_view *v) {
   v->slot = L->ws.slot;
   v->stamp = L->ws.stamp;
   v->cache = L->ws.cache;
+  v->trace = L->ws.trace;
+  v->timeline = reinterpret_cast<const int64_t *>(L->ws.timeline);
   v->stats = L->ws.stats;
   v->error_word = L->ws.err;
   return EPOCH_OK;
@@ -425,6 +434,12 @@ epoch_status epoch_path_counters(epoch_layer *L, int64_t *cold, int64_t *hot, in
 epoch_status epoch_set_wait_timeout(epoch_layer *L, int64_t timeout_ns) {
   if (L == nullptr || timeout_ns < 1000) return EPOCH_EINVAL;
   L->dims.timeout_ns = timeout_ns;
+  return EPOCH_OK;
+}
+
+epoch_status epoch_set_tracing(epoch_layer *L, int32_t enable) {
+  if (L == nullptr) return EPOCH_EINVAL;
+  L->dims.trace = enable ? 1 : 0;
   return EPOCH_OK;
 }
 

@@ -111,6 +111,8 @@ __global__ void __launch_bounds__(256) k_down_simt(Dims d, Weights w, Work ws) {
 
 cudaError_t launch_up_simt(const Dims &d, const Weights &w, const Work &ws, const void *x, cudaStream_t s) {
   const int blocks = 2 * num_sms();
+  static bool carve_ = (prefer_max_shared(k_up_simt) == cudaSuccess);
+  (void)carve_;
   k_up_simt<<<blocks, 256, d.H * sizeof(float), s>>>(d, w, ws, static_cast<const float *>(x));
   return cudaGetLastError();
 }
@@ -118,6 +120,8 @@ cudaError_t launch_up_simt(const Dims &d, const Weights &w, const Work &ws, cons
 cudaError_t launch_down_simt(const Dims &d, const Weights &w, const Work &ws, cudaStream_t s) {
   const int blocks = 2 * num_sms();
   const int inter = d.I > d.I_s ? d.I : d.I_s;
+  static bool carve_ = (prefer_max_shared(k_down_simt) == cudaSuccess);
+  (void)carve_;
   k_down_simt<<<blocks, 256, inter * sizeof(float), s>>>(d, w, ws);
   return cudaGetLastError();
 }

@@ -56,7 +56,10 @@ struct Cfg {
   static constexpr int TMEM_COLS = USED_COLS <= 32 ? 32 : USED_COLS <= 64 ? 64 : USED_COLS <= 128 ? 128
                                    : USED_COLS <= 256 ? 256 : 512;
   static constexpr int NBARS = 2 * STAGES + 2 * NBUF + 1;
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + NBARS * 8 + 16;
+  // epilogue staging: per epilogue warp, 32 token columns x 32 rows, padded rows
+  static constexpr int STG_ROW = MODE == M_UP ? 80 : 144;  // bytes per staged column (64 / 128 B + pad)
+  static constexpr int STG_BYTES = 32 * STG_ROW;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 4 * STG_BYTES + NBARS * 8 + 16;
   static_assert(TN % 16 == 0 && TN >= 16 && TN <= 256, "MMA N");
   static_assert(USED_COLS <= 512, "TMEM");
   static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -166,7 +169,8 @@ __global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcPa
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sA = sbase;                                   // [STAGES][NA] A tiles
   const uint32_t sB = sbase + STAGES * C::NA * C::A_BYTES;     // [STAGES] B tiles
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * C::STAGE_BYTES);
+  uint8_t *stage_out = smem + STAGES * C::STAGE_BYTES;  // [4][STG_BYTES] epilogue transposes
+  uint64_t *bars = reinterpret_cast<uint64_t *>(stage_out + 4 * C::STG_BYTES);
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
@@ -178,10 +182,20 @@ __global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcPa
 
   const Dims &d = p.d;
   const Work &ws = p.ws;
+  const KernelMark mark_(d, ws, MODE == M_GATE ? K_GATE : MODE == M_UP ? K_UP : K_DOWN);
   const int total = MODE == M_GATE ? p.gate_tiles : (MODE == M_UP ? ws.ctrl->tiles_up : ws.ctrl->tiles_dn);
   if (static_cast<int>(blockIdx.x) >= total) return;
   const int wid = warp_id(), lane = lane_id();
   const uint64_t tmo = static_cast<uint64_t>(d.timeout_ns);
+  int64_t *trace = (d.trace && blockIdx.x < kTraceCtas)
+                       ? ws.trace + (static_cast<size_t>(MODE) * kTraceCtas + blockIdx.x) * kTraceFields
+                       : nullptr;
+  if (trace && threadIdx.x == 0) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    trace[0] = static_cast<int64_t>(globaltimer_ns());
+    trace[7] = smid;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -204,6 +218,7 @@ __global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcPa
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (trace && threadIdx.x == 0) trace[1] = static_cast<int64_t>(globaltimer_ns());
 
   if (wid == 0) {
     if (lane == 0) {
@@ -249,15 +264,19 @@ __global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcPa
           if (armed & (1u << s)) mbar_drain(full_bar(s), (armed_par >> s) & 1u, 50000000ull);
       }
     }
+    __syncwarp();  // the whole warp reaches the final barrier (and the dealloc) together
   } else if (wid == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
       int stage = 0, buf = 0;
       uint32_t phase = 0, bphase = 0;
-      bool ok = true;
+      bool ok = true, first = true;
+      int64_t n_tiles = 0, n_cols = 0;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         const Tile t = decode<MODE, TN>(p, tile);
         const int n_mma = ((t.n_valid + 15) / 16) * 16;
+        ++n_tiles;
+        n_cols += t.n_valid;
         const uint32_t idesc = idesc_bf16_f32(BM, n_mma);
         if (!mbar_wait_bounded(tempty_bar(buf), bphase ^ 1u, abort_flag, ws.err, tmo)) break;
         tc_fence_after();
@@ -268,6 +287,10 @@ __global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcPa
             break;
           }
           tc_fence_after();
+          if (trace && first) {
+            trace[2] = static_cast<int64_t>(globaltimer_ns());
+            first = false;
+          }
           const uint32_t a_src = sA + stage * C::NA * C::A_BYTES;
           const uint64_t ad0 = sw128_kmajor_desc(a_src);
           const uint64_t ad1 = sw128_kmajor_desc(a_src + C::A_BYTES);
@@ -293,11 +316,20 @@ __global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcPa
       }
       tc_commit(done_bar);
       mbar_drain(done_bar, 0, 50000000ull);
+      if (trace) {
+        trace[3] = static_cast<int64_t>(globaltimer_ns());
+        trace[5] = n_tiles;
+        trace[6] = n_cols;
+      }
     }
+    __syncwarp();
   } else {
     // ---------------- epilogue (warps 2..5; warp w reads TMEM lanes 32*(w%4)..)
+    // Per 32 token columns: two 32-column TMEM loads and one wait, the values
+    // of this warp's 32 rows staged column-major in shared memory, then lane c
+    // writes token column c's 32 contiguous outputs with 16-byte stores.
     const int q = wid & 3;
-    const int row = q * 32 + lane;
+    uint8_t *stg = stage_out + (wid - 2) * C::STG_BYTES;
     int buf = 0;
     uint32_t bphase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -305,29 +337,46 @@ __global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcPa
       if (!mbar_wait_bounded(tfull_bar(buf), bphase, abort_flag, ws.err, tmo)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * C::ACC_COLS);
-      for (int c0 = 0; c0 < t.n_valid; c0 += 16) {
-        float v0[16], v1[16];
-        tmem_ld16(tb + c0, v0);
-        if (C::NA == 2) tmem_ld16(tb + TN + c0, v1);
+      const int rows_valid = min(32, max(0, t.m_limit - q * 32));
+      const int esz = MODE == M_UP ? 2 : 4;
+      const bool vec_ok = rows_valid == 32 && ((t.ld * esz) & 15) == 0;
+      for (int c0 = 0; c0 < t.n_valid; c0 += 32) {
+        float v0[32], v1[32];
+        tmem_ld32(tb + c0, v0);
+        if (C::NA == 2) tmem_ld32(tb + TN + c0, v1);
         tmem_ld_wait();
-        if (row < t.m_limit) {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int orow = t.out_row0 + c0 + c;
-            if (c0 + c < t.n_valid) {
-              if (orow < 0 || orow >= t.out_rows) {
-                set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-                continue;
-              }
-              const size_t o = static_cast<size_t>(orow) * t.ld + t.col0 + row;
-              if (MODE == M_UP) {
-                static_cast<__nv_bfloat16 *>(t.out)[o] = __float2bfloat16_rn(silu(v0[c]) * v1[c]);
-              } else {
-                static_cast<float *>(t.out)[o] = v0[c];
-              }
+        for (int c = 0; c < 32; ++c) {
+          if (MODE == M_UP) {
+            reinterpret_cast<__nv_bfloat16 *>(stg + c * C::STG_ROW)[lane] =
+                __float2bfloat16_rn(silu_fast(v0[c]) * v1[c]);
+          } else {
+            reinterpret_cast<float *>(stg + c * C::STG_ROW)[lane] = v0[c];
+          }
+        }
+        __syncwarp();
+        const int col = c0 + lane;  // token column written by this lane
+        const int orow = t.out_row0 + col;
+        if (col < t.n_valid) {
+          if (orow < 0 || orow >= t.out_rows) {
+            set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+          } else if (vec_ok) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(stg + lane * C::STG_ROW);
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(t.out) +
+                                                   (static_cast<size_t>(orow) * t.ld + t.col0 + q * 32) * esz);
+#pragma unroll
+            for (int v = 0; v < 32 * esz / 16; ++v) dst[v] = src[v];
+          } else {
+            for (int r = 0; r < rows_valid; ++r) {
+              const size_t o = static_cast<size_t>(orow) * t.ld + t.col0 + q * 32 + r;
+              if (MODE == M_UP)
+                static_cast<__nv_bfloat16 *>(t.out)[o] = reinterpret_cast<const __nv_bfloat16 *>(stg + lane * C::STG_ROW)[r];
+              else
+                static_cast<float *>(t.out)[o] = reinterpret_cast<const float *>(stg + lane * C::STG_ROW)[r];
             }
           }
         }
+        __syncwarp();
       }
       tc_fence_before();
       mbar_arrive(tempty_bar(buf));
@@ -336,6 +385,7 @@ __global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcPa
         bphase ^= 1u;
       }
     }
+    if (trace && wid == 2 && lane == 0) trace[4] = static_cast<int64_t>(globaltimer_ns());
   }
   tc_fence_before();
   __syncthreads();
@@ -374,6 +424,8 @@ cudaError_t launch_pack_tiles(const void *src, int64_t rows, int64_t k, uint8_t 
   const int64_t chunks = rows * k / 8;
   int64_t blocks = (chunks + 255) / 256;
   if (blocks > 16 * num_sms()) blocks = 16 * num_sms();
+  static bool carve_ = (prefer_max_shared(k_pack_tiles) == cudaSuccess);
+  (void)carve_;
   k_pack_tiles<<<static_cast<int>(blocks), 256, 0, s>>>(static_cast<const uint4 *>(src), rows, k, dst, tile_stride,
                                                         tile_off);
   return cudaGetLastError();
@@ -430,8 +482,9 @@ static cudaError_t launch_tc(const TcParams &p, int grid, cudaStream_t s) {
   using C = Cfg<MODE, TN, STAGES>;
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e =
+    cudaError_t e =
         cudaFuncSetAttribute(k_tc_gemm<MODE, TN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e == cudaSuccess) e = prefer_max_shared(k_tc_gemm<MODE, TN, STAGES>);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }

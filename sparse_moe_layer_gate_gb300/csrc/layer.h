@@ -57,10 +57,18 @@ struct Work {
   uint8_t *pk_d;          // routed W_down: [E*H/128][I/64] x 16 KB
   uint8_t *pk_sgu;        // shared W_gate/W_up: [n_sh*I_s/128][H/64] x 32 KB
   uint8_t *pk_sd;         // shared W_down: [n_sh*H/128][I_s/64] x 16 KB
+  int64_t *trace;         // [3 kernels][kTraceCtas][8] per-CTA timeline (when tracing)
+  unsigned long long *timeline;  // [2][K_NUM]: first CTA entry, last CTA exit per kernel kind (ns)
   Ctrl *ctrl;
   epoch_iter_stats *stats;
   uint32_t *err;
 };
+
+// Per-CTA trace record of a tcgen05 kernel (globaltimer ns): entry, setup done,
+// first operand stage landed, last MMA committed, epilogue done, tiles, valid
+// token columns, SM id.
+constexpr int kTraceCtas = 1024;
+constexpr int kTraceFields = 8;
 
 constexpr int kTileBytes = 128 * 64 * 2;  // one packed 128 x 64 bf16 tile
 
@@ -75,6 +83,7 @@ struct Dims {
   int32_t tn_up, tn_dn;  // token-tile width of the tcgen05 grouped GEMMs (0 on the SIMT path)
   int32_t cmax;          // chunk capacity: ceil(Nmax / 32)
   int32_t max_tiles_up, max_tiles_dn;
+  int32_t trace;         // nonzero: tcgen05 kernels record per-CTA timelines
   int64_t timeout_ns;
 };
 
@@ -103,6 +112,30 @@ enum Kind {
   K_UP, K_DOWN, K_COMBINE, K_TEST, K_MEMSET, K_NUM
 };
 extern const char *const kKindName[K_NUM];
+
+#ifdef __CUDACC__
+// Records, while tracing, the earliest CTA entry and the latest CTA exit of a
+// kernel kind in the workspace timeline (globaltimer ns); a no-op otherwise.
+struct KernelMark {
+  unsigned long long *tl;
+  int kind;
+  __device__ __forceinline__ KernelMark(const Dims &d, const Work &ws, int k)
+      : tl(d.trace && threadIdx.x == 0 ? ws.timeline : nullptr), kind(k) {
+    if (tl) {
+      unsigned long long t;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t)::"memory");
+      atomicMin(tl + kind, t);
+    }
+  }
+  __device__ __forceinline__ ~KernelMark() {
+    if (tl) {
+      unsigned long long t;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t)::"memory");
+      atomicMax(tl + K_NUM + kind, t);
+    }
+  }
+};
+#endif
 
 // ------------------------------------------------------------ launchers
 // route.cu

@@ -197,6 +197,7 @@ __global__ void k_plan_topk(Dims d, const float *__restrict__ gparts, const floa
 // counts reach `threshold` (at least k; every expert when all_experts), and
 // clear the block's stamps and previous-decoded flags (cold path).
 __global__ void __launch_bounds__(1024) k_plan_support(Dims d, Work ws, int32_t threshold, int all_experts) {
+  const KernelMark mark_(d, ws, K_PLAN_SUPPORT);
   __shared__ int32_t cnt[1024];
   __shared__ int32_t sorted_cnt[1024];
   __shared__ int32_t len_s;
@@ -254,6 +255,7 @@ __global__ void __launch_bounds__(1024) k_plan_support(Dims d, Work ws, int32_t 
 // [j*c, (j+1)*c), so a block-wide exclusive scan keeps the fresh list ascending.
 __global__ void __launch_bounds__(1024) k_classify(Dims d, Work ws, const uint8_t *__restrict__ live,
                                                    const uint8_t *__restrict__ decoded) {
+  const KernelMark mark_(d, ws, K_CLASSIFY);
   constexpr int kThreads = 1024;
   __shared__ int32_t warp_sum[32];
   __shared__ int32_t cat[8];
@@ -378,6 +380,7 @@ __global__ void __launch_bounds__(1024) k_classify(Dims d, Work ws, const uint8_
 // no sort ("count exchange" of [W] section "FreshLane Dispatch", on chip).
 template <int EPL>
 __global__ void __launch_bounds__(1024) k_route(Dims d, Work ws, const float *__restrict__ bias) {
+  const KernelMark mark_(d, ws, K_ROUTE);
   __shared__ uint32_t mask[1024];
   const int chunk = blockIdx.x;
   const int n_fresh = ws.ctrl->n_fresh;
@@ -433,6 +436,7 @@ __global__ void __launch_bounds__(1024) k_route(Dims d, Work ws, const float *__
 // no tile, so their weights are never read ([W] section "FreshLane Dispatch":
 // invalid slots load no expert weights).
 __global__ void __launch_bounds__(1024) k_worklist(Dims d, Work ws) {
+  const KernelMark mark_(d, ws, K_WORKLIST);
   __shared__ int32_t tmp[33];
   __shared__ int32_t wsum[32];
   const int E = d.E, k = d.k;
@@ -538,6 +542,7 @@ __global__ void __launch_bounds__(1024) k_worklist(Dims d, Work ws) {
 // ---------------------------------------------------------------- permute
 // Xp[l] = x[wl_pos[l]]: one warp per worklist row, 16-byte vectors.
 __global__ void k_permute(Dims d, Work ws, const uint4 *__restrict__ x, int vec_per_row) {
+  const KernelMark mark_(d, ws, K_PERMUTE);
   const int n = ws.ctrl->n_edges;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   uint4 *xp = reinterpret_cast<uint4 *>(ws.xp);
@@ -588,6 +593,7 @@ __device__ __forceinline__ void store8(__nv_bfloat16 *p, const float (&v)[8]) {
 // residual), rounded once: the dense shard is restored at the layer boundary.
 template <typename T>
 __global__ void __launch_bounds__(128) k_combine(Dims d, Work ws, const T *__restrict__ x, T *__restrict__ y) {
+  const KernelMark mark_(d, ws, K_COMBINE);
   const int t = blockIdx.x;
   if (t >= d.n_pos) return;
   const int f = ws.fidx[t];
@@ -678,20 +684,30 @@ cudaError_t launch_gate_simt(const Dims &d, const Weights &w, const Work &ws, co
   const int outputs = d.n_pos * d.E;
   int blocks = (outputs + 7) / 8;
   if (blocks > 8 * num_sms()) blocks = 8 * num_sms();
-  if (bf16)
+  if (bf16) {
+    static bool carve_ = (prefer_max_shared(k_gate_simt<__nv_bfloat16>) == cudaSuccess);
+    (void)carve_;
     k_gate_simt<__nv_bfloat16><<<blocks, 256, 0, s>>>(d, static_cast<const __nv_bfloat16 *>(x),
                                                       static_cast<const __nv_bfloat16 *>(w.w_router), ws.gparts);
-  else
+  } else {
+    static bool carve_ = (prefer_max_shared(k_gate_simt<float>) == cudaSuccess);
+    (void)carve_;
     k_gate_simt<float><<<blocks, 256, 0, s>>>(d, static_cast<const float *>(x),
                                               static_cast<const float *>(w.w_router), ws.gparts);
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_plan_topk(const Dims &d, const Weights &w, const Work &ws, cudaStream_t s) {
   int blocks = (d.n_pos + 7) / 8;
   switch (epl_for(d.E)) {
-#define EPOCH_CASE(N) \
-  case N: k_plan_topk<N><<<blocks, 256, 0, s>>>(d, ws.gparts, w.b_router, ws.plan_counts); break;
+#define EPOCH_CASE(N)                                                                  \
+  case N: {                                                                            \
+    static bool c_ = (prefer_max_shared(k_plan_topk<N>) == cudaSuccess);               \
+    (void)c_;                                                                          \
+    k_plan_topk<N><<<blocks, 256, 0, s>>>(d, ws.gparts, w.b_router, ws.plan_counts);  \
+    break;                                                                             \
+  }
     EPOCH_CASE(1) EPOCH_CASE(2) EPOCH_CASE(4) EPOCH_CASE(8) EPOCH_CASE(16) EPOCH_CASE(32)
 #undef EPOCH_CASE
   }
@@ -700,12 +716,16 @@ cudaError_t launch_plan_topk(const Dims &d, const Weights &w, const Work &ws, cu
 
 cudaError_t launch_plan_support(const Dims &d, const Work &ws, int32_t threshold, int all_experts,
                                 cudaStream_t s) {
+  static bool carve_ = (prefer_max_shared(k_plan_support) == cudaSuccess);
+  (void)carve_;
   k_plan_support<<<1, 1024, 0, s>>>(d, ws, threshold, all_experts);
   return cudaGetLastError();
 }
 
 cudaError_t launch_classify(const Dims &d, const Work &ws, const uint8_t *live, const uint8_t *decoded,
                             cudaStream_t s) {
+  static bool carve_ = (prefer_max_shared(k_classify) == cudaSuccess);
+  (void)carve_;
   k_classify<<<1, 1024, 0, s>>>(d, ws, live, decoded);
   return cudaGetLastError();
 }
@@ -713,8 +733,13 @@ cudaError_t launch_classify(const Dims &d, const Work &ws, const uint8_t *live, 
 cudaError_t launch_route(const Dims &d, const Weights &w, const Work &ws, cudaStream_t s) {
   const int chunks = (d.Nmax + 31) / 32;
   switch (epl_for(d.E)) {
-#define EPOCH_CASE(N) \
-  case N: k_route<N><<<chunks, 1024, 0, s>>>(d, ws, w.b_router); break;
+#define EPOCH_CASE(N)                                                    \
+  case N: {                                                              \
+    static bool c_ = (prefer_max_shared(k_route<N>) == cudaSuccess);     \
+    (void)c_;                                                            \
+    k_route<N><<<chunks, 1024, 0, s>>>(d, ws, w.b_router);               \
+    break;                                                               \
+  }
     EPOCH_CASE(1) EPOCH_CASE(2) EPOCH_CASE(4) EPOCH_CASE(8) EPOCH_CASE(16) EPOCH_CASE(32)
 #undef EPOCH_CASE
   }
@@ -722,6 +747,8 @@ cudaError_t launch_route(const Dims &d, const Weights &w, const Work &ws, cudaSt
 }
 
 cudaError_t launch_worklist(const Dims &d, const Work &ws, cudaStream_t s) {
+  static bool carve_ = (prefer_max_shared(k_worklist) == cudaSuccess);
+  (void)carve_;
   k_worklist<<<d.E + 1, 1024, 0, s>>>(d, ws);
   return cudaGetLastError();
 }
@@ -730,20 +757,29 @@ cudaError_t launch_permute(const Dims &d, const Work &ws, const void *x, int bf1
   const int vec = d.H * (bf16 ? 2 : 4) / 16;
   int blocks = (d.Nmax * d.k + 7) / 8;
   if (blocks > 4 * num_sms()) blocks = 4 * num_sms();
+  static bool carve_ = (prefer_max_shared(k_permute) == cudaSuccess);
+  (void)carve_;
   k_permute<<<blocks, 256, 0, s>>>(d, ws, static_cast<const uint4 *>(x), vec);
   return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const Dims &d, const Work &ws, const void *x, void *y, int bf16, cudaStream_t s) {
-  if (bf16)
+  if (bf16) {
+    static bool carve_ = (prefer_max_shared(k_combine<__nv_bfloat16>) == cudaSuccess);
+    (void)carve_;
     k_combine<__nv_bfloat16><<<d.n_pos, 128, 0, s>>>(d, ws, static_cast<const __nv_bfloat16 *>(x),
                                                      static_cast<__nv_bfloat16 *>(y));
-  else
+  } else {
+    static bool carve_ = (prefer_max_shared(k_combine<float>) == cudaSuccess);
+    (void)carve_;
     k_combine<float><<<d.n_pos, 128, 0, s>>>(d, ws, static_cast<const float *>(x), static_cast<float *>(y));
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_wait_test(uint32_t *err, int64_t timeout_ns, cudaStream_t s) {
+  static bool carve_ = (prefer_max_shared(k_wait_test) == cudaSuccess);
+  (void)carve_;
   k_wait_test<<<1, 32, 0, s>>>(err, timeout_ns);
   return cudaGetLastError();
 }

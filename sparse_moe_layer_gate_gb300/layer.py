@@ -120,6 +120,24 @@ class EpochLayer:
         B.check(B.lib().epoch_test_wait_timeout(self.handle, int(ns), _stream(stream)),
                 "epoch_test_wait_timeout")
 
+    def set_tracing(self, on: bool) -> None:
+        B.check(B.lib().epoch_set_tracing(self.handle, 1 if on else 0), "epoch_set_tracing")
+
+    def read_trace(self, stream=None) -> np.ndarray:
+        """[3, 1024, 8] int64 per-CTA timelines of the last gate/up/down launches."""
+        v = B.epoch_debug_view()
+        B.check(B.lib().epoch_debug_pointers(self.handle, C.byref(v)), "epoch_debug_pointers")
+        return self._copy(v.trace, 3 * 1024 * 8, np.int64, stream).reshape(3, 1024, 8)
+
+    def read_timeline(self, stream=None) -> dict:
+        """{kernel: (first entry ns, last exit ns)} of the last traced iteration."""
+        v = B.epoch_debug_view()
+        B.check(B.lib().epoch_debug_pointers(self.handle, C.byref(v)), "epoch_debug_pointers")
+        raw = self._copy(v.timeline, 2 * B.EPOCH_PROF_KINDS, np.uint64, stream).reshape(2, -1)
+        names = ["gate", "plan_topk", "plan_support", "classify", "route", "worklist", "permute",
+                 "expert_up", "expert_down", "combine", "wait_test", "memset"]
+        return {n: (int(raw[0, i]), int(raw[1, i])) for i, n in enumerate(names) if raw[1, i] > 0}
+
     def set_profiling(self, on: bool) -> None:
         B.check(B.lib().epoch_set_profiling(self.handle, 1 if on else 0), "epoch_set_profiling")
 
