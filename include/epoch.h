@@ -138,6 +138,7 @@ typedef struct {
   const float *logit_parts;    /* [n_logit_parts][max_positions][E] partial sums of x W_r^T over
                                   disjoint slices of H (no bias); G = their sum + b_router */
   int32_t n_logit_parts;
+  const float *logits;         /* [max_positions][E] G of the last iteration, bias included */
   const int32_t *fresh_pos;    /* [n_fresh] ascending fresh positions */
   const int32_t *sel;          /* [n_fresh][k] selected experts, selection order */
   const float *sel_w;          /* [n_fresh][k] routing weights */
@@ -148,10 +149,11 @@ typedef struct {
   const void *cache;           /* [max_positions][H] routed-output cache, layer dtype */
   const epoch_iter_stats *stats;
   const uint32_t *error_word;
-  /* [3][1024][8] int64 per-CTA timelines of the last gate (0), expert-up (1)
-   * and expert-down (2) launches while tracing is on: globaltimer ns at entry,
-   * setup done, first operand stage landed, last MMA committed, epilogue done;
-   * tiles processed, valid token columns, SM id. */
+  /* [4][1024][8] int64 per-CTA timelines of the last launches while tracing is
+   * on (globaltimer ns). Rows 0-2, gate / expert-up / expert-down: entry,
+   * setup done, first operand stage landed, last MMA committed, epilogue done,
+   * tiles processed, valid token columns, SM id. Row 3, routing: entry, then
+   * the end of the classify, compaction, top-k and worklist phases, kernel end. */
   const int64_t *trace;
   /* [2][EPOCH_PROF_KINDS] while tracing: first CTA entry and last CTA exit
    * (globaltimer ns) of each kernel kind in the last iteration, in the order

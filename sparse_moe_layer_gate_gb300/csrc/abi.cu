@@ -106,6 +106,7 @@ size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   t.plan_counts = static_cast<int32_t *>(take(E * 4));
   t.cache = take(N * H * act);
   t.gparts = static_cast<float *>(take(static_cast<size_t>(sk_max_for(c)) * N * E * 4));
+  t.logits = static_cast<float *>(take(N * E * 4));
   t.fidx = static_cast<int32_t *>(take(N * 4));
   t.fresh_pos = static_cast<int32_t *>(take(N * 4));
   t.sel = static_cast<int32_t *>(take(N * k * 4));
@@ -132,7 +133,9 @@ size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   } else {
     t.pk_gu = t.pk_d = t.pk_sgu = t.pk_sd = nullptr;
   }
-  t.trace = static_cast<int64_t *>(take(3ull * kTraceCtas * kTraceFields * 8));
+  t.blk = static_cast<int32_t *>(take(static_cast<size_t>(kMaxRoutingGrid) * kBlkFields * 4));
+  t.gbar = static_cast<unsigned int *>(take(16));
+  t.trace = static_cast<int64_t *>(take(4ull * kTraceCtas * kTraceFields * 8));
   t.timeline = static_cast<unsigned long long *>(take(2ull * K_NUM * 8));
   t.ctrl = static_cast<Ctrl *>(take(sizeof(Ctrl)));
   t.stats = static_cast<epoch_iter_stats *>(take(sizeof(epoch_iter_stats)));
@@ -344,10 +347,7 @@ epoch_status epoch_moe_iter(epoch_layer *L, const void *x, const uint8_t *live, 
   }
   CUtensorMap x_maps[2];
   EPOCH_TRY(run_gate(L, d, x, x_maps, s));
-  EPOCH_TRY(run(L, K_CLASSIFY, s, [&] { return launch_classify(d, L->ws, live, decoded, s); }));
-  EPOCH_TRY(run(L, K_ROUTE, s, [&] { return launch_route(d, L->w, L->ws, s); }));
-  EPOCH_TRY(run(L, K_WORKLIST, s, [&] { return launch_worklist(d, L->ws, s); }));
-  EPOCH_TRY(run(L, K_PERMUTE, s, [&] { return launch_permute(d, L->ws, x, L->bf16, s); }));
+  EPOCH_TRY(run(L, K_ROUTING, s, [&] { return launch_routing(d, L->w, L->ws, live, decoded, x, L->bf16, s); }));
   if (L->bf16) {
     EPOCH_TRY(run(L, K_UP, s, [&] { return launch_up_tc(d, L->maps, L->ws, x_maps[1], s); }));
     EPOCH_TRY(run(L, K_DOWN, s, [&] { return launch_down_tc(d, L->maps, L->ws, s); }));
@@ -398,6 +398,7 @@ epoch_status epoch_debug_pointers(epoch_layer *L, epoch_debug_view *v) {
   v->support_len = &L->ws.ctrl->support_len;
   v->plan_counts = L->ws.plan_counts;
   v->logit_parts = L->ws.gparts;
+  v->logits = L->ws.logits;
   v->n_logit_parts = L->last_sk;
   v->fresh_pos = L->ws.fresh_pos;
   v->sel = L->ws.sel;

@@ -183,6 +183,7 @@ __global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcPa
   const Dims &d = p.d;
   const Work &ws = p.ws;
   const KernelMark mark_(d, ws, MODE == M_GATE ? K_GATE : MODE == M_UP ? K_UP : K_DOWN);
+  if (MODE == M_GATE && blockIdx.x == 0 && threadIdx.x == 0) *ws.gbar = 0u;  // next routing launch
   const int total = MODE == M_GATE ? p.gate_tiles : (MODE == M_UP ? ws.ctrl->tiles_up : ws.ctrl->tiles_dn);
   if (static_cast<int>(blockIdx.x) >= total) return;
   const int wid = warp_id(), lane = lane_id();

@@ -34,6 +34,7 @@ struct Work {
   void *cache;            // [Nmax][H] routed-output cache, layer dtype
   // one iteration
   float *gparts;          // [SK][Nmax][E] split-K partial logits (no bias)
+  float *logits;          // [Nmax][E] G = sum of the partials + bias (routing kernel, phase A)
   int32_t *fidx;          // [Nmax] fresh index of a position, -1 if reused
   int32_t *fresh_pos;     // [Nmax] ascending fresh positions
   int32_t *sel;           // [Nmax][k]
@@ -57,7 +58,9 @@ struct Work {
   uint8_t *pk_d;          // routed W_down: [E*H/128][I/64] x 16 KB
   uint8_t *pk_sgu;        // shared W_gate/W_up: [n_sh*I_s/128][H/64] x 32 KB
   uint8_t *pk_sd;         // shared W_down: [n_sh*H/128][I_s/64] x 16 KB
-  int64_t *trace;         // [3 kernels][kTraceCtas][8] per-CTA timeline (when tracing)
+  int32_t *blk;           // [kMaxRoutingGrid][kBlkFields] per-CTA partials of the routing kernel
+  unsigned int *gbar;     // grid-barrier counter of the routing kernel (zeroed by the gate kernel)
+  int64_t *trace;         // [4 kernels][kTraceCtas][8] per-CTA timeline (when tracing)
   unsigned long long *timeline;  // [2][K_NUM]: first CTA entry, last CTA exit per kernel kind (ns)
   Ctrl *ctrl;
   epoch_iter_stats *stats;
@@ -71,6 +74,9 @@ constexpr int kTraceCtas = 1024;
 constexpr int kTraceFields = 8;
 
 constexpr int kTileBytes = 128 * 64 * 2;  // one packed 128 x 64 bf16 tile
+constexpr int kMaxRoutingGrid = 1024;
+constexpr int kBlkFields = 8;
+constexpr int kRoutingThreads = 512;
 
 // Shapes and per-call values handed to every kernel by value.
 struct Dims {
@@ -108,8 +114,7 @@ constexpr int kBoxRows[4] = {32, 64, 128, 256};
 
 // Kernel kinds, for profiling and launch counting.
 enum Kind {
-  K_GATE = 0, K_PLAN_TOPK, K_PLAN_SUPPORT, K_CLASSIFY, K_ROUTE, K_WORKLIST, K_PERMUTE,
-  K_UP, K_DOWN, K_COMBINE, K_TEST, K_MEMSET, K_NUM
+  K_GATE = 0, K_PLAN_TOPK, K_PLAN_SUPPORT, K_ROUTING, K_UP, K_DOWN, K_COMBINE, K_TEST, K_NUM
 };
 extern const char *const kKindName[K_NUM];
 
@@ -144,11 +149,8 @@ cudaError_t launch_gate_simt(const Dims &d, const Weights &w, const Work &ws, co
 cudaError_t launch_plan_topk(const Dims &d, const Weights &w, const Work &ws, cudaStream_t s);
 cudaError_t launch_plan_support(const Dims &d, const Work &ws, int32_t threshold, int all_experts,
                                 cudaStream_t s);
-cudaError_t launch_classify(const Dims &d, const Work &ws, const uint8_t *live, const uint8_t *decoded,
-                            cudaStream_t s);
-cudaError_t launch_route(const Dims &d, const Weights &w, const Work &ws, cudaStream_t s);
-cudaError_t launch_worklist(const Dims &d, const Work &ws, cudaStream_t s);
-cudaError_t launch_permute(const Dims &d, const Work &ws, const void *x, int bf16, cudaStream_t s);
+cudaError_t launch_routing(const Dims &d, const Weights &w, const Work &ws, const uint8_t *live,
+                           const uint8_t *decoded, const void *x, int bf16, cudaStream_t s);
 cudaError_t launch_combine(const Dims &d, const Work &ws, const void *x, void *y, int bf16, cudaStream_t s);
 cudaError_t launch_wait_test(uint32_t *err, int64_t timeout_ns, cudaStream_t s);
 

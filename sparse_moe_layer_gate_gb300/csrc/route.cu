@@ -19,9 +19,8 @@
 
 namespace epoch {
 
-const char *const kKindName[K_NUM] = {"gate",     "plan_topk", "plan_support", "classify",
-                                      "route",    "worklist",  "permute",      "expert_up",
-                                      "expert_down", "combine", "wait_test",   "memset"};
+const char *const kKindName[K_NUM] = {"gate",        "plan_topk",   "plan_support", "routing",
+                                      "expert_up",   "expert_down", "combine",      "wait_test"};
 
 // ---------------------------------------------------------------- helpers
 
@@ -66,14 +65,16 @@ __device__ __forceinline__ void lane_logits(const float *__restrict__ gparts, in
           v[4 * q + 3] += a.w;
         }
       }
-      const float4 *bs = reinterpret_cast<const float4 *>(bias + e0);
+      if (bias != nullptr) {
+        const float4 *bs = reinterpret_cast<const float4 *>(bias + e0);
 #pragma unroll
-      for (int q = 0; q < EPL / 4; ++q) {
-        const float4 b = __ldg(bs + q);
-        v[4 * q] += b.x;
-        v[4 * q + 1] += b.y;
-        v[4 * q + 2] += b.z;
-        v[4 * q + 3] += b.w;
+        for (int q = 0; q < EPL / 4; ++q) {
+          const float4 b = __ldg(bs + q);
+          v[4 * q] += b.x;
+          v[4 * q + 1] += b.y;
+          v[4 * q + 2] += b.z;
+          v[4 * q + 3] += b.w;
+        }
       }
       return;
     }
@@ -84,41 +85,69 @@ __device__ __forceinline__ void lane_logits(const float *__restrict__ gparts, in
     if (e < E) {
       float g = 0.f;
       for (int s = 0; s < SK; ++s) g += __ldg(gparts + (static_cast<size_t>(s) * Nmax + t) * E + e);
-      v[c] = g + __ldg(bias + e);
+      v[c] = bias != nullptr ? g + __ldg(bias + e) : g;
     } else {
       v[c] = -INFINITY;
     }
   }
 }
 
-// Top-k of one position by one warp over lane-owned experts lane*EPL + c;
-// ineligible experts never win. Every lane gets the selection (order: value
-// desc, id asc) in sel/val.
+// Top-k of one position by one warp. Lane l owns the EPL experts
+// [l*EPL, l*EPL + EPL) with logits v (ineligible ones must not win). Each lane
+// sorts its own entries (value desc, id asc) with a bitonic network; then k
+// rounds pick the best list head across the warp and pop it from its lane.
+// On return, lane j < k holds selection j: *my_sel (expert) and *my_val (logit).
 template <int EPL>
-__device__ __forceinline__ void warp_topk(const float (&v)[EPL], const bool (&ok)[EPL], int k, int (&sel)[16],
-                                          float (&val)[16]) {
-  bool taken[EPL];
+__device__ __forceinline__ void warp_topk(float (&v)[EPL], const bool (&ok)[EPL], int k, int *my_sel,
+                                          float *my_val) {
+  const int lane = lane_id();
+  int id[EPL];
 #pragma unroll
-  for (int c = 0; c < EPL; ++c) taken[c] = !ok[c];
-  const int e0 = lane_id() * EPL;
+  for (int c = 0; c < EPL; ++c) {
+    id[c] = ok[c] ? lane * EPL + c : INT_MAX;
+    if (!ok[c]) v[c] = -INFINITY;
+  }
+  // bitonic sort, descending in (value, then lower id first)
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    if (j < k) {
-      float bv = -INFINITY;
-      int bi = INT_MAX;
+  for (int size = 2; size <= EPL; size <<= 1) {
 #pragma unroll
-      for (int c = 0; c < EPL; ++c) {
-        if (!taken[c] && ranks_before(v[c], e0 + c, bv, bi)) {
-          bv = v[c];
-          bi = e0 + c;
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool desc = (i & size) == 0;
+          const bool swap = desc ? ranks_before(v[j], id[j], v[i], id[i]) : ranks_before(v[i], id[i], v[j], id[j]);
+          if (swap) {
+            const float tv = v[i];
+            v[i] = v[j];
+            v[j] = tv;
+            const int ti = id[i];
+            id[i] = id[j];
+            id[j] = ti;
+          }
         }
       }
-      warp_best(bv, bi);
-      sel[j] = bi;
-      val[j] = bv;
+    }
+  }
+  *my_sel = -1;
+  *my_val = -INFINITY;
+  for (int j = 0; j < k; ++j) {
+    float bv = v[0];
+    int bi = id[0];
+    warp_best(bv, bi);
+    if (lane == j) {
+      *my_sel = bi;
+      *my_val = bv;
+    }
+    if (id[0] == bi) {  // the winning lane pops its head
 #pragma unroll
-      for (int c = 0; c < EPL; ++c)
-        if (e0 + c == bi) taken[c] = true;
+      for (int c = 0; c + 1 < EPL; ++c) {
+        v[c] = v[c + 1];
+        id[c] = id[c + 1];
+      }
+      v[EPL - 1] = -INFINITY;
+      id[EPL - 1] = INT_MAX;
     }
   }
 }
@@ -156,7 +185,9 @@ __device__ __forceinline__ int block_excl_scan(int v, int *warp_tmp, int *total)
 // G part 0 = x W_r^T for fp32 layers: one warp per (position, expert), lanes
 // split H, fixed-order reduction (deterministic).
 template <typename T>
-__global__ void k_gate_simt(Dims d, const T *__restrict__ x, const T *__restrict__ wr, float *__restrict__ g) {
+__global__ void k_gate_simt(Dims d, const T *__restrict__ x, const T *__restrict__ wr, float *__restrict__ g,
+                            unsigned int *gbar) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) *gbar = 0u;  // grid barrier of the next routing launch
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int lane = lane_id();
   for (int o = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; o < d.n_pos * d.E; o += warps) {
@@ -184,12 +215,10 @@ __global__ void k_plan_topk(Dims d, const float *__restrict__ gparts, const floa
     lane_logits<EPL>(gparts, d.SK, d.Nmax, d.E, t, bias, v);
 #pragma unroll
     for (int c = 0; c < EPL; ++c) ok[c] = lane * EPL + c < d.E;
-    int sel[16];
-    float val[16];
-    warp_topk<EPL>(v, ok, d.k, sel, val);
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-      if (j < d.k && j == lane) atomicAdd(&counts[sel[j]], 1);
+    int sel;
+    float val;
+    warp_topk<EPL>(v, ok, d.k, &sel, &val);
+    if (lane < d.k) atomicAdd(&counts[sel], 1);
   }
 }
 
@@ -250,285 +279,77 @@ __global__ void __launch_bounds__(1024) k_plan_support(Dims d, Work ws, int32_t 
   }
 }
 
-// ---------------------------------------------------------------- classify + compact
-// One CTA of 1024 threads; thread j owns the consecutive positions
-// [j*c, (j+1)*c), so a block-wide exclusive scan keeps the fresh list ascending.
-__global__ void __launch_bounds__(1024) k_classify(Dims d, Work ws, const uint8_t *__restrict__ live,
-                                                   const uint8_t *__restrict__ decoded) {
-  const KernelMark mark_(d, ws, K_CLASSIFY);
-  constexpr int kThreads = 1024;
-  __shared__ int32_t warp_sum[32];
-  __shared__ int32_t cat[8];
-  const int tid = threadIdx.x;
-  if (tid < 8) cat[tid] = 0;
-  if (tid < d.E) ws.expert_cnt[tid] = 0;  // the route kernel counts each expert's rows
-  const int n = d.n_pos;
-  const int per = (n + kThreads - 1) / kThreads;
-  const int lo = min(tid * per, n), hi = min(lo + per, n);
-
-  // pass 1: liveness anomalies (decoded -> live) and malformed flags
-  int anomaly = 0, bad = 0;
-  for (int t = lo; t < hi; ++t) {
-    const bool lv = live[t] != 0, dc = decoded[t] != 0;
-    const bool is_live = lv || !dc;
-    bad += (lv == dc);
-    anomaly |= (is_live && ws.prev_dec[t]);
-  }
-  const int any_anomaly = __syncthreads_or(anomaly);
-  const bool force = d.host_fallback || any_anomaly;
-
-  // pass 2: categories and fresh flags
-  int nf = 0;
-  int c_live = 0, c_new = 0, c_miss = 0, c_stale = 0, c_forced = 0, c_reuse = 0;
-  for (int t = lo; t < hi; ++t) {
-    const bool lv = live[t] != 0, dc = decoded[t] != 0;
-    const bool is_live = lv || !dc;
-    const int st = ws.stamp[t];
-    bool fresh = true;
-    if (is_live) {
-      ++c_live;
-    } else if (!ws.prev_dec[t]) {
-      ++c_new;
-    } else if (st < 0) {
-      ++c_miss;
-    } else if (d.R != INT_MAX && d.iter - st >= d.R) {
-      ++c_stale;
-    } else if (force) {
-      ++c_forced;
-    } else {
-      ++c_reuse;
-      fresh = false;
-    }
-    nf += fresh;
-  }
-  // block exclusive scan of nf
-  const int lane = lane_id(), wid = warp_id();
-  int incl = nf;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) warp_sum[wid] = incl;
+// ---------------------------------------------------------------- fused routing
+// Grid-wide barrier of the cooperative routing kernel: every CTA arrives once
+// per phase; a CTA whose wait expires sets the timeout bit and the whole grid
+// unwinds (the others time out at this or the next barrier).
+__device__ __forceinline__ bool grid_sync(unsigned int *bar, unsigned int target, uint32_t *err, uint64_t tmo,
+                                          int *s_ok) {
   __syncthreads();
-  if (wid == 0) {
-    int ws_v = warp_sum[lane];
-    int wi = ws_v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += v;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(bar, 1u);
+    const uint64_t t0 = globaltimer_ns();
+    int ok = 1;
+    for (;;) {
+      unsigned int v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(bar) : "memory");
+      if (v >= target) break;
+      if (globaltimer_ns() - t0 > tmo) {
+        set_error(err, EPOCH_DEVERR_TIMEOUT);
+        ok = 0;
+        break;
+      }
+      __nanosleep(40);
     }
-    warp_sum[lane] = wi - ws_v;  // exclusive warp offsets
+    __threadfence();
+    *s_ok = ok;
   }
   __syncthreads();
-  int f = warp_sum[wid] + incl - nf;
-
-  // pass 3: write the compact list, stamps and the new previous-decoded flags
-  for (int t = lo; t < hi; ++t) {
-    const bool lv = live[t] != 0, dc = decoded[t] != 0;
-    const bool is_live = lv || !dc;
-    const int st = ws.stamp[t];
-    const bool reuse = !is_live && ws.prev_dec[t] && st >= 0 && !(d.R != INT_MAX && d.iter - st >= d.R) && !force;
-    if (!reuse) {
-      ws.fresh_pos[f] = t;
-      ws.fidx[t] = f;
-      ws.stamp[t] = d.iter;
-      ++f;
-    } else {
-      ws.fidx[t] = -1;
-    }
-    ws.prev_dec[t] = is_live ? 0 : 1;
-  }
-  atomicAdd(&cat[0], c_live);
-  atomicAdd(&cat[1], c_new);
-  atomicAdd(&cat[2], c_miss);
-  atomicAdd(&cat[3], c_stale);
-  atomicAdd(&cat[4], c_forced);
-  atomicAdd(&cat[5], c_reuse);
-  atomicAdd(&cat[6], bad);
-  __syncthreads();
-  if (tid == 0) {
-    const int n_fresh = n - cat[5];
-    const int fb = (d.host_fallback ? 1 : 0) | (any_anomaly ? 2 : 0);
-    ws.ctrl->n_fresh = n_fresh;
-    ws.ctrl->fallback = fb;
-    ws.ctrl->n_edges = n_fresh * d.k;
-    epoch_iter_stats *st = ws.stats;
-    st->iteration = d.iter;
-    st->n_pos = n;
-    st->n_live = cat[0];
-    st->n_new = cat[1];
-    st->n_miss = cat[2];
-    st->n_stale = cat[3];
-    st->n_forced = cat[4];
-    st->n_reuse = cat[5];
-    st->n_fresh = n_fresh;
-    st->n_edges = n_fresh * d.k;
-    st->support_len = fb ? d.E : ws.ctrl->support_len;
-    st->fallback = fb;
-    st->bad_flags = cat[6];
-    if (cat[6]) set_error(ws.err, EPOCH_DEVERR_FLAGS);
-  }
+  return *s_ok != 0;
 }
 
-// ---------------------------------------------------------------- restricted top-k
-// One CTA of 32 warps per chunk of 32 fresh positions, one warp per position.
-// Each fresh position takes its top-k over the support (every expert on a
-// fallback) and softmax weights over the selected logits, and sets bit p of the
-// chunk's per-expert mask; mask popcounts give the worklist its offsets with
-// no sort ("count exchange" of [W] section "FreshLane Dispatch", on chip).
-template <int EPL>
-__global__ void __launch_bounds__(1024) k_route(Dims d, Work ws, const float *__restrict__ bias) {
-  const KernelMark mark_(d, ws, K_ROUTE);
-  __shared__ uint32_t mask[1024];
-  const int chunk = blockIdx.x;
-  const int n_fresh = ws.ctrl->n_fresh;
-  if (chunk * 32 >= n_fresh) return;
-  for (int e = threadIdx.x; e < d.E; e += blockDim.x) mask[e] = 0;
-  __syncthreads();
-  const int lane = lane_id(), p = warp_id();
-  const int f = chunk * 32 + p;
-  if (f < n_fresh) {
-    const int t = ws.fresh_pos[f];
-    const bool all = ws.ctrl->fallback != 0;
-    float v[EPL];
-    bool ok[EPL];
-    lane_logits<EPL>(ws.gparts, d.SK, d.Nmax, d.E, t, bias, v);
+// Grouped-GEMM tile lists, written by every warp of the routing grid: groups
+// are the routed experts with rows, then the shared experts over every
+// position; each CTA computes the per-group tile offsets in shared memory
+// (s_bu, s_bd: [G2 + 1]) and warp gw writes the tiles of groups gw, gw + W, ...
+// with its lanes in parallel.
+__device__ void write_tile_lists(const Dims &d, const Work &ws, const int32_t *s_off, int32_t *tmp, int32_t *s_bu,
+                                 int32_t *s_bd, int n) {
+  const int tid = threadIdx.x, lane = lane_id();
+  const int E = d.E, G2 = E + d.n_sh;
+  int tu[2] = {0, 0}, td[2] = {0, 0}, hit = 0;
 #pragma unroll
-    for (int c = 0; c < EPL; ++c) {
-      const int e = lane * EPL + c;
-      ok[c] = e < d.E && (all || ws.support_mask[e]);
-    }
-    int sel[16];
-    float val[16];
-    warp_topk<EPL>(v, ok, d.k, sel, val);
-    float denom = 0.f;
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-      if (j < d.k) denom += expf(val[j] - val[0]);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      if (j < d.k && j == lane) {
-        const int e = sel[j];
-        ws.sel[f * d.k + j] = e;
-        ws.selw[f * d.k + j] = expf(val[j] - val[0]) / denom;
-        if (e >= 0 && e < d.E) atomicOr(&mask[e], 1u << p);
-        else set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+  for (int h = 0; h < 2; ++h) {
+    const int g = 2 * tid + h;
+    if (g < G2) {
+      const bool routed = g < E;
+      const int rows = routed ? s_off[g + 1] - s_off[g] : n;
+      hit += routed && rows > 0;
+      if (rows > 0 && d.tn_up > 0) {
+        tu[h] = ((rows + d.tn_up - 1) / d.tn_up) * ((routed ? d.I : d.I_s) / 128);
+        td[h] = ((rows + d.tn_dn - 1) / d.tn_dn) * (d.H / 128);
       }
     }
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < d.E; e += blockDim.x) {
-    const uint32_t m = mask[e];
-    ws.chunk_mask[static_cast<size_t>(e) * d.cmax + chunk] = m;
-    if (m) atomicAdd(&ws.expert_cnt[e], __popc(m));
-  }
-}
-
-// ---------------------------------------------------------------- worklist
-// CTA e < E places expert e's rows: row offsets[e] + (rows of expert e in
-// earlier chunks) + (bits of its chunk mask below p), so rows are grouped by
-// expert with positions ascending, with no sort and no atomics; warp w of the
-// CTA takes chunk w of each 32-chunk pass. The last CTA writes the expert
-// offsets and the grouped-GEMM tile lists: routed experts with at least one
-// row, then the shared experts over every position; experts with no rows get
-// no tile, so their weights are never read ([W] section "FreshLane Dispatch":
-// invalid slots load no expert weights).
-__global__ void __launch_bounds__(1024) k_worklist(Dims d, Work ws) {
-  const KernelMark mark_(d, ws, K_WORKLIST);
-  __shared__ int32_t tmp[33];
-  __shared__ int32_t wsum[32];
-  const int E = d.E, k = d.k;
-  const int tid = threadIdx.x, lane = lane_id(), wid = warp_id();
-  const int n_fresh = ws.ctrl->n_fresh;
-  const int n_chunks = (n_fresh + 31) / 32;
-  if (static_cast<int>(blockIdx.x) < E) {
-    const int e = blockIdx.x;
-    if (ws.expert_cnt[e] == 0) return;
-    int part = 0;
-    for (int q = tid; q < e; q += blockDim.x) part += ws.expert_cnt[q];
-    int off;
-    (void)block_excl_scan(part, tmp, &off);
-    int run = 0;
-    for (int c0 = 0; c0 < n_chunks; c0 += 32) {
-      const int c = c0 + wid;
-      const uint32_t m = c < n_chunks ? ws.chunk_mask[static_cast<size_t>(e) * d.cmax + c] : 0u;
-      if (lane == 0) wsum[wid] = __popc(m);
-      __syncthreads();
-      if (wid == 0) {
-        const int x = wsum[lane];
-        int xi = x;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int u = __shfl_up_sync(0xffffffffu, xi, o);
-          if (lane >= o) xi += u;
-        }
-        wsum[lane] = xi - x;
-        if (lane == 31) tmp[32] = xi;
-      }
-      __syncthreads();
-      if ((m >> lane) & 1u) {
-        const int f = c * 32 + lane;
-        const int dst = off + run + wsum[wid] + __popc(m & ((1u << lane) - 1u));
-        if (dst < 0 || dst >= d.Nmax * k || f >= n_fresh) {
-          set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-        } else {
-          ws.wl_pos[dst] = ws.fresh_pos[f];
-          for (int j = 0; j < k; ++j)
-            if (ws.sel[f * k + j] == e) ws.slot[f * k + j] = dst;
-        }
-      }
-      run += tmp[32];
-      __syncthreads();
-    }
-    return;
-  }
-  // ---- last CTA: offsets and tile lists
-  const int cnt = tid < E ? ws.expert_cnt[tid] : 0;
-  int total;
-  const int off = block_excl_scan(cnt, tmp, &total);
-  if (tid < E) ws.offsets[tid] = off;
-  if (tid == 0) ws.offsets[E] = total;
-  const int G = E + d.n_sh;
-  const bool routed = tid < E;
-  const bool grp = tid < G;
-  const int rows = routed ? cnt : (grp ? d.n_pos : 0);
-  const int r0 = routed ? off : 0;
-  int tu = 0, td = 0;
-  if (grp && rows > 0 && d.tn_up > 0) {
-    tu = ((rows + d.tn_up - 1) / d.tn_up) * ((routed ? d.I : d.I_s) / 128);
-    td = ((rows + d.tn_dn - 1) / d.tn_dn) * (d.H / 128);
   }
   int n_up, n_dn, n_hit;
-  const int bu = block_excl_scan(tu, tmp, &n_up);
-  const int bd = block_excl_scan(td, tmp, &n_dn);
-  (void)block_excl_scan(routed && cnt > 0 ? 1 : 0, tmp, &n_hit);
-  if (tu > 0) {
-    const int nt = (rows + d.tn_up - 1) / d.tn_up;
-    const int mt = (routed ? d.I : d.I_s) / 128;
-    for (int q = 0; q < tu; ++q) {
-      const int m = q / nt, tt = q % nt;
-      const int slot = bu + q;
-      if (slot < d.max_tiles_up)
-        ws.tiles_up[slot] = make_int4(tid, m, r0 + tt * d.tn_up, min(d.tn_up, rows - tt * d.tn_up));
-      else
-        set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-    }
-    (void)mt;
+  const int bu = block_excl_scan(tu[0] + tu[1], tmp, &n_up);
+  const int bd = block_excl_scan(td[0] + td[1], tmp, &n_dn);
+  (void)block_excl_scan(hit, tmp, &n_hit);
+  if (2 * tid < G2) {
+    s_bu[2 * tid] = bu;
+    s_bd[2 * tid] = bd;
   }
-  if (td > 0) {
-    const int nt = (rows + d.tn_dn - 1) / d.tn_dn;
-    for (int q = 0; q < td; ++q) {
-      const int m = q / nt, tt = q % nt;
-      const int slot = bd + q;
-      if (slot < d.max_tiles_dn)
-        ws.tiles_dn[slot] = make_int4(tid, m, r0 + tt * d.tn_dn, min(d.tn_dn, rows - tt * d.tn_dn));
-      else
-        set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-    }
+  if (2 * tid + 1 < G2) {
+    s_bu[2 * tid + 1] = bu + tu[0];
+    s_bd[2 * tid + 1] = bd + td[0];
   }
   if (tid == 0) {
+    s_bu[G2] = n_up;
+    s_bd[G2] = n_dn;
+  }
+  __syncthreads();
+  if (blockIdx.x == 0 && tid == 0) {
     const int up = min(n_up, d.max_tiles_up), dn = min(n_dn, d.max_tiles_dn);
     ws.ctrl->n_hit = n_hit;
     ws.ctrl->tiles_up = up;
@@ -537,26 +358,330 @@ __global__ void __launch_bounds__(1024) k_worklist(Dims d, Work ws) {
     ws.stats->tiles_up = up;
     ws.stats->tiles_down = dn;
   }
-}
-
-// ---------------------------------------------------------------- permute
-// Xp[l] = x[wl_pos[l]]: one warp per worklist row, 16-byte vectors.
-__global__ void k_permute(Dims d, Work ws, const uint4 *__restrict__ x, int vec_per_row) {
-  const KernelMark mark_(d, ws, K_PERMUTE);
-  const int n = ws.ctrl->n_edges;
-  const int warps = (gridDim.x * blockDim.x) >> 5;
-  uint4 *xp = reinterpret_cast<uint4 *>(ws.xp);
-  for (int l = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; l < n; l += warps) {
-    const int t = ws.wl_pos[l];
-    if (t < 0 || t >= d.n_pos) {
-      if (lane_id() == 0) set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-      continue;
+  if (d.tn_up <= 0) return;
+  const int nw = kRoutingThreads / 32;
+  const int W = gridDim.x * nw;
+  for (int g = blockIdx.x * nw + warp_id(); g < G2; g += W) {
+    const bool routed = g < E;
+    const int rows = routed ? s_off[g + 1] - s_off[g] : n;
+    const int r0 = routed ? s_off[g] : 0;
+    if (rows <= 0) continue;
+    const int ntu = (rows + d.tn_up - 1) / d.tn_up, ntd = (rows + d.tn_dn - 1) / d.tn_dn;
+    const int cu = s_bu[g + 1] - s_bu[g], cd = s_bd[g + 1] - s_bd[g];
+    for (int q = lane; q < cu; q += 32) {
+      const int m = q / ntu, tt = q % ntu;
+      const int slot = s_bu[g] + q;
+      if (slot < d.max_tiles_up)
+        ws.tiles_up[slot] = make_int4(g, m, r0 + tt * d.tn_up, min(d.tn_up, rows - tt * d.tn_up));
+      else
+        set_error(ws.err, EPOCH_DEVERR_BOUNDS);
     }
-    const uint4 *src = x + static_cast<size_t>(t) * vec_per_row;
-    uint4 *dst = xp + static_cast<size_t>(l) * vec_per_row;
-    for (int v = lane_id(); v < vec_per_row; v += 32) dst[v] = src[v];
+    for (int q = lane; q < cd; q += 32) {
+      const int m = q / ntd, tt = q % ntd;
+      const int slot = s_bd[g] + q;
+      if (slot < d.max_tiles_dn)
+        ws.tiles_dn[slot] = make_int4(g, m, r0 + tt * d.tn_dn, min(d.tn_dn, rows - tt * d.tn_dn));
+      else
+        set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+    }
   }
 }
+
+enum BlkField { B_SLICE = 0, B_REUSE, B_ANOM, B_BAD, B_LIVE, B_NEW, B_MISS, B_STALE };
+
+// One cooperative launch (one CTA per SM, 16 warps) runs the whole routing
+// side of an iteration in four phases separated by grid barriers:
+//  A  classify ([W] section "Liveness-Shard Parallelism"): each CTA takes a
+//     slice of positions -- live (still Mask), newly decoded (D_i \ D_{i-1}),
+//     decoded without a row, decoded with a row at least R iterations old, or
+//     stable decoded (Z_i, reuses its cached row). A decoded -> live transition
+//     anywhere, or a host-detected mismatch, makes the iteration full fresh
+//     ([W] sections "Two Clocks", "cold、hot-update、hot-skip").
+//  A' compaction: slice offsets from the per-CTA counts, an ascending fresh
+//     list, stamps of fresh rows, the new previous-decoded flags, statistics.
+//  B  one warp per fresh position: top-k of its logits over the support mask
+//     (every expert on a fallback), softmax weights over the selected logits
+//     ([W] section "Expert Atlas", step three); bit (f mod 32) of word
+//     (e, f / 32) marks that fresh position f selected expert e.
+//  C  worklist ([W] section "FreshLane Dispatch": pack, count exchange,
+//     compact dispatch -- here on chip): expert offsets from the counts; one
+//     warp per (expert, 32-position chunk) places its rows at
+//     offset(e) + rows of e in earlier chunks + bits below p, so rows are
+//     grouped by expert with positions ascending, and copies each row of x
+//     into the compact buffer. CTA 0 writes the grouped-GEMM tile lists.
+template <int EPL>
+__global__ void __launch_bounds__(kRoutingThreads) k_routing(Dims d, Work ws, const float *__restrict__ bias,
+                                                             const uint8_t *__restrict__ live,
+                                                             const uint8_t *__restrict__ decoded,
+                                                             const uint4 *__restrict__ x, int vec_per_row) {
+  const KernelMark mark_(d, ws, K_ROUTING);
+  int64_t *trace_r = (d.trace && blockIdx.x < kTraceCtas)
+                         ? ws.trace + (3ull * kTraceCtas + blockIdx.x) * kTraceFields
+                         : nullptr;
+  if (trace_r && threadIdx.x == 0) trace_r[0] = static_cast<int64_t>(globaltimer_ns());
+  __shared__ int32_t tmp[33];
+  __shared__ int32_t s_cat[kBlkFields];
+  __shared__ int32_t s_off[1025];
+  __shared__ int32_t s_bu[1025];
+  __shared__ int32_t s_bd[1025];
+  __shared__ int s_ok;
+  const int G = gridDim.x, b = blockIdx.x, tid = threadIdx.x;
+  const int lane = lane_id(), wid = warp_id(), nwarps = kRoutingThreads / 32;
+  const int n = d.n_pos, E = d.E, k = d.k;
+  const uint64_t tmo = static_cast<uint64_t>(d.timeout_ns);
+  const int n_chunks = (n + 31) / 32;
+
+  // ---- phase A: classify this CTA's slice, clear the selection masks
+  if (tid < kBlkFields) s_cat[tid] = 0;
+  for (int q = b * kRoutingThreads + tid; q < E * n_chunks; q += G * kRoutingThreads)
+    ws.chunk_mask[static_cast<size_t>(q / n_chunks) * d.cmax + (q % n_chunks)] = 0u;
+  // G = split-K partials summed in a fixed order + bias, every position
+  if ((E & 3) == 0) {
+    const int e4 = E / 4;
+    for (int q = b * kRoutingThreads + tid; q < n * e4; q += G * kRoutingThreads) {
+      const int row = q / e4, c4 = q % e4;
+      float4 acc = __ldg(reinterpret_cast<const float4 *>(ws.gparts + static_cast<size_t>(row) * E) + c4);
+      for (int sk = 1; sk < d.SK; ++sk) {
+        const float4 p4 = __ldg(reinterpret_cast<const float4 *>(ws.gparts + (static_cast<size_t>(sk) * d.Nmax + row) * E) + c4);
+        acc.x += p4.x; acc.y += p4.y; acc.z += p4.z; acc.w += p4.w;
+      }
+      const float4 b4 = __ldg(reinterpret_cast<const float4 *>(bias) + c4);
+      acc.x += b4.x; acc.y += b4.y; acc.z += b4.z; acc.w += b4.w;
+      reinterpret_cast<float4 *>(ws.logits + static_cast<size_t>(row) * E)[c4] = acc;
+    }
+  } else {
+    for (int q = b * kRoutingThreads + tid; q < n * E; q += G * kRoutingThreads) {
+      const int row = q / E, e = q % E;
+      float g = ws.gparts[static_cast<size_t>(row) * E + e];
+      for (int sk = 1; sk < d.SK; ++sk) g += ws.gparts[(static_cast<size_t>(sk) * d.Nmax + row) * E + e];
+      ws.logits[static_cast<size_t>(row) * E + e] = g + bias[e];
+    }
+  }
+  const int per = (n + G - 1) / G;
+  const int lo = min(b * per, n), hi = min(lo + per, n);
+  const int t = lo + tid;
+  const bool mine = t < hi;
+  bool is_live = false, reuse = false;
+  __syncthreads();  // s_cat cleared
+  if (mine) {
+    const bool lv = live[t] != 0, dc = decoded[t] != 0;
+    is_live = lv || !dc;
+    const bool prev = ws.prev_dec[t] != 0;
+    const int st = ws.stamp[t];
+    int cat;
+    if (is_live) cat = B_LIVE;
+    else if (!prev) cat = B_NEW;
+    else if (st < 0) cat = B_MISS;
+    else if (d.R != INT_MAX && d.iter - st >= d.R) cat = B_STALE;
+    else cat = B_REUSE;
+    reuse = cat == B_REUSE;
+    atomicAdd(&s_cat[cat], 1);
+    if (lv == dc) atomicAdd(&s_cat[B_BAD], 1);
+    if (is_live && prev) s_cat[B_ANOM] = 1;
+  }
+  __syncthreads();
+  if (tid < kBlkFields) ws.blk[b * kBlkFields + tid] = tid == B_SLICE ? hi - lo : s_cat[tid];
+  if (!grid_sync(ws.gbar, 1u * G, ws.err, tmo, &s_ok)) return;
+  if (trace_r && tid == 0) trace_r[1] = static_cast<int64_t>(globaltimer_ns());
+
+  // ---- phase A': fresh list in position order
+  int anom = 0, before = 0, total = 0, sum_cat[kBlkFields];
+#pragma unroll
+  for (int c = 0; c < kBlkFields; ++c) sum_cat[c] = 0;
+  for (int j = tid; j < G; j += kRoutingThreads) anom |= ws.blk[j * kBlkFields + B_ANOM];
+  const bool any_anom = __syncthreads_or(anom) != 0;
+  const bool force = d.host_fallback || any_anom;
+  {
+    int part_before = 0, part_total = 0;
+    for (int j = tid; j < G; j += kRoutingThreads) {
+      const int fr = ws.blk[j * kBlkFields + B_SLICE] - (force ? 0 : ws.blk[j * kBlkFields + B_REUSE]);
+      part_total += fr;
+      if (j < b) part_before += fr;
+    }
+    (void)block_excl_scan(part_before, tmp, &before);
+    (void)block_excl_scan(part_total, tmp, &total);
+  }
+  const bool fresh = mine && (!reuse || force);
+  int cnt_unused;
+  const int rank = block_excl_scan(fresh ? 1 : 0, tmp, &cnt_unused);
+  if (mine) {
+    if (fresh) {
+      const int f = before + rank;
+      ws.fresh_pos[f] = t;
+      ws.fidx[t] = f;
+      ws.stamp[t] = d.iter;
+    } else {
+      ws.fidx[t] = -1;
+    }
+    ws.prev_dec[t] = is_live ? 0 : 1;
+  }
+  const int n_fresh = total;
+  if (!grid_sync(ws.gbar, 2u * G, ws.err, tmo, &s_ok)) return;
+  if (trace_r && tid == 0) trace_r[2] = static_cast<int64_t>(globaltimer_ns());
+
+  // ---- phase B: support-restricted top-k, one warp per fresh position
+  for (int f = b * nwarps + wid; f < n_fresh; f += G * nwarps) {
+    const int tp = ws.fresh_pos[f];
+    float v[EPL];
+    bool ok[EPL];
+    lane_logits<EPL>(ws.logits, 1, d.Nmax, E, tp, nullptr, v);
+#pragma unroll
+    for (int c = 0; c < EPL; ++c) {
+      const int e = lane * EPL + c;
+      ok[c] = e < E && (force || ws.support_mask[e]);
+    }
+    int sel;
+    float val;
+    warp_topk<EPL>(v, ok, k, &sel, &val);
+    const float top = __shfl_sync(0xffffffffu, val, 0);
+    const float ex = lane < k ? expf(val - top) : 0.f;
+    float denom = 0.f;  // summed in selection order j = 0..k-1 (deterministic)
+    for (int j = 0; j < k; ++j) denom += __shfl_sync(0xffffffffu, ex, j);
+    if (lane < k) {
+      if (sel < 0 || sel >= E) {
+        set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+      } else {
+        ws.sel[f * k + lane] = sel;
+        ws.selw[f * k + lane] = ex / denom;
+        atomicOr(&ws.chunk_mask[static_cast<size_t>(sel) * d.cmax + (f >> 5)], 1u << (f & 31));
+      }
+    }
+  }
+  if (!grid_sync(ws.gbar, 3u * G, ws.err, tmo, &s_ok)) return;
+  if (trace_r && tid == 0) trace_r[3] = static_cast<int64_t>(globaltimer_ns());
+
+  // ---- phase C: expert offsets, worklist rows, compact copies of x, tile lists
+  const int fresh_chunks = (n_fresh + 31) / 32;
+  {
+    // rows of each expert = popcount of its selection masks (every CTA derives
+    // the offsets itself; no global counters)
+    int cnt2[2] = {0, 0};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int e = 2 * tid + h;
+      if (e < E) {
+        const uint32_t *row = ws.chunk_mask + static_cast<size_t>(e) * d.cmax;
+        int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+        int c = 0;
+        for (; c + 4 <= fresh_chunks; c += 4) {
+          a0 += __popc(row[c]);
+          a1 += __popc(row[c + 1]);
+          a2 += __popc(row[c + 2]);
+          a3 += __popc(row[c + 3]);
+        }
+        for (; c < fresh_chunks; ++c) a0 += __popc(row[c]);
+        cnt2[h] = a0 + a1 + a2 + a3;
+      }
+    }
+    const int c0 = cnt2[0], c1 = cnt2[1];
+    int tot;
+    const int o = block_excl_scan(c0 + c1, tmp, &tot);
+    if (2 * tid < E) s_off[2 * tid] = o;
+    if (2 * tid + 1 < E) s_off[2 * tid + 1] = o + c0;
+    if (tid == 0) s_off[E] = tot;
+    __syncthreads();
+  }
+  for (int pair = b * nwarps + wid; pair < E * fresh_chunks; pair += G * nwarps) {
+    const int e = pair / fresh_chunks, c = pair % fresh_chunks;
+    const uint32_t *row = ws.chunk_mask + static_cast<size_t>(e) * d.cmax;
+    const uint32_t m = row[c];
+    if (m == 0u) continue;
+    int before_c = 0;
+    for (int c2 = lane; c2 < c; c2 += 32) before_c += __popc(row[c2]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) before_c += __shfl_xor_sync(0xffffffffu, before_c, o);
+    if ((m >> lane) & 1u) {  // lane p places the edge of fresh position 32 c + p
+      const int f = c * 32 + lane;
+      const int dst = s_off[e] + before_c + __popc(m & ((1u << lane) - 1u));
+      if (dst < 0 || dst >= d.Nmax * k || f >= n_fresh) {
+        set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+      } else {
+        ws.wl_pos[dst] = ws.fresh_pos[f];
+        for (int j = 0; j < k; ++j)
+          if (ws.sel[f * k + j] == e) ws.slot[f * k + j] = dst;
+      }
+    }
+  }
+  if (trace_r && tid == 0) trace_r[4] = static_cast<int64_t>(globaltimer_ns());
+  if (!grid_sync(ws.gbar, 4u * G, ws.err, tmo, &s_ok)) return;
+  // after the last barrier nothing waits on CTA 0: statistics, offsets, tiles
+  if (b == 0) {
+    // sums of the per-CTA category counts: thread j reads CTA j's record (two
+    // 16-byte loads), then a warp-shuffle and shared-memory reduction
+    for (int j = tid; j < G; j += kRoutingThreads) {
+      const int4 u = reinterpret_cast<const int4 *>(ws.blk + j * kBlkFields)[0];
+      const int4 w2 = reinterpret_cast<const int4 *>(ws.blk + j * kBlkFields)[1];
+      sum_cat[0] += u.x; sum_cat[1] += u.y; sum_cat[2] += u.z; sum_cat[3] += u.w;
+      sum_cat[4] += w2.x; sum_cat[5] += w2.y; sum_cat[6] += w2.z; sum_cat[7] += w2.w;
+    }
+#pragma unroll
+    for (int c = 0; c < kBlkFields; ++c) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum_cat[c] += __shfl_xor_sync(0xffffffffu, sum_cat[c], o);
+    }
+    if (tid < kBlkFields) s_cat[tid] = 0;
+    __syncthreads();
+    if (lane == 0) {
+#pragma unroll
+      for (int c = 0; c < kBlkFields; ++c) atomicAdd(&s_cat[c], sum_cat[c]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int c = 0; c < kBlkFields; ++c) sum_cat[c] = s_cat[c];
+    if (tid == 0) {
+      const int fb = (d.host_fallback ? 1 : 0) | (any_anom ? 2 : 0);
+      ws.ctrl->n_fresh = n_fresh;
+      ws.ctrl->fallback = fb;
+      ws.ctrl->n_edges = n_fresh * k;
+      epoch_iter_stats *st = ws.stats;
+      st->iteration = d.iter;
+      st->n_pos = n;
+      st->n_live = sum_cat[B_LIVE];
+      st->n_new = sum_cat[B_NEW];
+      st->n_miss = sum_cat[B_MISS];
+      st->n_stale = sum_cat[B_STALE];
+      st->n_forced = force ? sum_cat[B_REUSE] : 0;
+      st->n_reuse = force ? 0 : sum_cat[B_REUSE];
+      st->n_fresh = n_fresh;
+      st->n_edges = n_fresh * k;
+      st->support_len = fb ? E : ws.ctrl->support_len;
+      st->fallback = fb;
+      st->bad_flags = sum_cat[B_BAD];
+      if (sum_cat[B_BAD]) set_error(ws.err, EPOCH_DEVERR_FLAGS);
+    }
+    for (int e = tid; e <= E; e += kRoutingThreads) ws.offsets[e] = s_off[e];
+  }
+  write_tile_lists(d, ws, s_off, tmp, s_bu, s_bd, n);
+
+  // ---- phase D: copy each worklist row of x into the compact buffer
+  const int n_edges = n_fresh * k;
+  for (int l = b * nwarps + wid; l < n_edges; l += G * nwarps) {
+    const int tp = ws.wl_pos[l];
+    if (tp < 0 || tp >= n) {
+      if (lane == 0) set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+      continue;
+    }
+    const uint4 *src = x + static_cast<size_t>(tp) * vec_per_row;
+    uint4 *out = reinterpret_cast<uint4 *>(ws.xp) + static_cast<size_t>(l) * vec_per_row;
+    // all loads of a batch are issued before its stores (the destination may
+    // alias nothing the loads read, but the compiler cannot know that)
+    for (int v0 = 0; v0 < vec_per_row; v0 += 32 * 8) {
+      uint4 buf[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int v = v0 + q * 32 + lane;
+        if (v < vec_per_row) buf[q] = __ldg(src + v);
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int v = v0 + q * 32 + lane;
+        if (v < vec_per_row) out[v] = buf[q];
+      }
+    }
+  }
+  if (trace_r && tid == 0) trace_r[5] = static_cast<int64_t>(globaltimer_ns());
+}
+
 
 // ---------------------------------------------------------------- combine + cache
 // Eight consecutive elements of a row, loaded/stored as one or two 16-byte vectors.
@@ -688,12 +813,12 @@ cudaError_t launch_gate_simt(const Dims &d, const Weights &w, const Work &ws, co
     static bool carve_ = (prefer_max_shared(k_gate_simt<__nv_bfloat16>) == cudaSuccess);
     (void)carve_;
     k_gate_simt<__nv_bfloat16><<<blocks, 256, 0, s>>>(d, static_cast<const __nv_bfloat16 *>(x),
-                                                      static_cast<const __nv_bfloat16 *>(w.w_router), ws.gparts);
+                                                      static_cast<const __nv_bfloat16 *>(w.w_router), ws.gparts, ws.gbar);
   } else {
     static bool carve_ = (prefer_max_shared(k_gate_simt<float>) == cudaSuccess);
     (void)carve_;
     k_gate_simt<float><<<blocks, 256, 0, s>>>(d, static_cast<const float *>(x),
-                                              static_cast<const float *>(w.w_router), ws.gparts);
+                                              static_cast<const float *>(w.w_router), ws.gparts, ws.gbar);
   }
   return cudaGetLastError();
 }
@@ -722,46 +847,39 @@ cudaError_t launch_plan_support(const Dims &d, const Work &ws, int32_t threshold
   return cudaGetLastError();
 }
 
-cudaError_t launch_classify(const Dims &d, const Work &ws, const uint8_t *live, const uint8_t *decoded,
-                            cudaStream_t s) {
-  static bool carve_ = (prefer_max_shared(k_classify) == cudaSuccess);
-  (void)carve_;
-  k_classify<<<1, 1024, 0, s>>>(d, ws, live, decoded);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_route(const Dims &d, const Weights &w, const Work &ws, cudaStream_t s) {
-  const int chunks = (d.Nmax + 31) / 32;
+// Cooperative launch (the phases wait on one another through grid barriers,
+// so every CTA must be resident): one CTA per SM, capped at what fits.
+cudaError_t launch_routing(const Dims &d, const Weights &w, const Work &ws, const uint8_t *live,
+                           const uint8_t *decoded, const void *x, int bf16, cudaStream_t s) {
+  int grid = num_sms();
+  if (grid > kMaxRoutingGrid) grid = kMaxRoutingGrid;
+  // slices of at most kRoutingThreads positions per CTA
+  const int min_grid = (d.n_pos + kRoutingThreads - 1) / kRoutingThreads;
+  if (grid < min_grid) return cudaErrorInvalidConfiguration;
+  const int vec = d.H * (bf16 ? 2 : 4) / 16;
+  const float *bias = w.b_router;
+  const uint4 *xv = static_cast<const uint4 *>(x);
+  Dims dd = d;
+  Work ww = ws;
+  void *args[] = {&dd, &ww, const_cast<float **>(&bias), const_cast<uint8_t **>(&live),
+                  const_cast<uint8_t **>(&decoded), const_cast<uint4 **>(&xv), const_cast<int *>(&vec)};
   switch (epl_for(d.E)) {
-#define EPOCH_CASE(N)                                                    \
-  case N: {                                                              \
-    static bool c_ = (prefer_max_shared(k_route<N>) == cudaSuccess);     \
-    (void)c_;                                                            \
-    k_route<N><<<chunks, 1024, 0, s>>>(d, ws, w.b_router);               \
-    break;                                                               \
+#define EPOCH_CASE(N)                                                                                    \
+  case N: {                                                                                              \
+    static bool c_ = (prefer_max_shared(k_routing<N>) == cudaSuccess);                                   \
+    (void)c_;                                                                                            \
+    return cudaLaunchCooperativeKernel(reinterpret_cast<void *>(k_routing<N>), dim3(grid), dim3(kRoutingThreads), \
+                                       args, 0, s);                                                      \
   }
     EPOCH_CASE(1) EPOCH_CASE(2) EPOCH_CASE(4) EPOCH_CASE(8) EPOCH_CASE(16) EPOCH_CASE(32)
 #undef EPOCH_CASE
   }
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_worklist(const Dims &d, const Work &ws, cudaStream_t s) {
-  static bool carve_ = (prefer_max_shared(k_worklist) == cudaSuccess);
-  (void)carve_;
-  k_worklist<<<d.E + 1, 1024, 0, s>>>(d, ws);
-  return cudaGetLastError();
-}
 
-cudaError_t launch_permute(const Dims &d, const Work &ws, const void *x, int bf16, cudaStream_t s) {
-  const int vec = d.H * (bf16 ? 2 : 4) / 16;
-  int blocks = (d.Nmax * d.k + 7) / 8;
-  if (blocks > 4 * num_sms()) blocks = 4 * num_sms();
-  static bool carve_ = (prefer_max_shared(k_permute) == cudaSuccess);
-  (void)carve_;
-  k_permute<<<blocks, 256, 0, s>>>(d, ws, static_cast<const uint4 *>(x), vec);
-  return cudaGetLastError();
-}
+
+
 
 cudaError_t launch_combine(const Dims &d, const Work &ws, const void *x, void *y, int bf16, cudaStream_t s) {
   if (bf16) {

@@ -124,19 +124,20 @@ class EpochLayer:
         B.check(B.lib().epoch_set_tracing(self.handle, 1 if on else 0), "epoch_set_tracing")
 
     def read_trace(self, stream=None) -> np.ndarray:
-        """[3, 1024, 8] int64 per-CTA timelines of the last gate/up/down launches."""
+        """[4, 1024, 8] int64 per-CTA timelines of the last gate/up/down/routing launches."""
         v = B.epoch_debug_view()
         B.check(B.lib().epoch_debug_pointers(self.handle, C.byref(v)), "epoch_debug_pointers")
-        return self._copy(v.trace, 3 * 1024 * 8, np.int64, stream).reshape(3, 1024, 8)
+        return self._copy(v.trace, 4 * 1024 * 8, np.int64, stream).reshape(4, 1024, 8)
 
     def read_timeline(self, stream=None) -> dict:
         """{kernel: (first entry ns, last exit ns)} of the last traced iteration."""
         v = B.epoch_debug_view()
         B.check(B.lib().epoch_debug_pointers(self.handle, C.byref(v)), "epoch_debug_pointers")
-        raw = self._copy(v.timeline, 2 * B.EPOCH_PROF_KINDS, np.uint64, stream).reshape(2, -1)
-        names = ["gate", "plan_topk", "plan_support", "classify", "route", "worklist", "permute",
-                 "expert_up", "expert_down", "combine", "wait_test", "memset"]
-        return {n: (int(raw[0, i]), int(raw[1, i])) for i, n in enumerate(names) if raw[1, i] > 0}
+        p = B.epoch_profile()
+        B.check(B.lib().epoch_read_profile(self.handle, C.byref(p)), "epoch_read_profile")
+        nk = sum(1 for i in range(B.EPOCH_PROF_KINDS) if p.name[i])
+        raw = self._copy(v.timeline, 2 * nk, np.uint64, stream).reshape(2, nk)
+        return {p.name[i].decode(): (int(raw[0, i]), int(raw[1, i])) for i in range(nk) if raw[1, i] > 0}
 
     def set_profiling(self, on: bool) -> None:
         B.check(B.lib().epoch_set_profiling(self.handle, 1 if on else 0), "epoch_set_profiling")
@@ -188,6 +189,7 @@ class EpochLayer:
         if "logits" in parts:
             raw = self._copy(v.logit_parts, v.n_logit_parts * N * E, np.float32, stream)
             d["logit_parts"] = raw.reshape(v.n_logit_parts, N, E)[:, :n_pos]
+            d["logits"] = self._copy(v.logits, N * E, np.float32, stream).reshape(N, E)[:n_pos]
         if "cache" in parts:
             cdt = np.uint16 if self.dtype == "bf16" else np.float32
             d["cache"] = self._copy(v.cache, n_pos * self.hidden, cdt, stream).reshape(n_pos, self.hidden)
