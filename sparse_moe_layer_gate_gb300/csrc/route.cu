@@ -16,6 +16,7 @@
 
 #include "common.cuh"
 #include "layer.h"
+#include "topk.cuh"
 
 namespace epoch {
 
@@ -23,134 +24,6 @@ const char *const kKindName[K_NUM] = {"gate",        "plan_topk",   "plan_suppor
                                       "expert_up",   "expert_down", "combine",      "wait_test"};
 
 // ---------------------------------------------------------------- helpers
-
-// (value desc, id asc) order used for every top-k: true if (va, ia) ranks first.
-__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
-}
-
-// Warp-wide arg-best of (v, id) pairs; every lane returns the winner.
-__device__ __forceinline__ void warp_best(float &v, int &id) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, id, o);
-    if (ranks_before(ov, oi, v, id)) {
-      v = ov;
-      id = oi;
-    }
-  }
-}
-
-// Logits of the EPL consecutive experts [lane*EPL, lane*EPL + EPL) of position
-// t: split-K partial sums in a fixed order, then the bias. Experts >= E get
-// -inf. Vector loads when the row is 16-byte aligned.
-template <int EPL>
-__device__ __forceinline__ void lane_logits(const float *__restrict__ gparts, int SK, int Nmax, int E, int t,
-                                            const float *__restrict__ bias, float (&v)[EPL]) {
-  const int e0 = lane_id() * EPL;
-#pragma unroll
-  for (int c = 0; c < EPL; ++c) v[c] = 0.f;
-  if constexpr (EPL % 4 == 0) {
-    if ((E & 3) == 0 && e0 + EPL <= E) {
-#pragma unroll 4
-      for (int s = 0; s < SK; ++s) {
-        const float4 *src = reinterpret_cast<const float4 *>(gparts + (static_cast<size_t>(s) * Nmax + t) * E + e0);
-#pragma unroll
-        for (int q = 0; q < EPL / 4; ++q) {
-          const float4 a = __ldg(src + q);
-          v[4 * q] += a.x;
-          v[4 * q + 1] += a.y;
-          v[4 * q + 2] += a.z;
-          v[4 * q + 3] += a.w;
-        }
-      }
-      if (bias != nullptr) {
-        const float4 *bs = reinterpret_cast<const float4 *>(bias + e0);
-#pragma unroll
-        for (int q = 0; q < EPL / 4; ++q) {
-          const float4 b = __ldg(bs + q);
-          v[4 * q] += b.x;
-          v[4 * q + 1] += b.y;
-          v[4 * q + 2] += b.z;
-          v[4 * q + 3] += b.w;
-        }
-      }
-      return;
-    }
-  }
-#pragma unroll
-  for (int c = 0; c < EPL; ++c) {
-    const int e = e0 + c;
-    if (e < E) {
-      float g = 0.f;
-      for (int s = 0; s < SK; ++s) g += __ldg(gparts + (static_cast<size_t>(s) * Nmax + t) * E + e);
-      v[c] = bias != nullptr ? g + __ldg(bias + e) : g;
-    } else {
-      v[c] = -INFINITY;
-    }
-  }
-}
-
-// Top-k of one position by one warp. Lane l owns the EPL experts
-// [l*EPL, l*EPL + EPL) with logits v (ineligible ones must not win). Each lane
-// sorts its own entries (value desc, id asc) with a bitonic network; then k
-// rounds pick the best list head across the warp and pop it from its lane.
-// On return, lane j < k holds selection j: *my_sel (expert) and *my_val (logit).
-template <int EPL>
-__device__ __forceinline__ void warp_topk(float (&v)[EPL], const bool (&ok)[EPL], int k, int *my_sel,
-                                          float *my_val) {
-  const int lane = lane_id();
-  int id[EPL];
-#pragma unroll
-  for (int c = 0; c < EPL; ++c) {
-    id[c] = ok[c] ? lane * EPL + c : INT_MAX;
-    if (!ok[c]) v[c] = -INFINITY;
-  }
-  // bitonic sort, descending in (value, then lower id first)
-#pragma unroll
-  for (int size = 2; size <= EPL; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const bool desc = (i & size) == 0;
-          const bool swap = desc ? ranks_before(v[j], id[j], v[i], id[i]) : ranks_before(v[i], id[i], v[j], id[j]);
-          if (swap) {
-            const float tv = v[i];
-            v[i] = v[j];
-            v[j] = tv;
-            const int ti = id[i];
-            id[i] = id[j];
-            id[j] = ti;
-          }
-        }
-      }
-    }
-  }
-  *my_sel = -1;
-  *my_val = -INFINITY;
-  for (int j = 0; j < k; ++j) {
-    float bv = v[0];
-    int bi = id[0];
-    warp_best(bv, bi);
-    if (lane == j) {
-      *my_sel = bi;
-      *my_val = bv;
-    }
-    if (id[0] == bi) {  // the winning lane pops its head
-#pragma unroll
-      for (int c = 0; c + 1 < EPL; ++c) {
-        v[c] = v[c + 1];
-        id[c] = id[c + 1];
-      }
-      v[EPL - 1] = -INFINITY;
-      id[EPL - 1] = INT_MAX;
-    }
-  }
-}
 
 // Exclusive scan over a CTA of up to 1024 threads; *total gets the sum.
 __device__ __forceinline__ int block_excl_scan(int v, int *warp_tmp, int *total) {
