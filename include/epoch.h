@@ -249,6 +249,25 @@ epoch_status epoch_reset_profile(epoch_layer *layer);
  * EPOCH_DEVERR_TIMEOUT and return. Exercises the timeout path without a hang. */
 epoch_status epoch_test_wait_timeout(epoch_layer *layer, int64_t timeout_ns, epoch_stream stream);
 
+/* Block planner for callers that cannot allocate device memory (graph capture
+ * into a fixed pool, allocator-free runtimes with a pre-planned arena, serving
+ * loops that forbid cudaMalloc between requests); it needs no epoch_layer.
+ * The pages have no counterpart: this is an interface variant of the cold-path
+ * planner of epoch_plan_block (same ranking and coverage rule, see tau) taking
+ * the router logits the caller already holds.
+ *  logits_dev [n_pos][n_experts] float, bias included (device, 16-byte aligned);
+ *  top_k, tau as in epoch_layer_config; outputs support_ids_dev [n_experts]
+ *  (experts in rank order) and support_len_dev [1] (device).
+ * Its only scratch, the per-expert hit counts, is a fixed file-scope device
+ * array of 1024 int32 (4 KB) that every GPU loading the library holds until
+ * exit; n_experts > 1024 returns EPOCH_EINVAL. No call allocates memory. The
+ * first call on a device looks up the array's device address (do it before any
+ * stream capture); every call clears the counts it uses. All calls share the
+ * array: calls that overlap on the GPU race and must be serialised. */
+epoch_status epoch_plan_support_noalloc(const float *logits_dev, int32_t n_pos, int32_t n_experts, int32_t top_k,
+                                        double tau, int32_t *support_ids_dev, int32_t *support_len_dev,
+                                        epoch_stream stream);
+
 /* Releases host state only (the caller frees the workspace and weights). NULL is ignored. */
 void epoch_layer_destroy(epoch_layer *layer);
 

@@ -81,6 +81,8 @@ _SIGS = {
     "epoch_read_profile": (C.c_int, [C.c_void_p, C.POINTER(epoch_profile)]),
     "epoch_reset_profile": (C.c_int, [C.c_void_p]),
     "epoch_test_wait_timeout": (C.c_int, [C.c_void_p, C.c_int64, C.c_void_p]),
+    "epoch_plan_support_noalloc": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_double,
+                                             C.c_void_p, C.c_void_p, C.c_void_p]),
     "epoch_layer_destroy": (None, [C.c_void_p]),
     "epoch_status_str": (C.c_char_p, [C.c_int]),
 }

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libepoch.so")
-SOURCES = ["abi.cu", "route.cu", "gemm_simt.cu", "gemm_tc.cu"]
+SOURCES = ["abi.cu", "route.cu", "gemm_simt.cu", "gemm_tc.cu", "plan_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
