@@ -38,8 +38,7 @@ L2_FLUSH_BYTES = 256 << 20
 
 # DRAM traffic of one expert_up launch from an ncu capture, tied to the kernel
 # source it was measured on (null once that source changes).
-TRAFFIC = {"expert_up": {"bytes_per_launch": 161.43e6, "source_sha": "70ae87a5aa7f377c",
-                         "capture": "profiles/expert_up_llada2_mini.md (steady-state iteration 20)"}}
+TRAFFIC = {"experts": None}
 
 
 def parse():
@@ -105,10 +104,10 @@ def iteration_work(wl, st):
     return flops, nbytes
 
 
-def up_kernel_bytes(wl, st):
-    """Algorithmic bytes of one expert_up launch: W_gate and W_up of every hit
-    routed expert and of the shared experts, read once."""
-    return 2 * wl.hidden * 2 * (st["n_hit_experts"] * wl.inter + wl.n_shared * wl.shared_inter)
+def experts_kernel_bytes(wl, st):
+    """Algorithmic bytes of one experts launch (up and down projections): W_gate,
+    W_up and W_down of every hit routed expert and of the shared experts, read once."""
+    return 3 * wl.hidden * 2 * (st["n_hit_experts"] * wl.inter + wl.n_shared * wl.shared_inter)
 
 
 def source_sha():
@@ -315,11 +314,11 @@ def run_epoch(args, rank, world):
     path_frac = sum(t_roof) / (float(iter_mean_ms.sum()) / 1e3)
     bound_iters = sum(1 for f, b in work if b / (hbm * 1e9) >= f / (tc * 1e12))
 
-    up = prof.get("expert_up", {"launches": 0, "total_ms": 0.0})
-    up_bytes = sum(up_kernel_bytes(wl, st) for st in stats) / wl.iters
+    up = prof.get("experts", {"launches": 0, "total_ms": 0.0})
+    up_bytes = sum(experts_kernel_bytes(wl, st) for st in stats) / wl.iters
     up_ms = up["total_ms"] / max(up["launches"], 1)
     up_gbs = up_bytes / (up_ms / 1e3) / 1e9 if up_ms > 0 else None
-    tr = TRAFFIC.get("expert_up")
+    tr = TRAFFIC.get("experts")
     traffic = tr["bytes_per_launch"] if tr and tr.get("source_sha") == source_sha() else None
     kernels = {k: {"launches": v["launches"], "avg_us": 1e3 * v["total_ms"] / max(v["launches"], 1),
                    "share": v["total_ms"] / max(sum(x["total_ms"] for kk, x in prof.items()
@@ -344,7 +343,7 @@ def run_epoch(args, rank, world):
         "path_roofline": {"frac": path_frac, "hbm_bound_iters": bound_iters, "iters": wl.iters,
                           "roofline_us_per_iter": 1e6 * sum(t_roof) / wl.iters,
                           "peak_hbm_gbs": hbm, "peak_bf16_tflops": tc, "peaks": f"of {src}"},
-        "roofline": {"kernel": "expert_up", "bound": "hbm", "achieved": up_gbs, "peak": hbm, "unit": "GB/s",
+        "roofline": {"kernel": "experts", "bound": "hbm", "achieved": up_gbs, "peak": hbm, "unit": "GB/s",
                      "frac": (up_gbs / hbm) if up_gbs else None, "traffic": traffic,
                      "algorithmic_bytes_per_launch": up_bytes, "avg_launch_us": 1e3 * up_ms,
                      "peak_source": f"of {src} (STREAM copy, burst)"},

@@ -76,7 +76,7 @@ typedef enum { EPOCH_F32 = 0, EPOCH_BF16 = 1 } epoch_dtype;
  *    age of [W] section "decoded-cache 的刷新周期为什么默认取 5".
  *  residual: nonzero makes y = x + routed + shared (chains a stack of layers).
  * Constraints (else EPOCH_EINVAL): 1 <= top_k <= n_experts <= 1024, top_k <= 16;
- *  bf16: H, I and shared_inter multiples of 128; f32: multiples of 4;
+ *  bf16: H a multiple of 256, I and shared_inter multiples of 128; f32: multiples of 4;
  *  1 <= max_positions <= 16384. */
 typedef struct {
   int32_t hidden;

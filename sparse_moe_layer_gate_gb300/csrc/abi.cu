@@ -64,6 +64,7 @@ bool valid_config(const epoch_layer_config *c) {
   if (c->refresh_R < 1) return false;
   const int q = c->dtype == EPOCH_BF16 ? 128 : 4;
   if (c->hidden % q || c->inter % q) return false;
+  if (c->dtype == EPOCH_BF16 && c->hidden % kBmDn) return false;  // down tiles cover 256 rows of H
   if (c->n_shared > 0 && c->shared_inter % q) return false;
   return true;
 }
@@ -76,13 +77,12 @@ int sk_max_for(const epoch_layer_config &c) {
 
 // Capacity of the grouped-GEMM tile lists: every group splits into token tiles
 // of tn rows (at most rows/tn + 1 each) times its M tiles of 128.
-void tile_caps(const epoch_layer_config &c, int tn, int *up, int *dn) {
+void tile_caps(const epoch_layer_config &c, int tn_up, int tn_dn, int *up, int *dn) {
   const long N = c.max_positions, k = c.top_k, E = c.n_experts, nsh = c.n_shared;
   const long Is = c.n_shared ? c.shared_inter : 0;
-  const long routed_t = (N * k + tn - 1) / tn + E;
-  const long shared_t = nsh * ((N + tn - 1) / tn);
-  *up = static_cast<int>(routed_t * (c.inter / 128) + shared_t * (Is / 128));
-  *dn = static_cast<int>((routed_t + shared_t) * (c.hidden / 128));
+  *up = static_cast<int>(((N * k + tn_up - 1) / tn_up + E) * (c.inter / 128) +
+                         nsh * ((N + tn_up - 1) / tn_up) * (Is / 128));
+  *dn = static_cast<int>(((N * k + tn_dn - 1) / tn_dn + E + nsh * ((N + tn_dn - 1) / tn_dn)) * (c.hidden / kBmDn));
 }
 
 // Lays the workspace out (base == nullptr: only measures). Returns total bytes.
@@ -115,9 +115,12 @@ size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   t.expert_cnt = static_cast<int32_t *>(take(E * 4));
   t.offsets = static_cast<int32_t *>(take((E + 1) * 4));
   int cap_up = 0, cap_dn = 0;
-  if (c.dtype == EPOCH_BF16) tile_caps(c, kTnUp, &cap_up, &cap_dn);
+  if (c.dtype == EPOCH_BF16) tile_caps(c, kTnUp, kTnDn, &cap_up, &cap_dn);
   t.tiles_up = static_cast<int4 *>(take(static_cast<size_t>(cap_up) * 16 + 16));
   t.tiles_dn = static_cast<int4 *>(take(static_cast<size_t>(cap_dn) * 16 + 16));
+  t.up_needed = static_cast<int32_t *>(take((E + nsh) * 4));
+  t.done_up = static_cast<int32_t *>(take((E + nsh) * 4));
+  t.tile_ctr = static_cast<int32_t *>(take(16));
   t.wl_pos = static_cast<int32_t *>(take(N * k * 4));
   t.slot = static_cast<int32_t *>(take(N * k * 4));
   t.xp = take(N * k * H * act);
@@ -250,7 +253,7 @@ epoch_status epoch_layer_create(const epoch_layer_config *cfg, const epoch_layer
   d.tn_up = L->bf16 ? kTnUp : 0;
   d.tn_dn = L->bf16 ? kTnDn : 0;
   d.cmax = (cfg->max_positions + 31) / 32;
-  if (L->bf16) tile_caps(*cfg, kTnUp, &d.max_tiles_up, &d.max_tiles_dn);
+  if (L->bf16) tile_caps(*cfg, kTnUp, kTnDn, &d.max_tiles_up, &d.max_tiles_dn);
   d.timeout_ns = 2000000000ll;
   memset(&L->maps, 0, sizeof(L->maps));
   if (L->bf16) {
@@ -281,13 +284,13 @@ epoch_status epoch_layer_create(const epoch_layer_config *cfg, const epoch_layer
   if (L->bf16) {
     // expert weights -> packed swizzled tiles (gate and up tiles interleaved)
     const int64_t H = d.H, E = d.E, I = d.I, nsh = d.n_sh, Is = d.I_s, T = kTileBytes;
-    cudaError_t e = launch_pack_tiles(w->w_gate, E * I, H, L->ws.pk_gu, 2 * T, 0, nullptr);
-    if (e == cudaSuccess) e = launch_pack_tiles(w->w_up, E * I, H, L->ws.pk_gu, 2 * T, T, nullptr);
-    if (e == cudaSuccess) e = launch_pack_tiles(w->w_down, E * H, I, L->ws.pk_d, T, 0, nullptr);
+    cudaError_t e = launch_pack_tiles(w->w_gate, E * I, H, L->ws.pk_gu, 2 * T, 0, 1, nullptr);
+    if (e == cudaSuccess) e = launch_pack_tiles(w->w_up, E * I, H, L->ws.pk_gu, 2 * T, T, 1, nullptr);
+    if (e == cudaSuccess) e = launch_pack_tiles(w->w_down, E * H, I, L->ws.pk_d, 2 * T, 0, 2, nullptr);
     if (e == cudaSuccess && nsh > 0) {
-      e = launch_pack_tiles(w->ws_gate, nsh * Is, H, L->ws.pk_sgu, 2 * T, 0, nullptr);
-      if (e == cudaSuccess) e = launch_pack_tiles(w->ws_up, nsh * Is, H, L->ws.pk_sgu, 2 * T, T, nullptr);
-      if (e == cudaSuccess) e = launch_pack_tiles(w->ws_down, nsh * H, Is, L->ws.pk_sd, T, 0, nullptr);
+      e = launch_pack_tiles(w->ws_gate, nsh * Is, H, L->ws.pk_sgu, 2 * T, 0, 1, nullptr);
+      if (e == cudaSuccess) e = launch_pack_tiles(w->ws_up, nsh * Is, H, L->ws.pk_sgu, 2 * T, T, 1, nullptr);
+      if (e == cudaSuccess) e = launch_pack_tiles(w->ws_down, nsh * H, Is, L->ws.pk_sd, 2 * T, 0, 2, nullptr);
     }
     if (e != cudaSuccess) {
       delete L;
@@ -349,8 +352,7 @@ epoch_status epoch_moe_iter(epoch_layer *L, const void *x, const uint8_t *live, 
   EPOCH_TRY(run_gate(L, d, x, x_maps, s));
   EPOCH_TRY(run(L, K_ROUTING, s, [&] { return launch_routing(d, L->w, L->ws, live, decoded, x, L->bf16, s); }));
   if (L->bf16) {
-    EPOCH_TRY(run(L, K_UP, s, [&] { return launch_up_tc(d, L->maps, L->ws, x_maps[1], s); }));
-    EPOCH_TRY(run(L, K_DOWN, s, [&] { return launch_down_tc(d, L->maps, L->ws, s); }));
+    EPOCH_TRY(run(L, K_UP, s, [&] { return launch_experts_tc(d, L->maps, L->ws, x_maps[1], s); }));
   } else {
     EPOCH_TRY(run(L, K_UP, s, [&] { return launch_up_simt(d, L->w, L->ws, x, s); }));
     EPOCH_TRY(run(L, K_DOWN, s, [&] { return launch_down_simt(d, L->w, L->ws, s); }));

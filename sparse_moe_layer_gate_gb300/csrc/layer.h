@@ -44,6 +44,9 @@ struct Work {
   int32_t *offsets;       // [E+1]
   int4 *tiles_up;         // [max_tiles_up] {group, m tile, first row, valid rows}
   int4 *tiles_dn;         // [max_tiles_dn]
+  int32_t *up_needed;     // [E + n_sh] up tiles of each group (down tiles wait for all of them)
+  int32_t *done_up;       // [E + n_sh] up tiles of each group finished this iteration
+  int32_t *tile_ctr;      // next tile of the expert kernel (dynamic scheduling)
   int32_t *wl_pos;        // [Nmax*k] expert-sorted worklist positions
   int32_t *slot;          // [Nmax][k] worklist row of selection (f, j)
   void *xp;               // [Nmax*k][H] permuted fresh rows
@@ -55,9 +58,9 @@ struct Work {
   // 128 rows x 64 columns in the 128-byte-swizzled K-major layout the tensor
   // cores read, tile (row block rb, K block kb) at index rb * (K / 64) + kb:
   uint8_t *pk_gu;         // routed W_gate/W_up: [E*I/128][H/64] x (gate tile, up tile) = 32 KB
-  uint8_t *pk_d;          // routed W_down: [E*H/128][I/64] x 16 KB
+  uint8_t *pk_d;          // routed W_down: [E*H/256][I/64] x (two 128-row tiles) = 32 KB
   uint8_t *pk_sgu;        // shared W_gate/W_up: [n_sh*I_s/128][H/64] x 32 KB
-  uint8_t *pk_sd;         // shared W_down: [n_sh*H/128][I_s/64] x 16 KB
+  uint8_t *pk_sd;         // shared W_down: [n_sh*H/256][I_s/64] x 32 KB
   int32_t *blk;           // [kMaxRoutingGrid][kBlkFields] per-CTA partials of the routing kernel
   unsigned int *gbar;     // grid-barrier counter of the routing kernel (zeroed by the gate kernel)
   int64_t *trace;         // [4 kernels][kTraceCtas][8] per-CTA timeline (when tracing)
@@ -160,19 +163,20 @@ cudaError_t launch_down_simt(const Dims &d, const Weights &w, const Work &ws, cu
 
 // gemm_tc.cu (bf16 layers, tcgen05 + TMA)
 // Packs row-major [rows][k] bf16 into swizzled tiles at dst + t * tile_stride + tile_off.
+// Tiles of `pair` consecutive row blocks that share a K block are stored adjacent.
 cudaError_t launch_pack_tiles(const void *src, int64_t rows, int64_t k, uint8_t *dst, int64_t tile_stride,
-                              int64_t tile_off, cudaStream_t s);
+                              int64_t tile_off, int pair, cudaStream_t s);
 bool tma_encode_init();
 bool encode_kmajor_bf16(CUtensorMap *map, const void *base, uint64_t k_elems, uint64_t rows, uint32_t box_rows);
 int tc_gate_splits(const Dims &d);
 constexpr int kTnGate = 128;  // gate token tile (x box rows)
-constexpr int kTnUp = 256;    // grouped-GEMM token tiles
-constexpr int kTnDn = 256;
+constexpr int kTnUp = 128;    // grouped-GEMM token tiles (up and down)
+constexpr int kTnDn = 128;
+constexpr int kBmDn = 256;    // rows of H per down tile (two 128-row MMAs)
 cudaError_t launch_gate_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map,
                            cudaStream_t s);
-cudaError_t launch_up_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map256,
-                         cudaStream_t s);
-cudaError_t launch_down_tc(const Dims &d, const Maps &m, const Work &ws, cudaStream_t s);
+cudaError_t launch_experts_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map_up,
+                              cudaStream_t s);
 
 int num_sms();
 

@@ -20,8 +20,8 @@
 
 namespace epoch {
 
-const char *const kKindName[K_NUM] = {"gate",        "plan_topk",   "plan_support", "routing",
-                                      "expert_up",   "expert_down", "combine",      "wait_test"};
+const char *const kKindName[K_NUM] = {"gate",    "plan_topk",   "plan_support", "routing",
+                                      "experts", "expert_down", "combine",      "wait_test"};
 
 // ---------------------------------------------------------------- helpers
 
@@ -182,33 +182,80 @@ __device__ __forceinline__ bool grid_sync(unsigned int *bar, unsigned int target
   return *s_ok != 0;
 }
 
-// Grouped-GEMM tile lists, written by every warp of the routing grid: groups
-// are the routed experts with rows, then the shared experts over every
-// position; each CTA computes the per-group tile offsets in shared memory
-// (s_bu, s_bd: [G2 + 1]) and warp gw writes the tiles of groups gw, gw + W, ...
-// with its lanes in parallel.
-__device__ void write_tile_lists(const Dims &d, const Work &ws, const int32_t *s_off, int32_t *tmp, int32_t *s_bu,
-                                 int32_t *s_bd, int n) {
-  const int tid = threadIdx.x, lane = lane_id();
+// Grouped-GEMM tile lists, built by one CTA. Groups are the shared experts
+// (over every position) and the routed experts with rows, ordered heaviest
+// first -- shared, then routed by descending row count, lower id first on ties
+// -- so that the expert kernel, which hands tiles out in list order, starts the
+// longest chains first. The order is a single unsigned key per group (shared
+// bit, clamped row count, inverted id: all keys distinct), and a group's rank is
+// the number of larger keys, counted over broadcast 16-byte shared loads. The
+// per-group tile offsets follow from two block scans in rank order (s_bu, s_bd:
+// [G2 + 1]); a thread writes the tiles of one routed group, a warp those of one
+// shared group (rows of every position, many tiles). up_needed[g] is the number
+// of up tiles of group g.
+constexpr int kKeySlots = 1024 + 16;
+__device__ void write_tile_lists(const Dims &d, const Work &ws, const int32_t *s_off, int32_t *tmp, uint32_t *s_key,
+                                 int32_t *s_bu, int32_t *s_bd, int32_t *s_rank, int n, int64_t *trace_r) {
+  const int tid = threadIdx.x, lane = lane_id(), wid = warp_id(), nwarps = kRoutingThreads / 32;
   const int E = d.E, G2 = E + d.n_sh;
+  const int G2p = (G2 + 15) & ~15;
+  auto rows_of = [&](int g) { return g < E ? s_off[g + 1] - s_off[g] : n; };
+  for (int g = tid; g < G2p; g += kRoutingThreads) {
+    uint32_t key = 0u;  // padding: below every group
+    if (g < G2) {
+      const uint32_t rows = static_cast<uint32_t>(min(rows_of(g), (1 << 19) - 1));
+      key = (g >= E ? 1u << 30 : 0u) | (rows << 11) | static_cast<uint32_t>(2047 - g);
+    }
+    s_key[g] = key;
+  }
+  __syncthreads();
+  for (int g = tid; g < G2; g += kRoutingThreads) {
+    const uint32_t mine = s_key[g];
+    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+    const uint4 *k4 = reinterpret_cast<const uint4 *>(s_key);
+    for (int h = 0; h < G2p / 4; h += 4) {
+      const uint4 a = k4[h], b = k4[h + 1], c = k4[h + 2], e = k4[h + 3];
+      r0 += (a.x > mine) + (a.y > mine) + (a.z > mine) + (a.w > mine);
+      r1 += (b.x > mine) + (b.y > mine) + (b.z > mine) + (b.w > mine);
+      r2 += (c.x > mine) + (c.y > mine) + (c.z > mine) + (c.w > mine);
+      r3 += (e.x > mine) + (e.y > mine) + (e.z > mine) + (e.w > mine);
+    }
+    s_rank[g] = r0 + r1 + r2 + r3;
+  }
+  __syncthreads();
+  if (trace_r && tid == 0) trace_r[6] = static_cast<int64_t>(globaltimer_ns());
+  // tile counts in rank order: thread tid owns ranks 2 tid and 2 tid + 1
   int tu[2] = {0, 0}, td[2] = {0, 0}, hit = 0;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int g = 2 * tid + h;
     if (g < G2) {
       const bool routed = g < E;
-      const int rows = routed ? s_off[g + 1] - s_off[g] : n;
+      const int rows = rows_of(g);
       hit += routed && rows > 0;
       if (rows > 0 && d.tn_up > 0) {
-        tu[h] = ((rows + d.tn_up - 1) / d.tn_up) * ((routed ? d.I : d.I_s) / 128);
-        td[h] = ((rows + d.tn_dn - 1) / d.tn_dn) * (d.H / 128);
+        s_bu[s_rank[g]] = ((rows + d.tn_up - 1) / d.tn_up) * ((routed ? d.I : d.I_s) / 128);
+        s_bd[s_rank[g]] = ((rows + d.tn_dn - 1) / d.tn_dn) * (d.H / kBmDn);
+      } else {
+        s_bu[s_rank[g]] = 0;
+        s_bd[s_rank[g]] = 0;
       }
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int r = 2 * tid + h;
+    if (r < G2) {
+      tu[h] = s_bu[r];
+      td[h] = s_bd[r];
     }
   }
   int n_up, n_dn, n_hit;
   const int bu = block_excl_scan(tu[0] + tu[1], tmp, &n_up);
   const int bd = block_excl_scan(td[0] + td[1], tmp, &n_dn);
   (void)block_excl_scan(hit, tmp, &n_hit);
+  // s_bu/s_bd now become offsets by rank
   if (2 * tid < G2) {
     s_bu[2 * tid] = bu;
     s_bd[2 * tid] = bd;
@@ -220,9 +267,6 @@ __device__ void write_tile_lists(const Dims &d, const Work &ws, const int32_t *s
   if (tid == 0) {
     s_bu[G2] = n_up;
     s_bd[G2] = n_dn;
-  }
-  __syncthreads();
-  if (blockIdx.x == 0 && tid == 0) {
     const int up = min(n_up, d.max_tiles_up), dn = min(n_dn, d.max_tiles_dn);
     ws.ctrl->n_hit = n_hit;
     ws.ctrl->tiles_up = up;
@@ -231,33 +275,36 @@ __device__ void write_tile_lists(const Dims &d, const Work &ws, const int32_t *s
     ws.stats->tiles_up = up;
     ws.stats->tiles_down = dn;
   }
-  if (d.tn_up <= 0) return;
-  const int nw = kRoutingThreads / 32;
-  const int W = gridDim.x * nw;
-  for (int g = blockIdx.x * nw + warp_id(); g < G2; g += W) {
-    const bool routed = g < E;
-    const int rows = routed ? s_off[g + 1] - s_off[g] : n;
-    const int r0 = routed ? s_off[g] : 0;
-    if (rows <= 0) continue;
+  __syncthreads();
+  // the tiles of group g: up tiles (m, t) in m-major order, then down tiles
+  auto group_tiles = [&](int g, int q0, int dq) {
+    const int rows = rows_of(g);
+    const int rk = s_rank[g];
+    const int bu0 = s_bu[rk], cu = s_bu[rk + 1] - bu0;
+    const int bd0 = s_bd[rk], cd = s_bd[rk + 1] - bd0;
+    if (q0 == 0) ws.up_needed[g] = cu;
+    if (rows <= 0 || d.tn_up <= 0) return;
+    const int r0 = g < E ? s_off[g] : 0;
     const int ntu = (rows + d.tn_up - 1) / d.tn_up, ntd = (rows + d.tn_dn - 1) / d.tn_dn;
-    const int cu = s_bu[g + 1] - s_bu[g], cd = s_bd[g + 1] - s_bd[g];
-    for (int q = lane; q < cu; q += 32) {
-      const int m = q / ntu, tt = q % ntu;
-      const int slot = s_bu[g] + q;
-      if (slot < d.max_tiles_up)
-        ws.tiles_up[slot] = make_int4(g, m, r0 + tt * d.tn_up, min(d.tn_up, rows - tt * d.tn_up));
+    for (int q = q0; q < cu; q += dq) {
+      const int m = q / ntu, tt = q - m * ntu;
+      if (bu0 + q < d.max_tiles_up)
+        ws.tiles_up[bu0 + q] = make_int4(g, m, r0 + tt * d.tn_up, min(d.tn_up, rows - tt * d.tn_up));
       else
         set_error(ws.err, EPOCH_DEVERR_BOUNDS);
     }
-    for (int q = lane; q < cd; q += 32) {
-      const int m = q / ntd, tt = q % ntd;
-      const int slot = s_bd[g] + q;
-      if (slot < d.max_tiles_dn)
-        ws.tiles_dn[slot] = make_int4(g, m, r0 + tt * d.tn_dn, min(d.tn_dn, rows - tt * d.tn_dn));
+    for (int q = q0; q < cd; q += dq) {
+      const int m = q / ntd, tt = q - m * ntd;
+      if (bd0 + q < d.max_tiles_dn)
+        ws.tiles_dn[bd0 + q] = make_int4(g, m, r0 + tt * d.tn_dn, min(d.tn_dn, rows - tt * d.tn_dn));
       else
         set_error(ws.err, EPOCH_DEVERR_BOUNDS);
     }
-  }
+  };
+  for (int g = tid; g < E; g += kRoutingThreads) group_tiles(g, 0, 1);
+  for (int sh = 0; sh < d.n_sh; ++sh)
+    if (wid == nwarps - 1 - sh % nwarps) group_tiles(E + sh, lane, 32);
+  if (trace_r && tid == 0) trace_r[7] = static_cast<int64_t>(globaltimer_ns());
 }
 
 enum BlkField { B_SLICE = 0, B_REUSE, B_ANOM, B_BAD, B_LIVE, B_NEW, B_MISS, B_STALE };
@@ -297,6 +344,8 @@ __global__ void __launch_bounds__(kRoutingThreads) k_routing(Dims d, Work ws, co
   __shared__ int32_t s_off[1025];
   __shared__ int32_t s_bu[1025];
   __shared__ int32_t s_bd[1025];
+  __shared__ int32_t s_rank[1024];
+  __shared__ __align__(16) uint32_t s_key[kKeySlots];
   __shared__ int s_ok;
   const int G = gridDim.x, b = blockIdx.x, tid = threadIdx.x;
   const int lane = lane_id(), wid = warp_id(), nwarps = kRoutingThreads / 32;
@@ -308,6 +357,8 @@ __global__ void __launch_bounds__(kRoutingThreads) k_routing(Dims d, Work ws, co
   if (tid < kBlkFields) s_cat[tid] = 0;
   for (int q = b * kRoutingThreads + tid; q < E * n_chunks; q += G * kRoutingThreads)
     ws.chunk_mask[static_cast<size_t>(q / n_chunks) * d.cmax + (q % n_chunks)] = 0u;
+  for (int g = b * kRoutingThreads + tid; g < E + d.n_sh; g += G * kRoutingThreads) ws.done_up[g] = 0;
+  if (b == 0 && tid == 0) *ws.tile_ctr = 0;  // the expert kernel hands tiles out from this counter
   // G = split-K partials summed in a fixed order + bias, every position
   if ((E & 3) == 0) {
     const int e4 = E / 4;
@@ -454,30 +505,42 @@ __global__ void __launch_bounds__(kRoutingThreads) k_routing(Dims d, Work ws, co
     if (tid == 0) s_off[E] = tot;
     __syncthreads();
   }
-  for (int pair = b * nwarps + wid; pair < E * fresh_chunks; pair += G * nwarps) {
-    const int e = pair / fresh_chunks, c = pair % fresh_chunks;
-    const uint32_t *row = ws.chunk_mask + static_cast<size_t>(e) * d.cmax;
-    const uint32_t m = row[c];
-    if (m == 0u) continue;
-    int before_c = 0;
-    for (int c2 = lane; c2 < c; c2 += 32) before_c += __popc(row[c2]);
+  // With more than one CTA, CTA 0 builds the statistics and the tile lists
+  // (nothing later in this kernel waits on it) while the others place the
+  // worklist rows, meet at barrier 4 and copy the rows.
+  const bool split = G > 1;
+  const int wb = split ? b - 1 : b, wg = split ? G - 1 : G;  // worker CTAs
+  if (!(split && b == 0)) {
+    for (int pair = wb * nwarps + wid; pair < E * fresh_chunks; pair += wg * nwarps) {
+      const int e = pair / fresh_chunks, c = pair % fresh_chunks;
+      const uint32_t *row = ws.chunk_mask + static_cast<size_t>(e) * d.cmax;
+      const uint32_t m = row[c];
+      if (m == 0u) continue;
+      int before_c = 0;
+      for (int c2 = lane; c2 < c; c2 += 32) before_c += __popc(row[c2]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) before_c += __shfl_xor_sync(0xffffffffu, before_c, o);
-    if ((m >> lane) & 1u) {  // lane p places the edge of fresh position 32 c + p
-      const int f = c * 32 + lane;
-      const int dst = s_off[e] + before_c + __popc(m & ((1u << lane) - 1u));
-      if (dst < 0 || dst >= d.Nmax * k || f >= n_fresh) {
-        set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-      } else {
-        ws.wl_pos[dst] = ws.fresh_pos[f];
-        for (int j = 0; j < k; ++j)
-          if (ws.sel[f * k + j] == e) ws.slot[f * k + j] = dst;
+      for (int o = 16; o > 0; o >>= 1) before_c += __shfl_xor_sync(0xffffffffu, before_c, o);
+      if ((m >> lane) & 1u) {  // lane p places the edge of fresh position 32 c + p
+        const int f = c * 32 + lane;
+        const int dst = s_off[e] + before_c + __popc(m & ((1u << lane) - 1u));
+        if (dst < 0 || dst >= d.Nmax * k || f >= n_fresh) {
+          set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+        } else {
+          ws.wl_pos[dst] = ws.fresh_pos[f];
+          for (int j = 0; j < k; ++j)
+            if (ws.sel[f * k + j] == e) ws.slot[f * k + j] = dst;
+        }
       }
     }
+    if (trace_r && tid == 0) trace_r[4] = static_cast<int64_t>(globaltimer_ns());
+    if (split) {
+      if (!grid_sync(ws.gbar, 3u * G + (G - 1), ws.err, tmo, &s_ok)) return;
+    } else {
+      __syncthreads();
+    }
+  } else if (trace_r && tid == 0) {
+    trace_r[4] = static_cast<int64_t>(globaltimer_ns());
   }
-  if (trace_r && tid == 0) trace_r[4] = static_cast<int64_t>(globaltimer_ns());
-  if (!grid_sync(ws.gbar, 4u * G, ws.err, tmo, &s_ok)) return;
-  // after the last barrier nothing waits on CTA 0: statistics, offsets, tiles
   if (b == 0) {
     // sums of the per-CTA category counts: thread j reads CTA j's record (two
     // 16-byte loads), then a warp-shuffle and shared-memory reduction
@@ -523,12 +586,14 @@ __global__ void __launch_bounds__(kRoutingThreads) k_routing(Dims d, Work ws, co
       if (sum_cat[B_BAD]) set_error(ws.err, EPOCH_DEVERR_FLAGS);
     }
     for (int e = tid; e <= E; e += kRoutingThreads) ws.offsets[e] = s_off[e];
+    if (trace_r && tid == 0) trace_r[5] = static_cast<int64_t>(globaltimer_ns());
+    write_tile_lists(d, ws, s_off, tmp, s_key, s_bu, s_bd, s_rank, n, trace_r);
+    if (split) return;
   }
-  write_tile_lists(d, ws, s_off, tmp, s_bu, s_bd, n);
 
   // ---- phase D: copy each worklist row of x into the compact buffer
   const int n_edges = n_fresh * k;
-  for (int l = b * nwarps + wid; l < n_edges; l += G * nwarps) {
+  for (int l = wb * nwarps + wid; l < n_edges; l += wg * nwarps) {
     const int tp = ws.wl_pos[l];
     if (tp < 0 || tp >= n) {
       if (lane == 0) set_error(ws.err, EPOCH_DEVERR_BOUNDS);
