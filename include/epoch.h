@@ -150,10 +150,16 @@ typedef struct {
   const epoch_iter_stats *stats;
   const uint32_t *error_word;
   /* [4][1024][8] int64 per-CTA timelines of the last launches while tracing is
-   * on (globaltimer ns). Rows 0-2, gate / expert-up / expert-down: entry,
-   * setup done, first operand stage landed, last MMA committed, epilogue done,
-   * tiles processed, valid token columns, SM id. Row 3, routing: entry, then
-   * the end of the classify, compaction, top-k and worklist phases, kernel end. */
+   * on (globaltimer ns). Row 0, gate: entry, setup done, first operand stage
+   * landed, last MMA committed, epilogue done, tiles, valid token columns, SM
+   * id. Row 1, experts: entry, inputs loaded, first stage landed, last MMA
+   * complete, epilogue done, tiles, ns the producer waited for up tiles, SM id.
+   * Row 2, expert epilogue: ns busy, ns waiting for accumulators, longest tile
+   * epilogue in ns, that tile's group (bit 30 set: down tile) and valid rows,
+   * start and end of the last tile's epilogue, SM id. Row 3, routing: entry,
+   * then the ends of the classify, compaction, top-k and worklist phases, the
+   * kernel end; CTA 0 instead records fields 4-6 around the statistics and
+   * the tile prefix it writes. */
   const int64_t *trace;
   /* [2][EPOCH_PROF_KINDS] while tracing: first CTA entry and last CTA exit
    * (globaltimer ns) of each kernel kind in the last iteration, in the order

@@ -75,16 +75,6 @@ int sk_max_for(const epoch_layer_config &c) {
   return kb < 16 ? kb : 16;
 }
 
-// Capacity of the grouped-GEMM tile lists: every group splits into token tiles
-// of tn rows (at most rows/tn + 1 each) times its M tiles of 128.
-void tile_caps(const epoch_layer_config &c, int tn_up, int tn_dn, int *up, int *dn) {
-  const long N = c.max_positions, k = c.top_k, E = c.n_experts, nsh = c.n_shared;
-  const long Is = c.n_shared ? c.shared_inter : 0;
-  *up = static_cast<int>(((N * k + tn_up - 1) / tn_up + E) * (c.inter / 128) +
-                         nsh * ((N + tn_up - 1) / tn_up) * (Is / 128));
-  *dn = static_cast<int>(((N * k + tn_dn - 1) / tn_dn + E + nsh * ((N + tn_dn - 1) / tn_dn)) * (c.hidden / kBmDn));
-}
-
 // Lays the workspace out (base == nullptr: only measures). Returns total bytes.
 size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   size_t off = 0;
@@ -114,13 +104,10 @@ size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   t.chunk_mask = static_cast<uint32_t *>(take(chunks * E * 4));
   t.expert_cnt = static_cast<int32_t *>(take(E * 4));
   t.offsets = static_cast<int32_t *>(take((E + 1) * 4));
-  int cap_up = 0, cap_dn = 0;
-  if (c.dtype == EPOCH_BF16) tile_caps(c, kTnUp, kTnDn, &cap_up, &cap_dn);
-  t.tiles_up = static_cast<int4 *>(take(static_cast<size_t>(cap_up) * 16 + 16));
-  t.tiles_dn = static_cast<int4 *>(take(static_cast<size_t>(cap_dn) * 16 + 16));
-  t.up_needed = static_cast<int32_t *>(take((E + nsh) * 4));
+  t.grp_list = static_cast<int32_t *>(take((E + nsh + 1) * 4));
   t.done_up = static_cast<int32_t *>(take((E + nsh) * 4));
   t.tile_ctr = static_cast<int32_t *>(take(16));
+  t.sh_ctr = static_cast<int32_t *>(take(16));
   t.wl_pos = static_cast<int32_t *>(take(N * k * 4));
   t.slot = static_cast<int32_t *>(take(N * k * 4));
   t.xp = take(N * k * H * act);
@@ -138,6 +125,7 @@ size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   }
   t.blk = static_cast<int32_t *>(take(static_cast<size_t>(kMaxRoutingGrid) * kBlkFields * 4));
   t.gbar = static_cast<unsigned int *>(take(16));
+  t.route_done = static_cast<unsigned int *>(take(16));
   t.trace = static_cast<int64_t *>(take(4ull * kTraceCtas * kTraceFields * 8));
   t.timeline = static_cast<unsigned long long *>(take(2ull * K_NUM * 8));
   t.ctrl = static_cast<Ctrl *>(take(sizeof(Ctrl)));
@@ -250,10 +238,9 @@ epoch_status epoch_layer_create(const epoch_layer_config *cfg, const epoch_layer
   d.SK = 1;
   d.R = cfg->refresh_R;
   d.residual = cfg->residual ? 1 : 0;
-  d.tn_up = L->bf16 ? kTnUp : 0;
-  d.tn_dn = L->bf16 ? kTnDn : 0;
+  d.tn = L->bf16 ? kTnUp : 0;
   d.cmax = (cfg->max_positions + 31) / 32;
-  if (L->bf16) tile_caps(*cfg, kTnUp, kTnDn, &d.max_tiles_up, &d.max_tiles_dn);
+  d.route_ctas = routing_grid();
   d.timeout_ns = 2000000000ll;
   memset(&L->maps, 0, sizeof(L->maps));
   if (L->bf16) {

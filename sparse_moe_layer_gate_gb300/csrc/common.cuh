@@ -32,6 +32,17 @@ __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 // ------------------------------------------------------------------ error word
 __device__ __forceinline__ void set_error(uint32_t *err, uint32_t bits) { atomicOr(err, bits); }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start (prologue: barriers, TMEM, descriptor prefetch)
+// while its predecessor in the stream is still running; pdl_wait() blocks until
+// the predecessor grid has completed and its memory is visible (it returns at
+// once when no predecessor is in flight), so every read of a predecessor's
+// output, and every write the predecessor could still race with, comes after
+// it. pdl_trigger() lets the successor's launch begin once every CTA of this
+// grid has triggered or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t)::"memory");
@@ -196,6 +207,14 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 
 // 32 lanes x 32 bits, 16 consecutive columns per thread: thread l of the warp
 // reads TMEM lane (lane base + l), columns [col, col + 16).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
   asm volatile(

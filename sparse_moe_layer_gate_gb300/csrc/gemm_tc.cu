@@ -33,33 +33,35 @@ namespace epoch {
 constexpr int BM = 128;
 constexpr int BK = 64;
 
-enum Mode { M_GATE = 0, M_UP = 1, M_DOWN = 2 };
+// Rows of the per-CTA trace: 0 gate, 1 experts, 2 expert epilogue (the routing kernel uses row 3).
+constexpr int kTraceRowGate = 0;
+constexpr int kTraceRowExperts = 1;
+constexpr int kTraceRowEpilogue = 2;  // expert-kernel epilogue summary
 
 struct __align__(128) TcParams {
-  CUtensorMap a0;    // GATE: W_r (UP and DOWN stream packed weight tiles instead)
-  CUtensorMap b[4];  // GATE: b[0] = x; UP: Xp; DOWN: A (routed) -- boxes of 32/64/128/256 rows
-  CUtensorMap bs;    // UP: x; DOWN: A (shared) -- box of TN rows
-  CUtensorMap b2[4]; // fused expert kernel: A (routed) for the down tiles
-  CUtensorMap bs2;   // fused expert kernel: A (shared) for the down tiles
+  CUtensorMap a0;    // gate: W_r [E][H]
+  CUtensorMap b[4];  // gate: b[0] = x; experts: Xp (routed up tiles), boxes of 32/64/128/256 rows
+  CUtensorMap bs;    // experts: x (shared up tiles), box of kTnUp rows
+  CUtensorMap b2[4]; // experts: A (routed down tiles), boxes of 32/64/128/256 rows
+  CUtensorMap bs2;   // experts: A (shared down tiles), box of kTnUp rows
   Dims d;
   Work ws;
   int32_t gate_tiles;
 };
 
-template <int MODE, int TN, int STAGES>
-struct Cfg {
-  static constexpr int NA = MODE == M_UP ? 2 : 1;
+template <int TN, int STAGES>
+struct GateCfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = TN * BK * 2;
-  static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES;
-  static constexpr int ACC_COLS = NA * TN;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int ACC_COLS = TN;
   static constexpr int NBUF = 2 * ACC_COLS <= 512 ? 2 : 1;
   static constexpr int USED_COLS = NBUF * ACC_COLS;
   static constexpr int TMEM_COLS = USED_COLS <= 32 ? 32 : USED_COLS <= 64 ? 64 : USED_COLS <= 128 ? 128
                                    : USED_COLS <= 256 ? 256 : 512;
   static constexpr int NBARS = 2 * STAGES + 2 * NBUF + 1;
-  // epilogue staging: per epilogue warp, 32 token columns x 32 rows, padded rows
-  static constexpr int STG_ROW = MODE == M_UP ? 80 : 144;  // bytes per staged column (64 / 128 B + pad)
+  // epilogue staging: per epilogue warp, 32 token columns x 32 fp32 rows, padded
+  static constexpr int STG_ROW = 144;
   static constexpr int STG_BYTES = 32 * STG_ROW;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 4 * STG_BYTES + NBARS * 8 + 16;
   static_assert(TN % 16 == 0 && TN >= 16 && TN <= 256, "MMA N");
@@ -67,90 +69,34 @@ struct Cfg {
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
-struct Tile {
-  const uint8_t *a_src;   // UP/DOWN: first packed weight tile of the (group, m) row block
-  int a_stride;           // bytes between consecutive K blocks of packed weights
-  const CUtensorMap *mb;  // B-operand map (box chosen for the tile)
-  int a_row, b_row;       // rows in the A (weights) and B (tokens) tensor maps
-  int shared;             // group is a shared expert (selects the *s maps)
-  int k0, nk;             // first K element, number of BK blocks
-  int n_valid;            // valid token columns
-  int b_bytes;            // bytes of one B box
-  int out_row0;           // output row of column 0
-  int out_rows;           // rows in the output buffer (bounds check)
-  int ld;                 // output leading dimension
-  int col0;               // output column of MMA row 0
-  int m_limit;            // valid MMA rows
-  void *out;
+struct GateTile {
+  int a_row, b_row;  // rows in the W_r and x tensor maps
+  int k0, nk;        // first K element, number of BK blocks
+  int n_valid;       // valid token columns
+  int out_row0;      // output row of column 0
+  int col0;          // output column of MMA row 0
+  int m_limit;       // valid MMA rows (experts)
+  float *out;
 };
 
-template <int MODE, int TN>
-__device__ __forceinline__ Tile decode(const TcParams &p, int tile) {
+// Gate tile t = (split ks, expert block m, token tile tt), token tiles fastest.
+template <int TN>
+__device__ __forceinline__ GateTile gate_tile(const TcParams &p, int tile) {
   const Dims &d = p.d;
-  const Work &ws = p.ws;
-  Tile t;
-  if (MODE == M_GATE) {
-    const int mt = (d.E + BM - 1) / BM, nt = (d.n_pos + TN - 1) / TN;
-    const int ks = tile / (mt * nt), rem = tile % (mt * nt);
-    const int m = rem / nt, tt = rem % nt;
-    const int kspan = d.H / d.SK;
-    t.mb = &p.b[0];
-    t.a_row = m * BM;
-    t.b_row = tt * TN;
-    t.shared = 0;
-    t.k0 = ks * kspan;
-    t.nk = kspan / BK;
-    t.n_valid = min(TN, d.n_pos - tt * TN);
-    t.b_bytes = TN * BK * 2;
-    t.out_row0 = tt * TN;
-    t.out_rows = d.Nmax;
-    t.ld = d.E;
-    t.col0 = m * BM;
-    t.m_limit = min(BM, d.E - m * BM);
-    t.out = ws.gparts + static_cast<size_t>(ks) * d.Nmax * d.E;
-    return t;
-  }
-  const int4 td = MODE == M_UP ? ws.tiles_up[tile] : ws.tiles_dn[tile];
-  const int g = td.x, m = td.y, r0 = td.z;
-  t.n_valid = td.w;
-  t.shared = g >= d.E;
-  const int s = g - d.E;
-  if (t.shared) {
-    t.mb = &p.bs;
-    t.b_bytes = TN * BK * 2;
-  } else {
-    const int bi = t.n_valid <= 32 ? 0 : t.n_valid <= 64 ? 1 : t.n_valid <= 128 ? 2 : 3;
-    t.mb = &p.b[bi];
-    t.b_bytes = (32 << bi) * BK * 2;  // box rows 32, 64, 128, 256
-  }
+  GateTile t;
+  const int mt = (d.E + BM - 1) / BM, nt = (d.n_pos + TN - 1) / TN;
+  const int ks = tile / (mt * nt), rem = tile % (mt * nt);
+  const int m = rem / nt, tt = rem % nt;
+  const int kspan = d.H / d.SK;
+  t.a_row = m * BM;
+  t.b_row = tt * TN;
+  t.k0 = ks * kspan;
+  t.nk = kspan / BK;
+  t.n_valid = min(TN, d.n_pos - tt * TN);
+  t.out_row0 = tt * TN;
   t.col0 = m * BM;
-  t.m_limit = BM;
-  t.k0 = 0;
-  if (MODE == M_UP) {
-    const int nkb = d.H / BK;
-    const size_t rb = t.shared ? static_cast<size_t>(s) * (d.I_s / BM) + m : static_cast<size_t>(g) * (d.I / BM) + m;
-    t.a_src = (t.shared ? ws.pk_sgu : ws.pk_gu) + rb * nkb * (2 * kTileBytes);
-    t.a_stride = 2 * kTileBytes;
-    t.a_row = t.shared ? s * d.I_s + m * BM : g * d.I + m * BM;
-    t.b_row = r0;
-    t.out_row0 = t.shared ? s * d.Nmax + r0 : r0;
-    t.nk = d.H / BK;
-    t.ld = t.shared ? d.I_s : d.I;
-    t.out = t.shared ? ws.a_sh : ws.a_int;
-    t.out_rows = t.shared ? d.n_sh * d.Nmax : d.Nmax * d.k;
-  } else {
-    const int nkb = (t.shared ? d.I_s : d.I) / BK;
-    const size_t rb = t.shared ? static_cast<size_t>(s) * (d.H / BM) + m : static_cast<size_t>(g) * (d.H / BM) + m;
-    t.a_src = (t.shared ? ws.pk_sd : ws.pk_d) + rb * nkb * kTileBytes;
-    t.a_stride = kTileBytes;
-    t.a_row = t.shared ? s * d.H + m * BM : g * d.H + m * BM;
-    t.b_row = t.shared ? s * d.Nmax + r0 : r0;
-    t.out_row0 = t.b_row;
-    t.nk = (t.shared ? d.I_s : d.I) / BK;
-    t.ld = d.H;
-    t.out = t.shared ? static_cast<void *>(ws.o_sh) : static_cast<void *>(ws.o_int);
-    t.out_rows = t.shared ? d.n_sh * d.Nmax : d.Nmax * d.k;
-  }
+  t.m_limit = min(BM, d.E - m * BM);
+  t.out = p.ws.gparts + static_cast<size_t>(ks) * d.Nmax * d.E;
   return t;
 }
 
@@ -163,14 +109,18 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-template <int MODE, int TN, int STAGES>
-__global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcParams p) {
-  using C = Cfg<MODE, TN, STAGES>;
+template <int TN, int STAGES>
+__global__ void __launch_bounds__(192, 1) k_tc_gate(const __grid_constant__ TcParams p) {
+  using C = GateCfg<TN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base (the 128-byte swizzle pattern repeats every 1024
+  // bytes), offset from the __shared__ array itself so that every pointer
+  // derived from it stays in the shared state space (shared loads and stores,
+  // never ordered behind the epilogue's global stores)
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sA = sbase;                                   // [STAGES][NA] A tiles
-  const uint32_t sB = sbase + STAGES * C::NA * C::A_BYTES;     // [STAGES] B tiles
+  const uint32_t sA = sbase;                          // [STAGES] W_r tiles
+  const uint32_t sB = sbase + STAGES * C::A_BYTES;     // [STAGES] x tiles
   uint8_t *stage_out = smem + STAGES * C::STAGE_BYTES;  // [4][STG_BYTES] epilogue transposes
   uint64_t *bars = reinterpret_cast<uint64_t *>(stage_out + 4 * C::STG_BYTES);
   const uint32_t bar0 = smem_u32(bars);
@@ -184,14 +134,25 @@ __global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcPa
 
   const Dims &d = p.d;
   const Work &ws = p.ws;
-  const KernelMark mark_(d, ws, MODE == M_GATE ? K_GATE : MODE == M_UP ? K_UP : K_DOWN);
-  if (MODE == M_GATE && blockIdx.x == 0 && threadIdx.x == 0) *ws.gbar = 0u;  // next routing launch
-  const int total = MODE == M_GATE ? p.gate_tiles : (MODE == M_UP ? ws.ctrl->tiles_up : ws.ctrl->tiles_dn);
+  const KernelMark mark_(d, ws, K_GATE);
+  pdl_wait();
+  pdl_trigger();  // the routing kernel may start its launch; it waits for this grid to finish
+  if (blockIdx.x == 0) {
+    // counters of the routing and expert kernels that follow: the grid barrier,
+    // and the shared-expert tiles the expert kernel starts before routing ends
+    if (threadIdx.x == 0) {
+      *ws.gbar = 0u;
+      *ws.route_done = 0u;
+      *ws.sh_ctr = 0;
+    }
+    for (int s = threadIdx.x; s < d.n_sh; s += blockDim.x) ws.done_up[d.E + s] = 0;
+  }
+  const int total = p.gate_tiles;
   if (static_cast<int>(blockIdx.x) >= total) return;
   const int wid = warp_id(), lane = lane_id();
   const uint64_t tmo = static_cast<uint64_t>(d.timeout_ns);
   int64_t *trace = (d.trace && blockIdx.x < kTraceCtas)
-                       ? ws.trace + (static_cast<size_t>(MODE) * kTraceCtas + blockIdx.x) * kTraceFields
+                       ? ws.trace + (static_cast<size_t>(kTraceRowGate) * kTraceCtas + blockIdx.x) * kTraceFields
                        : nullptr;
   if (trace && threadIdx.x == 0) {
     uint32_t smid;
@@ -226,7 +187,7 @@ __global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcPa
   if (wid == 0) {
     if (lane == 0) {
       // ---------------- TMA producer
-      if (MODE == M_GATE) tma_prefetch_desc(&p.a0);
+      tma_prefetch_desc(&p.a0);
       tma_prefetch_desc(&p.b[0]);
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_b = policy_evict_last();
@@ -234,10 +195,8 @@ __global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcPa
       uint32_t phase = 0, armed = 0, armed_par = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const Tile t = decode<MODE, TN>(p, tile);
-        const CUtensorMap *ma0 = &p.a0;
-        const CUtensorMap *mb = t.mb;
-        const uint32_t tx = C::NA * C::A_BYTES + t.b_bytes;
+        const GateTile t = gate_tile<TN>(p, tile);
+        const uint32_t tx = C::A_BYTES + C::B_BYTES;
         for (int kb = 0; kb < t.nk; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, ws.err, tmo)) {
             ok = false;
@@ -245,15 +204,8 @@ __global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcPa
           }
           mbar_arrive_expect_tx(full_bar(stage), tx);
           const int kc = t.k0 + kb * BK;
-          const uint32_t a_dst = sA + stage * C::NA * C::A_BYTES;
-          if (MODE == M_GATE) {
-            tma_load_2d(a_dst, ma0, kc, t.a_row, full_bar(stage), pol_w);
-          } else {
-            // packed weights: the stage's A tiles are one contiguous run
-            bulk_load(a_dst, t.a_src + static_cast<size_t>(kb) * t.a_stride, C::NA * C::A_BYTES, full_bar(stage),
-                      pol_w);
-          }
-          tma_load_2d(sB + stage * C::B_BYTES, mb, kc, t.b_row, full_bar(stage), pol_b);
+          tma_load_2d(sA + stage * C::A_BYTES, &p.a0, kc, t.a_row, full_bar(stage), pol_w);
+          tma_load_2d(sB + stage * C::B_BYTES, &p.b[0], kc, t.b_row, full_bar(stage), pol_b);
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -276,7 +228,7 @@ __global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcPa
       bool ok = true, first = true;
       int64_t n_tiles = 0, n_cols = 0;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const Tile t = decode<MODE, TN>(p, tile);
+        const GateTile t = gate_tile<TN>(p, tile);
         const int n_mma = ((t.n_valid + 15) / 16) * 16;
         ++n_tiles;
         n_cols += t.n_valid;
@@ -294,15 +246,12 @@ __global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcPa
             trace[2] = static_cast<int64_t>(globaltimer_ns());
             first = false;
           }
-          const uint32_t a_src = sA + stage * C::NA * C::A_BYTES;
-          const uint64_t ad0 = sw128_kmajor_desc(a_src);
-          const uint64_t ad1 = sw128_kmajor_desc(a_src + C::A_BYTES);
+          const uint64_t ad0 = sw128_kmajor_desc(sA + stage * C::A_BYTES);
           const uint64_t bd = sw128_kmajor_desc(sB + stage * C::B_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint32_t acc = (kb | kk) != 0;
             tc_mma_bf16(d0, ad0 + 2u * kk, bd + 2u * kk, idesc, acc);
-            if (C::NA == 2) tc_mma_bf16(d0 + TN, ad1 + 2u * kk, bd + 2u * kk, idesc, acc);
           }
           tc_commit(empty_bar(stage));
           if (++stage == STAGES) {
@@ -328,55 +277,48 @@ __global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcPa
     __syncwarp();
   } else {
     // ---------------- epilogue (warps 2..5; warp w reads TMEM lanes 32*(w%4)..)
-    // Per 32 token columns: two 32-column TMEM loads and one wait, the values
-    // of this warp's 32 rows staged column-major in shared memory, then lane c
-    // writes token column c's 32 contiguous outputs with 16-byte stores.
+    // Per 32 token columns: one 32-column TMEM load, the values of this warp's
+    // 32 rows staged token by token in shared memory, then eight lanes store
+    // one token's 32 contiguous logits (128 bytes) together, four tokens per
+    // instruction.
     const int q = wid & 3;
     uint8_t *stg = stage_out + (wid - 2) * C::STG_BYTES;
     int buf = 0;
     uint32_t bphase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const Tile t = decode<MODE, TN>(p, tile);
+      const GateTile t = gate_tile<TN>(p, tile);
       if (!mbar_wait_bounded(tfull_bar(buf), bphase, abort_flag, ws.err, tmo)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * C::ACC_COLS);
       const int rows_valid = min(32, max(0, t.m_limit - q * 32));
-      const int esz = MODE == M_UP ? 2 : 4;
-      const bool vec_ok = rows_valid == 32 && ((t.ld * esz) & 15) == 0;
+      const bool vec_ok = rows_valid == 32 && ((d.E * 4) & 15) == 0;
       for (int c0 = 0; c0 < t.n_valid; c0 += 32) {
-        float v0[32], v1[32];
+        float v0[32];
         tmem_ld32(tb + c0, v0);
-        if (C::NA == 2) tmem_ld32(tb + TN + c0, v1);
         tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          if (MODE == M_UP) {
-            reinterpret_cast<__nv_bfloat16 *>(stg + c * C::STG_ROW)[lane] =
-                __float2bfloat16_rn(silu_fast(v0[c]) * v1[c]);
-          } else {
-            reinterpret_cast<float *>(stg + c * C::STG_ROW)[lane] = v0[c];
-          }
-        }
+        for (int c = 0; c < 32; ++c) reinterpret_cast<float *>(stg + c * C::STG_ROW)[lane] = v0[c];
         __syncwarp();
-        const int col = c0 + lane;  // token column written by this lane
-        const int orow = t.out_row0 + col;
-        if (col < t.n_valid) {
-          if (orow < 0 || orow >= t.out_rows) {
-            set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-          } else if (vec_ok) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(stg + lane * C::STG_ROW);
-            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(t.out) +
-                                                   (static_cast<size_t>(orow) * t.ld + t.col0 + q * 32) * esz);
-#pragma unroll
-            for (int v = 0; v < 32 * esz / 16; ++v) dst[v] = src[v];
-          } else {
-            for (int r = 0; r < rows_valid; ++r) {
-              const size_t o = static_cast<size_t>(orow) * t.ld + t.col0 + q * 32 + r;
-              if (MODE == M_UP)
-                static_cast<__nv_bfloat16 *>(t.out)[o] = reinterpret_cast<const __nv_bfloat16 *>(stg + lane * C::STG_ROW)[r];
-              else
-                static_cast<float *>(t.out)[o] = reinterpret_cast<const float *>(stg + lane * C::STG_ROW)[r];
+        const int ncol = min(32, t.n_valid - c0);
+        if (vec_ok) {
+          const int v = lane & 7;
+          for (int c = lane >> 3; c < ncol; c += 4) {
+            const int orow = t.out_row0 + c0 + c;
+            if (orow < 0 || orow >= d.Nmax) {
+              set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+              continue;
             }
+            reinterpret_cast<uint4 *>(t.out + static_cast<size_t>(orow) * d.E + t.col0 + q * 32)[v] =
+                *reinterpret_cast<const uint4 *>(stg + c * C::STG_ROW + v * 16);
+          }
+        } else if (lane < ncol) {
+          const int orow = t.out_row0 + c0 + lane;
+          if (orow < 0 || orow >= d.Nmax) {
+            set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+          } else {
+            for (int r = 0; r < rows_valid; ++r)
+              t.out[static_cast<size_t>(orow) * d.E + t.col0 + q * 32 + r] =
+                  reinterpret_cast<const float *>(stg + lane * C::STG_ROW)[r];
           }
         }
         __syncwarp();
@@ -400,29 +342,96 @@ __global__ void __launch_bounds__(192, 1) k_tc_gemm(const __grid_constant__ TcPa
 
 // ---------------------------------------------------------------- fused expert kernel
 // Up and down projections of every group in one persistent cooperative launch
-// (one CTA per SM). Each CTA takes tiles blockIdx.x, + gridDim.x, ... of the
-// list [all up tiles, then all down tiles]. Both kinds are two 128-row MMAs
-// sharing one token tile of <= 128 tokens: an up tile (group g, 128 rows of I)
-// multiplies the gate and up rows and writes silu(gate) * up as bf16, then
-// counts itself done for g; a down tile (g, 256 rows of H) waits until every up
-// tile of g is done before loading its activations (its weight copies go out
-// first), so the down work of lightly loaded experts runs while heavy up tiles
-// are still streaming, with no launch in between. Every tile uses one
-// 256-column TMEM accumulator buffer, double-buffered; a 48 KB stage holds
-// 32 KB of packed weights (one contiguous run) and a 16 KB token tile.
+// (one CTA per SM). Tiles of the list [all up tiles, then all down tiles] are
+// handed out one at a time from a global counter, so a CTA that drew short
+// tiles draws more. Both kinds are two 128-row MMAs sharing one token tile of
+// <= 128 tokens: an up tile (group g, 128 rows of I) multiplies the gate and up
+// rows and writes silu(gate) * up as bf16, then counts itself done for g; a
+// down tile (g, 256 rows of H) waits until every up tile of g is done before
+// loading its activations (its weight copies go out first), so the down work of
+// lightly loaded experts runs while heavy up tiles are still streaming, with no
+// launch in between. Every tile uses one 256-column TMEM accumulator buffer,
+// double-buffered; a 48 KB stage holds 32 KB of packed weights (one contiguous
+// run) and a 16 KB token tile.
 constexpr int kExpStages = 4;
 constexpr int kExpStage = 48 * 1024;
 constexpr int kExpStg = 32 * 144;  // epilogue staging per warp (fp32 worst case)
-constexpr int kExpSched = 4;  // tile-id ring between the producer and the MMA / epilogue warps
+constexpr int kExpSched = 4;  // decoded-tile ring between the producer and the MMA / epilogue warps
 constexpr int kExpBars = 2 * kExpStages + 2 * 2 + 1 + 2 * kExpSched;
-constexpr int kExpSmem = 1024 + kExpStages * kExpStage + 4 * kExpStg + kExpBars * 8 + 16 + kExpSched * 4;
+constexpr int kExpGroups = 1028;  // capacity of the group list and offset copies (E + n_sh + 1 <= 1025)
+// shared-memory carve-up, from the 1024-aligned base
+constexpr int kExpOffBars = kExpStages * kExpStage + 4 * kExpStg;
+constexpr int kExpOffSlot = kExpOffBars + kExpBars * 8;           // TMEM address, abort flag
+constexpr int kExpOffRing = (kExpOffSlot + 16 + 15) & ~15;        // int4 [kExpSched]
+constexpr int kExpOffPref = kExpOffRing + 16 * kExpSched;         // int32 [kExpGroups] group list
+constexpr int kExpOffOffs = kExpOffPref + 4 * kExpGroups;         // int32 [kExpGroups]
+constexpr int kExpSmem = 1024 + kExpOffOffs + 4 * kExpGroups;
 static_assert(kExpSmem <= 227 * 1024, "shared memory");
+static_assert(kTnUp == kTnDn, "up and down tiles share the token tiling");
+
+// Decoded tile as handed through the ring: x = group | kDownBit for a down
+// tile (-1 ends the stream), y = row block, z = first token row, w = valid rows.
+constexpr int kDownBit = 1 << 30;
+
+// Tile q of the list [all up tiles, then all down tiles] -> decoded tile and
+// the up-tile count of its group. list = the routing kernel's group list:
+// entry p holds the token tiles of the groups before p (<< kGrpIdBits) and the
+// group of p; the shared experts come first (p < n_sh). offs = expert row
+// offsets. Within a group the tiles run row block by row block, token tiles
+// fastest, so tiles drawn close together share a weight row block in L2. Up
+// tiles of the shared experts come first (I_s / 128 row blocks each), then
+// those of the routed experts (I / 128); down tiles have H / 256 row blocks in
+// every group. Returns false when the list and the offsets disagree.
+__device__ __forceinline__ bool locate(const Dims &d, const int32_t *list, const int32_t *offs, int q, int n_up,
+                                      int4 *td, int *need) {
+  const int G2 = d.E + d.n_sh;
+  auto pref = [&](int p) { return list[p] >> kGrpIdBits; };
+  const bool up = q < n_up;
+  int base_q = 0, base_t = 0, mult, lo = 0, hi = G2;
+  if (up) {
+    const int a_sh = (d.I_s / BM) * pref(d.n_sh);
+    if (q < a_sh) {
+      mult = d.I_s / BM;
+      hi = d.n_sh;
+    } else {
+      base_q = a_sh;
+      base_t = pref(d.n_sh);
+      mult = d.I / BM;
+      lo = d.n_sh;
+    }
+  } else {
+    q -= n_up;
+    mult = d.H / kBmDn;
+  }
+  const int key = base_t + (q - base_q) / mult;
+  // largest p in [lo, hi) with pref(p) <= key
+  int l = lo, h = hi;
+  while (h - l > 1) {
+    const int mid = (l + h) >> 1;
+    if (pref(mid) <= key) l = mid;
+    else h = mid;
+  }
+  const int nt = pref(l + 1) - pref(l);
+  const int qq = q - base_q - mult * (pref(l) - base_t);
+  if (nt <= 0 || qq < 0 || qq >= mult * nt) return false;
+  const int m = qq / nt, tt = qq - m * nt;
+  const int g = list[l] & ((1 << kGrpIdBits) - 1);
+  const bool shared = g >= d.E;
+  if (shared != (l < d.n_sh) || g >= G2) return false;
+  const int rows = shared ? d.n_pos : offs[g + 1] - offs[g];
+  const int r0 = (shared ? 0 : offs[g]) + tt * kTnUp;
+  const int n_valid = min(kTnUp, rows - tt * kTnUp);
+  if (n_valid <= 0) return false;
+  *td = make_int4(g | (up ? 0 : kDownBit), m, r0, n_valid);
+  *need = nt * ((shared ? d.I_s : d.I) / BM);
+  return true;
+}
 
 struct XTile {
   bool up;                // up tile (else down)
   int g;                  // group
   const uint8_t *a_src;   // first packed weight tile of the row block
-  int a_bytes;            // weight bytes per K block (32 KB up, 16 KB down)
+  int a_bytes;            // weight bytes per K block (32 KB: two 128-row tiles)
   int nk;                 // K blocks
   const CUtensorMap *mb;  // token-operand map (box chosen for the tile)
   int b_row, b_bytes;
@@ -431,13 +440,12 @@ struct XTile {
   void *out;
 };
 
-__device__ __forceinline__ XTile xdecode(const TcParams &p, int tile, int n_up) {
+__device__ __forceinline__ XTile xdecode(const TcParams &p, int4 td) {
   const Dims &d = p.d;
   const Work &ws = p.ws;
   XTile t;
-  t.up = tile < n_up;
-  const int4 td = t.up ? ws.tiles_up[tile] : ws.tiles_dn[tile - n_up];
-  const int g = td.x, m = td.y, r0 = td.z;
+  t.up = (td.x & kDownBit) == 0;
+  const int g = td.x & (kDownBit - 1), m = td.y, r0 = td.z;
   t.g = g;
   t.n_valid = td.w;
   const bool shared = g >= d.E;
@@ -451,7 +459,7 @@ __device__ __forceinline__ XTile xdecode(const TcParams &p, int tile, int n_up) 
     t.a_bytes = 2 * kTileBytes;
     t.nk = nkb;
     t.mb = shared ? &p.bs : &p.b[bi];
-    t.b_bytes = (shared ? d.tn_up : (32 << bi)) * BK * 2;
+    t.b_bytes = (shared ? kTnUp : (32 << bi)) * BK * 2;
     t.b_row = r0;
     t.out_row0 = shared ? s * d.Nmax + r0 : r0;
     t.ld = shared ? d.I_s : d.I;
@@ -461,13 +469,13 @@ __device__ __forceinline__ XTile xdecode(const TcParams &p, int tile, int n_up) 
     // 256 rows of H: two 128-row blocks sharing the token tile; the packed pair
     // of a K block is one contiguous 32 KB run
     const int nkb = (shared ? d.I_s : d.I) / BK;
-    const size_t pb = shared ? static_cast<size_t>(s) * (d.H / (2 * BM)) + m : static_cast<size_t>(g) * (d.H / (2 * BM)) + m;
+    const size_t pb = shared ? static_cast<size_t>(s) * (d.H / kBmDn) + m : static_cast<size_t>(g) * (d.H / kBmDn) + m;
     t.a_src = (shared ? ws.pk_sd : ws.pk_d) + pb * nkb * (2 * kTileBytes);
     t.a_bytes = 2 * kTileBytes;
     t.nk = nkb;
-    t.col0 = m * 2 * BM;
+    t.col0 = m * kBmDn;
     t.mb = shared ? &p.bs2 : &p.b2[bi];
-    t.b_bytes = (shared ? d.tn_dn : (32 << bi)) * BK * 2;
+    t.b_bytes = (shared ? kTnDn : (32 << bi)) * BK * 2;
     t.b_row = shared ? s * d.Nmax + r0 : r0;
     t.out_row0 = t.b_row;
     t.ld = d.H;
@@ -479,10 +487,14 @@ __device__ __forceinline__ XTile xdecode(const TcParams &p, int tile, int n_up) 
 
 __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base (the 128-byte swizzle pattern repeats every 1024
+  // bytes), offset from the __shared__ array itself so that every pointer
+  // derived from it stays in the shared state space (shared loads and stores,
+  // never ordered behind the epilogue's global stores)
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   uint8_t *stage_out = smem + kExpStages * kExpStage;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(stage_out + 4 * kExpStg);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kExpOffBars);
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kExpStages + s); };
@@ -491,19 +503,19 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
   const uint32_t done_bar = bar0 + 8u * (2 * kExpStages + 4);
   auto sfull_bar = [&](int i) { return bar0 + 8u * (2 * kExpStages + 5 + i); };
   auto sempty_bar = [&](int i) { return bar0 + 8u * (2 * kExpStages + 5 + kExpSched + i); };
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kExpBars);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kExpOffSlot);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  volatile int *s_tile = reinterpret_cast<volatile int *>(tmem_slot + 4);  // [kExpSched]
+  int4 *s_td = reinterpret_cast<int4 *>(smem + kExpOffRing);
+  int32_t *s_list = reinterpret_cast<int32_t *>(smem + kExpOffPref);
+  int32_t *s_offs = reinterpret_cast<int32_t *>(smem + kExpOffOffs);
 
   const Dims &d = p.d;
   const Work &ws = p.ws;
   const KernelMark mark_(d, ws, K_UP);
-  const int n_up = ws.ctrl->tiles_up;
-  const int total = n_up + ws.ctrl->tiles_dn;
   const int wid = warp_id(), lane = lane_id();
   const uint64_t tmo = static_cast<uint64_t>(d.timeout_ns);
   int64_t *trace = (d.trace && blockIdx.x < kTraceCtas)
-                       ? ws.trace + (static_cast<size_t>(M_UP) * kTraceCtas + blockIdx.x) * kTraceFields
+                       ? ws.trace + (static_cast<size_t>(kTraceRowExperts) * kTraceCtas + blockIdx.x) * kTraceFields
                        : nullptr;
   if (trace && threadIdx.x == 0) {
     uint32_t smid;
@@ -532,98 +544,152 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
+  pdl_trigger();  // the combine kernel may start its launch; it waits for this grid to finish
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   if (trace && threadIdx.x == 0) trace[1] = static_cast<int64_t>(globaltimer_ns());
+  // The shared experts' up tiles read only x and their weights: they are drawn
+  // from sh_ctr (zeroed by the gate kernel, like their done counters) while the
+  // routing kernel may still run, so the longest dependency chain of the
+  // iteration starts early. Every other tile -- routed up tiles, then the down
+  // tiles of every group -- is drawn from tile_ctr after the producer has seen
+  // every routing CTA finish (the route_done count) and loaded the group list
+  // and expert offsets.
+  const int nt_sh = (d.n_pos + kTnUp - 1) / kTnUp;
+  const int a_sh = d.n_sh * nt_sh * (d.I_s / BM);  // shared up tiles (the first of the full list)
 
   if (wid == 0) {
+    // ---------------- producer: weight bulk copies + token TMA loads (lane 0)
+    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_b = policy_evict_last();
+    int stage = 0, j = 0;
+    uint32_t phase = 0, armed = 0, armed_par = 0;
+    bool ok = true;
+    uint64_t waited = 0;
+    // Issues the operand copies of one tile; a down tile first waits until every
+    // up tile of its group (`need` of them) has written its activations.
+    auto issue = [&](const int4 &td, int need) -> bool {
+      const XTile t = xdecode(p, td);
+      const uint32_t tx = t.a_bytes + t.b_bytes;
+      // a down tile's weights do not depend on the up tiles: its first stages'
+      // weight copies go out before the dependency wait, their token loads after
+      const int pre = t.up ? 0 : min(t.nk, 2);
+      int pre_stage[2] = {0, 0};
+      for (int kb = 0; kb < pre; ++kb) {
+        if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, ws.err, tmo)) return false;
+        mbar_arrive_expect_tx(full_bar(stage), tx);
+        bulk_load(sbase + stage * kExpStage, t.a_src + static_cast<size_t>(kb) * t.a_bytes, t.a_bytes,
+                  full_bar(stage), pol_w);
+        pre_stage[kb] = stage;
+        armed |= 1u << stage;
+        armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == kExpStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!t.up) {
+        const uint64_t t0 = globaltimer_ns();
+        for (;;) {
+          int done;
+          asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(done) : "l"(ws.done_up + t.g) : "memory");
+          if (done >= need) break;
+          if (*abort_flag) return false;
+          if (globaltimer_ns() - t0 > tmo) {
+            set_error(ws.err, EPOCH_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+            return false;
+          }
+          __nanosleep(64);
+        }
+        waited += globaltimer_ns() - t0;
+        asm volatile("fence.proxy.async.global;" ::: "memory");  // generic writes -> TMA reads
+        for (int kb = 0; kb < pre; ++kb)
+          tma_load_2d(sbase + pre_stage[kb] * kExpStage + 2 * kTileBytes, t.mb, kb * BK, t.b_row,
+                      full_bar(pre_stage[kb]), pol_b);
+      }
+      for (int kb = pre; kb < t.nk; ++kb) {
+        if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, ws.err, tmo)) return false;
+        mbar_arrive_expect_tx(full_bar(stage), tx);
+        const uint32_t st = sbase + stage * kExpStage;
+        bulk_load(st, t.a_src + static_cast<size_t>(kb) * t.a_bytes, t.a_bytes, full_bar(stage), pol_w);
+        tma_load_2d(st + 2 * kTileBytes, t.mb, kb * BK, t.b_row, full_bar(stage), pol_b);
+        armed |= 1u << stage;
+        armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == kExpStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      return true;
+    };
     if (lane == 0) {
-      // ---------------- producer: weight bulk copies + token TMA loads
+      tma_prefetch_desc(&p.bs);
       tma_prefetch_desc(&p.b[0]);
       tma_prefetch_desc(&p.b2[0]);
-      const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_b = policy_evict_last();
-      int stage = 0;
-      uint32_t phase = 0, armed = 0, armed_par = 0;
-      bool ok = true;
-      uint64_t waited = 0;
-      for (int j = 0; ok; ++j) {
-        // next tile from the global counter, handed to the MMA and epilogue warps
+      // shared up tiles, before the routing kernel has finished
+      for (; ok; ++j) {
+        const int slot = j % kExpSched;
+        if (!mbar_wait_bounded(sempty_bar(slot), ((j / kExpSched) & 1) ^ 1u, abort_flag, ws.err, tmo)) {
+          ok = false;
+          break;
+        }
+        const int tile = atomicAdd(ws.sh_ctr, 1);
+        if (tile >= a_sh) break;  // slot j stays free for the next phase
+        const int per = nt_sh * (d.I_s / BM);
+        const int sidx = tile / per, qq = tile - sidx * per, m = qq / nt_sh, tt = qq - m * nt_sh;
+        const int4 td = make_int4(d.E + sidx, m, tt * kTnUp, min(kTnUp, d.n_pos - tt * kTnUp));
+        s_td[slot] = td;
+        mbar_arrive(sfull_bar(slot));
+        ok = issue(td, 0);
+      }
+    }
+    // wait until every routing CTA has counted itself done (acquire: its writes
+    // are visible to this warp after the __syncwarp)
+    if (lane == 0 && ok) {
+      const uint64_t t0 = globaltimer_ns();
+      for (;;) {
+        unsigned int v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ws.route_done) : "memory");
+        if (v >= static_cast<unsigned int>(d.route_ctas)) break;
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        if (globaltimer_ns() - t0 > tmo) {
+          set_error(ws.err, EPOCH_DEVERR_TIMEOUT);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        __nanosleep(32);
+      }
+    }
+    __syncwarp();
+    for (int i = lane; i <= d.E + d.n_sh; i += 32) s_list[i] = ws.grp_list[i];
+    for (int i = lane; i <= d.E; i += 32) s_offs[i] = ws.offsets[i];
+    const int n_up = ws.ctrl->tiles_up;
+    const int total = n_up + ws.ctrl->tiles_dn - a_sh;  // tiles drawn from tile_ctr
+    __syncwarp();
+    if (lane == 0) {
+      if (trace) trace[2] = static_cast<int64_t>(globaltimer_ns());
+      for (; ok; ++j) {
         const int slot = j % kExpSched;
         if (!mbar_wait_bounded(sempty_bar(slot), ((j / kExpSched) & 1) ^ 1u, abort_flag, ws.err, tmo)) break;
-        int tile = atomicAdd(ws.tile_ctr, 1);
-        if (tile >= total) tile = -1;
-        s_tile[slot] = tile;
+        const int tile = atomicAdd(ws.tile_ctr, 1);
+        int4 td = make_int4(-1, 0, 0, 0);
+        int need = 0;
+        if (tile < total && !locate(d, s_list, s_offs, tile + a_sh, n_up, &td, &need)) {
+          set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+          *abort_flag = 1;
+          td.x = -1;
+        }
+        s_td[slot] = td;
         mbar_arrive(sfull_bar(slot));
-        if (tile < 0) break;
-        const XTile t = xdecode(p, tile, n_up);
-        const uint32_t tx = t.a_bytes + t.b_bytes;
-        // a down tile's weights do not depend on the up tiles: its first stages'
-        // weight copies go out before the dependency wait, their token loads after
-        const int pre = t.up ? 0 : min(t.nk, 2);
-        int pre_stage[2] = {0, 0};
-        for (int kb = 0; kb < pre; ++kb) {
-          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, ws.err, tmo)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(full_bar(stage), tx);
-          bulk_load(sbase + stage * kExpStage, t.a_src + static_cast<size_t>(kb) * t.a_bytes, t.a_bytes,
-                    full_bar(stage), pol_w);
-          pre_stage[kb] = stage;
-          armed |= 1u << stage;
-          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-          if (++stage == kExpStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        if (!t.up) {
-          // wait until every up tile of this group has written its activations
-          const int need = ws.up_needed[t.g];
-          const uint64_t t0 = globaltimer_ns();
-          for (;;) {
-            int done;
-            asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(done) : "l"(ws.done_up + t.g) : "memory");
-            if (done >= need) break;
-            if (*abort_flag) {
-              ok = false;
-              break;
-            }
-            if (globaltimer_ns() - t0 > tmo) {
-              set_error(ws.err, EPOCH_DEVERR_TIMEOUT);
-              *abort_flag = 1;
-              ok = false;
-              break;
-            }
-            __nanosleep(64);
-          }
-          if (!ok) break;
-          waited += globaltimer_ns() - t0;
-          asm volatile("fence.proxy.async.global;" ::: "memory");  // generic writes -> TMA reads
-          for (int kb = 0; kb < pre; ++kb)
-            tma_load_2d(sbase + pre_stage[kb] * kExpStage + 2 * kTileBytes, t.mb, kb * BK, t.b_row,
-                        full_bar(pre_stage[kb]), pol_b);
-        }
-        for (int kb = pre; kb < t.nk; ++kb) {
-          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, ws.err, tmo)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(full_bar(stage), tx);
-          const uint32_t st = sbase + stage * kExpStage;
-          bulk_load(st, t.a_src + static_cast<size_t>(kb) * t.a_bytes, t.a_bytes, full_bar(stage), pol_w);
-          tma_load_2d(st + 2 * kTileBytes, t.mb, kb * BK, t.b_row, full_bar(stage), pol_b);
-          armed |= 1u << stage;
-          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-          if (++stage == kExpStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
+        if (td.x < 0) break;
+        ok = issue(td, need);
       }
       if (!ok) {
         for (int s = 0; s < kExpStages; ++s)
@@ -637,15 +703,15 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
       // ---------------- MMA issuer
       int stage = 0, buf = 0;
       uint32_t phase = 0, bphase = 0;
-      bool ok = true, first = true;
+      bool ok = true;
       int64_t n_tiles = 0;
       for (int j = 0; ok; ++j) {
         const int slot = j % kExpSched;
         if (!mbar_wait_bounded(sfull_bar(slot), (j / kExpSched) & 1, abort_flag, ws.err, tmo)) break;
-        const int tile = s_tile[slot];
+        const int4 td = s_td[slot];
         mbar_arrive(sempty_bar(slot));
-        if (tile < 0) break;
-        const XTile t = xdecode(p, tile, n_up);
+        if (td.x < 0) break;
+        const XTile t = xdecode(p, td);
         const int n_mma = ((t.n_valid + 15) / 16) * 16;
         const uint32_t idesc = idesc_bf16_f32(BM, n_mma);
         ++n_tiles;
@@ -659,10 +725,6 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
             break;
           }
           tc_fence_after();
-          if (trace && first) {
-            trace[2] = static_cast<int64_t>(globaltimer_ns());
-            first = false;
-          }
           const uint32_t st = sbase + stage * kExpStage;
           const uint64_t ad0 = sw128_kmajor_desc(st);
           const uint64_t ad1 = sw128_kmajor_desc(st + kTileBytes);
@@ -700,16 +762,21 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
     uint8_t *stg = stage_out + (wid - 2) * kExpStg;
     int buf = 0;
     uint32_t bphase = 0;
+    // epilogue trace (warp 2): ns busy, ns waiting for accumulators, longest tile
+    const bool etr = trace != nullptr && wid == 2;
+    int64_t e_busy = 0, e_wait = 0, e_max = 0, e_max_x = 0, e_max_n = 0, e_last0 = 0, e_last1 = 0;
     for (int j = 0;; ++j) {
       const int slot = j % kExpSched;
       if (!mbar_wait_bounded(sfull_bar(slot), (j / kExpSched) & 1, abort_flag, ws.err, tmo)) break;
-      const int tile = s_tile[slot];
+      const int4 td = s_td[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(sempty_bar(slot));
-      if (tile < 0) break;
-      const XTile t = xdecode(p, tile, n_up);
+      if (td.x < 0) break;
+      const XTile t = xdecode(p, td);
+      const int64_t tw0 = etr ? static_cast<int64_t>(globaltimer_ns()) : 0;
       if (!mbar_wait_bounded(tfull_bar(buf), bphase, abort_flag, ws.err, tmo)) break;
       tc_fence_after();
+      const int64_t tw1 = etr ? static_cast<int64_t>(globaltimer_ns()) : 0;
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * 256);
       const int esz = t.up ? 2 : 4;
       const int row_bytes = t.up ? 80 : 144;
@@ -717,38 +784,54 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
       const int halves = t.up ? 1 : 2;  // down: the two 128-row blocks are two output column blocks
       for (int hb = 0; hb < halves; ++hb) {
         for (int c0 = 0; c0 < t.n_valid; c0 += 32) {
-          float v0[32];
-          tmem_ld32(tb + hb * 128 + c0, v0);
-          if (t.up) {
-            float v1[32];
-            tmem_ld32(tb + 128 + c0, v1);
-            tmem_ld_wait();
+          const int ncol = min(32, t.n_valid - c0);
+          // stage the valid token columns 8 at a time: the loop body is short, so
+          // the epilogue fetches few instruction lines when it runs cold (it runs
+          // once per tile, while the memory system is saturated by weight reads)
+#pragma unroll 1
+          for (int cc = 0; cc < ncol; cc += 8) {
+            float a[8];
+            tmem_ld8(tb + hb * 128 + c0 + cc, a);
+            if (t.up) {
+              float b[8];
+              tmem_ld8(tb + 128 + c0 + cc, b);
+              tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-              reinterpret_cast<__nv_bfloat16 *>(stg + c * row_bytes)[lane] =
-                  __float2bfloat16_rn(silu_fast(v0[c]) * v1[c]);
-          } else {
-            tmem_ld_wait();
+              for (int c = 0; c < 8; ++c)
+                reinterpret_cast<__nv_bfloat16 *>(stg + (cc + c) * row_bytes)[lane] =
+                    __float2bfloat16_rn(silu_fast(a[c]) * b[c]);
+            } else {
+              tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) reinterpret_cast<float *>(stg + c * row_bytes)[lane] = v0[c];
+              for (int c = 0; c < 8; ++c) reinterpret_cast<float *>(stg + (cc + c) * row_bytes)[lane] = a[c];
+            }
           }
           __syncwarp();
-          const int col = c0 + lane;
-          const int orow = t.out_row0 + col;
-          if (col < t.n_valid) {
+          const size_t col_off = static_cast<size_t>(t.col0 + hb * 128 + q * 32);
+          if (vec_ok) {
+            // a token's 32 outputs of this warp are 32 * esz contiguous bytes: `per`
+            // lanes store them together, so one instruction writes whole lines of
+            // 32 / per tokens
+            const int per = 2 * esz, v = lane % per;
+            for (int c = lane / per; c < ncol; c += 32 / per) {
+              const int orow = t.out_row0 + c0 + c;
+              if (orow < 0 || orow >= t.out_rows) {
+                set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+                continue;
+              }
+              *reinterpret_cast<uint4 *>(static_cast<uint8_t *>(t.out) +
+                                         (static_cast<size_t>(orow) * t.ld + col_off) * esz + v * 16) =
+                  *reinterpret_cast<const uint4 *>(stg + c * row_bytes + v * 16);
+            }
+          } else if (lane < ncol) {
+            const int orow = t.out_row0 + c0 + lane;
             if (orow < 0 || orow >= t.out_rows) {
               set_error(ws.err, EPOCH_DEVERR_BOUNDS);
             } else {
-              uint8_t *dst = static_cast<uint8_t *>(t.out) +
-                             (static_cast<size_t>(orow) * t.ld + t.col0 + hb * 128 + q * 32) * esz;
+              uint8_t *dst = static_cast<uint8_t *>(t.out) + (static_cast<size_t>(orow) * t.ld + col_off) * esz;
               const uint8_t *src = stg + lane * row_bytes;
-              if (vec_ok) {
-                for (int v = 0; v < 32 * esz / 16; ++v)
-                  reinterpret_cast<uint4 *>(dst)[v] = reinterpret_cast<const uint4 *>(src)[v];
-              } else {
-                for (int b = 0; b < 32 * esz; b += 2)
-                  *reinterpret_cast<uint16_t *>(dst + b) = *reinterpret_cast<const uint16_t *>(src + b);
-              }
+              for (int b = 0; b < 32 * esz; b += 2)
+                *reinterpret_cast<uint16_t *>(dst + b) = *reinterpret_cast<const uint16_t *>(src + b);
             }
           }
           __syncwarp();
@@ -765,12 +848,35 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
           atomicAdd(ws.done_up + t.g, 1);
         }
       }
+      if (etr) {
+        const int64_t tw2 = static_cast<int64_t>(globaltimer_ns());
+        e_wait += tw1 - tw0;
+        e_busy += tw2 - tw1;
+        if (tw2 - tw1 > e_max) {
+          e_max = tw2 - tw1;
+          e_max_x = td.x;
+          e_max_n = td.w;
+        }
+        e_last0 = tw1;
+        e_last1 = tw2;
+      }
       if (++buf == 2) {
         buf = 0;
         bphase ^= 1u;
       }
     }
-    if (trace && wid == 2 && lane == 0) trace[4] = static_cast<int64_t>(globaltimer_ns());
+    if (etr && lane == 0) {
+      trace[4] = static_cast<int64_t>(globaltimer_ns());
+      int64_t *tr2 = ws.trace + (static_cast<size_t>(kTraceRowEpilogue) * kTraceCtas + blockIdx.x) * kTraceFields;
+      tr2[0] = e_busy;
+      tr2[1] = e_wait;
+      tr2[2] = e_max;
+      tr2[3] = e_max_x;
+      tr2[4] = e_max_n;
+      tr2[5] = e_last0;
+      tr2[6] = e_last1;
+      tr2[7] = trace[7];
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -863,18 +969,17 @@ int tc_gate_splits(const Dims &d) {
   return sk;
 }
 
-template <int MODE, int TN, int STAGES>
-static cudaError_t launch_tc(const TcParams &p, int grid, cudaStream_t s) {
-  using C = Cfg<MODE, TN, STAGES>;
+template <int TN, int STAGES>
+static cudaError_t launch_gate(const TcParams &p, int grid, cudaStream_t s) {
+  using C = GateCfg<TN, STAGES>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(k_tc_gemm<MODE, TN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e == cudaSuccess) e = prefer_max_shared(k_tc_gemm<MODE, TN, STAGES>);
+    cudaError_t e = cudaFuncSetAttribute(k_tc_gate<TN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e == cudaSuccess) e = prefer_max_shared(k_tc_gate<TN, STAGES>);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  k_tc_gemm<MODE, TN, STAGES><<<grid, 192, C::SMEM, s>>>(p);
+  k_tc_gate<TN, STAGES><<<grid, 192, C::SMEM, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -893,7 +998,7 @@ cudaError_t launch_gate_tc(const Dims &d, const Maps &m, const Work &ws, const C
   const int tiles = ((d.E + BM - 1) / BM) * ((d.n_pos + kTnGate - 1) / kTnGate) * d.SK;
   p.gate_tiles = tiles;
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  return launch_tc<M_GATE, kTnGate, kStGate>(p, grid, s);
+  return launch_gate<kTnGate, kStGate>(p, grid, s);
 }
 
 cudaError_t launch_experts_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map_up,
@@ -913,10 +1018,14 @@ cudaError_t launch_experts_tc(const Dims &d, const Maps &m, const Work &ws, cons
   }
   p.bs = x_map_up;
   p.bs2 = m.a_sh;
-  // every CTA must be resident: down tiles wait for up tiles of other CTAs
+  // Down tiles wait for up tiles of other CTAs, but never for a CTA that has
+  // not started: tiles are drawn from one increasing counter and every up tile
+  // precedes every down tile, so each awaited up tile is held by a running CTA
+  // whose MMA and epilogue finish it independently of its producer's waits.
+  // The launch therefore needs no co-residency guarantee.
   void *args[] = {&p};
-  return cudaLaunchCooperativeKernel(reinterpret_cast<void *>(k_tc_experts), dim3(num_sms()), dim3(192), args,
-                                     kExpSmem, s);
+  return launch_kernel(reinterpret_cast<void *>(k_tc_experts), dim3(num_sms()), dim3(192), kExpSmem, s, args, false,
+                       true);
 }
 
 }  // namespace epoch

@@ -42,11 +42,12 @@ struct Work {
   uint32_t *chunk_mask;   // [E][cmax] bit p of word c: fresh position 32c + p selected expert e
   int32_t *expert_cnt;    // [E] worklist rows of each expert
   int32_t *offsets;       // [E+1]
-  int4 *tiles_up;         // [max_tiles_up] {group, m tile, first row, valid rows}
-  int4 *tiles_dn;         // [max_tiles_dn]
-  int32_t *up_needed;     // [E + n_sh] up tiles of each group (down tiles wait for all of them)
-  int32_t *done_up;       // [E + n_sh] up tiles of each group finished this iteration
-  int32_t *tile_ctr;      // next tile of the expert kernel (dynamic scheduling)
+  int32_t *grp_list;      // [E + n_sh + 1] expert-kernel groups in list order: token tiles of the
+                          // groups before << kGrpIdBits | group (shared experts E..E+n_sh-1)
+  int32_t *done_up;       // [E + n_sh] up tiles of each group finished this iteration (by group id;
+                          // routed entries zeroed by the routing kernel, shared ones by the gate kernel)
+  int32_t *tile_ctr;      // next routed-up or down tile of the expert kernel (zeroed by the routing kernel)
+  int32_t *sh_ctr;        // next shared-expert up tile of the expert kernel (zeroed by the gate kernel)
   int32_t *wl_pos;        // [Nmax*k] expert-sorted worklist positions
   int32_t *slot;          // [Nmax][k] worklist row of selection (f, j)
   void *xp;               // [Nmax*k][H] permuted fresh rows
@@ -63,6 +64,7 @@ struct Work {
   uint8_t *pk_sd;         // shared W_down: [n_sh*H/256][I_s/64] x 32 KB
   int32_t *blk;           // [kMaxRoutingGrid][kBlkFields] per-CTA partials of the routing kernel
   unsigned int *gbar;     // grid-barrier counter of the routing kernel (zeroed by the gate kernel)
+  unsigned int *route_done;  // routing CTAs finished (zeroed by the gate kernel)
   int64_t *trace;         // [4 kernels][kTraceCtas][8] per-CTA timeline (when tracing)
   unsigned long long *timeline;  // [2][K_NUM]: first CTA entry, last CTA exit per kernel kind (ns)
   Ctrl *ctrl;
@@ -89,10 +91,10 @@ struct Dims {
   int32_t n_pos;
   int32_t iter;
   int32_t host_fallback;
-  int32_t tn_up, tn_dn;  // token-tile width of the tcgen05 grouped GEMMs (0 on the SIMT path)
+  int32_t tn;            // token-tile width of the tcgen05 expert kernel (0 on the SIMT path)
   int32_t cmax;          // chunk capacity: ceil(Nmax / 32)
-  int32_t max_tiles_up, max_tiles_dn;
   int32_t trace;         // nonzero: tcgen05 kernels record per-CTA timelines
+  int32_t route_ctas;    // CTAs of the routing launch (routing_grid())
   int64_t timeout_ns;
 };
 
@@ -170,14 +172,24 @@ bool tma_encode_init();
 bool encode_kmajor_bf16(CUtensorMap *map, const void *base, uint64_t k_elems, uint64_t rows, uint32_t box_rows);
 int tc_gate_splits(const Dims &d);
 constexpr int kTnGate = 128;  // gate token tile (x box rows)
-constexpr int kTnUp = 128;    // grouped-GEMM token tiles (up and down)
+constexpr int kTnUp = 128;    // expert-kernel token tiles (up and down)
 constexpr int kTnDn = 128;
 constexpr int kBmDn = 256;    // rows of H per down tile (two 128-row MMAs)
+constexpr int kGrpIdBits = 11;  // group id field of a grp_list entry (E + n_sh <= 1024 < 2^11)
 cudaError_t launch_gate_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map,
                            cudaStream_t s);
 cudaError_t launch_experts_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map_up,
                               cudaStream_t s);
 
 int num_sms();
+int routing_grid();
+
+// cudaLaunchKernelEx of `fn`: cooperative (every CTA co-resident, for grid
+// barriers) and/or programmatic (may start before the previous kernel in the
+// stream ends; the kernel calls pdl_wait before touching its inputs). When the
+// driver rejects a programmatic launch the kernel is launched once more
+// without it, and later launches of this process skip it.
+cudaError_t launch_kernel(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void **args,
+                          bool cooperative, bool programmatic);
 
 }  // namespace epoch

@@ -59,8 +59,15 @@ __device__ __forceinline__ int block_excl_scan(int v, int *warp_tmp, int *total)
 // split H, fixed-order reduction (deterministic).
 template <typename T>
 __global__ void k_gate_simt(Dims d, const T *__restrict__ x, const T *__restrict__ wr, float *__restrict__ g,
-                            unsigned int *gbar) {
-  if (blockIdx.x == 0 && threadIdx.x == 0) *gbar = 0u;  // grid barrier of the next routing launch
+                            Work ws) {
+  if (blockIdx.x == 0) {  // counters of the next routing and expert launches
+    if (threadIdx.x == 0) {
+      *ws.gbar = 0u;
+      *ws.route_done = 0u;
+      *ws.sh_ctr = 0;
+    }
+    for (int s = threadIdx.x; s < d.n_sh; s += blockDim.x) ws.done_up[d.E + s] = 0;
+  }
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int lane = lane_id();
   for (int o = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; o < d.n_pos * d.E; o += warps) {
@@ -182,92 +189,76 @@ __device__ __forceinline__ bool grid_sync(unsigned int *bar, unsigned int target
   return *s_ok != 0;
 }
 
-// Grouped-GEMM tile lists, built by one CTA. Groups are the shared experts
-// (over every position) and the routed experts with rows, ordered heaviest
-// first -- shared, then routed by descending row count, lower id first on ties
-// -- so that the expert kernel, which hands tiles out in list order, starts the
-// longest chains first. The order is a single unsigned key per group (shared
-// bit, clamped row count, inverted id: all keys distinct), and a group's rank is
-// the number of larger keys, counted over broadcast 16-byte shared loads. The
-// per-group tile offsets follow from two block scans in rank order (s_bu, s_bd:
-// [G2 + 1]); a thread writes the tiles of one routed group, a warp those of one
-// shared group (rows of every position, many tiles). up_needed[g] is the number
-// of up tiles of group g.
-constexpr int kKeySlots = 1024 + 16;
-__device__ void write_tile_lists(const Dims &d, const Work &ws, const int32_t *s_off, int32_t *tmp, uint32_t *s_key,
-                                 int32_t *s_bu, int32_t *s_bd, int32_t *s_rank, int n, int64_t *trace_r) {
-  const int tid = threadIdx.x, lane = lane_id(), wid = warp_id(), nwarps = kRoutingThreads / 32;
+// Tile bookkeeping of the expert kernel, written by one CTA. The groups -- the
+// shared experts (every position) and the routed experts -- are listed widest
+// first, so that the expert kernel, which hands tiles out in list order, ends
+// on narrow tiles whose epilogues are short: the shared experts, then routed
+// experts with >= 96 rows, >= 32 rows, fewer (an expert with no row holds no
+// tile and its weights are never read), by id within a class. The order comes
+// from a stable counting sort: per-class counts packed two to an int, two
+// block scans. grp_list[p] = (token tiles of the groups before p) <<
+// kGrpIdBits | group of p, grp_list[E + n_sh] = all token tiles << kGrpIdBits.
+// The expert kernel decodes its tile indices from this list and the expert
+// offsets; tile totals and the number of hit experts go to the control block
+// and the statistics.
+__device__ void write_group_tiles(const Dims &d, const Work &ws, const int32_t *s_off, int32_t *tmp, int n) {
+  const int tid = threadIdx.x;
   const int E = d.E, G2 = E + d.n_sh;
-  const int G2p = (G2 + 15) & ~15;
-  auto rows_of = [&](int g) { return g < E ? s_off[g + 1] - s_off[g] : n; };
-  for (int g = tid; g < G2p; g += kRoutingThreads) {
-    uint32_t key = 0u;  // padding: below every group
-    if (g < G2) {
-      const uint32_t rows = static_cast<uint32_t>(min(rows_of(g), (1 << 19) - 1));
-      key = (g >= E ? 1u << 30 : 0u) | (rows << 11) | static_cast<uint32_t>(2047 - g);
-    }
-    s_key[g] = key;
-  }
-  __syncthreads();
-  for (int g = tid; g < G2; g += kRoutingThreads) {
-    const uint32_t mine = s_key[g];
-    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-    const uint4 *k4 = reinterpret_cast<const uint4 *>(s_key);
-    for (int h = 0; h < G2p / 4; h += 4) {
-      const uint4 a = k4[h], b = k4[h + 1], c = k4[h + 2], e = k4[h + 3];
-      r0 += (a.x > mine) + (a.y > mine) + (a.z > mine) + (a.w > mine);
-      r1 += (b.x > mine) + (b.y > mine) + (b.z > mine) + (b.w > mine);
-      r2 += (c.x > mine) + (c.y > mine) + (c.z > mine) + (c.w > mine);
-      r3 += (e.x > mine) + (e.y > mine) + (e.z > mine) + (e.w > mine);
-    }
-    s_rank[g] = r0 + r1 + r2 + r3;
-  }
-  __syncthreads();
-  if (trace_r && tid == 0) trace_r[6] = static_cast<int64_t>(globaltimer_ns());
-  // tile counts in rank order: thread tid owns ranks 2 tid and 2 tid + 1
-  int tu[2] = {0, 0}, td[2] = {0, 0}, hit = 0;
+  // thread tid holds groups 2 tid, 2 tid + 1 (id order; G2 <= 2 * kRoutingThreads)
+  int cls[2] = {-1, -1}, nt[2] = {0, 0}, hit = 0;
+  int pk[2] = {0, 0};  // this thread's count of each class: 0, 1 in pk[0], 2, 3 in pk[1] (16-bit fields)
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int g = 2 * tid + h;
     if (g < G2) {
-      const bool routed = g < E;
-      const int rows = rows_of(g);
-      hit += routed && rows > 0;
-      if (rows > 0 && d.tn_up > 0) {
-        s_bu[s_rank[g]] = ((rows + d.tn_up - 1) / d.tn_up) * ((routed ? d.I : d.I_s) / 128);
-        s_bd[s_rank[g]] = ((rows + d.tn_dn - 1) / d.tn_dn) * (d.H / kBmDn);
-      } else {
-        s_bu[s_rank[g]] = 0;
-        s_bd[s_rank[g]] = 0;
-      }
+      const bool shared = g >= E;
+      const int rows = shared ? n : s_off[g + 1] - s_off[g];
+      nt[h] = d.tn > 0 ? (rows + d.tn - 1) / d.tn : 0;
+      hit += !shared && rows > 0;
+      const int c = shared ? 3 : rows >= 96 ? 2 : rows >= 32 ? 1 : 0;
+      cls[h] = c;
+      pk[c >> 1] += 1 << (16 * (c & 1));
     }
   }
-  __syncthreads();
+  int tot0, tot1, n_hit;
+  const int ex0 = block_excl_scan(pk[0], tmp, &tot0);
+  const int ex1 = block_excl_scan(pk[1], tmp, &tot1);
+  (void)block_excl_scan(hit, tmp, &n_hit);
+  auto field = [](int packed, int c) { return (packed >> (16 * (c & 1))) & 0xffff; };
+  const int count3 = field(tot1, 3), count2 = field(tot1, 2), count1 = field(tot0, 1);
+  const int base[4] = {count3 + count2 + count1, count3 + count2, count3, 0};
+  int pos[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const int r = 2 * tid + h;
-    if (r < G2) {
-      tu[h] = s_bu[r];
-      td[h] = s_bd[r];
+    const int c = cls[h];
+    if (c < 0) continue;
+    pos[h] = base[c] + field(c < 2 ? ex0 : ex1, c) + (h == 1 && cls[0] == c ? 1 : 0);
+    ws.grp_list[pos[h]] = (nt[h] << kGrpIdBits) | (2 * tid + h);  // token tiles until the prefix below
+  }
+  __syncthreads();  // the list in sorted order is visible to the whole CTA
+  int g_at[2] = {0, 0}, nt_at[2] = {0, 0};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int p = 2 * tid + h;
+    if (p < G2) {
+      const int v = ws.grp_list[p];
+      g_at[h] = v & ((1 << kGrpIdBits) - 1);
+      nt_at[h] = v >> kGrpIdBits;
     }
   }
-  int n_up, n_dn, n_hit;
-  const int bu = block_excl_scan(tu[0] + tu[1], tmp, &n_up);
-  const int bd = block_excl_scan(td[0] + td[1], tmp, &n_dn);
-  (void)block_excl_scan(hit, tmp, &n_hit);
-  // s_bu/s_bd now become offsets by rank
-  if (2 * tid < G2) {
-    s_bu[2 * tid] = bu;
-    s_bd[2 * tid] = bd;
+  int total;
+  const int before = block_excl_scan(nt_at[0] + nt_at[1], tmp, &total);
+  if (total >= (1 << (31 - kGrpIdBits))) {
+    if (tid == 0) set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+    total = 0;
   }
-  if (2 * tid + 1 < G2) {
-    s_bu[2 * tid + 1] = bu + tu[0];
-    s_bd[2 * tid + 1] = bd + td[0];
-  }
+  if (2 * tid < G2) ws.grp_list[2 * tid] = (before << kGrpIdBits) | g_at[0];
+  if (2 * tid + 1 < G2) ws.grp_list[2 * tid + 1] = ((before + nt_at[0]) << kGrpIdBits) | g_at[1];
   if (tid == 0) {
-    s_bu[G2] = n_up;
-    s_bd[G2] = n_dn;
-    const int up = min(n_up, d.max_tiles_up), dn = min(n_dn, d.max_tiles_dn);
+    ws.grp_list[G2] = total << kGrpIdBits;
+    const int t_sh = d.tn > 0 ? d.n_sh * ((n + d.tn - 1) / d.tn) : 0;
+    const int up = d.tn > 0 && total > 0 ? (d.I_s / 128) * t_sh + (d.I / 128) * (total - t_sh) : 0;
+    const int dn = d.tn > 0 && total > 0 ? (d.H / kBmDn) * total : 0;
     ws.ctrl->n_hit = n_hit;
     ws.ctrl->tiles_up = up;
     ws.ctrl->tiles_dn = dn;
@@ -275,36 +266,6 @@ __device__ void write_tile_lists(const Dims &d, const Work &ws, const int32_t *s
     ws.stats->tiles_up = up;
     ws.stats->tiles_down = dn;
   }
-  __syncthreads();
-  // the tiles of group g: up tiles (m, t) in m-major order, then down tiles
-  auto group_tiles = [&](int g, int q0, int dq) {
-    const int rows = rows_of(g);
-    const int rk = s_rank[g];
-    const int bu0 = s_bu[rk], cu = s_bu[rk + 1] - bu0;
-    const int bd0 = s_bd[rk], cd = s_bd[rk + 1] - bd0;
-    if (q0 == 0) ws.up_needed[g] = cu;
-    if (rows <= 0 || d.tn_up <= 0) return;
-    const int r0 = g < E ? s_off[g] : 0;
-    const int ntu = (rows + d.tn_up - 1) / d.tn_up, ntd = (rows + d.tn_dn - 1) / d.tn_dn;
-    for (int q = q0; q < cu; q += dq) {
-      const int m = q / ntu, tt = q - m * ntu;
-      if (bu0 + q < d.max_tiles_up)
-        ws.tiles_up[bu0 + q] = make_int4(g, m, r0 + tt * d.tn_up, min(d.tn_up, rows - tt * d.tn_up));
-      else
-        set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-    }
-    for (int q = q0; q < cd; q += dq) {
-      const int m = q / ntd, tt = q - m * ntd;
-      if (bd0 + q < d.max_tiles_dn)
-        ws.tiles_dn[bd0 + q] = make_int4(g, m, r0 + tt * d.tn_dn, min(d.tn_dn, rows - tt * d.tn_dn));
-      else
-        set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-    }
-  };
-  for (int g = tid; g < E; g += kRoutingThreads) group_tiles(g, 0, 1);
-  for (int sh = 0; sh < d.n_sh; ++sh)
-    if (wid == nwarps - 1 - sh % nwarps) group_tiles(E + sh, lane, 32);
-  if (trace_r && tid == 0) trace_r[7] = static_cast<int64_t>(globaltimer_ns());
 }
 
 enum BlkField { B_SLICE = 0, B_REUSE, B_ANOM, B_BAD, B_LIVE, B_NEW, B_MISS, B_STALE };
@@ -330,22 +291,19 @@ enum BlkField { B_SLICE = 0, B_REUSE, B_ANOM, B_BAD, B_LIVE, B_NEW, B_MISS, B_ST
 //     grouped by expert with positions ascending, and copies each row of x
 //     into the compact buffer. CTA 0 writes the grouped-GEMM tile lists.
 template <int EPL>
-__global__ void __launch_bounds__(kRoutingThreads) k_routing(Dims d, Work ws, const float *__restrict__ bias,
-                                                             const uint8_t *__restrict__ live,
-                                                             const uint8_t *__restrict__ decoded,
-                                                             const uint4 *__restrict__ x, int vec_per_row) {
+__device__ __forceinline__ void routing_body(const Dims &d, const Work &ws, const float *__restrict__ bias,
+                                             const uint8_t *__restrict__ live, const uint8_t *__restrict__ decoded,
+                                             const uint4 *__restrict__ x, int vec_per_row) {
   const KernelMark mark_(d, ws, K_ROUTING);
   int64_t *trace_r = (d.trace && blockIdx.x < kTraceCtas)
                          ? ws.trace + (3ull * kTraceCtas + blockIdx.x) * kTraceFields
                          : nullptr;
+  pdl_wait();
+  pdl_trigger();
   if (trace_r && threadIdx.x == 0) trace_r[0] = static_cast<int64_t>(globaltimer_ns());
   __shared__ int32_t tmp[33];
   __shared__ int32_t s_cat[kBlkFields];
   __shared__ int32_t s_off[1025];
-  __shared__ int32_t s_bu[1025];
-  __shared__ int32_t s_bd[1025];
-  __shared__ int32_t s_rank[1024];
-  __shared__ __align__(16) uint32_t s_key[kKeySlots];
   __shared__ int s_ok;
   const int G = gridDim.x, b = blockIdx.x, tid = threadIdx.x;
   const int lane = lane_id(), wid = warp_id(), nwarps = kRoutingThreads / 32;
@@ -357,7 +315,9 @@ __global__ void __launch_bounds__(kRoutingThreads) k_routing(Dims d, Work ws, co
   if (tid < kBlkFields) s_cat[tid] = 0;
   for (int q = b * kRoutingThreads + tid; q < E * n_chunks; q += G * kRoutingThreads)
     ws.chunk_mask[static_cast<size_t>(q / n_chunks) * d.cmax + (q % n_chunks)] = 0u;
-  for (int g = b * kRoutingThreads + tid; g < E + d.n_sh; g += G * kRoutingThreads) ws.done_up[g] = 0;
+  // routed experts' up-tile counters (the shared experts' are the gate kernel's:
+  // the expert kernel may already be counting them while this kernel runs)
+  for (int g = b * kRoutingThreads + tid; g < E; g += G * kRoutingThreads) ws.done_up[g] = 0;
   if (b == 0 && tid == 0) *ws.tile_ctr = 0;  // the expert kernel hands tiles out from this counter
   // G = split-K partials summed in a fixed order + bias, every position
   if ((E & 3) == 0) {
@@ -505,7 +465,7 @@ __global__ void __launch_bounds__(kRoutingThreads) k_routing(Dims d, Work ws, co
     if (tid == 0) s_off[E] = tot;
     __syncthreads();
   }
-  // With more than one CTA, CTA 0 builds the statistics and the tile lists
+  // With more than one CTA, CTA 0 writes the statistics and the tile prefix
   // (nothing later in this kernel waits on it) while the others place the
   // worklist rows, meet at barrier 4 and copy the rows.
   const bool split = G > 1;
@@ -587,7 +547,8 @@ __global__ void __launch_bounds__(kRoutingThreads) k_routing(Dims d, Work ws, co
     }
     for (int e = tid; e <= E; e += kRoutingThreads) ws.offsets[e] = s_off[e];
     if (trace_r && tid == 0) trace_r[5] = static_cast<int64_t>(globaltimer_ns());
-    write_tile_lists(d, ws, s_off, tmp, s_key, s_bu, s_bd, s_rank, n, trace_r);
+    write_group_tiles(d, ws, s_off, tmp, n);
+    if (trace_r && tid == 0) trace_r[6] = static_cast<int64_t>(globaltimer_ns());
     if (split) return;
   }
 
@@ -618,6 +579,23 @@ __global__ void __launch_bounds__(kRoutingThreads) k_routing(Dims d, Work ws, co
     }
   }
   if (trace_r && tid == 0) trace_r[5] = static_cast<int64_t>(globaltimer_ns());
+}
+
+// The launch: after its last write every CTA counts itself into route_done
+// (zeroed by the gate kernel) with release semantics; the expert kernel, which
+// may already be running (programmatic dependent launch), acquires that count
+// instead of waiting for this grid to retire.
+template <int EPL>
+__global__ void __launch_bounds__(kRoutingThreads) k_routing(Dims d, Work ws, const float *__restrict__ bias,
+                                                             const uint8_t *__restrict__ live,
+                                                             const uint8_t *__restrict__ decoded,
+                                                             const uint4 *__restrict__ x, int vec_per_row) {
+  routing_body<EPL>(d, ws, bias, live, decoded, x, vec_per_row);
+  __syncthreads();  // every return in the body is uniform over the CTA
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(ws.route_done, 1u);
+  }
 }
 
 
@@ -657,6 +635,7 @@ __device__ __forceinline__ void store8(__nv_bfloat16 *p, const float (&v)[8]) {
 template <typename T>
 __global__ void __launch_bounds__(128) k_combine(Dims d, Work ws, const T *__restrict__ x, T *__restrict__ y) {
   const KernelMark mark_(d, ws, K_COMBINE);
+  pdl_wait();
   const int t = blockIdx.x;
   if (t >= d.n_pos) return;
   const int f = ws.fidx[t];
@@ -731,6 +710,14 @@ static int epl_for(int E) {
   return epl <= 1 ? 1 : epl <= 2 ? 2 : epl <= 4 ? 4 : epl <= 8 ? 8 : epl <= 16 ? 16 : 32;
 }
 
+// One routing CTA per SM (at most kMaxRoutingGrid). The grid barriers need
+// every CTA resident at once, which holds without a cooperative launch: the
+// kernel is launched while the gate kernel (at most one CTA per SM, and never
+// waiting on routing) may still run, so CTAs that do not fit yet start as gate
+// CTAs retire, and the kernels after it are launched only once every routing
+// CTA has started (programmatic launch trigger). Every wait is bounded anyway.
+int routing_grid() { return num_sms() < kMaxRoutingGrid ? num_sms() : kMaxRoutingGrid; }
+
 int num_sms() {
   static int n = 0;
   if (n == 0) {
@@ -742,6 +729,39 @@ int num_sms() {
   return n;
 }
 
+cudaError_t launch_kernel(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void **args,
+                          bool cooperative, bool programmatic) {
+  static bool pdl_ok = true;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (cooperative) {
+    attr[n].id = cudaLaunchAttributeCooperative;
+    attr[n].val.cooperative = 1;
+    ++n;
+  }
+  const bool pdl = programmatic && pdl_ok;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+  if (e != cudaSuccess && pdl && (e == cudaErrorInvalidValue || e == cudaErrorNotSupported)) {
+    (void)cudaGetLastError();
+    pdl_ok = false;
+    cfg.numAttrs = n - 1;
+    e = cudaLaunchKernelExC(&cfg, fn, args);
+  }
+  return e;
+}
+
 cudaError_t launch_gate_simt(const Dims &d, const Weights &w, const Work &ws, const void *x, int bf16,
                              cudaStream_t s) {
   const int outputs = d.n_pos * d.E;
@@ -751,12 +771,12 @@ cudaError_t launch_gate_simt(const Dims &d, const Weights &w, const Work &ws, co
     static bool carve_ = (prefer_max_shared(k_gate_simt<__nv_bfloat16>) == cudaSuccess);
     (void)carve_;
     k_gate_simt<__nv_bfloat16><<<blocks, 256, 0, s>>>(d, static_cast<const __nv_bfloat16 *>(x),
-                                                      static_cast<const __nv_bfloat16 *>(w.w_router), ws.gparts, ws.gbar);
+                                                      static_cast<const __nv_bfloat16 *>(w.w_router), ws.gparts, ws);
   } else {
     static bool carve_ = (prefer_max_shared(k_gate_simt<float>) == cudaSuccess);
     (void)carve_;
     k_gate_simt<float><<<blocks, 256, 0, s>>>(d, static_cast<const float *>(x),
-                                              static_cast<const float *>(w.w_router), ws.gparts, ws.gbar);
+                                              static_cast<const float *>(w.w_router), ws.gparts, ws);
   }
   return cudaGetLastError();
 }
@@ -789,8 +809,7 @@ cudaError_t launch_plan_support(const Dims &d, const Work &ws, int32_t threshold
 // so every CTA must be resident): one CTA per SM, capped at what fits.
 cudaError_t launch_routing(const Dims &d, const Weights &w, const Work &ws, const uint8_t *live,
                            const uint8_t *decoded, const void *x, int bf16, cudaStream_t s) {
-  int grid = num_sms();
-  if (grid > kMaxRoutingGrid) grid = kMaxRoutingGrid;
+  const int grid = routing_grid();
   // slices of at most kRoutingThreads positions per CTA
   const int min_grid = (d.n_pos + kRoutingThreads - 1) / kRoutingThreads;
   if (grid < min_grid) return cudaErrorInvalidConfiguration;
@@ -806,8 +825,8 @@ cudaError_t launch_routing(const Dims &d, const Weights &w, const Work &ws, cons
   case N: {                                                                                              \
     static bool c_ = (prefer_max_shared(k_routing<N>) == cudaSuccess);                                   \
     (void)c_;                                                                                            \
-    return cudaLaunchCooperativeKernel(reinterpret_cast<void *>(k_routing<N>), dim3(grid), dim3(kRoutingThreads), \
-                                       args, 0, s);                                                      \
+    return launch_kernel(reinterpret_cast<void *>(k_routing<N>), dim3(grid), dim3(kRoutingThreads), 0, s, args, \
+                         false, true);                                                                   \
   }
     EPOCH_CASE(1) EPOCH_CASE(2) EPOCH_CASE(4) EPOCH_CASE(8) EPOCH_CASE(16) EPOCH_CASE(32)
 #undef EPOCH_CASE
@@ -823,13 +842,17 @@ cudaError_t launch_combine(const Dims &d, const Work &ws, const void *x, void *y
   if (bf16) {
     static bool carve_ = (prefer_max_shared(k_combine<__nv_bfloat16>) == cudaSuccess);
     (void)carve_;
-    k_combine<__nv_bfloat16><<<d.n_pos, 128, 0, s>>>(d, ws, static_cast<const __nv_bfloat16 *>(x),
-                                                     static_cast<__nv_bfloat16 *>(y));
-  } else {
-    static bool carve_ = (prefer_max_shared(k_combine<float>) == cudaSuccess);
-    (void)carve_;
-    k_combine<float><<<d.n_pos, 128, 0, s>>>(d, ws, static_cast<const float *>(x), static_cast<float *>(y));
+    const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(x);
+    __nv_bfloat16 *yb = static_cast<__nv_bfloat16 *>(y);
+    Dims dd = d;
+    Work ww = ws;
+    void *args[] = {&dd, &ww, &xb, &yb};
+    return launch_kernel(reinterpret_cast<void *>(k_combine<__nv_bfloat16>), dim3(d.n_pos), dim3(128), 0, s, args,
+                         false, true);
   }
+  static bool carve_ = (prefer_max_shared(k_combine<float>) == cudaSuccess);
+  (void)carve_;
+  k_combine<float><<<d.n_pos, 128, 0, s>>>(d, ws, static_cast<const float *>(x), static_cast<float *>(y));
   return cudaGetLastError();
 }
 

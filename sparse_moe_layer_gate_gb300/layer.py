@@ -124,7 +124,7 @@ class EpochLayer:
         B.check(B.lib().epoch_set_tracing(self.handle, 1 if on else 0), "epoch_set_tracing")
 
     def read_trace(self, stream=None) -> np.ndarray:
-        """[4, 1024, 8] int64 per-CTA timelines of the last gate/up/down/routing launches."""
+        """[4, 1024, 8] int64 per-CTA trace rows: gate, experts, expert epilogue, routing."""
         v = B.epoch_debug_view()
         B.check(B.lib().epoch_debug_pointers(self.handle, C.byref(v)), "epoch_debug_pointers")
         return self._copy(v.trace, 4 * 1024 * 8, np.int64, stream).reshape(4, 1024, 8)
