@@ -33,6 +33,7 @@ struct epoch_layer {
   bool planned;
   int32_t n_pos_plan;
   int32_t last_iter;
+  int32_t state_rd;  // half of the double-buffered iteration state the next iteration reads
   int64_t n_cold, n_hot, n_fallback, n_launch;
   // profiling
   bool prof;
@@ -89,8 +90,8 @@ size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   const size_t act = c.dtype == EPOCH_BF16 ? 2 : 4;
   const size_t chunks = (N + 31) / 32;
   Work t;
-  t.stamp = static_cast<int32_t *>(take(N * 4));
-  t.prev_dec = static_cast<uint8_t *>(take(N));
+  t.stamp = static_cast<int32_t *>(take(2 * N * 4));
+  t.prev_dec = static_cast<uint8_t *>(take(2 * N));
   t.support_mask = static_cast<uint8_t *>(take(E));
   t.support_ids = static_cast<int32_t *>(take(E * 4));
   t.plan_counts = static_cast<int32_t *>(take(E * 4));
@@ -107,14 +108,13 @@ size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   t.grp_list = static_cast<int32_t *>(take((E + nsh + 1) * 4));
   t.done_up = static_cast<int32_t *>(take((E + nsh) * 4));
   t.tile_ctr = static_cast<int32_t *>(take(16));
-  t.sh_ctr = static_cast<int32_t *>(take(16));
   t.wl_pos = static_cast<int32_t *>(take(N * k * 4));
   t.slot = static_cast<int32_t *>(take(N * k * 4));
   t.xp = take(N * k * H * act);
   t.a_int = take(N * k * I * act);
   t.a_sh = take(nsh * N * Is * act + 16);
-  t.o_int = static_cast<float *>(take(N * k * H * 4));
-  t.o_sh = static_cast<float *>(take(nsh * N * H * 4 + 16));
+  t.o_int = take(N * k * H * act);
+  t.o_sh = take(nsh * N * H * act + 16);
   if (c.dtype == EPOCH_BF16) {
     t.pk_gu = static_cast<uint8_t *>(take(E * I * H * 2 * 2));
     t.pk_d = static_cast<uint8_t *>(take(E * H * I * 2));
@@ -123,7 +123,6 @@ size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   } else {
     t.pk_gu = t.pk_d = t.pk_sgu = t.pk_sd = nullptr;
   }
-  t.blk = static_cast<int32_t *>(take(static_cast<size_t>(kMaxRoutingGrid) * kBlkFields * 4));
   t.gbar = static_cast<unsigned int *>(take(16));
   t.route_done = static_cast<unsigned int *>(take(16));
   t.trace = static_cast<int64_t *>(take(4ull * kTraceCtas * kTraceFields * 8));
@@ -177,6 +176,7 @@ Dims call_dims(const epoch_layer *L, int32_t n_pos, int32_t iter, int host_fallb
   d.n_pos = n_pos;
   d.iter = iter;
   d.host_fallback = host_fallback;
+  d.state_rd = L->state_rd;
   return d;
 }
 
@@ -263,7 +263,7 @@ epoch_status epoch_layer_create(const epoch_layer_config *cfg, const epoch_layer
   }
   // empty cache, no plan: zero the workspace, stamps = -1, support = every expert
   if (cudaMemset(workspace, 0, bytes) != cudaSuccess ||
-      cudaMemset(L->ws.stamp, 0xFF, sizeof(int32_t) * d.Nmax) != cudaSuccess ||
+      cudaMemset(L->ws.stamp, 0xFF, 2 * sizeof(int32_t) * d.Nmax) != cudaSuccess ||
       cudaMemset(L->ws.support_mask, 1, d.E) != cudaSuccess) {
     delete L;
     return EPOCH_ECUDA;
@@ -295,6 +295,7 @@ epoch_status epoch_layer_create(const epoch_layer_config *cfg, const epoch_layer
   L->planned = false;
   L->n_pos_plan = 0;
   L->last_iter = -1;
+  L->state_rd = 0;
   L->prof = false;
   for (int i = 0; i < K_NUM; ++i) {
     L->total_ms[i] = 0.0;
@@ -338,6 +339,7 @@ epoch_status epoch_moe_iter(epoch_layer *L, const void *x, const uint8_t *live, 
   CUtensorMap x_maps[2];
   EPOCH_TRY(run_gate(L, d, x, x_maps, s));
   EPOCH_TRY(run(L, K_ROUTING, s, [&] { return launch_routing(d, L->w, L->ws, live, decoded, x, L->bf16, s); }));
+  L->state_rd ^= 1;  // the routing kernel wrote the new state into the other half
   if (L->bf16) {
     EPOCH_TRY(run(L, K_UP, s, [&] { return launch_experts_tc(d, L->maps, L->ws, x_maps[1], s); }));
   } else {
@@ -395,7 +397,7 @@ epoch_status epoch_debug_pointers(epoch_layer *L, epoch_debug_view *v) {
   v->offsets = L->ws.offsets;
   v->wl_pos = L->ws.wl_pos;
   v->slot = L->ws.slot;
-  v->stamp = L->ws.stamp;
+  v->stamp = L->ws.stamp + static_cast<size_t>(L->state_rd) * L->cfg.max_positions;
   v->cache = L->ws.cache;
   v->trace = L->ws.trace;
   v->timeline = reinterpret_cast<const int64_t *>(L->ws.timeline);

@@ -6,8 +6,9 @@
 // compact rows ("light-traffic expert kernel", walk-through page
 // "Epoch 完全拆解:把扩散块编译成稀疏 MoE 服务单元", section "FreshLane Dispatch").
 //
-// Rows: [0, L) are worklist edges (expert from the offsets), then n_shared
-// blocks of n_pos rows for the shared experts over every position.
+// Rows: [0, L) are worklist edges (expert from the offsets, token row of x
+// from the worklist position), then n_shared blocks of n_pos rows for the
+// shared experts over every position.
 #include "common.cuh"
 #include "layer.h"
 
@@ -37,7 +38,12 @@ __global__ void __launch_bounds__(256) k_up_simt(Dims d, Weights w, Work ws, con
     int inter;
     if (r < L) {
       const int e = expert_of_row(ws.offsets, d.E, r);
-      src = static_cast<const float *>(ws.xp) + static_cast<size_t>(r) * d.H;
+      int tp = ws.wl_pos[r];  // worklist row r is fresh position tp
+      if (tp < 0 || tp >= d.n_pos) {
+        if (threadIdx.x == 0) set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+        tp = 0;
+      }
+      src = x + static_cast<size_t>(tp) * d.H;
       wg = static_cast<const float *>(w.w_gate) + static_cast<size_t>(e) * d.I * d.H;
       wu = static_cast<const float *>(w.w_up) + static_cast<size_t>(e) * d.I * d.H;
       dst = static_cast<float *>(ws.a_int) + static_cast<size_t>(r) * d.I;
@@ -86,13 +92,13 @@ __global__ void __launch_bounds__(256) k_down_simt(Dims d, Weights w, Work ws) {
       const int e = expert_of_row(ws.offsets, d.E, r);
       src = static_cast<const float *>(ws.a_int) + static_cast<size_t>(r) * d.I;
       wd = static_cast<const float *>(w.w_down) + static_cast<size_t>(e) * d.H * d.I;
-      dst = ws.o_int + static_cast<size_t>(r) * d.H;
+      dst = static_cast<float *>(ws.o_int) + static_cast<size_t>(r) * d.H;
       inter = d.I;
     } else {
       const int s = (r - L) / d.n_pos, t = (r - L) % d.n_pos;
       src = static_cast<const float *>(ws.a_sh) + (static_cast<size_t>(s) * d.Nmax + t) * d.I_s;
       wd = static_cast<const float *>(w.ws_down) + static_cast<size_t>(s) * d.H * d.I_s;
-      dst = ws.o_sh + (static_cast<size_t>(s) * d.Nmax + t) * d.H;
+      dst = static_cast<float *>(ws.o_sh) + (static_cast<size_t>(s) * d.Nmax + t) * d.H;
       inter = d.I_s;
     }
     __syncthreads();

@@ -1,26 +1,28 @@
-// tcgen05 + TMA grouped GEMMs of the Epoch MoE layer (bf16 in, fp32 accumulate).
+// tcgen05 + TMA GEMMs of the Epoch MoE layer (bf16 in, fp32 accumulate).
 //
-// Three contractions share one persistent, warp-specialised kernel:
-//   GATE  G^T = W_r x^T, split along H (the route kernel sums the splits in a
-//         fixed order and adds the bias) -- router logits for every position
-//         ([W] section "Expert Atlas": G in R^{N x E}, recomputed every iteration);
-//   UP    per group g: A_g = silu(X_g W_gate,g^T) * (X_g W_up,g^T) -> bf16;
-//   DOWN  per group g: O_g = A_g W_down,g^T -> fp32.
-// Groups are the routed experts with at least one worklist row, then the
-// shared experts over every position; each routed expert runs once over its
-// compact rows (the "light-traffic expert kernel" of [W] section
-// "FreshLane Dispatch"); experts with no row produce no tile, so their weights
-// are never read ("invalid slots load no expert weights", same section).
+// Two persistent, warp-specialised kernels:
+//   k_tc_gate     G^T = W_r x^T, split along H (the routing kernel sums the
+//                 splits in a fixed order and adds the bias) -- router logits
+//                 for every position ([W] section "Expert Atlas": G in
+//                 R^{N x E}, recomputed every iteration);
+//   k_tc_experts  per group g, UP: A_g = silu(X_g W_gate,g^T) * (X_g W_up,g^T)
+//                 and DOWN: O_g = A_g W_down,g^T, both stored as bf16, in one
+//                 launch with per-group dependencies.
+// Groups are the routed experts with at least one worklist row and the shared
+// experts over every position; each routed expert runs once over its compact
+// rows (the "light-traffic expert kernel" of [W] section "FreshLane
+// Dispatch"); experts with no row produce no tile, so their weights are never
+// read ("invalid slots load no expert weights", same section).
 // [W] = walk-through page "Epoch 完全拆解:把扩散块编译成稀疏 MoE 服务单元".
 //
 // Swap-AB: weight rows are the MMA M dimension (128) and tokens the N
-// dimension (16..TN, rounded up to 16 per tile), because an expert may hold
-// from one to a thousand rows. Roles per CTA (192 threads): warp 0 issues TMA
-// loads into a STAGES-deep shared-memory ring (128-byte swizzle, K-major),
-// warp 1 issues tcgen05.mma into TMEM accumulators (double-buffered when they
-// fit, so the epilogue of one tile overlaps the next tile's main loop), warps
-// 2-5 read TMEM with tcgen05.ld and store. One CTA per SM, persistent over a
-// device-resident tile count: no host synchronisation.
+// dimension (16..128, rounded up to 16 per tile), because an expert may hold
+// from one to a thousand rows. Roles per CTA (192 threads): warp 0 issues the
+// operand copies into a shared-memory ring (128-byte swizzle, K-major), warp 1
+// issues tcgen05.mma into TMEM accumulators (double-buffered, so the epilogue
+// of one tile overlaps the next tile's main loop), warps 2-5 read TMEM with
+// tcgen05.ld and store. One CTA per SM, persistent over a device-resident tile
+// count: no host synchronisation.
 #include <cudaTypedefs.h>
 
 #include <cstring>
@@ -138,15 +140,14 @@ __global__ void __launch_bounds__(192, 1) k_tc_gate(const __grid_constant__ TcPa
   pdl_wait();
   pdl_trigger();  // the routing kernel may start its launch; it waits for this grid to finish
   if (blockIdx.x == 0) {
-    // counters of the routing and expert kernels that follow: the grid barrier,
-    // and the shared-expert tiles the expert kernel starts before routing ends
+    // counters of the routing launch that follows: its grid barrier and the
+    // count of its finished CTAs (which the expert kernel waits for)
     if (threadIdx.x == 0) {
       *ws.gbar = 0u;
       *ws.route_done = 0u;
-      *ws.sh_ctr = 0;
     }
-    for (int s = threadIdx.x; s < d.n_sh; s += blockDim.x) ws.done_up[d.E + s] = 0;
   }
+  clear_selection_masks(d, ws);
   const int total = p.gate_tiles;
   if (static_cast<int>(blockIdx.x) >= total) return;
   const int wid = warp_id(), lane = lane_id();
@@ -355,7 +356,7 @@ __global__ void __launch_bounds__(192, 1) k_tc_gate(const __grid_constant__ TcPa
 // run) and a 16 KB token tile.
 constexpr int kExpStages = 4;
 constexpr int kExpStage = 48 * 1024;
-constexpr int kExpStg = 32 * 144;  // epilogue staging per warp (fp32 worst case)
+constexpr int kExpStg = 32 * 80;  // epilogue staging per warp: 32 tokens x 32 bf16 rows, padded
 constexpr int kExpSched = 4;  // decoded-tile ring between the producer and the MMA / epilogue warps
 constexpr int kExpBars = 2 * kExpStages + 2 * 2 + 1 + 2 * kExpSched;
 constexpr int kExpGroups = 1028;  // capacity of the group list and offset copies (E + n_sh + 1 <= 1025)
@@ -479,7 +480,7 @@ __device__ __forceinline__ XTile xdecode(const TcParams &p, int4 td) {
     t.b_row = shared ? s * d.Nmax + r0 : r0;
     t.out_row0 = t.b_row;
     t.ld = d.H;
-    t.out = shared ? static_cast<void *>(ws.o_sh) : static_cast<void *>(ws.o_int);
+    t.out = shared ? ws.o_sh : ws.o_int;
     t.out_rows = shared ? d.n_sh * d.Nmax : d.Nmax * d.k;
   }
   return t;
@@ -550,21 +551,16 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   if (trace && threadIdx.x == 0) trace[1] = static_cast<int64_t>(globaltimer_ns());
-  // The shared experts' up tiles read only x and their weights: they are drawn
-  // from sh_ctr (zeroed by the gate kernel, like their done counters) while the
-  // routing kernel may still run, so the longest dependency chain of the
-  // iteration starts early. Every other tile -- routed up tiles, then the down
-  // tiles of every group -- is drawn from tile_ctr after the producer has seen
+  // The prologue above may overlap the routing kernel (programmatic dependent
+  // launch); the producer draws tiles from tile_ctr only after it has seen
   // every routing CTA finish (the route_done count) and loaded the group list
   // and expert offsets.
-  const int nt_sh = (d.n_pos + kTnUp - 1) / kTnUp;
-  const int a_sh = d.n_sh * nt_sh * (d.I_s / BM);  // shared up tiles (the first of the full list)
 
   if (wid == 0) {
     // ---------------- producer: weight bulk copies + token TMA loads (lane 0)
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_b = policy_evict_last();
-    int stage = 0, j = 0;
+    int stage = 0;
     uint32_t phase = 0, armed = 0, armed_par = 0;
     bool ok = true;
     uint64_t waited = 0;
@@ -629,22 +625,6 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
       tma_prefetch_desc(&p.bs);
       tma_prefetch_desc(&p.b[0]);
       tma_prefetch_desc(&p.b2[0]);
-      // shared up tiles, before the routing kernel has finished
-      for (; ok; ++j) {
-        const int slot = j % kExpSched;
-        if (!mbar_wait_bounded(sempty_bar(slot), ((j / kExpSched) & 1) ^ 1u, abort_flag, ws.err, tmo)) {
-          ok = false;
-          break;
-        }
-        const int tile = atomicAdd(ws.sh_ctr, 1);
-        if (tile >= a_sh) break;  // slot j stays free for the next phase
-        const int per = nt_sh * (d.I_s / BM);
-        const int sidx = tile / per, qq = tile - sidx * per, m = qq / nt_sh, tt = qq - m * nt_sh;
-        const int4 td = make_int4(d.E + sidx, m, tt * kTnUp, min(kTnUp, d.n_pos - tt * kTnUp));
-        s_td[slot] = td;
-        mbar_arrive(sfull_bar(slot));
-        ok = issue(td, 0);
-      }
     }
     // wait until every routing CTA has counted itself done (acquire: its writes
     // are visible to this warp after the __syncwarp)
@@ -664,24 +644,24 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
           ok = false;
           break;
         }
-        __nanosleep(32);
+        __nanosleep(128);
       }
     }
     __syncwarp();
     for (int i = lane; i <= d.E + d.n_sh; i += 32) s_list[i] = ws.grp_list[i];
     for (int i = lane; i <= d.E; i += 32) s_offs[i] = ws.offsets[i];
     const int n_up = ws.ctrl->tiles_up;
-    const int total = n_up + ws.ctrl->tiles_dn - a_sh;  // tiles drawn from tile_ctr
+    const int total = n_up + ws.ctrl->tiles_dn;
     __syncwarp();
     if (lane == 0) {
       if (trace) trace[2] = static_cast<int64_t>(globaltimer_ns());
-      for (; ok; ++j) {
+      for (int j = 0; ok; ++j) {
         const int slot = j % kExpSched;
         if (!mbar_wait_bounded(sempty_bar(slot), ((j / kExpSched) & 1) ^ 1u, abort_flag, ws.err, tmo)) break;
         const int tile = atomicAdd(ws.tile_ctr, 1);
         int4 td = make_int4(-1, 0, 0, 0);
         int need = 0;
-        if (tile < total && !locate(d, s_list, s_offs, tile + a_sh, n_up, &td, &need)) {
+        if (tile < total && !locate(d, s_list, s_offs, tile, n_up, &td, &need)) {
           set_error(ws.err, EPOCH_DEVERR_BOUNDS);
           *abort_flag = 1;
           td.x = -1;
@@ -778,8 +758,8 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
       tc_fence_after();
       const int64_t tw1 = etr ? static_cast<int64_t>(globaltimer_ns()) : 0;
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * 256);
-      const int esz = t.up ? 2 : 4;
-      const int row_bytes = t.up ? 80 : 144;
+      const int esz = 2;  // bf16 outputs (activations and expert outputs)
+      const int row_bytes = 80;
       const bool vec_ok = ((t.ld * esz) & 15) == 0;
       const int halves = t.up ? 1 : 2;  // down: the two 128-row blocks are two output column blocks
       for (int hb = 0; hb < halves; ++hb) {
@@ -803,7 +783,8 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
             } else {
               tmem_ld_wait();
 #pragma unroll
-              for (int c = 0; c < 8; ++c) reinterpret_cast<float *>(stg + (cc + c) * row_bytes)[lane] = a[c];
+              for (int c = 0; c < 8; ++c)
+                reinterpret_cast<__nv_bfloat16 *>(stg + (cc + c) * row_bytes)[lane] = __float2bfloat16_rn(a[c]);
             }
           }
           __syncwarp();

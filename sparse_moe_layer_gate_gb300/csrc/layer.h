@@ -26,8 +26,9 @@ struct Ctrl {
 // Device pointers carved from the caller's workspace.
 struct Work {
   // block-lifetime state
-  int32_t *stamp;         // [Nmax] iteration of the row's last fresh compute, -1 none
-  uint8_t *prev_dec;      // [Nmax] decoded at the previous iteration
+  int32_t *stamp;         // [2][Nmax] iteration of the row's last fresh compute, -1 none
+  uint8_t *prev_dec;      // [2][Nmax] decoded at the previous iteration
+                          // (both double-buffered: an iteration reads half state_rd, writes the other)
   uint8_t *support_mask;  // [E]
   int32_t *support_ids;   // [E] ranked experts
   int32_t *plan_counts;   // [E] block-start hit counts
@@ -44,17 +45,15 @@ struct Work {
   int32_t *offsets;       // [E+1]
   int32_t *grp_list;      // [E + n_sh + 1] expert-kernel groups in list order: token tiles of the
                           // groups before << kGrpIdBits | group (shared experts E..E+n_sh-1)
-  int32_t *done_up;       // [E + n_sh] up tiles of each group finished this iteration (by group id;
-                          // routed entries zeroed by the routing kernel, shared ones by the gate kernel)
-  int32_t *tile_ctr;      // next routed-up or down tile of the expert kernel (zeroed by the routing kernel)
-  int32_t *sh_ctr;        // next shared-expert up tile of the expert kernel (zeroed by the gate kernel)
+  int32_t *done_up;       // [E + n_sh] up tiles of each group finished this iteration (by group id)
+  int32_t *tile_ctr;      // next tile of the expert kernel (dynamic scheduling)
   int32_t *wl_pos;        // [Nmax*k] expert-sorted worklist positions
   int32_t *slot;          // [Nmax][k] worklist row of selection (f, j)
-  void *xp;               // [Nmax*k][H] permuted fresh rows
+  void *xp;               // [Nmax*k][H] token rows of the worklist (x at wl_pos), expert-sorted
   void *a_int;            // [Nmax*k][I] SwiGLU activations of routed edges
   void *a_sh;             // [n_sh*Nmax][I_s] SwiGLU activations of shared experts
-  float *o_int;           // [Nmax*k][H] routed expert outputs
-  float *o_sh;            // [n_sh*Nmax][H] shared expert outputs
+  void *o_int;            // [Nmax*k][H] routed expert outputs, layer dtype
+  void *o_sh;             // [n_sh*Nmax][H] shared expert outputs, layer dtype
   // expert weights of bf16 layers, packed once at creation into 16 KB tiles of
   // 128 rows x 64 columns in the 128-byte-swizzled K-major layout the tensor
   // cores read, tile (row block rb, K block kb) at index rb * (K / 64) + kb:
@@ -62,7 +61,6 @@ struct Work {
   uint8_t *pk_d;          // routed W_down: [E*H/256][I/64] x (two 128-row tiles) = 32 KB
   uint8_t *pk_sgu;        // shared W_gate/W_up: [n_sh*I_s/128][H/64] x 32 KB
   uint8_t *pk_sd;         // shared W_down: [n_sh*H/256][I_s/64] x 32 KB
-  int32_t *blk;           // [kMaxRoutingGrid][kBlkFields] per-CTA partials of the routing kernel
   unsigned int *gbar;     // grid-barrier counter of the routing kernel (zeroed by the gate kernel)
   unsigned int *route_done;  // routing CTAs finished (zeroed by the gate kernel)
   int64_t *trace;         // [4 kernels][kTraceCtas][8] per-CTA timeline (when tracing)
@@ -80,7 +78,7 @@ constexpr int kTraceFields = 8;
 
 constexpr int kTileBytes = 128 * 64 * 2;  // one packed 128 x 64 bf16 tile
 constexpr int kMaxRoutingGrid = 1024;
-constexpr int kBlkFields = 8;
+constexpr int kBlkFields = 8;  // per-CTA counters of the routing kernel
 constexpr int kRoutingThreads = 512;
 
 // Shapes and per-call values handed to every kernel by value.
@@ -91,6 +89,7 @@ struct Dims {
   int32_t n_pos;
   int32_t iter;
   int32_t host_fallback;
+  int32_t state_rd;      // half of stamp / prev_dec holding the previous iteration's state
   int32_t tn;            // token-tile width of the tcgen05 expert kernel (0 on the SIMT path)
   int32_t cmax;          // chunk capacity: ceil(Nmax / 32)
   int32_t trace;         // nonzero: tcgen05 kernels record per-CTA timelines
@@ -158,6 +157,16 @@ cudaError_t launch_routing(const Dims &d, const Weights &w, const Work &ws, cons
                            const uint8_t *decoded, const void *x, int bf16, cudaStream_t s);
 cudaError_t launch_combine(const Dims &d, const Work &ws, const void *x, void *y, int bf16, cudaStream_t s);
 cudaError_t launch_wait_test(uint32_t *err, int64_t timeout_ns, cudaStream_t s);
+#ifdef __CUDACC__
+// Zeroes the selection-mask words the next routing launch may set (experts x
+// ceil(n_pos / 32) chunks); run by the gate kernels, whose completion the
+// routing kernel waits for before its first atomicOr.
+__device__ __forceinline__ void clear_selection_masks(const Dims &d, const Work &ws) {
+  const int nch = (d.n_pos + 31) / 32;
+  for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < d.E * nch; q += gridDim.x * blockDim.x)
+    ws.chunk_mask[static_cast<size_t>(q / nch) * d.cmax + q % nch] = 0u;
+}
+#endif
 
 // gemm_simt.cu (fp32 layers)
 cudaError_t launch_up_simt(const Dims &d, const Weights &w, const Work &ws, const void *x, cudaStream_t s);

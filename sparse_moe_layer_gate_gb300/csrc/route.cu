@@ -64,10 +64,9 @@ __global__ void k_gate_simt(Dims d, const T *__restrict__ x, const T *__restrict
     if (threadIdx.x == 0) {
       *ws.gbar = 0u;
       *ws.route_done = 0u;
-      *ws.sh_ctr = 0;
     }
-    for (int s = threadIdx.x; s < d.n_sh; s += blockDim.x) ws.done_up[d.E + s] = 0;
   }
+  clear_selection_masks(d, ws);
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int lane = lane_id();
   for (int o = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; o < d.n_pos * d.E; o += warps) {
@@ -153,7 +152,7 @@ __global__ void __launch_bounds__(1024) k_plan_support(Dims d, Work ws, int32_t 
     ws.support_mask[tid] = rank < len ? 1 : 0;
   }
   if (tid == 0) ws.ctrl->support_len = len;
-  for (int t = tid; t < d.Nmax; t += blockDim.x) {
+  for (int t = tid; t < 2 * d.Nmax; t += blockDim.x) {  // both halves of the iteration state
     ws.stamp[t] = -1;
     ws.prev_dec[t] = 0;
   }
@@ -206,7 +205,7 @@ __device__ void write_group_tiles(const Dims &d, const Work &ws, const int32_t *
   const int E = d.E, G2 = E + d.n_sh;
   // thread tid holds groups 2 tid, 2 tid + 1 (id order; G2 <= 2 * kRoutingThreads)
   int cls[2] = {-1, -1}, nt[2] = {0, 0}, hit = 0;
-  int pk[2] = {0, 0};  // this thread's count of each class: 0, 1 in pk[0], 2, 3 in pk[1] (16-bit fields)
+  int pk0 = 0, pk1 = 0;  // this thread's count of each class: 0, 1 in pk0, 2, 3 in pk1 (16-bit fields)
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int g = 2 * tid + h;
@@ -217,23 +216,23 @@ __device__ void write_group_tiles(const Dims &d, const Work &ws, const int32_t *
       hit += !shared && rows > 0;
       const int c = shared ? 3 : rows >= 96 ? 2 : rows >= 32 ? 1 : 0;
       cls[h] = c;
-      pk[c >> 1] += 1 << (16 * (c & 1));
+      if (c < 2) pk0 += 1 << (16 * (c & 1));
+      else pk1 += 1 << (16 * (c & 1));
     }
   }
   int tot0, tot1, n_hit;
-  const int ex0 = block_excl_scan(pk[0], tmp, &tot0);
-  const int ex1 = block_excl_scan(pk[1], tmp, &tot1);
+  const int ex0 = block_excl_scan(pk0, tmp, &tot0);
+  const int ex1 = block_excl_scan(pk1, tmp, &tot1);
   (void)block_excl_scan(hit, tmp, &n_hit);
   auto field = [](int packed, int c) { return (packed >> (16 * (c & 1))) & 0xffff; };
   const int count3 = field(tot1, 3), count2 = field(tot1, 2), count1 = field(tot0, 1);
-  const int base[4] = {count3 + count2 + count1, count3 + count2, count3, 0};
-  int pos[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int c = cls[h];
     if (c < 0) continue;
-    pos[h] = base[c] + field(c < 2 ? ex0 : ex1, c) + (h == 1 && cls[0] == c ? 1 : 0);
-    ws.grp_list[pos[h]] = (nt[h] << kGrpIdBits) | (2 * tid + h);  // token tiles until the prefix below
+    const int base = c == 3 ? 0 : c == 2 ? count3 : c == 1 ? count3 + count2 : count3 + count2 + count1;
+    const int pos = base + field(c < 2 ? ex0 : ex1, c) + (h == 1 && cls[0] == c ? 1 : 0);
+    ws.grp_list[pos] = (nt[h] << kGrpIdBits) | (2 * tid + h);  // token tiles until the prefix below
   }
   __syncthreads();  // the list in sorted order is visible to the whole CTA
   int g_at[2] = {0, 0}, nt_at[2] = {0, 0};
@@ -268,7 +267,9 @@ __device__ void write_group_tiles(const Dims &d, const Work &ws, const int32_t *
   }
 }
 
-enum BlkField { B_SLICE = 0, B_REUSE, B_ANOM, B_BAD, B_LIVE, B_NEW, B_MISS, B_STALE };
+// Position categories of the routing kernel, and the per-CTA counters it sums.
+enum Category { C_LIVE = 0, C_NEW, C_MISS, C_STALE, C_REUSE, C_BAD, C_ANOM, C_REUSE_BEFORE };
+static_assert(C_REUSE_BEFORE < kBlkFields, "category counters");
 
 // One cooperative launch (one CTA per SM, 16 warps) runs the whole routing
 // side of an iteration in four phases separated by grid barriers:
@@ -298,120 +299,162 @@ __device__ __forceinline__ void routing_body(const Dims &d, const Work &ws, cons
   int64_t *trace_r = (d.trace && blockIdx.x < kTraceCtas)
                          ? ws.trace + (3ull * kTraceCtas + blockIdx.x) * kTraceFields
                          : nullptr;
-  pdl_wait();
-  pdl_trigger();
   if (trace_r && threadIdx.x == 0) trace_r[0] = static_cast<int64_t>(globaltimer_ns());
+  pdl_trigger();  // the expert kernel may start its launch; it waits on route_done
   __shared__ int32_t tmp[33];
   __shared__ int32_t s_cat[kBlkFields];
   __shared__ int32_t s_off[1025];
+  __shared__ int16_t s_rank[kRoutingThreads];  // rank of each slice row in the slice's fresh rows, -1 reused
   __shared__ int s_ok;
   const int G = gridDim.x, b = blockIdx.x, tid = threadIdx.x;
   const int lane = lane_id(), wid = warp_id(), nwarps = kRoutingThreads / 32;
   const int n = d.n_pos, E = d.E, k = d.k;
   const uint64_t tmo = static_cast<uint64_t>(d.timeout_ns);
-  const int n_chunks = (n + 31) / 32;
 
-  // ---- phase A: classify this CTA's slice, clear the selection masks
-  if (tid < kBlkFields) s_cat[tid] = 0;
-  for (int q = b * kRoutingThreads + tid; q < E * n_chunks; q += G * kRoutingThreads)
-    ws.chunk_mask[static_cast<size_t>(q / n_chunks) * d.cmax + (q % n_chunks)] = 0u;
-  // routed experts' up-tile counters (the shared experts' are the gate kernel's:
-  // the expert kernel may already be counting them while this kernel runs)
-  for (int g = b * kRoutingThreads + tid; g < E; g += G * kRoutingThreads) ws.done_up[g] = 0;
-  if (b == 0 && tid == 0) *ws.tile_ctr = 0;  // the expert kernel hands tiles out from this counter
-  // G = split-K partials summed in a fixed order + bias, every position
-  if ((E & 3) == 0) {
-    const int e4 = E / 4;
-    for (int q = b * kRoutingThreads + tid; q < n * e4; q += G * kRoutingThreads) {
-      const int row = q / e4, c4 = q % e4;
-      float4 acc = __ldg(reinterpret_cast<const float4 *>(ws.gparts + static_cast<size_t>(row) * E) + c4);
-      for (int sk = 1; sk < d.SK; ++sk) {
-        const float4 p4 = __ldg(reinterpret_cast<const float4 *>(ws.gparts + (static_cast<size_t>(sk) * d.Nmax + row) * E) + c4);
-        acc.x += p4.x; acc.y += p4.y; acc.z += p4.z; acc.w += p4.w;
-      }
-      const float4 b4 = __ldg(reinterpret_cast<const float4 *>(bias) + c4);
-      acc.x += b4.x; acc.y += b4.y; acc.z += b4.z; acc.w += b4.w;
-      reinterpret_cast<float4 *>(ws.logits + static_cast<size_t>(row) * E)[c4] = acc;
-    }
-  } else {
-    for (int q = b * kRoutingThreads + tid; q < n * E; q += G * kRoutingThreads) {
-      const int row = q / E, e = q % E;
-      float g = ws.gparts[static_cast<size_t>(row) * E + e];
-      for (int sk = 1; sk < d.SK; ++sk) g += ws.gparts[(static_cast<size_t>(sk) * d.Nmax + row) * E + e];
-      ws.logits[static_cast<size_t>(row) * E + e] = g + bias[e];
-    }
-  }
-  const int per = (n + G - 1) / G;
+  // ---- phase 1a, while the gate kernel may still run: it reads only the
+  // masks and the previous iteration's state and writes only this iteration's.
+  // Every CTA classifies every position from the previous state
+  // (double-buffered: read half rd, write half rd ^ 1, so no CTA can overwrite
+  // what another still reads), which gives the anomaly flag, the fresh count
+  // and this CTA's offset in the fresh list; then it writes the new state of
+  // its own slice of positions.
+  const int rd = d.state_rd & 1, wr = rd ^ 1;
+  const int32_t *stamp_old = ws.stamp + static_cast<size_t>(rd) * d.Nmax;
+  const uint8_t *prev_old = ws.prev_dec + static_cast<size_t>(rd) * d.Nmax;
+  int32_t *stamp_new = ws.stamp + static_cast<size_t>(wr) * d.Nmax;
+  uint8_t *prev_new = ws.prev_dec + static_cast<size_t>(wr) * d.Nmax;
+  const int per = (n + G - 1) / G;  // <= kRoutingThreads (the launch checks the grid)
   const int lo = min(b * per, n), hi = min(lo + per, n);
-  const int t = lo + tid;
-  const bool mine = t < hi;
-  bool is_live = false, reuse = false;
-  __syncthreads();  // s_cat cleared
-  if (mine) {
-    const bool lv = live[t] != 0, dc = decoded[t] != 0;
-    is_live = lv || !dc;
-    const bool prev = ws.prev_dec[t] != 0;
-    const int st = ws.stamp[t];
-    int cat;
-    if (is_live) cat = B_LIVE;
-    else if (!prev) cat = B_NEW;
-    else if (st < 0) cat = B_MISS;
-    else if (d.R != INT_MAX && d.iter - st >= d.R) cat = B_STALE;
-    else cat = B_REUSE;
-    reuse = cat == B_REUSE;
-    atomicAdd(&s_cat[cat], 1);
-    if (lv == dc) atomicAdd(&s_cat[B_BAD], 1);
-    if (is_live && prev) s_cat[B_ANOM] = 1;
+  if (tid < kBlkFields) s_cat[tid] = 0;
+  for (int g = b * kRoutingThreads + tid; g < E + d.n_sh; g += G * kRoutingThreads) ws.done_up[g] = 0;
+  if (b == 0 && tid == 0) *ws.tile_ctr = 0;  // the expert kernel hands tiles out from this counter
+  // positions beyond this call's n_pos keep their state
+  for (int t = n + b * kRoutingThreads + tid; t < d.Nmax; t += G * kRoutingThreads) {
+    stamp_new[t] = stamp_old[t];
+    prev_new[t] = prev_old[t];
   }
-  __syncthreads();
-  if (tid < kBlkFields) ws.blk[b * kBlkFields + tid] = tid == B_SLICE ? hi - lo : s_cat[tid];
-  if (!grid_sync(ws.gbar, 1u * G, ws.err, tmo, &s_ok)) return;
+  // category of position t: live (still Mask, or not decoded), newly decoded,
+  // decoded without a row, decoded with a row at least R iterations old, or
+  // stable decoded (reuses its cached row)
+  // (packed: category | live << 4 | contradictory flags << 5 | decoded -> live << 6)
+  auto classify = [&](int t) -> int {
+    const bool lv = live[t] != 0, dc = decoded[t] != 0;
+    const bool il = lv || !dc, prev = prev_old[t] != 0;
+    const int st = stamp_old[t];
+    const int flags = (il ? 16 : 0) | (lv == dc ? 32 : 0) | (il && prev ? 64 : 0);
+    if (il) return C_LIVE | flags;
+    if (!prev) return C_NEW | flags;
+    if (st < 0) return C_MISS | flags;
+    if (d.R != INT_MAX && d.iter - st >= d.R) return C_STALE | flags;
+    return C_REUSE | flags;
+  };
+  {
+    int cnt[kBlkFields];
+#pragma unroll
+    for (int c = 0; c < kBlkFields; ++c) cnt[c] = 0;
+    for (int t = tid; t < n; t += kRoutingThreads) {
+      const int code = classify(t), c = code & 15;
+#pragma unroll
+      for (int q = 0; q < C_BAD; ++q) cnt[q] += c == q;
+      cnt[C_BAD] += (code >> 5) & 1;
+      cnt[C_ANOM] |= (code >> 6) & 1;
+      cnt[C_REUSE_BEFORE] += c == C_REUSE && t < lo;
+    }
+#pragma unroll
+    for (int c = 0; c < kBlkFields; ++c) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) cnt[c] += __shfl_xor_sync(0xffffffffu, cnt[c], o);
+    }
+    __syncthreads();  // s_cat cleared
+    if (lane == 0) {
+#pragma unroll
+      for (int c = 0; c < kBlkFields; ++c) atomicAdd(&s_cat[c], cnt[c]);
+    }
+    __syncthreads();
+  }
+  const bool any_anom = s_cat[C_ANOM] != 0;
+  const bool force = d.host_fallback || any_anom;
+  const int n_fresh = force ? n : n - s_cat[C_REUSE];
+  const int fresh_before = force ? lo : lo - s_cat[C_REUSE_BEFORE];
+  if (b == 0 && tid == 0) {
+    const int fb = (d.host_fallback ? 1 : 0) | (any_anom ? 2 : 0);
+    ws.ctrl->n_fresh = n_fresh;
+    ws.ctrl->fallback = fb;
+    ws.ctrl->n_edges = n_fresh * k;
+    epoch_iter_stats *st = ws.stats;
+    st->iteration = d.iter;
+    st->n_pos = n;
+    st->n_live = s_cat[C_LIVE];
+    st->n_new = s_cat[C_NEW];
+    st->n_miss = s_cat[C_MISS];
+    st->n_stale = s_cat[C_STALE];
+    st->n_forced = force ? s_cat[C_REUSE] : 0;
+    st->n_reuse = force ? 0 : s_cat[C_REUSE];
+    st->n_fresh = n_fresh;
+    st->n_edges = n_fresh * k;
+    st->support_len = fb ? E : ws.ctrl->support_len;
+    st->fallback = fb;
+    st->bad_flags = s_cat[C_BAD];
+    if (s_cat[C_BAD]) set_error(ws.err, EPOCH_DEVERR_FLAGS);
+  }
+  {
+    const int t = lo + tid;
+    const bool mine = t < hi;
+    bool il = false, fresh = false;
+    if (mine) {
+      const int code = classify(t);
+      il = (code & 16) != 0;
+      fresh = (code & 15) != C_REUSE || force;
+    }
+    int slice_fresh;
+    const int rank = block_excl_scan(fresh ? 1 : 0, tmp, &slice_fresh);
+    if (mine) {
+      if (fresh) {
+        const int f = fresh_before + rank;
+        ws.fresh_pos[f] = t;
+        ws.fidx[t] = f;
+        stamp_new[t] = d.iter;
+      } else {
+        ws.fidx[t] = -1;
+        stamp_new[t] = stamp_old[t];
+      }
+      prev_new[t] = il ? 0 : 1;
+      s_rank[tid] = static_cast<int16_t>(fresh ? rank : -1);
+    }
+  }
+  __syncthreads();  // s_rank
   if (trace_r && tid == 0) trace_r[1] = static_cast<int64_t>(globaltimer_ns());
 
-  // ---- phase A': fresh list in position order
-  int anom = 0, before = 0, total = 0, sum_cat[kBlkFields];
-#pragma unroll
-  for (int c = 0; c < kBlkFields; ++c) sum_cat[c] = 0;
-  for (int j = tid; j < G; j += kRoutingThreads) anom |= ws.blk[j * kBlkFields + B_ANOM];
-  const bool any_anom = __syncthreads_or(anom) != 0;
-  const bool force = d.host_fallback || any_anom;
-  {
-    int part_before = 0, part_total = 0;
-    for (int j = tid; j < G; j += kRoutingThreads) {
-      const int fr = ws.blk[j * kBlkFields + B_SLICE] - (force ? 0 : ws.blk[j * kBlkFields + B_REUSE]);
-      part_total += fr;
-      if (j < b) part_before += fr;
-    }
-    (void)block_excl_scan(part_before, tmp, &before);
-    (void)block_excl_scan(part_total, tmp, &total);
-  }
-  const bool fresh = mine && (!reuse || force);
-  int cnt_unused;
-  const int rank = block_excl_scan(fresh ? 1 : 0, tmp, &cnt_unused);
-  if (mine) {
-    if (fresh) {
-      const int f = before + rank;
-      ws.fresh_pos[f] = t;
-      ws.fidx[t] = f;
-      ws.stamp[t] = d.iter;
-    } else {
-      ws.fidx[t] = -1;
-    }
-    ws.prev_dec[t] = is_live ? 0 : 1;
-  }
-  const int n_fresh = total;
-  if (!grid_sync(ws.gbar, 2u * G, ws.err, tmo, &s_ok)) return;
+  // ---- phase 1b, after the gate kernel: one warp per slice row sums G from
+  // the split-K partials in a fixed order plus the bias, writes the row, and
+  // for a fresh position takes the top-k over the support mask (every expert on
+  // a fallback) and the softmax weights over the selected logits ([W] section
+  // "Expert Atlas", step three); bit (f mod 32) of word (e, f / 32) marks that
+  // fresh position f selected expert e (words zeroed by the gate kernel).
+  pdl_wait();
   if (trace_r && tid == 0) trace_r[2] = static_cast<int64_t>(globaltimer_ns());
-
-  // ---- phase B: support-restricted top-k, one warp per fresh position
-  for (int f = b * nwarps + wid; f < n_fresh; f += G * nwarps) {
-    const int tp = ws.fresh_pos[f];
+  for (int r = wid; r < hi - lo; r += nwarps) {
+    const int t = lo + r;
     float v[EPL];
+    lane_logits<EPL>(ws.gparts, d.SK, d.Nmax, E, t, bias, v);
+    float *lrow = ws.logits + static_cast<size_t>(t) * E;
+    const int e0 = lane * EPL;
+    if (EPL % 4 == 0 && (E & 3) == 0 && e0 + EPL <= E) {
+#pragma unroll
+      for (int q = 0; q < EPL / 4; ++q)
+        reinterpret_cast<float4 *>(lrow + e0)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    } else {
+#pragma unroll
+      for (int c = 0; c < EPL; ++c)
+        if (e0 + c < E) lrow[e0 + c] = v[c];
+    }
+    const int rank = s_rank[r];
+    if (rank < 0) continue;
+    const int f = fresh_before + rank;
     bool ok[EPL];
-    lane_logits<EPL>(ws.logits, 1, d.Nmax, E, tp, nullptr, v);
 #pragma unroll
     for (int c = 0; c < EPL; ++c) {
-      const int e = lane * EPL + c;
+      const int e = e0 + c;
       ok[c] = e < E && (force || ws.support_mask[e]);
     }
     int sel;
@@ -422,7 +465,7 @@ __device__ __forceinline__ void routing_body(const Dims &d, const Work &ws, cons
     float denom = 0.f;  // summed in selection order j = 0..k-1 (deterministic)
     for (int j = 0; j < k; ++j) denom += __shfl_sync(0xffffffffu, ex, j);
     if (lane < k) {
-      if (sel < 0 || sel >= E) {
+      if (sel < 0 || sel >= E || f >= n_fresh) {
         set_error(ws.err, EPOCH_DEVERR_BOUNDS);
       } else {
         ws.sel[f * k + lane] = sel;
@@ -431,7 +474,7 @@ __device__ __forceinline__ void routing_body(const Dims &d, const Work &ws, cons
       }
     }
   }
-  if (!grid_sync(ws.gbar, 3u * G, ws.err, tmo, &s_ok)) return;
+  if (!grid_sync(ws.gbar, 1u * G, ws.err, tmo, &s_ok)) return;
   if (trace_r && tid == 0) trace_r[3] = static_cast<int64_t>(globaltimer_ns());
 
   // ---- phase C: expert offsets, worklist rows, compact copies of x, tile lists
@@ -465,9 +508,10 @@ __device__ __forceinline__ void routing_body(const Dims &d, const Work &ws, cons
     if (tid == 0) s_off[E] = tot;
     __syncthreads();
   }
-  // With more than one CTA, CTA 0 writes the statistics and the tile prefix
-  // (nothing later in this kernel waits on it) while the others place the
-  // worklist rows, meet at barrier 4 and copy the rows.
+  // With more than one CTA, CTA 0 writes the expert offsets and the group list
+  // while the others place the worklist rows, meet at a second barrier and copy
+  // each worklist row of x into the compact buffer; the expert kernel starts
+  // once every CTA has counted itself done.
   const bool split = G > 1;
   const int wb = split ? b - 1 : b, wg = split ? G - 1 : G;  // worker CTAs
   if (!(split && b == 0)) {
@@ -494,7 +538,7 @@ __device__ __forceinline__ void routing_body(const Dims &d, const Work &ws, cons
     }
     if (trace_r && tid == 0) trace_r[4] = static_cast<int64_t>(globaltimer_ns());
     if (split) {
-      if (!grid_sync(ws.gbar, 3u * G + (G - 1), ws.err, tmo, &s_ok)) return;
+      if (!grid_sync(ws.gbar, 1u * G + (G - 1), ws.err, tmo, &s_ok)) return;
     } else {
       __syncthreads();
     }
@@ -502,49 +546,6 @@ __device__ __forceinline__ void routing_body(const Dims &d, const Work &ws, cons
     trace_r[4] = static_cast<int64_t>(globaltimer_ns());
   }
   if (b == 0) {
-    // sums of the per-CTA category counts: thread j reads CTA j's record (two
-    // 16-byte loads), then a warp-shuffle and shared-memory reduction
-    for (int j = tid; j < G; j += kRoutingThreads) {
-      const int4 u = reinterpret_cast<const int4 *>(ws.blk + j * kBlkFields)[0];
-      const int4 w2 = reinterpret_cast<const int4 *>(ws.blk + j * kBlkFields)[1];
-      sum_cat[0] += u.x; sum_cat[1] += u.y; sum_cat[2] += u.z; sum_cat[3] += u.w;
-      sum_cat[4] += w2.x; sum_cat[5] += w2.y; sum_cat[6] += w2.z; sum_cat[7] += w2.w;
-    }
-#pragma unroll
-    for (int c = 0; c < kBlkFields; ++c) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) sum_cat[c] += __shfl_xor_sync(0xffffffffu, sum_cat[c], o);
-    }
-    if (tid < kBlkFields) s_cat[tid] = 0;
-    __syncthreads();
-    if (lane == 0) {
-#pragma unroll
-      for (int c = 0; c < kBlkFields; ++c) atomicAdd(&s_cat[c], sum_cat[c]);
-    }
-    __syncthreads();
-#pragma unroll
-    for (int c = 0; c < kBlkFields; ++c) sum_cat[c] = s_cat[c];
-    if (tid == 0) {
-      const int fb = (d.host_fallback ? 1 : 0) | (any_anom ? 2 : 0);
-      ws.ctrl->n_fresh = n_fresh;
-      ws.ctrl->fallback = fb;
-      ws.ctrl->n_edges = n_fresh * k;
-      epoch_iter_stats *st = ws.stats;
-      st->iteration = d.iter;
-      st->n_pos = n;
-      st->n_live = sum_cat[B_LIVE];
-      st->n_new = sum_cat[B_NEW];
-      st->n_miss = sum_cat[B_MISS];
-      st->n_stale = sum_cat[B_STALE];
-      st->n_forced = force ? sum_cat[B_REUSE] : 0;
-      st->n_reuse = force ? 0 : sum_cat[B_REUSE];
-      st->n_fresh = n_fresh;
-      st->n_edges = n_fresh * k;
-      st->support_len = fb ? E : ws.ctrl->support_len;
-      st->fallback = fb;
-      st->bad_flags = sum_cat[B_BAD];
-      if (sum_cat[B_BAD]) set_error(ws.err, EPOCH_DEVERR_FLAGS);
-    }
     for (int e = tid; e <= E; e += kRoutingThreads) ws.offsets[e] = s_off[e];
     if (trace_r && tid == 0) trace_r[5] = static_cast<int64_t>(globaltimer_ns());
     write_group_tiles(d, ws, s_off, tmp, n);
@@ -552,7 +553,7 @@ __device__ __forceinline__ void routing_body(const Dims &d, const Work &ws, cons
     if (split) return;
   }
 
-  // ---- phase D: copy each worklist row of x into the compact buffer
+  // ---- phase 3: copy each worklist row of x into the compact buffer
   const int n_edges = n_fresh * k;
   for (int l = wb * nwarps + wid; l < n_edges; l += wg * nwarps) {
     const int tp = ws.wl_pos[l];
@@ -627,7 +628,8 @@ __device__ __forceinline__ void store8(__nv_bfloat16 *p, const float (&v)[8]) {
   *reinterpret_cast<uint4 *>(p) = u;
 }
 
-// One CTA per position, 8 elements per thread per pass. Fresh t:
+// One CTA per position, 8 elements per thread per pass. Expert outputs O are
+// stored in the layer dtype. Fresh t:
 // r = sum_j w_j O[slot(t, j)] (j ascending, fp32) and the cache row is refilled
 // ([W] section "Liveness-Shard Parallelism": Y[F_i] = Y_F); reused t: r = the
 // cached row (Y[not F_i] = C_l[not F_i]). Then y = r + shared outputs (+ x when
@@ -660,7 +662,7 @@ __global__ void __launch_bounds__(128) k_combine(Dims d, Work ws, const T *__res
       for (int q = 0; q < 8; ++q) r[q] = 0.f;
       for (int j = 0; j < k; ++j) {
         float o[8];
-        load8(ws.o_int + static_cast<size_t>(slot_s[j]) * H + h0, o);
+        load8(static_cast<const T *>(ws.o_int) + static_cast<size_t>(slot_s[j]) * H + h0, o);
         const float wj = w_s[j];
 #pragma unroll
         for (int q = 0; q < 8; ++q) r[q] = fmaf(wj, o[q], r[q]);
@@ -671,7 +673,7 @@ __global__ void __launch_bounds__(128) k_combine(Dims d, Work ws, const T *__res
     }
     for (int s = 0; s < d.n_sh; ++s) {
       float o[8];
-      load8(ws.o_sh + (static_cast<size_t>(s) * d.Nmax + t) * H + h0, o);
+      load8(static_cast<const T *>(ws.o_sh) + (static_cast<size_t>(s) * d.Nmax + t) * H + h0, o);
 #pragma unroll
       for (int q = 0; q < 8; ++q) r[q] += o[q];
     }
@@ -813,11 +815,11 @@ cudaError_t launch_routing(const Dims &d, const Weights &w, const Work &ws, cons
   // slices of at most kRoutingThreads positions per CTA
   const int min_grid = (d.n_pos + kRoutingThreads - 1) / kRoutingThreads;
   if (grid < min_grid) return cudaErrorInvalidConfiguration;
-  const int vec = d.H * (bf16 ? 2 : 4) / 16;
   const float *bias = w.b_router;
-  const uint4 *xv = static_cast<const uint4 *>(x);
   Dims dd = d;
   Work ww = ws;
+  const int vec = d.H * (bf16 ? 2 : 4) / 16;
+  const uint4 *xv = static_cast<const uint4 *>(x);
   void *args[] = {&dd, &ww, const_cast<float **>(&bias), const_cast<uint8_t **>(&live),
                   const_cast<uint8_t **>(&decoded), const_cast<uint4 **>(&xv), const_cast<int *>(&vec)};
   switch (epl_for(d.E)) {

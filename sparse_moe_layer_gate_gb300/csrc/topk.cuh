@@ -15,17 +15,16 @@ __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib)
   return va > vb || (va == vb && ia < ib);
 }
 
-// Warp-wide arg-best of (v, id) pairs; every lane returns the winner.
-__device__ __forceinline__ void warp_best(float &v, int &id) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, id, o);
-    if (ranks_before(ov, oi, v, id)) {
-      v = ov;
-      id = oi;
-    }
-  }
+// Unsigned key with the order of the float value: positive values get the
+// sign bit set, negative values are inverted. -0 is folded into +0 and NaN into
+// -inf first, so keys compare exactly like ranks_before's values.
+__device__ __forceinline__ unsigned order_key(float v) {
+  const float c = v != v ? -INFINITY : v + 0.0f;
+  const unsigned b = __float_as_uint(c);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(unsigned k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
 // Logits of the EPL consecutive experts [lane*EPL, lane*EPL + EPL) of position
@@ -116,17 +115,22 @@ __device__ __forceinline__ void warp_topk(float (&v)[EPL], const bool (&ok)[EPL]
       }
     }
   }
+  // k rounds over the lanes' list heads. A head's value is mapped to an
+  // unsigned key whose order is the float order (-0 folded into +0 and NaN
+  // into -inf, so equal values share a key); one warp max-reduction finds the
+  // best value, a min-reduction the lowest id among the lanes holding it, and
+  // the winning lane pops its head.
   *my_sel = -1;
   *my_val = -INFINITY;
   for (int j = 0; j < k; ++j) {
-    float bv = v[0];
-    int bi = id[0];
-    warp_best(bv, bi);
+    const unsigned key = order_key(v[0]);
+    const unsigned best = __reduce_max_sync(0xffffffffu, key);
+    const int bi = __reduce_min_sync(0xffffffffu, key == best ? id[0] : INT_MAX);
     if (lane == j) {
       *my_sel = bi;
-      *my_val = bv;
+      *my_val = key_value(best);
     }
-    if (id[0] == bi) {  // the winning lane pops its head
+    if (id[0] == bi) {
 #pragma unroll
       for (int c = 0; c + 1 < EPL; ++c) {
         v[c] = v[c + 1];
