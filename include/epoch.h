@@ -135,9 +135,6 @@ typedef struct {
   const int32_t *support_ids;  /* [E] experts in rank order; first *support_len valid */
   const int32_t *support_len;  /* [1] */
   const int32_t *plan_counts;  /* [E] block-start top-k hit counts */
-  const float *logit_parts;    /* [n_logit_parts][max_positions][E] partial sums of x W_r^T over
-                                  disjoint slices of H (no bias); G = their sum + b_router */
-  int32_t n_logit_parts;
   const float *logits;         /* [max_positions][E] G of the last iteration, bias included */
   const int32_t *fresh_pos;    /* [n_fresh] ascending fresh positions */
   const int32_t *sel;          /* [n_fresh][k] selected experts, selection order */

@@ -45,7 +45,7 @@ class epoch_iter_stats(C.Structure):
 
 class epoch_debug_view(C.Structure):
     _fields_ = [("support_ids", C.c_void_p), ("support_len", C.c_void_p), ("plan_counts", C.c_void_p),
-                ("logit_parts", C.c_void_p), ("n_logit_parts", C.c_int32), ("logits", C.c_void_p),
+                ("logits", C.c_void_p),
                 ("fresh_pos", C.c_void_p),
                 ("sel", C.c_void_p), ("sel_w", C.c_void_p), ("offsets", C.c_void_p),
                 ("wl_pos", C.c_void_p), ("slot", C.c_void_p), ("stamp", C.c_void_p),

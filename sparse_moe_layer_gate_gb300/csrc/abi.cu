@@ -22,13 +22,11 @@ using namespace epoch;
 
 struct epoch_layer {
   epoch_layer_config cfg;
-  Dims dims;  // static part (n_pos, iter, host_fallback, SK filled per call)
+  Dims dims;  // static part (n_pos, iter, host_fallback filled per call)
   Weights w;
   Work ws;
   Maps maps;
   bool bf16;
-  int sk_max;
-  int last_sk;
   // block-plan state
   bool planned;
   int32_t n_pos_plan;
@@ -70,12 +68,6 @@ bool valid_config(const epoch_layer_config *c) {
   return true;
 }
 
-int sk_max_for(const epoch_layer_config &c) {
-  if (c.dtype != EPOCH_BF16) return 1;
-  const int kb = c.hidden / 64;
-  return kb < 16 ? kb : 16;
-}
-
 // Lays the workspace out (base == nullptr: only measures). Returns total bytes.
 size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   size_t off = 0;
@@ -96,7 +88,6 @@ size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   t.support_ids = static_cast<int32_t *>(take(E * 4));
   t.plan_counts = static_cast<int32_t *>(take(E * 4));
   t.cache = take(N * H * act);
-  t.gparts = static_cast<float *>(take(static_cast<size_t>(sk_max_for(c)) * N * E * 4));
   t.logits = static_cast<float *>(take(N * E * 4));
   t.fidx = static_cast<int32_t *>(take(N * 4));
   t.fresh_pos = static_cast<int32_t *>(take(N * 4));
@@ -180,22 +171,16 @@ Dims call_dims(const epoch_layer *L, int32_t n_pos, int32_t iter, int host_fallb
   return d;
 }
 
-// G for every position: tcgen05 split-K for bf16 layers, FFMA for fp32 layers.
-// x_maps[0] (box kTnGate rows) feeds the gate, x_maps[1] (box kTnUp rows) the
-// shared experts' up-projection.
+// G = x W_r^T + b for every position: tcgen05 for bf16 layers, FFMA for fp32
+// layers. x_maps[0] (box kTnGate rows) feeds the gate, x_maps[1] (box kTnUp
+// rows) the shared experts' up-projection.
 epoch_status run_gate(epoch_layer *L, Dims &d, const void *x, CUtensorMap *x_maps, cudaStream_t s) {
   if (L->bf16) {
-    d.SK = tc_gate_splits(d);
-    if (d.SK > L->sk_max) d.SK = L->sk_max;
-    while ((d.H / 64) % d.SK) --d.SK;
     if (!encode_kmajor_bf16(&x_maps[0], x, d.H, d.n_pos, kTnGate) ||
         !encode_kmajor_bf16(&x_maps[1], x, d.H, d.n_pos, kTnUp))
       return EPOCH_ECUDA;
-    L->last_sk = d.SK;
-    return run(L, K_GATE, s, [&] { return launch_gate_tc(d, L->maps, L->ws, x_maps[0], s); });
+    return run(L, K_GATE, s, [&] { return launch_gate_tc(d, L->maps, L->ws, x_maps[0], L->w.b_router, s); });
   }
-  d.SK = 1;
-  L->last_sk = 1;
   return run(L, K_GATE, s, [&] { return launch_gate_simt(d, L->w, L->ws, x, 0, s); });
 }
 
@@ -222,8 +207,6 @@ epoch_status epoch_layer_create(const epoch_layer_config *cfg, const epoch_layer
   if (L == nullptr) return EPOCH_ECUDA;
   L->cfg = *cfg;
   L->bf16 = cfg->dtype == EPOCH_BF16;
-  L->sk_max = sk_max_for(*cfg);
-  L->last_sk = 1;
   carve(*cfg, static_cast<char *>(workspace), &L->ws);
   L->w = Weights{w->w_router, w->b_router, w->w_gate, w->w_up, w->w_down, w->ws_gate, w->ws_up, w->ws_down};
   Dims &d = L->dims;
@@ -235,7 +218,6 @@ epoch_status epoch_layer_create(const epoch_layer_config *cfg, const epoch_layer
   d.n_sh = cfg->n_shared;
   d.I_s = cfg->n_shared ? cfg->shared_inter : 128;
   d.Nmax = cfg->max_positions;
-  d.SK = 1;
   d.R = cfg->refresh_R;
   d.residual = cfg->residual ? 1 : 0;
   d.tn = L->bf16 ? kTnUp : 0;
@@ -388,9 +370,7 @@ epoch_status epoch_debug_pointers(epoch_layer *L, epoch_debug_view *v) {
   v->support_ids = L->ws.support_ids;
   v->support_len = &L->ws.ctrl->support_len;
   v->plan_counts = L->ws.plan_counts;
-  v->logit_parts = L->ws.gparts;
   v->logits = L->ws.logits;
-  v->n_logit_parts = L->last_sk;
   v->fresh_pos = L->ws.fresh_pos;
   v->sel = L->ws.sel;
   v->sel_w = L->ws.selw;

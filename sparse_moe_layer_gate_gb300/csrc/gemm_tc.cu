@@ -1,10 +1,9 @@
 // tcgen05 + TMA GEMMs of the Epoch MoE layer (bf16 in, fp32 accumulate).
 //
 // Two persistent, warp-specialised kernels:
-//   k_tc_gate     G^T = W_r x^T, split along H (the routing kernel sums the
-//                 splits in a fixed order and adds the bias) -- router logits
-//                 for every position ([W] section "Expert Atlas": G in
-//                 R^{N x E}, recomputed every iteration);
+//   k_tc_gate     G = x W_r^T + b for every position, one CTA per (128
+//                 experts, 32 tokens) tile over all of H ([W] section "Expert
+//                 Atlas": G in R^{N x E}, recomputed every iteration);
 //   k_tc_experts  per group g, UP: A_g = silu(X_g W_gate,g^T) * (X_g W_up,g^T)
 //                 and DOWN: O_g = A_g W_down,g^T, both stored as bf16, in one
 //                 launch with per-group dependencies.
@@ -49,7 +48,13 @@ struct __align__(128) TcParams {
   Dims d;
   Work ws;
   int32_t gate_tiles;
+  const float *bias;  // gate: router bias [E]
 };
+
+// The gate accumulates H in chunks of kGateChunkKb K blocks (256 elements), one
+// TMEM accumulator per chunk, and the epilogue adds the chunks in order in fp32:
+// a 2048- or 4096-term dot product is not one long tensor-core accumulation.
+constexpr int kGateChunkKb = 4;
 
 template <int TN, int STAGES>
 struct GateCfg {
@@ -66,7 +71,7 @@ struct GateCfg {
   static constexpr int STG_ROW = 144;
   static constexpr int STG_BYTES = 32 * STG_ROW;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 4 * STG_BYTES + NBARS * 8 + 16;
-  static_assert(TN % 16 == 0 && TN >= 16 && TN <= 256, "MMA N");
+  static_assert(TN == 32, "the epilogue reads one 32-column accumulator per chunk");
   static_assert(USED_COLS <= 512, "TMEM");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
@@ -81,24 +86,23 @@ struct GateTile {
   float *out;
 };
 
-// Gate tile t = (split ks, expert block m, token tile tt), token tiles fastest.
+// Gate tile t = (expert block m, token tile tt), token tiles fastest; the
+// whole of H in one accumulator (no split partials, one fixed summation order).
 template <int TN>
 __device__ __forceinline__ GateTile gate_tile(const TcParams &p, int tile) {
   const Dims &d = p.d;
   GateTile t;
-  const int mt = (d.E + BM - 1) / BM, nt = (d.n_pos + TN - 1) / TN;
-  const int ks = tile / (mt * nt), rem = tile % (mt * nt);
-  const int m = rem / nt, tt = rem % nt;
-  const int kspan = d.H / d.SK;
+  const int nt = (d.n_pos + TN - 1) / TN;
+  const int m = tile / nt, tt = tile % nt;
   t.a_row = m * BM;
   t.b_row = tt * TN;
-  t.k0 = ks * kspan;
-  t.nk = kspan / BK;
+  t.k0 = 0;
+  t.nk = d.H / BK;
   t.n_valid = min(TN, d.n_pos - tt * TN);
   t.out_row0 = tt * TN;
   t.col0 = m * BM;
   t.m_limit = min(BM, d.E - m * BM);
-  t.out = p.ws.gparts + static_cast<size_t>(ks) * d.Nmax * d.E;
+  t.out = p.ws.logits;
   return t;
 }
 
@@ -234,10 +238,16 @@ __global__ void __launch_bounds__(192, 1) k_tc_gate(const __grid_constant__ TcPa
         ++n_tiles;
         n_cols += t.n_valid;
         const uint32_t idesc = idesc_bf16_f32(BM, n_mma);
-        if (!mbar_wait_bounded(tempty_bar(buf), bphase ^ 1u, abort_flag, ws.err, tmo)) break;
-        tc_fence_after();
-        const uint32_t d0 = tmem_base + static_cast<uint32_t>(buf * C::ACC_COLS);
+        uint32_t d0 = 0;
         for (int kb = 0; kb < t.nk; ++kb) {
+          if (kb % kGateChunkKb == 0) {  // a new chunk starts in the next accumulator buffer
+            if (!mbar_wait_bounded(tempty_bar(buf), bphase ^ 1u, abort_flag, ws.err, tmo)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            d0 = tmem_base + static_cast<uint32_t>(buf * C::ACC_COLS);
+          }
           if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, ws.err, tmo)) {
             ok = false;
             break;
@@ -251,7 +261,7 @@ __global__ void __launch_bounds__(192, 1) k_tc_gate(const __grid_constant__ TcPa
           const uint64_t bd = sw128_kmajor_desc(sB + stage * C::B_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint32_t acc = (kb | kk) != 0;
+            const uint32_t acc = ((kb % kGateChunkKb) | kk) != 0;
             tc_mma_bf16(d0, ad0 + 2u * kk, bd + 2u * kk, idesc, acc);
           }
           tc_commit(empty_bar(stage));
@@ -259,13 +269,15 @@ __global__ void __launch_bounds__(192, 1) k_tc_gate(const __grid_constant__ TcPa
             stage = 0;
             phase ^= 1u;
           }
+          if (kb % kGateChunkKb == kGateChunkKb - 1 || kb == t.nk - 1) {  // chunk done
+            tc_commit(tfull_bar(buf));
+            if (++buf == C::NBUF) {
+              buf = 0;
+              bphase ^= 1u;
+            }
+          }
         }
         if (!ok) break;
-        tc_commit(tfull_bar(buf));
-        if (++buf == C::NBUF) {
-          buf = 0;
-          bphase ^= 1u;
-        }
       }
       tc_commit(done_bar);
       mbar_drain(done_bar, 0, 50000000ull);
@@ -278,27 +290,50 @@ __global__ void __launch_bounds__(192, 1) k_tc_gate(const __grid_constant__ TcPa
     __syncwarp();
   } else {
     // ---------------- epilogue (warps 2..5; warp w reads TMEM lanes 32*(w%4)..)
-    // Per 32 token columns: one 32-column TMEM load, the values of this warp's
-    // 32 rows staged token by token in shared memory, then eight lanes store
-    // one token's 32 contiguous logits (128 bytes) together, four tokens per
-    // instruction.
+    // Per chunk: one 32-column TMEM load added into registers; then the sums
+    // of this warp's 32 rows (+ bias) are staged token by token in shared
+    // memory and eight lanes store one token's 32 contiguous logits (128 bytes)
+    // together, four tokens per instruction.
     const int q = wid & 3;
     uint8_t *stg = stage_out + (wid - 2) * C::STG_BYTES;
     int buf = 0;
     uint32_t bphase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
       const GateTile t = gate_tile<TN>(p, tile);
-      if (!mbar_wait_bounded(tfull_bar(buf), bphase, abort_flag, ws.err, tmo)) break;
-      tc_fence_after();
-      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * C::ACC_COLS);
-      const int rows_valid = min(32, max(0, t.m_limit - q * 32));
-      const bool vec_ok = rows_valid == 32 && ((d.E * 4) & 15) == 0;
-      for (int c0 = 0; c0 < t.n_valid; c0 += 32) {
-        float v0[32];
-        tmem_ld32(tb + c0, v0);
+      // sum the chunk accumulators in chunk order (fp32), then add the bias
+      float sum[TN];
+#pragma unroll
+      for (int c = 0; c < TN; ++c) sum[c] = 0.f;
+      const int n_chunks = (t.nk + kGateChunkKb - 1) / kGateChunkKb;
+      for (int ch = 0; ch < n_chunks; ++ch) {
+        if (!mbar_wait_bounded(tfull_bar(buf), bphase, abort_flag, ws.err, tmo)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * C::ACC_COLS);
+        float v0[TN];
+        tmem_ld32(tb, v0);
         tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) reinterpret_cast<float *>(stg + c * C::STG_ROW)[lane] = v0[c];
+        for (int c = 0; c < TN; ++c) sum[c] += v0[c];
+        tc_fence_before();
+        mbar_arrive(tempty_bar(buf));
+        if (++buf == C::NBUF) {
+          buf = 0;
+          bphase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      const int rows_valid = min(32, max(0, t.m_limit - q * 32));
+      const int e_row = t.col0 + q * 32 + lane;  // this lane's TMEM row = expert
+      const float bias_r = e_row < d.E ? __ldg(p.bias + e_row) : 0.f;
+      const bool vec_ok = rows_valid == 32 && ((d.E * 4) & 15) == 0;
+      {
+        const int c0 = 0;
+#pragma unroll
+        for (int c = 0; c < TN; ++c) reinterpret_cast<float *>(stg + c * C::STG_ROW)[lane] = sum[c] + bias_r;
         __syncwarp();
         const int ncol = min(32, t.n_valid - c0);
         if (vec_ok) {
@@ -323,12 +358,6 @@ __global__ void __launch_bounds__(192, 1) k_tc_gate(const __grid_constant__ TcPa
           }
         }
         __syncwarp();
-      }
-      tc_fence_before();
-      mbar_arrive(tempty_bar(buf));
-      if (++buf == C::NBUF) {
-        buf = 0;
-        bphase ^= 1u;
       }
     }
     if (trace && wid == 2 && lane == 0) trace[4] = static_cast<int64_t>(globaltimer_ns());
@@ -934,21 +963,7 @@ bool encode_kmajor_bf16(CUtensorMap *map, const void *base, uint64_t k_elems, ui
   return r == CUDA_SUCCESS;
 }
 
-constexpr int kStGate = 6;
-
-// Split count of the gate along H: enough (m, n, split) tiles to cover the SMs,
-// each split a whole number of 64-wide K blocks.
-int tc_gate_splits(const Dims &d) {
-  const int tiles_mn = ((d.E + BM - 1) / BM) * ((d.n_pos + kTnGate - 1) / kTnGate);
-  const int kb = d.H / BK;
-  int target = num_sms() / (tiles_mn > 0 ? tiles_mn : 1);
-  if (target < 1) target = 1;
-  if (target > 16) target = 16;
-  int sk = 1;
-  for (int c = 1; c <= target; ++c)
-    if (kb % c == 0) sk = c;
-  return sk;
-}
+constexpr int kStGate = 8;  // 20 KB stages (a 128 x 64 W_r tile and a 32 x 64 x tile)
 
 template <int TN, int STAGES>
 static cudaError_t launch_gate(const TcParams &p, int grid, cudaStream_t s) {
@@ -971,12 +986,13 @@ static void base_params(TcParams &p, const Dims &d, const Work &ws) {
 }
 
 cudaError_t launch_gate_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map,
-                           cudaStream_t s) {
+                           const float *bias, cudaStream_t s) {
   TcParams p;
   base_params(p, d, ws);
   p.a0 = m.w_router;
+  p.bias = bias;
   p.b[0] = x_map;
-  const int tiles = ((d.E + BM - 1) / BM) * ((d.n_pos + kTnGate - 1) / kTnGate) * d.SK;
+  const int tiles = ((d.E + BM - 1) / BM) * ((d.n_pos + kTnGate - 1) / kTnGate);
   p.gate_tiles = tiles;
   const int grid = tiles < num_sms() ? tiles : num_sms();
   return launch_gate<kTnGate, kStGate>(p, grid, s);

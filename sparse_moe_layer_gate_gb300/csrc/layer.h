@@ -34,8 +34,7 @@ struct Work {
   int32_t *plan_counts;   // [E] block-start hit counts
   void *cache;            // [Nmax][H] routed-output cache, layer dtype
   // one iteration
-  float *gparts;          // [SK][Nmax][E] split-K partial logits (no bias)
-  float *logits;          // [Nmax][E] G = sum of the partials + bias (routing kernel, phase A)
+  float *logits;          // [Nmax][E] G = x W_r^T + b (gate kernel)
   int32_t *fidx;          // [Nmax] fresh index of a position, -1 if reused
   int32_t *fresh_pos;     // [Nmax] ascending fresh positions
   int32_t *sel;           // [Nmax][k]
@@ -83,7 +82,7 @@ constexpr int kRoutingThreads = 512;
 
 // Shapes and per-call values handed to every kernel by value.
 struct Dims {
-  int32_t H, E, I, k, n_sh, I_s, Nmax, SK;
+  int32_t H, E, I, k, n_sh, I_s, Nmax;
   int32_t R;         // refresh period (INT32_MAX = never)
   int32_t residual;
   int32_t n_pos;
@@ -179,14 +178,13 @@ cudaError_t launch_pack_tiles(const void *src, int64_t rows, int64_t k, uint8_t 
                               int64_t tile_off, int pair, cudaStream_t s);
 bool tma_encode_init();
 bool encode_kmajor_bf16(CUtensorMap *map, const void *base, uint64_t k_elems, uint64_t rows, uint32_t box_rows);
-int tc_gate_splits(const Dims &d);
-constexpr int kTnGate = 128;  // gate token tile (x box rows)
+constexpr int kTnGate = 32;   // gate token tile (x box rows)
 constexpr int kTnUp = 128;    // expert-kernel token tiles (up and down)
 constexpr int kTnDn = 128;
 constexpr int kBmDn = 256;    // rows of H per down tile (two 128-row MMAs)
 constexpr int kGrpIdBits = 11;  // group id field of a grp_list entry (E + n_sh <= 1024 < 2^11)
 cudaError_t launch_gate_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map,
-                           cudaStream_t s);
+                           const float *bias, cudaStream_t s);
 cudaError_t launch_experts_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map_up,
                               cudaStream_t s);
 

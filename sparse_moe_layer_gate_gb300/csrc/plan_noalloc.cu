@@ -58,7 +58,7 @@ __global__ void k_noalloc_topk(const float *__restrict__ logits, int n_pos, int 
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n_pos; t += warps) {
     float v[EPL];
     bool ok[EPL];
-    lane_logits<EPL>(logits, 1, n_pos, E, t, nullptr, v);
+    lane_logits<EPL>(logits + static_cast<size_t>(t) * E, E, v);
 #pragma unroll
     for (int c = 0; c < EPL; ++c) ok[c] = lane * EPL + c < E;
     int sel;

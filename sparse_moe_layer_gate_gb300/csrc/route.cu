@@ -55,11 +55,11 @@ __device__ __forceinline__ int block_excl_scan(int v, int *warp_tmp, int *total)
 }
 
 // ---------------------------------------------------------------- gate (SIMT)
-// G part 0 = x W_r^T for fp32 layers: one warp per (position, expert), lanes
+// G = x W_r^T + b for fp32 layers: one warp per (position, expert), lanes
 // split H, fixed-order reduction (deterministic).
 template <typename T>
-__global__ void k_gate_simt(Dims d, const T *__restrict__ x, const T *__restrict__ wr, float *__restrict__ g,
-                            Work ws) {
+__global__ void k_gate_simt(Dims d, const T *__restrict__ x, const T *__restrict__ wr, const float *__restrict__ bias,
+                            float *__restrict__ g, Work ws) {
   if (blockIdx.x == 0) {  // counters of the next routing and expert launches
     if (threadIdx.x == 0) {
       *ws.gbar = 0u;
@@ -77,21 +77,20 @@ __global__ void k_gate_simt(Dims d, const T *__restrict__ x, const T *__restrict
     for (int h = lane; h < d.H; h += 32) acc = fmaf(to_f32(xr[h]), to_f32(wrow[h]), acc);
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-    if (lane == 0) g[static_cast<size_t>(t) * d.E + e] = acc;
+    if (lane == 0) g[static_cast<size_t>(t) * d.E + e] = acc + bias[e];
   }
 }
 
 // ---------------------------------------------------------------- block plan
 // Dense top-k of every position over all experts -> hit counts (integer atomics).
 template <int EPL>
-__global__ void k_plan_topk(Dims d, const float *__restrict__ gparts, const float *__restrict__ bias,
-                            int32_t *__restrict__ counts) {
+__global__ void k_plan_topk(Dims d, const float *__restrict__ logits, int32_t *__restrict__ counts) {
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int lane = lane_id();
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < d.n_pos; t += warps) {
     float v[EPL];
     bool ok[EPL];
-    lane_logits<EPL>(gparts, d.SK, d.Nmax, d.E, t, bias, v);
+    lane_logits<EPL>(logits + static_cast<size_t>(t) * d.E, d.E, v);
 #pragma unroll
     for (int c = 0; c < EPL; ++c) ok[c] = lane * EPL + c < d.E;
     int sel;
@@ -292,7 +291,7 @@ static_assert(C_REUSE_BEFORE < kBlkFields, "category counters");
 //     grouped by expert with positions ascending, and copies each row of x
 //     into the compact buffer. CTA 0 writes the grouped-GEMM tile lists.
 template <int EPL>
-__device__ __forceinline__ void routing_body(const Dims &d, const Work &ws, const float *__restrict__ bias,
+__device__ __forceinline__ void routing_body(const Dims &d, const Work &ws,
                                              const uint8_t *__restrict__ live, const uint8_t *__restrict__ decoded,
                                              const uint4 *__restrict__ x, int vec_per_row) {
   const KernelMark mark_(d, ws, K_ROUTING);
@@ -425,32 +424,19 @@ __device__ __forceinline__ void routing_body(const Dims &d, const Work &ws, cons
   __syncthreads();  // s_rank
   if (trace_r && tid == 0) trace_r[1] = static_cast<int64_t>(globaltimer_ns());
 
-  // ---- phase 1b, after the gate kernel: one warp per slice row sums G from
-  // the split-K partials in a fixed order plus the bias, writes the row, and
-  // for a fresh position takes the top-k over the support mask (every expert on
-  // a fallback) and the softmax weights over the selected logits ([W] section
+  // ---- phase 1b, after the gate kernel: one warp per fresh row of the slice
+  // takes the top-k of its logits over the support mask (every expert on a
+  // fallback) and the softmax weights over the selected logits ([W] section
   // "Expert Atlas", step three); bit (f mod 32) of word (e, f / 32) marks that
   // fresh position f selected expert e (words zeroed by the gate kernel).
   pdl_wait();
   if (trace_r && tid == 0) trace_r[2] = static_cast<int64_t>(globaltimer_ns());
   for (int r = wid; r < hi - lo; r += nwarps) {
-    const int t = lo + r;
-    float v[EPL];
-    lane_logits<EPL>(ws.gparts, d.SK, d.Nmax, E, t, bias, v);
-    float *lrow = ws.logits + static_cast<size_t>(t) * E;
-    const int e0 = lane * EPL;
-    if (EPL % 4 == 0 && (E & 3) == 0 && e0 + EPL <= E) {
-#pragma unroll
-      for (int q = 0; q < EPL / 4; ++q)
-        reinterpret_cast<float4 *>(lrow + e0)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-    } else {
-#pragma unroll
-      for (int c = 0; c < EPL; ++c)
-        if (e0 + c < E) lrow[e0 + c] = v[c];
-    }
     const int rank = s_rank[r];
     if (rank < 0) continue;
-    const int f = fresh_before + rank;
+    const int t = lo + r, f = fresh_before + rank, e0 = lane * EPL;
+    float v[EPL];
+    lane_logits<EPL>(ws.logits + static_cast<size_t>(t) * E, E, v);
     bool ok[EPL];
 #pragma unroll
     for (int c = 0; c < EPL; ++c) {
@@ -587,11 +573,11 @@ __device__ __forceinline__ void routing_body(const Dims &d, const Work &ws, cons
 // may already be running (programmatic dependent launch), acquires that count
 // instead of waiting for this grid to retire.
 template <int EPL>
-__global__ void __launch_bounds__(kRoutingThreads) k_routing(Dims d, Work ws, const float *__restrict__ bias,
+__global__ void __launch_bounds__(kRoutingThreads) k_routing(Dims d, Work ws,
                                                              const uint8_t *__restrict__ live,
                                                              const uint8_t *__restrict__ decoded,
                                                              const uint4 *__restrict__ x, int vec_per_row) {
-  routing_body<EPL>(d, ws, bias, live, decoded, x, vec_per_row);
+  routing_body<EPL>(d, ws, live, decoded, x, vec_per_row);
   __syncthreads();  // every return in the body is uniform over the CTA
   if (threadIdx.x == 0) {
     __threadfence();
@@ -773,12 +759,13 @@ cudaError_t launch_gate_simt(const Dims &d, const Weights &w, const Work &ws, co
     static bool carve_ = (prefer_max_shared(k_gate_simt<__nv_bfloat16>) == cudaSuccess);
     (void)carve_;
     k_gate_simt<__nv_bfloat16><<<blocks, 256, 0, s>>>(d, static_cast<const __nv_bfloat16 *>(x),
-                                                      static_cast<const __nv_bfloat16 *>(w.w_router), ws.gparts, ws);
+                                                      static_cast<const __nv_bfloat16 *>(w.w_router), w.b_router,
+                                                      ws.logits, ws);
   } else {
     static bool carve_ = (prefer_max_shared(k_gate_simt<float>) == cudaSuccess);
     (void)carve_;
     k_gate_simt<float><<<blocks, 256, 0, s>>>(d, static_cast<const float *>(x),
-                                              static_cast<const float *>(w.w_router), ws.gparts, ws);
+                                              static_cast<const float *>(w.w_router), w.b_router, ws.logits, ws);
   }
   return cudaGetLastError();
 }
@@ -790,7 +777,7 @@ cudaError_t launch_plan_topk(const Dims &d, const Weights &w, const Work &ws, cu
   case N: {                                                                            \
     static bool c_ = (prefer_max_shared(k_plan_topk<N>) == cudaSuccess);               \
     (void)c_;                                                                          \
-    k_plan_topk<N><<<blocks, 256, 0, s>>>(d, ws.gparts, w.b_router, ws.plan_counts);  \
+    k_plan_topk<N><<<blocks, 256, 0, s>>>(d, ws.logits, ws.plan_counts);              \
     break;                                                                             \
   }
     EPOCH_CASE(1) EPOCH_CASE(2) EPOCH_CASE(4) EPOCH_CASE(8) EPOCH_CASE(16) EPOCH_CASE(32)
@@ -815,13 +802,12 @@ cudaError_t launch_routing(const Dims &d, const Weights &w, const Work &ws, cons
   // slices of at most kRoutingThreads positions per CTA
   const int min_grid = (d.n_pos + kRoutingThreads - 1) / kRoutingThreads;
   if (grid < min_grid) return cudaErrorInvalidConfiguration;
-  const float *bias = w.b_router;
   Dims dd = d;
   Work ww = ws;
   const int vec = d.H * (bf16 ? 2 : 4) / 16;
   const uint4 *xv = static_cast<const uint4 *>(x);
-  void *args[] = {&dd, &ww, const_cast<float **>(&bias), const_cast<uint8_t **>(&live),
-                  const_cast<uint8_t **>(&decoded), const_cast<uint4 **>(&xv), const_cast<int *>(&vec)};
+  void *args[] = {&dd, &ww, const_cast<uint8_t **>(&live), const_cast<uint8_t **>(&decoded),
+                  const_cast<uint4 **>(&xv), const_cast<int *>(&vec)};
   switch (epl_for(d.E)) {
 #define EPOCH_CASE(N)                                                                                    \
   case N: {                                                                                              \

@@ -27,54 +27,28 @@ __device__ __forceinline__ float key_value(unsigned k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Logits of the EPL consecutive experts [lane*EPL, lane*EPL + EPL) of position
-// t: split-K partial sums in a fixed order, then the bias. Experts >= E get
-// -inf. Vector loads when the row is 16-byte aligned.
+// The EPL consecutive logits [lane*EPL, lane*EPL + EPL) of one row of G
+// (E floats); experts >= E get -inf. Vector loads when the row is 16-byte
+// aligned. The row was written by an earlier kernel (read-only path).
 template <int EPL>
-__device__ __forceinline__ void lane_logits(const float *__restrict__ gparts, int SK, int Nmax, int E, int t,
-                                            const float *__restrict__ bias, float (&v)[EPL]) {
+__device__ __forceinline__ void lane_logits(const float *__restrict__ row, int E, float (&v)[EPL]) {
   const int e0 = lane_id() * EPL;
-#pragma unroll
-  for (int c = 0; c < EPL; ++c) v[c] = 0.f;
   if constexpr (EPL % 4 == 0) {
     if ((E & 3) == 0 && e0 + EPL <= E) {
-#pragma unroll 4
-      for (int s = 0; s < SK; ++s) {
-        const float4 *src = reinterpret_cast<const float4 *>(gparts + (static_cast<size_t>(s) * Nmax + t) * E + e0);
+      const float4 *src = reinterpret_cast<const float4 *>(row + e0);
 #pragma unroll
-        for (int q = 0; q < EPL / 4; ++q) {
-          const float4 a = __ldg(src + q);
-          v[4 * q] += a.x;
-          v[4 * q + 1] += a.y;
-          v[4 * q + 2] += a.z;
-          v[4 * q + 3] += a.w;
-        }
-      }
-      if (bias != nullptr) {
-        const float4 *bs = reinterpret_cast<const float4 *>(bias + e0);
-#pragma unroll
-        for (int q = 0; q < EPL / 4; ++q) {
-          const float4 b = __ldg(bs + q);
-          v[4 * q] += b.x;
-          v[4 * q + 1] += b.y;
-          v[4 * q + 2] += b.z;
-          v[4 * q + 3] += b.w;
-        }
+      for (int q = 0; q < EPL / 4; ++q) {
+        const float4 a = __ldg(src + q);
+        v[4 * q] = a.x;
+        v[4 * q + 1] = a.y;
+        v[4 * q + 2] = a.z;
+        v[4 * q + 3] = a.w;
       }
       return;
     }
   }
 #pragma unroll
-  for (int c = 0; c < EPL; ++c) {
-    const int e = e0 + c;
-    if (e < E) {
-      float g = 0.f;
-      for (int s = 0; s < SK; ++s) g += __ldg(gparts + (static_cast<size_t>(s) * Nmax + t) * E + e);
-      v[c] = bias != nullptr ? g + __ldg(bias + e) : g;
-    } else {
-      v[c] = -INFINITY;
-    }
-  }
+  for (int c = 0; c < EPL; ++c) v[c] = e0 + c < E ? __ldg(row + e0 + c) : -INFINITY;
 }
 
 // Top-k of one position by one warp. Lane l owns the EPL experts

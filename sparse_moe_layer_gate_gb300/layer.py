@@ -166,7 +166,7 @@ class EpochLayer:
     def debug(self, n_pos: int, parts=("plan", "iter"), stream=None) -> dict:
         """Host copies of internal arrays. parts: "plan" (support, hit counts),
         "iter" (fresh list, selections, weights, worklist, stamps), "logits"
-        (split partial logits), "cache" (routed-output cache rows)."""
+        (G of the last iteration), "cache" (routed-output cache rows)."""
         v = B.epoch_debug_view()
         B.check(B.lib().epoch_debug_pointers(self.handle, C.byref(v)), "epoch_debug_pointers")
         st = self.stats(stream)
@@ -187,8 +187,6 @@ class EpochLayer:
             d["slot"] = self._copy(v.slot, nf * k, np.int32, stream).reshape(nf, k)
             d["stamp"] = self._copy(v.stamp, n_pos, np.int32, stream)
         if "logits" in parts:
-            raw = self._copy(v.logit_parts, v.n_logit_parts * N * E, np.float32, stream)
-            d["logit_parts"] = raw.reshape(v.n_logit_parts, N, E)[:, :n_pos]
             d["logits"] = self._copy(v.logits, N * E, np.float32, stream).reshape(N, E)[:n_pos]
         if "cache" in parts:
             cdt = np.uint16 if self.dtype == "bf16" else np.float32
