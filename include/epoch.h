@@ -137,26 +137,26 @@ typedef struct {
   const int32_t *plan_counts;  /* [E] block-start top-k hit counts */
   const float *logits;         /* [max_positions][E] G of the last iteration, bias included */
   const int32_t *fresh_pos;    /* [n_fresh] ascending fresh positions */
-  const int32_t *sel;          /* [n_fresh][k] selected experts, selection order */
-  const float *sel_w;          /* [n_fresh][k] routing weights */
+  const int32_t *sel;          /* [max_positions][k] selected experts of position t, selection order
+                                  (rows of the fresh positions hold this iteration's values) */
+  const float *sel_w;          /* [max_positions][k] routing weights, same rows */
   const int32_t *offsets;      /* [E+1] worklist offsets per expert */
   const int32_t *wl_pos;       /* [n_edges] positions of the expert-sorted worklist */
-  const int32_t *slot;         /* [n_fresh][k] worklist row of each selection */
+  const int32_t *slot;         /* [max_positions][k] worklist row of each selection, same rows */
   const int32_t *stamp;        /* [max_positions] iteration of each row's last fresh compute, -1 none */
   const void *cache;           /* [max_positions][H] routed-output cache, layer dtype */
   const epoch_iter_stats *stats;
   const uint32_t *error_word;
   /* [4][1024][8] int64 per-CTA timelines of the last launches while tracing is
-   * on (globaltimer ns). Row 0, gate: entry, setup done, first operand stage
-   * landed, last MMA committed, epilogue done, tiles, valid token columns, SM
-   * id. Row 1, experts: entry, inputs loaded, first stage landed, last MMA
-   * complete, epilogue done, tiles, ns the producer waited for up tiles, SM id.
-   * Row 2, expert epilogue: ns busy, ns waiting for accumulators, longest tile
-   * epilogue in ns, that tile's group (bit 30 set: down tile) and valid rows,
-   * start and end of the last tile's epilogue, SM id. Row 3, routing: entry,
-   * then the ends of the classify, compaction, top-k and worklist phases, the
-   * kernel end; CTA 0 instead records fields 4-6 around the statistics and
-   * the tile prefix it writes. */
+   * on (globaltimer ns). Row 0, gate (bf16 layers): entry, setup done, first
+   * operand stage landed, last MMA issued, epilogue done, position tile, H
+   * slice (cluster rank), SM id. Row 1, experts: entry, setup done, worklist
+   * received, last MMA complete, epilogue done, tiles, ns the producer waited
+   * for up tiles, SM id. Row 2, expert epilogue: ns busy, ns waiting for
+   * accumulators, longest tile epilogue in ns, that tile's group (bit 30 set:
+   * down tile) and valid rows, start and end of the last tile's epilogue, SM
+   * id. Row 3, worklist kernel (one CTA): entry, gate finished, expert counts
+   * done, offsets and tile list done, worklist published, end. */
   const int64_t *trace;
   /* [2][EPOCH_PROF_KINDS] while tracing: first CTA entry and last CTA exit
    * (globaltimer ns) of each kernel kind in the last iteration, in the order

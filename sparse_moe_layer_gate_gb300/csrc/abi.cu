@@ -32,6 +32,7 @@ struct epoch_layer {
   int32_t n_pos_plan;
   int32_t last_iter;
   int32_t state_rd;  // half of the double-buffered iteration state the next iteration reads
+  uint32_t seq;      // sequence number of the last iteration call
   int64_t n_cold, n_hot, n_fallback, n_launch;
   // profiling
   bool prof;
@@ -89,16 +90,18 @@ size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   t.plan_counts = static_cast<int32_t *>(take(E * 4));
   t.cache = take(N * H * act);
   t.logits = static_cast<float *>(take(N * E * 4));
+  t.cat = static_cast<uint8_t *>(take(N));
   t.fidx = static_cast<int32_t *>(take(N * 4));
   t.fresh_pos = static_cast<int32_t *>(take(N * 4));
   t.sel = static_cast<int32_t *>(take(N * k * 4));
   t.selw = static_cast<float *>(take(N * k * 4));
-  t.chunk_mask = static_cast<uint32_t *>(take(chunks * E * 4));
-  t.expert_cnt = static_cast<int32_t *>(take(E * 4));
+  t.sel_words = static_cast<uint32_t *>(take(2 * chunks * E * 4));
+  t.pre = static_cast<int32_t *>(take(chunks * E * 4));
   t.offsets = static_cast<int32_t *>(take((E + 1) * 4));
   t.grp_list = static_cast<int32_t *>(take((E + nsh + 1) * 4));
   t.done_up = static_cast<int32_t *>(take((E + nsh) * 4));
   t.tile_ctr = static_cast<int32_t *>(take(16));
+  t.sh_ctr = static_cast<int32_t *>(take(2 * (1 + nsh * ((N + kTnUp - 1) / kTnUp)) * 4));
   t.wl_pos = static_cast<int32_t *>(take(N * k * 4));
   t.slot = static_cast<int32_t *>(take(N * k * 4));
   t.xp = take(N * k * H * act);
@@ -114,9 +117,8 @@ size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   } else {
     t.pk_gu = t.pk_d = t.pk_sgu = t.pk_sd = nullptr;
   }
-  t.gbar = static_cast<unsigned int *>(take(16));
   t.route_done = static_cast<unsigned int *>(take(16));
-  t.trace = static_cast<int64_t *>(take(4ull * kTraceCtas * kTraceFields * 8));
+  t.trace = static_cast<int64_t *>(take(static_cast<size_t>(kTraceRows) * kTraceCtas * kTraceFields * 8));
   t.timeline = static_cast<unsigned long long *>(take(2ull * K_NUM * 8));
   t.ctrl = static_cast<Ctrl *>(take(sizeof(Ctrl)));
   t.stats = static_cast<epoch_iter_stats *>(take(sizeof(epoch_iter_stats)));
@@ -171,17 +173,20 @@ Dims call_dims(const epoch_layer *L, int32_t n_pos, int32_t iter, int host_fallb
   return d;
 }
 
-// G = x W_r^T + b for every position: tcgen05 for bf16 layers, FFMA for fp32
-// layers. x_maps[0] (box kTnGate rows) feeds the gate, x_maps[1] (box kTnUp
-// rows) the shared experts' up-projection.
-epoch_status run_gate(epoch_layer *L, Dims &d, const void *x, CUtensorMap *x_maps, cudaStream_t s) {
+// G = x W_r^T + b for every position: tcgen05 for bf16 layers (whose gate
+// kernel also classifies the positions and takes their top-k, except in plan
+// mode), FFMA for fp32 layers (followed by the select kernel). *x_map_up gets
+// x with boxes of kTnUp rows (shared-expert up tiles).
+epoch_status run_gate(epoch_layer *L, Dims &d, const void *x, const uint8_t *live, const uint8_t *decoded,
+                      CUtensorMap *x_map_up, cudaStream_t s) {
   if (L->bf16) {
-    if (!encode_kmajor_bf16(&x_maps[0], x, d.H, d.n_pos, kTnGate) ||
-        !encode_kmajor_bf16(&x_maps[1], x, d.H, d.n_pos, kTnUp))
-      return EPOCH_ECUDA;
-    return run(L, K_GATE, s, [&] { return launch_gate_tc(d, L->maps, L->ws, x_maps[0], L->w.b_router, s); });
+    if (!encode_kmajor_bf16(x_map_up, x, d.H, d.n_pos, kTnUp)) return EPOCH_ECUDA;
+    return run(L, K_GATE, s,
+               [&] { return launch_gate_tc(d, L->maps, L->ws, x, L->w.b_router, live, decoded, s); });
   }
-  return run(L, K_GATE, s, [&] { return launch_gate_simt(d, L->w, L->ws, x, 0, s); });
+  EPOCH_TRY(run(L, K_GATE, s, [&] { return launch_gate_simt(d, L->w, L->ws, x, 0, s); }));
+  if (d.plan_mode) return EPOCH_OK;
+  return run(L, K_SELECT, s, [&] { return launch_select(d, L->ws, live, decoded, s); });
 }
 
 }  // namespace
@@ -222,7 +227,6 @@ epoch_status epoch_layer_create(const epoch_layer_config *cfg, const epoch_layer
   d.residual = cfg->residual ? 1 : 0;
   d.tn = L->bf16 ? kTnUp : 0;
   d.cmax = (cfg->max_positions + 31) / 32;
-  d.route_ctas = routing_grid();
   d.timeout_ns = 2000000000ll;
   memset(&L->maps, 0, sizeof(L->maps));
   if (L->bf16) {
@@ -231,7 +235,7 @@ epoch_status epoch_layer_create(const epoch_layer_config *cfg, const epoch_layer
       return EPOCH_ECUDA;
     }
     const uint64_t H = d.H, E = d.E, I = d.I, N = d.Nmax, k = d.k, nsh = d.n_sh, Is = d.I_s;
-    bool ok = encode_kmajor_bf16(&L->maps.w_router, w->w_router, H, E, 128);
+    bool ok = encode_kmajor_bf16(&L->maps.w_router, w->w_router, H, E, 128) && gate_tc_supported(d);
     for (int b = 0; ok && b < 4; ++b)
       ok = encode_kmajor_bf16(&L->maps.xp[b], L->ws.xp, H, N * k, kBoxRows[b]) &&
            encode_kmajor_bf16(&L->maps.a_int[b], L->ws.a_int, I, N * k, kBoxRows[b]);
@@ -278,6 +282,7 @@ epoch_status epoch_layer_create(const epoch_layer_config *cfg, const epoch_layer
   L->n_pos_plan = 0;
   L->last_iter = -1;
   L->state_rd = 0;
+  L->seq = 0;
   L->prof = false;
   for (int i = 0; i < K_NUM; ++i) {
     L->total_ms[i] = 0.0;
@@ -291,8 +296,9 @@ epoch_status epoch_plan_block(epoch_layer *L, const void *x, int32_t n_pos, epoc
   if (L == nullptr || !aligned16(x) || n_pos < 1 || n_pos > L->cfg.max_positions) return EPOCH_EINVAL;
   cudaStream_t s = S(stream);
   Dims d = call_dims(L, n_pos, 0, 0);
-  CUtensorMap x_maps[2];
-  EPOCH_TRY(run_gate(L, d, x, x_maps, s));
+  d.plan_mode = 1;
+  CUtensorMap x_map_up;
+  EPOCH_TRY(run_gate(L, d, x, nullptr, nullptr, &x_map_up, s));
   if (cudaMemsetAsync(L->ws.plan_counts, 0, sizeof(int32_t) * d.E, s) != cudaSuccess) return EPOCH_ECUDA;
   EPOCH_TRY(run(L, K_PLAN_TOPK, s, [&] { return launch_plan_topk(d, L->w, L->ws, s); }));
   const double tau = L->cfg.tau;
@@ -318,12 +324,14 @@ epoch_status epoch_moe_iter(epoch_layer *L, const void *x, const uint8_t *live, 
         cudaMemsetAsync(L->ws.timeline + K_NUM, 0, K_NUM * 8, s) != cudaSuccess)
       return EPOCH_ECUDA;
   }
-  CUtensorMap x_maps[2];
-  EPOCH_TRY(run_gate(L, d, x, x_maps, s));
-  EPOCH_TRY(run(L, K_ROUTING, s, [&] { return launch_routing(d, L->w, L->ws, live, decoded, x, L->bf16, s); }));
-  L->state_rd ^= 1;  // the routing kernel wrote the new state into the other half
+  d.seq = ++L->seq;
+  CUtensorMap x_map_up;
+  EPOCH_TRY(run_gate(L, d, x, live, decoded, &x_map_up, s));
+  EPOCH_TRY(run(L, K_ROUTING, s, [&] { return launch_route(d, L->ws, s); }));
+  L->state_rd ^= 1;  // this iteration wrote the new state into the other half
   if (L->bf16) {
-    EPOCH_TRY(run(L, K_UP, s, [&] { return launch_experts_tc(d, L->maps, L->ws, x_maps[1], s); }));
+    EPOCH_TRY(run(L, K_PERMUTE, s, [&] { return launch_permute(d, L->ws, x, s); }));
+    EPOCH_TRY(run(L, K_UP, s, [&] { return launch_experts_tc(d, L->maps, L->ws, x_map_up, x, s); }));
   } else {
     EPOCH_TRY(run(L, K_UP, s, [&] { return launch_up_simt(d, L->w, L->ws, x, s); }));
     EPOCH_TRY(run(L, K_DOWN, s, [&] { return launch_down_simt(d, L->w, L->ws, s); }));

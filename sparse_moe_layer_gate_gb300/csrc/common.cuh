@@ -133,6 +133,46 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
       : "memory");
 }
 
+// Four rows of a 2-D tensor map whose box is one row high (tile::gather4): rows
+// r0..r3 of columns [c0, c0 + box width) land one after another at dst, each
+// with the map's swizzle as it applies at its shared-memory address (so four
+// gathers at dst, dst + 512, ... fill a 128-byte-swizzled K-major tile exactly
+// as one tiled load of the same rows would).
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t r0, int32_t r1,
+                                            int32_t r2, int32_t r3, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// ------------------------------------------------------------------ thread-block clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Cluster-wide barrier in two halves; every thread of every CTA of the cluster
+// arrives once per phase (convergent warps: .aligned).
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// No memory clobber: a run of these loads issues back to back (they stay
+// ordered after the cluster barrier, which is volatile asm too).
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+
 // L2 eviction policies for TMA loads: streamed expert weights are read once
 // per tile and should not push reused activations out of L2.
 __device__ __forceinline__ uint64_t policy_evict_first() {

@@ -28,83 +28,29 @@
 
 #include "common.cuh"
 #include "layer.h"
+#include "select.cuh"
 
 namespace epoch {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
 
-// Rows of the per-CTA trace: 0 gate, 1 experts, 2 expert epilogue (the routing kernel uses row 3).
+// Rows of the per-CTA trace: 0 gate, 1 experts, 2 expert epilogue (the worklist kernel uses row 3).
 constexpr int kTraceRowGate = 0;
 constexpr int kTraceRowExperts = 1;
 constexpr int kTraceRowEpilogue = 2;  // expert-kernel epilogue summary
+constexpr int kTraceRowGateEpi = 4;   // gate epilogue steps
 
 struct __align__(128) TcParams {
-  CUtensorMap a0;    // gate: W_r [E][H]
-  CUtensorMap b[4];  // gate: b[0] = x; experts: Xp (routed up tiles), boxes of 32/64/128/256 rows
+  CUtensorMap b[4];  // experts: xp (routed up tiles), boxes of 32/64/128/256 rows
   CUtensorMap bs;    // experts: x (shared up tiles), box of kTnUp rows
   CUtensorMap b2[4]; // experts: A (routed down tiles), boxes of 32/64/128/256 rows
   CUtensorMap bs2;   // experts: A (shared down tiles), box of kTnUp rows
   Dims d;
   Work ws;
-  int32_t gate_tiles;
-  const float *bias;  // gate: router bias [E]
+  const uint4 *x;    // x rows, copied into xp at the worklist positions
+  int32_t vec_per_row;  // 16-byte vectors per row of x
 };
-
-// The gate accumulates H in chunks of kGateChunkKb K blocks (256 elements), one
-// TMEM accumulator per chunk, and the epilogue adds the chunks in order in fp32:
-// a 2048- or 4096-term dot product is not one long tensor-core accumulation.
-constexpr int kGateChunkKb = 4;
-
-template <int TN, int STAGES>
-struct GateCfg {
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = TN * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int ACC_COLS = TN;
-  static constexpr int NBUF = 2 * ACC_COLS <= 512 ? 2 : 1;
-  static constexpr int USED_COLS = NBUF * ACC_COLS;
-  static constexpr int TMEM_COLS = USED_COLS <= 32 ? 32 : USED_COLS <= 64 ? 64 : USED_COLS <= 128 ? 128
-                                   : USED_COLS <= 256 ? 256 : 512;
-  static constexpr int NBARS = 2 * STAGES + 2 * NBUF + 1;
-  // epilogue staging: per epilogue warp, 32 token columns x 32 fp32 rows, padded
-  static constexpr int STG_ROW = 144;
-  static constexpr int STG_BYTES = 32 * STG_ROW;
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 4 * STG_BYTES + NBARS * 8 + 16;
-  static_assert(TN == 32, "the epilogue reads one 32-column accumulator per chunk");
-  static_assert(USED_COLS <= 512, "TMEM");
-  static_assert(SMEM <= 227 * 1024, "shared memory");
-};
-
-struct GateTile {
-  int a_row, b_row;  // rows in the W_r and x tensor maps
-  int k0, nk;        // first K element, number of BK blocks
-  int n_valid;       // valid token columns
-  int out_row0;      // output row of column 0
-  int col0;          // output column of MMA row 0
-  int m_limit;       // valid MMA rows (experts)
-  float *out;
-};
-
-// Gate tile t = (expert block m, token tile tt), token tiles fastest; the
-// whole of H in one accumulator (no split partials, one fixed summation order).
-template <int TN>
-__device__ __forceinline__ GateTile gate_tile(const TcParams &p, int tile) {
-  const Dims &d = p.d;
-  GateTile t;
-  const int nt = (d.n_pos + TN - 1) / TN;
-  const int m = tile / nt, tt = tile % nt;
-  t.a_row = m * BM;
-  t.b_row = tt * TN;
-  t.k0 = 0;
-  t.nk = d.H / BK;
-  t.n_valid = min(TN, d.n_pos - tt * TN);
-  t.out_row0 = tt * TN;
-  t.col0 = m * BM;
-  t.m_limit = min(BM, d.E - m * BM);
-  t.out = p.ws.logits;
-  return t;
-}
 
 // Waits for a phase without the abort check (teardown after an abort: lets
 // copies and MMAs already issued land before the CTA exits).
@@ -115,259 +61,301 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-template <int TN, int STAGES>
-__global__ void __launch_bounds__(192, 1) k_tc_gate(const __grid_constant__ TcParams p) {
-  using C = GateCfg<TN, STAGES>;
+// ---------------------------------------------------------------- gate
+// G = x W_r^T + b for every position ([W] section "Expert Atlas": G in
+// R^{N x E}, recomputed every iteration), then, in the same launch, each
+// position's classification and support-restricted top-k.
+//
+// A cluster of CS CTAs owns a tile of TN positions and every expert: CTA r of
+// the cluster multiplies H-slice r (H / CS columns) on the tensor cores
+// (tcgen05.mma, M = 128 experts per block, N = TN positions, fp32 in TMEM),
+// writes its fp32 partial sums to its shared memory, and after a cluster
+// barrier sums the CS partials of its own TN / CS positions in rank order
+// (fixed order: the result does not depend on timing) straight from the other
+// CTAs' shared memory, adds the bias and writes G. It then classifies those
+// positions and takes the top-k of the fresh ones from the rows it holds.
+// Splitting H over the cluster gives 128 CTAs for 1024 positions, each
+// streaming 160 KB, instead of a few CTAs streaming all of W_r.
+struct __align__(128) GateParams {
+  CUtensorMap wr;  // W_r [E][H], box 64 x 128
+  CUtensorMap x;   // x [n_pos][H], box 64 x TN
+  Dims d;
+  Work ws;
+  const float *bias;
+  const uint8_t *live, *decoded;
+  int32_t cs;      // CTAs per cluster (H slices)
+  int32_t tn;      // positions per cluster tile (multiple of 16, <= 256, multiple of cs)
+  int32_t tcols;   // TMEM columns allocated
+  int32_t stages;  // operand ring depth
+  int32_t region0; // bytes of the ring / partial-sum region
+};
+
+// Shared-memory layout of the gate (from the 1024-aligned base): region0 (the
+// operand ring, reused for the fp32 partials [TN][E_pad] once the MMAs are
+// done), the reduced rows [TN / CS][E_pad], the support mask [1024], barriers.
+__host__ __device__ inline int gate_e_pad(int E) { return ((E + 127) / 128) * 128; }
+__host__ __device__ inline int gate_stage_bytes(int E, int TN) { return (gate_e_pad(E) / 128) * kTileBytes + TN * 64 * 2; }
+
+template <int EPL>
+__global__ void __launch_bounds__(256, 1) k_tc_gate(const __grid_constant__ GateParams p) {
   extern __shared__ uint8_t smem_raw[];
-  // 1024-byte aligned base (the 128-byte swizzle pattern repeats every 1024
-  // bytes), offset from the __shared__ array itself so that every pointer
-  // derived from it stays in the shared state space (shared loads and stores,
-  // never ordered behind the epilogue's global stores)
+  // 1024-byte aligned base (the 128-byte swizzle pattern repeats every 1024 bytes)
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sA = sbase;                          // [STAGES] W_r tiles
-  const uint32_t sB = sbase + STAGES * C::A_BYTES;     // [STAGES] x tiles
-  uint8_t *stage_out = smem + STAGES * C::STAGE_BYTES;  // [4][STG_BYTES] epilogue transposes
-  uint64_t *bars = reinterpret_cast<uint64_t *>(stage_out + 4 * C::STG_BYTES);
+  const Dims &d = p.d;
+  const Work &ws = p.ws;
+  const int MB = (d.E + 127) / 128, E_pad = MB * 128;
+  const int CS = p.cs, TN = p.tn, TPC = TN / CS, STAGES = p.stages;
+  const int nkb = d.H / CS / BK;
+  const int W_BYTES = MB * kTileBytes, STAGE = W_BYTES + TN * BK * 2;
+  float *partial = reinterpret_cast<float *>(smem);                   // [TN][E_pad], after the main loop
+  float *rows = reinterpret_cast<float *>(smem + p.region0);          // [TPC][E_pad] reduced rows
+  float *s_bias = rows + TPC * E_pad;                                   // [E_pad]
+  uint8_t *s_support = reinterpret_cast<uint8_t *>(s_bias + E_pad);       // [1024]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(s_support + 1024);
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
-  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + C::NBUF + b); };
-  const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 2 * C::NBUF);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::NBARS);
+  const uint32_t done_bar = bar0 + 8u * (2 * STAGES);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  int *s_anom = reinterpret_cast<int *>(tmem_slot + 2);
+  int *s_code = reinterpret_cast<int *>(tmem_slot + 4);  // [TPC] classification codes of the own positions
+  int *s_stamp = s_code + 64;                             // [TPC] their previous stamps
 
-  const Dims &d = p.d;
-  const Work &ws = p.ws;
   const KernelMark mark_(d, ws, K_GATE);
   pdl_wait();
-  pdl_trigger();  // the routing kernel may start its launch; it waits for this grid to finish
-  if (blockIdx.x == 0) {
-    // counters of the routing launch that follows: its grid barrier and the
-    // count of its finished CTAs (which the expert kernel waits for)
-    if (threadIdx.x == 0) {
-      *ws.gbar = 0u;
-      *ws.route_done = 0u;
-    }
-  }
-  clear_selection_masks(d, ws);
-  const int total = p.gate_tiles;
-  if (static_cast<int>(blockIdx.x) >= total) return;
-  const int wid = warp_id(), lane = lane_id();
+  pdl_trigger();  // the worklist kernel may start its launch; it waits for this grid to finish
+  const int tid = threadIdx.x, wid = warp_id(), lane = lane_id();
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int tile = blockIdx.x / CS;
   const uint64_t tmo = static_cast<uint64_t>(d.timeout_ns);
+  // TMEM columns: MB accumulators of TN columns (the readers load 32-column runs)
+  const uint32_t tcols = static_cast<uint32_t>(p.tcols);
   int64_t *trace = (d.trace && blockIdx.x < kTraceCtas)
                        ? ws.trace + (static_cast<size_t>(kTraceRowGate) * kTraceCtas + blockIdx.x) * kTraceFields
                        : nullptr;
-  if (trace && threadIdx.x == 0) {
+  if (trace && tid == 0) {
     uint32_t smid;
     asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
     trace[0] = static_cast<int64_t>(globaltimer_ns());
     trace[7] = smid;
   }
-
-  if (threadIdx.x == 0) {
+  if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
-    for (int b = 0; b < C::NBUF; ++b) {
-      mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), 128);
-    }
     mbar_init(done_bar, 1);
     *abort_flag = 0;
+    *s_anom = 0;
     mbar_fence_init();
   }
-  if (wid == 0) {
-    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+  if (wid == 1) {
+    tmem_alloc(smem_u32(tmem_slot), tcols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  if (trace && threadIdx.x == 0) trace[1] = static_cast<int64_t>(globaltimer_ns());
+  if (trace && tid == 0) trace[1] = static_cast<int64_t>(globaltimer_ns());
+  const int k0 = rank * (d.H / CS);
 
   if (wid == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer
-      tma_prefetch_desc(&p.a0);
-      tma_prefetch_desc(&p.b[0]);
-      const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_b = policy_evict_last();
-      int stage = 0;
-      uint32_t phase = 0, armed = 0, armed_par = 0;
+      // ---------------- TMA producer: MB W_r tiles and one x tile per K block
+      tma_prefetch_desc(&p.wr);
+      tma_prefetch_desc(&p.x);
+      const uint64_t pol_w = policy_evict_last();  // every cluster reads the same W_r slice
+      const uint64_t pol_x = policy_evict_last();  // the expert kernel reads x again
+      uint32_t armed = 0, armed_par = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const GateTile t = gate_tile<TN>(p, tile);
-        const uint32_t tx = C::A_BYTES + C::B_BYTES;
-        for (int kb = 0; kb < t.nk; ++kb) {
-          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, ws.err, tmo)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(full_bar(stage), tx);
-          const int kc = t.k0 + kb * BK;
-          tma_load_2d(sA + stage * C::A_BYTES, &p.a0, kc, t.a_row, full_bar(stage), pol_w);
-          tma_load_2d(sB + stage * C::B_BYTES, &p.b[0], kc, t.b_row, full_bar(stage), pol_b);
-          armed |= 1u << stage;
-          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      if (!ok) {
-        for (int s = 0; s < STAGES; ++s)
-          if (armed & (1u << s)) mbar_drain(full_bar(s), (armed_par >> s) & 1u, 50000000ull);
-      }
-    }
-    __syncwarp();  // the whole warp reaches the final barrier (and the dealloc) together
-  } else if (wid == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
-      int stage = 0, buf = 0;
-      uint32_t phase = 0, bphase = 0;
-      bool ok = true, first = true;
-      int64_t n_tiles = 0, n_cols = 0;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const GateTile t = gate_tile<TN>(p, tile);
-        const int n_mma = ((t.n_valid + 15) / 16) * 16;
-        ++n_tiles;
-        n_cols += t.n_valid;
-        const uint32_t idesc = idesc_bf16_f32(BM, n_mma);
-        uint32_t d0 = 0;
-        for (int kb = 0; kb < t.nk; ++kb) {
-          if (kb % kGateChunkKb == 0) {  // a new chunk starts in the next accumulator buffer
-            if (!mbar_wait_bounded(tempty_bar(buf), bphase ^ 1u, abort_flag, ws.err, tmo)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            d0 = tmem_base + static_cast<uint32_t>(buf * C::ACC_COLS);
-          }
-          if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, ws.err, tmo)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          if (trace && first) {
-            trace[2] = static_cast<int64_t>(globaltimer_ns());
-            first = false;
-          }
-          const uint64_t ad0 = sw128_kmajor_desc(sA + stage * C::A_BYTES);
-          const uint64_t bd = sw128_kmajor_desc(sB + stage * C::B_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint32_t acc = ((kb % kGateChunkKb) | kk) != 0;
-            tc_mma_bf16(d0, ad0 + 2u * kk, bd + 2u * kk, idesc, acc);
-          }
-          tc_commit(empty_bar(stage));
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-          if (kb % kGateChunkKb == kGateChunkKb - 1 || kb == t.nk - 1) {  // chunk done
-            tc_commit(tfull_bar(buf));
-            if (++buf == C::NBUF) {
-              buf = 0;
-              bphase ^= 1u;
-            }
-          }
-        }
-        if (!ok) break;
-      }
-      tc_commit(done_bar);
-      mbar_drain(done_bar, 0, 50000000ull);
-      if (trace) {
-        trace[3] = static_cast<int64_t>(globaltimer_ns());
-        trace[5] = n_tiles;
-        trace[6] = n_cols;
-      }
-    }
-    __syncwarp();
-  } else {
-    // ---------------- epilogue (warps 2..5; warp w reads TMEM lanes 32*(w%4)..)
-    // Per chunk: one 32-column TMEM load added into registers; then the sums
-    // of this warp's 32 rows (+ bias) are staged token by token in shared
-    // memory and eight lanes store one token's 32 contiguous logits (128 bytes)
-    // together, four tokens per instruction.
-    const int q = wid & 3;
-    uint8_t *stg = stage_out + (wid - 2) * C::STG_BYTES;
-    int buf = 0;
-    uint32_t bphase = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-      const GateTile t = gate_tile<TN>(p, tile);
-      // sum the chunk accumulators in chunk order (fp32), then add the bias
-      float sum[TN];
-#pragma unroll
-      for (int c = 0; c < TN; ++c) sum[c] = 0.f;
-      const int n_chunks = (t.nk + kGateChunkKb - 1) / kGateChunkKb;
-      for (int ch = 0; ch < n_chunks; ++ch) {
-        if (!mbar_wait_bounded(tfull_bar(buf), bphase, abort_flag, ws.err, tmo)) {
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int stage = kb % STAGES;
+        const uint32_t phase = static_cast<uint32_t>(kb / STAGES) & 1u;
+        if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, ws.err, tmo)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * C::ACC_COLS);
-        float v0[TN];
-        tmem_ld32(tb, v0);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < TN; ++c) sum[c] += v0[c];
-        tc_fence_before();
-        mbar_arrive(tempty_bar(buf));
-        if (++buf == C::NBUF) {
-          buf = 0;
-          bphase ^= 1u;
-        }
+        mbar_arrive_expect_tx(full_bar(stage), STAGE);
+        const uint32_t st = sbase + stage * STAGE;
+        const int kc = k0 + kb * BK;
+        for (int mb = 0; mb < MB; ++mb) tma_load_2d(st + mb * kTileBytes, &p.wr, kc, mb * BM, full_bar(stage), pol_w);
+        tma_load_2d(st + W_BYTES, &p.x, kc, tile * TN, full_bar(stage), pol_x);
+        armed |= 1u << stage;
+        armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
       }
-      if (!ok) break;
-      const int rows_valid = min(32, max(0, t.m_limit - q * 32));
-      const int e_row = t.col0 + q * 32 + lane;  // this lane's TMEM row = expert
-      const float bias_r = e_row < d.E ? __ldg(p.bias + e_row) : 0.f;
-      const bool vec_ok = rows_valid == 32 && ((d.E * 4) & 15) == 0;
-      {
-        const int c0 = 0;
-#pragma unroll
-        for (int c = 0; c < TN; ++c) reinterpret_cast<float *>(stg + c * C::STG_ROW)[lane] = sum[c] + bias_r;
-        __syncwarp();
-        const int ncol = min(32, t.n_valid - c0);
-        if (vec_ok) {
-          const int v = lane & 7;
-          for (int c = lane >> 3; c < ncol; c += 4) {
-            const int orow = t.out_row0 + c0 + c;
-            if (orow < 0 || orow >= d.Nmax) {
-              set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-              continue;
+      if (!ok) {  // let copies already issued land before the region is reused
+        for (int s = 0; s < STAGES; ++s)
+          if (armed & (1u << s)) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(full_bar(s), (armed_par >> s) & 1u) && globaltimer_ns() - t0 < 50000000ull) {
             }
-            reinterpret_cast<uint4 *>(t.out + static_cast<size_t>(orow) * d.E + t.col0 + q * 32)[v] =
-                *reinterpret_cast<const uint4 *>(stg + c * C::STG_ROW + v * 16);
           }
-        } else if (lane < ncol) {
-          const int orow = t.out_row0 + c0 + lane;
-          if (orow < 0 || orow >= d.Nmax) {
-            set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-          } else {
-            for (int r = 0; r < rows_valid; ++r)
-              t.out[static_cast<size_t>(orow) * d.E + t.col0 + q * 32 + r] =
-                  reinterpret_cast<const float *>(stg + lane * C::STG_ROW)[r];
-          }
-        }
-        __syncwarp();
       }
     }
-    if (trace && wid == 2 && lane == 0) trace[4] = static_cast<int64_t>(globaltimer_ns());
+    __syncwarp();
+  } else if (wid == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer: accumulator mb = experts [128 mb, 128 mb + 128) x TN positions
+      const uint32_t idesc = idesc_bf16_f32(BM, TN);
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int stage = kb % STAGES;
+        const uint32_t phase = static_cast<uint32_t>(kb / STAGES) & 1u;
+        if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, ws.err, tmo)) break;
+        tc_fence_after();
+        if (trace && kb == 0) trace[2] = static_cast<int64_t>(globaltimer_ns());
+        const uint32_t st = sbase + stage * STAGE;
+        const uint64_t bd = sw128_kmajor_desc(st + W_BYTES);
+        for (int mb = 0; mb < MB; ++mb) {
+          const uint64_t ad = sw128_kmajor_desc(st + mb * kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc_mma_bf16(tmem_base + static_cast<uint32_t>(mb * TN), ad + 2u * kk, bd + 2u * kk, idesc,
+                        (kb | kk) != 0);
+        }
+        tc_commit(empty_bar(stage));
+      }
+      tc_commit(done_bar);  // also on an abort, so the readers below never wait forever
+      if (trace) trace[3] = static_cast<int64_t>(globaltimer_ns());
+    }
+    __syncwarp();
+  } else {
+    // ---------------- warps 2-7, while the operands stream: the support mask,
+    // and the decoded -> live scan (any anomaly anywhere makes every position
+    // fresh with every expert eligible)
+    for (int e = tid - 64; e < E_pad; e += 192) {
+      s_support[e] = e < d.E ? ws.support_mask[e] : 0;
+      s_bias[e] = e < d.E ? __ldg(p.bias + e) : 0.f;
+    }
+    if (!d.plan_mode) {
+      const int rd = d.state_rd & 1;
+      // classification of this CTA's own positions (the fallback decision comes later)
+      const int j = tid - 64, t = tile * TN + rank * TPC + j;
+      if (j < TPC && t < d.n_pos) {
+        const int st = ws.stamp[static_cast<size_t>(rd) * d.Nmax + t];
+        s_stamp[j] = st;
+        s_code[j] = classify_code(d, p.live[t] != 0, p.decoded[t] != 0,
+                                  ws.prev_dec[static_cast<size_t>(rd) * d.Nmax + t] != 0, st);
+      }
+      if (any_anomaly(d, p.live, p.decoded, ws.prev_dec + static_cast<size_t>(rd) * d.Nmax, tid - 64, 192))
+        atomicOr(s_anom, 1);
+    }
   }
+  if (wid >= 4) {
+    // ---------------- warps 4-7: TMEM -> fp32 partials [position][expert] in shared memory
+    if (mbar_wait_bounded(done_bar, 0, abort_flag, ws.err, tmo)) {
+      tc_fence_after();
+      const int q = wid & 3;  // TMEM lanes 32q.. = experts 32q.. of each block
+      for (int mb = 0; mb < MB; ++mb) {
+        for (int c0 = 0; c0 < TN; c0 += 32) {
+          float v[32];
+          tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(mb * TN + c0), v);
+          tmem_ld_wait();
+          const int nc = min(32, TN - c0);
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (c < nc) partial[(c0 + c) * E_pad + mb * BM + q * 32 + lane] = v[c];
+        }
+      }
+    }
+  }
+  int64_t *trace2 = trace ? ws.trace + (static_cast<size_t>(kTraceRowGateEpi) * kTraceCtas + blockIdx.x) * kTraceFields
+                          : nullptr;
   tc_fence_before();
   __syncthreads();
-  if (wid == 0) {
+  if (trace2 && tid == 0) trace2[0] = static_cast<int64_t>(globaltimer_ns());
+  if (wid == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    tmem_dealloc(tmem_base, tcols);
   }
+  // every CTA of the cluster has its partials in shared memory
+  cluster_arrive();
+  cluster_wait();
+  if (trace2 && tid == 0) trace2[1] = static_cast<int64_t>(globaltimer_ns());
+  // ---------------- reduce positions [rank * TPC, rank * TPC + TPC) of the tile over the cluster
+  const int t_own = tile * TN + rank * TPC;
+  const int e4n = E_pad / 4;
+  const uint32_t pbase = smem_u32(partial);
+  const bool vec_out = (d.E & 3) == 0;
+  // units of 4 experts x 1 position, kGateBatch per thread at a time: every
+  // rank's partials of a batch are requested before any is summed (one round
+  // trip over the cluster per batch)
+  constexpr int kGateBatch = 3;
+  const int n_units = TPC * e4n;
+  for (int u0 = tid; u0 < n_units; u0 += kGateBatch * blockDim.x) {
+    float4 v[kGateBatch][8];
+#pragma unroll
+    for (int b = 0; b < kGateBatch; ++b) {
+      const int u = u0 + b * blockDim.x;
+      if (u < n_units) {
+        const int j = u / e4n, e = (u % e4n) * 4;
+        const uint32_t off = static_cast<uint32_t>(((rank * TPC + j) * E_pad + e) * 4);
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          if (s < CS) v[b][s] = ld_dsmem_f4(mapa_shared(pbase + off, static_cast<uint32_t>(s)));
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kGateBatch; ++b) {
+      const int u = u0 + b * blockDim.x;
+      if (u >= n_units) continue;
+      const int j = u / e4n, e = (u % e4n) * 4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int s = 0; s < 8; ++s)
+        if (s < CS) {  // rank order
+          acc.x += v[b][s].x;
+          acc.y += v[b][s].y;
+          acc.z += v[b][s].z;
+          acc.w += v[b][s].w;
+        }
+      float g[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) g[c] = e + c < d.E ? g[c] + s_bias[e + c] : -INFINITY;
+      *reinterpret_cast<float4 *>(rows + j * E_pad + e) = make_float4(g[0], g[1], g[2], g[3]);
+      const int t = t_own + j;
+      if (t < d.n_pos && e < d.E) {
+        float *dst = ws.logits + static_cast<size_t>(t) * d.E + e;
+        if (vec_out) {
+          *reinterpret_cast<float4 *>(dst) = make_float4(g[0], g[1], g[2], g[3]);
+        } else {
+          for (int c = 0; c < 4 && e + c < d.E; ++c) dst[c] = g[c];
+        }
+      }
+    }
+  }
+  cluster_arrive();  // this CTA has read the other CTAs' partials
+  __syncthreads();   // rows[] complete
+  if (trace2 && tid == 0) trace2[2] = static_cast<int64_t>(globaltimer_ns());
+  if (!d.plan_mode) {
+    // ---------------- classification and top-k of the positions this CTA owns
+    const bool force = d.host_fallback != 0 || *s_anom != 0;
+    uint32_t *words = words_written(d, ws);
+    for (int j = wid; j < TPC; j += 8) {
+      const int t = t_own + j;
+      if (t >= d.n_pos) continue;
+      const int code = s_code[j];
+      const bool fresh = force || (code & 15) != C_REUSE;
+      if (lane == 0) record_position(d, ws, t, code, fresh ? d.iter : s_stamp[j]);
+      if (!fresh) continue;
+      float v[EPL];
+#pragma unroll
+      for (int c = 0; c < EPL; ++c) {
+        const int e = lane * EPL + c;
+        v[c] = e < E_pad ? rows[j * E_pad + e] : -INFINITY;
+      }
+      select_position<EPL>(d, ws, t, v, s_support, force, words);
+    }
+  }
+  if (trace && tid == 0) {
+    trace[4] = static_cast<int64_t>(globaltimer_ns());
+    trace[5] = tile;
+    trace[6] = rank;
+  }
+  cluster_wait();  // no CTA leaves while another may still read its partials
+  if (trace2 && tid == 0) trace2[3] = static_cast<int64_t>(globaltimer_ns());
 }
 
 // ---------------------------------------------------------------- fused expert kernel
@@ -403,58 +391,56 @@ static_assert(kTnUp == kTnDn, "up and down tiles share the token tiling");
 // tile (-1 ends the stream), y = row block, z = first token row, w = valid rows.
 constexpr int kDownBit = 1 << 30;
 
-// Tile q of the list [all up tiles, then all down tiles] -> decoded tile and
-// the up-tile count of its group. list = the routing kernel's group list:
-// entry p holds the token tiles of the groups before p (<< kGrpIdBits) and the
-// group of p; the shared experts come first (p < n_sh). offs = expert row
-// offsets. Within a group the tiles run row block by row block, token tiles
-// fastest, so tiles drawn close together share a weight row block in L2. Up
-// tiles of the shared experts come first (I_s / 128 row blocks each), then
-// those of the routed experts (I / 128); down tiles have H / 256 row blocks in
-// every group. Returns false when the list and the offsets disagree.
+// Routed tile q of the list [all up tiles, then all down tiles] -> decoded
+// tile and the up-tile count of its group. list = the worklist kernel's group
+// list: entry p holds the token tiles of the groups before p (<< kGrpIdBits)
+// and the expert of p. offs = expert row offsets. Within a group the tiles run
+// row block by row block, token tiles fastest, so tiles drawn close together
+// share a weight row block in L2. Up tiles have I / 128 row blocks, down tiles
+// H / 256. Returns false when the list and the offsets disagree.
 __device__ __forceinline__ bool locate(const Dims &d, const int32_t *list, const int32_t *offs, int q, int n_up,
                                       int4 *td, int *need) {
-  const int G2 = d.E + d.n_sh;
   auto pref = [&](int p) { return list[p] >> kGrpIdBits; };
   const bool up = q < n_up;
-  int base_q = 0, base_t = 0, mult, lo = 0, hi = G2;
-  if (up) {
-    const int a_sh = (d.I_s / BM) * pref(d.n_sh);
-    if (q < a_sh) {
-      mult = d.I_s / BM;
-      hi = d.n_sh;
-    } else {
-      base_q = a_sh;
-      base_t = pref(d.n_sh);
-      mult = d.I / BM;
-      lo = d.n_sh;
-    }
-  } else {
-    q -= n_up;
-    mult = d.H / kBmDn;
-  }
-  const int key = base_t + (q - base_q) / mult;
-  // largest p in [lo, hi) with pref(p) <= key
-  int l = lo, h = hi;
+  if (!up) q -= n_up;
+  const int mult = up ? d.I / BM : d.H / kBmDn;
+  const int key = q / mult;
+  // largest p in [0, E) with pref(p) <= key
+  int l = 0, h = d.E;
   while (h - l > 1) {
     const int mid = (l + h) >> 1;
     if (pref(mid) <= key) l = mid;
     else h = mid;
   }
   const int nt = pref(l + 1) - pref(l);
-  const int qq = q - base_q - mult * (pref(l) - base_t);
+  const int qq = q - mult * pref(l);
   if (nt <= 0 || qq < 0 || qq >= mult * nt) return false;
   const int m = qq / nt, tt = qq - m * nt;
   const int g = list[l] & ((1 << kGrpIdBits) - 1);
-  const bool shared = g >= d.E;
-  if (shared != (l < d.n_sh) || g >= G2) return false;
-  const int rows = shared ? d.n_pos : offs[g + 1] - offs[g];
-  const int r0 = (shared ? 0 : offs[g]) + tt * kTnUp;
+  if (g >= d.E) return false;
+  const int rows = offs[g + 1] - offs[g];
+  const int r0 = offs[g] + tt * kTnUp;
   const int n_valid = min(kTnUp, rows - tt * kTnUp);
   if (n_valid <= 0) return false;
   *td = make_int4(g | (up ? 0 : kDownBit), m, r0, n_valid);
-  *need = nt * ((shared ? d.I_s : d.I) / BM);
+  *need = nt * (d.I / BM);
   return true;
+}
+
+// Shared-expert tile q: the up tiles of every (shared expert s, token tile
+// tt, row block m), then the down tiles, token tiles before row blocks so that
+// the down tiles of the first token tiles become ready first. A down tile
+// (s, tt) needs the I_s / 128 up tiles of (s, tt).
+__device__ __forceinline__ int4 shared_tile(const Dims &d, int q, int *need, int *tt_out) {
+  const int nt = (d.n_pos + kTnUp - 1) / kTnUp, mu = d.I_s / BM, md = d.H / kBmDn;
+  const int n_up = d.n_sh * nt * mu;
+  const bool up = q < n_up;
+  if (!up) q -= n_up;
+  const int mm = up ? mu : md;
+  const int s = q / (nt * mm), r = q - s * nt * mm, tt = r / mm, m = r - tt * mm;
+  *need = mu;
+  *tt_out = tt;
+  return make_int4((d.E + s) | (up ? 0 : kDownBit), m, tt * kTnUp, min(kTnUp, d.n_pos - tt * kTnUp));
 }
 
 struct XTile {
@@ -464,6 +450,7 @@ struct XTile {
   int a_bytes;            // weight bytes per K block (32 KB: two 128-row tiles)
   int nk;                 // K blocks
   const CUtensorMap *mb;  // token-operand map (box chosen for the tile)
+  bool routed_up;         // token rows come from xp, filled by this kernel's copy phase
   int b_row, b_bytes;
   int n_valid;
   int out_row0, out_rows, ld, col0;
@@ -489,6 +476,7 @@ __device__ __forceinline__ XTile xdecode(const TcParams &p, int4 td) {
     t.a_bytes = 2 * kTileBytes;
     t.nk = nkb;
     t.mb = shared ? &p.bs : &p.b[bi];
+    t.routed_up = !shared;
     t.b_bytes = (shared ? kTnUp : (32 << bi)) * BK * 2;
     t.b_row = r0;
     t.out_row0 = shared ? s * d.Nmax + r0 : r0;
@@ -505,6 +493,7 @@ __device__ __forceinline__ XTile xdecode(const TcParams &p, int4 td) {
     t.nk = nkb;
     t.col0 = m * kBmDn;
     t.mb = shared ? &p.bs2 : &p.b2[bi];
+    t.routed_up = false;
     t.b_bytes = (shared ? kTnDn : (32 << bi)) * BK * 2;
     t.b_row = shared ? s * d.Nmax + r0 : r0;
     t.out_row0 = t.b_row;
@@ -580,28 +569,55 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   if (trace && threadIdx.x == 0) trace[1] = static_cast<int64_t>(globaltimer_ns());
-  // The prologue above may overlap the routing kernel (programmatic dependent
-  // launch); the producer draws tiles from tile_ctr only after it has seen
-  // every routing CTA finish (the route_done count) and loaded the group list
-  // and expert offsets.
+  // The prologue above may overlap the gate and worklist kernels (programmatic
+  // dependent launch). Shared-expert tiles need no routing and start at once;
+  // the routed tiles wait until the worklist kernel has published this call's
+  // worklist (route_done = this call's sequence number, acquire).
+  const int par = static_cast<int>(d.seq & 1u);
+  int32_t *shc = ws.sh_ctr + static_cast<size_t>(par) * sh_stride(d);  // [0] tile counter, then done counts
+  const int nt_max = (d.Nmax + kTnUp - 1) / kTnUp;
+  const int nt_sh = (d.n_pos + kTnUp - 1) / kTnUp;
+  const int n_sh_up = d.tn > 0 ? d.n_sh * nt_sh * (d.I_s / BM) : 0;
+  const int n_sh_dn = d.tn > 0 ? d.n_sh * nt_sh * (d.H / kBmDn) : 0;
+  auto wait_worklist = [&]() -> bool {
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+      unsigned int v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ws.route_done) : "memory");
+      if (v == d.seq) return true;
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > tmo) {
+        set_error(ws.err, EPOCH_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+      }
+      __nanosleep(32);
+    }
+  };
 
+  int64_t *trace7 = trace ? ws.trace + (6ull * kTraceCtas + blockIdx.x) * kTraceFields : nullptr;
   if (wid == 0) {
-    // ---------------- producer: weight bulk copies + token TMA loads (lane 0)
+    // ---------------- producer warp (lane 0 issues): per K block, a 32 KB run of
+    // packed weights (bulk copy) and the tile's token rows (tiled TMA load: x
+    // for shared-expert up tiles, xp for routed up tiles, activations for down
+    // tiles)
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_b = policy_evict_last();
     int stage = 0;
     uint32_t phase = 0, armed = 0, armed_par = 0;
     bool ok = true;
     uint64_t waited = 0;
-    // Issues the operand copies of one tile; a down tile first waits until every
-    // up tile of its group (`need` of them) has written its activations.
-    auto issue = [&](const int4 &td, int need) -> bool {
+    // Issues the operand copies of one tile. Token rows that this launch
+    // produces -- routed up tiles: xp rows (copy warps); down tiles: the
+    // activations of the group's up tiles -- are awaited (flag >= target)
+    // after the weight copies of the first stages have gone out.
+    int64_t waited_by[3] = {0, 0, 0};  // ns waiting for: xp rows, routed up tiles, shared up tiles
+    auto issue = [&](const int4 &td, const int32_t *flag, int target, int wait_kind) -> bool {
       const XTile t = xdecode(p, td);
       const uint32_t tx = t.a_bytes + t.b_bytes;
-      // a down tile's weights do not depend on the up tiles: its first stages'
-      // weight copies go out before the dependency wait, their token loads after
-      const int pre = t.up ? 0 : min(t.nk, 2);
-      int pre_stage[2] = {0, 0};
+      const bool dep = flag != nullptr;
+      const int pre = dep ? min(t.nk, t.up ? kExpStages : 2) : 0;
+      int pre_stage[kExpStages] = {0, 0, 0, 0};
       for (int kb = 0; kb < pre; ++kb) {
         if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, ws.err, tmo)) return false;
         mbar_arrive_expect_tx(full_bar(stage), tx);
@@ -615,21 +631,23 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
           phase ^= 1u;
         }
       }
-      if (!t.up) {
+      if (dep) {
         const uint64_t t0 = globaltimer_ns();
         for (;;) {
           int done;
-          asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(done) : "l"(ws.done_up + t.g) : "memory");
-          if (done >= need) break;
+          asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(done) : "l"(flag) : "memory");
+          if (done >= target) break;
           if (*abort_flag) return false;
           if (globaltimer_ns() - t0 > tmo) {
             set_error(ws.err, EPOCH_DEVERR_TIMEOUT);
             *abort_flag = 1;
             return false;
           }
-          __nanosleep(64);
+          __nanosleep(32);
         }
-        waited += globaltimer_ns() - t0;
+        const int64_t w_ns = static_cast<int64_t>(globaltimer_ns() - t0);
+        waited += w_ns;
+        waited_by[wait_kind] += w_ns;
         asm volatile("fence.proxy.async.global;" ::: "memory");  // generic writes -> TMA reads
         for (int kb = 0; kb < pre; ++kb)
           tma_load_2d(sbase + pre_stage[kb] * kExpStage + 2 * kTileBytes, t.mb, kb * BK, t.b_row,
@@ -650,64 +668,90 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
       }
       return true;
     };
+    int j = 0;  // tiles handed through the ring
+    auto post = [&](const int4 &td) -> bool {
+      const int slot = j % kExpSched;
+      if (!mbar_wait_bounded(sempty_bar(slot), ((j / kExpSched) & 1) ^ 1u, abort_flag, ws.err, tmo)) return false;
+      s_td[slot] = td;
+      mbar_arrive(sfull_bar(slot));
+      ++j;
+      return true;
+    };
     if (lane == 0) {
       tma_prefetch_desc(&p.bs);
-      tma_prefetch_desc(&p.b[0]);
-      tma_prefetch_desc(&p.b2[0]);
+      tma_prefetch_desc(&p.bs2);
+      // phase A: the shared experts' up tiles (they read x; no routing needed)
+      while (ok) {
+        const int q = atomicAdd(shc, 1);
+        if (q >= n_sh_up) break;
+        int need, tt;
+        const int4 td = shared_tile(d, q, &need, &tt);
+        ok = post(td) && issue(td, nullptr, 0, 0);
+      }
+      if (trace) trace7[3] = static_cast<int64_t>(globaltimer_ns());
+      if (ok) ok = wait_worklist();
+      if (trace) trace7[4] = static_cast<int64_t>(globaltimer_ns());
     }
-    // wait until every routing CTA has counted itself done (acquire: its writes
-    // are visible to this warp after the __syncwarp)
-    if (lane == 0 && ok) {
-      const uint64_t t0 = globaltimer_ns();
-      for (;;) {
-        unsigned int v;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ws.route_done) : "memory");
-        if (v >= static_cast<unsigned int>(d.route_ctas)) break;
-        if (*abort_flag) {
-          ok = false;
-          break;
-        }
-        if (globaltimer_ns() - t0 > tmo) {
-          set_error(ws.err, EPOCH_DEVERR_TIMEOUT);
-          *abort_flag = 1;
-          ok = false;
-          break;
-        }
-        __nanosleep(128);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    // phase B: the routed experts' tiles
+    if (ok) {
+      for (int i = lane; i <= d.E; i += 32) {
+        s_list[i] = ws.grp_list[i];
+        s_offs[i] = ws.offsets[i];
       }
     }
-    __syncwarp();
-    for (int i = lane; i <= d.E + d.n_sh; i += 32) s_list[i] = ws.grp_list[i];
-    for (int i = lane; i <= d.E; i += 32) s_offs[i] = ws.offsets[i];
-    const int n_up = ws.ctrl->tiles_up;
-    const int total = n_up + ws.ctrl->tiles_dn;
     __syncwarp();
     if (lane == 0) {
       if (trace) trace[2] = static_cast<int64_t>(globaltimer_ns());
-      for (int j = 0; ok; ++j) {
-        const int slot = j % kExpSched;
-        if (!mbar_wait_bounded(sempty_bar(slot), ((j / kExpSched) & 1) ^ 1u, abort_flag, ws.err, tmo)) break;
+      tma_prefetch_desc(&p.b[0]);
+      tma_prefetch_desc(&p.b2[0]);
+      // tile list of this phase: routed up tiles, the shared experts' down
+      // tiles (their up tiles ran in phase A), routed down tiles
+      const int n_up = ok ? ws.ctrl->tiles_up : 0;
+      const int total = ok ? n_up + n_sh_dn + ws.ctrl->tiles_dn : 0;
+      const int L = s_offs[d.E];
+      const int copied = L * p.vec_per_row;  // vectors the permute kernel copies into xp
+      while (ok) {
         const int tile = atomicAdd(ws.tile_ctr, 1);
-        int4 td = make_int4(-1, 0, 0, 0);
+        if (tile >= total) break;
+        int4 td;
         int need = 0;
-        if (tile < total && !locate(d, s_list, s_offs, tile, n_up, &td, &need)) {
-          set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-          *abort_flag = 1;
-          td.x = -1;
+        const int32_t *flag;
+        if (tile >= n_up && tile < n_up + n_sh_dn) {
+          int tt;
+          td = shared_tile(d, n_sh_up + tile - n_up, &need, &tt);
+          flag = shc + 1 + ((td.x & (kDownBit - 1)) - d.E) * nt_max + tt;
+        } else {
+          if (!locate(d, s_list, s_offs, tile < n_up ? tile : tile - n_sh_dn, n_up, &td, &need)) {
+            set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          const bool down = (td.x & kDownBit) != 0;
+          flag = down ? ws.done_up + (td.x & (kDownBit - 1)) : ws.tile_ctr + 2;
+          if (!down) need = copied;
         }
-        s_td[slot] = td;
-        mbar_arrive(sfull_bar(slot));
-        if (td.x < 0) break;
-        ok = issue(td, need);
+        const int kind = tile >= n_up && tile < n_up + n_sh_dn ? 2 : tile < n_up ? 0 : 1;
+        ok = post(td) && issue(td, flag, need, kind);
       }
+      if (ok) ok = post(make_int4(-1, 0, 0, 0));  // end of the stream
       if (!ok) {
         for (int s = 0; s < kExpStages; ++s)
           if (armed & (1u << s)) mbar_drain(full_bar(s), (armed_par >> s) & 1u, 50000000ull);
       }
-      if (trace) trace[6] = static_cast<int64_t>(waited);
+      if (trace) {
+        trace[6] = static_cast<int64_t>(waited);
+        trace7[0] = waited_by[0];
+        trace7[1] = waited_by[1];
+        trace7[2] = waited_by[2];
+      }
     }
     __syncwarp();
-  } else if (wid == 1) {
+  }
+  if (wid == 1) {
+
+
     if (lane == 0) {
       // ---------------- MMA issuer
       int stage = 0, buf = 0;
@@ -765,7 +809,7 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
       }
     }
     __syncwarp();
-  } else {
+  } else if (wid >= 2) {
     // ---------------- epilogue (warps 2..5; warp w reads TMEM lanes 32*(w%4)..)
     const int q = wid & 3;
     uint8_t *stg = stage_out + (wid - 2) * kExpStg;
@@ -855,7 +899,7 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
         if (wid == 2 && lane == 0) {
           __threadfence();
           asm volatile("fence.proxy.async.global;" ::: "memory");
-          atomicAdd(ws.done_up + t.g, 1);
+          atomicAdd(t.g >= d.E ? shc + 1 + (t.g - d.E) * nt_max + t.b_row / kTnUp : ws.done_up + t.g, 1);
         }
       }
       if (etr) {
@@ -888,6 +932,10 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
       tr2[7] = trace[7];
     }
   }
+  // The worklist kernel finishes its bookkeeping (fresh list, slots, statistics)
+  // after publishing the worklist; this grid completes only after it, so the
+  // combine kernel, which waits for this grid, sees those writes.
+  if (threadIdx.x == 0) pdl_wait();
   tc_fence_before();
   __syncthreads();
   if (wid == 0) {
@@ -963,43 +1011,139 @@ bool encode_kmajor_bf16(CUtensorMap *map, const void *base, uint64_t k_elems, ui
   return r == CUDA_SUCCESS;
 }
 
-constexpr int kStGate = 8;  // 20 KB stages (a 128 x 64 W_r tile and a 32 x 64 x tile)
+// Gate launch geometry. CTAs per cluster (H slices): 8 when H / 8 is a whole
+// number of 64-column K blocks, else 4. Positions per cluster tile: as few as
+// let every cluster of the launch be resident at once (the device holds a
+// limited number of clusters, measured once), at least 32, a multiple of 16,
+// at most 256 (one MMA) and within shared memory.
+struct GateGeom {
+  int tn, cs, tcols, stages, region0, smem;
+};
+constexpr int kGateSmemCap = 227 * 1024;
 
-template <int TN, int STAGES>
-static cudaError_t launch_gate(const TcParams &p, int grid, cudaStream_t s) {
-  using C = GateCfg<TN, STAGES>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_tc_gate<TN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e == cudaSuccess) e = prefer_max_shared(k_tc_gate<TN, STAGES>);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  k_tc_gate<TN, STAGES><<<grid, 192, C::SMEM, s>>>(p);
-  return cudaGetLastError();
+static GateGeom gate_geom_for(const Dims &d, int tn) {
+  GateGeom g;
+  g.cs = (d.H / 8) % BK == 0 ? 8 : 4;
+  g.tn = tn;
+  const int nkb = d.H / g.cs / BK;
+  const int stage = gate_stage_bytes(d.E, tn);
+  const int budget = 200 * 1024;
+  g.stages = budget / stage < 4 ? budget / stage : 4;
+  if (g.stages > nkb) g.stages = nkb;
+  if (g.stages < 1) g.stages = 1;
+  const int e_pad = gate_e_pad(d.E);
+  const int partial = tn * e_pad * 4;
+  g.region0 = g.stages * stage > partial ? g.stages * stage : partial;
+  const int rows = (tn / g.cs) * e_pad * 4;
+  g.smem = 1024 + g.region0 + rows + e_pad * 4 + 1024 + (2 * g.stages + 1) * 8 + 16 + 2 * 64 * 4;
+  const int cols = (e_pad / BM - 1) * tn + ((tn + 31) / 32) * 32;
+  g.tcols = cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512;
+  if (cols > 512) g.smem = kGateSmemCap + 1;  // does not fit: rejected by the caller
+  return g;
 }
 
-static void base_params(TcParams &p, const Dims &d, const Work &ws) {
+static const void *gate_fn(const Dims &d) {
+  const int epl = (d.E + 31) / 32;
+  if (epl <= 1) return reinterpret_cast<const void *>(k_tc_gate<1>);
+  if (epl <= 2) return reinterpret_cast<const void *>(k_tc_gate<2>);
+  if (epl <= 4) return reinterpret_cast<const void *>(k_tc_gate<4>);
+  if (epl <= 8) return reinterpret_cast<const void *>(k_tc_gate<8>);
+  if (epl <= 16) return reinterpret_cast<const void *>(k_tc_gate<16>);
+  return reinterpret_cast<const void *>(k_tc_gate<32>);
+}
+
+// Shared-memory limits of every instantiation of the gate, set once.
+static bool gate_attributes() {
+  static const bool ok = [] {
+    const void *fns[] = {reinterpret_cast<const void *>(k_tc_gate<1>), reinterpret_cast<const void *>(k_tc_gate<2>),
+                         reinterpret_cast<const void *>(k_tc_gate<4>), reinterpret_cast<const void *>(k_tc_gate<8>),
+                         reinterpret_cast<const void *>(k_tc_gate<16>), reinterpret_cast<const void *>(k_tc_gate<32>)};
+    for (const void *fn : fns)
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kGateSmemCap) != cudaSuccess ||
+          prefer_max_shared(fn) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+      }
+    return true;
+  }();
+  return ok;
+}
+
+// Clusters of the gate's shape the device can hold at once (0: none).
+static int gate_max_clusters(const Dims &d, int cs) {
+  static int cached[2] = {-1, -1};
+  int &c = cached[cs == 8 ? 1 : 0];
+  if (c >= 0) return c;
+  const void *fn = gate_fn(d);
+  if (!gate_attributes()) return 0;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = cs;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 160 * 1024;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  c = n;
+  return c;
+}
+
+static GateGeom gate_geom(const Dims &d) {
+  const int cs = (d.H / 8) % BK == 0 ? 8 : 4;
+  const int maxc = gate_max_clusters(d, cs);
+  int tn = maxc > 0 ? (d.n_pos + maxc - 1) / maxc : 32;
+  tn = ((tn + 15) / 16) * 16;
+  if (tn < 32) tn = 32;
+  if (tn > 256) tn = 256;
+  GateGeom g = gate_geom_for(d, tn);
+  while (g.smem > kGateSmemCap && tn > 32) {  // large E: narrower tiles, more waves
+    tn -= 16;
+    g = gate_geom_for(d, tn);
+  }
+  return g;
+}
+
+bool gate_tc_supported(const Dims &d) {
+  Dims dd = d;
+  dd.n_pos = d.Nmax;
+  const GateGeom g = gate_geom(dd);
+  return gate_max_clusters(d, g.cs) > 0 && g.smem <= kGateSmemCap && gate_geom_for(d, 32).smem <= kGateSmemCap;
+}
+
+cudaError_t launch_gate_tc(const Dims &d, const Maps &m, const Work &ws, const void *x, const float *bias,
+                           const uint8_t *live, const uint8_t *decoded, cudaStream_t s) {
+  const GateGeom g = gate_geom(d);
+  if (g.smem > kGateSmemCap || !gate_attributes()) return cudaErrorInvalidConfiguration;
+  GateParams p;
   memset(&p, 0, sizeof(p));
+  p.wr = m.w_router;
+  if (!encode_kmajor_bf16(&p.x, x, d.H, d.n_pos, g.tn)) return cudaErrorInvalidValue;
   p.d = d;
   p.ws = ws;
-}
-
-cudaError_t launch_gate_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map,
-                           const float *bias, cudaStream_t s) {
-  TcParams p;
-  base_params(p, d, ws);
-  p.a0 = m.w_router;
   p.bias = bias;
-  p.b[0] = x_map;
-  const int tiles = ((d.E + BM - 1) / BM) * ((d.n_pos + kTnGate - 1) / kTnGate);
-  p.gate_tiles = tiles;
-  const int grid = tiles < num_sms() ? tiles : num_sms();
-  return launch_gate<kTnGate, kStGate>(p, grid, s);
+  p.live = live;
+  p.decoded = decoded;
+  p.cs = g.cs;
+  p.tn = g.tn;
+  p.tcols = g.tcols;
+  p.stages = g.stages;
+  p.region0 = g.region0;
+  const void *fn = gate_fn(d);
+  const int tiles = (d.n_pos + g.tn - 1) / g.tn;
+  void *args[] = {&p};
+  return launch_kernel(fn, dim3(tiles * g.cs), dim3(256), g.smem, s, args, false, g.cs);
 }
 
 cudaError_t launch_experts_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map_up,
-                              cudaStream_t s) {
+                              const void *x, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k_tc_experts, cudaFuncAttributeMaxDynamicSharedMemorySize, kExpSmem);
@@ -1008,11 +1152,15 @@ cudaError_t launch_experts_tc(const Dims &d, const Maps &m, const Work &ws, cons
     attr_set = true;
   }
   TcParams p;
-  base_params(p, d, ws);
+  memset(&p, 0, sizeof(p));
+  p.d = d;
+  p.ws = ws;
   for (int i = 0; i < 4; ++i) {
     p.b[i] = m.xp[i];
     p.b2[i] = m.a_int[i];
   }
+  p.x = static_cast<const uint4 *>(x);
+  p.vec_per_row = d.H * 2 / 16;
   p.bs = x_map_up;
   p.bs2 = m.a_sh;
   // Down tiles wait for up tiles of other CTAs, but never for a CTA that has
@@ -1021,8 +1169,7 @@ cudaError_t launch_experts_tc(const Dims &d, const Maps &m, const Work &ws, cons
   // whose MMA and epilogue finish it independently of its producer's waits.
   // The launch therefore needs no co-residency guarantee.
   void *args[] = {&p};
-  return launch_kernel(reinterpret_cast<void *>(k_tc_experts), dim3(num_sms()), dim3(192), kExpSmem, s, args, false,
-                       true);
+  return launch_kernel(reinterpret_cast<void *>(k_tc_experts), dim3(num_sms()), dim3(192), kExpSmem, s, args, true);
 }
 
 }  // namespace epoch

@@ -35,19 +35,24 @@ struct Work {
   void *cache;            // [Nmax][H] routed-output cache, layer dtype
   // one iteration
   float *logits;          // [Nmax][E] G = x W_r^T + b (gate kernel)
+  uint8_t *cat;           // [Nmax] classification code of each position (category | flag bits)
   int32_t *fidx;          // [Nmax] fresh index of a position, -1 if reused
   int32_t *fresh_pos;     // [Nmax] ascending fresh positions
-  int32_t *sel;           // [Nmax][k]
-  float *selw;            // [Nmax][k]
-  uint32_t *chunk_mask;   // [E][cmax] bit p of word c: fresh position 32c + p selected expert e
-  int32_t *expert_cnt;    // [E] worklist rows of each expert
+  int32_t *sel;           // [Nmax][k] selected experts of position t (fresh positions only)
+  float *selw;            // [Nmax][k] their routing weights
+  uint32_t *sel_words;    // [2][E][cmax] bit t%32 of word (e, t/32): fresh position t selected expert e;
+                          // the iteration writes half state_rd ^ 1 and clears half state_rd
+  int32_t *pre;           // [E][cmax] selected positions of expert e in words before word c
   int32_t *offsets;       // [E+1]
   int32_t *grp_list;      // [E + n_sh + 1] expert-kernel groups in list order: token tiles of the
                           // groups before << kGrpIdBits | group (shared experts E..E+n_sh-1)
   int32_t *done_up;       // [E + n_sh] up tiles of each group finished this iteration (by group id)
-  int32_t *tile_ctr;      // next tile of the expert kernel (dynamic scheduling)
+  int32_t *tile_ctr;      // routed tiles: [0] next tile of the expert kernel (dynamic scheduling),
+                          // [2] 16-byte vectors of worklist rows copied into xp
+  int32_t *sh_ctr;        // shared-expert tiles, [2 (call parity)][sh_stride]: [0] next tile, then the
+                          // finished up tiles of each (shared expert, token tile)
   int32_t *wl_pos;        // [Nmax*k] expert-sorted worklist positions
-  int32_t *slot;          // [Nmax][k] worklist row of selection (f, j)
+  int32_t *slot;          // [Nmax][k] worklist row of selection (t, j)
   void *xp;               // [Nmax*k][H] token rows of the worklist (x at wl_pos), expert-sorted
   void *a_int;            // [Nmax*k][I] SwiGLU activations of routed edges
   void *a_sh;             // [n_sh*Nmax][I_s] SwiGLU activations of shared experts
@@ -60,9 +65,8 @@ struct Work {
   uint8_t *pk_d;          // routed W_down: [E*H/256][I/64] x (two 128-row tiles) = 32 KB
   uint8_t *pk_sgu;        // shared W_gate/W_up: [n_sh*I_s/128][H/64] x 32 KB
   uint8_t *pk_sd;         // shared W_down: [n_sh*H/256][I_s/64] x 32 KB
-  unsigned int *gbar;     // grid-barrier counter of the routing kernel (zeroed by the gate kernel)
-  unsigned int *route_done;  // routing CTAs finished (zeroed by the gate kernel)
-  int64_t *trace;         // [4 kernels][kTraceCtas][8] per-CTA timeline (when tracing)
+  unsigned int *route_done;  // sequence number of the last call whose worklist is complete
+  int64_t *trace;         // [kTraceRows][kTraceCtas][8] per-CTA timeline (when tracing)
   unsigned long long *timeline;  // [2][K_NUM]: first CTA entry, last CTA exit per kernel kind (ns)
   Ctrl *ctrl;
   epoch_iter_stats *stats;
@@ -74,11 +78,10 @@ struct Work {
 // token columns, SM id.
 constexpr int kTraceCtas = 1024;
 constexpr int kTraceFields = 8;
+constexpr int kTraceRows = 7;
 
 constexpr int kTileBytes = 128 * 64 * 2;  // one packed 128 x 64 bf16 tile
-constexpr int kMaxRoutingGrid = 1024;
-constexpr int kBlkFields = 8;  // per-CTA counters of the routing kernel
-constexpr int kRoutingThreads = 512;
+constexpr int kRouteThreads = 512;        // the one CTA of the worklist kernel
 
 // Shapes and per-call values handed to every kernel by value.
 struct Dims {
@@ -88,11 +91,12 @@ struct Dims {
   int32_t n_pos;
   int32_t iter;
   int32_t host_fallback;
-  int32_t state_rd;      // half of stamp / prev_dec holding the previous iteration's state
+  int32_t state_rd;      // half of stamp / prev_dec / sel_words holding the previous iteration's state
   int32_t tn;            // token-tile width of the tcgen05 expert kernel (0 on the SIMT path)
-  int32_t cmax;          // chunk capacity: ceil(Nmax / 32)
-  int32_t trace;         // nonzero: tcgen05 kernels record per-CTA timelines
-  int32_t route_ctas;    // CTAs of the routing launch (routing_grid())
+  int32_t cmax;          // words per expert of sel_words: ceil(Nmax / 32)
+  int32_t trace;         // nonzero: kernels record per-CTA timelines
+  int32_t plan_mode;     // gate kernels: 1 = block plan (logits only), 0 = iteration
+  uint32_t seq;          // sequence number of this call (route_done handshake)
   int64_t timeout_ns;
 };
 
@@ -117,7 +121,7 @@ constexpr int kBoxRows[4] = {32, 64, 128, 256};
 
 // Kernel kinds, for profiling and launch counting.
 enum Kind {
-  K_GATE = 0, K_PLAN_TOPK, K_PLAN_SUPPORT, K_ROUTING, K_UP, K_DOWN, K_COMBINE, K_TEST, K_NUM
+  K_GATE = 0, K_PLAN_TOPK, K_PLAN_SUPPORT, K_ROUTING, K_UP, K_DOWN, K_COMBINE, K_TEST, K_SELECT, K_PERMUTE, K_NUM
 };
 extern const char *const kKindName[K_NUM];
 
@@ -149,23 +153,15 @@ struct KernelMark {
 // route.cu
 cudaError_t launch_gate_simt(const Dims &d, const Weights &w, const Work &ws, const void *x, int bf16,
                              cudaStream_t s);
+cudaError_t launch_select(const Dims &d, const Work &ws, const uint8_t *live, const uint8_t *decoded,
+                          cudaStream_t s);
 cudaError_t launch_plan_topk(const Dims &d, const Weights &w, const Work &ws, cudaStream_t s);
 cudaError_t launch_plan_support(const Dims &d, const Work &ws, int32_t threshold, int all_experts,
                                 cudaStream_t s);
-cudaError_t launch_routing(const Dims &d, const Weights &w, const Work &ws, const uint8_t *live,
-                           const uint8_t *decoded, const void *x, int bf16, cudaStream_t s);
+cudaError_t launch_route(const Dims &d, const Work &ws, cudaStream_t s);
+cudaError_t launch_permute(const Dims &d, const Work &ws, const void *x, cudaStream_t s);
 cudaError_t launch_combine(const Dims &d, const Work &ws, const void *x, void *y, int bf16, cudaStream_t s);
 cudaError_t launch_wait_test(uint32_t *err, int64_t timeout_ns, cudaStream_t s);
-#ifdef __CUDACC__
-// Zeroes the selection-mask words the next routing launch may set (experts x
-// ceil(n_pos / 32) chunks); run by the gate kernels, whose completion the
-// routing kernel waits for before its first atomicOr.
-__device__ __forceinline__ void clear_selection_masks(const Dims &d, const Work &ws) {
-  const int nch = (d.n_pos + 31) / 32;
-  for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < d.E * nch; q += gridDim.x * blockDim.x)
-    ws.chunk_mask[static_cast<size_t>(q / nch) * d.cmax + q % nch] = 0u;
-}
-#endif
 
 // gemm_simt.cu (fp32 layers)
 cudaError_t launch_up_simt(const Dims &d, const Weights &w, const Work &ws, const void *x, cudaStream_t s);
@@ -178,25 +174,29 @@ cudaError_t launch_pack_tiles(const void *src, int64_t rows, int64_t k, uint8_t 
                               int64_t tile_off, int pair, cudaStream_t s);
 bool tma_encode_init();
 bool encode_kmajor_bf16(CUtensorMap *map, const void *base, uint64_t k_elems, uint64_t rows, uint32_t box_rows);
-constexpr int kTnGate = 32;   // gate token tile (x box rows)
 constexpr int kTnUp = 128;    // expert-kernel token tiles (up and down)
 constexpr int kTnDn = 128;
+// Entries per call parity of Work::sh_ctr.
+__host__ __device__ inline int sh_stride(const Dims &d) { return 1 + d.n_sh * ((d.Nmax + kTnUp - 1) / kTnUp); }
 constexpr int kBmDn = 256;    // rows of H per down tile (two 128-row MMAs)
 constexpr int kGrpIdBits = 11;  // group id field of a grp_list entry (E + n_sh <= 1024 < 2^11)
-cudaError_t launch_gate_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map,
-                           const float *bias, cudaStream_t s);
+cudaError_t launch_gate_tc(const Dims &d, const Maps &m, const Work &ws, const void *x, const float *bias,
+                           const uint8_t *live, const uint8_t *decoded, cudaStream_t s);
+// x_map_up: x with boxes of kTnUp rows (shared-expert up tiles); x: the same
+// rows, which the kernel copies into the compact worklist rows xp.
 cudaError_t launch_experts_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map_up,
-                              cudaStream_t s);
+                              const void *x, cudaStream_t s);
+// Checks that the gate's thread-block clusters can be scheduled on this device.
+bool gate_tc_supported(const Dims &d);
 
 int num_sms();
-int routing_grid();
 
-// cudaLaunchKernelEx of `fn`: cooperative (every CTA co-resident, for grid
-// barriers) and/or programmatic (may start before the previous kernel in the
-// stream ends; the kernel calls pdl_wait before touching its inputs). When the
-// driver rejects a programmatic launch the kernel is launched once more
-// without it, and later launches of this process skip it.
+// cudaLaunchKernelEx of `fn`: programmatic (may start before the previous
+// kernel in the stream ends; the kernel calls pdl_wait before touching its
+// inputs) and/or with thread-block clusters of `cluster` CTAs along x (0: no
+// cluster attribute). When the driver rejects a programmatic launch the kernel
+// is launched once more without it, and later launches of this process skip it.
 cudaError_t launch_kernel(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void **args,
-                          bool cooperative, bool programmatic);
+                          bool programmatic, int cluster = 0);
 
 }  // namespace epoch

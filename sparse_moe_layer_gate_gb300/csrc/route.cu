@@ -16,12 +16,13 @@
 
 #include "common.cuh"
 #include "layer.h"
+#include "select.cuh"
 #include "topk.cuh"
 
 namespace epoch {
 
-const char *const kKindName[K_NUM] = {"gate",    "plan_topk",   "plan_support", "routing",
-                                      "experts", "expert_down", "combine",      "wait_test"};
+const char *const kKindName[K_NUM] = {"gate",    "plan_topk",   "plan_support", "routing", "experts",
+                                      "expert_down", "combine", "wait_test", "select", "permute"};
 
 // ---------------------------------------------------------------- helpers
 
@@ -60,13 +61,7 @@ __device__ __forceinline__ int block_excl_scan(int v, int *warp_tmp, int *total)
 template <typename T>
 __global__ void k_gate_simt(Dims d, const T *__restrict__ x, const T *__restrict__ wr, const float *__restrict__ bias,
                             float *__restrict__ g, Work ws) {
-  if (blockIdx.x == 0) {  // counters of the next routing and expert launches
-    if (threadIdx.x == 0) {
-      *ws.gbar = 0u;
-      *ws.route_done = 0u;
-    }
-  }
-  clear_selection_masks(d, ws);
+  (void)ws;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int lane = lane_id();
   for (int o = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; o < d.n_pos * d.E; o += warps) {
@@ -157,229 +152,359 @@ __global__ void __launch_bounds__(1024) k_plan_support(Dims d, Work ws, int32_t 
   }
 }
 
-// ---------------------------------------------------------------- fused routing
-// Grid-wide barrier of the cooperative routing kernel: every CTA arrives once
-// per phase; a CTA whose wait expires sets the timeout bit and the whole grid
-// unwinds (the others time out at this or the next barrier).
-__device__ __forceinline__ bool grid_sync(unsigned int *bar, unsigned int target, uint32_t *err, uint64_t tmo,
-                                          int *s_ok) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(bar, 1u);
-    const uint64_t t0 = globaltimer_ns();
-    int ok = 1;
-    for (;;) {
-      unsigned int v;
-      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(bar) : "memory");
-      if (v >= target) break;
-      if (globaltimer_ns() - t0 > tmo) {
-        set_error(err, EPOCH_DEVERR_TIMEOUT);
-        ok = 0;
-        break;
-      }
-      __nanosleep(40);
-    }
-    __threadfence();
-    *s_ok = ok;
+// ---------------------------------------------------------------- select (fp32 layers)
+// Classification and support-restricted top-k of every position from the
+// logits of the FFMA gate (the tcgen05 gate of bf16 layers does the same in its
+// epilogue): one warp per position. Every CTA first scans all positions for a
+// decoded -> live transition, which makes every position fresh with every
+// expert eligible.
+template <int EPL>
+__global__ void __launch_bounds__(256) k_select(Dims d, Work ws, const uint8_t *__restrict__ live,
+                                                const uint8_t *__restrict__ decoded) {
+  const KernelMark mark_(d, ws, K_SELECT);
+  pdl_wait();
+  const int rd = d.state_rd & 1;
+  const bool anom = __syncthreads_or(
+      any_anomaly(d, live, decoded, ws.prev_dec + static_cast<size_t>(rd) * d.Nmax, threadIdx.x, blockDim.x) ? 1 : 0);
+  const bool force = d.host_fallback != 0 || anom;
+  uint32_t *words = words_written(d, ws);
+  const int lane = lane_id(), warps = gridDim.x * (blockDim.x >> 5);
+  for (int t = blockIdx.x * (blockDim.x >> 5) + warp_id(); t < d.n_pos; t += warps) {
+    int fresh = 0;
+    if (lane == 0) fresh = classify_and_update(d, ws, live, decoded, t, force) ? 1 : 0;
+    fresh = __shfl_sync(0xffffffffu, fresh, 0);
+    if (!fresh) continue;
+    float v[EPL];
+    lane_logits<EPL>(ws.logits + static_cast<size_t>(t) * d.E, d.E, v);
+    select_position<EPL>(d, ws, t, v, ws.support_mask, force, words);
   }
-  __syncthreads();
-  return *s_ok != 0;
 }
 
-// Tile bookkeeping of the expert kernel, written by one CTA. The groups -- the
-// shared experts (every position) and the routed experts -- are listed widest
-// first, so that the expert kernel, which hands tiles out in list order, ends
-// on narrow tiles whose epilogues are short: the shared experts, then routed
-// experts with >= 96 rows, >= 32 rows, fewer (an expert with no row holds no
-// tile and its weights are never read), by id within a class. The order comes
-// from a stable counting sort: per-class counts packed two to an int, two
-// block scans. grp_list[p] = (token tiles of the groups before p) <<
-// kGrpIdBits | group of p, grp_list[E + n_sh] = all token tiles << kGrpIdBits.
-// The expert kernel decodes its tile indices from this list and the expert
-// offsets; tile totals and the number of hit experts go to the control block
-// and the statistics.
-__device__ void write_group_tiles(const Dims &d, const Work &ws, const int32_t *s_off, int32_t *tmp, int n) {
-  const int tid = threadIdx.x;
-  const int E = d.E, G2 = E + d.n_sh;
-  // thread tid holds groups 2 tid, 2 tid + 1 (id order; G2 <= 2 * kRoutingThreads)
-  int cls[2] = {-1, -1}, nt[2] = {0, 0}, hit = 0;
-  int pk0 = 0, pk1 = 0;  // this thread's count of each class: 0, 1 in pk0, 2, 3 in pk1 (16-bit fields)
+// ---------------------------------------------------------------- worklist
+// Tile bookkeeping of the expert kernel for the routed experts (the shared
+// experts' tiles need no routing and are enumerated by the expert kernel
+// itself). Groups are listed widest first, so that the expert kernel, which
+// hands tiles out in list order, ends on narrow tiles whose epilogues are
+// short: routed experts with >= 96 rows, >= 32 rows, fewer (an expert with no
+// row holds no tile and its weights are never read), by id within a class
+// (stable counting sort; per-class counts packed two to an int, two block
+// scans). grp_list[p] = (token tiles of the groups before p) << kGrpIdBits |
+// expert of p, grp_list[E] = all token tiles << kGrpIdBits. Thread tid handles
+// experts [tid * gpt, tid * gpt + gpt).
+__device__ void write_group_tiles(const Dims &d, const Work &ws, const int32_t *s_off, int32_t *tmp,
+                                  int32_t *s_list) {
+  const int tid = threadIdx.x, E = d.E;
+  constexpr int kMaxGpt = 4;  // E <= 1024 with >= 256 threads
+  const int gpt = (E + blockDim.x - 1) / blockDim.x;
+  const int g0 = tid * gpt;
+  int cls[kMaxGpt], nt[kMaxGpt];
+  int pk0 = 0, pk1 = 0, hit = 0;  // class counts: 0, 1 in pk0, 2 in pk1 (16-bit fields)
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int g = 2 * tid + h;
-    if (g < G2) {
-      const bool shared = g >= E;
-      const int rows = shared ? n : s_off[g + 1] - s_off[g];
+  for (int h = 0; h < kMaxGpt; ++h) {
+    const int g = g0 + h;
+    cls[h] = -1;
+    nt[h] = 0;
+    if (h < gpt && g < E) {
+      const int rows = s_off[g + 1] - s_off[g];
       nt[h] = d.tn > 0 ? (rows + d.tn - 1) / d.tn : 0;
-      hit += !shared && rows > 0;
-      const int c = shared ? 3 : rows >= 96 ? 2 : rows >= 32 ? 1 : 0;
+      hit += rows > 0;
+      const int c = rows >= 96 ? 2 : rows >= 32 ? 1 : 0;
       cls[h] = c;
-      if (c < 2) pk0 += 1 << (16 * (c & 1));
-      else pk1 += 1 << (16 * (c & 1));
+      if (c < 2) pk0 += 1 << (16 * c);
+      else pk1 += 1;
     }
   }
   int tot0, tot1, n_hit;
   const int ex0 = block_excl_scan(pk0, tmp, &tot0);
   const int ex1 = block_excl_scan(pk1, tmp, &tot1);
   (void)block_excl_scan(hit, tmp, &n_hit);
-  auto field = [](int packed, int c) { return (packed >> (16 * (c & 1))) & 0xffff; };
-  const int count3 = field(tot1, 3), count2 = field(tot1, 2), count1 = field(tot0, 1);
+  const int count2 = tot1 & 0xffff, count1 = (tot0 >> 16) & 0xffff;
+  int run[3] = {ex0 & 0xffff, (ex0 >> 16) & 0xffff, ex1 & 0xffff};
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
+  for (int h = 0; h < kMaxGpt; ++h) {
     const int c = cls[h];
     if (c < 0) continue;
-    const int base = c == 3 ? 0 : c == 2 ? count3 : c == 1 ? count3 + count2 : count3 + count2 + count1;
-    const int pos = base + field(c < 2 ? ex0 : ex1, c) + (h == 1 && cls[0] == c ? 1 : 0);
-    ws.grp_list[pos] = (nt[h] << kGrpIdBits) | (2 * tid + h);  // token tiles until the prefix below
+    const int base = c == 2 ? 0 : c == 1 ? count2 : count2 + count1;
+    s_list[base + run[c]++] = (nt[h] << kGrpIdBits) | (g0 + h);  // token tiles until the prefix below
   }
   __syncthreads();  // the list in sorted order is visible to the whole CTA
-  int g_at[2] = {0, 0}, nt_at[2] = {0, 0};
+  int v[kMaxGpt], sum = 0;
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int p = 2 * tid + h;
-    if (p < G2) {
-      const int v = ws.grp_list[p];
-      g_at[h] = v & ((1 << kGrpIdBits) - 1);
-      nt_at[h] = v >> kGrpIdBits;
-    }
+  for (int h = 0; h < kMaxGpt; ++h) {
+    const int p = g0 + h;
+    v[h] = h < gpt && p < E ? s_list[p] : 0;
+    sum += v[h] >> kGrpIdBits;
   }
   int total;
-  const int before = block_excl_scan(nt_at[0] + nt_at[1], tmp, &total);
+  int before = block_excl_scan(sum, tmp, &total);
   if (total >= (1 << (31 - kGrpIdBits))) {
     if (tid == 0) set_error(ws.err, EPOCH_DEVERR_BOUNDS);
     total = 0;
+    before = 0;
   }
-  if (2 * tid < G2) ws.grp_list[2 * tid] = (before << kGrpIdBits) | g_at[0];
-  if (2 * tid + 1 < G2) ws.grp_list[2 * tid + 1] = ((before + nt_at[0]) << kGrpIdBits) | g_at[1];
+#pragma unroll
+  for (int h = 0; h < kMaxGpt; ++h) {
+    const int p = g0 + h;
+    if (h < gpt && p < E) {
+      ws.grp_list[p] = (before << kGrpIdBits) | (v[h] & ((1 << kGrpIdBits) - 1));
+      before += v[h] >> kGrpIdBits;
+    }
+  }
   if (tid == 0) {
-    ws.grp_list[G2] = total << kGrpIdBits;
-    const int t_sh = d.tn > 0 ? d.n_sh * ((n + d.tn - 1) / d.tn) : 0;
-    const int up = d.tn > 0 && total > 0 ? (d.I_s / 128) * t_sh + (d.I / 128) * (total - t_sh) : 0;
-    const int dn = d.tn > 0 && total > 0 ? (d.H / kBmDn) * total : 0;
+    ws.grp_list[E] = total << kGrpIdBits;
+    const int up = d.tn > 0 ? (d.I / 128) * total : 0;
+    const int dn = d.tn > 0 ? (d.H / kBmDn) * total : 0;
+    const int nt_sh = d.tn > 0 ? d.n_sh * ((d.n_pos + d.tn - 1) / d.tn) : 0;
     ws.ctrl->n_hit = n_hit;
     ws.ctrl->tiles_up = up;
     ws.ctrl->tiles_dn = dn;
     ws.stats->n_hit_experts = n_hit;
-    ws.stats->tiles_up = up;
-    ws.stats->tiles_down = dn;
+    ws.stats->tiles_up = up + (d.I_s / 128) * nt_sh;
+    ws.stats->tiles_down = dn + (d.H / kBmDn) * nt_sh;
   }
 }
 
-// Position categories of the routing kernel, and the per-CTA counters it sums.
-enum Category { C_LIVE = 0, C_NEW, C_MISS, C_STALE, C_REUSE, C_BAD, C_ANOM, C_REUSE_BEFORE };
-static_assert(C_REUSE_BEFORE < kBlkFields, "category counters");
+// One CTA builds the iteration's worklist from the selection words the gate
+// (or select) kernel set ([W] section "FreshLane Dispatch": pack, count
+// exchange -> offsets, compact dispatch -- here the count exchange is a
+// popcount over per-expert bitmasks on one chip). Only experts that can hold a
+// selection are visited: the support, or every expert on a fallback. Every
+// step before the worklist is published reads shared memory only, after one
+// batched load of the candidates' words (global memory round trips, not
+// arithmetic, bound this kernel):
+//  1 rows of each candidate expert and per-word prefixes (one warp per expert);
+//  2 expert offsets (scan), the expert kernel's group list and tile counts;
+//  3 worklist positions, expert-major, positions ascending: the row of fresh
+//    position t for expert e is offset(e) + rows of e before t;
+//  4 publish (route_done = this call's sequence number, release), so the
+//    expert kernel, already running, starts on the routed tiles;
+//  5 then, off the critical path: the ascending fresh list, the worklist row of
+//    every selection (for the combine), statistics, the state of positions
+//    beyond n_pos, the cleared selection words and shared-expert counters of
+//    the next iteration.
+constexpr int kRouteSmemWords = 12 * 1024;  // candidate words (and prefixes) kept in shared memory
 
-// One cooperative launch (one CTA per SM, 16 warps) runs the whole routing
-// side of an iteration in four phases separated by grid barriers:
-//  A  classify ([W] section "Liveness-Shard Parallelism"): each CTA takes a
-//     slice of positions -- live (still Mask), newly decoded (D_i \ D_{i-1}),
-//     decoded without a row, decoded with a row at least R iterations old, or
-//     stable decoded (Z_i, reuses its cached row). A decoded -> live transition
-//     anywhere, or a host-detected mismatch, makes the iteration full fresh
-//     ([W] sections "Two Clocks", "cold、hot-update、hot-skip").
-//  A' compaction: slice offsets from the per-CTA counts, an ascending fresh
-//     list, stamps of fresh rows, the new previous-decoded flags, statistics.
-//  B  one warp per fresh position: top-k of its logits over the support mask
-//     (every expert on a fallback), softmax weights over the selected logits
-//     ([W] section "Expert Atlas", step three); bit (f mod 32) of word
-//     (e, f / 32) marks that fresh position f selected expert e.
-//  C  worklist ([W] section "FreshLane Dispatch": pack, count exchange,
-//     compact dispatch -- here on chip): expert offsets from the counts; one
-//     warp per (expert, 32-position chunk) places its rows at
-//     offset(e) + rows of e in earlier chunks + bits below p, so rows are
-//     grouped by expert with positions ascending, and copies each row of x
-//     into the compact buffer. CTA 0 writes the grouped-GEMM tile lists.
-template <int EPL>
-__device__ __forceinline__ void routing_body(const Dims &d, const Work &ws,
-                                             const uint8_t *__restrict__ live, const uint8_t *__restrict__ decoded,
-                                             const uint4 *__restrict__ x, int vec_per_row) {
+__global__ void __launch_bounds__(kRouteThreads) k_route(Dims d, Work ws) {
   const KernelMark mark_(d, ws, K_ROUTING);
-  int64_t *trace_r = (d.trace && blockIdx.x < kTraceCtas)
-                         ? ws.trace + (3ull * kTraceCtas + blockIdx.x) * kTraceFields
-                         : nullptr;
-  if (trace_r && threadIdx.x == 0) trace_r[0] = static_cast<int64_t>(globaltimer_ns());
-  pdl_trigger();  // the expert kernel may start its launch; it waits on route_done
+  pdl_trigger();  // the expert kernel may start its launch; it waits on route_done for routed tiles
+  extern __shared__ uint32_t s_dyn[];
   __shared__ int32_t tmp[33];
-  __shared__ int32_t s_cat[kBlkFields];
   __shared__ int32_t s_off[1025];
-  __shared__ int16_t s_rank[kRoutingThreads];  // rank of each slice row in the slice's fresh rows, -1 reused
-  __shared__ int s_ok;
-  const int G = gridDim.x, b = blockIdx.x, tid = threadIdx.x;
-  const int lane = lane_id(), wid = warp_id(), nwarps = kRoutingThreads / 32;
-  const int n = d.n_pos, E = d.E, k = d.k;
-  const uint64_t tmo = static_cast<uint64_t>(d.timeout_ns);
-
-  // ---- phase 1a, while the gate kernel may still run: it reads only the
-  // masks and the previous iteration's state and writes only this iteration's.
-  // Every CTA classifies every position from the previous state
-  // (double-buffered: read half rd, write half rd ^ 1, so no CTA can overwrite
-  // what another still reads), which gives the anomaly flag, the fresh count
-  // and this CTA's offset in the fresh list; then it writes the new state of
-  // its own slice of positions.
+  __shared__ int16_t s_cand[1024];  // candidate experts (support ranking, or every expert)
+  __shared__ int16_t s_cidx[1024];  // candidate index of an expert, -1 if none
+  __shared__ int32_t s_cat[8];
+  __shared__ int s_force, s_anom, s_supp;
+  const int tid = threadIdx.x, lane = lane_id(), wid = warp_id(), nw = kRouteThreads / 32;
+  const int n = d.n_pos, E = d.E, k = d.k, cmax = d.cmax;
+  const int nch = (n + 31) >> 5;
   const int rd = d.state_rd & 1, wr = rd ^ 1;
-  const int32_t *stamp_old = ws.stamp + static_cast<size_t>(rd) * d.Nmax;
-  const uint8_t *prev_old = ws.prev_dec + static_cast<size_t>(rd) * d.Nmax;
-  int32_t *stamp_new = ws.stamp + static_cast<size_t>(wr) * d.Nmax;
-  uint8_t *prev_new = ws.prev_dec + static_cast<size_t>(wr) * d.Nmax;
-  const int per = (n + G - 1) / G;  // <= kRoutingThreads (the launch checks the grid)
-  const int lo = min(b * per, n), hi = min(lo + per, n);
-  if (tid < kBlkFields) s_cat[tid] = 0;
-  for (int g = b * kRoutingThreads + tid; g < E + d.n_sh; g += G * kRoutingThreads) ws.done_up[g] = 0;
-  if (b == 0 && tid == 0) *ws.tile_ctr = 0;  // the expert kernel hands tiles out from this counter
-  // positions beyond this call's n_pos keep their state
-  for (int t = n + b * kRoutingThreads + tid; t < d.Nmax; t += G * kRoutingThreads) {
-    stamp_new[t] = stamp_old[t];
-    prev_new[t] = prev_old[t];
-  }
-  // category of position t: live (still Mask, or not decoded), newly decoded,
-  // decoded without a row, decoded with a row at least R iterations old, or
-  // stable decoded (reuses its cached row)
-  // (packed: category | live << 4 | contradictory flags << 5 | decoded -> live << 6)
-  auto classify = [&](int t) -> int {
-    const bool lv = live[t] != 0, dc = decoded[t] != 0;
-    const bool il = lv || !dc, prev = prev_old[t] != 0;
-    const int st = stamp_old[t];
-    const int flags = (il ? 16 : 0) | (lv == dc ? 32 : 0) | (il && prev ? 64 : 0);
-    if (il) return C_LIVE | flags;
-    if (!prev) return C_NEW | flags;
-    if (st < 0) return C_MISS | flags;
-    if (d.R != INT_MAX && d.iter - st >= d.R) return C_STALE | flags;
-    return C_REUSE | flags;
+  int64_t *trace = (d.trace && blockIdx.x < kTraceCtas) ? ws.trace + (3ull * kTraceCtas + blockIdx.x) * kTraceFields
+                                                         : nullptr;
+  if (trace && tid == 0) trace[0] = static_cast<int64_t>(globaltimer_ns());
+  // the block plan (written before this iteration began) can be read at once
+  if (tid < 8) s_cat[tid] = 0;
+  if (tid == 0) s_supp = min(E, ws.ctrl->support_len);
+  for (int e = tid; e < E; e += kRouteThreads) s_cand[e] = static_cast<int16_t>(ws.support_ids[e]);
+  for (int e = tid; e <= E; e += kRouteThreads) s_off[e] = 0;
+  pdl_wait();  // the gate / select kernel has finished: selection words, selections, codes
+  if (trace && tid == 0) trace[1] = static_cast<int64_t>(globaltimer_ns());
+  const uint32_t *words = ws.sel_words + static_cast<size_t>(wr) * E * cmax;
+
+  // Candidates: the support, or every expert on a host-detected fallback.
+  // Their words are requested together with the decoded -> live scan of the
+  // codes the gate wrote (one round trip); an anomaly found there turns the
+  // iteration into a fallback and the words of every expert are loaded.
+  uint32_t *sw = s_dyn;
+  int32_t *sp = reinterpret_cast<int32_t *>(s_dyn + kRouteSmemWords);
+  auto load_words = [&](int n_c) {
+    for (int q0 = tid; q0 < n_c * nch; q0 += kRouteThreads * 8) {
+      uint32_t v[8];
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        const int q = q0 + b * kRouteThreads;
+        v[b] = q < n_c * nch ? words[static_cast<size_t>(s_cand[q / nch]) * cmax + q % nch] : 0u;
+      }
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        const int q = q0 + b * kRouteThreads;
+        if (q < n_c * nch) sw[q] = v[b];
+      }
+    }
   };
+  if (d.host_fallback)
+    for (int e = tid; e < E; e += kRouteThreads) s_cand[e] = static_cast<int16_t>(e);
+  __syncthreads();
+  int n_cand = d.host_fallback ? E : s_supp;
+  bool in_smem = n_cand * nch <= kRouteSmemWords;
   {
-    int cnt[kBlkFields];
-#pragma unroll
-    for (int c = 0; c < kBlkFields; ++c) cnt[c] = 0;
-    for (int t = tid; t < n; t += kRoutingThreads) {
-      const int code = classify(t), c = code & 15;
-#pragma unroll
-      for (int q = 0; q < C_BAD; ++q) cnt[q] += c == q;
-      cnt[C_BAD] += (code >> 5) & 1;
-      cnt[C_ANOM] |= (code >> 6) & 1;
-      cnt[C_REUSE_BEFORE] += c == C_REUSE && t < lo;
-    }
-#pragma unroll
-    for (int c = 0; c < kBlkFields; ++c) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) cnt[c] += __shfl_xor_sync(0xffffffffu, cnt[c], o);
-    }
-    __syncthreads();  // s_cat cleared
-    if (lane == 0) {
-#pragma unroll
-      for (int c = 0; c < kBlkFields; ++c) atomicAdd(&s_cat[c], cnt[c]);
+    int anom = 0;
+    for (int t = tid; t < n; t += kRouteThreads) anom |= ws.cat[t] & kCodeAnom;
+    if (in_smem) load_words(n_cand);
+    const int any = __syncthreads_or(anom);
+    if (tid == 0) {
+      s_anom = any != 0;
+      s_force = (d.host_fallback != 0 || any != 0) ? 1 : 0;
     }
     __syncthreads();
   }
-  const bool any_anom = s_cat[C_ANOM] != 0;
-  const bool force = d.host_fallback || any_anom;
-  const int n_fresh = force ? n : n - s_cat[C_REUSE];
-  const int fresh_before = force ? lo : lo - s_cat[C_REUSE_BEFORE];
-  if (b == 0 && tid == 0) {
-    const int fb = (d.host_fallback ? 1 : 0) | (any_anom ? 2 : 0);
+  const bool force = s_force != 0;
+  if (force && !d.host_fallback) {  // anomaly: every expert is a candidate
+    for (int e = tid; e < E; e += kRouteThreads) s_cand[e] = static_cast<int16_t>(e);
+    __syncthreads();
+    n_cand = E;
+    in_smem = n_cand * nch <= kRouteSmemWords;
+    if (in_smem) load_words(n_cand);
+  }
+  for (int e = tid; e < E; e += kRouteThreads) s_cidx[e] = -1;
+  __syncthreads();
+  for (int i = tid; i < n_cand; i += kRouteThreads) s_cidx[s_cand[i]] = static_cast<int16_t>(i);
+  int64_t *trace2 = trace ? ws.trace + (5ull * kTraceCtas + blockIdx.x) * kTraceFields : nullptr;
+  if (trace2 && tid == 0) trace2[0] = static_cast<int64_t>(globaltimer_ns());
+  __syncthreads();
+  auto word = [&](int ci, int c) -> uint32_t {
+    return in_smem ? sw[ci * nch + c] : words[static_cast<size_t>(s_cand[ci]) * cmax + c];
+  };
+  auto pre = [&](int ci, int c) -> int32_t & {
+    return in_smem ? sp[ci * nch + c] : ws.pre[static_cast<size_t>(s_cand[ci]) * cmax + c];
+  };
+
+  // ---- 1: rows of each candidate expert and the per-word prefixes
+  {
+    const int cpl = (nch + 31) / 32;
+    for (int ci = wid; ci < n_cand; ci += nw) {
+      const int c0 = min(nch, lane * cpl), c1 = min(nch, c0 + cpl);
+      int sum = 0;
+      for (int c = c0; c < c1; ++c) sum += __popc(word(ci, c));
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      int run = incl - sum;
+      for (int c = c0; c < c1; ++c) {
+        pre(ci, c) = run;
+        run += __popc(word(ci, c));
+      }
+      if (lane == 31) s_off[s_cand[ci]] = incl;  // count, scanned below
+    }
+  }
+  __syncthreads();
+  if (trace && tid == 0) trace[2] = static_cast<int64_t>(globaltimer_ns());
+
+  // ---- 2: offsets (thread tid scans experts [tid * gpt, tid * gpt + gpt)), group list, counters
+  int n_edges;
+  {
+    const int gpt = (E + kRouteThreads - 1) / kRouteThreads;
+    const int g0 = tid * gpt;
+    int c[4] = {0, 0, 0, 0}, sum = 0;
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+      if (h < gpt && g0 + h < E) {
+        c[h] = s_off[g0 + h];
+        sum += c[h];
+      }
+    int before = block_excl_scan(sum, tmp, &n_edges);
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+      if (h < gpt && g0 + h < E) {
+        s_off[g0 + h] = before;
+        before += c[h];
+      }
+    if (tid == 0) s_off[E] = n_edges;
+  }
+  __syncthreads();
+  for (int e = tid; e <= E; e += kRouteThreads) ws.offsets[e] = s_off[e];
+  if (trace2 && tid == 0) trace2[1] = static_cast<int64_t>(globaltimer_ns());
+  write_group_tiles(d, ws, s_off, tmp, reinterpret_cast<int32_t *>(s_dyn + 2 * kRouteSmemWords));
+  for (int g = tid; g < E; g += kRouteThreads) ws.done_up[g] = 0;
+  if (tid == 0) {
+    ws.tile_ctr[0] = 0;  // routed tiles drawn
+    ws.tile_ctr[2] = 0;  // 16-byte vectors of worklist rows copied into xp
+    ws.ctrl->n_edges = n_edges;
+  }
+  if (trace && tid == 0) trace[3] = static_cast<int64_t>(globaltimer_ns());
+
+  // ---- 3: worklist positions, one thread per candidate word
+  for (int q = tid; q < n_cand * nch; q += kRouteThreads) {
+    const int ci = q / nch, c = q - ci * nch;
+    uint32_t w = word(ci, c);
+    if (w == 0u) continue;
+    int dst = s_off[s_cand[ci]] + pre(ci, c);
+    while (w) {
+      const int b = __ffs(w) - 1;
+      w &= w - 1u;
+      if (dst < 0 || dst >= d.Nmax * k) {
+        set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+        break;
+      }
+      ws.wl_pos[dst++] = 32 * c + b;
+    }
+  }
+  // ---- 4: publish the worklist (every thread's writes, then one release)
+  if (trace2 && tid == 0) trace2[2] = static_cast<int64_t>(globaltimer_ns());
+  __syncthreads();
+  if (tid == 0) {
+    if (trace2) trace2[3] = static_cast<int64_t>(globaltimer_ns());
+    __threadfence();
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ws.route_done), "r"(d.seq) : "memory");
+  }
+  if (trace && tid == 0) trace[4] = static_cast<int64_t>(globaltimer_ns());
+
+  // ---- 5: fresh list, selection slots, statistics; thread tid owns a
+  // contiguous range of positions so the fresh list comes out ascending
+  const int ppt = (n + kRouteThreads - 1) / kRouteThreads;
+  const int p0 = min(n, tid * ppt), p1 = min(n, p0 + ppt);
+  int cnt[5] = {0, 0, 0, 0, 0}, bad = 0;
+  for (int t = p0; t < p1; ++t) {
+    const int code = ws.cat[t];
+    const int c = code & 15;
+#pragma unroll
+    for (int q = 0; q < 5; ++q) cnt[q] += c == q;
+    bad += (code & kCodeBad) ? 1 : 0;
+  }
+  int n_fresh;
+  int f = block_excl_scan((p1 - p0) - (force ? 0 : cnt[C_REUSE]), tmp, &n_fresh);
+  for (int t = p0; t < p1; ++t) {
+    const bool fresh = force || (ws.cat[t] & 15) != C_REUSE;
+    if (!fresh) {
+      ws.fidx[t] = -1;
+      continue;
+    }
+    ws.fresh_pos[f] = t;
+    ws.fidx[t] = f++;
+    const int c = t >> 5;
+    const uint32_t below = (1u << (t & 31)) - 1u;
+    for (int j = 0; j < k; ++j) {
+      const int e = ws.sel[static_cast<size_t>(t) * k + j];
+      if (e < 0 || e >= E) {
+        set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+        ws.slot[static_cast<size_t>(t) * k + j] = 0;
+        continue;
+      }
+      const int ci = s_cidx[e];
+      if (ci < 0) {
+        set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+        ws.slot[static_cast<size_t>(t) * k + j] = 0;
+        continue;
+      }
+      ws.slot[static_cast<size_t>(t) * k + j] = s_off[e] + pre(ci, c) + __popc(word(ci, c) & below);
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < 5; ++q) cnt[q] = __reduce_add_sync(0xffffffffu, cnt[q]);
+  bad = __reduce_add_sync(0xffffffffu, bad);
+  if (lane == 0) {
+#pragma unroll
+    for (int q = 0; q < 5; ++q) atomicAdd(&s_cat[q], cnt[q]);
+    atomicAdd(&s_cat[5], bad);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const int fb = (d.host_fallback ? 1 : 0) | (s_anom ? 2 : 0);
+    if (n_fresh * k != n_edges) set_error(ws.err, EPOCH_DEVERR_BOUNDS);
     ws.ctrl->n_fresh = n_fresh;
     ws.ctrl->fallback = fb;
-    ws.ctrl->n_edges = n_fresh * k;
     epoch_iter_stats *st = ws.stats;
     st->iteration = d.iter;
     st->n_pos = n;
@@ -390,201 +515,94 @@ __device__ __forceinline__ void routing_body(const Dims &d, const Work &ws,
     st->n_forced = force ? s_cat[C_REUSE] : 0;
     st->n_reuse = force ? 0 : s_cat[C_REUSE];
     st->n_fresh = n_fresh;
-    st->n_edges = n_fresh * k;
+    st->n_edges = n_edges;
     st->support_len = fb ? E : ws.ctrl->support_len;
     st->fallback = fb;
-    st->bad_flags = s_cat[C_BAD];
-    if (s_cat[C_BAD]) set_error(ws.err, EPOCH_DEVERR_FLAGS);
+    st->bad_flags = s_cat[5];
+    if (s_cat[5]) set_error(ws.err, EPOCH_DEVERR_FLAGS);
   }
-  {
-    const int t = lo + tid;
-    const bool mine = t < hi;
-    bool il = false, fresh = false;
-    if (mine) {
-      const int code = classify(t);
-      il = (code & 16) != 0;
-      fresh = (code & 15) != C_REUSE || force;
-    }
-    int slice_fresh;
-    const int rank = block_excl_scan(fresh ? 1 : 0, tmp, &slice_fresh);
-    if (mine) {
-      if (fresh) {
-        const int f = fresh_before + rank;
-        ws.fresh_pos[f] = t;
-        ws.fidx[t] = f;
-        stamp_new[t] = d.iter;
-      } else {
-        ws.fidx[t] = -1;
-        stamp_new[t] = stamp_old[t];
-      }
-      prev_new[t] = il ? 0 : 1;
-      s_rank[tid] = static_cast<int16_t>(fresh ? rank : -1);
-    }
+  // positions beyond this call's n_pos keep their state
+  for (int t = n + tid; t < d.Nmax; t += kRouteThreads) {
+    ws.stamp[static_cast<size_t>(wr) * d.Nmax + t] = ws.stamp[static_cast<size_t>(rd) * d.Nmax + t];
+    ws.prev_dec[static_cast<size_t>(wr) * d.Nmax + t] = ws.prev_dec[static_cast<size_t>(rd) * d.Nmax + t];
   }
-  __syncthreads();  // s_rank
-  if (trace_r && tid == 0) trace_r[1] = static_cast<int64_t>(globaltimer_ns());
+  // the words and the shared-expert tile counters of the next iteration start at zero
+  uint32_t *next = ws.sel_words + static_cast<size_t>(rd) * E * cmax;
+  for (int q = tid; q < E * cmax; q += kRouteThreads) next[q] = 0u;
+  const int nxt = static_cast<int>((d.seq + 1u) & 1u);
+  int32_t *sh = ws.sh_ctr + static_cast<size_t>(nxt) * sh_stride(d);
+  for (int q = tid; q < sh_stride(d); q += kRouteThreads) sh[q] = 0;
+  if (trace && tid == 0) trace[5] = static_cast<int64_t>(globaltimer_ns());
+}
 
-  // ---- phase 1b, after the gate kernel: one warp per fresh row of the slice
-  // takes the top-k of its logits over the support mask (every expert on a
-  // fallback) and the softmax weights over the selected logits ([W] section
-  // "Expert Atlas", step three); bit (f mod 32) of word (e, f / 32) marks that
-  // fresh position f selected expert e (words zeroed by the gate kernel).
-  pdl_wait();
-  if (trace_r && tid == 0) trace_r[2] = static_cast<int64_t>(globaltimer_ns());
-  for (int r = wid; r < hi - lo; r += nwarps) {
-    const int rank = s_rank[r];
-    if (rank < 0) continue;
-    const int t = lo + r, f = fresh_before + rank, e0 = lane * EPL;
-    float v[EPL];
-    lane_logits<EPL>(ws.logits + static_cast<size_t>(t) * E, E, v);
-    bool ok[EPL];
-#pragma unroll
-    for (int c = 0; c < EPL; ++c) {
-      const int e = e0 + c;
-      ok[c] = e < E && (force || ws.support_mask[e]);
-    }
-    int sel;
-    float val;
-    warp_topk<EPL>(v, ok, k, &sel, &val);
-    const float top = __shfl_sync(0xffffffffu, val, 0);
-    const float ex = lane < k ? expf(val - top) : 0.f;
-    float denom = 0.f;  // summed in selection order j = 0..k-1 (deterministic)
-    for (int j = 0; j < k; ++j) denom += __shfl_sync(0xffffffffu, ex, j);
-    if (lane < k) {
-      if (sel < 0 || sel >= E || f >= n_fresh) {
-        set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-      } else {
-        ws.sel[f * k + lane] = sel;
-        ws.selw[f * k + lane] = ex / denom;
-        atomicOr(&ws.chunk_mask[static_cast<size_t>(sel) * d.cmax + (f >> 5)], 1u << (f & 31));
+// ---------------------------------------------------------------- permute
+// Copies the token rows of the worklist into the compact buffer xp (row l = x
+// at wl_pos[l], [W] section "FreshLane Dispatch": compact dispatch), so the
+// expert kernel loads each expert's rows as one tiled TMA box. Launched right
+// behind the worklist kernel, it waits for the worklist to be published
+// (route_done = this call's sequence number), copies its share of the 16-byte
+// vectors and adds their count to tile_ctr[2]; the expert kernel's routed up
+// tiles start once that count reaches L * (vectors per row). Before exiting it
+// waits for the worklist kernel to complete, so that the kernels after it see
+// that kernel's remaining writes.
+constexpr int kPermuteThreads = 256;
+// Small footprint (256 threads, at most 40 registers): its CTAs must fit beside
+// the gate's and the expert kernel's on every SM, or the expert kernel, launched
+// behind it, could not start its shared-expert tiles early.
+__global__ void __launch_bounds__(kPermuteThreads, 6) k_permute(Dims d, Work ws, const uint4 *__restrict__ x, int vpr) {
+  pdl_trigger();
+  __shared__ int s_ok, s_L;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    int ok = 1;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+      unsigned int v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ws.route_done) : "memory");
+      if (v == d.seq) break;
+      if (globaltimer_ns() - t0 > static_cast<uint64_t>(d.timeout_ns)) {
+        set_error(ws.err, EPOCH_DEVERR_TIMEOUT);
+        ok = 0;
+        break;
       }
+      __nanosleep(32);
     }
+    s_ok = ok;
+    s_L = ok ? ws.ctrl->n_edges : 0;
   }
-  if (!grid_sync(ws.gbar, 1u * G, ws.err, tmo, &s_ok)) return;
-  if (trace_r && tid == 0) trace_r[3] = static_cast<int64_t>(globaltimer_ns());
-
-  // ---- phase C: expert offsets, worklist rows, compact copies of x, tile lists
-  const int fresh_chunks = (n_fresh + 31) / 32;
-  {
-    // rows of each expert = popcount of its selection masks (every CTA derives
-    // the offsets itself; no global counters)
-    int cnt2[2] = {0, 0};
+  __syncthreads();
+  const int L = s_L;
+  const long long units = static_cast<long long>(L) * vpr;
+  const long long u0 = units * blockIdx.x / gridDim.x, u1 = units * (blockIdx.x + 1) / gridDim.x;
+  uint4 *xp = static_cast<uint4 *>(ws.xp);
+  for (long long base = u0; base < u1; base += kPermuteThreads * 4) {
+    uint4 buf[4];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int e = 2 * tid + h;
-      if (e < E) {
-        const uint32_t *row = ws.chunk_mask + static_cast<size_t>(e) * d.cmax;
-        int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
-        int c = 0;
-        for (; c + 4 <= fresh_chunks; c += 4) {
-          a0 += __popc(row[c]);
-          a1 += __popc(row[c + 1]);
-          a2 += __popc(row[c + 2]);
-          a3 += __popc(row[c + 3]);
-        }
-        for (; c < fresh_chunks; ++c) a0 += __popc(row[c]);
-        cnt2[h] = a0 + a1 + a2 + a3;
-      }
-    }
-    const int c0 = cnt2[0], c1 = cnt2[1];
-    int tot;
-    const int o = block_excl_scan(c0 + c1, tmp, &tot);
-    if (2 * tid < E) s_off[2 * tid] = o;
-    if (2 * tid + 1 < E) s_off[2 * tid + 1] = o + c0;
-    if (tid == 0) s_off[E] = tot;
-    __syncthreads();
-  }
-  // With more than one CTA, CTA 0 writes the expert offsets and the group list
-  // while the others place the worklist rows, meet at a second barrier and copy
-  // each worklist row of x into the compact buffer; the expert kernel starts
-  // once every CTA has counted itself done.
-  const bool split = G > 1;
-  const int wb = split ? b - 1 : b, wg = split ? G - 1 : G;  // worker CTAs
-  if (!(split && b == 0)) {
-    for (int pair = wb * nwarps + wid; pair < E * fresh_chunks; pair += wg * nwarps) {
-      const int e = pair / fresh_chunks, c = pair % fresh_chunks;
-      const uint32_t *row = ws.chunk_mask + static_cast<size_t>(e) * d.cmax;
-      const uint32_t m = row[c];
-      if (m == 0u) continue;
-      int before_c = 0;
-      for (int c2 = lane; c2 < c; c2 += 32) before_c += __popc(row[c2]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) before_c += __shfl_xor_sync(0xffffffffu, before_c, o);
-      if ((m >> lane) & 1u) {  // lane p places the edge of fresh position 32 c + p
-        const int f = c * 32 + lane;
-        const int dst = s_off[e] + before_c + __popc(m & ((1u << lane) - 1u));
-        if (dst < 0 || dst >= d.Nmax * k || f >= n_fresh) {
+    for (int q = 0; q < 4; ++q) {
+      const long long u = base + tid + kPermuteThreads * q;
+      if (u < u1) {
+        const int r = static_cast<int>(u / vpr), v = static_cast<int>(u - static_cast<long long>(r) * vpr);
+        int pos = ws.wl_pos[r];
+        if (pos < 0 || pos >= d.n_pos) {
           set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-        } else {
-          ws.wl_pos[dst] = ws.fresh_pos[f];
-          for (int j = 0; j < k; ++j)
-            if (ws.sel[f * k + j] == e) ws.slot[f * k + j] = dst;
+          pos = 0;
         }
+        buf[q] = __ldg(x + static_cast<size_t>(pos) * vpr + v);
       }
     }
-    if (trace_r && tid == 0) trace_r[4] = static_cast<int64_t>(globaltimer_ns());
-    if (split) {
-      if (!grid_sync(ws.gbar, 1u * G + (G - 1), ws.err, tmo, &s_ok)) return;
-    } else {
-      __syncthreads();
-    }
-  } else if (trace_r && tid == 0) {
-    trace_r[4] = static_cast<int64_t>(globaltimer_ns());
-  }
-  if (b == 0) {
-    for (int e = tid; e <= E; e += kRoutingThreads) ws.offsets[e] = s_off[e];
-    if (trace_r && tid == 0) trace_r[5] = static_cast<int64_t>(globaltimer_ns());
-    write_group_tiles(d, ws, s_off, tmp, n);
-    if (trace_r && tid == 0) trace_r[6] = static_cast<int64_t>(globaltimer_ns());
-    if (split) return;
-  }
-
-  // ---- phase 3: copy each worklist row of x into the compact buffer
-  const int n_edges = n_fresh * k;
-  for (int l = wb * nwarps + wid; l < n_edges; l += wg * nwarps) {
-    const int tp = ws.wl_pos[l];
-    if (tp < 0 || tp >= n) {
-      if (lane == 0) set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-      continue;
-    }
-    const uint4 *src = x + static_cast<size_t>(tp) * vec_per_row;
-    uint4 *out = reinterpret_cast<uint4 *>(ws.xp) + static_cast<size_t>(l) * vec_per_row;
-    // all loads of a batch are issued before its stores (the destination may
-    // alias nothing the loads read, but the compiler cannot know that)
-    for (int v0 = 0; v0 < vec_per_row; v0 += 32 * 8) {
-      uint4 buf[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int v = v0 + q * 32 + lane;
-        if (v < vec_per_row) buf[q] = __ldg(src + v);
-      }
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int v = v0 + q * 32 + lane;
-        if (v < vec_per_row) out[v] = buf[q];
-      }
+    for (int q = 0; q < 4; ++q) {
+      const long long u = base + tid + kPermuteThreads * q;
+      if (u < u1) xp[u] = buf[q];
     }
   }
-  if (trace_r && tid == 0) trace_r[5] = static_cast<int64_t>(globaltimer_ns());
-}
-
-// The launch: after its last write every CTA counts itself into route_done
-// (zeroed by the gate kernel) with release semantics; the expert kernel, which
-// may already be running (programmatic dependent launch), acquires that count
-// instead of waiting for this grid to retire.
-template <int EPL>
-__global__ void __launch_bounds__(kRoutingThreads) k_routing(Dims d, Work ws,
-                                                             const uint8_t *__restrict__ live,
-                                                             const uint8_t *__restrict__ decoded,
-                                                             const uint4 *__restrict__ x, int vec_per_row) {
-  routing_body<EPL>(d, ws, live, decoded, x, vec_per_row);
-  __syncthreads();  // every return in the body is uniform over the CTA
-  if (threadIdx.x == 0) {
+  __syncthreads();
+  if (tid == 0 && s_ok && u1 > u0) {
     __threadfence();
-    atomicAdd(ws.route_done, 1u);
+    atomicAdd(ws.tile_ctr + 2, static_cast<int>(u1 - u0));
   }
+  pdl_wait();
 }
-
 
 // ---------------------------------------------------------------- combine + cache
 // Eight consecutive elements of a row, loaded/stored as one or two 16-byte vectors.
@@ -632,13 +650,13 @@ __global__ void __launch_bounds__(128) k_combine(Dims d, Work ws, const T *__res
   __shared__ int32_t slot_s[16];
   __shared__ float w_s[16];
   if (f >= 0 && threadIdx.x < k) {
-    int sl = ws.slot[f * k + threadIdx.x];
+    int sl = ws.slot[static_cast<size_t>(t) * k + threadIdx.x];
     if (sl < 0 || sl >= d.Nmax * k) {
       set_error(ws.err, EPOCH_DEVERR_BOUNDS);
       sl = 0;
     }
     slot_s[threadIdx.x] = sl;
-    w_s[threadIdx.x] = ws.selw[f * k + threadIdx.x];
+    w_s[threadIdx.x] = ws.selw[static_cast<size_t>(t) * k + threadIdx.x];
   }
   __syncthreads();
   for (int h0 = threadIdx.x * 8; h0 < H; h0 += blockDim.x * 8) {
@@ -698,14 +716,6 @@ static int epl_for(int E) {
   return epl <= 1 ? 1 : epl <= 2 ? 2 : epl <= 4 ? 4 : epl <= 8 ? 8 : epl <= 16 ? 16 : 32;
 }
 
-// One routing CTA per SM (at most kMaxRoutingGrid). The grid barriers need
-// every CTA resident at once, which holds without a cooperative launch: the
-// kernel is launched while the gate kernel (at most one CTA per SM, and never
-// waiting on routing) may still run, so CTAs that do not fit yet start as gate
-// CTAs retire, and the kernels after it are launched only once every routing
-// CTA has started (programmatic launch trigger). Every wait is bounded anyway.
-int routing_grid() { return num_sms() < kMaxRoutingGrid ? num_sms() : kMaxRoutingGrid; }
-
 int num_sms() {
   static int n = 0;
   if (n == 0) {
@@ -718,13 +728,15 @@ int num_sms() {
 }
 
 cudaError_t launch_kernel(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void **args,
-                          bool cooperative, bool programmatic) {
+                          bool programmatic, int cluster) {
   static bool pdl_ok = true;
   cudaLaunchAttribute attr[2];
   int n = 0;
-  if (cooperative) {
-    attr[n].id = cudaLaunchAttributeCooperative;
-    attr[n].val.cooperative = 1;
+  if (cluster > 0) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
     ++n;
   }
   const bool pdl = programmatic && pdl_ok;
@@ -794,37 +806,50 @@ cudaError_t launch_plan_support(const Dims &d, const Work &ws, int32_t threshold
   return cudaGetLastError();
 }
 
-// Cooperative launch (the phases wait on one another through grid barriers,
-// so every CTA must be resident): one CTA per SM, capped at what fits.
-cudaError_t launch_routing(const Dims &d, const Weights &w, const Work &ws, const uint8_t *live,
-                           const uint8_t *decoded, const void *x, int bf16, cudaStream_t s) {
-  const int grid = routing_grid();
-  // slices of at most kRoutingThreads positions per CTA
-  const int min_grid = (d.n_pos + kRoutingThreads - 1) / kRoutingThreads;
-  if (grid < min_grid) return cudaErrorInvalidConfiguration;
-  Dims dd = d;
-  Work ww = ws;
-  const int vec = d.H * (bf16 ? 2 : 4) / 16;
-  const uint4 *xv = static_cast<const uint4 *>(x);
-  void *args[] = {&dd, &ww, const_cast<uint8_t **>(&live), const_cast<uint8_t **>(&decoded),
-                  const_cast<uint4 **>(&xv), const_cast<int *>(&vec)};
+cudaError_t launch_select(const Dims &d, const Work &ws, const uint8_t *live, const uint8_t *decoded,
+                          cudaStream_t s) {
+  int blocks = (d.n_pos + 7) / 8;
+  if (blocks > 2 * num_sms()) blocks = 2 * num_sms();
   switch (epl_for(d.E)) {
-#define EPOCH_CASE(N)                                                                                    \
-  case N: {                                                                                              \
-    static bool c_ = (prefer_max_shared(k_routing<N>) == cudaSuccess);                                   \
-    (void)c_;                                                                                            \
-    return launch_kernel(reinterpret_cast<void *>(k_routing<N>), dim3(grid), dim3(kRoutingThreads), 0, s, args, \
-                         false, true);                                                                   \
+#define EPOCH_CASE(N)                                                                  \
+  case N: {                                                                            \
+    static bool c_ = (prefer_max_shared(k_select<N>) == cudaSuccess);                  \
+    (void)c_;                                                                          \
+    k_select<N><<<blocks, 256, 0, s>>>(d, ws, live, decoded);                          \
+    break;                                                                             \
   }
     EPOCH_CASE(1) EPOCH_CASE(2) EPOCH_CASE(4) EPOCH_CASE(8) EPOCH_CASE(16) EPOCH_CASE(32)
 #undef EPOCH_CASE
   }
-  return cudaErrorInvalidValue;
+  return cudaGetLastError();
 }
 
+cudaError_t launch_permute(const Dims &d, const Work &ws, const void *x, cudaStream_t s) {
+  static bool c_ = (prefer_max_shared(k_permute) == cudaSuccess);
+  (void)c_;
+  Dims dd = d;
+  Work ww = ws;
+  const uint4 *xv = static_cast<const uint4 *>(x);
+  int vpr = d.H * 2 / 16;
+  void *args[] = {&dd, &ww, &xv, &vpr};
+  // two CTAs per SM: both still fit beside a gate CTA
+  return launch_kernel(reinterpret_cast<void *>(k_permute), dim3(2 * num_sms()), dim3(kPermuteThreads), 0, s, args,
+                       true);
+}
 
-
-
+// One CTA, launched programmatically: it starts while the gate kernel runs and
+// waits for it (pdl_wait) before reading its outputs.
+cudaError_t launch_route(const Dims &d, const Work &ws, cudaStream_t s) {
+  if (d.E > 4 * kRouteThreads) return cudaErrorInvalidConfiguration;
+  constexpr size_t kDyn = (2 * kRouteSmemWords + 1024) * 4;  // words, prefixes, group list
+  static bool c_ = (prefer_max_shared(k_route) == cudaSuccess &&
+                    cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn) == cudaSuccess);
+  if (!c_) return cudaErrorInvalidConfiguration;
+  Dims dd = d;
+  Work ww = ws;
+  void *args[] = {&dd, &ww};
+  return launch_kernel(reinterpret_cast<void *>(k_route), dim3(1), dim3(kRouteThreads), kDyn, s, args, true);
+}
 
 cudaError_t launch_combine(const Dims &d, const Work &ws, const void *x, void *y, int bf16, cudaStream_t s) {
   if (bf16) {
@@ -836,7 +861,7 @@ cudaError_t launch_combine(const Dims &d, const Work &ws, const void *x, void *y
     Work ww = ws;
     void *args[] = {&dd, &ww, &xb, &yb};
     return launch_kernel(reinterpret_cast<void *>(k_combine<__nv_bfloat16>), dim3(d.n_pos), dim3(128), 0, s, args,
-                         false, true);
+                         true);
   }
   static bool carve_ = (prefer_max_shared(k_combine<float>) == cudaSuccess);
   (void)carve_;

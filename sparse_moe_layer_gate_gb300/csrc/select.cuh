@@ -1,0 +1,135 @@
+// Per-position classification and support-restricted top-k of one iteration,
+// shared by the tcgen05 gate's epilogue (bf16 layers) and the select kernel
+// that follows the FFMA gate (fp32 layers).
+//
+// Walk-through page "Epoch 完全拆解:把扩散块编译成稀疏 MoE 服务单元":
+//  - section "Liveness-Shard Parallelism": Z_i (stable decoded positions whose
+//    cached routed row is reused), N_i = D_i \ D_{i-1} (newly decoded), and the
+//    fresh set F_i = everything else (still-live Mask positions, new commits,
+//    decoded rows without a cached row or with one at least R iterations old);
+//  - section "Expert Atlas", step three: top-k of G[t, .] restricted to the
+//    block's support, weights from the selected logits;
+//  - sections "Two Clocks" and "cold、hot-update、hot-skip": any liveness
+//    anomaly (a decoded position turning live) sends the iteration back to
+//    the full fresh path with every expert eligible.
+#pragma once
+
+#include <climits>
+
+#include "common.cuh"
+#include "layer.h"
+#include "topk.cuh"
+
+namespace epoch {
+
+// Position categories; a code packs the category with three flag bits.
+enum Category { C_LIVE = 0, C_NEW, C_MISS, C_STALE, C_REUSE };
+constexpr int kCodeLive = 16;  // treated as live (live flag set, or decoded flag clear)
+constexpr int kCodeBad = 32;   // contradictory flags (both or neither set)
+constexpr int kCodeAnom = 64;  // decoded at the previous iteration, live now
+
+// Category of a position from its flags and the previous iteration's state:
+// live (still Mask, or not decoded), newly decoded, decoded without a row,
+// decoded with a row at least R iterations old, or stable decoded (reuses its
+// cached row).
+__device__ __forceinline__ int classify_code(const Dims &d, bool lv, bool dc, bool prev, int stamp) {
+  const bool il = lv || !dc;
+  const int flags = (il ? kCodeLive : 0) | (lv == dc ? kCodeBad : 0) | (il && prev ? kCodeAnom : 0);
+  if (il) return C_LIVE | flags;
+  if (!prev) return C_NEW | flags;
+  if (stamp < 0) return C_MISS | flags;
+  if (d.R != INT_MAX && d.iter - stamp >= d.R) return C_STALE | flags;
+  return C_REUSE | flags;
+}
+
+// 0x80 in every byte of x that is zero, 0 elsewhere.
+__device__ __forceinline__ uint32_t zero_bytes(uint32_t x) {
+  const uint32_t t = (x & 0x7F7F7F7Fu) + 0x7F7F7F7Fu;
+  return ~(t | x | 0x7F7F7F7Fu);
+}
+
+// True if any position turned from decoded to live (decoded at the previous
+// iteration, now live or not decoded), over this thread's share of the
+// positions: thread `part` of `parts` takes 4-position words part, part +
+// parts, ... (the caller ORs the answers of all its threads). The flags are
+// read four at a time, with no branch between the loads.
+__device__ __forceinline__ bool any_anomaly(const Dims &d, const uint8_t *__restrict__ live,
+                                            const uint8_t *__restrict__ decoded,
+                                            const uint8_t *__restrict__ prev_old, int part, int parts) {
+  const bool vec = ((reinterpret_cast<uintptr_t>(live) | reinterpret_cast<uintptr_t>(decoded) |
+                     reinterpret_cast<uintptr_t>(prev_old)) & 3u) == 0;
+  const int n4 = vec ? d.n_pos / 4 : 0;
+  uint32_t any = 0;
+  const uint32_t *l4 = reinterpret_cast<const uint32_t *>(live);
+  const uint32_t *d4 = reinterpret_cast<const uint32_t *>(decoded);
+  const uint32_t *p4 = reinterpret_cast<const uint32_t *>(prev_old);
+#pragma unroll 4
+  for (int q = part; q < n4; q += parts) {
+    const uint32_t lv = l4[q], dc = d4[q], pv = p4[q];
+    any |= ((~zero_bytes(lv)) | zero_bytes(dc)) & ~zero_bytes(pv) & 0x80808080u;
+  }
+  for (int t = 4 * n4 + part; t < d.n_pos; t += parts)
+    any |= static_cast<uint32_t>((live[t] != 0) | (decoded[t] == 0)) & static_cast<uint32_t>(prev_old[t] != 0);
+  return any != 0;
+}
+
+// Records position t's code and this iteration's state: its stamp (this
+// iteration if fresh, else the previous one) and decoded flag.
+__device__ __forceinline__ void record_position(const Dims &d, const Work &ws, int t, int code, int32_t stamp) {
+  const int wr = (d.state_rd & 1) ^ 1;
+  ws.cat[t] = static_cast<uint8_t>(code);
+  ws.stamp[static_cast<size_t>(wr) * d.Nmax + t] = stamp;
+  ws.prev_dec[static_cast<size_t>(wr) * d.Nmax + t] = (code & kCodeLive) ? 0 : 1;
+}
+
+// Classification of position t by one thread: writes its code and this
+// iteration's state and returns whether t is fresh.
+__device__ __forceinline__ bool classify_and_update(const Dims &d, const Work &ws, const uint8_t *__restrict__ live,
+                                                    const uint8_t *__restrict__ decoded, int t, bool force) {
+  const int rd = d.state_rd & 1;
+  const int32_t st = ws.stamp[static_cast<size_t>(rd) * d.Nmax + t];
+  const int code = classify_code(d, live[t] != 0, decoded[t] != 0, ws.prev_dec[static_cast<size_t>(rd) * d.Nmax + t] != 0, st);
+  const bool fresh = force || (code & 15) != C_REUSE;
+  record_position(d, ws, t, code, fresh ? d.iter : st);
+  return fresh;
+}
+
+// Top-k of fresh position t by one warp over the eligible experts (every
+// expert when `force`, else the support mask), ordered by logit desc, lower id
+// first; weights = softmax over the k selected logits, summed in selection
+// order. Lane l holds the logits v of experts [l*EPL, l*EPL + EPL). Writes
+// sel/selw of t and sets bit t of the selected experts' words in `words`.
+template <int EPL>
+__device__ __forceinline__ void select_position(const Dims &d, const Work &ws, int t, float (&v)[EPL],
+                                                const uint8_t *support_mask, bool force, uint32_t *words) {
+  const int lane = lane_id(), e0 = lane * EPL, k = d.k;
+  bool ok[EPL];
+#pragma unroll
+  for (int c = 0; c < EPL; ++c) {
+    const int e = e0 + c;
+    ok[c] = e < d.E && (force || support_mask[e] != 0);
+  }
+  int sel;
+  float val;
+  warp_topk<EPL>(v, ok, k, &sel, &val);
+  const float top = __shfl_sync(0xffffffffu, val, 0);
+  const float ex = lane < k ? expf(val - top) : 0.f;
+  float denom = 0.f;
+  for (int j = 0; j < k; ++j) denom += __shfl_sync(0xffffffffu, ex, j);
+  if (lane < k) {
+    if (sel < 0 || sel >= d.E) {
+      set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+    } else {
+      ws.sel[static_cast<size_t>(t) * k + lane] = sel;
+      ws.selw[static_cast<size_t>(t) * k + lane] = ex / denom;
+      atomicOr(&words[static_cast<size_t>(sel) * d.cmax + (t >> 5)], 1u << (t & 31));
+    }
+  }
+}
+
+// Selection words this iteration writes (the other half is cleared for the next one).
+__device__ __forceinline__ uint32_t *words_written(const Dims &d, const Work &ws) {
+  return ws.sel_words + static_cast<size_t>((d.state_rd & 1) ^ 1) * d.E * d.cmax;
+}
+
+}  // namespace epoch

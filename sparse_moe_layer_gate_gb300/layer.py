@@ -124,10 +124,11 @@ class EpochLayer:
         B.check(B.lib().epoch_set_tracing(self.handle, 1 if on else 0), "epoch_set_tracing")
 
     def read_trace(self, stream=None) -> np.ndarray:
-        """[4, 1024, 8] int64 per-CTA trace rows: gate, experts, expert epilogue, routing."""
+        """[7, 1024, 8] int64 per-CTA trace rows: gate, experts, expert epilogue,
+        worklist kernel, gate epilogue steps, worklist kernel steps, expert waits."""
         v = B.epoch_debug_view()
         B.check(B.lib().epoch_debug_pointers(self.handle, C.byref(v)), "epoch_debug_pointers")
-        return self._copy(v.trace, 4 * 1024 * 8, np.int64, stream).reshape(4, 1024, 8)
+        return self._copy(v.trace, 7 * 1024 * 8, np.int64, stream).reshape(7, 1024, 8)
 
     def read_timeline(self, stream=None) -> dict:
         """{kernel: (first entry ns, last exit ns)} of the last traced iteration."""
@@ -179,12 +180,15 @@ class EpochLayer:
             d["support_ids"] = self._copy(v.support_ids, E, np.int32, stream)
             d["plan_counts"] = self._copy(v.plan_counts, E, np.int32, stream)
         if "iter" in parts:
-            d["fresh_pos"] = self._copy(v.fresh_pos, nf, np.int32, stream)
-            d["sel"] = self._copy(v.sel, nf * k, np.int32, stream).reshape(nf, k)
-            d["sel_w"] = self._copy(v.sel_w, nf * k, np.float32, stream).reshape(nf, k)
+            # selections, weights and slots are stored per position; rows of the
+            # fresh positions, in fresh-list order
+            fp = self._copy(v.fresh_pos, nf, np.int32, stream)
+            d["fresh_pos"] = fp
+            d["sel"] = self._copy(v.sel, n_pos * k, np.int32, stream).reshape(n_pos, k)[fp]
+            d["sel_w"] = self._copy(v.sel_w, n_pos * k, np.float32, stream).reshape(n_pos, k)[fp]
             d["offsets"] = self._copy(v.offsets, E + 1, np.int32, stream)
             d["wl_pos"] = self._copy(v.wl_pos, ne, np.int32, stream)
-            d["slot"] = self._copy(v.slot, nf * k, np.int32, stream).reshape(nf, k)
+            d["slot"] = self._copy(v.slot, n_pos * k, np.int32, stream).reshape(n_pos, k)[fp]
             d["stamp"] = self._copy(v.stamp, n_pos, np.int32, stream)
         if "logits" in parts:
             d["logits"] = self._copy(v.logits, N * E, np.float32, stream).reshape(N, E)[:n_pos]
