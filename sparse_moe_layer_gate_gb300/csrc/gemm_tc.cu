@@ -96,8 +96,14 @@ struct __align__(128) GateParams {
 __host__ __device__ inline int gate_e_pad(int E) { return ((E + 127) / 128) * 128; }
 __host__ __device__ inline int gate_stage_bytes(int E, int TN) { return (gate_e_pad(E) / 128) * kTileBytes + TN * 64 * 2; }
 
+// 12 warps: 0 issues the TMA loads, 1 the MMAs, 4-7 read TMEM; all of them
+// reduce, and each takes the top-k of one of the CTA's positions (up to 12).
+constexpr int kGateThreads = 384;
+
+// At most 104 registers a thread, so that a CTA of the row-permute kernel
+// (launched while the gate runs) still fits beside a gate CTA.
 template <int EPL>
-__global__ void __launch_bounds__(256, 1) k_tc_gate(const __grid_constant__ GateParams p) {
+__global__ void __maxnreg__(104) k_tc_gate(const __grid_constant__ GateParams p) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base (the 128-byte swizzle pattern repeats every 1024 bytes)
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -222,10 +228,10 @@ __global__ void __launch_bounds__(256, 1) k_tc_gate(const __grid_constant__ Gate
     }
     __syncwarp();
   } else {
-    // ---------------- warps 2-7, while the operands stream: the support mask,
+    // ---------------- warps 2-11, while the operands stream: the support mask,
     // and the decoded -> live scan (any anomaly anywhere makes every position
     // fresh with every expert eligible)
-    for (int e = tid - 64; e < E_pad; e += 192) {
+    for (int e = tid - 64; e < E_pad; e += kGateThreads - 64) {
       s_support[e] = e < d.E ? ws.support_mask[e] : 0;
       s_bias[e] = e < d.E ? __ldg(p.bias + e) : 0.f;
     }
@@ -239,11 +245,12 @@ __global__ void __launch_bounds__(256, 1) k_tc_gate(const __grid_constant__ Gate
         s_code[j] = classify_code(d, p.live[t] != 0, p.decoded[t] != 0,
                                   ws.prev_dec[static_cast<size_t>(rd) * d.Nmax + t] != 0, st);
       }
-      if (any_anomaly(d, p.live, p.decoded, ws.prev_dec + static_cast<size_t>(rd) * d.Nmax, tid - 64, 192))
+      if (any_anomaly(d, p.live, p.decoded, ws.prev_dec + static_cast<size_t>(rd) * d.Nmax, tid - 64,
+                      kGateThreads - 64))
         atomicOr(s_anom, 1);
     }
   }
-  if (wid >= 4) {
+  if (wid >= 4 && wid < 8) {
     // ---------------- warps 4-7: TMEM -> fp32 partials [position][expert] in shared memory
     if (mbar_wait_bounded(done_bar, 0, abort_flag, ws.err, tmo)) {
       tc_fence_after();
@@ -282,7 +289,7 @@ __global__ void __launch_bounds__(256, 1) k_tc_gate(const __grid_constant__ Gate
   // units of 4 experts x 1 position, kGateBatch per thread at a time: every
   // rank's partials of a batch are requested before any is summed (one round
   // trip over the cluster per batch)
-  constexpr int kGateBatch = 3;
+  constexpr int kGateBatch = 2;
   const int n_units = TPC * e4n;
   for (int u0 = tid; u0 < n_units; u0 += kGateBatch * blockDim.x) {
     float4 v[kGateBatch][8];
@@ -333,7 +340,7 @@ __global__ void __launch_bounds__(256, 1) k_tc_gate(const __grid_constant__ Gate
     // ---------------- classification and top-k of the positions this CTA owns
     const bool force = d.host_fallback != 0 || *s_anom != 0;
     uint32_t *words = words_written(d, ws);
-    for (int j = wid; j < TPC; j += 8) {
+    for (int j = wid; j < TPC; j += kGateThreads / 32) {
       const int t = t_own + j;
       if (t >= d.n_pos) continue;
       const int code = s_code[j];
@@ -386,6 +393,13 @@ constexpr int kExpOffOffs = kExpOffPref + 4 * kExpGroups;         // int32 [kExp
 constexpr int kExpSmem = 1024 + kExpOffOffs + 4 * kExpGroups;
 static_assert(kExpSmem <= 227 * 1024, "shared memory");
 static_assert(kTnUp == kTnDn, "up and down tiles share the token tiling");
+
+// The shared experts' up tiles need no routing: with kSharedUpEarly the expert
+// kernel runs them while the gate and worklist kernels still run (phase A);
+// otherwise they lead the tile list that follows the worklist (measured
+// slightly faster on the LLaDA2.0-mini-shaped layer: CTAs that took shared
+// tiles early were late for the routed ones).
+constexpr bool kSharedUpEarly = false;
 
 // Decoded tile as handed through the ring: x = group | kDownBit for a down
 // tile (-1 ends the stream), y = row block, z = first token row, w = valid rows.
@@ -681,7 +695,7 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
       tma_prefetch_desc(&p.bs);
       tma_prefetch_desc(&p.bs2);
       // phase A: the shared experts' up tiles (they read x; no routing needed)
-      while (ok) {
+      while (ok && kSharedUpEarly) {
         const int q = atomicAdd(shc, 1);
         if (q >= n_sh_up) break;
         int need, tt;
@@ -705,34 +719,46 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
       if (trace) trace[2] = static_cast<int64_t>(globaltimer_ns());
       tma_prefetch_desc(&p.b[0]);
       tma_prefetch_desc(&p.b2[0]);
-      // tile list of this phase: routed up tiles, the shared experts' down
-      // tiles (their up tiles ran in phase A), routed down tiles
+      // tile list of this phase, in segments: [the shared experts' up tiles,
+      // unless phase A ran them], routed up tiles, the shared experts' down
+      // tiles, routed down tiles
       const int n_up = ok ? ws.ctrl->tiles_up : 0;
-      const int total = ok ? n_up + n_sh_dn + ws.ctrl->tiles_dn : 0;
+      const int sh_up_here = kSharedUpEarly ? 0 : n_sh_up;
+      const int seg_end[4] = {sh_up_here, sh_up_here + n_up, sh_up_here + n_up + n_sh_dn,
+                              sh_up_here + n_up + n_sh_dn + (ok ? ws.ctrl->tiles_dn : 0)};
+      const int total = ok ? seg_end[3] : 0;
       const int L = s_offs[d.E];
       const int copied = L * p.vec_per_row;  // vectors the permute kernel copies into xp
       while (ok) {
         const int tile = atomicAdd(ws.tile_ctr, 1);
         if (tile >= total) break;
+        const int seg = tile < seg_end[0] ? 0 : tile < seg_end[1] ? 1 : tile < seg_end[2] ? 2 : 3;
         int4 td;
-        int need = 0;
-        const int32_t *flag;
-        if (tile >= n_up && tile < n_up + n_sh_dn) {
+        int need = 0, kind = 0;
+        const int32_t *flag = nullptr;
+        if (seg == 0 || seg == 2) {  // shared experts: up tiles first, then down tiles
           int tt;
-          td = shared_tile(d, n_sh_up + tile - n_up, &need, &tt);
-          flag = shc + 1 + ((td.x & (kDownBit - 1)) - d.E) * nt_max + tt;
+          td = shared_tile(d, seg == 0 ? tile : n_sh_up + tile - seg_end[1], &need, &tt);
+          if (seg == 2) {
+            flag = shc + 1 + ((td.x & (kDownBit - 1)) - d.E) * nt_max + tt;
+            kind = 2;
+          }
         } else {
-          if (!locate(d, s_list, s_offs, tile < n_up ? tile : tile - n_sh_dn, n_up, &td, &need)) {
+          const int q = seg == 1 ? tile - seg_end[0] : n_up + tile - seg_end[2];
+          if (!locate(d, s_list, s_offs, q, n_up, &td, &need)) {
             set_error(ws.err, EPOCH_DEVERR_BOUNDS);
             *abort_flag = 1;
             ok = false;
             break;
           }
-          const bool down = (td.x & kDownBit) != 0;
-          flag = down ? ws.done_up + (td.x & (kDownBit - 1)) : ws.tile_ctr + 2;
-          if (!down) need = copied;
+          if (seg == 1) {
+            flag = ws.tile_ctr + 2;
+            need = copied;
+          } else {
+            flag = ws.done_up + (td.x & (kDownBit - 1));
+            kind = 1;
+          }
         }
-        const int kind = tile >= n_up && tile < n_up + n_sh_dn ? 2 : tile < n_up ? 0 : 1;
         ok = post(td) && issue(td, flag, need, kind);
       }
       if (ok) ok = post(make_int4(-1, 0, 0, 0));  // end of the stream
@@ -1083,7 +1109,7 @@ static int gate_max_clusters(const Dims &d, int cs) {
   attr.val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cs);
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(kGateThreads);
   cfg.dynamicSmemBytes = 160 * 1024;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
@@ -1139,7 +1165,7 @@ cudaError_t launch_gate_tc(const Dims &d, const Maps &m, const Work &ws, const v
   const void *fn = gate_fn(d);
   const int tiles = (d.n_pos + g.tn - 1) / g.tn;
   void *args[] = {&p};
-  return launch_kernel(fn, dim3(tiles * g.cs), dim3(256), g.smem, s, args, false, g.cs);
+  return launch_kernel(fn, dim3(tiles * g.cs), dim3(kGateThreads), g.smem, s, args, false, g.cs);
 }
 
 cudaError_t launch_experts_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map_up,
