@@ -638,29 +638,59 @@ __device__ __forceinline__ void store8(__nv_bfloat16 *p, const float (&v)[8]) {
 // ([W] section "Liveness-Shard Parallelism": Y[F_i] = Y_F); reused t: r = the
 // cached row (Y[not F_i] = C_l[not F_i]). Then y = r + shared outputs (+ x when
 // residual), rounded once: the dense shard is restored at the layer boundary.
+// Two dependent rounds of loads: the fresh index, slots, weights, cached row,
+// shared outputs and x together (selections are stored per position), then the
+// k expert-output rows of a fresh position.
 template <typename T>
 __global__ void __launch_bounds__(128) k_combine(Dims d, Work ws, const T *__restrict__ x, T *__restrict__ y) {
   const KernelMark mark_(d, ws, K_COMBINE);
   pdl_wait();
   const int t = blockIdx.x;
   if (t >= d.n_pos) return;
-  const int f = ws.fidx[t];
   const int H = d.H, k = d.k;
+  constexpr int kPasses = 4;  // rows up to 4 * 128 * 8 elements stay in registers
   T *cache = reinterpret_cast<T *>(ws.cache) + static_cast<size_t>(t) * H;
   __shared__ int32_t slot_s[16];
   __shared__ float w_s[16];
-  if (f >= 0 && threadIdx.x < k) {
-    int sl = ws.slot[static_cast<size_t>(t) * k + threadIdx.x];
-    if (sl < 0 || sl >= d.Nmax * k) {
-      set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-      sl = 0;
-    }
-    slot_s[threadIdx.x] = sl;
+  __shared__ int f_s;
+  if (threadIdx.x < k) {
+    slot_s[threadIdx.x] = ws.slot[static_cast<size_t>(t) * k + threadIdx.x];
     w_s[threadIdx.x] = ws.selw[static_cast<size_t>(t) * k + threadIdx.x];
   }
+  if (threadIdx.x == 0) f_s = ws.fidx[t];
+  // first round, independent of the slots: cached row, shared outputs, x
+  float base[kPasses][8];
+#pragma unroll
+  for (int pass = 0; pass < kPasses; ++pass) {
+    const int h0 = (pass * blockDim.x + threadIdx.x) * 8;
+    if (h0 >= H) break;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) base[pass][q] = 0.f;
+    for (int s = 0; s < d.n_sh; ++s) {
+      float o[8];
+      load8(static_cast<const T *>(ws.o_sh) + (static_cast<size_t>(s) * d.Nmax + t) * H + h0, o);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) base[pass][q] += o[q];
+    }
+    if (d.residual) {
+      float xv[8];
+      load8(x + static_cast<size_t>(t) * H + h0, xv);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) base[pass][q] += xv[q];
+    }
+  }
   __syncthreads();
-  for (int h0 = threadIdx.x * 8; h0 < H; h0 += blockDim.x * 8) {
-    float r[8];
+  const int f = f_s;
+  for (int j = threadIdx.x; f >= 0 && j < k; j += blockDim.x) {
+    if (slot_s[j] < 0 || slot_s[j] >= d.Nmax * k) {
+      set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+      slot_s[j] = 0;
+    }
+  }
+  __syncthreads();
+  // routed part of one 8-element run at h0: the weighted expert outputs of a
+  // fresh position (refilling its cache row), else its cached row
+  auto routed8 = [&](int h0, float (&r)[8]) {
     if (f >= 0) {
 #pragma unroll
       for (int q = 0; q < 8; ++q) r[q] = 0.f;
@@ -675,6 +705,21 @@ __global__ void __launch_bounds__(128) k_combine(Dims d, Work ws, const T *__res
     } else {
       load8(cache + h0, r);
     }
+  };
+#pragma unroll
+  for (int pass = 0; pass < kPasses; ++pass) {
+    const int h0 = (pass * blockDim.x + threadIdx.x) * 8;
+    if (h0 >= H) break;
+    float r[8];
+    routed8(h0, r);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) r[q] += base[pass][q];
+    store8(y + static_cast<size_t>(t) * H + h0, r);
+  }
+  // rows wider than kPasses passes: the rest loaded here
+  for (int h0 = (kPasses * blockDim.x + threadIdx.x) * 8; h0 < H; h0 += blockDim.x * 8) {
+    float r[8];
+    routed8(h0, r);
     for (int s = 0; s < d.n_sh; ++s) {
       float o[8];
       load8(static_cast<const T *>(ws.o_sh) + (static_cast<size_t>(s) * d.Nmax + t) * H + h0, o);
