@@ -55,6 +55,40 @@ __device__ __forceinline__ int block_excl_scan(int v, int *warp_tmp, int *total)
   return r;
 }
 
+// Exclusive scan of four values at once over a CTA of up to 1024 threads
+// (independent components, one pass); *total gets the sums.
+__device__ __forceinline__ int4 block_excl_scan4(int4 v, int4 *warp_tmp, int4 *total) {
+  const int lane = lane_id(), wid = warp_id(), nw = (blockDim.x + 31) >> 5;
+  auto scan = [&](int4 a) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int ux = __shfl_up_sync(0xffffffffu, a.x, o), uy = __shfl_up_sync(0xffffffffu, a.y, o);
+      const int uz = __shfl_up_sync(0xffffffffu, a.z, o), uw = __shfl_up_sync(0xffffffffu, a.w, o);
+      if (lane >= o) {
+        a.x += ux;
+        a.y += uy;
+        a.z += uz;
+        a.w += uw;
+      }
+    }
+    return a;
+  };
+  const int4 incl = scan(v);
+  if (lane == 31) warp_tmp[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int4 x = lane < nw ? warp_tmp[lane] : make_int4(0, 0, 0, 0);
+    const int4 xi = scan(x);
+    warp_tmp[lane] = make_int4(xi.x - x.x, xi.y - x.y, xi.z - x.z, xi.w - x.w);
+    if (lane == 31) warp_tmp[32] = xi;
+  }
+  __syncthreads();
+  const int4 b = warp_tmp[wid];
+  *total = warp_tmp[32];
+  __syncthreads();
+  return make_int4(b.x + incl.x - v.x, b.y + incl.y - v.y, b.z + incl.z - v.z, b.w + incl.w - v.w);
+}
+
 // ---------------------------------------------------------------- gate (SIMT)
 // G = x W_r^T + b for fp32 layers: one warp per (position, expert), lanes
 // split H, fixed-order reduction (deterministic).
@@ -181,89 +215,6 @@ __global__ void __launch_bounds__(256) k_select(Dims d, Work ws, const uint8_t *
 }
 
 // ---------------------------------------------------------------- worklist
-// Tile bookkeeping of the expert kernel for the routed experts (the shared
-// experts' tiles need no routing and are enumerated by the expert kernel
-// itself). Groups are listed widest first, so that the expert kernel, which
-// hands tiles out in list order, ends on narrow tiles whose epilogues are
-// short: routed experts with >= 96 rows, >= 32 rows, fewer (an expert with no
-// row holds no tile and its weights are never read), by id within a class
-// (stable counting sort; per-class counts packed two to an int, two block
-// scans). grp_list[p] = (token tiles of the groups before p) << kGrpIdBits |
-// expert of p, grp_list[E] = all token tiles << kGrpIdBits. Thread tid handles
-// experts [tid * gpt, tid * gpt + gpt).
-__device__ void write_group_tiles(const Dims &d, const Work &ws, const int32_t *s_off, int32_t *tmp,
-                                  int32_t *s_list) {
-  const int tid = threadIdx.x, E = d.E;
-  constexpr int kMaxGpt = 4;  // E <= 1024 with >= 256 threads
-  const int gpt = (E + blockDim.x - 1) / blockDim.x;
-  const int g0 = tid * gpt;
-  int cls[kMaxGpt], nt[kMaxGpt];
-  int pk0 = 0, pk1 = 0, hit = 0;  // class counts: 0, 1 in pk0, 2 in pk1 (16-bit fields)
-#pragma unroll
-  for (int h = 0; h < kMaxGpt; ++h) {
-    const int g = g0 + h;
-    cls[h] = -1;
-    nt[h] = 0;
-    if (h < gpt && g < E) {
-      const int rows = s_off[g + 1] - s_off[g];
-      nt[h] = d.tn > 0 ? (rows + d.tn - 1) / d.tn : 0;
-      hit += rows > 0;
-      const int c = rows >= 96 ? 2 : rows >= 32 ? 1 : 0;
-      cls[h] = c;
-      if (c < 2) pk0 += 1 << (16 * c);
-      else pk1 += 1;
-    }
-  }
-  int tot0, tot1, n_hit;
-  const int ex0 = block_excl_scan(pk0, tmp, &tot0);
-  const int ex1 = block_excl_scan(pk1, tmp, &tot1);
-  (void)block_excl_scan(hit, tmp, &n_hit);
-  const int count2 = tot1 & 0xffff, count1 = (tot0 >> 16) & 0xffff;
-  int run[3] = {ex0 & 0xffff, (ex0 >> 16) & 0xffff, ex1 & 0xffff};
-#pragma unroll
-  for (int h = 0; h < kMaxGpt; ++h) {
-    const int c = cls[h];
-    if (c < 0) continue;
-    const int base = c == 2 ? 0 : c == 1 ? count2 : count2 + count1;
-    s_list[base + run[c]++] = (nt[h] << kGrpIdBits) | (g0 + h);  // token tiles until the prefix below
-  }
-  __syncthreads();  // the list in sorted order is visible to the whole CTA
-  int v[kMaxGpt], sum = 0;
-#pragma unroll
-  for (int h = 0; h < kMaxGpt; ++h) {
-    const int p = g0 + h;
-    v[h] = h < gpt && p < E ? s_list[p] : 0;
-    sum += v[h] >> kGrpIdBits;
-  }
-  int total;
-  int before = block_excl_scan(sum, tmp, &total);
-  if (total >= (1 << (31 - kGrpIdBits))) {
-    if (tid == 0) set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-    total = 0;
-    before = 0;
-  }
-#pragma unroll
-  for (int h = 0; h < kMaxGpt; ++h) {
-    const int p = g0 + h;
-    if (h < gpt && p < E) {
-      ws.grp_list[p] = (before << kGrpIdBits) | (v[h] & ((1 << kGrpIdBits) - 1));
-      before += v[h] >> kGrpIdBits;
-    }
-  }
-  if (tid == 0) {
-    ws.grp_list[E] = total << kGrpIdBits;
-    const int up = d.tn > 0 ? (d.I / 128) * total : 0;
-    const int dn = d.tn > 0 ? (d.H / kBmDn) * total : 0;
-    const int nt_sh = d.tn > 0 ? d.n_sh * ((d.n_pos + d.tn - 1) / d.tn) : 0;
-    ws.ctrl->n_hit = n_hit;
-    ws.ctrl->tiles_up = up;
-    ws.ctrl->tiles_dn = dn;
-    ws.stats->n_hit_experts = n_hit;
-    ws.stats->tiles_up = up + (d.I_s / 128) * nt_sh;
-    ws.stats->tiles_down = dn + (d.H / kBmDn) * nt_sh;
-  }
-}
-
 // One CTA builds the iteration's worklist from the selection words the gate
 // (or select) kernel set ([W] section "FreshLane Dispatch": pack, count
 // exchange -> offsets, compact dispatch -- here the count exchange is a
@@ -284,11 +235,12 @@ __device__ void write_group_tiles(const Dims &d, const Work &ws, const int32_t *
 //    the next iteration.
 constexpr int kRouteSmemWords = 12 * 1024;  // candidate words (and prefixes) kept in shared memory
 
-__global__ void __launch_bounds__(kRouteThreads) k_route(Dims d, Work ws) {
+__global__ void __launch_bounds__(kRouteThreads, 1) k_route(Dims d, Work ws) {
   const KernelMark mark_(d, ws, K_ROUTING);
   pdl_trigger();  // the expert kernel may start its launch; it waits on route_done for routed tiles
   extern __shared__ uint32_t s_dyn[];
   __shared__ int32_t tmp[33];
+  __shared__ int4 tmp4[33];
   __shared__ int32_t s_off[1025];
   __shared__ int16_t s_cand[1024];  // candidate experts (support ranking, or every expert)
   __shared__ int16_t s_cidx[1024];  // candidate index of an expert, -1 if none
@@ -392,31 +344,66 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(Dims d, Work ws) {
   __syncthreads();
   if (trace && tid == 0) trace[2] = static_cast<int64_t>(globaltimer_ns());
 
-  // ---- 2: offsets (thread tid scans experts [tid * gpt, tid * gpt + gpt)), group list, counters
-  int n_edges;
+  // ---- 2: one scan over the experts in id order (thread tid owns [tid * gpt,
+  // tid * gpt + gpt)) gives the expert offsets and, per row-count class of the
+  // group list (2: >= 96 rows, 1: >= 32, 0: fewer; listed in that order, by id
+  // within a class), the list positions and token-tile prefixes: .x rows,
+  // .y experts of class 0 | class 1 << 16, .z experts of class 2 | its tiles
+  // << 16, .w tiles of class 0 | class 1 << 16.
+  int n_edges, n_tiles;
   {
     const int gpt = (E + kRouteThreads - 1) / kRouteThreads;
     const int g0 = tid * gpt;
-    int c[4] = {0, 0, 0, 0}, sum = 0;
+    auto cls_of = [](int r) { return r >= 96 ? 2 : r >= 32 ? 1 : 0; };
+    int c[4] = {0, 0, 0, 0};
+    int4 v = make_int4(0, 0, 0, 0);
 #pragma unroll
     for (int h = 0; h < 4; ++h)
       if (h < gpt && g0 + h < E) {
-        c[h] = s_off[g0 + h];
-        sum += c[h];
+        const int r = s_off[g0 + h], k2 = cls_of(r), nt = d.tn > 0 ? (r + d.tn - 1) / d.tn : 0;
+        c[h] = r;
+        v.x += r;
+        if (k2 == 0) {
+          v.y += 1;
+          v.w += nt;
+        } else if (k2 == 1) {
+          v.y += 1 << 16;
+          v.w += nt << 16;
+        } else {
+          v.z += 1 | (nt << 16);
+        }
       }
-    int before = block_excl_scan(sum, tmp, &n_edges);
+    int4 tot;
+    const int4 ex = block_excl_scan4(v, reinterpret_cast<int4 *>(tmp4), &tot);
+    const int n2 = tot.z & 0xffff, n1 = tot.y >> 16;
+    const int t2 = tot.z >> 16, t1 = tot.w >> 16, t0 = tot.w & 0xffff;
+    const int pos_base[3] = {n2 + n1, n2, 0};
+    const int tile_base[3] = {t2 + t1, t2, 0};
+    int rank[3] = {ex.y & 0xffff, ex.y >> 16, ex.z & 0xffff};
+    int tb[3] = {ex.w & 0xffff, ex.w >> 16, ex.z >> 16};
+    int before = ex.x;
+    n_edges = tot.x;
+    n_tiles = t0 + t1 + t2;
 #pragma unroll
     for (int h = 0; h < 4; ++h)
       if (h < gpt && g0 + h < E) {
-        s_off[g0 + h] = before;
-        before += c[h];
+        const int e = g0 + h, r = c[h], k2 = cls_of(r), nt = d.tn > 0 ? (r + d.tn - 1) / d.tn : 0;
+        s_off[e] = before;
+        ws.offsets[e] = before;
+        before += r;
+        ws.grp_list[pos_base[k2] + rank[k2]++] = ((tile_base[k2] + tb[k2]) << kGrpIdBits) | e;
+        tb[k2] += nt;
       }
-    if (tid == 0) s_off[E] = n_edges;
+    if (tid == 0) {
+      s_off[E] = n_edges;
+      ws.offsets[E] = n_edges;
+      ws.grp_list[E] = n_tiles << kGrpIdBits;
+      ws.ctrl->tiles_up = d.tn > 0 ? (d.I / 128) * n_tiles : 0;
+      ws.ctrl->tiles_dn = d.tn > 0 ? (d.H / kBmDn) * n_tiles : 0;
+    }
   }
   __syncthreads();
-  for (int e = tid; e <= E; e += kRouteThreads) ws.offsets[e] = s_off[e];
   if (trace2 && tid == 0) trace2[1] = static_cast<int64_t>(globaltimer_ns());
-  write_group_tiles(d, ws, s_off, tmp, reinterpret_cast<int32_t *>(s_dyn + 2 * kRouteSmemWords));
   for (int g = tid; g < E; g += kRouteThreads) ws.done_up[g] = 0;
   if (tid == 0) {
     ws.tile_ctr[0] = 0;  // routed tiles drawn
@@ -499,8 +486,18 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(Dims d, Work ws) {
     for (int q = 0; q < 5; ++q) atomicAdd(&s_cat[q], cnt[q]);
     atomicAdd(&s_cat[5], bad);
   }
+  // experts with at least one row (statistics)
+  int hit = 0;
+  for (int e = tid; e < E; e += kRouteThreads) hit += s_off[e + 1] > s_off[e];
+  hit = __reduce_add_sync(0xffffffffu, hit);
+  if (lane == 0) atomicAdd(&s_cat[6], hit);
   __syncthreads();
   if (tid == 0) {
+    const int nt_sh = d.tn > 0 ? d.n_sh * ((n + d.tn - 1) / d.tn) : 0;
+    ws.ctrl->n_hit = s_cat[6];
+    ws.stats->n_hit_experts = s_cat[6];
+    ws.stats->tiles_up = (d.tn > 0 ? (d.I / 128) * n_tiles : 0) + (d.I_s / 128) * nt_sh;
+    ws.stats->tiles_down = (d.tn > 0 ? (d.H / kBmDn) * n_tiles : 0) + (d.H / kBmDn) * nt_sh;
     const int fb = (d.host_fallback ? 1 : 0) | (s_anom ? 2 : 0);
     if (n_fresh * k != n_edges) set_error(ws.err, EPOCH_DEVERR_BOUNDS);
     ws.ctrl->n_fresh = n_fresh;
