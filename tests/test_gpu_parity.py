@@ -71,6 +71,21 @@ def test_sweep_largest_batch_first_iterations():
     assert_clean(block_parity(synth.sweep_workload(64, 0.95, 4), n_iters=3))
 
 
+def test_every_expert_eligible_at_2048_positions():
+    """tau = 1 keeps all 256 experts: the candidates' selection words (256 x 64)
+    exceed the worklist kernel's shared-memory staging, which then reads them
+    from global memory."""
+    assert_clean(block_parity(synth.sweep_workload(64, 1.0, 4), n_iters=2))
+
+
+def test_wide_router_320_experts():
+    """E = 320 > 256: the gate's wider per-lane top-k and larger partial-sum
+    tiles (three 128-expert MMA blocks per tile)."""
+    wl = TINY_BF16.replace(name="tiny_bf16_e320", wid=7, iid=7, n_experts=320, top_k=4, tau=0.8, iters=4,
+                           description="tiny bf16 layer with 320 routed experts, top-4")
+    assert_clean(block_parity(wl))
+
+
 def test_tau1_R1_is_dense_moe():
     """tau = 1 and R = 1: every position fresh with every expert eligible, so the
     layer equals the dense MoE formula at every iteration."""
