@@ -156,6 +156,12 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 // Cluster-wide barrier in two halves; every thread of every CTA of the cluster
 // arrives once per phase (convergent warps: .aligned).
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+// Arrival without release semantics: for a CTA whose only obligation is that
+// its reads of other CTAs' shared memory have completed (their values are
+// already in registers), so it need not wait for its own global stores.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {

@@ -128,6 +128,7 @@ __global__ void __maxnreg__(104) k_tc_gate(const __grid_constant__ GateParams p)
   int *s_anom = reinterpret_cast<int *>(tmem_slot + 2);
   int *s_code = reinterpret_cast<int *>(tmem_slot + 4);  // [TPC] classification codes of the own positions
   int *s_stamp = s_code + 64;                             // [TPC] their previous stamps
+  uint2 *s_scr = reinterpret_cast<uint2 *>(s_stamp + 64);  // [warps][32] top-k scratch
 
   const KernelMark mark_(d, ws, K_GATE);
   pdl_wait();
@@ -333,7 +334,7 @@ __global__ void __maxnreg__(104) k_tc_gate(const __grid_constant__ GateParams p)
       }
     }
   }
-  cluster_arrive();  // this CTA has read the other CTAs' partials
+  cluster_arrive_relaxed();  // this CTA's reads of the other CTAs' partials are complete
   __syncthreads();   // rows[] complete
   if (trace2 && tid == 0) trace2[2] = static_cast<int64_t>(globaltimer_ns());
   if (!d.plan_mode) {
@@ -353,7 +354,7 @@ __global__ void __maxnreg__(104) k_tc_gate(const __grid_constant__ GateParams p)
         const int e = lane * EPL + c;
         v[c] = e < E_pad ? rows[j * E_pad + e] : -INFINITY;
       }
-      select_position<EPL>(d, ws, t, v, s_support, force, words);
+      select_position<EPL>(d, ws, t, v, s_support, force, words, s_scr + 32 * wid);
     }
   }
   if (trace && tid == 0) {
@@ -1061,7 +1062,8 @@ static GateGeom gate_geom_for(const Dims &d, int tn) {
   const int partial = tn * e_pad * 4;
   g.region0 = g.stages * stage > partial ? g.stages * stage : partial;
   const int rows = (tn / g.cs) * e_pad * 4;
-  g.smem = 1024 + g.region0 + rows + e_pad * 4 + 1024 + (2 * g.stages + 1) * 8 + 16 + 2 * 64 * 4;
+  g.smem = 1024 + g.region0 + rows + e_pad * 4 + 1024 + (2 * g.stages + 1) * 8 + 16 + 2 * 64 * 4 +
+           (kGateThreads / 32) * 32 * 8;
   const int cols = (e_pad / BM - 1) * tn + ((tn + 31) / 32) * 32;
   g.tcols = cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512;
   if (cols > 512) g.smem = kGateSmemCap + 1;  // does not fit: rejected by the caller

@@ -53,6 +53,7 @@ static int32_t *counts_address(int device, cudaError_t *err) {
 // Dense top-k of every position over all E experts; one warp per position.
 template <int EPL>
 __global__ void k_noalloc_topk(const float *__restrict__ logits, int n_pos, int E, int k, int32_t *counts) {
+  __shared__ uint2 s_scr[8][32];  // top-k scratch of each warp (256 threads)
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int lane = lane_id();
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n_pos; t += warps) {
@@ -63,7 +64,7 @@ __global__ void k_noalloc_topk(const float *__restrict__ logits, int n_pos, int 
     for (int c = 0; c < EPL; ++c) ok[c] = lane * EPL + c < E;
     int sel;
     float val;
-    warp_topk<EPL>(v, ok, k, &sel, &val);
+    warp_topk<EPL>(v, ok, k, &sel, &val, s_scr[warp_id()]);
     if (lane < k) atomicAdd(&counts[sel], 1);
   }
 }

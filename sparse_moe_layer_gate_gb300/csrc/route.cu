@@ -114,6 +114,7 @@ __global__ void k_gate_simt(Dims d, const T *__restrict__ x, const T *__restrict
 // Dense top-k of every position over all experts -> hit counts (integer atomics).
 template <int EPL>
 __global__ void k_plan_topk(Dims d, const float *__restrict__ logits, int32_t *__restrict__ counts) {
+  __shared__ uint2 s_scr[8][32];  // top-k scratch of each warp (256 threads)
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int lane = lane_id();
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < d.n_pos; t += warps) {
@@ -124,7 +125,7 @@ __global__ void k_plan_topk(Dims d, const float *__restrict__ logits, int32_t *_
     for (int c = 0; c < EPL; ++c) ok[c] = lane * EPL + c < d.E;
     int sel;
     float val;
-    warp_topk<EPL>(v, ok, d.k, &sel, &val);
+    warp_topk<EPL>(v, ok, d.k, &sel, &val, s_scr[warp_id()]);
     if (lane < d.k) atomicAdd(&counts[sel], 1);
   }
 }
@@ -196,6 +197,7 @@ template <int EPL>
 __global__ void __launch_bounds__(256) k_select(Dims d, Work ws, const uint8_t *__restrict__ live,
                                                 const uint8_t *__restrict__ decoded) {
   const KernelMark mark_(d, ws, K_SELECT);
+  __shared__ uint2 s_scr[8][32];  // top-k scratch of each warp
   pdl_wait();
   const int rd = d.state_rd & 1;
   const bool anom = __syncthreads_or(
@@ -210,7 +212,7 @@ __global__ void __launch_bounds__(256) k_select(Dims d, Work ws, const uint8_t *
     if (!fresh) continue;
     float v[EPL];
     lane_logits<EPL>(ws.logits + static_cast<size_t>(t) * d.E, d.E, v);
-    select_position<EPL>(d, ws, t, v, ws.support_mask, force, words);
+    select_position<EPL>(d, ws, t, v, ws.support_mask, force, words, s_scr[warp_id()]);
   }
 }
 

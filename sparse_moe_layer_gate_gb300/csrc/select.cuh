@@ -97,11 +97,13 @@ __device__ __forceinline__ bool classify_and_update(const Dims &d, const Work &w
 // Top-k of fresh position t by one warp over the eligible experts (every
 // expert when `force`, else the support mask), ordered by logit desc, lower id
 // first; weights = softmax over the k selected logits, summed in selection
-// order. Lane l holds the logits v of experts [l*EPL, l*EPL + EPL). Writes
-// sel/selw of t and sets bit t of the selected experts' words in `words`.
+// order. Lane l holds the logits v of experts [l*EPL, l*EPL + EPL); `scratch`
+// is the warp's 32 entries of shared memory for the top-k. Writes sel/selw of
+// t and sets bit t of the selected experts' words in `words`.
 template <int EPL>
-__device__ __forceinline__ void select_position(const Dims &d, const Work &ws, int t, float (&v)[EPL],
-                                                const uint8_t *support_mask, bool force, uint32_t *words) {
+__device__ __forceinline__ void select_position(const Dims &d, const Work &ws, int t, const float (&v)[EPL],
+                                                const uint8_t *support_mask, bool force, uint32_t *words,
+                                                uint2 *scratch) {
   const int lane = lane_id(), e0 = lane * EPL, k = d.k;
   bool ok[EPL];
 #pragma unroll
@@ -111,7 +113,7 @@ __device__ __forceinline__ void select_position(const Dims &d, const Work &ws, i
   }
   int sel;
   float val;
-  warp_topk<EPL>(v, ok, k, &sel, &val);
+  warp_topk<EPL>(v, ok, k, &sel, &val, scratch);
   const float top = __shfl_sync(0xffffffffu, val, 0);
   const float ex = lane < k ? expf(val - top) : 0.f;
   float denom = 0.f;

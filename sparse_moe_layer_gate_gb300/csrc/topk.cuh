@@ -10,14 +10,9 @@
 
 namespace epoch {
 
-// (value desc, id asc) order used for every top-k: true if (va, ia) ranks first.
-__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
-}
-
 // Unsigned key with the order of the float value: positive values get the
 // sign bit set, negative values are inverted. -0 is folded into +0 and NaN into
-// -inf first, so keys compare exactly like ranks_before's values.
+// -inf first, so equal values share a key and NaN ranks with -inf.
 __device__ __forceinline__ unsigned order_key(float v) {
   const float c = v != v ? -INFINITY : v + 0.0f;
   const unsigned b = __float_as_uint(c);
@@ -52,66 +47,111 @@ __device__ __forceinline__ void lane_logits(const float *__restrict__ row, int E
 }
 
 // Top-k of one position by one warp. Lane l owns the EPL experts
-// [l*EPL, l*EPL + EPL) with logits v (ineligible ones must not win). Each lane
-// sorts its own entries (value desc, id asc) with a bitonic network; then k
-// rounds pick the best list head across the warp and pop it from its lane.
-// On return, lane j < k holds selection j: *my_sel (expert) and *my_val (logit).
+// [l*EPL, l*EPL + EPL) with logits v; entries with ok false never win. Every
+// comparison is on (order key desc, id asc). `scratch` is 32 entries of
+// shared memory owned by the calling warp.
+//
+// Each lane finds its best entry, and the warp ranks the 32 lane bests. The
+// k-th best lane best is a threshold: the k lanes ranked before it each hold
+// an entry at or above it, so every one of the k best entries is at or above
+// it too. Usually only a few entries pass; they are compacted into `scratch`,
+// each is ranked against the others, and the entry of rank j lands in slot j.
+// When more than 32 pass (values clustered in a few lanes) or k > 16, k rounds
+// take the best remaining lane best instead (a warp max, then the lowest lane
+// holding it: lanes own ascending id ranges, so that is the lowest id).
+// On return, lane j < k holds selection j: *my_sel (expert; -1 if fewer than
+// j + 1 entries are eligible) and *my_val (its logit, -0 read as +0 and NaN as
+// -inf).
 template <int EPL>
-__device__ __forceinline__ void warp_topk(float (&v)[EPL], const bool (&ok)[EPL], int k, int *my_sel,
-                                          float *my_val) {
+__device__ __forceinline__ void warp_topk(const float (&v)[EPL], const bool (&ok)[EPL], int k, int *my_sel,
+                                          float *my_val, uint2 *scratch) {
+  constexpr unsigned kAll = 0xffffffffu;
   const int lane = lane_id();
-  int id[EPL];
+  unsigned key[EPL];  // 0: ineligible or taken (every real key, -inf's included, is above it)
 #pragma unroll
-  for (int c = 0; c < EPL; ++c) {
-    id[c] = ok[c] ? lane * EPL + c : INT_MAX;
-    if (!ok[c]) v[c] = -INFINITY;
-  }
-  // bitonic sort, descending in (value, then lower id first)
+  for (int c = 0; c < EPL; ++c) key[c] = ok[c] ? order_key(v[c]) : 0u;
+  unsigned bk = key[0];  // this lane's best: highest key, lowest index on equal keys
+  int bc = 0;
 #pragma unroll
-  for (int size = 2; size <= EPL; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const bool desc = (i & size) == 0;
-          const bool swap = desc ? ranks_before(v[j], id[j], v[i], id[i]) : ranks_before(v[i], id[i], v[j], id[j]);
-          if (swap) {
-            const float tv = v[i];
-            v[i] = v[j];
-            v[j] = tv;
-            const int ti = id[i];
-            id[i] = id[j];
-            id[j] = ti;
-          }
-        }
-      }
+  for (int c = 1; c < EPL; ++c)
+    if (key[c] > bk) {
+      bk = key[c];
+      bc = c;
     }
-  }
-  // k rounds over the lanes' list heads. A head's value is mapped to an
-  // unsigned key whose order is the float order (-0 folded into +0 and NaN
-  // into -inf, so equal values share a key); one warp max-reduction finds the
-  // best value, a min-reduction the lowest id among the lanes holding it, and
-  // the winning lane pops its head.
   *my_sel = -1;
   *my_val = -INFINITY;
+  if (k <= 16) {
+    int r = 0;  // rank of this lane's best among the lane bests
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const unsigned o = __shfl_sync(kAll, bk, i);
+      r += (o > bk) || (o == bk && i < lane);
+    }
+    const unsigned tb = __ballot_sync(kAll, r == k - 1 && bk != 0u);
+    unsigned tkey = 0u;  // no threshold (fewer than k lanes hold an eligible entry): every eligible entry passes
+    int tid = INT_MAX;
+    if (tb) {
+      const int tl = __ffs(tb) - 1;
+      tkey = __shfl_sync(kAll, bk, tl);
+      tid = __shfl_sync(kAll, lane * EPL + bc, tl);
+    }
+    unsigned cm = 0u;
+#pragma unroll
+    for (int c = 0; c < EPL; ++c)
+      if (key[c] != 0u && (key[c] > tkey || (key[c] == tkey && lane * EPL + c <= tid))) cm |= 1u << c;
+    const int cnt = __popc(cm);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kAll, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int total = __shfl_sync(kAll, incl, 31);
+    if (total <= 32) {
+      int pos = incl - cnt;
+#pragma unroll
+      for (int c = 0; c < EPL; ++c)
+        if ((cm >> c) & 1u) scratch[pos++] = make_uint2(key[c], static_cast<unsigned>(lane * EPL + c));
+      __syncwarp();
+      const uint2 mine = lane < total ? scratch[lane] : make_uint2(0u, 0u);
+      int rk = 0;
+      for (int i = 0; i < total; ++i) {
+        const uint2 o = scratch[i];
+        rk += (o.x > mine.x) || (o.x == mine.x && o.y < mine.y);
+      }
+      __syncwarp();
+      if (lane < total && rk < k) scratch[rk] = mine;
+      __syncwarp();
+      if (lane < k && lane < total) {
+        const uint2 sel = scratch[lane];
+        *my_sel = static_cast<int>(sel.y);
+        *my_val = key_value(sel.x);
+      }
+      __syncwarp();
+      return;
+    }
+  }
   for (int j = 0; j < k; ++j) {
-    const unsigned key = order_key(v[0]);
-    const unsigned best = __reduce_max_sync(0xffffffffu, key);
-    const int bi = __reduce_min_sync(0xffffffffu, key == best ? id[0] : INT_MAX);
-    if (lane == j) {
-      *my_sel = bi;
+    const unsigned best = __reduce_max_sync(kAll, bk);
+    const unsigned hold = __ballot_sync(kAll, bk == best && bk != 0u);
+    const int win = __ffs(hold) - 1;  // -1: nothing eligible is left
+    const int wsel = __shfl_sync(kAll, lane * EPL + bc, win < 0 ? 0 : win);
+    if (lane == j && win >= 0) {
+      *my_sel = wsel;
       *my_val = key_value(best);
     }
-    if (id[0] == bi) {
+    if (lane == win) {  // take the entry, then this lane's next best
 #pragma unroll
-      for (int c = 0; c + 1 < EPL; ++c) {
-        v[c] = v[c + 1];
-        id[c] = id[c + 1];
-      }
-      v[EPL - 1] = -INFINITY;
-      id[EPL - 1] = INT_MAX;
+      for (int c = 0; c < EPL; ++c)
+        if (c == bc) key[c] = 0u;
+      bk = key[0];
+      bc = 0;
+#pragma unroll
+      for (int c = 1; c < EPL; ++c)
+        if (key[c] > bk) {
+          bk = key[c];
+          bc = c;
+        }
     }
   }
 }

@@ -8,7 +8,8 @@ distribution:
 
 * hidden states: x_0 ~ N(0, 1); x_{i+1} = x_i + 0.05 * N(0, 1) per iteration;
 * router weight W_r ~ N(0, std = 1/sqrt(H)); router bias b_e = log of a
-  Zipf(s) probability at a seeded rank permutation of the experts;
+  Zipf(s) probability at a seeded rank permutation of the experts (or, for
+  tie tests, minus the rank's group index, groups of `bias_levels` ranks);
 * expert weights W_gate, W_up ~ N(0, 1/sqrt(H)), W_down ~ N(0, 1/sqrt(I));
 * commit schedules: per block of 32 positions, a number of still-live
   positions is committed after each iteration, chosen by a seeded U(0, 1)
@@ -52,6 +53,7 @@ class Workload:
     commit: str            # "top4" | "one" | "rand1to4" | "linear_live"
     layers: int = 1
     residual: bool = False  # y = x + routed + shared (used to chain a stack)
+    bias_levels: Optional[int] = None  # router bias in groups of this many equal values (exact ties)
     description: str = ""
 
     @property
@@ -147,6 +149,9 @@ def router_payload(wl: Workload, layer: int = 0):
     ranks = _rng(wl.wid, layer, _T_BIAS_PERM).permutation(E) + 1
     harmonic = np.sum(np.arange(1, E + 1, dtype=np.float64) ** (-wl.zipf_s))
     bias = (-wl.zipf_s * np.log(ranks.astype(np.float64)) - np.log(harmonic)).astype(np.float32)
+    if wl.bias_levels:
+        # experts of ranks [1, levels] share bias 0, the next `levels` ranks -1, ...
+        bias = (-np.floor((ranks - 1) / wl.bias_levels)).astype(np.float32)
     return w, bias
 
 

@@ -86,6 +86,24 @@ def test_wide_router_320_experts():
     assert_clean(block_parity(wl))
 
 
+def test_exact_ties_break_to_lower_expert_id():
+    """x = 0 makes every logit exactly its bias on both sides; a bias in groups
+    of equal values then puts exact ties inside every top-k (plan and
+    iterations), and each must go to the lower expert id, with no near-tie
+    allowance. Covers one expert per lane (E = 16) and eight per lane
+    (E = 256, ties within and across lanes)."""
+    for wl in (TINY_BF16.replace(name="tiny_bf16_ties", top_k=4, tau=1.0, bias_levels=3, iters=3),
+               TINY_BF16.replace(name="e256_ties", wid=8, n_experts=256, top_k=8, tau=1.0, bias_levels=5,
+                                 iters=3)):
+        live, dec = synth.block_masks(wl, 3)
+        x = np.zeros((wl.n_pos, wl.hidden), dtype=np.uint16)  # bf16 zeros
+        steps = [dict(op="plan", x=x)] + [dict(op="iter", x=x, live=live[i], dec=dec[i], i=i) for i in range(3)]
+        rep = scenario_parity(wl, steps)
+        assert_clean(rep)
+        assert not rep.near_ties, rep.near_ties[:5]
+        assert rep.iterations == 3
+
+
 def test_tau1_R1_is_dense_moe():
     """tau = 1 and R = 1: every position fresh with every expert eligible, so the
     layer equals the dense MoE formula at every iteration."""
