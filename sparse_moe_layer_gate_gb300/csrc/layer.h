@@ -78,7 +78,7 @@ struct Work {
 // token columns, SM id.
 constexpr int kTraceCtas = 1024;
 constexpr int kTraceFields = 8;
-constexpr int kTraceRows = 7;
+constexpr int kTraceRows = 9;
 
 constexpr int kTileBytes = 128 * 64 * 2;  // one packed 128 x 64 bf16 tile
 constexpr int kRouteThreads = 512;        // the one CTA of the worklist kernel

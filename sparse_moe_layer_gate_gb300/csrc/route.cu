@@ -254,7 +254,12 @@ __global__ void __launch_bounds__(kRouteThreads, 1) k_route(Dims d, Work ws) {
   const int rd = d.state_rd & 1, wr = rd ^ 1;
   int64_t *trace = (d.trace && blockIdx.x < kTraceCtas) ? ws.trace + (3ull * kTraceCtas + blockIdx.x) * kTraceFields
                                                          : nullptr;
-  if (trace && tid == 0) trace[0] = static_cast<int64_t>(globaltimer_ns());
+  if (trace && tid == 0) {
+    trace[0] = static_cast<int64_t>(globaltimer_ns());
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    trace[7] = smid;
+  }
   // the block plan (written before this iteration began) can be read at once
   if (tid < 8) s_cat[tid] = 0;
   if (tid == 0) s_supp = min(E, ws.ctrl->support_len);
@@ -531,6 +536,14 @@ __global__ void __launch_bounds__(kRouteThreads, 1) k_route(Dims d, Work ws) {
   const int nxt = static_cast<int>((d.seq + 1u) & 1u);
   int32_t *sh = ws.sh_ctr + static_cast<size_t>(nxt) * sh_stride(d);
   for (int q = tid; q < sh_stride(d); q += kRouteThreads) sh[q] = 0;
+  // ---- 6: publish the bookkeeping (route_done[1] = this call's sequence
+  // number, release) for the combine kernel, which reads the fresh index,
+  // slots and weights before the expert outputs exist
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ws.route_done + 1), "r"(d.seq) : "memory");
+  }
   if (trace && tid == 0) trace[5] = static_cast<int64_t>(globaltimer_ns());
 }
 
@@ -541,17 +554,31 @@ __global__ void __launch_bounds__(kRouteThreads, 1) k_route(Dims d, Work ws) {
 // behind the worklist kernel, it waits for the worklist to be published
 // (route_done = this call's sequence number), copies its share of the 16-byte
 // vectors and adds their count to tile_ctr[2]; the expert kernel's routed up
-// tiles start once that count reaches L * (vectors per row). Before exiting it
-// waits for the worklist kernel to complete, so that the kernels after it see
-// that kernel's remaining writes.
-constexpr int kPermuteThreads = 256;
-// Small footprint (256 threads, at most 40 registers): its CTAs must fit beside
-// the gate's and the expert kernel's on every SM, or the expert kernel, launched
-// behind it, could not start its shared-expert tiles early.
-__global__ void __launch_bounds__(kPermuteThreads, 6) k_permute(Dims d, Work ws, const uint4 *__restrict__ x, int vpr) {
+// tiles start once that count reaches L * (vectors per row). It exits as soon
+// as its copies are counted (it does not wait for the worklist kernel to
+// finish: its CTAs would hold SMs the expert kernel needs); the combine kernel
+// waits for the worklist kernel's bookkeeping through route_done[1].
+// One CTA per SM (the block scheduler spreads a grid of one CTA per SM over
+// every SM before it stacks any; a larger grid stacked several CTAs on the SMs
+// the gate leaves free, and an expert CTA could not start there until they
+// left). 384 threads, at most 56 registers: a CTA fits beside a gate CTA, and
+// two fit beside an expert CTA (the scheduler still puts two on a few SMs).
+constexpr int kPermuteThreads = 384;
+constexpr int kPermuteVec = 8;  // 16-byte vectors per thread per round
+constexpr int kTraceRowPermute = 8;
+__global__ void __maxnreg__(56) k_permute(Dims d, Work ws, const uint4 *__restrict__ x, int vpr) {
   pdl_trigger();
   __shared__ int s_ok, s_L;
   const int tid = threadIdx.x;
+  int64_t *trace = (d.trace && blockIdx.x < kTraceCtas && tid == 0)
+                       ? ws.trace + (static_cast<size_t>(kTraceRowPermute) * kTraceCtas + blockIdx.x) * kTraceFields
+                       : nullptr;
+  if (trace) {
+    trace[0] = static_cast<int64_t>(globaltimer_ns());
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    trace[7] = smid;
+  }
   if (tid == 0) {
     int ok = 1;
     const uint64_t t0 = globaltimer_ns();
@@ -568,57 +595,59 @@ __global__ void __launch_bounds__(kPermuteThreads, 6) k_permute(Dims d, Work ws,
     }
     s_ok = ok;
     s_L = ok ? ws.ctrl->n_edges : 0;
+    if (trace) trace[1] = static_cast<int64_t>(globaltimer_ns());
   }
   __syncthreads();
-  const int L = s_L;
-  const long long units = static_cast<long long>(L) * vpr;
-  const long long u0 = units * blockIdx.x / gridDim.x, u1 = units * (blockIdx.x + 1) / gridDim.x;
+  // rows [r0, r1) of the worklist; warp w copies rows r0 + w, r0 + w + 12, ...,
+  // lane l the vectors l, l + 32, ... of a row. The warp's row positions are
+  // loaded first, one per lane, so the row copies do not wait on them one by one.
+  const int L = s_L, lane = lane_id(), wid = warp_id(), nw = kPermuteThreads / 32;
+  const int r0 = static_cast<int>(static_cast<long long>(L) * blockIdx.x / gridDim.x);
+  const int r1 = static_cast<int>(static_cast<long long>(L) * (blockIdx.x + 1) / gridDim.x);
   uint4 *xp = static_cast<uint4 *>(ws.xp);
-  for (long long base = u0; base < u1; base += kPermuteThreads * 4) {
-    uint4 buf[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const long long u = base + tid + kPermuteThreads * q;
-      if (u < u1) {
-        const int r = static_cast<int>(u / vpr), v = static_cast<int>(u - static_cast<long long>(r) * vpr);
-        int pos = ws.wl_pos[r];
-        if (pos < 0 || pos >= d.n_pos) {
-          set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-          pos = 0;
-        }
-        buf[q] = __ldg(x + static_cast<size_t>(pos) * vpr + v);
+  for (int rb = r0 + wid; rb < r1; rb += 32 * nw) {
+    int my_pos = 0;
+    const int rl = rb + lane * nw;  // this lane's row of the batch
+    if (rl < r1) {
+      my_pos = ws.wl_pos[rl];
+      if (my_pos < 0 || my_pos >= d.n_pos) {
+        set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+        my_pos = 0;
       }
     }
+    const int nb = min(32, (r1 - rb + nw - 1) / nw);  // rows of this batch
+#pragma unroll 1
+    for (int b = 0; b < nb; ++b) {
+      const int row = rb + b * nw;
+      const int pos = __shfl_sync(0xffffffffu, my_pos, b);
+      const uint4 *src = x + static_cast<size_t>(pos) * vpr;
+      uint4 *dst = xp + static_cast<size_t>(row) * vpr;
+#pragma unroll 1
+      for (int v0 = 0; v0 < vpr; v0 += 32 * kPermuteVec) {
+        uint4 buf[kPermuteVec];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const long long u = base + tid + kPermuteThreads * q;
-      if (u < u1) xp[u] = buf[q];
+        for (int q = 0; q < kPermuteVec; ++q) {
+          const int v = v0 + lane + 32 * q;
+          if (v < vpr) buf[q] = __ldg(src + v);
+        }
+#pragma unroll
+        for (int q = 0; q < kPermuteVec; ++q) {
+          const int v = v0 + lane + 32 * q;
+          if (v < vpr) dst[v] = buf[q];
+        }
+      }
     }
   }
   __syncthreads();
-  if (tid == 0 && s_ok && u1 > u0) {
+  if (tid == 0 && s_ok && r1 > r0) {
     __threadfence();
-    atomicAdd(ws.tile_ctr + 2, static_cast<int>(u1 - u0));
+    atomicAdd(ws.tile_ctr + 2, (r1 - r0) * vpr);
   }
-  pdl_wait();
+  if (trace) trace[2] = static_cast<int64_t>(globaltimer_ns());
 }
 
 // ---------------------------------------------------------------- combine + cache
-// Eight consecutive elements of a row, loaded/stored as one or two 16-byte vectors.
-__device__ __forceinline__ void load8(const float *p, float (&v)[8]) {
-  const float4 a = *reinterpret_cast<const float4 *>(p), b = *reinterpret_cast<const float4 *>(p + 4);
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&v)[8]) {
-  const uint4 u = *reinterpret_cast<const uint4 *>(p);
-  const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float2 f = __bfloat1622float2(h[q]);
-    v[2 * q] = f.x;
-    v[2 * q + 1] = f.y;
-  }
-}
+// Eight consecutive elements of a row, stored as one or two 16-byte vectors.
 __device__ __forceinline__ void store8(float *p, const float (&v)[8]) {
   *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
   *reinterpret_cast<float4 *>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
@@ -631,108 +660,180 @@ __device__ __forceinline__ void store8(__nv_bfloat16 *p, const float (&v)[8]) {
   *reinterpret_cast<uint4 *>(p) = u;
 }
 
+constexpr int kTraceRowCombine = 7;
+
+// Eight consecutive elements of a row as loaded (converted after every load of
+// a run has been issued).
+template <typename T> struct Row8;
+template <> struct Row8<__nv_bfloat16> {
+  uint4 u;
+  __device__ __forceinline__ void load(const __nv_bfloat16 *p) { u = *reinterpret_cast<const uint4 *>(p); }
+  __device__ __forceinline__ void get(float (&v)[8]) const {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 f = __bfloat1622float2(h[q]);
+      v[2 * q] = f.x;
+      v[2 * q + 1] = f.y;
+    }
+  }
+};
+template <> struct Row8<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float *p) {
+    a = *reinterpret_cast<const float4 *>(p);
+    b = *reinterpret_cast<const float4 *>(p + 4);
+  }
+  __device__ __forceinline__ void get(float (&v)[8]) const {
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+};
+
 // One CTA per position, 8 elements per thread per pass. Expert outputs O are
 // stored in the layer dtype. Fresh t:
 // r = sum_j w_j O[slot(t, j)] (j ascending, fp32) and the cache row is refilled
 // ([W] section "Liveness-Shard Parallelism": Y[F_i] = Y_F); reused t: r = the
 // cached row (Y[not F_i] = C_l[not F_i]). Then y = r + shared outputs (+ x when
 // residual), rounded once: the dense shard is restored at the layer boundary.
-// Two dependent rounds of loads: the fresh index, slots, weights, cached row,
-// shared outputs and x together (selections are stored per position), then the
-// k expert-output rows of a fresh position.
+// The fresh index, slots and weights come from the worklist kernel's
+// bookkeeping and are read while the experts still run (route_done[1] = this
+// call's sequence number); once the expert grid has finished, each pass
+// requests every row it needs (the k expert-output rows or the cached row,
+// the shared outputs, x) before using any of them.
 template <typename T>
-__global__ void __launch_bounds__(128) k_combine(Dims d, Work ws, const T *__restrict__ x, T *__restrict__ y) {
+__global__ void __launch_bounds__(128, 7) k_combine(Dims d, Work ws, const T *__restrict__ x, T *__restrict__ y) {
   const KernelMark mark_(d, ws, K_COMBINE);
-  pdl_wait();
+  int64_t *trace = (d.trace && blockIdx.x < kTraceCtas && threadIdx.x == 0)
+                       ? ws.trace + (static_cast<size_t>(kTraceRowCombine) * kTraceCtas + blockIdx.x) * kTraceFields
+                       : nullptr;
+  if (trace) {
+    trace[0] = static_cast<int64_t>(globaltimer_ns());
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    trace[7] = smid;
+  }
   const int t = blockIdx.x;
-  if (t >= d.n_pos) return;
   const int H = d.H, k = d.k;
-  constexpr int kPasses = 4;  // rows up to 4 * 128 * 8 elements stay in registers
-  T *cache = reinterpret_cast<T *>(ws.cache) + static_cast<size_t>(t) * H;
   __shared__ int32_t slot_s[16];
   __shared__ float w_s[16];
   __shared__ int f_s;
-  if (threadIdx.x < k) {
-    slot_s[threadIdx.x] = ws.slot[static_cast<size_t>(t) * k + threadIdx.x];
-    w_s[threadIdx.x] = ws.selw[static_cast<size_t>(t) * k + threadIdx.x];
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+      unsigned int v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ws.route_done + 1) : "memory");
+      if (v == d.seq) break;
+      if (globaltimer_ns() - t0 > static_cast<uint64_t>(d.timeout_ns)) {
+        set_error(ws.err, EPOCH_DEVERR_TIMEOUT);
+        break;
+      }
+      __nanosleep(64);
+    }
   }
-  if (threadIdx.x == 0) f_s = ws.fidx[t];
-  // first round, independent of the slots: cached row, shared outputs, x
-  float base[kPasses][8];
+  __syncthreads();
+  if (t < d.n_pos) {
+    if (threadIdx.x < k) {
+      int sl = ws.slot[static_cast<size_t>(t) * k + threadIdx.x];
+      slot_s[threadIdx.x] = sl;
+      w_s[threadIdx.x] = ws.selw[static_cast<size_t>(t) * k + threadIdx.x];
+    }
+    if (threadIdx.x == 0) f_s = ws.fidx[t];
+  }
+  pdl_wait();  // the expert outputs of this call are complete
+  if (trace) trace[1] = static_cast<int64_t>(globaltimer_ns());
+  if (t >= d.n_pos) return;
+  __syncthreads();
+  const int f = f_s;
+  if (f >= 0 && threadIdx.x < k && (slot_s[threadIdx.x] < 0 || slot_s[threadIdx.x] >= d.Nmax * k)) {
+    set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+    slot_s[threadIdx.x] = 0;
+  }
+  __syncthreads();
+  if (trace) trace[2] = static_cast<int64_t>(globaltimer_ns());
+  T *cache = reinterpret_cast<T *>(ws.cache) + static_cast<size_t>(t) * H;
+  const T *o_int = static_cast<const T *>(ws.o_int);
+  const T *o_sh = static_cast<const T *>(ws.o_sh) + static_cast<size_t>(t) * H;
+  constexpr int kU = sizeof(T) == 2 ? 4 : 2;  // expert rows requested together (at most 72 registers)
+  constexpr int kS = 2;                       // shared-expert rows requested with them
+#pragma unroll 1
+  for (int h0 = threadIdx.x * 8; h0 < H; h0 += blockDim.x * 8) {
+    Row8<T> ro[kU], rs[kS], rx;
+    if (f >= 0) {
 #pragma unroll
-  for (int pass = 0; pass < kPasses; ++pass) {
-    const int h0 = (pass * blockDim.x + threadIdx.x) * 8;
-    if (h0 >= H) break;
+      for (int j = 0; j < kU; ++j)
+        if (j < k) ro[j].load(o_int + static_cast<size_t>(slot_s[j]) * H + h0);
+    } else {
+      ro[0].load(cache + h0);
+    }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) base[pass][q] = 0.f;
-    for (int s = 0; s < d.n_sh; ++s) {
+    for (int s = 0; s < kS; ++s)
+      if (s < d.n_sh) rs[s].load(o_sh + static_cast<size_t>(s) * d.Nmax * H + h0);
+    if (d.residual) rx.load(x + static_cast<size_t>(t) * H + h0);
+    // shared outputs (+ x) in expert order
+    float base[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) base[q] = 0.f;
+#pragma unroll
+    for (int s = 0; s < kS; ++s)
+      if (s < d.n_sh) {
+        float o[8];
+        rs[s].get(o);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) base[q] += o[q];
+      }
+#pragma unroll 1
+    for (int s = kS; s < d.n_sh; ++s) {
+      Row8<T> r2;
+      r2.load(o_sh + static_cast<size_t>(s) * d.Nmax * H + h0);
       float o[8];
-      load8(static_cast<const T *>(ws.o_sh) + (static_cast<size_t>(s) * d.Nmax + t) * H + h0, o);
+      r2.get(o);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) base[pass][q] += o[q];
+      for (int q = 0; q < 8; ++q) base[q] += o[q];
     }
     if (d.residual) {
       float xv[8];
-      load8(x + static_cast<size_t>(t) * H + h0, xv);
+      rx.get(xv);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) base[pass][q] += xv[q];
+      for (int q = 0; q < 8; ++q) base[q] += xv[q];
     }
-  }
-  __syncthreads();
-  const int f = f_s;
-  for (int j = threadIdx.x; f >= 0 && j < k; j += blockDim.x) {
-    if (slot_s[j] < 0 || slot_s[j] >= d.Nmax * k) {
-      set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-      slot_s[j] = 0;
-    }
-  }
-  __syncthreads();
-  // routed part of one 8-element run at h0: the weighted expert outputs of a
-  // fresh position (refilling its cache row), else its cached row
-  auto routed8 = [&](int h0, float (&r)[8]) {
+    // routed part: weighted expert outputs (refilling the cache row), or the cached row
+    float r[8];
     if (f >= 0) {
 #pragma unroll
       for (int q = 0; q < 8; ++q) r[q] = 0.f;
-      for (int j = 0; j < k; ++j) {
-        float o[8];
-        load8(static_cast<const T *>(ws.o_int) + static_cast<size_t>(slot_s[j]) * H + h0, o);
-        const float wj = w_s[j];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) r[q] = fmaf(wj, o[q], r[q]);
+      for (int j = 0; j < kU; ++j)
+        if (j < k) {
+          float o[8];
+          ro[j].get(o);
+          const float wj = w_s[j];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) r[q] = fmaf(wj, o[q], r[q]);
+        }
+#pragma unroll 1
+      for (int j0 = kU; j0 < k; j0 += kU) {  // further rows, kU at a time
+#pragma unroll
+        for (int j = 0; j < kU; ++j)
+          if (j0 + j < k) ro[j].load(o_int + static_cast<size_t>(slot_s[j0 + j]) * H + h0);
+#pragma unroll
+        for (int j = 0; j < kU; ++j)
+          if (j0 + j < k) {
+            float o[8];
+            ro[j].get(o);
+            const float wj = w_s[j0 + j];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) r[q] = fmaf(wj, o[q], r[q]);
+          }
       }
       store8(cache + h0, r);
     } else {
-      load8(cache + h0, r);
+      ro[0].get(r);
     }
-  };
 #pragma unroll
-  for (int pass = 0; pass < kPasses; ++pass) {
-    const int h0 = (pass * blockDim.x + threadIdx.x) * 8;
-    if (h0 >= H) break;
-    float r[8];
-    routed8(h0, r);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) r[q] += base[pass][q];
+    for (int q = 0; q < 8; ++q) r[q] += base[q];
     store8(y + static_cast<size_t>(t) * H + h0, r);
   }
-  // rows wider than kPasses passes: the rest loaded here
-  for (int h0 = (kPasses * blockDim.x + threadIdx.x) * 8; h0 < H; h0 += blockDim.x * 8) {
-    float r[8];
-    routed8(h0, r);
-    for (int s = 0; s < d.n_sh; ++s) {
-      float o[8];
-      load8(static_cast<const T *>(ws.o_sh) + (static_cast<size_t>(s) * d.Nmax + t) * H + h0, o);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) r[q] += o[q];
-    }
-    if (d.residual) {
-      float xv[8];
-      load8(x + static_cast<size_t>(t) * H + h0, xv);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) r[q] += xv[q];
-    }
-    store8(y + static_cast<size_t>(t) * H + h0, r);
-  }
+  if (trace) trace[3] = static_cast<int64_t>(globaltimer_ns());
 }
 
 // ---------------------------------------------------------------- bounded-wait test
@@ -876,8 +977,7 @@ cudaError_t launch_permute(const Dims &d, const Work &ws, const void *x, cudaStr
   const uint4 *xv = static_cast<const uint4 *>(x);
   int vpr = d.H * 2 / 16;
   void *args[] = {&dd, &ww, &xv, &vpr};
-  // two CTAs per SM: both still fit beside a gate CTA
-  return launch_kernel(reinterpret_cast<void *>(k_permute), dim3(2 * num_sms()), dim3(kPermuteThreads), 0, s, args,
+  return launch_kernel(reinterpret_cast<void *>(k_permute), dim3(num_sms()), dim3(kPermuteThreads), 0, s, args,
                        true);
 }
 

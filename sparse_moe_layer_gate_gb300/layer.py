@@ -124,11 +124,12 @@ class EpochLayer:
         B.check(B.lib().epoch_set_tracing(self.handle, 1 if on else 0), "epoch_set_tracing")
 
     def read_trace(self, stream=None) -> np.ndarray:
-        """[7, 1024, 8] int64 per-CTA trace rows: gate, experts, expert epilogue,
-        worklist kernel, gate epilogue steps, worklist kernel steps, expert waits."""
+        """[9, 1024, 8] int64 per-CTA trace rows: gate, experts, expert epilogue,
+        worklist kernel, gate epilogue steps, worklist kernel steps, expert waits,
+        combine, permute."""
         v = B.epoch_debug_view()
         B.check(B.lib().epoch_debug_pointers(self.handle, C.byref(v)), "epoch_debug_pointers")
-        return self._copy(v.trace, 7 * 1024 * 8, np.int64, stream).reshape(7, 1024, 8)
+        return self._copy(v.trace, 9 * 1024 * 8, np.int64, stream).reshape(9, 1024, 8)
 
     def read_timeline(self, stream=None) -> dict:
         """{kernel: (first entry ns, last exit ns)} of the last traced iteration."""
