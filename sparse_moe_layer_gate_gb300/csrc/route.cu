@@ -561,12 +561,14 @@ __global__ void __launch_bounds__(kRouteThreads, 1) k_route(Dims d, Work ws) {
 // One CTA per SM (the block scheduler spreads a grid of one CTA per SM over
 // every SM before it stacks any; a larger grid stacked several CTAs on the SMs
 // the gate leaves free, and an expert CTA could not start there until they
-// left). 384 threads, at most 56 registers: a CTA fits beside a gate CTA, and
-// two fit beside an expert CTA (the scheduler still puts two on a few SMs).
+// left). 384 threads, at most 64 registers: a CTA fits beside a gate CTA or an
+// expert CTA. (With fewer registers the scheduler stacked two or three on the
+// SMs the gate leaves free, and an SM sub-partition's registers then no longer
+// held an expert CTA's warps beside them.)
 constexpr int kPermuteThreads = 384;
 constexpr int kPermuteVec = 8;  // 16-byte vectors per thread per round
 constexpr int kTraceRowPermute = 8;
-__global__ void __maxnreg__(56) k_permute(Dims d, Work ws, const uint4 *__restrict__ x, int vpr) {
+__global__ void __maxnreg__(64) k_permute(Dims d, Work ws, const uint4 *__restrict__ x, int vpr) {
   pdl_trigger();
   __shared__ int s_ok, s_L;
   const int tid = threadIdx.x;
