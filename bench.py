@@ -38,10 +38,10 @@ L2_FLUSH_BYTES = 256 << 20
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one expert-kernel
 # launch: the ncu capture at iteration 20 of the accounting block (231.9 MB read,
-# 3.2 MB written; every iteration of this workload hits the same 34 routed
+# 3.0 MB written; every iteration of this workload hits the same 34 routed
 # experts), tied to the kernel source it was measured on (null once that
 # source changes).
-TRAFFIC = {"experts": {"bytes_per_launch": 235.13e6, "source_sha": "61def3e1e1fd62ca"}}
+TRAFFIC = {"experts": {"bytes_per_launch": 234.92e6, "source_sha": "5b34676a3a716582"}}
 
 
 def parse():
