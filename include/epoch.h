@@ -218,6 +218,23 @@ epoch_status epoch_moe_iter(epoch_layer *layer, const void *x_dev, const uint8_t
                             const uint8_t *decoded_dev, int32_t n_pos, int32_t iteration, void *y_dev,
                             epoch_stream stream);
 
+/* Lifecycle paths of an iteration inside a block ([W] section "cold、hot-update、
+ * hot-skip"): 0 is the hot-skip path of epoch_moe_iter (the support of the
+ * block plan is reused). EPOCH_PATH_HOT_UPDATE rebuilds the support first,
+ * with the block-plan rule (tau), from this iteration's own router logits; the
+ * cache, stamps and decoded flags are kept (an update counter or a drifting
+ * support is the caller's trigger). EPOCH_PATH_REFRESH is the refresh path:
+ * every position goes through the fresh routed path (each cached row counts as
+ * stale this iteration, so the selection stays within the support) and every
+ * row's age restarts. The two may be combined. */
+typedef enum { EPOCH_PATH_HOT_UPDATE = 1, EPOCH_PATH_REFRESH = 2 } epoch_path;
+
+/* epoch_moe_iter on a chosen path (path: a bitwise OR of epoch_path values, or
+ * 0). EPOCH_EINVAL for unknown path bits, otherwise as epoch_moe_iter. */
+epoch_status epoch_moe_iter_path(epoch_layer *layer, const void *x_dev, const uint8_t *live_dev,
+                                 const uint8_t *decoded_dev, int32_t n_pos, int32_t iteration, int32_t path,
+                                 void *y_dev, epoch_stream stream);
+
 /* Ends the block: the plan, cache and stamps become invalid; the next
  * epoch_moe_iter without a new plan runs as a fallback. Host-only, no sync. */
 epoch_status epoch_block_end(epoch_layer *layer);
@@ -242,6 +259,10 @@ epoch_status epoch_debug_copy(void *host_dst, const void *dev_src, size_t bytes,
 /* Host-side counters of the lifecycle paths: plans (cold), normal iterations
  * (hot-skip), host-detected fallbacks. Any pointer may be NULL. */
 epoch_status epoch_path_counters(epoch_layer *layer, int64_t *cold, int64_t *hot, int64_t *fallback);
+
+/* Iterations that took the hot-update path, and the refresh path (host-side
+ * counts; both also count as hot or fallback above). Any pointer may be NULL. */
+epoch_status epoch_path_counters_ex(epoch_layer *layer, int64_t *hot_update, int64_t *refresh);
 
 /* Bounded device waits: a wait that makes no progress for timeout_ns gives up,
  * sets EPOCH_DEVERR_TIMEOUT and lets the kernel return (default 2e9 ns). */

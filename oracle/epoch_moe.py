@@ -42,6 +42,10 @@ Readings taken where the pages are silent:
   * selection uses raw logits (bias included); ties go to the lower expert id;
     weights are a softmax over the k selected logits (they sum to 1);
   * refresh: a decoded position is stale when i - stamp >= R (R = None: never);
+    a refresh-path iteration makes every cached row stale (R = 0 for that
+    iteration) and keeps the support;
+  * hot-update: the support is rebuilt with the block-plan rule from the
+    current iteration's logits; cache, stamps and decoded flags are kept;
   * the expert is SwiGLU: E(x) = W_down (silu(W_gate x) * (W_up x)), silu(z) = z / (1 + e^-z);
   * a position flagged both live and decoded, or neither, is treated as live;
     a decoded -> live transition is an anomaly that makes the whole iteration
@@ -51,8 +55,10 @@ Readings taken where the pages are silent:
 Parity pins (tests/test_oracle_pins.py): brute-force top-k over all k-subsets,
 minimal-cardinality support by brute force over expert subsets, hand-worked
 fresh-set schedules (tests/golden/), closed-form silu values, the dense-MoE
-special case (tau = 1, R = 1) against an all-experts masked formulation, and the
-cache/staleness invariants. Outputs after many iterations with reused rows are
+special case (tau = 1, R = 1) against an all-experts masked formulation, the
+cache/staleness invariants, and the hot-update and refresh paths (the rebuilt
+support equals a block plan on the same input; a refresh iteration equals a
+from-scratch restricted MoE on every position). Outputs after many iterations with reused rows are
 pinned only through those invariants.
 """
 from __future__ import annotations
@@ -290,6 +296,19 @@ class LayerOracle:
         self.last_iter = -1
         return self.plan
 
+    # hot-update path ([W] "cold、hot-update、hot-skip": inside a block, the
+    # support is rebuilt from the current router logits, e.g. when an update
+    # counter expires). Same rule as the block plan, on this iteration's x; the
+    # per-position cache, stamps and decoded flags are kept.
+    def hot_update(self, x: np.ndarray) -> PlanResult:
+        N = x.shape[0]
+        G = gate_logits(x, self.w_router, self.b_router)
+        cnt = hit_counts(G, self.k)
+        ranked, slen = plan_support(cnt, self.k, self.tau, N)
+        self.support_mask = np.zeros(self.E, dtype=bool)
+        self.support_mask[ranked[:slen]] = True
+        return PlanResult(G, cnt, ranked, slen, coverage_threshold(self.tau, N, self.k))
+
     def adopt_support(self, ranked: np.ndarray, slen: int) -> None:
         """Replace the plan's support (used after a logged near-tie at plan time)."""
         self.support_mask = np.zeros(self.E, dtype=bool)
@@ -300,15 +319,25 @@ class LayerOracle:
 
     def iterate(self, x: np.ndarray, live: np.ndarray, decoded: np.ndarray, i: int,
                 adopt: Optional[Callable[[int, np.ndarray, np.ndarray, np.ndarray],
-                                         Optional[np.ndarray]]] = None
-                ) -> IterResult:
+                                         Optional[np.ndarray]]] = None,
+                hot_update: bool = False, refresh: bool = False) -> IterResult:
         """One refinement iteration. ``adopt(t, sel, g_row, eligible)`` may return a
         replacement selection for position t (the parity harness uses it after a
-        logged near-tie)."""
+        logged near-tie).
+
+        hot_update: rebuild the support from this iteration's logits first (see
+        ``hot_update``). refresh: the refresh path ([W] "cold、hot-update、
+        hot-skip") -- every position goes through the fresh routed path, which
+        resets the age of every cached row; read here as a refresh period of 0
+        for this iteration (each cached row counts as stale), so the selection
+        stays restricted to the support and nothing else changes."""
         N = x.shape[0]
         host_fallback = (not self.planned) or (i != self.last_iter + 1) or (N != self.n_pos)
+        if hot_update:
+            self.hot_update(x)
         G = gate_logits(x, self.w_router, self.b_router)
-        cl = classify_positions(live, decoded, self.prev_decoded, self.stamp, i, self.R, host_fallback)
+        R = 0 if refresh else self.R
+        cl = classify_positions(live, decoded, self.prev_decoded, self.stamp, i, R, host_fallback)
         fallback = host_fallback or cl.anomaly
         eligible = np.ones(self.E, dtype=bool) if fallback else self.support_mask
 

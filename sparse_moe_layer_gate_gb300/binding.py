@@ -67,6 +67,8 @@ _SIGS = {
     "epoch_plan_block": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p]),
     "epoch_moe_iter": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32,
                                  C.c_void_p, C.c_void_p]),
+    "epoch_moe_iter_path": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32,
+                                      C.c_int32, C.c_void_p, C.c_void_p]),
     "epoch_block_end": (C.c_int, [C.c_void_p]),
     "epoch_get_status": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(C.c_uint32)]),
     "epoch_clear_status": (C.c_int, [C.c_void_p, C.c_void_p]),
@@ -75,6 +77,7 @@ _SIGS = {
     "epoch_debug_copy": (C.c_int, [C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
     "epoch_path_counters": (C.c_int, [C.c_void_p, C.POINTER(C.c_int64), C.POINTER(C.c_int64),
                                       C.POINTER(C.c_int64)]),
+    "epoch_path_counters_ex": (C.c_int, [C.c_void_p, C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
     "epoch_set_wait_timeout": (C.c_int, [C.c_void_p, C.c_int64]),
     "epoch_set_tracing": (C.c_int, [C.c_void_p, C.c_int32]),
     "epoch_set_profiling": (C.c_int, [C.c_void_p, C.c_int32]),
@@ -138,6 +141,15 @@ def epoch_plan_block(layer: int, x_ptr: int, n_pos: int, stream: int = 0) -> int
 def epoch_moe_iter(layer: int, x_ptr: int, live_ptr: int, decoded_ptr: int, n_pos: int, iteration: int,
                    y_ptr: int, stream: int = 0) -> int:
     return lib().epoch_moe_iter(layer, x_ptr, live_ptr, decoded_ptr, n_pos, iteration, y_ptr, stream)
+
+
+PATH_HOT_UPDATE = 1  # epoch_path values
+PATH_REFRESH = 2
+
+
+def epoch_moe_iter_path(layer: int, x_ptr: int, live_ptr: int, decoded_ptr: int, n_pos: int, iteration: int,
+                        path: int, y_ptr: int, stream: int = 0) -> int:
+    return lib().epoch_moe_iter_path(layer, x_ptr, live_ptr, decoded_ptr, n_pos, iteration, path, y_ptr, stream)
 
 
 def epoch_block_end(layer: int) -> int:

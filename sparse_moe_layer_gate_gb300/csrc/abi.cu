@@ -34,6 +34,7 @@ struct epoch_layer {
   int32_t state_rd;  // half of the double-buffered iteration state the next iteration reads
   uint32_t seq;      // sequence number of the last iteration call
   int64_t n_cold, n_hot, n_fallback, n_launch;
+  int64_t n_hot_update, n_refresh;
   // profiling
   bool prof;
   struct Pending {
@@ -304,7 +305,7 @@ epoch_status epoch_plan_block(epoch_layer *L, const void *x, int32_t n_pos, epoc
   const double tau = L->cfg.tau;
   const int all = tau >= 1.0;
   const int32_t T = static_cast<int32_t>(std::ceil(tau * static_cast<double>(n_pos * L->cfg.top_k)));
-  EPOCH_TRY(run(L, K_PLAN_SUPPORT, s, [&] { return launch_plan_support(d, L->ws, T, all, s); }));
+  EPOCH_TRY(run(L, K_PLAN_SUPPORT, s, [&] { return launch_plan_support(d, L->ws, T, all, 1, s); }));
   L->planned = true;
   L->n_pos_plan = n_pos;
   L->last_iter = -1;
@@ -312,13 +313,15 @@ epoch_status epoch_plan_block(epoch_layer *L, const void *x, int32_t n_pos, epoc
   return EPOCH_OK;
 }
 
-epoch_status epoch_moe_iter(epoch_layer *L, const void *x, const uint8_t *live, const uint8_t *decoded,
-                            int32_t n_pos, int32_t iteration, void *y, epoch_stream stream) {
+epoch_status epoch_moe_iter_path(epoch_layer *L, const void *x, const uint8_t *live, const uint8_t *decoded,
+                                 int32_t n_pos, int32_t iteration, int32_t path, void *y, epoch_stream stream) {
   if (L == nullptr || !aligned16(x) || !aligned16(y) || live == nullptr || decoded == nullptr) return EPOCH_EINVAL;
   if (n_pos < 1 || n_pos > L->cfg.max_positions || iteration < 0) return EPOCH_EINVAL;
+  if ((path & ~(EPOCH_PATH_HOT_UPDATE | EPOCH_PATH_REFRESH)) != 0) return EPOCH_EINVAL;
   cudaStream_t s = S(stream);
   const int host_fallback = !L->planned || iteration != L->last_iter + 1 || n_pos != L->n_pos_plan;
   Dims d = call_dims(L, n_pos, iteration, host_fallback);
+  if (path & EPOCH_PATH_REFRESH) d.R = 0;  // every cached row counts as stale: all positions fresh
   if (d.trace) {
     if (cudaMemsetAsync(L->ws.timeline, 0xFF, K_NUM * 8, s) != cudaSuccess ||
         cudaMemsetAsync(L->ws.timeline + K_NUM, 0, K_NUM * 8, s) != cudaSuccess)
@@ -326,7 +329,24 @@ epoch_status epoch_moe_iter(epoch_layer *L, const void *x, const uint8_t *live, 
   }
   d.seq = ++L->seq;
   CUtensorMap x_map_up;
-  EPOCH_TRY(run_gate(L, d, x, live, decoded, &x_map_up, s));
+  if (path & EPOCH_PATH_HOT_UPDATE) {
+    // hot-update path: logits of this iteration, the support rebuilt from them
+    // (block-plan rule, state kept), then classification and top-k over it
+    d.plan_mode = 1;
+    EPOCH_TRY(run_gate(L, d, x, live, decoded, &x_map_up, s));
+    if (cudaMemsetAsync(L->ws.plan_counts, 0, sizeof(int32_t) * d.E, s) != cudaSuccess) return EPOCH_ECUDA;
+    EPOCH_TRY(run(L, K_PLAN_TOPK, s, [&] { return launch_plan_topk(d, L->w, L->ws, s); }));
+    const double tau = L->cfg.tau;
+    const int all = tau >= 1.0;
+    const int32_t T = static_cast<int32_t>(std::ceil(tau * static_cast<double>(n_pos * L->cfg.top_k)));
+    EPOCH_TRY(run(L, K_PLAN_SUPPORT, s, [&] { return launch_plan_support(d, L->ws, T, all, 0, s); }));
+    d.plan_mode = 0;
+    EPOCH_TRY(run(L, K_SELECT, s, [&] { return launch_select(d, L->ws, live, decoded, s); }));
+    ++L->n_hot_update;
+  } else {
+    EPOCH_TRY(run_gate(L, d, x, live, decoded, &x_map_up, s));
+  }
+  if (path & EPOCH_PATH_REFRESH) ++L->n_refresh;
   EPOCH_TRY(run(L, K_ROUTING, s, [&] { return launch_route(d, L->ws, s); }));
   L->state_rd ^= 1;  // this iteration wrote the new state into the other half
   if (L->bf16) {
@@ -341,6 +361,11 @@ epoch_status epoch_moe_iter(epoch_layer *L, const void *x, const uint8_t *live, 
   if (host_fallback) ++L->n_fallback;
   else ++L->n_hot;
   return EPOCH_OK;
+}
+
+epoch_status epoch_moe_iter(epoch_layer *L, const void *x, const uint8_t *live, const uint8_t *decoded,
+                            int32_t n_pos, int32_t iteration, void *y, epoch_stream stream) {
+  return epoch_moe_iter_path(L, x, live, decoded, n_pos, iteration, 0, y, stream);
 }
 
 epoch_status epoch_block_end(epoch_layer *L) {
@@ -408,6 +433,13 @@ epoch_status epoch_path_counters(epoch_layer *L, int64_t *cold, int64_t *hot, in
   if (cold) *cold = L->n_cold;
   if (hot) *hot = L->n_hot;
   if (fallback) *fallback = L->n_fallback;
+  return EPOCH_OK;
+}
+
+epoch_status epoch_path_counters_ex(epoch_layer *L, int64_t *hot_update, int64_t *refresh) {
+  if (L == nullptr) return EPOCH_EINVAL;
+  if (hot_update) *hot_update = L->n_hot_update;
+  if (refresh) *refresh = L->n_refresh;
   return EPOCH_OK;
 }
 

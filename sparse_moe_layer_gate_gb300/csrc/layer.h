@@ -156,8 +156,9 @@ cudaError_t launch_gate_simt(const Dims &d, const Weights &w, const Work &ws, co
 cudaError_t launch_select(const Dims &d, const Work &ws, const uint8_t *live, const uint8_t *decoded,
                           cudaStream_t s);
 cudaError_t launch_plan_topk(const Dims &d, const Weights &w, const Work &ws, cudaStream_t s);
+// clear_state: also reset every stamp and decoded flag (a block plan; not a hot update).
 cudaError_t launch_plan_support(const Dims &d, const Work &ws, int32_t threshold, int all_experts,
-                                cudaStream_t s);
+                                int clear_state, cudaStream_t s);
 cudaError_t launch_route(const Dims &d, const Work &ws, cudaStream_t s);
 cudaError_t launch_permute(const Dims &d, const Work &ws, const void *x, cudaStream_t s);
 cudaError_t launch_combine(const Dims &d, const Work &ws, const void *x, void *y, int bf16, cudaStream_t s);

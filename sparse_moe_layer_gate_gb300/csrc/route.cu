@@ -131,9 +131,11 @@ __global__ void k_plan_topk(Dims d, const float *__restrict__ logits, int32_t *_
 }
 
 // One CTA: rank experts by (count desc, id asc), take the smallest prefix whose
-// counts reach `threshold` (at least k; every expert when all_experts), and
-// clear the block's stamps and previous-decoded flags (cold path).
-__global__ void __launch_bounds__(1024) k_plan_support(Dims d, Work ws, int32_t threshold, int all_experts) {
+// counts reach `threshold` (at least k; every expert when all_experts), and,
+// for a block plan (cold path), clear the block's stamps and previous-decoded
+// flags; a hot update keeps them.
+__global__ void __launch_bounds__(1024) k_plan_support(Dims d, Work ws, int32_t threshold, int all_experts,
+                                                       int clear_state) {
   const KernelMark mark_(d, ws, K_PLAN_SUPPORT);
   __shared__ int32_t cnt[1024];
   __shared__ int32_t sorted_cnt[1024];
@@ -181,9 +183,11 @@ __global__ void __launch_bounds__(1024) k_plan_support(Dims d, Work ws, int32_t 
     ws.support_mask[tid] = rank < len ? 1 : 0;
   }
   if (tid == 0) ws.ctrl->support_len = len;
-  for (int t = tid; t < 2 * d.Nmax; t += blockDim.x) {  // both halves of the iteration state
-    ws.stamp[t] = -1;
-    ws.prev_dec[t] = 0;
+  if (clear_state) {
+    for (int t = tid; t < 2 * d.Nmax; t += blockDim.x) {  // both halves of the iteration state
+      ws.stamp[t] = -1;
+      ws.prev_dec[t] = 0;
+    }
   }
 }
 
@@ -946,10 +950,10 @@ cudaError_t launch_plan_topk(const Dims &d, const Weights &w, const Work &ws, cu
 }
 
 cudaError_t launch_plan_support(const Dims &d, const Work &ws, int32_t threshold, int all_experts,
-                                cudaStream_t s) {
+                                int clear_state, cudaStream_t s) {
   static bool carve_ = (prefer_max_shared(k_plan_support) == cudaSuccess);
   (void)carve_;
-  k_plan_support<<<1, 1024, 0, s>>>(d, ws, threshold, all_experts);
+  k_plan_support<<<1, 1024, 0, s>>>(d, ws, threshold, all_experts, clear_state);
   return cudaGetLastError();
 }
 

@@ -78,7 +78,10 @@ class EpochLayer:
                 "epoch_plan_block")
 
     def moe_iter(self, x: torch.Tensor, live: torch.Tensor, decoded: torch.Tensor, iteration: int,
-                 y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                 y: Optional[torch.Tensor] = None, stream=None, hot_update: bool = False,
+                 refresh: bool = False) -> torch.Tensor:
+        """One iteration; hot_update / refresh select the lifecycle path
+        (epoch_moe_iter_path), the default being the hot-skip path."""
         self._check_x(x)
         n = x.shape[0]
         for m in (live, decoded):
@@ -86,8 +89,14 @@ class EpochLayer:
                 raise ValueError("live/decoded must be contiguous uint8 CUDA tensors of n_pos flags")
         if y is None:
             y = torch.empty_like(x)
-        B.check(B.epoch_moe_iter(self.handle, x.data_ptr(), live.data_ptr(), decoded.data_ptr(), n,
-                                 int(iteration), y.data_ptr(), _stream(stream)), "epoch_moe_iter")
+        path = (B.PATH_HOT_UPDATE if hot_update else 0) | (B.PATH_REFRESH if refresh else 0)
+        if path:
+            B.check(B.epoch_moe_iter_path(self.handle, x.data_ptr(), live.data_ptr(), decoded.data_ptr(), n,
+                                          int(iteration), path, y.data_ptr(), _stream(stream)),
+                    "epoch_moe_iter_path")
+        else:
+            B.check(B.epoch_moe_iter(self.handle, x.data_ptr(), live.data_ptr(), decoded.data_ptr(), n,
+                                     int(iteration), y.data_ptr(), _stream(stream)), "epoch_moe_iter")
         return y
 
     def block_end(self) -> None:
@@ -106,6 +115,12 @@ class EpochLayer:
 
     def clear_status(self, stream=None) -> None:
         B.check(B.lib().epoch_clear_status(self.handle, _stream(stream)), "epoch_clear_status")
+
+    def path_counters_ex(self):
+        """(hot-update iterations, refresh iterations)."""
+        hu, rf = C.c_int64(0), C.c_int64(0)
+        B.check(B.lib().epoch_path_counters_ex(self.handle, C.byref(hu), C.byref(rf)), "epoch_path_counters_ex")
+        return hu.value, rf.value
 
     def path_counters(self):
         c, h, f = C.c_int64(), C.c_int64(), C.c_int64()

@@ -114,7 +114,26 @@ def check_plan(orc: oracle.LayerOracle, gplan: dict, x0: np.ndarray, wl, rep: Re
     return op
 
 
-def check_iteration(orc, step: GpuStep, live, dec, i: int, wl, rep: Report, tag: str):
+def check_hot_update(orc: oracle.LayerOracle, gplan: dict, x0: np.ndarray, wl, rep: Report, tag: str):
+    """The support a hot-update iteration rebuilt (oracle.hot_update on the same
+    input; near-ties as for the block plan)."""
+    op = orc.hot_update(x0)
+    glen = gplan["support_len"]
+    gids = gplan["support_ids"]
+    same = glen == op.support_len and np.array_equal(gids[:glen], op.ranked[:glen])
+    if not (same and np.array_equal(gplan["plan_counts"], op.counts)):
+        everyone = np.ones(wl.n_experts, dtype=bool)
+        ties = [t for t in range(x0.shape[0]) if oracle.near_tie(op.G[t], everyone, wl.top_k, NEAR_TIE)]
+        if ties:
+            rep.near_ties.append(f"{tag} hot update: near-tie at positions {ties[:8]}; adopting GPU support")
+            orc.adopt_support(gids, glen)
+        else:
+            rep.mismatches.append(f"{tag} hot update: support/counts differ without a near-tie "
+                                  f"(gpu len {glen}, oracle len {op.support_len})")
+    return op
+
+
+def check_iteration(orc, step: GpuStep, live, dec, i: int, wl, rep: Report, tag: str, refresh: bool = False):
     g = step.dbg
     gsel = {int(t): g["sel"][f] for f, t in enumerate(g["fresh_pos"])}
 
@@ -129,7 +148,7 @@ def check_iteration(orc, step: GpuStep, live, dec, i: int, wl, rep: Report, tag:
         return None
 
     x64 = synth.to_f64(step.x, wl.dtype)
-    res = orc.iterate(x64, live, dec, i, adopt=adopt)
+    res = orc.iterate(x64, live, dec, i, adopt=adopt, refresh=refresh)
     st = g["stats"]
     cl = res.classified
     exp = dict(n_live=cl.n_live, n_new=cl.n_new, n_miss=cl.n_miss, n_stale=cl.n_stale, n_forced=cl.n_forced,
@@ -195,7 +214,8 @@ def scenario_parity(wl, steps, max_positions: Optional[int] = None, layer=None) 
     """Interleaved GPU/oracle run of an explicit call sequence on one layer.
 
     steps: dicts with "op" in {"plan", "iter", "end"}; "plan" takes "x" (payload
-    [n, H]); "iter" takes "x", "live", "dec" (uint8 [n]) and "i".
+    [n, H]); "iter" takes "x", "live", "dec" (uint8 [n]) and "i", and optionally
+    "hot_update" / "refresh" (the lifecycle path of the iteration).
     """
     maxp = max_positions or wl.n_pos
     lay = layer or layer_for_workload(wl, 0, max_positions=maxp)
@@ -216,10 +236,13 @@ def scenario_parity(wl, steps, max_positions: Optional[int] = None, layer=None) 
             x = payload_to_torch(st["x"], wl.dtype, dev)
             lv = torch.from_numpy(np.ascontiguousarray(st["live"], dtype=np.uint8)).to(dev)
             dc = torch.from_numpy(np.ascontiguousarray(st["dec"], dtype=np.uint8)).to(dev)
-            y = lay.moe_iter(x, lv, dc, st["i"])
-            dbg = lay.debug(x.shape[0], parts=("iter",))
+            hu, rf = bool(st.get("hot_update")), bool(st.get("refresh"))
+            y = lay.moe_iter(x, lv, dc, st["i"], hot_update=hu, refresh=rf)
+            dbg = lay.debug(x.shape[0], parts=("plan", "iter") if hu else ("iter",))
             step = GpuStep(st["x"], tensor_to_f64(y), dbg)
-            check_iteration(orc, step, st["live"], st["dec"], st["i"], wl, rep, tag)
+            if hu:
+                check_hot_update(orc, dbg, synth.to_f64(st["x"], wl.dtype), wl, rep, tag)
+            check_iteration(orc, step, st["live"], st["dec"], st["i"], wl, rep, tag, refresh=rf)
     if layer is None:
         lay.close()
     return rep

@@ -104,6 +104,30 @@ def test_exact_ties_break_to_lower_expert_id():
         assert rep.iterations == 3
 
 
+@pytest.mark.parametrize("name", ["tiny_bf16", "tiny_fp32"])
+def test_hot_update_and_refresh_paths(name):
+    """Lifecycle paths inside a block: hot-update iterations rebuild the support
+    from their own logits (once with hidden states from another block, so that
+    the support moves), refresh iterations send every position through the
+    fresh path; both against the oracle, and counted."""
+    wl = TINY_BF16 if name == "tiny_bf16" else synth.WORKLOADS["tiny_fp32"].replace(tau=0.6, refresh_R=None)
+    n_it = 8
+    xs, live, dec = _steps_from(wl, n_it)
+    other = synth.hidden_states(wl, 1, block=1)[0]
+    paths = {3: dict(hot_update=True), 5: dict(refresh=True), 6: dict(hot_update=True, refresh=True)}
+    steps = [dict(op="plan", x=xs[0])]
+    for i in range(n_it):
+        st = dict(op="iter", x=other if i == 3 else xs[i], live=live[i], dec=dec[i], i=i)
+        st.update(paths.get(i, {}))
+        steps.append(st)
+    lay = layer_for_workload(wl, 0)
+    rep = scenario_parity(wl, steps, layer=lay)
+    assert_clean(rep)
+    assert rep.iterations == n_it
+    assert lay.path_counters_ex() == (2, 2)
+    lay.close()
+
+
 def test_tau1_R1_is_dense_moe():
     """tau = 1 and R = 1: every position fresh with every expert eligible, so the
     layer equals the dense MoE formula at every iteration."""

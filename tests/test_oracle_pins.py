@@ -244,14 +244,15 @@ def test_fresh_schedules_golden(sched):
 
 # ------------------------------------------------------------------ dense special case
 
-def masked_dense(x, wr, b, experts, k, shared=()):
+def masked_dense(x, wr, b, experts, k, shared=(), eligible=None):
     """Every expert on every token, combined with a [N, E] weight matrix that is
-    zero outside each token's brute-force top-k."""
+    zero outside each token's brute-force top-k (over `eligible`, default all)."""
     G = x @ wr.T + b
     N, E = G.shape
+    elig = np.ones(E, bool) if eligible is None else np.asarray(eligible, bool)
     Wt = np.zeros((N, E))
     for t in range(N):
-        s = sorted(brute_topk(G[t], np.ones(E, bool), k))
+        s = sorted(brute_topk(G[t], elig, k))
         ex = np.exp(G[t, s] - G[t, s].max())
         Wt[t, s] = ex / ex.sum()
     y = np.zeros_like(x)
@@ -419,6 +420,66 @@ def test_both_or_neither_flag_is_treated_live():
     dec2 = np.array([1, 1, 0, 1], np.uint8)      # position 2 neither -> live
     res = lay.iterate(x, live, dec2, 3)
     assert res.classified.bad_flags == 1 and 2 in res.fresh_pos.tolist()
+
+
+def test_refresh_path_recomputes_every_position_over_the_support():
+    """A refresh-path iteration sends every position through the fresh routed
+    path with the block's support: y equals the restricted MoE computed from
+    scratch, every stamp becomes this iteration, and the following iteration
+    reuses the refreshed rows."""
+    N, E, k = 12, 8, 2
+    lay, wr, b, experts, shared = tiny_layer(E=E, H=5, I=4, k=k, tau=0.6, R=None, n_shared=1,
+                                             seed=71, max_positions=N)
+    rng = np.random.default_rng(72)
+    x = rng.normal(size=(N, 5))
+    plan = lay.plan_block(x)
+    assert plan.support_len < E
+    dec = np.zeros(N, np.uint8)
+    for i in range(4):
+        lay.iterate(x + 0.05 * i, 1 - dec, dec, i)
+        dec[rng.choice(np.nonzero(dec == 0)[0], size=3, replace=False)] = 1
+    x4 = x + 0.3
+    res = lay.iterate(x4, 1 - dec, dec, 4, refresh=True)
+    assert res.fresh_pos.size == N and not res.fallback and res.n_edges == k * N
+    assert res.classified.n_reuse == 0 and res.classified.n_forced == 0
+    np.testing.assert_allclose(res.y, masked_dense(x4, wr, b, experts, k, shared, eligible=lay.support_mask),
+                               rtol=1e-12, atol=1e-12)
+    assert np.all(lay.stamp[:N] == 4)
+    x5 = x + 0.4
+    res5 = lay.iterate(x5, 1 - dec, dec, 5)     # no refresh: decoded rows come from the cache
+    assert set(res5.fresh_pos.tolist()) == set(np.nonzero(dec == 0)[0].tolist())
+    for t in np.nonzero(dec == 1)[0]:
+        assert np.array_equal(res5.routed[t], res.routed[t])
+
+
+def test_hot_update_rebuilds_the_support_from_current_logits():
+    """A hot-update iteration rebuilds the support with the block-plan rule from
+    its own input (the same support a new block plan on that input would give)
+    and keeps every cached row, stamp and decoded flag."""
+    N, E, k = 16, 10, 2
+    lay, wr, b, experts, shared = tiny_layer(E=E, H=5, I=4, k=k, tau=0.5, R=None, n_shared=0,
+                                             seed=81, max_positions=N)
+    rng = np.random.default_rng(82)
+    x = rng.normal(size=(N, 5))
+    lay.plan_block(x)
+    old = lay.support_mask.copy()
+    dec = np.zeros(N, np.uint8)
+    lay.iterate(x, 1 - dec, dec, 0)
+    dec[:10] = 1
+    r1 = lay.iterate(x, 1 - dec, dec, 1)
+    stamps = lay.stamp.copy()
+    x2 = rng.normal(size=(N, 5)) * 3.0          # routing moves elsewhere
+    res = lay.iterate(x2, 1 - dec, dec, 2, hot_update=True)
+    ref, *_ = tiny_layer(E=E, H=5, I=4, k=k, tau=0.5, R=None, n_shared=0, seed=81, max_positions=N)
+    ref.plan_block(x2)
+    assert np.array_equal(lay.support_mask, ref.support_mask)
+    assert not np.array_equal(lay.support_mask, old)
+    assert not res.fallback
+    assert set(res.wl_expert.tolist()) <= set(np.nonzero(lay.support_mask)[0].tolist())
+    for t in range(10):                          # stable decoded rows: the cache, untouched
+        assert t not in res.fresh_pos.tolist()
+        assert np.array_equal(res.routed[t], r1.routed[t])
+        assert lay.stamp[t] == stamps[t]
 
 
 # ------------------------------------------------------------------ mutations
