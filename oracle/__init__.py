@@ -10,6 +10,11 @@ from .epoch_moe import (  # noqa: F401
     IterResult,
     LayerOracle,
     PlanResult,
+    Router,
+    chosen_groups,
+    group_scores,
+    route_position,
+    sigmoid,
     classify_positions,
     coverage_threshold,
     dense_moe,

@@ -119,6 +119,100 @@ def near_tie(g_row: np.ndarray, eligible: np.ndarray, k: int, eps: float = 1e-5)
     return bool(np.any(np.abs(np.diff(vals)) <= eps))
 
 
+# ------------------------------------------------------------------ router variants
+
+@dataclasses.dataclass(frozen=True)
+class Router:
+    """How a position's router logits become a selection and its weights.
+
+    "softmax" (default): G = x W_r^T + b; top-k of G over the eligible experts;
+    weights = softmax over the k selected logits.
+
+    "sigmoid_group" (the group-limited rule of routers in the LLaDA2.0 /
+    DeepSeek-V3 family, which [W] "Expert Atlas" step three names as "the
+    model's group-limited top-k rule", applied to the support): G = x W_r^T
+    (no bias); scores s = sigmoid(G); selection scores c = s + b (the bias only
+    steers the selection); the experts form n_group groups of consecutive ids;
+    a group's score is the sum of the two largest c among its eligible experts
+    (one eligible: that c; none: never chosen); the topk_group best groups
+    (score desc, lower group id first) are chosen, and further groups in that
+    order while the chosen ones hold fewer than k eligible experts; the
+    selection is the top-k of c over the eligible experts of the chosen groups
+    (c desc, lower id first); weights = s of the selected experts divided by
+    their sum."""
+    kind: str = "softmax"
+    n_group: int = 1
+    topk_group: int = 1
+
+
+def sigmoid(z: np.ndarray) -> np.ndarray:
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def group_scores(c: np.ndarray, eligible: np.ndarray, n_group: int) -> np.ndarray:
+    """Per group of consecutive experts: sum of its two largest eligible c
+    (one eligible: that value; none: -inf)."""
+    E = c.shape[0]
+    gs = E // n_group
+    out = np.full(n_group, -np.inf)
+    for g in range(n_group):
+        vals = sorted((c[e] for e in range(g * gs, (g + 1) * gs) if eligible[e]), reverse=True)
+        if vals:
+            out[g] = sum(vals[:2])
+    return out
+
+
+def chosen_groups(scores: np.ndarray, n_elig: np.ndarray, topk_group: int, k: int) -> np.ndarray:
+    """Groups with an eligible expert, ranked by score desc (lower id first):
+    the first topk_group, then more in rank order while the chosen ones hold
+    fewer than k eligible experts."""
+    n_group = scores.shape[0]
+    order = sorted(range(n_group), key=lambda g: (-scores[g], g))
+    chosen = np.zeros(n_group, dtype=bool)
+    n_chosen = held = 0
+    for g in order:
+        if n_elig[g] == 0:
+            continue
+        if n_chosen >= topk_group and held >= k:
+            break
+        chosen[g] = True
+        n_chosen += 1
+        held += int(n_elig[g])
+    return chosen
+
+
+def route_position(g_row: np.ndarray, b_router: np.ndarray, eligible: np.ndarray, k: int,
+                   router: Router) -> Tuple[np.ndarray, np.ndarray]:
+    """(selected experts in selection order, their weights) of one position
+    whose router logits are g_row (bias already included for "softmax")."""
+    if router.kind == "softmax":
+        sel = topk_select(g_row, eligible, k)
+        return sel, renorm_softmax(g_row[sel])
+    s = sigmoid(g_row)
+    c = s + b_router
+    E = g_row.shape[0]
+    gs = E // router.n_group
+    n_elig = np.array([int(np.sum(eligible[g * gs:(g + 1) * gs])) for g in range(router.n_group)])
+    groups = chosen_groups(group_scores(c, eligible, router.n_group), n_elig, router.topk_group, k)
+    in_groups = np.repeat(groups, gs)
+    sel = topk_select(c, eligible & in_groups, k)
+    return sel, s[sel] / np.sum(s[sel])
+
+
+def route_near_tie(g_row: np.ndarray, b_router: np.ndarray, eligible: np.ndarray, k: int,
+                   router: Router, eps: float = 1e-5) -> bool:
+    """near_tie for either router: for "sigmoid_group" the selection scores c
+    and the group scores are both checked."""
+    if router.kind == "softmax":
+        return near_tie(g_row, eligible, k, eps)
+    c = sigmoid(g_row) + b_router
+    if near_tie(c, eligible, k, eps):
+        return True
+    sc = np.sort(group_scores(c, eligible, router.n_group))[::-1]
+    sc = sc[np.isfinite(sc)][: router.topk_group + 1]
+    return bool(np.any(np.abs(np.diff(sc)) <= eps))
+
+
 # ------------------------------------------------------------------ block plan
 
 def hit_counts(G: np.ndarray, k: int) -> np.ndarray:
@@ -257,7 +351,7 @@ class LayerOracle:
                  w_router: np.ndarray, b_router: np.ndarray,
                  expert: Callable[[int], ExpertWeights],
                  shared: Sequence[ExpertWeights] = (), residual: bool = False,
-                 max_positions: int):
+                 max_positions: int, router: Router = Router()):
         self.E = n_experts
         self.k = top_k
         self.tau = tau
@@ -277,13 +371,43 @@ class LayerOracle:
         self.last_iter = -1
         self.support_mask = np.ones(self.E, dtype=bool)
         self.plan: Optional[PlanResult] = None
+        self.router = router
+
+    def logits(self, x: np.ndarray) -> np.ndarray:
+        """Router logits G (the bias is part of G only for the softmax router)."""
+        if self.router.kind == "softmax":
+            return gate_logits(x, self.w_router, self.b_router)
+        return gate_logits(x, self.w_router, np.zeros_like(self.b_router))
+
+    def select(self, g_row: np.ndarray, eligible: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+        return route_position(g_row, self.b_router, eligible, self.k, self.router)
+
+    def weights(self, g_row: np.ndarray, sel: np.ndarray) -> np.ndarray:
+        if self.router.kind == "softmax":
+            return renorm_softmax(g_row[sel])
+        s = sigmoid(g_row[sel])
+        return s / np.sum(s)
+
+    def near_tie(self, g_row: np.ndarray, eligible: np.ndarray, eps: float = 1e-5) -> bool:
+        return route_near_tie(g_row, self.b_router, eligible, self.k, self.router, eps)
+
+    def counts(self, G: np.ndarray) -> np.ndarray:
+        """Block-plan hit counts: each position's selection with every expert eligible."""
+        if self.router.kind == "softmax":
+            return hit_counts(G, self.k)
+        everyone = np.ones(self.E, dtype=bool)
+        cnt = np.zeros(self.E, dtype=np.int64)
+        for t in range(G.shape[0]):
+            for e in self.select(G[t], everyone)[0]:
+                cnt[e] += 1
+        return cnt
 
     # cold path ([W] "cold、hot-update、hot-skip": clear the per-block cache,
     # initialise the live set, build the support of each layer)
     def plan_block(self, x: np.ndarray) -> PlanResult:
         N = x.shape[0]
-        G = gate_logits(x, self.w_router, self.b_router)
-        cnt = hit_counts(G, self.k)
+        G = self.logits(x)
+        cnt = self.counts(G)
         ranked, slen = plan_support(cnt, self.k, self.tau, N)
         self.plan = PlanResult(G, cnt, ranked, slen, coverage_threshold(self.tau, N, self.k))
         self.support_mask = np.zeros(self.E, dtype=bool)
@@ -302,8 +426,8 @@ class LayerOracle:
     # per-position cache, stamps and decoded flags are kept.
     def hot_update(self, x: np.ndarray) -> PlanResult:
         N = x.shape[0]
-        G = gate_logits(x, self.w_router, self.b_router)
-        cnt = hit_counts(G, self.k)
+        G = self.logits(x)
+        cnt = self.counts(G)
         ranked, slen = plan_support(cnt, self.k, self.tau, N)
         self.support_mask = np.zeros(self.E, dtype=bool)
         self.support_mask[ranked[:slen]] = True
@@ -335,7 +459,7 @@ class LayerOracle:
         host_fallback = (not self.planned) or (i != self.last_iter + 1) or (N != self.n_pos)
         if hot_update:
             self.hot_update(x)
-        G = gate_logits(x, self.w_router, self.b_router)
+        G = self.logits(x)
         R = 0 if refresh else self.R
         cl = classify_positions(live, decoded, self.prev_decoded, self.stamp, i, R, host_fallback)
         fallback = host_fallback or cl.anomaly
@@ -346,13 +470,14 @@ class LayerOracle:
         sel = np.zeros((F, self.k), dtype=np.int64)
         w = np.zeros((F, self.k))
         for f, t in enumerate(fresh_pos):
-            s = topk_select(G[t], eligible, self.k)
+            s, wt = self.select(G[t], eligible)
             if adopt is not None:
                 repl = adopt(int(t), s, G[t], eligible)
                 if repl is not None:
                     s = np.asarray(repl, dtype=np.int64)
+                    wt = self.weights(G[t], s)
             sel[f] = s
-            w[f] = renorm_softmax(G[t, s])
+            w[f] = wt
 
         # worklist: every (position, selection) edge, grouped by expert, positions ascending
         edges = sorted(((int(sel[f, j]), int(fresh_pos[f]), j, f)

@@ -482,6 +482,102 @@ def test_hot_update_rebuilds_the_support_from_current_logits():
         assert lay.stamp[t] == stamps[t]
 
 
+# ------------------------------------------------------------------ group-limited sigmoid router
+
+def test_grouped_router_with_one_group_is_plain_topk_of_biased_sigmoid():
+    """One group: the rule reduces to the top-k of sigmoid(G) + b over the
+    eligible experts (brute force), weights = their sigmoid scores normalised."""
+    rng = np.random.default_rng(91)
+    router = oracle.Router("sigmoid_group", 1, 1)
+    for trial in range(300):
+        E = int(rng.integers(3, 9))
+        g = rng.normal(size=E)
+        b = rng.integers(-2, 3, size=E) * 0.25
+        elig = rng.random(E) < 0.8
+        if elig.sum() < 2:
+            elig[:2] = True
+        k = int(rng.integers(1, elig.sum() + 1))
+        sel, w = oracle.route_position(g, b, elig, k, router)
+        c = 1.0 / (1.0 + np.exp(-g)) + b
+        assert set(sel.tolist()) == brute_topk(c, elig, k)
+        s = 1.0 / (1.0 + np.exp(-g[sel]))
+        np.testing.assert_allclose(w, s / s.sum(), rtol=1e-15)
+        assert all(c[a_] > c[b_] or (c[a_] == c[b_] and a_ < b_) for a_, b_ in zip(sel, sel[1:]))
+
+
+def test_grouped_router_properties():
+    """Several groups: the selection is the brute-force top-k over the chosen
+    groups; a chosen group (among the first topk_group) never scores below an
+    unchosen one that holds an eligible expert; the chosen groups hold at least
+    k eligible experts; when every group holds two eligible experts, a common
+    shift of the bias leaves the selection unchanged; the weights ignore the
+    bias."""
+    rng = np.random.default_rng(92)
+    for trial in range(300):
+        n_group = int(rng.choice([2, 4]))
+        gs = int(rng.choice([2, 3]))
+        E = n_group * gs
+        topk_group = int(rng.integers(1, n_group + 1))
+        router = oracle.Router("sigmoid_group", n_group, topk_group)
+        g = rng.normal(size=E)
+        b = rng.normal(size=E) * 0.5
+        elig = rng.random(E) < 0.7
+        if elig.sum() < 2:
+            elig[rng.choice(E, 2, replace=False)] = True
+        k = int(rng.integers(1, min(4, elig.sum()) + 1))
+        sel, w = oracle.route_position(g, b, elig, k, router)
+        c = 1.0 / (1.0 + np.exp(-g)) + b
+        # group scores by sorting each group's eligible scores
+        score = np.full(n_group, -np.inf)
+        for q in range(n_group):
+            v = np.sort(c[q * gs:(q + 1) * gs][elig[q * gs:(q + 1) * gs]])[::-1]
+            if v.size:
+                score[q] = v[:2].sum()
+        groups = set(int(e) // gs for e in sel)
+        in_groups = np.array([e // gs in groups for e in range(E)])
+        n_in = int(np.sum(elig & in_groups))
+        assert len(sel) == k and n_in >= k
+        # every group holding a selected expert is among the best-scoring groups that hold one
+        best = sorted([q for q in range(n_group) if elig[q * gs:(q + 1) * gs].any()],
+                      key=lambda q: (-score[q], q))
+        assert groups <= set(best[:max(topk_group, len(groups))])
+        chosen = oracle.chosen_groups(score, np.array([elig[q * gs:(q + 1) * gs].sum() for q in range(n_group)]),
+                                      topk_group, k)
+        allowed = elig & np.repeat(chosen, gs)
+        assert set(sel.tolist()) == brute_topk(c, allowed, k)
+        if all(elig[q * gs:(q + 1) * gs].sum() >= 2 for q in range(n_group)):
+            # every group score sums two entries: a common shift keeps every order
+            sel2, w2 = oracle.route_position(g, b + 0.375, elig, k, router)
+            assert np.array_equal(sel, sel2)
+        s = 1.0 / (1.0 + np.exp(-g[sel]))
+        np.testing.assert_allclose(w, s / s.sum(), rtol=1e-15)
+
+
+def test_grouped_router_layer_counts_match_selection():
+    """The block plan of a grouped-router layer counts each position's
+    selection with every expert eligible, and its logits carry no bias."""
+    N, E, k = 10, 8, 2
+    rng = np.random.default_rng(93)
+    wr = rng.normal(size=(E, 5))
+    b = rng.normal(size=E)
+    experts = [(rng.normal(size=(4, 5)), rng.normal(size=(4, 5)), rng.normal(size=(5, 4))) for _ in range(E)]
+    router = oracle.Router("sigmoid_group", 4, 2)
+    lay = oracle.LayerOracle(n_experts=E, top_k=k, tau=0.8, refresh_R=None, w_router=wr, b_router=b,
+                             expert=lambda e: experts[e], max_positions=N, router=router)
+    x = rng.normal(size=(N, 5))
+    plan = lay.plan_block(x)
+    np.testing.assert_allclose(plan.G, x @ wr.T, rtol=1e-15, atol=1e-15)
+    cnt = np.zeros(E, dtype=np.int64)
+    for t in range(N):
+        for e in oracle.route_position(x[t] @ wr.T, b, np.ones(E, bool), k, router)[0]:
+            cnt[e] += 1
+    assert np.array_equal(plan.counts, cnt)
+    res = lay.iterate(x, np.ones(N, np.uint8), np.zeros(N, np.uint8), 0)
+    for f, t in enumerate(res.fresh_pos):
+        sel, w = oracle.route_position(res.G[t], b, lay.support_mask, k, router)
+        assert np.array_equal(res.sel[f], sel)
+
+
 # ------------------------------------------------------------------ mutations
 
 def _pins_pass():
@@ -490,7 +586,11 @@ def _pins_pass():
               test_topk_golden, test_topk_bruteforce, test_plan_golden,
               test_plan_minimal_support_bruteforce, test_iteration_invariants,
               lambda: test_tau1_R1_equals_dense_moe(1),
-              lambda: [test_fresh_schedules_golden(s) for s in load_schedules()]]
+              lambda: [test_fresh_schedules_golden(s) for s in load_schedules()],
+              test_grouped_router_with_one_group_is_plain_topk_of_biased_sigmoid,
+              test_grouped_router_properties, test_grouped_router_layer_counts_match_selection,
+              test_refresh_path_recomputes_every_position_over_the_support,
+              test_hot_update_rebuilds_the_support_from_current_logits]
     for c in checks:
         try:
             c()
@@ -539,6 +639,28 @@ def _mut_stale_strict(live, decoded, prev, stamp, i, R, force):
 CLASSIFY_ORIG = om.classify_positions
 
 
+def _mut_group_top1(c, eligible, n_group):
+    E = c.shape[0]
+    gs = E // n_group
+    out = np.full(n_group, -np.inf)
+    for g in range(n_group):
+        vals = [c[e] for e in range(g * gs, (g + 1) * gs) if eligible[e]]
+        if vals:
+            out[g] = max(vals)
+    return out
+
+
+def _mut_groups_ignore_k(scores, n_elig, topk_group, k):
+    return CHOSEN_ORIG(scores, n_elig, topk_group, 0)
+
+
+CHOSEN_ORIG = om.chosen_groups
+
+
+def _mut_sigmoid_neg(z):
+    return 1.0 / (1.0 + np.exp(z))
+
+
 @pytest.mark.parametrize("name,attr,mutant", [
     ("tie to higher id", "rank_eligible", _mut_rank_desc_ids),
     ("dropped router bias", "gate_logits", _mut_gate_no_bias),
@@ -547,6 +669,9 @@ CLASSIFY_ORIG = om.classify_positions
     ("weights not renormalised", "renorm_softmax", _mut_softmax_unnormalised),
     ("support one too long", "plan_support", _mut_plan_off_by_one),
     ("refresh one iteration late", "classify_positions", _mut_stale_strict),
+    ("group score from the best expert only", "group_scores", _mut_group_top1),
+    ("groups not extended to k eligible experts", "chosen_groups", _mut_groups_ignore_k),
+    ("sigmoid of -G", "sigmoid", _mut_sigmoid_neg),
 ])
 def test_planted_mistakes_are_caught(monkeypatch, name, attr, mutant):
     assert _pins_pass()
