@@ -75,9 +75,20 @@ typedef enum { EPOCH_F32 = 0, EPOCH_BF16 = 1 } epoch_dtype;
  *    iterations old is recomputed (EPOCH_REFRESH_NEVER: never) -- the bounded
  *    age of [W] section "decoded-cache 的刷新周期为什么默认取 5".
  *  residual: nonzero makes y = x + routed + shared (chains a stack of layers).
+ *  router: EPOCH_ROUTER_SOFTMAX (0): G = x W_r^T + b, top-k of G over the
+ *    eligible experts, weights = softmax over the k selected logits.
+ *    EPOCH_ROUTER_SIGMOID_GROUP (1), the group-limited rule that [W] section
+ *    "Expert Atlas" (step three) runs inside the support: G = x W_r^T (no bias);
+ *    scores s = sigmoid(G); selection scores c = s + b; the experts form
+ *    n_group groups of consecutive ids, a group's score being the sum of its two
+ *    best eligible c; the topk_group best groups (and further ones in that order
+ *    while they hold fewer than k eligible experts) are searched for the top-k
+ *    of c; weights = the selected s divided by their sum. The block plan's hit
+ *    counts use the same rule with every expert eligible.
  * Constraints (else EPOCH_EINVAL): 1 <= top_k <= n_experts <= 1024, top_k <= 16;
  *  bf16: H a multiple of 256, I and shared_inter multiples of 128; f32: multiples of 4;
- *  1 <= max_positions <= 16384. */
+ *  1 <= max_positions <= 16384; router 1: 1 <= n_group <= 32, n_experts a
+ *  multiple of n_group, 1 <= topk_group <= n_group (router 0 ignores both). */
 typedef struct {
   int32_t hidden;
   int32_t n_experts;
@@ -90,7 +101,12 @@ typedef struct {
   double tau;
   int32_t refresh_R;
   int32_t residual;
+  int32_t router;
+  int32_t n_group;
+  int32_t topk_group;
 } epoch_layer_config;
+
+enum { EPOCH_ROUTER_SOFTMAX = 0, EPOCH_ROUTER_SIGMOID_GROUP = 1 };
 
 /* Weights, all device pointers of the layer dtype unless noted.
  *  w_router [E][H], b_router [E] (float); w_gate, w_up [E][I][H]; w_down [E][H][I];

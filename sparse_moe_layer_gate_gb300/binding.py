@@ -24,7 +24,8 @@ class epoch_layer_config(C.Structure):
     _fields_ = [("hidden", C.c_int32), ("n_experts", C.c_int32), ("inter", C.c_int32),
                 ("top_k", C.c_int32), ("n_shared", C.c_int32), ("shared_inter", C.c_int32),
                 ("max_positions", C.c_int32), ("dtype", C.c_int32), ("tau", C.c_double),
-                ("refresh_R", C.c_int32), ("residual", C.c_int32)]
+                ("refresh_R", C.c_int32), ("residual", C.c_int32), ("router", C.c_int32),
+                ("n_group", C.c_int32), ("topk_group", C.c_int32)]
 
 
 class epoch_layer_weights(C.Structure):

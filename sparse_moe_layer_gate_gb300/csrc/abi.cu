@@ -67,6 +67,11 @@ bool valid_config(const epoch_layer_config *c) {
   if (c->hidden % q || c->inter % q) return false;
   if (c->dtype == EPOCH_BF16 && c->hidden % kBmDn) return false;  // down tiles cover 256 rows of H
   if (c->n_shared > 0 && c->shared_inter % q) return false;
+  if (c->router != EPOCH_ROUTER_SOFTMAX && c->router != EPOCH_ROUTER_SIGMOID_GROUP) return false;
+  if (c->router == EPOCH_ROUTER_SIGMOID_GROUP &&
+      (c->n_group < 1 || c->n_group > 32 || c->n_experts % c->n_group || c->topk_group < 1 ||
+       c->topk_group > c->n_group))
+    return false;
   return true;
 }
 
@@ -187,7 +192,7 @@ epoch_status run_gate(epoch_layer *L, Dims &d, const void *x, const uint8_t *liv
   }
   EPOCH_TRY(run(L, K_GATE, s, [&] { return launch_gate_simt(d, L->w, L->ws, x, 0, s); }));
   if (d.plan_mode) return EPOCH_OK;
-  return run(L, K_SELECT, s, [&] { return launch_select(d, L->ws, live, decoded, s); });
+  return run(L, K_SELECT, s, [&] { return launch_select(d, L->ws, live, decoded, L->w.b_router, s); });
 }
 
 }  // namespace
@@ -226,6 +231,9 @@ epoch_status epoch_layer_create(const epoch_layer_config *cfg, const epoch_layer
   d.Nmax = cfg->max_positions;
   d.R = cfg->refresh_R;
   d.residual = cfg->residual ? 1 : 0;
+  d.router = cfg->router;
+  d.n_group = cfg->router ? cfg->n_group : 1;
+  d.topk_group = cfg->router ? cfg->topk_group : 1;
   d.tn = L->bf16 ? kTnUp : 0;
   d.cmax = (cfg->max_positions + 31) / 32;
   d.timeout_ns = 2000000000ll;
@@ -341,7 +349,7 @@ epoch_status epoch_moe_iter_path(epoch_layer *L, const void *x, const uint8_t *l
     const int32_t T = static_cast<int32_t>(std::ceil(tau * static_cast<double>(n_pos * L->cfg.top_k)));
     EPOCH_TRY(run(L, K_PLAN_SUPPORT, s, [&] { return launch_plan_support(d, L->ws, T, all, 0, s); }));
     d.plan_mode = 0;
-    EPOCH_TRY(run(L, K_SELECT, s, [&] { return launch_select(d, L->ws, live, decoded, s); }));
+    EPOCH_TRY(run(L, K_SELECT, s, [&] { return launch_select(d, L->ws, live, decoded, L->w.b_router, s); }));
     ++L->n_hot_update;
   } else {
     EPOCH_TRY(run_gate(L, d, x, live, decoded, &x_map_up, s));

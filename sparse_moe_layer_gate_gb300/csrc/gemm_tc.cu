@@ -72,8 +72,10 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint64
 // writes its fp32 partial sums to its shared memory, and after a cluster
 // barrier sums the CS partials of its own TN / CS positions in rank order
 // (fixed order: the result does not depend on timing) straight from the other
-// CTAs' shared memory, adds the bias and writes G. It then classifies those
-// positions and takes the top-k of the fresh ones from the rows it holds.
+// CTAs' shared memory, adds the bias (softmax router; the group-limited
+// sigmoid router keeps G = x W_r^T and adds the bias to its selection scores)
+// and writes G. It then classifies those positions and takes the top-k of the
+// fresh ones from the rows it holds.
 // Splitting H over the cluster gives 128 CTAs for 1024 positions, each
 // streaming 160 KB, instead of a few CTAs streaming all of W_r.
 struct __align__(128) GateParams {
@@ -321,7 +323,7 @@ __global__ void __maxnreg__(104) k_tc_gate(const __grid_constant__ GateParams p)
         }
       float g[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) g[c] = e + c < d.E ? g[c] + s_bias[e + c] : -INFINITY;
+      for (int c = 0; c < 4; ++c) g[c] = e + c < d.E ? (d.router ? g[c] : g[c] + s_bias[e + c]) : -INFINITY;
       *reinterpret_cast<float4 *>(rows + j * E_pad + e) = make_float4(g[0], g[1], g[2], g[3]);
       const int t = t_own + j;
       if (t < d.n_pos && e < d.E) {
@@ -354,7 +356,7 @@ __global__ void __maxnreg__(104) k_tc_gate(const __grid_constant__ GateParams p)
         const int e = lane * EPL + c;
         v[c] = e < E_pad ? rows[j * E_pad + e] : -INFINITY;
       }
-      select_position<EPL>(d, ws, t, v, s_support, force, words, s_scr + 32 * wid);
+      select_position<EPL>(d, ws, t, v, s_support, force, words, s_scr + 32 * wid, s_bias);
     }
   }
   if (trace && tid == 0) {

@@ -96,6 +96,8 @@ struct Dims {
   int32_t cmax;          // words per expert of sel_words: ceil(Nmax / 32)
   int32_t trace;         // nonzero: kernels record per-CTA timelines
   int32_t plan_mode;     // gate kernels: 1 = block plan (logits only), 0 = iteration
+  int32_t router;        // 0: softmax over the selected logits (bias in G); 1: group-limited sigmoid
+  int32_t n_group, topk_group;  // group rule of router 1
   uint32_t seq;          // sequence number of this call (route_done handshake)
   int64_t timeout_ns;
 };
@@ -154,6 +156,7 @@ struct KernelMark {
 cudaError_t launch_gate_simt(const Dims &d, const Weights &w, const Work &ws, const void *x, int bf16,
                              cudaStream_t s);
 cudaError_t launch_select(const Dims &d, const Work &ws, const uint8_t *live, const uint8_t *decoded,
+                          const float *bias,
                           cudaStream_t s);
 cudaError_t launch_plan_topk(const Dims &d, const Weights &w, const Work &ws, cudaStream_t s);
 // clear_state: also reset every stamp and decoded flag (a block plan; not a hot update).

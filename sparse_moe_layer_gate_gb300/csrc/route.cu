@@ -106,14 +106,15 @@ __global__ void k_gate_simt(Dims d, const T *__restrict__ x, const T *__restrict
     for (int h = lane; h < d.H; h += 32) acc = fmaf(to_f32(xr[h]), to_f32(wrow[h]), acc);
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-    if (lane == 0) g[static_cast<size_t>(t) * d.E + e] = acc + bias[e];
+    if (lane == 0) g[static_cast<size_t>(t) * d.E + e] = d.router ? acc : acc + bias[e];
   }
 }
 
 // ---------------------------------------------------------------- block plan
 // Dense top-k of every position over all experts -> hit counts (integer atomics).
 template <int EPL>
-__global__ void k_plan_topk(Dims d, const float *__restrict__ logits, int32_t *__restrict__ counts) {
+__global__ void k_plan_topk(Dims d, const float *__restrict__ logits, const float *__restrict__ bias,
+                            int32_t *__restrict__ counts) {
   __shared__ uint2 s_scr[8][32];  // top-k scratch of each warp (256 threads)
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int lane = lane_id();
@@ -125,8 +126,16 @@ __global__ void k_plan_topk(Dims d, const float *__restrict__ logits, int32_t *_
     for (int c = 0; c < EPL; ++c) ok[c] = lane * EPL + c < d.E;
     int sel;
     float val;
+    if (d.router != 0) {  // the group-limited sigmoid rule, every expert eligible
+#pragma unroll
+      for (int c = 0; c < EPL; ++c) {
+        const int e = lane * EPL + c;
+        v[c] = e < d.E ? 1.f / (1.f + expf(-v[c])) + bias[e] : -INFINITY;
+      }
+      warp_group_limit<EPL>(v, ok, d.E, d.n_group, d.topk_group, d.k);
+    }
     warp_topk<EPL>(v, ok, d.k, &sel, &val, s_scr[warp_id()]);
-    if (lane < d.k) atomicAdd(&counts[sel], 1);
+    if (lane < d.k && sel >= 0) atomicAdd(&counts[sel], 1);
   }
 }
 
@@ -199,7 +208,7 @@ __global__ void __launch_bounds__(1024) k_plan_support(Dims d, Work ws, int32_t 
 // expert eligible.
 template <int EPL>
 __global__ void __launch_bounds__(256) k_select(Dims d, Work ws, const uint8_t *__restrict__ live,
-                                                const uint8_t *__restrict__ decoded) {
+                                                const uint8_t *__restrict__ decoded, const float *__restrict__ bias) {
   const KernelMark mark_(d, ws, K_SELECT);
   __shared__ uint2 s_scr[8][32];  // top-k scratch of each warp
   pdl_wait();
@@ -216,7 +225,7 @@ __global__ void __launch_bounds__(256) k_select(Dims d, Work ws, const uint8_t *
     if (!fresh) continue;
     float v[EPL];
     lane_logits<EPL>(ws.logits + static_cast<size_t>(t) * d.E, d.E, v);
-    select_position<EPL>(d, ws, t, v, ws.support_mask, force, words, s_scr[warp_id()]);
+    select_position<EPL>(d, ws, t, v, ws.support_mask, force, words, s_scr[warp_id()], bias);
   }
 }
 
@@ -940,7 +949,7 @@ cudaError_t launch_plan_topk(const Dims &d, const Weights &w, const Work &ws, cu
   case N: {                                                                            \
     static bool c_ = (prefer_max_shared(k_plan_topk<N>) == cudaSuccess);               \
     (void)c_;                                                                          \
-    k_plan_topk<N><<<blocks, 256, 0, s>>>(d, ws.logits, ws.plan_counts);              \
+    k_plan_topk<N><<<blocks, 256, 0, s>>>(d, ws.logits, w.b_router, ws.plan_counts);              \
     break;                                                                             \
   }
     EPOCH_CASE(1) EPOCH_CASE(2) EPOCH_CASE(4) EPOCH_CASE(8) EPOCH_CASE(16) EPOCH_CASE(32)
@@ -958,7 +967,7 @@ cudaError_t launch_plan_support(const Dims &d, const Work &ws, int32_t threshold
 }
 
 cudaError_t launch_select(const Dims &d, const Work &ws, const uint8_t *live, const uint8_t *decoded,
-                          cudaStream_t s) {
+                          const float *bias, cudaStream_t s) {
   int blocks = (d.n_pos + 7) / 8;
   if (blocks > 2 * num_sms()) blocks = 2 * num_sms();
   switch (epl_for(d.E)) {
@@ -966,7 +975,7 @@ cudaError_t launch_select(const Dims &d, const Work &ws, const uint8_t *live, co
   case N: {                                                                            \
     static bool c_ = (prefer_max_shared(k_select<N>) == cudaSuccess);                  \
     (void)c_;                                                                          \
-    k_select<N><<<blocks, 256, 0, s>>>(d, ws, live, decoded);                          \
+    k_select<N><<<blocks, 256, 0, s>>>(d, ws, live, decoded, bias);                          \
     break;                                                                             \
   }
     EPOCH_CASE(1) EPOCH_CASE(2) EPOCH_CASE(4) EPOCH_CASE(8) EPOCH_CASE(16) EPOCH_CASE(32)

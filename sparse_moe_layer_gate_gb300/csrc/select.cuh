@@ -100,10 +100,15 @@ __device__ __forceinline__ bool classify_and_update(const Dims &d, const Work &w
 // order. Lane l holds the logits v of experts [l*EPL, l*EPL + EPL); `scratch`
 // is the warp's 32 entries of shared memory for the top-k. Writes sel/selw of
 // t and sets bit t of the selected experts' words in `words`.
+//
+// Group-limited sigmoid router (d.router == 1; v holds x W_r^T without the
+// bias): scores s = sigmoid(v), selection scores c = s + bias, the group rule
+// of warp_group_limit, the top-k of c, weights = the selected s divided by
+// their sum in selection order.
 template <int EPL>
 __device__ __forceinline__ void select_position(const Dims &d, const Work &ws, int t, const float (&v)[EPL],
                                                 const uint8_t *support_mask, bool force, uint32_t *words,
-                                                uint2 *scratch) {
+                                                uint2 *scratch, const float *bias) {
   const int lane = lane_id(), e0 = lane * EPL, k = d.k;
   bool ok[EPL];
 #pragma unroll
@@ -112,18 +117,42 @@ __device__ __forceinline__ void select_position(const Dims &d, const Work &ws, i
     ok[c] = e < d.E && (force || support_mask[e] != 0);
   }
   int sel;
-  float val;
-  warp_topk<EPL>(v, ok, k, &sel, &val, scratch);
-  const float top = __shfl_sync(0xffffffffu, val, 0);
-  const float ex = lane < k ? expf(val - top) : 0.f;
-  float denom = 0.f;
-  for (int j = 0; j < k; ++j) denom += __shfl_sync(0xffffffffu, ex, j);
+  float val, wgt;
+  if (d.router == 0) {
+    warp_topk<EPL>(v, ok, k, &sel, &val, scratch);
+    const float top = __shfl_sync(0xffffffffu, val, 0);
+    const float ex = lane < k ? expf(val - top) : 0.f;
+    float denom = 0.f;
+    for (int j = 0; j < k; ++j) denom += __shfl_sync(0xffffffffu, ex, j);
+    wgt = ex / denom;
+  } else {
+    float cs[EPL];
+#pragma unroll
+    for (int c = 0; c < EPL; ++c) {
+      const int e = e0 + c;
+      cs[c] = e < d.E ? 1.f / (1.f + expf(-v[c])) + bias[e] : -INFINITY;
+    }
+    warp_group_limit<EPL>(cs, ok, d.E, d.n_group, d.topk_group, k);
+    warp_topk<EPL>(cs, ok, k, &sel, &val, scratch);
+    // the selected expert's logit, from the lane that owns it
+    const int owner = sel >= 0 ? sel / EPL : 0, idx = sel >= 0 ? sel - owner * EPL : 0;
+    float z = 0.f;
+#pragma unroll
+    for (int c = 0; c < EPL; ++c) {
+      const float o = __shfl_sync(0xffffffffu, v[c], owner);
+      if (c == idx) z = o;
+    }
+    const float sg = lane < k ? 1.f / (1.f + expf(-z)) : 0.f;
+    float denom = 0.f;
+    for (int j = 0; j < k; ++j) denom += __shfl_sync(0xffffffffu, sg, j);
+    wgt = sg / denom;
+  }
   if (lane < k) {
     if (sel < 0 || sel >= d.E) {
       set_error(ws.err, EPOCH_DEVERR_BOUNDS);
     } else {
       ws.sel[static_cast<size_t>(t) * k + lane] = sel;
-      ws.selw[static_cast<size_t>(t) * k + lane] = ex / denom;
+      ws.selw[static_cast<size_t>(t) * k + lane] = wgt;
       atomicOr(&words[static_cast<size_t>(sel) * d.cmax + (t >> 5)], 1u << (t & 31));
     }
   }

@@ -156,4 +156,68 @@ __device__ __forceinline__ void warp_topk(const float (&v)[EPL], const bool (&ok
   }
 }
 
+// Group-limited eligibility (the group rule of sigmoid routers): the E experts
+// form n_group groups of gs = E / n_group consecutive ids. Lane l owns the
+// EPL experts [l*EPL, l*EPL + EPL) with selection scores c (eligible where ok).
+// A group's score is the sum of its two largest eligible c (one eligible: that
+// c); groups with an eligible expert are ranked by score desc, lower group id
+// first; the first topk_group are chosen, and further ones in rank order while
+// the chosen groups hold fewer than k eligible experts. Clears ok[] outside
+// the chosen groups. n_group <= 32.
+template <int EPL>
+__device__ __forceinline__ void warp_group_limit(const float (&c)[EPL], bool (&ok)[EPL], int E, int n_group,
+                                                 int topk_group, int k) {
+  constexpr unsigned kAll = 0xffffffffu;
+  const int lane = lane_id(), gs = E / n_group;
+  float my_score = -INFINITY;  // lane g < n_group: group g's score and eligible count
+  int my_cnt = 0;
+  for (int g = 0; g < n_group; ++g) {
+    unsigned k1 = 0u, k2 = 0u;  // this lane's two best keys in group g (0: none)
+    int cnt = 0;
+#pragma unroll
+    for (int q = 0; q < EPL; ++q) {
+      const int e = lane * EPL + q;
+      if (ok[q] && e / gs == g) {
+        const unsigned key = order_key(c[q]);
+        ++cnt;
+        if (key > k1) {
+          k2 = k1;
+          k1 = key;
+        } else if (key > k2) {
+          k2 = key;
+        }
+      }
+    }
+    const unsigned m1 = __reduce_max_sync(kAll, k1);
+    const unsigned hold = __ballot_sync(kAll, k1 == m1 && k1 != 0u);
+    const int wl = hold ? __ffs(hold) - 1 : -1;
+    const unsigned m2 = __reduce_max_sync(kAll, lane == wl ? k2 : k1);  // the best key left
+    const int n = static_cast<int>(__reduce_add_sync(kAll, static_cast<unsigned>(cnt)));
+    if (lane == g) {
+      my_cnt = n;
+      my_score = m1 == 0u ? -INFINITY : (m2 == 0u ? key_value(m1) : key_value(m1) + key_value(m2));
+    }
+  }
+  int r = 0;  // rank among the groups holding an eligible expert
+#pragma unroll 4
+  for (int i = 0; i < 32; ++i) {
+    const float os = __shfl_sync(kAll, my_score, i);
+    const int oc = __shfl_sync(kAll, my_cnt, i);
+    r += (i < n_group && oc > 0) && (os > my_score || (os == my_score && i < lane));
+  }
+  int before = 0;  // eligible experts of the groups ranked before
+#pragma unroll 4
+  for (int i = 0; i < 32; ++i) {
+    const int orr = __shfl_sync(kAll, r, i);
+    const int oc = __shfl_sync(kAll, my_cnt, i);
+    before += (i < n_group && oc > 0 && orr < r) ? oc : 0;
+  }
+  const unsigned chosen = __ballot_sync(kAll, lane < n_group && my_cnt > 0 && (r < topk_group || before < k));
+#pragma unroll
+  for (int q = 0; q < EPL; ++q) {
+    const int e = lane * EPL + q;
+    if (ok[q] && !((chosen >> (e / gs)) & 1u)) ok[q] = false;
+  }
+}
+
 }  // namespace epoch

@@ -15,6 +15,7 @@ from . import binding as B
 
 _TORCH_DT = {"bf16": torch.bfloat16, "f32": torch.float32}
 _ABI_DT = {"bf16": B.EPOCH_BF16, "f32": B.EPOCH_F32}
+_ROUTER = {"softmax": 0, "sigmoid_group": 1}  # EPOCH_ROUTER_SOFTMAX, EPOCH_ROUTER_SIGMOID_GROUP
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
@@ -37,7 +38,8 @@ class EpochLayer:
 
     def __init__(self, *, hidden: int, n_experts: int, inter: int, top_k: int, max_positions: int,
                  dtype: str, tau: float, refresh_R: Optional[int], weights: Dict[str, torch.Tensor],
-                 n_shared: int = 0, shared_inter: Optional[int] = None, residual: bool = False):
+                 n_shared: int = 0, shared_inter: Optional[int] = None, residual: bool = False,
+                 router: str = "softmax", n_group: int = 1, topk_group: int = 1):
         self.dtype = dtype
         self.hidden, self.n_experts, self.inter, self.top_k = hidden, n_experts, inter, top_k
         self.n_shared = n_shared
@@ -47,7 +49,8 @@ class EpochLayer:
             shared_inter=(shared_inter or inter) if n_shared else 0, max_positions=max_positions,
             dtype=_ABI_DT[dtype], tau=float(tau),
             refresh_R=B.EPOCH_REFRESH_NEVER if refresh_R is None else int(refresh_R),
-            residual=1 if residual else 0)
+            residual=1 if residual else 0, router=_ROUTER[router], n_group=int(n_group),
+            topk_group=int(topk_group))
         tdt = _TORCH_DT[dtype]
         for name, t in weights.items():
             if not (t.is_cuda and t.is_contiguous()):
@@ -261,4 +264,4 @@ def layer_for_workload(wl, layer_index: int = 0, device="cuda", threads: Optiona
     return EpochLayer(hidden=wl.hidden, n_experts=wl.n_experts, inter=wl.inter, top_k=wl.top_k,
                       max_positions=max_positions or wl.n_pos, dtype=wl.dtype, tau=wl.tau, refresh_R=wl.refresh_R,
                       weights=weights, n_shared=wl.n_shared, shared_inter=wl.shared_inter,
-                      residual=wl.residual)
+                      residual=wl.residual, router=wl.router, n_group=wl.n_group, topk_group=wl.topk_group)

@@ -9,7 +9,8 @@ distribution:
 * hidden states: x_0 ~ N(0, 1); x_{i+1} = x_i + 0.05 * N(0, 1) per iteration;
 * router weight W_r ~ N(0, std = 1/sqrt(H)); router bias b_e = log of a
   Zipf(s) probability at a seeded rank permutation of the experts (or, for
-  tie tests, minus the rank's group index, groups of `bias_levels` ranks);
+  tie tests, minus the rank's group index, groups of `bias_levels` ranks;
+  for the group-limited sigmoid router, 0.05 x the centred log-probability);
 * expert weights W_gate, W_up ~ N(0, 1/sqrt(H)), W_down ~ N(0, 1/sqrt(I));
 * commit schedules: per block of 32 positions, a number of still-live
   positions is committed after each iteration, chosen by a seeded U(0, 1)
@@ -54,6 +55,9 @@ class Workload:
     layers: int = 1
     residual: bool = False  # y = x + routed + shared (used to chain a stack)
     bias_levels: Optional[int] = None  # router bias in groups of this many equal values (exact ties)
+    router: str = "softmax"  # or "sigmoid_group" (group-limited sigmoid router)
+    n_group: int = 1
+    topk_group: int = 1
     description: str = ""
 
     @property
@@ -152,6 +156,11 @@ def router_payload(wl: Workload, layer: int = 0):
     if wl.bias_levels:
         # experts of ranks [1, levels] share bias 0, the next `levels` ranks -1, ...
         bias = (-np.floor((ranks - 1) / wl.bias_levels)).astype(np.float32)
+    elif wl.router == "sigmoid_group":
+        # a selection bias on sigmoid scores in (0, 1): the same Zipf ranks,
+        # centred and scaled to a spread of a few tenths
+        lp = -wl.zipf_s * np.log(ranks.astype(np.float64))
+        bias = (0.05 * (lp - lp.mean())).astype(np.float32)
     return w, bias
 
 

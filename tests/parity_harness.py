@@ -49,7 +49,8 @@ def oracle_layer(wl, layer_index: int = 0, max_positions: Optional[int] = None) 
     return oracle.LayerOracle(n_experts=wl.n_experts, top_k=wl.top_k, tau=wl.tau, refresh_R=wl.refresh_R,
                               w_router=synth.to_f64(wr, wl.dtype), b_router=b.astype(np.float64),
                               expert=expert, shared=shared, residual=wl.residual,
-                              max_positions=max_positions or wl.n_pos)
+                              max_positions=max_positions or wl.n_pos,
+                              router=oracle.Router(wl.router, wl.n_group, wl.topk_group))
 
 
 def tensor_to_f64(t: torch.Tensor) -> np.ndarray:
@@ -104,7 +105,7 @@ def check_plan(orc: oracle.LayerOracle, gplan: dict, x0: np.ndarray, wl, rep: Re
     counts_same = np.array_equal(gplan["plan_counts"], op.counts)
     if not (same and counts_same):
         everyone = np.ones(wl.n_experts, dtype=bool)
-        ties = [t for t in range(x0.shape[0]) if oracle.near_tie(op.G[t], everyone, wl.top_k, NEAR_TIE)]
+        ties = [t for t in range(x0.shape[0]) if orc.near_tie(op.G[t], everyone, NEAR_TIE)]
         if ties:
             rep.near_ties.append(f"{tag} plan: near-tie at positions {ties[:8]}; adopting GPU support")
             orc.adopt_support(gids, glen)
@@ -123,7 +124,7 @@ def check_hot_update(orc: oracle.LayerOracle, gplan: dict, x0: np.ndarray, wl, r
     same = glen == op.support_len and np.array_equal(gids[:glen], op.ranked[:glen])
     if not (same and np.array_equal(gplan["plan_counts"], op.counts)):
         everyone = np.ones(wl.n_experts, dtype=bool)
-        ties = [t for t in range(x0.shape[0]) if oracle.near_tie(op.G[t], everyone, wl.top_k, NEAR_TIE)]
+        ties = [t for t in range(x0.shape[0]) if orc.near_tie(op.G[t], everyone, NEAR_TIE)]
         if ties:
             rep.near_ties.append(f"{tag} hot update: near-tie at positions {ties[:8]}; adopting GPU support")
             orc.adopt_support(gids, glen)
@@ -141,7 +142,7 @@ def check_iteration(orc, step: GpuStep, live, dec, i: int, wl, rep: Report, tag:
         mine = gsel.get(t)
         if mine is None or np.array_equal(mine, s):
             return None
-        if oracle.near_tie(g_row, eligible, wl.top_k, NEAR_TIE):
+        if orc.near_tie(g_row, eligible, NEAR_TIE):
             rep.near_ties.append(f"{tag} i={i} t={t}: gpu {list(mine)} oracle {list(s)} (near-tie)")
             return mine
         rep.mismatches.append(f"{tag} i={i} t={t}: selection gpu {list(mine)} oracle {list(s)}")

@@ -128,6 +128,24 @@ def test_hot_update_and_refresh_paths(name):
     lay.close()
 
 
+@pytest.mark.parametrize("name", ["tiny_bf16_grouped", "e256_bf16_grouped", "tiny_fp32_grouped"])
+def test_group_limited_sigmoid_router(name):
+    """Group-limited sigmoid router: selection on sigmoid scores plus the bias
+    within the best groups, weights from the selected sigmoid scores; block
+    plan counts by the same rule."""
+    wl = {
+        "tiny_bf16_grouped": TINY_BF16.replace(name=name, wid=9, router="sigmoid_group", n_group=4, topk_group=2,
+                                               iters=6),
+        "e256_bf16_grouped": TINY_BF16.replace(name=name, wid=10, n_experts=256, top_k=8, tau=0.95,
+                                               router="sigmoid_group", n_group=8, topk_group=4, iters=6),
+        "tiny_fp32_grouped": synth.WORKLOADS["tiny_fp32"].replace(name=name, wid=11, router="sigmoid_group",
+                                                                   n_group=4, topk_group=2, iters=6),
+    }[name]
+    rep = block_parity(wl)
+    assert_clean(rep)
+    assert rep.iterations == 6
+
+
 def test_tau1_R1_is_dense_moe():
     """tau = 1 and R = 1: every position fresh with every expert eligible, so the
     layer equals the dense MoE formula at every iteration."""
