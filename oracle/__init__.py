@@ -9,7 +9,10 @@ live in the separate ``synth`` package).
 from .epoch_moe import (  # noqa: F401
     IterResult,
     LayerOracle,
+    AtlasResult,
     PlanResult,
+    atlas_support,
+    softmax_rows,
     Router,
     chosen_groups,
     group_scores,

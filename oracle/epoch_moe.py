@@ -58,7 +58,10 @@ fresh-set schedules (tests/golden/), closed-form silu values, the dense-MoE
 special case (tau = 1, R = 1) against an all-experts masked formulation, the
 cache/staleness invariants, and the hot-update and refresh paths (the rebuilt
 support equals a block plan on the same input; a refresh iteration equals a
-from-scratch restricted MoE on every position). Outputs after many iterations with reused rows are
+from-scratch restricted MoE on every position), the group-limited sigmoid
+router (its one-group reduction to a brute-force top-k, group properties), and
+the Expert Atlas planner (a hand-worked example, its no-floor and all-experts
+special cases, and |U| recomputed independently). Outputs after many iterations with reused rows are
 pinned only through those invariants.
 """
 from __future__ import annotations
@@ -248,6 +251,93 @@ def plan_support(cnt: np.ndarray, k: int, tau: float, n_pos: int) -> Tuple[np.nd
         covered += int(cnt[ranked[j]])
         j += 1
     return ranked, min(max(j, k), E)
+
+
+# ------------------------------------------------------------------ Expert Atlas planner
+
+@dataclasses.dataclass
+class AtlasResult:
+    support: np.ndarray      # expert ids in the order they entered the support
+    covered_ok: bool         # |U| <= (1 - q) N at the end
+    n_under: int             # |U|, tokens below their coverage floor
+    rounds: int              # repair rounds run
+    popularity: np.ndarray   # p_e
+
+
+def softmax_rows(G: np.ndarray) -> np.ndarray:
+    """Dense router probabilities of every position over all experts."""
+    m = np.max(G, axis=1, keepdims=True)
+    ex = np.exp(G - m)
+    return ex / np.sum(ex, axis=1, keepdims=True)
+
+
+def atlas_support(G: np.ndarray, k: int, m: int, B: int, alpha: float, q: float, beta: float,
+                  c: int) -> AtlasResult:
+    """The Expert Atlas planner ([W] section "Expert Atlas"), for the softmax router.
+
+    Extended candidates: each token's top K_ext = k + m experts by logit (lower
+    id first on ties), with weights W[t, j] = the dense router probability of
+    candidate j. Coverage floor r_t = alpha * (mass of the token's top-k
+    candidates); covered mass C_t(S) = sum of W[t, j] over candidates in S;
+    under-covered tokens U = {t : C_t < r_t}. Step one: the B experts of
+    largest popularity p_e = sum of W over the candidate edges to e (lower id
+    first on ties), or the k most popular when B < k (every token must still
+    be able to select k experts). Step two, while |U| > (1 - q) N: for every
+    expert e not in S, G_e = sum over t in U and candidates j of t pointing to
+    e of min(W[t, j], r_t - C_t), and H_e = number of t in U with C_t + (t's
+    candidate mass on e) >= r_t; the at most c experts of largest positive
+    score H_e + beta G_e (lower id first on ties) join S; the loop ends when no
+    score is positive."""
+    N, E = G.shape
+    K = min(k + m, E)
+    P = softmax_rows(G)
+    cand = np.zeros((N, K), dtype=np.int64)
+    W = np.zeros((N, K))
+    for t in range(N):
+        cand[t] = rank_eligible(G[t], np.ones(E, dtype=bool))[:K]
+        W[t] = P[t, cand[t]]
+    r = alpha * W[:, :k].sum(axis=1)
+    pop = np.zeros(E)
+    for t in range(N):
+        for j in range(K):
+            pop[cand[t, j]] += W[t, j]
+    by_pop = sorted(range(E), key=lambda e: (-pop[e], e))
+    support = list(by_pop[:min(max(B, k), E)])
+    in_s = np.zeros(E, dtype=bool)
+    in_s[support] = True
+
+    def coverage():
+        return np.array([sum(W[t, j] for j in range(K) if in_s[cand[t, j]]) for t in range(N)])
+
+    rounds = 0
+    C = coverage()
+    under = [t for t in range(N) if C[t] < r[t]]
+    while len(under) > (1.0 - q) * N:
+        Gs = np.zeros(E)
+        Hs = np.zeros(E)
+        for t in under:
+            mass = {}
+            for j in range(K):
+                e = int(cand[t, j])
+                if in_s[e]:
+                    continue
+                Gs[e] += min(W[t, j], r[t] - C[t])
+                mass[e] = mass.get(e, 0.0) + W[t, j]
+            for e, w in mass.items():
+                if C[t] + w >= r[t]:
+                    Hs[e] += 1
+        score = Hs + beta * Gs
+        pos = [e for e in range(E) if not in_s[e] and score[e] > 0]
+        if not pos:
+            break
+        add = sorted(pos, key=lambda e: (-score[e], e))[:c]
+        for e in add:
+            in_s[e] = True
+            support.append(e)
+        rounds += 1
+        C = coverage()
+        under = [t for t in range(N) if C[t] < r[t]]
+    return AtlasResult(np.array(support, dtype=np.int64), len(under) <= (1.0 - q) * N, len(under), rounds, pop)
 
 
 # ------------------------------------------------------------------ liveness

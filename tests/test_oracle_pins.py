@@ -578,6 +578,68 @@ def test_grouped_router_layer_counts_match_selection():
         assert np.array_equal(res.sel[f], sel)
 
 
+# ------------------------------------------------------------------ Expert Atlas planner
+
+def test_atlas_hand_worked_example():
+    """Three tokens, four experts, k = 1, m = 1, B = 1, alpha = 1, q = 1, beta = 1,
+    c = 1, logits = log of these router probabilities:
+        t0 [.5 .3 .1 .1]  candidates e0 (.5), e1 (.3)  floor .5
+        t1 [.1 .6 .2 .1]  candidates e1 (.6), e2 (.2)  floor .6
+        t2 [.1 .1 .2 .6]  candidates e3 (.6), e2 (.2)  floor .6
+    Popularity e0 .5, e1 .9, e2 .4, e3 .6 -> S = {e1}; covered t0 .3, t1 .6, t2 0,
+    so U = {t0, t2}. Round 1: e0: G = min(.5, .2) = .2, H = 1 (.3 + .5 >= .5),
+    score 1.2; e2: G = .2, H = 0, score .2; e3: G = .6, H = 1 (0 + .6 >= .6),
+    score 1.6 -> e3 joins. U = {t0}. Round 2: e0 scores 1.2 -> joins; U empty.
+    Worked by hand from the formulas of the "Expert Atlas" section."""
+    P = np.array([[.5, .3, .1, .1], [.1, .6, .2, .1], [.1, .1, .2, .6]])
+    res = oracle.atlas_support(np.log(P), k=1, m=1, B=1, alpha=1.0, q=1.0, beta=1.0, c=1)
+    assert res.support.tolist() == [1, 3, 0]
+    assert res.rounds == 2 and res.covered_ok and res.n_under == 0
+    np.testing.assert_allclose(res.popularity, [.5, .9, .4, .6], rtol=1e-12)
+
+
+def _atlas_under(G, k, m, alpha, support):
+    """|U| for a support, recomputed with vectorised numpy."""
+    E = G.shape[1]
+    P = np.exp(G - G.max(axis=1, keepdims=True))
+    P /= P.sum(axis=1, keepdims=True)
+    order = np.lexsort((np.broadcast_to(np.arange(E), G.shape), -G), axis=1)[:, :k + m]
+    W = np.take_along_axis(P, order, axis=1)
+    inside = np.isin(order, support)
+    return int(np.sum((W * inside).sum(axis=1) < alpha * W[:, :k].sum(axis=1)))
+
+
+def test_atlas_special_cases_and_invariants():
+    rng = np.random.default_rng(101)
+    for trial in range(60):
+        N, E = int(rng.integers(4, 40)), int(rng.integers(4, 20))
+        k = int(rng.integers(1, min(4, E) + 1))
+        m = int(rng.integers(0, 4))
+        B = int(rng.integers(1, E + 1))
+        alpha, q = float(rng.uniform(0.3, 1.0)), float(rng.uniform(0.5, 1.0))
+        beta, c = float(rng.uniform(0.1, 2.0)), int(rng.integers(1, 4))
+        G = rng.normal(size=(N, E)) * 2
+        res = oracle.atlas_support(G, k, m, B, alpha, q, beta, c)
+        sup = res.support.tolist()
+        assert len(set(sup)) == len(sup) and len(sup) >= min(k, E)
+        assert len(sup) <= min(max(B, k), E) + c * res.rounds
+        n_under = _atlas_under(G, k, m, alpha, sup)
+        assert n_under == res.n_under
+        assert res.covered_ok == (n_under <= (1 - q) * N)
+        # no floor: the B most popular experts, nothing repaired
+        r0 = oracle.atlas_support(G, k, m, B, 0.0, q, beta, c)
+        P = np.exp(G - G.max(axis=1, keepdims=True))
+        P /= P.sum(axis=1, keepdims=True)
+        order = np.lexsort((np.broadcast_to(np.arange(E), G.shape), -G), axis=1)[:, :min(k + m, E)]
+        pop = np.zeros(E)
+        np.add.at(pop, order.ravel(), np.take_along_axis(P, order, axis=1).ravel())
+        top = sorted(range(E), key=lambda e: (-pop[e], e))[:max(B, k)]
+        assert r0.rounds == 0 and set(r0.support.tolist()) == set(top)
+        # every expert from the start: nothing under-covered
+        rall = oracle.atlas_support(G, k, m, E, alpha, q, beta, c)
+        assert rall.rounds == 0 and rall.n_under == 0 and len(rall.support) == E
+
+
 # ------------------------------------------------------------------ mutations
 
 def _pins_pass():
@@ -590,7 +652,8 @@ def _pins_pass():
               test_grouped_router_with_one_group_is_plain_topk_of_biased_sigmoid,
               test_grouped_router_properties, test_grouped_router_layer_counts_match_selection,
               test_refresh_path_recomputes_every_position_over_the_support,
-              test_hot_update_rebuilds_the_support_from_current_logits]
+              test_hot_update_rebuilds_the_support_from_current_logits,
+              test_atlas_hand_worked_example, test_atlas_special_cases_and_invariants]
     for c in checks:
         try:
             c()
