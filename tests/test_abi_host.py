@@ -58,6 +58,13 @@ def test_workspace_size_and_config_validation(lib):
         assert B.epoch_workspace_bytes(good_cfg(**b)) == 0, b
     # fp32 layers only need multiples of 4
     assert B.epoch_workspace_bytes(good_cfg(dtype=B.EPOCH_F32, hidden=256, inter=132, shared_inter=132)) > 0
+    # router variants: the group-limited sigmoid router needs a valid group shape
+    assert B.epoch_workspace_bytes(good_cfg(router=1, n_group=8, topk_group=4)) > 0
+    assert B.epoch_workspace_bytes(good_cfg(router=0, n_group=0, topk_group=0)) > 0  # ignored
+    for b in [dict(router=2), dict(router=-1), dict(router=1, n_group=0, topk_group=1),
+              dict(router=1, n_group=33, topk_group=1), dict(router=1, n_group=3, topk_group=1),
+              dict(router=1, n_group=8, topk_group=0), dict(router=1, n_group=8, topk_group=9)]:
+        assert B.epoch_workspace_bytes(good_cfg(**b)) == 0, b
 
 
 def test_invalid_arguments_return_einval(lib):
@@ -76,6 +83,8 @@ def test_invalid_arguments_return_einval(lib):
                                   C.byref(out)) == B.EPOCH_EINVAL  # workspace too small
     assert lib.epoch_plan_block(None, C.c_void_p(4096), 32, None) == B.EPOCH_EINVAL
     assert lib.epoch_moe_iter(None, 4096, 4096, 4096, 32, 0, 4096, None) == B.EPOCH_EINVAL
+    assert lib.epoch_moe_iter_path(None, 4096, 4096, 4096, 32, 0, 1, 4096, None) == B.EPOCH_EINVAL
+    assert lib.epoch_path_counters_ex(None, None, None) == B.EPOCH_EINVAL
     assert lib.epoch_block_end(None) == B.EPOCH_EINVAL
     assert lib.epoch_get_status(None, None, None) == B.EPOCH_EINVAL
     assert lib.epoch_read_stats(None, None, None) == B.EPOCH_EINVAL
