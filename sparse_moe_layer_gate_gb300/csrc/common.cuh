@@ -133,20 +133,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
       : "memory");
 }
 
-// Four rows of a 2-D tensor map whose box is one row high (tile::gather4): rows
-// r0..r3 of columns [c0, c0 + box width) land one after another at dst, each
-// with the map's swizzle as it applies at its shared-memory address (so four
-// gathers at dst, dst + 512, ... fill a 128-byte-swizzled K-major tile exactly
-// as one tiled load of the same rows would).
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t r0, int32_t r1,
-                                            int32_t r2, int32_t r3, uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar), "l"(policy)
-      : "memory");
-}
-
 // ------------------------------------------------------------------ thread-block clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
