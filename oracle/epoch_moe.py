@@ -46,6 +46,9 @@ Readings taken where the pages are silent:
     iteration) and keeps the support;
   * hot-update: the support is rebuilt with the block-plan rule from the
     current iteration's logits; cache, stamps and decoded flags are kept;
+  * per-request supports (optional): every request_size consecutive positions
+    form one request with its own plan (its own counts and threshold), and a
+    position selects within its request's support;
   * the expert is SwiGLU: E(x) = W_down (silu(W_gate x) * (W_up x)), silu(z) = z / (1 + e^-z);
   * a position flagged both live and decoded, or neither, is treated as live;
     a decoded -> live transition is an anomaly that makes the whole iteration
@@ -61,7 +64,8 @@ support equals a block plan on the same input; a refresh iteration equals a
 from-scratch restricted MoE on every position), the group-limited sigmoid
 router (its one-group reduction to a brute-force top-k, group properties), and
 the Expert Atlas planner (a hand-worked example, its no-floor and all-experts
-special cases, and |U| recomputed independently). Outputs after many iterations with reused rows are
+special cases, and |U| recomputed independently), and per-request supports (a
+batch of requests equals one independent layer per request). Outputs after many iterations with reused rows are
 pinned only through those invariants.
 """
 from __future__ import annotations
@@ -441,7 +445,7 @@ class LayerOracle:
                  w_router: np.ndarray, b_router: np.ndarray,
                  expert: Callable[[int], ExpertWeights],
                  shared: Sequence[ExpertWeights] = (), residual: bool = False,
-                 max_positions: int, router: Router = Router()):
+                 max_positions: int, router: Router = Router(), request_size: Optional[int] = None):
         self.E = n_experts
         self.k = top_k
         self.tau = tau
@@ -462,6 +466,11 @@ class LayerOracle:
         self.support_mask = np.ones(self.E, dtype=bool)
         self.plan: Optional[PlanResult] = None
         self.router = router
+        # per-request supports: every request_size consecutive positions are one
+        # request (one diffusion block) with its own plan; None = one support
+        self.request_size = request_size
+        self.request_masks: Optional[np.ndarray] = None
+        self.request_plans: List[PlanResult] = []
 
     def logits(self, x: np.ndarray) -> np.ndarray:
         """Router logits G (the bias is part of G only for the softmax router)."""
@@ -494,14 +503,41 @@ class LayerOracle:
 
     # cold path ([W] "cold、hot-update、hot-skip": clear the per-block cache,
     # initialise the live set, build the support of each layer)
+    def _supports(self, G: np.ndarray) -> PlanResult:
+        """The plan rule on G: one support, or one per request (each request's
+        own positions, counts and threshold); support_mask is then their union."""
+        N = G.shape[0]
+        cnt = self.counts(G)
+        if self.request_size is None:
+            ranked, slen = plan_support(cnt, self.k, self.tau, N)
+            self.support_mask = np.zeros(self.E, dtype=bool)
+            self.support_mask[ranked[:slen]] = True
+            return PlanResult(G, cnt, ranked, slen, coverage_threshold(self.tau, N, self.k))
+        rs = self.request_size
+        n_req = (N + rs - 1) // rs
+        self.request_masks = np.zeros((n_req, self.E), dtype=bool)
+        self.request_plans = []
+        for r in range(n_req):
+            Gr = G[r * rs:min(N, (r + 1) * rs)]
+            cr = self.counts(Gr)
+            ranked, slen = plan_support(cr, self.k, self.tau, Gr.shape[0])
+            self.request_masks[r, ranked[:slen]] = True
+            self.request_plans.append(PlanResult(Gr, cr, ranked, slen,
+                                                 coverage_threshold(self.tau, Gr.shape[0], self.k)))
+        self.support_mask = self.request_masks.any(axis=0)
+        union = np.nonzero(self.support_mask)[0]
+        return PlanResult(G, cnt, union, int(union.size), coverage_threshold(self.tau, rs, self.k))
+
+    def eligible_for(self, t: int) -> np.ndarray:
+        """Experts position t may select (outside a fallback)."""
+        if self.request_size is None:
+            return self.support_mask
+        return self.request_masks[t // self.request_size]
+
     def plan_block(self, x: np.ndarray) -> PlanResult:
         N = x.shape[0]
         G = self.logits(x)
-        cnt = self.counts(G)
-        ranked, slen = plan_support(cnt, self.k, self.tau, N)
-        self.plan = PlanResult(G, cnt, ranked, slen, coverage_threshold(self.tau, N, self.k))
-        self.support_mask = np.zeros(self.E, dtype=bool)
-        self.support_mask[ranked[:slen]] = True
+        self.plan = self._supports(G)
         self.stamp[:] = -1
         self.prev_decoded[:] = False
         self.cache[:] = 0.0
@@ -515,13 +551,7 @@ class LayerOracle:
     # counter expires). Same rule as the block plan, on this iteration's x; the
     # per-position cache, stamps and decoded flags are kept.
     def hot_update(self, x: np.ndarray) -> PlanResult:
-        N = x.shape[0]
-        G = self.logits(x)
-        cnt = self.counts(G)
-        ranked, slen = plan_support(cnt, self.k, self.tau, N)
-        self.support_mask = np.zeros(self.E, dtype=bool)
-        self.support_mask[ranked[:slen]] = True
-        return PlanResult(G, cnt, ranked, slen, coverage_threshold(self.tau, N, self.k))
+        return self._supports(self.logits(x))
 
     def adopt_support(self, ranked: np.ndarray, slen: int) -> None:
         """Replace the plan's support (used after a logged near-tie at plan time)."""
@@ -553,13 +583,14 @@ class LayerOracle:
         R = 0 if refresh else self.R
         cl = classify_positions(live, decoded, self.prev_decoded, self.stamp, i, R, host_fallback)
         fallback = host_fallback or cl.anomaly
-        eligible = np.ones(self.E, dtype=bool) if fallback else self.support_mask
+        everyone = np.ones(self.E, dtype=bool)
 
         fresh_pos = np.nonzero(cl.fresh)[0]
         F = fresh_pos.shape[0]
         sel = np.zeros((F, self.k), dtype=np.int64)
         w = np.zeros((F, self.k))
         for f, t in enumerate(fresh_pos):
+            eligible = everyone if fallback else self.eligible_for(int(t))
             s, wt = self.select(G[t], eligible)
             if adopt is not None:
                 repl = adopt(int(t), s, G[t], eligible)

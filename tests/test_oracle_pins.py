@@ -578,6 +578,62 @@ def test_grouped_router_layer_counts_match_selection():
         assert np.array_equal(res.sel[f], sel)
 
 
+# ------------------------------------------------------------------ per-request supports
+
+def test_per_request_supports_equal_independent_layers():
+    """A batch of requests, each with its own support (its own diffusion block's
+    plan), gives every position the same selections and outputs as running one
+    layer per request on that request's positions alone."""
+    E, H, I, k, rs, n_req = 10, 5, 4, 2, 8, 3
+    N = rs * n_req
+    rng = np.random.default_rng(111)
+    wr = rng.normal(size=(E, H))
+    b = rng.normal(size=E)
+    experts = [(rng.normal(size=(I, H)), rng.normal(size=(I, H)), rng.normal(size=(H, I))) for _ in range(E)]
+    shared = [(rng.normal(size=(I, H)), rng.normal(size=(I, H)), rng.normal(size=(H, I)))]
+
+    def make(n, request_size=None):
+        return oracle.LayerOracle(n_experts=E, top_k=k, tau=0.6, refresh_R=3, w_router=wr, b_router=b,
+                                  expert=lambda e: experts[e], shared=shared, max_positions=n,
+                                  request_size=request_size)
+    batched = make(N, rs)
+    singles = [make(rs) for _ in range(n_req)]
+    # requests routed to different parts of the expert set
+    x = np.concatenate([rng.normal(size=(rs, H)) + 2.0 * rng.normal(size=H) for _ in range(n_req)])
+    batched.plan_block(x)
+    for r in range(n_req):
+        singles[r].plan_block(x[r * rs:(r + 1) * rs])
+        assert np.array_equal(batched.request_masks[r], singles[r].support_mask)
+    assert len({tuple(m) for m in batched.request_masks}) > 1   # the supports differ
+    dec = np.zeros(N, np.uint8)
+    for i in range(6):
+        xi = x + 0.05 * i
+        res = batched.iterate(xi, 1 - dec, dec, i)
+        assert not res.fallback
+        sel_b = {int(t): res.sel[f].tolist() for f, t in enumerate(res.fresh_pos)}
+        for r in range(n_req):
+            sl = slice(r * rs, (r + 1) * rs)
+            rr = singles[r].iterate(xi[sl], 1 - dec[sl], dec[sl], i)
+            np.testing.assert_allclose(res.y[sl], rr.y, rtol=1e-13, atol=1e-13)
+            for f, t in enumerate(rr.fresh_pos):
+                assert sel_b[r * rs + int(t)] == rr.sel[f].tolist()
+        live = np.nonzero(dec == 0)[0]
+        if live.size:
+            dec[rng.choice(live, size=min(4, live.size), replace=False)] = 1
+
+
+def test_one_request_is_the_single_support():
+    lay, wr, b, experts, shared = tiny_layer(E=8, k=2, tau=0.7, R=2, seed=121, max_positions=12)
+    one = oracle.LayerOracle(n_experts=8, top_k=2, tau=0.7, refresh_R=2, w_router=wr, b_router=b,
+                             expert=lambda e: experts[e], max_positions=12, request_size=12)
+    x = np.random.default_rng(122).normal(size=(12, 5))
+    lay.plan_block(x)
+    one.plan_block(x)
+    assert np.array_equal(lay.support_mask, one.request_masks[0])
+    live, dec = np.ones(12, np.uint8), np.zeros(12, np.uint8)
+    np.testing.assert_allclose(lay.iterate(x, live, dec, 0).y, one.iterate(x, live, dec, 0).y, rtol=1e-14)
+
+
 # ------------------------------------------------------------------ Expert Atlas planner
 
 def test_atlas_hand_worked_example():
@@ -653,7 +709,8 @@ def _pins_pass():
               test_grouped_router_properties, test_grouped_router_layer_counts_match_selection,
               test_refresh_path_recomputes_every_position_over_the_support,
               test_hot_update_rebuilds_the_support_from_current_logits,
-              test_atlas_hand_worked_example, test_atlas_special_cases_and_invariants]
+              test_atlas_hand_worked_example, test_atlas_special_cases_and_invariants,
+              test_per_request_supports_equal_independent_layers, test_one_request_is_the_single_support]
     for c in checks:
         try:
             c()
