@@ -9,6 +9,8 @@
  * per-position routed-output cache with stamps, and the scratch of one
  * iteration. A caller runs, per diffusion block:
  *     epoch_plan_block  (cold path, once)  ->  epoch_moe_iter (i = 0, 1, ...)  ->  epoch_block_end
+ * where any iteration may instead take the hot-update or refresh path
+ * (epoch_moe_iter_path).
  *
  * Conventions for every entry point:
  *  - Pointers named *_dev or documented as "device" are CUDA device pointers in
