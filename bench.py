@@ -73,6 +73,36 @@ def workload_config(wl, n_gpus):
             "l2": "flushed (256 MiB write) before every iteration, outside the timed region"}
 
 
+# ---------------------------------------------------------------- device layers
+
+def device_weights(wl, layer_index=0, device="cuda"):
+    """The workload's weights drawn by synth and uploaded (CUDA tensors by name)."""
+    import torch
+    import synth
+    from sparse_moe_layer_gate_gb300.layer import payload_to_torch
+    wr, b = synth.router_payload(wl, layer_index)
+    wg, wu, wd = synth.experts_payload(wl, layer_index)
+    w = {"w_router": payload_to_torch(wr, wl.dtype, device), "b_router": torch.from_numpy(b).to(device),
+         "w_gate": payload_to_torch(wg, wl.dtype, device), "w_up": payload_to_torch(wu, wl.dtype, device),
+         "w_down": payload_to_torch(wd, wl.dtype, device)}
+    del wg, wu, wd
+    if wl.n_shared:
+        sg, su, sd = synth.shared_experts_payload(wl, layer_index)
+        w.update(ws_gate=payload_to_torch(sg, wl.dtype, device), ws_up=payload_to_torch(su, wl.dtype, device),
+                 ws_down=payload_to_torch(sd, wl.dtype, device))
+    return w
+
+
+def device_layer(wl, layer_index=0, device="cuda", weights=None, max_positions=None):
+    """An EpochLayer of the workload's shape (weights shared when given)."""
+    from sparse_moe_layer_gate_gb300.layer import EpochLayer
+    w = weights if weights is not None else device_weights(wl, layer_index, device)
+    return EpochLayer(hidden=wl.hidden, n_experts=wl.n_experts, inter=wl.inter, top_k=wl.top_k,
+                      max_positions=max_positions or wl.n_pos, dtype=wl.dtype, tau=wl.tau, refresh_R=wl.refresh_R,
+                      weights=w, n_shared=wl.n_shared, shared_inter=wl.shared_inter, residual=wl.residual,
+                      router=wl.router, n_group=wl.n_group, topk_group=wl.topk_group)
+
+
 # ---------------------------------------------------------------- data parallelism (replicas only)
 
 def replica_workload(rank: int):
@@ -131,12 +161,13 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        self.path = None
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.fh = open(self.path, "w")
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix=f"epoch_clocks_{self.index}_", suffix=".csv")
+            self.fh = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
@@ -158,6 +189,7 @@ class ClockSampler:
                 parts = [p.strip() for p in line.split(",")]
                 if len(parts) >= 9:
                     rows.append(parts)
+        os.unlink(self.path)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
@@ -169,6 +201,16 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU oracle timing
+
+def host_cores():
+    """Cores this process may run on (the BLAS pool of the oracle uses them all
+    unless a thread-count variable caps it)."""
+    n = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            n = min(n, int(os.environ[var]))
+    return n
+
 
 def cpu_oracle_sample(wl, n_iters, budget_s=25.0, payload=None):
     """Times the float64 oracle (as it stands) on plan + the first iterations of
@@ -210,7 +252,7 @@ def cpu_oracle_sample(wl, n_iters, budget_s=25.0, payload=None):
         done += 1
         if t_plan + t_iter > budget_s:
             break
-    threads = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS") or str(os.cpu_count())
+    threads = host_cores()
     sample = (f"block plan + iterations 0..{done - 1} of one {wl.name} block (float64 numpy oracle; "
               f"plan {t_plan:.2f} s amortised over the sampled iterations)")
     return edges / (t_plan * done / wl.iters + t_iter), int(threads), sample, done
@@ -223,7 +265,7 @@ def run_epoch(args, rank, world):
     import torch
     import synth
     from sparse_moe_layer_gate_gb300 import builder
-    from sparse_moe_layer_gate_gb300.layer import layer_for_workload, payload_to_torch
+    from sparse_moe_layer_gate_gb300.layer import payload_to_torch
 
     if builder.is_stale():
         if rank == 0:
@@ -235,7 +277,7 @@ def run_epoch(args, rank, world):
     dev = torch.device("cuda", torch.cuda.current_device())
     wl = replica_workload(rank)
     payload = synth.experts_payload(wl)
-    lay = layer_for_workload(wl, device=dev)
+    lay = device_layer(wl, device=dev)
     xs_host = synth.hidden_states(wl)
     live_h, dec_h = synth.block_masks(wl)
     xs = [payload_to_torch(xs_host[i], wl.dtype, dev) for i in range(wl.iters)]

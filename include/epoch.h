@@ -214,10 +214,15 @@ epoch_status epoch_layer_create(const epoch_layer_config *cfg, const epoch_layer
 /* Cold path of a block ([W] section "cold、hot-update、hot-skip"): gate logits
  * G = x W_r^T + b for the n_pos positions of x [n_pos][H] (device, dtype), dense
  * top-k hit counts, the coverage support (see tau), and clears the stamps and
- * previous-decoded flags so that the block starts with an empty cache. The
- * support is readable through epoch_debug_pointers after a sync.
- * EPOCH_EINVAL if n_pos is not in [1, max_positions] or x is NULL/misaligned. */
-epoch_status epoch_plan_block(epoch_layer *layer, const void *x_dev, int32_t n_pos, epoch_stream stream);
+ * previous-decoded flags so that the block starts with an empty cache.
+ * Outputs (device, written in stream order; either may be NULL):
+ *  support_ids_dev [n_experts] int32: every expert in rank order (hit count
+ *    desc, id asc); the first *support_len_dev are the block's support;
+ *  support_len_dev [1] int32: |S|.
+ * EPOCH_EINVAL if n_pos is not in [1, max_positions] or x (or a non-NULL
+ * output) is NULL/misaligned (outputs need 4-byte alignment). */
+epoch_status epoch_plan_block(epoch_layer *layer, const void *x_dev, int32_t n_pos, epoch_stream stream,
+                              int32_t *support_ids_dev, int32_t *support_len_dev);
 
 /* One refinement iteration ([W] sections "Expert Atlas" step three,
  * "Liveness-Shard Parallelism", "FreshLane Dispatch"):
@@ -229,12 +234,14 @@ epoch_status epoch_plan_block(epoch_layer *layer, const void *x_dev, int32_t n_p
  *  expert-sorted worklist; runs the SwiGLU experts over it; and writes
  *  y = routed (+ shared) (+ x if residual), routed being the fresh result or the
  *  cached row. Fresh rows refill the cache and get stamp i.
+ *  stats_dev (device, may be NULL): receives this iteration's epoch_iter_stats
+ *  in stream order, with no host synchronisation (4-byte aligned).
  *  A full-fresh fallback with every expert eligible happens when no plan is
  *  active, i != previous iteration + 1, n_pos differs from the plan, or a
  *  decoded position becomes live. EPOCH_EINVAL on bad sizes or pointers. */
 epoch_status epoch_moe_iter(epoch_layer *layer, const void *x_dev, const uint8_t *live_dev,
                             const uint8_t *decoded_dev, int32_t n_pos, int32_t iteration, void *y_dev,
-                            epoch_stream stream);
+                            epoch_stream stream, epoch_iter_stats *stats_dev);
 
 /* Lifecycle paths of an iteration inside a block ([W] section "cold、hot-update、
  * hot-skip"): 0 is the hot-skip path of epoch_moe_iter (the support of the
@@ -251,7 +258,7 @@ typedef enum { EPOCH_PATH_HOT_UPDATE = 1, EPOCH_PATH_REFRESH = 2 } epoch_path;
  * 0). EPOCH_EINVAL for unknown path bits, otherwise as epoch_moe_iter. */
 epoch_status epoch_moe_iter_path(epoch_layer *layer, const void *x_dev, const uint8_t *live_dev,
                                  const uint8_t *decoded_dev, int32_t n_pos, int32_t iteration, int32_t path,
-                                 void *y_dev, epoch_stream stream);
+                                 void *y_dev, epoch_stream stream, epoch_iter_stats *stats_dev);
 
 /* Ends the block: the plan, cache and stamps become invalid; the next
  * epoch_moe_iter without a new plan runs as a fallback. Host-only, no sync. */
@@ -264,7 +271,8 @@ epoch_status epoch_get_status(epoch_layer *layer, epoch_stream stream, uint32_t 
 /* Clears the device error word (enqueued on the stream). */
 epoch_status epoch_clear_status(epoch_layer *layer, epoch_stream stream);
 
-/* Copies the last iteration's statistics to host memory (synchronises the stream). */
+/* Copies the last iteration's statistics to host memory (synchronises the
+ * stream; epoch_moe_iter's stats_dev output gives them without a sync). */
 epoch_status epoch_read_stats(epoch_layer *layer, epoch_iter_stats *out, epoch_stream stream);
 
 /* Device pointers of the layer's internal arrays (no copy, no sync). */
@@ -306,17 +314,26 @@ epoch_status epoch_test_wait_timeout(epoch_layer *layer, int64_t timeout_ns, epo
  * The pages have no counterpart: this is an interface variant of the cold-path
  * planner of epoch_plan_block (same ranking and coverage rule, see tau) taking
  * the router logits the caller already holds.
- *  logits_dev [n_pos][n_experts] float, bias included (device, 16-byte aligned);
- *  top_k, tau as in epoch_layer_config; outputs support_ids_dev [n_experts]
- *  (experts in rank order) and support_len_dev [1] (device).
+ *  logits_dev [n_pos][n_experts] float (device, 16-byte aligned): the router
+ *    logits as the layer's gate computes them -- bias included for
+ *    EPOCH_ROUTER_SOFTMAX, G = x W_r^T without the bias for
+ *    EPOCH_ROUTER_SIGMOID_GROUP;
+ *  top_k, tau, router, n_group, topk_group as in epoch_layer_config;
+ *  bias_dev [n_experts] float (device): the router bias, used by the
+ *    group-limited sigmoid router (may be NULL for the softmax router);
+ *  outputs support_ids_dev [n_experts] (experts in rank order) and
+ *  support_len_dev [1] (device).
  * Its only scratch, the per-expert hit counts, is a fixed file-scope device
  * array of 1024 int32 (4 KB) that every GPU loading the library holds until
- * exit; n_experts > 1024 returns EPOCH_EINVAL. No call allocates memory. The
- * first call on a device looks up the array's device address (do it before any
- * stream capture); every call clears the counts it uses. All calls share the
- * array: calls that overlap on the GPU race and must be serialised. */
+ * exit; n_experts > 1024 or n_pos > 2^26 returns EPOCH_EINVAL. No call
+ * allocates memory. Each call made outside stream capture looks up the
+ * array's device address; a call under capture reuses the address the last
+ * uncaptured call on that device found, so make the first call on each device
+ * before any capture. Every call clears the counts it uses. All calls share
+ * the array: calls that overlap on the GPU race and must be serialised. */
 epoch_status epoch_plan_support_noalloc(const float *logits_dev, int32_t n_pos, int32_t n_experts, int32_t top_k,
-                                        double tau, int32_t *support_ids_dev, int32_t *support_len_dev,
+                                        double tau, int32_t router, const float *bias_dev, int32_t n_group,
+                                        int32_t topk_group, int32_t *support_ids_dev, int32_t *support_len_dev,
                                         epoch_stream stream);
 
 /* Releases host state only (the caller frees the workspace and weights). NULL is ignored. */

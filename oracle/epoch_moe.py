@@ -426,6 +426,7 @@ class IterResult:
     fallback: bool
     host_fallback: bool
     classified: Classified
+    slot: np.ndarray              # [|F|, k] worklist row of selection (f, j)
 
     @property
     def n_edges(self) -> int:
@@ -642,7 +643,7 @@ class LayerOracle:
         self.prev_decoded[:N] = ~cl.is_live
         self.last_iter = i
         return IterResult(y, G, fresh_pos, sel, w, wl_expert, wl_pos, wl_j, offsets, routed,
-                          fallback, host_fallback, cl)
+                          fallback, host_fallback, cl, slot)
 
 
 def dense_moe(x: np.ndarray, w_router: np.ndarray, b_router: np.ndarray,

@@ -13,7 +13,7 @@ def __getattr__(name):
     if name in ("binding", "builder", "layer"):
         import importlib
         return importlib.import_module(f".{name}", __name__)
-    if name in ("EpochLayer", "layer_for_workload", "payload_to_torch"):
+    if name in ("EpochLayer", "payload_to_torch"):
         from . import layer as _layer
         return getattr(_layer, name)
     raise AttributeError(name)

@@ -34,11 +34,13 @@ class epoch_layer_weights(C.Structure):
                 ("ws_up", C.c_void_p), ("ws_down", C.c_void_p)]
 
 
+STATS_FIELDS = ("iteration", "n_pos", "n_live", "n_new", "n_miss", "n_stale", "n_forced", "n_reuse",
+                "n_fresh", "n_edges", "n_hit_experts", "support_len", "fallback", "bad_flags",
+                "tiles_up", "tiles_down")
+
+
 class epoch_iter_stats(C.Structure):
-    _fields_ = [(n, C.c_int32) for n in (
-        "iteration", "n_pos", "n_live", "n_new", "n_miss", "n_stale", "n_forced", "n_reuse",
-        "n_fresh", "n_edges", "n_hit_experts", "support_len", "fallback", "bad_flags",
-        "tiles_up", "tiles_down")]
+    _fields_ = [(n, C.c_int32) for n in STATS_FIELDS]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -65,11 +67,11 @@ _SIGS = {
     "epoch_workspace_bytes": (C.c_size_t, [C.POINTER(epoch_layer_config)]),
     "epoch_layer_create": (C.c_int, [C.POINTER(epoch_layer_config), C.POINTER(epoch_layer_weights),
                                      C.c_void_p, C.c_size_t, C.POINTER(C.c_void_p)]),
-    "epoch_plan_block": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p]),
+    "epoch_plan_block": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p]),
     "epoch_moe_iter": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32,
-                                 C.c_void_p, C.c_void_p]),
+                                 C.c_void_p, C.c_void_p, C.c_void_p]),
     "epoch_moe_iter_path": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32,
-                                      C.c_int32, C.c_void_p, C.c_void_p]),
+                                      C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p]),
     "epoch_block_end": (C.c_int, [C.c_void_p]),
     "epoch_get_status": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(C.c_uint32)]),
     "epoch_clear_status": (C.c_int, [C.c_void_p, C.c_void_p]),
@@ -86,6 +88,7 @@ _SIGS = {
     "epoch_reset_profile": (C.c_int, [C.c_void_p]),
     "epoch_test_wait_timeout": (C.c_int, [C.c_void_p, C.c_int64, C.c_void_p]),
     "epoch_plan_support_noalloc": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_double,
+                                             C.c_int32, C.c_void_p, C.c_int32, C.c_int32,
                                              C.c_void_p, C.c_void_p, C.c_void_p]),
     "epoch_layer_destroy": (None, [C.c_void_p]),
     "epoch_status_str": (C.c_char_p, [C.c_int]),
@@ -135,13 +138,14 @@ def epoch_layer_create(cfg, weights, workspace_ptr: int, nbytes: int) -> int:
     return out.value
 
 
-def epoch_plan_block(layer: int, x_ptr: int, n_pos: int, stream: int = 0) -> int:
-    return lib().epoch_plan_block(layer, x_ptr, n_pos, stream)
+def epoch_plan_block(layer: int, x_ptr: int, n_pos: int, stream: int = 0, support_ids_ptr: Optional[int] = None,
+                     support_len_ptr: Optional[int] = None) -> int:
+    return lib().epoch_plan_block(layer, x_ptr, n_pos, stream, support_ids_ptr, support_len_ptr)
 
 
 def epoch_moe_iter(layer: int, x_ptr: int, live_ptr: int, decoded_ptr: int, n_pos: int, iteration: int,
-                   y_ptr: int, stream: int = 0) -> int:
-    return lib().epoch_moe_iter(layer, x_ptr, live_ptr, decoded_ptr, n_pos, iteration, y_ptr, stream)
+                   y_ptr: int, stream: int = 0, stats_ptr: Optional[int] = None) -> int:
+    return lib().epoch_moe_iter(layer, x_ptr, live_ptr, decoded_ptr, n_pos, iteration, y_ptr, stream, stats_ptr)
 
 
 PATH_HOT_UPDATE = 1  # epoch_path values
@@ -149,8 +153,9 @@ PATH_REFRESH = 2
 
 
 def epoch_moe_iter_path(layer: int, x_ptr: int, live_ptr: int, decoded_ptr: int, n_pos: int, iteration: int,
-                        path: int, y_ptr: int, stream: int = 0) -> int:
-    return lib().epoch_moe_iter_path(layer, x_ptr, live_ptr, decoded_ptr, n_pos, iteration, path, y_ptr, stream)
+                        path: int, y_ptr: int, stream: int = 0, stats_ptr: Optional[int] = None) -> int:
+    return lib().epoch_moe_iter_path(layer, x_ptr, live_ptr, decoded_ptr, n_pos, iteration, path, y_ptr, stream,
+                                     stats_ptr)
 
 
 def epoch_block_end(layer: int) -> int:

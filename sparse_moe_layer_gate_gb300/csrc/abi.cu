@@ -52,6 +52,7 @@ namespace {
 constexpr size_t kAlign = 256;
 
 bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4_or_null(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 bool valid_config(const epoch_layer_config *c) {
   if (c == nullptr) return false;
@@ -301,8 +302,10 @@ epoch_status epoch_layer_create(const epoch_layer_config *cfg, const epoch_layer
   return EPOCH_OK;
 }
 
-epoch_status epoch_plan_block(epoch_layer *L, const void *x, int32_t n_pos, epoch_stream stream) {
+epoch_status epoch_plan_block(epoch_layer *L, const void *x, int32_t n_pos, epoch_stream stream,
+                              int32_t *support_ids_dev, int32_t *support_len_dev) {
   if (L == nullptr || !aligned16(x) || n_pos < 1 || n_pos > L->cfg.max_positions) return EPOCH_EINVAL;
+  if (!aligned4_or_null(support_ids_dev) || !aligned4_or_null(support_len_dev)) return EPOCH_EINVAL;
   cudaStream_t s = S(stream);
   Dims d = call_dims(L, n_pos, 0, 0);
   d.plan_mode = 1;
@@ -313,7 +316,8 @@ epoch_status epoch_plan_block(epoch_layer *L, const void *x, int32_t n_pos, epoc
   const double tau = L->cfg.tau;
   const int all = tau >= 1.0;
   const int32_t T = static_cast<int32_t>(std::ceil(tau * static_cast<double>(n_pos * L->cfg.top_k)));
-  EPOCH_TRY(run(L, K_PLAN_SUPPORT, s, [&] { return launch_plan_support(d, L->ws, T, all, 1, s); }));
+  EPOCH_TRY(run(L, K_PLAN_SUPPORT, s,
+                [&] { return launch_plan_support(d, L->ws, T, all, 1, support_ids_dev, support_len_dev, s); }));
   L->planned = true;
   L->n_pos_plan = n_pos;
   L->last_iter = -1;
@@ -322,13 +326,16 @@ epoch_status epoch_plan_block(epoch_layer *L, const void *x, int32_t n_pos, epoc
 }
 
 epoch_status epoch_moe_iter_path(epoch_layer *L, const void *x, const uint8_t *live, const uint8_t *decoded,
-                                 int32_t n_pos, int32_t iteration, int32_t path, void *y, epoch_stream stream) {
+                                 int32_t n_pos, int32_t iteration, int32_t path, void *y, epoch_stream stream,
+                                 epoch_iter_stats *stats_dev) {
   if (L == nullptr || !aligned16(x) || !aligned16(y) || live == nullptr || decoded == nullptr) return EPOCH_EINVAL;
+  if (!aligned4_or_null(stats_dev)) return EPOCH_EINVAL;
   if (n_pos < 1 || n_pos > L->cfg.max_positions || iteration < 0) return EPOCH_EINVAL;
   if ((path & ~(EPOCH_PATH_HOT_UPDATE | EPOCH_PATH_REFRESH)) != 0) return EPOCH_EINVAL;
   cudaStream_t s = S(stream);
   const int host_fallback = !L->planned || iteration != L->last_iter + 1 || n_pos != L->n_pos_plan;
   Dims d = call_dims(L, n_pos, iteration, host_fallback);
+  d.stats_out = stats_dev;
   if (path & EPOCH_PATH_REFRESH) d.R = 0;  // every cached row counts as stale: all positions fresh
   if (d.trace) {
     if (cudaMemsetAsync(L->ws.timeline, 0xFF, K_NUM * 8, s) != cudaSuccess ||
@@ -347,7 +354,8 @@ epoch_status epoch_moe_iter_path(epoch_layer *L, const void *x, const uint8_t *l
     const double tau = L->cfg.tau;
     const int all = tau >= 1.0;
     const int32_t T = static_cast<int32_t>(std::ceil(tau * static_cast<double>(n_pos * L->cfg.top_k)));
-    EPOCH_TRY(run(L, K_PLAN_SUPPORT, s, [&] { return launch_plan_support(d, L->ws, T, all, 0, s); }));
+    EPOCH_TRY(run(L, K_PLAN_SUPPORT, s,
+                  [&] { return launch_plan_support(d, L->ws, T, all, 0, nullptr, nullptr, s); }));
     d.plan_mode = 0;
     EPOCH_TRY(run(L, K_SELECT, s, [&] { return launch_select(d, L->ws, live, decoded, L->w.b_router, s); }));
     ++L->n_hot_update;
@@ -372,8 +380,9 @@ epoch_status epoch_moe_iter_path(epoch_layer *L, const void *x, const uint8_t *l
 }
 
 epoch_status epoch_moe_iter(epoch_layer *L, const void *x, const uint8_t *live, const uint8_t *decoded,
-                            int32_t n_pos, int32_t iteration, void *y, epoch_stream stream) {
-  return epoch_moe_iter_path(L, x, live, decoded, n_pos, iteration, 0, y, stream);
+                            int32_t n_pos, int32_t iteration, void *y, epoch_stream stream,
+                            epoch_iter_stats *stats_dev) {
+  return epoch_moe_iter_path(L, x, live, decoded, n_pos, iteration, 0, y, stream, stats_dev);
 }
 
 epoch_status epoch_block_end(epoch_layer *L) {

@@ -100,6 +100,7 @@ struct Dims {
   int32_t n_group, topk_group;  // group rule of router 1
   uint32_t seq;          // sequence number of this call (route_done handshake)
   int64_t timeout_ns;
+  epoch_iter_stats *stats_out;  // caller's copy of this iteration's statistics (nullable)
 };
 
 struct Weights {
@@ -160,8 +161,9 @@ cudaError_t launch_select(const Dims &d, const Work &ws, const uint8_t *live, co
                           cudaStream_t s);
 cudaError_t launch_plan_topk(const Dims &d, const Weights &w, const Work &ws, cudaStream_t s);
 // clear_state: also reset every stamp and decoded flag (a block plan; not a hot update).
+// ids_out / len_out: the caller's copies of the ranked experts and |S| (nullable).
 cudaError_t launch_plan_support(const Dims &d, const Work &ws, int32_t threshold, int all_experts,
-                                int clear_state, cudaStream_t s);
+                                int clear_state, int32_t *ids_out, int32_t *len_out, cudaStream_t s);
 cudaError_t launch_route(const Dims &d, const Work &ws, cudaStream_t s);
 cudaError_t launch_permute(const Dims &d, const Work &ws, const void *x, cudaStream_t s);
 cudaError_t launch_combine(const Dims &d, const Work &ws, const void *x, void *y, int bf16, cudaStream_t s);

@@ -144,7 +144,7 @@ __global__ void k_plan_topk(Dims d, const float *__restrict__ logits, const floa
 // for a block plan (cold path), clear the block's stamps and previous-decoded
 // flags; a hot update keeps them.
 __global__ void __launch_bounds__(1024) k_plan_support(Dims d, Work ws, int32_t threshold, int all_experts,
-                                                       int clear_state) {
+                                                       int clear_state, int32_t *ids_out, int32_t *len_out) {
   const KernelMark mark_(d, ws, K_PLAN_SUPPORT);
   __shared__ int32_t cnt[1024];
   __shared__ int32_t sorted_cnt[1024];
@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(1024) k_plan_support(Dims d, Work ws, int32_t 
       rank += (ce > c) || (ce == c && e < tid);
     }
     ws.support_ids[rank] = tid;
+    if (ids_out) ids_out[rank] = tid;
     sorted_cnt[rank] = c;
   }
   __syncthreads();
@@ -191,7 +192,10 @@ __global__ void __launch_bounds__(1024) k_plan_support(Dims d, Work ws, int32_t 
     }
     ws.support_mask[tid] = rank < len ? 1 : 0;
   }
-  if (tid == 0) ws.ctrl->support_len = len;
+  if (tid == 0) {
+    ws.ctrl->support_len = len;
+    if (len_out) *len_out = len;
+  }
   if (clear_state) {
     for (int t = tid; t < 2 * d.Nmax; t += blockDim.x) {  // both halves of the iteration state
       ws.stamp[t] = -1;
@@ -537,6 +541,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) k_route(Dims d, Work ws) {
     st->fallback = fb;
     st->bad_flags = s_cat[5];
     if (s_cat[5]) set_error(ws.err, EPOCH_DEVERR_FLAGS);
+    if (d.stats_out) *d.stats_out = *st;
   }
   // positions beyond this call's n_pos keep their state
   for (int t = n + tid; t < d.Nmax; t += kRouteThreads) {
@@ -959,10 +964,10 @@ cudaError_t launch_plan_topk(const Dims &d, const Weights &w, const Work &ws, cu
 }
 
 cudaError_t launch_plan_support(const Dims &d, const Work &ws, int32_t threshold, int all_experts,
-                                int clear_state, cudaStream_t s) {
+                                int clear_state, int32_t *ids_out, int32_t *len_out, cudaStream_t s) {
   static bool carve_ = (prefer_max_shared(k_plan_support) == cudaSuccess);
   (void)carve_;
-  k_plan_support<<<1, 1024, 0, s>>>(d, ws, threshold, all_experts, clear_state);
+  k_plan_support<<<1, 1024, 0, s>>>(d, ws, threshold, all_experts, clear_state, ids_out, len_out);
   return cudaGetLastError();
 }
 

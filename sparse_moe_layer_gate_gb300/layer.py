@@ -75,16 +75,25 @@ class EpochLayer:
         self.device = dev
 
     # ------------------------------------------------------------------ entry points
-    def plan_block(self, x: torch.Tensor, stream=None) -> None:
+    def plan_block(self, x: torch.Tensor, stream=None, support_ids: Optional[torch.Tensor] = None,
+                   support_len: Optional[torch.Tensor] = None) -> None:
+        """Cold path of a block. support_ids (int32 [E]) and support_len (int32
+        [1]), CUDA tensors, receive the ranked experts and |S| in stream order."""
         self._check_x(x)
-        B.check(B.epoch_plan_block(self.handle, x.data_ptr(), x.shape[0], _stream(stream)),
-                "epoch_plan_block")
+        for t, n in ((support_ids, self.n_experts), (support_len, 1)):
+            if t is not None and not (t.is_cuda and t.dtype == torch.int32 and t.is_contiguous()
+                                      and t.numel() >= n):
+                raise ValueError("support outputs must be contiguous int32 CUDA tensors")
+        B.check(B.epoch_plan_block(self.handle, x.data_ptr(), x.shape[0], _stream(stream), _ptr(support_ids),
+                                   _ptr(support_len)), "epoch_plan_block")
 
     def moe_iter(self, x: torch.Tensor, live: torch.Tensor, decoded: torch.Tensor, iteration: int,
                  y: Optional[torch.Tensor] = None, stream=None, hot_update: bool = False,
-                 refresh: bool = False) -> torch.Tensor:
+                 refresh: bool = False, stats: Optional[torch.Tensor] = None) -> torch.Tensor:
         """One iteration; hot_update / refresh select the lifecycle path
-        (epoch_moe_iter_path), the default being the hot-skip path."""
+        (epoch_moe_iter_path), the default being the hot-skip path. stats, an
+        int32 CUDA tensor of len(binding.STATS_FIELDS) entries, receives the
+        iteration's statistics in stream order (see stats_dict)."""
         self._check_x(x)
         n = x.shape[0]
         for m in (live, decoded):
@@ -92,15 +101,24 @@ class EpochLayer:
                 raise ValueError("live/decoded must be contiguous uint8 CUDA tensors of n_pos flags")
         if y is None:
             y = torch.empty_like(x)
+        if stats is not None and not (stats.is_cuda and stats.dtype == torch.int32 and stats.is_contiguous()
+                                       and stats.numel() >= len(B.STATS_FIELDS)):
+            raise ValueError("stats must be a contiguous int32 CUDA tensor of len(STATS_FIELDS) entries")
         path = (B.PATH_HOT_UPDATE if hot_update else 0) | (B.PATH_REFRESH if refresh else 0)
         if path:
             B.check(B.epoch_moe_iter_path(self.handle, x.data_ptr(), live.data_ptr(), decoded.data_ptr(), n,
-                                          int(iteration), path, y.data_ptr(), _stream(stream)),
+                                          int(iteration), path, y.data_ptr(), _stream(stream), _ptr(stats)),
                     "epoch_moe_iter_path")
         else:
             B.check(B.epoch_moe_iter(self.handle, x.data_ptr(), live.data_ptr(), decoded.data_ptr(), n,
-                                     int(iteration), y.data_ptr(), _stream(stream)), "epoch_moe_iter")
+                                     int(iteration), y.data_ptr(), _stream(stream), _ptr(stats)), "epoch_moe_iter")
         return y
+
+    @staticmethod
+    def stats_dict(stats: torch.Tensor) -> dict:
+        """Host view of a stats tensor that moe_iter filled."""
+        vals = stats.cpu().tolist()
+        return {n: int(vals[i]) for i, n in enumerate(B.STATS_FIELDS)}
 
     def block_end(self) -> None:
         B.check(B.epoch_block_end(self.handle), "epoch_block_end")
@@ -240,28 +258,3 @@ def payload_to_torch(payload: np.ndarray, dtype: str, device) -> torch.Tensor:
     else:
         t = torch.from_numpy(np.ascontiguousarray(payload, dtype=np.float32))
     return t.to(device)
-
-
-def layer_for_workload(wl, layer_index: int = 0, device="cuda", threads: Optional[int] = None,
-                       max_positions: Optional[int] = None) -> EpochLayer:
-    """Builds the device layer of a synth workload (weights generated by synth, uploaded)."""
-    import synth
-    wr, b = synth.router_payload(wl, layer_index)
-    wg, wu, wd = synth.experts_payload(wl, layer_index, threads)
-    weights = {
-        "w_router": payload_to_torch(wr, wl.dtype, device),
-        "b_router": torch.from_numpy(b).to(device),
-        "w_gate": payload_to_torch(wg, wl.dtype, device),
-        "w_up": payload_to_torch(wu, wl.dtype, device),
-        "w_down": payload_to_torch(wd, wl.dtype, device),
-    }
-    del wg, wu, wd
-    if wl.n_shared:
-        sg, su, sd = synth.shared_experts_payload(wl, layer_index, threads)
-        weights.update(ws_gate=payload_to_torch(sg, wl.dtype, device),
-                       ws_up=payload_to_torch(su, wl.dtype, device),
-                       ws_down=payload_to_torch(sd, wl.dtype, device))
-    return EpochLayer(hidden=wl.hidden, n_experts=wl.n_experts, inter=wl.inter, top_k=wl.top_k,
-                      max_positions=max_positions or wl.n_pos, dtype=wl.dtype, tau=wl.tau, refresh_R=wl.refresh_R,
-                      weights=weights, n_shared=wl.n_shared, shared_inter=wl.shared_inter,
-                      residual=wl.residual, router=wl.router, n_group=wl.n_group, topk_group=wl.topk_group)

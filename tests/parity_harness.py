@@ -8,10 +8,14 @@ flip the next layer's routing) and each iteration is checked:
 
 * fresh set, category counts, fallback flags, support, selections, worklist
   offsets and positions: bit-exact;
-* a selection that differs is accepted only when the oracle's float64 logits
-  hold a near-tie (two of the k+1 best eligible logits within 1e-5); the case
-  is logged and the oracle adopts the GPU's selection so nothing cascades;
-  the planner's support likewise;
+* worklist slots and the selection index of every worklist row: bit-exact;
+* a selection that differs is accepted only when it is a reordering of the
+  oracle's that rounding could produce (experts whose float64 scores lie within
+  1e-5 of each other trade places; nothing else may change); the case is
+  logged and the oracle adopts the GPU's selection so nothing cascades;
+* a block-plan support that differs is accepted only when the GPU's hit counts
+  differ from the oracle's by edges that near-tied positions could move, and
+  the GPU's support is the prefix rule applied to the GPU's own counts;
 * routing weights within 2e-5; y within max|dy| <= tol * max|y| (tol 1e-2 for
   bf16, 1e-5 for fp32).
 """
@@ -25,9 +29,40 @@ import torch
 
 import oracle
 import synth
-from sparse_moe_layer_gate_gb300.layer import layer_for_workload, payload_to_torch
+from sparse_moe_layer_gate_gb300.layer import EpochLayer, payload_to_torch
 
 NEAR_TIE = 1e-5
+
+
+def device_weights(wl, layer_index: int = 0, device="cuda", threads: Optional[int] = None) -> dict:
+    """The layer's weights drawn by synth and uploaded (CUDA tensors by name)."""
+    wr, b = synth.router_payload(wl, layer_index)
+    wg, wu, wd = synth.experts_payload(wl, layer_index, threads)
+    weights = {
+        "w_router": payload_to_torch(wr, wl.dtype, device),
+        "b_router": torch.from_numpy(b).to(device),
+        "w_gate": payload_to_torch(wg, wl.dtype, device),
+        "w_up": payload_to_torch(wu, wl.dtype, device),
+        "w_down": payload_to_torch(wd, wl.dtype, device),
+    }
+    del wg, wu, wd
+    if wl.n_shared:
+        sg, su, sd = synth.shared_experts_payload(wl, layer_index, threads)
+        weights.update(ws_gate=payload_to_torch(sg, wl.dtype, device),
+                       ws_up=payload_to_torch(su, wl.dtype, device),
+                       ws_down=payload_to_torch(sd, wl.dtype, device))
+    return weights
+
+
+def layer_for_workload(wl, layer_index: int = 0, device="cuda", threads: Optional[int] = None,
+                       max_positions: Optional[int] = None, weights: Optional[dict] = None) -> EpochLayer:
+    """The device layer of a synth workload; `weights` reuses uploaded tensors
+    (layers that differ only in tau, R or the position count share them)."""
+    weights = weights if weights is not None else device_weights(wl, layer_index, device, threads)
+    return EpochLayer(hidden=wl.hidden, n_experts=wl.n_experts, inter=wl.inter, top_k=wl.top_k,
+                      max_positions=max_positions or wl.n_pos, dtype=wl.dtype, tau=wl.tau, refresh_R=wl.refresh_R,
+                      weights=weights, n_shared=wl.n_shared, shared_inter=wl.shared_inter,
+                      residual=wl.residual, router=wl.router, n_group=wl.n_group, topk_group=wl.topk_group)
 
 
 def tol_for(dtype: str) -> float:
@@ -97,21 +132,131 @@ def run_gpu(wl, layers, xs_payload, live, dec, iters: List[int], plan: bool = Tr
     return rec
 
 
+# ------------------------------------------------------------------ near-tie rules
+#
+# A GPU result that differs from the oracle's is accepted only when the
+# difference is a reordering that rounding could produce: experts whose
+# float64 scores lie within NEAR_TIE of each other may trade places, nothing
+# else may. Accepted cases are logged and the oracle adopts the GPU's choice so
+# that nothing downstream cascades.
+
+def selection_scores(orc, g_row: np.ndarray, eligible: np.ndarray):
+    """(scores the selection ranks, experts that may be selected, whether the
+    group choice itself is near-tied) for one position: the logits over the
+    eligible experts (softmax router), or the selection scores
+    c = sigmoid(G) + b over the eligible experts of the groups that can be
+    chosen (group-limited router: a group whose score is within NEAR_TIE of the
+    last chosen group's may replace it)."""
+    if orc.router.kind == "softmax":
+        return g_row, eligible.copy(), False
+    c = oracle.sigmoid(g_row) + orc.b_router
+    E, ng = g_row.shape[0], orc.router.n_group
+    gs = E // ng
+    scores = oracle.group_scores(c, eligible, ng)
+    n_elig = np.array([int(np.sum(eligible[g * gs:(g + 1) * gs])) for g in range(ng)])
+    chosen = oracle.chosen_groups(scores, n_elig, orc.router.topk_group, orc.k)
+    low = np.min(scores[chosen]) if chosen.any() else np.inf
+    possible = chosen | (np.isfinite(scores) & (scores >= low - NEAR_TIE))
+    return c, eligible & np.repeat(possible, gs), bool(np.any(possible & ~chosen))
+
+
+def valid_reordering(scores: np.ndarray, allowed: np.ndarray, mine, k: int) -> bool:
+    """True when `mine` (k experts in selection order) is what an exact top-k
+    of scores perturbed by at most NEAR_TIE / 2 per entry could return over the
+    allowed experts: distinct, allowed, and each entry within NEAR_TIE of the
+    best allowed expert not selected before it."""
+    mine = [int(e) for e in mine]
+    if len(mine) != k or len(set(mine)) != k:
+        return False
+    if any(e < 0 or e >= scores.shape[0] or not allowed[e] for e in mine):
+        return False
+    rest = allowed.copy()
+    for e in mine:
+        best = np.max(scores[rest])
+        if scores[e] + NEAR_TIE < best:
+            return False
+        rest[e] = False
+    return True
+
+
+def flexible_edges(orc, G: np.ndarray):
+    """Per position of a block plan (every expert eligible): the experts that
+    a rounding-level change could drop from its selection and those that could
+    join it. Empty for positions without a near-tie at the selection's edge;
+    with a near-tied group choice every selected expert may leave and every
+    expert of the possible groups may join."""
+    E = G.shape[1]
+    everyone = np.ones(E, dtype=bool)
+    out = []
+    for t in range(G.shape[0]):
+        sel, _ = orc.select(G[t], everyone)
+        scores, allowed, group_flip = selection_scores(orc, G[t], everyone)
+        inside = np.zeros(E, dtype=bool)
+        inside[sel] = True
+        outside = allowed & ~inside
+        if not outside.any():
+            out.append((set(), set()))
+            continue
+        if group_flip:
+            out.append(({int(e) for e in sel}, {int(e) for e in np.nonzero(outside)[0]}))
+            continue
+        kth = np.min(scores[sel])
+        best_out = np.max(scores[outside])
+        leave = {int(e) for e in sel if scores[e] <= best_out + NEAR_TIE}
+        enter = {int(e) for e in np.nonzero(outside)[0] if scores[e] >= kth - NEAR_TIE}
+        out.append((leave, enter) if leave and enter else (set(), set()))
+    return out
+
+
+def counts_explained(orc, G: np.ndarray, oracle_counts: np.ndarray, gpu_counts: np.ndarray) -> bool:
+    """True when the GPU's block-plan hit counts differ from the oracle's only
+    by experts leaving and joining selections at near-tied positions: every
+    expert's surplus (deficit) is at most the number of positions where it
+    could join (leave), and the total number of moved edges fits the
+    positions' freedom."""
+    D = np.asarray(gpu_counts, dtype=np.int64) - np.asarray(oracle_counts, dtype=np.int64)
+    if not D.any():
+        return True
+    if D.sum() != 0:
+        return False
+    flex = flexible_edges(orc, G)
+    can_join = np.zeros(D.shape[0], dtype=np.int64)
+    can_leave = np.zeros(D.shape[0], dtype=np.int64)
+    moves = 0
+    for leave, enter in flex:
+        for e in leave:
+            can_leave[e] += 1
+        for e in enter:
+            can_join[e] += 1
+        moves += min(len(leave), len(enter))
+    if np.any(np.maximum(D, 0) > can_join) or np.any(np.maximum(-D, 0) > can_leave):
+        return False
+    return int(np.maximum(D, 0).sum()) <= moves
+
+
+def _check_support(orc, op, gplan: dict, n_pos: int, rep: Report, what: str) -> None:
+    glen = int(gplan["support_len"])
+    gids = np.asarray(gplan["support_ids"])
+    gcnt = np.asarray(gplan["plan_counts"])
+    if glen == op.support_len and np.array_equal(gids[:glen], op.ranked[:glen]) and \
+            np.array_equal(gcnt, op.counts):
+        return
+    if not counts_explained(orc, op.G, op.counts, gcnt):
+        rep.mismatches.append(f"{what}: hit counts differ beyond near-tied edges "
+                              f"(gpu len {glen}, oracle len {op.support_len})")
+        return
+    ranked, slen = oracle.plan_support(gcnt, orc.k, orc.tau, n_pos)
+    if glen != slen or not np.array_equal(gids[:glen], ranked[:slen]):
+        rep.mismatches.append(f"{what}: GPU support is not the prefix rule applied to the GPU's own counts")
+        return
+    moved = int(np.abs(gcnt - op.counts).sum()) // 2
+    rep.near_ties.append(f"{what}: {moved} edge(s) moved at near-tied positions; adopting GPU support")
+    orc.adopt_support(gids, glen)
+
+
 def check_plan(orc: oracle.LayerOracle, gplan: dict, x0: np.ndarray, wl, rep: Report, tag: str):
     op = orc.plan_block(x0)
-    glen = gplan["support_len"]
-    gids = gplan["support_ids"]
-    same = glen == op.support_len and np.array_equal(gids[:glen], op.ranked[:glen])
-    counts_same = np.array_equal(gplan["plan_counts"], op.counts)
-    if not (same and counts_same):
-        everyone = np.ones(wl.n_experts, dtype=bool)
-        ties = [t for t in range(x0.shape[0]) if orc.near_tie(op.G[t], everyone, NEAR_TIE)]
-        if ties:
-            rep.near_ties.append(f"{tag} plan: near-tie at positions {ties[:8]}; adopting GPU support")
-            orc.adopt_support(gids, glen)
-        else:
-            rep.mismatches.append(f"{tag} plan: support/counts differ without a near-tie "
-                                  f"(gpu len {glen}, oracle len {op.support_len})")
+    _check_support(orc, op, gplan, x0.shape[0], rep, f"{tag} plan")
     return op
 
 
@@ -119,18 +264,7 @@ def check_hot_update(orc: oracle.LayerOracle, gplan: dict, x0: np.ndarray, wl, r
     """The support a hot-update iteration rebuilt (oracle.hot_update on the same
     input; near-ties as for the block plan)."""
     op = orc.hot_update(x0)
-    glen = gplan["support_len"]
-    gids = gplan["support_ids"]
-    same = glen == op.support_len and np.array_equal(gids[:glen], op.ranked[:glen])
-    if not (same and np.array_equal(gplan["plan_counts"], op.counts)):
-        everyone = np.ones(wl.n_experts, dtype=bool)
-        ties = [t for t in range(x0.shape[0]) if orc.near_tie(op.G[t], everyone, NEAR_TIE)]
-        if ties:
-            rep.near_ties.append(f"{tag} hot update: near-tie at positions {ties[:8]}; adopting GPU support")
-            orc.adopt_support(gids, glen)
-        else:
-            rep.mismatches.append(f"{tag} hot update: support/counts differ without a near-tie "
-                                  f"(gpu len {glen}, oracle len {op.support_len})")
+    _check_support(orc, op, gplan, x0.shape[0], rep, f"{tag} hot update")
     return op
 
 
@@ -142,8 +276,9 @@ def check_iteration(orc, step: GpuStep, live, dec, i: int, wl, rep: Report, tag:
         mine = gsel.get(t)
         if mine is None or np.array_equal(mine, s):
             return None
-        if orc.near_tie(g_row, eligible, NEAR_TIE):
-            rep.near_ties.append(f"{tag} i={i} t={t}: gpu {list(mine)} oracle {list(s)} (near-tie)")
+        scores, allowed, _ = selection_scores(orc, g_row, eligible)
+        if valid_reordering(scores, allowed, mine, orc.k):
+            rep.near_ties.append(f"{tag} i={i} t={t}: gpu {list(mine)} oracle {list(s)} (in-tie reordering)")
             return mine
         rep.mismatches.append(f"{tag} i={i} t={t}: selection gpu {list(mine)} oracle {list(s)}")
         return None
@@ -167,6 +302,15 @@ def check_iteration(orc, step: GpuStep, live, dec, i: int, wl, rep: Report, tag:
         rep.mismatches.append(f"{tag} i={i}: worklist offsets differ")
     if not np.array_equal(g["wl_pos"], res.wl_pos):
         rep.mismatches.append(f"{tag} i={i}: worklist positions differ")
+    gslot = np.asarray(g["slot"])
+    if not np.array_equal(gslot, res.slot):
+        rep.mismatches.append(f"{tag} i={i}: worklist slots differ")
+    elif res.n_edges:
+        # which of its position's k selections each worklist row is
+        gj = np.full(res.n_edges, -1, dtype=np.int64)
+        gj[gslot.reshape(-1)] = np.tile(np.arange(orc.k), gslot.shape[0])
+        if not np.array_equal(gj, res.wl_j):
+            rep.mismatches.append(f"{tag} i={i}: worklist selection indices differ")
     if res.sel.size:
         werr = float(np.max(np.abs(g["sel_w"] - res.w)))
         if werr > 2e-5:

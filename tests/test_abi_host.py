@@ -81,9 +81,17 @@ def test_invalid_arguments_return_einval(lib):
                                   C.byref(out)) == B.EPOCH_EINVAL  # misaligned router
     assert lib.epoch_layer_create(C.byref(cfg), C.byref(w), C.c_void_p(4096), 16,
                                   C.byref(out)) == B.EPOCH_EINVAL  # workspace too small
-    assert lib.epoch_plan_block(None, C.c_void_p(4096), 32, None) == B.EPOCH_EINVAL
-    assert lib.epoch_moe_iter(None, 4096, 4096, 4096, 32, 0, 4096, None) == B.EPOCH_EINVAL
-    assert lib.epoch_moe_iter_path(None, 4096, 4096, 4096, 32, 0, 1, 4096, None) == B.EPOCH_EINVAL
+    assert lib.epoch_plan_block(None, C.c_void_p(4096), 32, None, None, None) == B.EPOCH_EINVAL
+    assert lib.epoch_moe_iter(None, 4096, 4096, 4096, 32, 0, 4096, None, None) == B.EPOCH_EINVAL
+    assert lib.epoch_moe_iter_path(None, 4096, 4096, 4096, 32, 0, 1, 4096, None, None) == B.EPOCH_EINVAL
+    # the allocation-free planner checks its sizes and router before any CUDA call
+    noalloc = lib.epoch_plan_support_noalloc
+    assert noalloc(None, 32, 16, 2, 0.9, 0, None, 1, 1, 4096, 4096, None) == B.EPOCH_EINVAL       # no logits
+    assert noalloc(4096, 32, 1025, 2, 0.9, 0, None, 1, 1, 4096, 4096, None) == B.EPOCH_EINVAL     # E > 1024
+    assert noalloc(4096, (1 << 26) + 1, 16, 2, 0.9, 0, None, 1, 1, 4096, 4096, None) == B.EPOCH_EINVAL
+    assert noalloc(4096, 32, 16, 2, 0.9, 1, None, 4, 2, 4096, 4096, None) == B.EPOCH_EINVAL       # no bias
+    assert noalloc(4096, 32, 16, 2, 0.9, 1, 4096, 3, 2, 4096, 4096, None) == B.EPOCH_EINVAL       # 16 % 3
+    assert noalloc(4096, 32, 16, 2, 0.9, 2, None, 1, 1, 4096, 4096, None) == B.EPOCH_EINVAL       # router
     assert lib.epoch_path_counters_ex(None, None, None) == B.EPOCH_EINVAL
     assert lib.epoch_block_end(None) == B.EPOCH_EINVAL
     assert lib.epoch_get_status(None, None, None) == B.EPOCH_EINVAL

@@ -5,13 +5,16 @@ finishes in seconds, plus edge cases: ragged position counts, an empty
 worklist, every fallback path, malformed flags, determinism and the bounded
 device wait.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import synth
-from parity_harness import block_parity, layer_for_workload, oracle_layer, payload_to_torch, scenario_parity
+from parity_harness import (block_parity, device_weights, layer_for_workload, oracle_layer, payload_to_torch,
+                            scenario_parity)
 
 pytestmark = pytest.mark.gpu
 
@@ -55,20 +58,81 @@ def test_llada2_mini_block():
 
 
 def test_llada2_flash_stack_of_four():
-    # ten iterations: cold, new commits every iteration and the first R=8 refreshes
-    rep = block_parity(synth.WORKLOADS["llada2_flash_x4"], n_iters=10)
+    """The whole block of all four layers: cold path, one commit per block per
+    iteration, the R = 8 refreshes, and the late iterations where most
+    positions reuse their cached rows."""
+    rep = block_parity(synth.WORKLOADS["llada2_flash_x4"])
     assert_clean(rep)
-    assert rep.iterations == 40
+    assert rep.iterations == 4 * 32
 
 
-@pytest.mark.parametrize("batch,tau,R", [(1, 0.9, 4), (1, 1.0, 1), (4, 0.95, None), (4, 0.99, 4),
-                                         (16, 1.0, 4), (1, 0.9, None)])
+# The sweep on the LLaDA2.0-mini-shaped layer: at every batch, every tau and
+# every R at least once, each over a whole 32-iteration block (the live
+# fraction falls from 100% to 0%). The remaining points of the 4 x 4 x 3 grid
+# run when EPOCH_FULL_SWEEP=1.
+SWEEP_POINTS = [(1, 0.9, 1), (1, 0.95, 4), (1, 0.99, None), (1, 1.0, 1),
+                (4, 0.9, 4), (4, 0.95, None), (4, 0.99, 1), (4, 1.0, 4),
+                (16, 0.9, None), (16, 0.95, 1), (16, 0.99, 4), (16, 1.0, None),
+                (64, 0.9, 1), (64, 0.95, 4), (64, 0.99, None), (64, 1.0, 1)]
+SWEEP_REST = [(b, t, r) for b in (1, 4, 16, 64) for t in (0.9, 0.95, 0.99, 1.0) for r in (1, 4, None)
+              if (b, t, r) not in SWEEP_POINTS]
+_SWEEP_WEIGHTS = {}
+
+
+def _sweep_parity(batch, tau, R):
+    wl = synth.sweep_workload(batch, tau, R)
+    if "w" not in _SWEEP_WEIGHTS:  # every point has the same layer weights
+        _SWEEP_WEIGHTS["w"] = device_weights(wl)
+    lay = layer_for_workload(wl, weights=_SWEEP_WEIGHTS["w"])
+    rep = block_parity(wl, layers=[lay])
+    lay.close()
+    assert_clean(rep)
+    assert rep.iterations == 32
+
+
+@pytest.mark.parametrize("batch,tau,R", SWEEP_POINTS)
 def test_sweep_points(batch, tau, R):
-    assert_clean(block_parity(synth.sweep_workload(batch, tau, R), n_iters=12))
+    _sweep_parity(batch, tau, R)
 
 
-def test_sweep_largest_batch_first_iterations():
-    assert_clean(block_parity(synth.sweep_workload(64, 0.95, 4), n_iters=3))
+@pytest.mark.skipif(os.environ.get("EPOCH_FULL_SWEEP") != "1", reason="full grid: set EPOCH_FULL_SWEEP=1")
+@pytest.mark.parametrize("batch,tau,R", SWEEP_REST)
+def test_sweep_rest_of_grid(batch, tau, R):
+    _sweep_parity(batch, tau, R)
+
+
+def test_boundary_outputs_support_and_stats():
+    """The support comes out of epoch_plan_block and the statistics out of
+    epoch_moe_iter (device outputs, no host synchronisation inside the calls);
+    both match the oracle."""
+    wl = TINY_BF16
+    lay = layer_for_workload(wl)
+    orc = oracle_layer(wl)
+    xs, live, dec = _steps_from(wl, 4)
+    E = wl.n_experts
+    ids = torch.full((E,), -1, dtype=torch.int32, device="cuda")
+    slen = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lay.plan_block(payload_to_torch(xs[0], wl.dtype, lay.device), support_ids=ids, support_len=slen)
+    stats = [torch.full((16,), -7, dtype=torch.int32, device="cuda") for _ in range(4)]
+    for i in range(4):
+        lay.moe_iter(payload_to_torch(xs[i], wl.dtype, lay.device), torch.from_numpy(live[i]).cuda(),
+                     torch.from_numpy(dec[i]).cuda(), i, stats=stats[i])
+    torch.cuda.synchronize()
+    op = orc.plan_block(synth.to_f64(xs[0], wl.dtype))
+    n = int(slen.item())
+    assert n == op.support_len
+    assert ids.cpu().numpy().tolist() == op.ranked.tolist()
+    for i in range(4):
+        res = orc.iterate(synth.to_f64(xs[i], wl.dtype), live[i], dec[i], i)
+        st = lay.stats_dict(stats[i])
+        cl = res.classified
+        want = dict(iteration=i, n_pos=wl.n_pos, n_live=cl.n_live, n_new=cl.n_new, n_miss=cl.n_miss,
+                    n_stale=cl.n_stale, n_forced=cl.n_forced, n_reuse=cl.n_reuse, n_fresh=len(res.fresh_pos),
+                    n_edges=res.n_edges, n_hit_experts=int(np.count_nonzero(np.diff(res.offsets))),
+                    support_len=n, fallback=0, bad_flags=0)
+        assert {k: st[k] for k in want} == want, (i, st, want)
+    assert lay.stats() == lay.stats_dict(stats[3])  # the synchronising read agrees
+    lay.close()
 
 
 def test_every_expert_eligible_at_2048_positions():
