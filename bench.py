@@ -53,6 +53,9 @@ def parse():
     ap.add_argument("--impl", default="epoch", choices=["epoch", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the other workload shapes and the sweep against dense")
+    ap.add_argument("--per-config-steps", type=int, default=3)
     return ap.parse_args()
 
 
@@ -100,7 +103,8 @@ def device_layer(wl, layer_index=0, device="cuda", weights=None, max_positions=N
     return EpochLayer(hidden=wl.hidden, n_experts=wl.n_experts, inter=wl.inter, top_k=wl.top_k,
                       max_positions=max_positions or wl.n_pos, dtype=wl.dtype, tau=wl.tau, refresh_R=wl.refresh_R,
                       weights=w, n_shared=wl.n_shared, shared_inter=wl.shared_inter, residual=wl.residual,
-                      router=wl.router, n_group=wl.n_group, topk_group=wl.topk_group)
+                      router=wl.router, n_group=wl.n_group, topk_group=wl.topk_group,
+                      raw_weights=wl.raw_weights, coverage=wl.coverage, request_size=wl.request_size)
 
 
 # ---------------------------------------------------------------- data parallelism (replicas only)
@@ -403,6 +407,146 @@ def run_epoch(args, rank, world):
     return out, wl, payload
 
 
+# ---------------------------------------------------------------- other workload shapes
+
+def stack_iteration_work(wl, stats_layers):
+    """Roofline time per iteration of a layer stack: the layers run one after
+    another, so their per-layer rooflines add up. Returns (t_roof list, edges)."""
+    hbm, tc, _, _ = peaks()
+    t_roof, edges = [], 0
+    for i in range(len(stats_layers[0])):
+        t = 0.0
+        for st_l in stats_layers:
+            f, b = iteration_work(wl, st_l[i])
+            t += max(f / (tc * 1e12), b / (hbm * 1e9))
+            edges += st_l[i]["n_edges"]
+        t_roof.append(t)
+    return t_roof, edges
+
+
+def time_stack(layers, wl, xs, lv, dc, flush, steps, warmup):
+    """Times whole blocks of a layer stack (plan + wl.iters iterations, each
+    iteration running every layer on the previous layer's output). Returns
+    (us per iteration by index, plan us per block, per-layer statistics)."""
+    import numpy as np
+    import torch
+    from sparse_moe_layer_gate_gb300 import binding as B
+    stream = torch.cuda.current_stream()
+    n_l = len(layers)
+    outs = [[torch.empty_like(xs[0]) for _ in range(wl.iters)] for _ in range(n_l)]
+    stats_dev = [torch.zeros((wl.iters, len(B.STATS_FIELDS)), dtype=torch.int32, device=xs[0].device)
+                 for _ in range(n_l)]
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    plan_in = [xs[0]]  # layer l's input at iteration 0 (layer l - 1's first output), set by the first block
+
+    def block(account=False):
+        evp = (mk(), mk())
+        evi = [(mk(), mk()) for _ in range(wl.iters)]
+        torch.cuda._sleep(10_000_000)  # lets the host queue the block ahead of the GPU
+        if not account:  # every layer's plan, from the inputs the accounting block saw
+            evp[0].record(stream)
+            for l, lay in enumerate(layers):
+                lay.plan_block(plan_in[l])
+            evp[1].record(stream)
+        for i in range(wl.iters):
+            flush.fill_(i & 0xFF)
+            evi[i][0].record(stream)
+            x = xs[i]
+            for l, lay in enumerate(layers):
+                if account and i == 0:
+                    lay.plan_block(x)
+                    if l > 0:
+                        plan_in.append(x.clone())
+                lay.moe_iter(x, lv[i], dc[i], i, outs[l][i], stats=stats_dev[l][i] if account else None)
+                x = outs[l][i]
+            evi[i][1].record(stream)
+        for lay in layers:
+            lay.block_end()
+        return evp, evi
+
+    block(account=True)
+    torch.cuda.synchronize()
+    stats = [[dict(zip(B.STATS_FIELDS, row)) for row in sd.cpu().tolist()] for sd in stats_dev]
+    for _ in range(warmup):
+        block()
+    recs = [block() for _ in range(steps)]
+    torch.cuda.synchronize()
+    iter_us = np.array([[1e3 * a.elapsed_time(b) for a, b in evi] for _, evi in recs]).mean(axis=0)
+    plan_us = float(np.mean([1e3 * p[0].elapsed_time(p[1]) for p, _ in recs]))
+    return iter_us, plan_us, stats
+
+
+def per_config_entry(wl, iter_us, plan_us, stats, layers_n=1):
+    t_roof, edges = stack_iteration_work(wl, stats)
+    t_meas = float(iter_us.sum()) / 1e6
+    return {"workload": f"{wl.name}: {wl.description}", "layers": layers_n,
+            "us_per_iter": float(iter_us.mean()), "us_per_iter_first": float(iter_us[0]),
+            "us_per_iter_last8": float(iter_us[-8:].mean()),
+            "edges_per_s": edges / t_meas, "edges_per_block": edges,
+            "roofline_us_per_iter": 1e6 * sum(t_roof) / len(t_roof),
+            "path_roofline_frac": sum(t_roof) / t_meas, "plan_us_per_block": plan_us,
+            "fresh_per_iter": [int(s["n_fresh"]) for s in stats[0]],
+            "support_len": int(stats[0][0]["support_len"])}
+
+
+def run_per_config(steps, warmup, dev):
+    """Throughput of the other workload shapes, and the sweep on the
+    LLaDA2.0-mini-shaped layer against dense (tau = 1, R = 1 through the same
+    kernels) on the same inputs; per point the us per iteration over a whole
+    block and the path's roofline fraction."""
+    import torch
+    import synth
+    from sparse_moe_layer_gate_gb300.layer import payload_to_torch
+    out = {}
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def inputs(wl):
+        xs_h = synth.hidden_states(wl)
+        lv_h, dc_h = synth.block_masks(wl)
+        return ([payload_to_torch(xs_h[i], wl.dtype, dev) for i in range(wl.iters)],
+                [torch.from_numpy(lv_h[i]).to(dev) for i in range(wl.iters)],
+                [torch.from_numpy(dc_h[i]).to(dev) for i in range(wl.iters)])
+
+    for name in ("llada_moe_7b", "llada2_flash_x4"):
+        wl = synth.WORKLOADS[name]
+        layers = [device_layer(wl, l, dev) for l in range(wl.layers)]
+        xs, lv, dc = inputs(wl)
+        iter_us, plan_us, stats = time_stack(layers, wl, xs, lv, dc, flush, steps, warmup)
+        out[name] = per_config_entry(wl, iter_us, plan_us, stats, wl.layers)
+        for lay in layers:
+            lay.close()
+        del layers, xs
+        torch.cuda.empty_cache()
+
+    points = []
+    weights = None
+    for batch in (1, 4, 16, 64):
+        dense_us = None
+        for tau, R in [(1.0, 1)] + [(t, r) for t in (0.9, 0.95, 0.99, 1.0) for r in (1, 4, None)
+                                    if (t, r) != (1.0, 1)]:
+            wl = synth.sweep_workload(batch, tau, R)
+            if weights is None:
+                weights = device_weights(wl, 0, dev)
+            lay = device_layer(wl, 0, dev, weights=weights)
+            xs, lv, dc = inputs(wl)
+            iter_us, plan_us, stats = time_stack([lay], wl, xs, lv, dc, flush, steps, warmup)
+            e = per_config_entry(wl, iter_us, plan_us, stats)
+            lay.close()
+            if dense_us is None:
+                dense_us = e["us_per_iter"]
+            points.append({"batch": batch, "tau": tau, "R": "inf" if R is None else R,
+                           "us_per_iter": round(e["us_per_iter"], 2),
+                           "path_roofline_frac": round(e["path_roofline_frac"], 3),
+                           "roofline_us_per_iter": round(e["roofline_us_per_iter"], 2),
+                           "edges_per_s": e["edges_per_s"], "support_len": e["support_len"],
+                           "speedup_vs_dense": round(dense_us / e["us_per_iter"], 3)})
+        torch.cuda.empty_cache()
+    out["sweep"] = {"dense": "tau = 1, R = 1 through the same kernels (every position fresh every iteration, "
+                             "every expert eligible) on the same inputs", "points": points}
+    return out
+
+
 def run_e2e(lay, wl, xs_host, live_h, dec_h, edges_per_block, steps, flush, dev, world, dist_on):
     """Same metric through the public call with host buffers: every iteration
     copies x and the masks from pinned host memory and reads y back, inside the
@@ -484,6 +628,9 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", rank)))
         dist.init_process_group("nccl")
     out, wl, payload = run_epoch(args, rank, world)
+    if rank == 0 and world == 1 and not args.no_per_config:
+        import torch
+        out["per_config"] = run_per_config(args.per_config_steps, 1, torch.device("cuda", torch.cuda.current_device()))
     if rank == 0:
         if not args.no_cpu_baseline:
             v, cores, sample, _ = cpu_oracle_sample(wl, wl.iters, budget_s=20.0, payload=payload)

@@ -87,10 +87,33 @@ typedef enum { EPOCH_F32 = 0, EPOCH_BF16 = 1 } epoch_dtype;
  *    while they hold fewer than k eligible experts) are searched for the top-k
  *    of c; weights = the selected s divided by their sum. The block plan's hit
  *    counts use the same rule with every expert eligible.
+ *  raw_weights: 0 renormalises the weights over the k selected experts (as
+ *    above); 1 keeps the router's own scores -- softmax router: each selected
+ *    expert's dense router probability (softmax of G over all E experts);
+ *    sigmoid router: the selected s.
+ *  coverage_check, coverage_alpha (alpha), coverage_q (q): nonzero checks the
+ *    support's coverage every iteration ([W] section "Expert Atlas" defines
+ *    it; section "cold、hot-update、hot-skip" sends a layer whose support no
+ *    longer covers the routing back to the full fresh path): a fresh position
+ *    is under-covered when its dense selection (the router's rule with every
+ *    expert eligible) has less than alpha of its raw score mass (dense
+ *    probabilities, or sigmoid scores) on support experts; when more than
+ *    (1 - q) of the fresh positions are, the next iteration runs full fresh
+ *    with every expert eligible (statistics: fallback bit 2, n_under).
+ *  request_size: 0 plans one support for all positions of a call. > 0 splits
+ *    the positions into requests of request_size consecutive positions (the
+ *    last may be shorter), each with its own block plan -- its own hit counts
+ *    and threshold ceil(tau * n_r * k) over its n_r positions -- and each
+ *    position selects within its request's support ([W] section "cold、
+ *    hot-update、hot-skip": a block plan belongs to one diffusion block). The
+ *    layer's support (epoch_plan_block's outputs, the statistics) is then the
+ *    union of the requests' supports, in ascending expert order.
  * Constraints (else EPOCH_EINVAL): 1 <= top_k <= n_experts <= 1024, top_k <= 16;
  *  bf16: H a multiple of 256, I and shared_inter multiples of 128; f32: multiples of 4;
  *  1 <= max_positions <= 16384; router 1: 1 <= n_group <= 32, n_experts a
- *  multiple of n_group, 1 <= topk_group <= n_group (router 0 ignores both). */
+ *  multiple of n_group, 1 <= topk_group <= n_group (router 0 ignores both);
+ *  raw_weights 0 or 1; with coverage_check, 0 <= coverage_alpha <= 1 and
+ *  0 <= coverage_q <= 1; 0 <= request_size <= max_positions. */
 typedef struct {
   int32_t hidden;
   int32_t n_experts;
@@ -106,6 +129,11 @@ typedef struct {
   int32_t router;
   int32_t n_group;
   int32_t topk_group;
+  int32_t raw_weights;
+  int32_t coverage_check;
+  double coverage_alpha;
+  double coverage_q;
+  int32_t request_size;
 } epoch_layer_config;
 
 enum { EPOCH_ROUTER_SOFTMAX = 0, EPOCH_ROUTER_SIGMOID_GROUP = 1 };
@@ -141,16 +169,19 @@ typedef struct {
   int32_t n_edges;     /* worklist length L = k |F_i| */
   int32_t n_hit_experts;
   int32_t support_len; /* experts eligible this iteration (E on a fallback) */
-  int32_t fallback;    /* bit 0: host-detected mismatch; bit 1: decoded->live anomaly */
+  int32_t fallback;    /* bit 0: host-detected mismatch; bit 1: decoded->live anomaly;
+                          bit 2: the previous iteration's support coverage fell short */
   int32_t bad_flags;   /* positions flagged both live and decoded, or neither */
   int32_t tiles_up;    /* grouped-GEMM tiles launched */
   int32_t tiles_down;
+  int32_t n_under;     /* fresh positions under the coverage floor (coverage_check; else 0) */
 } epoch_iter_stats;
 
 /* Device pointers into the workspace for inspection (valid after the stream
  * that ran the last call has been synchronised; read-only for the caller). */
 typedef struct {
-  const int32_t *support_ids;  /* [E] experts in rank order; first *support_len valid */
+  const int32_t *support_ids;  /* [E] experts in rank order (per-request supports: their union,
+                                  ascending); first *support_len valid */
   const int32_t *support_len;  /* [1] */
   const int32_t *plan_counts;  /* [E] block-start top-k hit counts */
   const float *logits;         /* [max_positions][E] G of the last iteration, bias included */
@@ -189,6 +220,12 @@ typedef struct {
    * (globaltimer ns) of each kernel kind in the last iteration, in the order
    * of epoch_profile.name. */
   const int64_t *timeline;
+  /* Support masks [R][E] (1: eligible), R = 1 or, with per-request supports,
+   * one row per request; with per-request supports also each request's ranked
+   * experts [R][E] and |S| [R] (plan_counts is then [R][E] too). */
+  const uint8_t *support_masks;
+  const int32_t *request_ids;
+  const int32_t *request_len;
 } epoch_debug_view;
 
 /* Per-kernel timing, accumulated while profiling is on. */

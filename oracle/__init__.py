@@ -21,6 +21,8 @@ from .epoch_moe import (  # noqa: F401
     classify_positions,
     coverage_threshold,
     dense_moe,
+    dense_probabilities,
+    selection_weights,
     gate_logits,
     hit_counts,
     near_tie,

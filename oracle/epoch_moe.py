@@ -40,7 +40,9 @@ Readings taken where the pages are silent:
     id asc); the support is the smallest prefix whose counts reach
     T = ceil(tau * N * k), at least k experts; tau >= 1 means every expert;
   * selection uses raw logits (bias included); ties go to the lower expert id;
-    weights are a softmax over the k selected logits (they sum to 1);
+    weights are a softmax over the k selected logits (they sum to 1), or, with
+    renormalisation off, the dense router probabilities of the selected experts
+    (the sigmoid router: the selected sigmoid scores);
   * refresh: a decoded position is stale when i - stamp >= R (R = None: never);
     a refresh-path iteration makes every cached row stale (R = 0 for that
     iteration) and keeps the support;
@@ -49,6 +51,11 @@ Readings taken where the pages are silent:
   * per-request supports (optional): every request_size consecutive positions
     form one request with its own plan (its own counts and threshold), and a
     position selects within its request's support;
+  * support-coverage check (optional, alpha and q): a fresh position is
+    under-covered when the support holds less than alpha of the raw score mass
+    of its dense selection; when more than (1 - q) of the fresh positions are,
+    the support falls short and the next iteration runs full fresh with every
+    expert eligible (a host fallback resets the check);
   * the expert is SwiGLU: E(x) = W_down (silu(W_gate x) * (W_up x)), silu(z) = z / (1 + e^-z);
   * a position flagged both live and decoded, or neither, is treated as live;
     a decoded -> live transition is an anomaly that makes the whole iteration
@@ -146,10 +153,17 @@ class Router:
     order while the chosen ones hold fewer than k eligible experts; the
     selection is the top-k of c over the eligible experts of the chosen groups
     (c desc, lower id first); weights = s of the selected experts divided by
-    their sum."""
+    their sum.
+
+    renormalize=False keeps the router's own scores as the weights instead of
+    dividing them by the selection's sum: for "softmax" the dense router
+    probability of each selected expert (softmax of G over all E experts, so the
+    weights add up to the selection's share of the routing mass), for
+    "sigmoid_group" the selected sigmoid scores s."""
     kind: str = "softmax"
     n_group: int = 1
     topk_group: int = 1
+    renormalize: bool = True
 
 
 def sigmoid(z: np.ndarray) -> np.ndarray:
@@ -188,13 +202,27 @@ def chosen_groups(scores: np.ndarray, n_elig: np.ndarray, topk_group: int, k: in
     return chosen
 
 
+def dense_probabilities(g_row: np.ndarray) -> np.ndarray:
+    """Softmax of one position's router logits over all experts."""
+    ex = np.exp(g_row - np.max(g_row))
+    return ex / np.sum(ex)
+
+
+def selection_weights(g_row: np.ndarray, sel: np.ndarray, router: Router) -> np.ndarray:
+    """Weights of the selected experts (see Router)."""
+    if router.kind == "softmax":
+        return renorm_softmax(g_row[sel]) if router.renormalize else dense_probabilities(g_row)[sel]
+    s = sigmoid(g_row[sel])
+    return s / np.sum(s) if router.renormalize else s
+
+
 def route_position(g_row: np.ndarray, b_router: np.ndarray, eligible: np.ndarray, k: int,
                    router: Router) -> Tuple[np.ndarray, np.ndarray]:
     """(selected experts in selection order, their weights) of one position
     whose router logits are g_row (bias already included for "softmax")."""
     if router.kind == "softmax":
         sel = topk_select(g_row, eligible, k)
-        return sel, renorm_softmax(g_row[sel])
+        return sel, selection_weights(g_row, sel, router)
     s = sigmoid(g_row)
     c = s + b_router
     E = g_row.shape[0]
@@ -203,7 +231,7 @@ def route_position(g_row: np.ndarray, b_router: np.ndarray, eligible: np.ndarray
     groups = chosen_groups(group_scores(c, eligible, router.n_group), n_elig, router.topk_group, k)
     in_groups = np.repeat(groups, gs)
     sel = topk_select(c, eligible & in_groups, k)
-    return sel, s[sel] / np.sum(s[sel])
+    return sel, selection_weights(g_row, sel, router)
 
 
 def route_near_tie(g_row: np.ndarray, b_router: np.ndarray, eligible: np.ndarray, k: int,
@@ -427,6 +455,8 @@ class IterResult:
     host_fallback: bool
     classified: Classified
     slot: np.ndarray              # [|F|, k] worklist row of selection (f, j)
+    shortfall_prev: bool = False  # full fresh because the previous iteration's support coverage fell short
+    n_under: int = 0              # fresh positions under the coverage floor (coverage check on)
 
     @property
     def n_edges(self) -> int:
@@ -446,7 +476,8 @@ class LayerOracle:
                  w_router: np.ndarray, b_router: np.ndarray,
                  expert: Callable[[int], ExpertWeights],
                  shared: Sequence[ExpertWeights] = (), residual: bool = False,
-                 max_positions: int, router: Router = Router(), request_size: Optional[int] = None):
+                 max_positions: int, router: Router = Router(), request_size: Optional[int] = None,
+                 coverage: Optional[Tuple[float, float]] = None):
         self.E = n_experts
         self.k = top_k
         self.tau = tau
@@ -472,6 +503,9 @@ class LayerOracle:
         self.request_size = request_size
         self.request_masks: Optional[np.ndarray] = None
         self.request_plans: List[PlanResult] = []
+        # support-coverage check (alpha, q) or None: see coverage_shortfall
+        self.coverage = coverage
+        self.shortfall = False
 
     def logits(self, x: np.ndarray) -> np.ndarray:
         """Router logits G (the bias is part of G only for the softmax router)."""
@@ -483,10 +517,7 @@ class LayerOracle:
         return route_position(g_row, self.b_router, eligible, self.k, self.router)
 
     def weights(self, g_row: np.ndarray, sel: np.ndarray) -> np.ndarray:
-        if self.router.kind == "softmax":
-            return renorm_softmax(g_row[sel])
-        s = sigmoid(g_row[sel])
-        return s / np.sum(s)
+        return selection_weights(g_row, sel, self.router)
 
     def near_tie(self, g_row: np.ndarray, eligible: np.ndarray, eps: float = 1e-5) -> bool:
         return route_near_tie(g_row, self.b_router, eligible, self.k, self.router, eps)
@@ -545,6 +576,7 @@ class LayerOracle:
         self.planned = True
         self.n_pos = N
         self.last_iter = -1
+        self.shortfall = False
         return self.plan
 
     # hot-update path ([W] "cold、hot-update、hot-skip": inside a block, the
@@ -562,6 +594,27 @@ class LayerOracle:
     def block_end(self) -> None:
         self.planned = False
 
+    def coverage_shortfall(self, G: np.ndarray, fresh_pos: np.ndarray) -> Tuple[int, bool]:
+        """Support coverage of an iteration's fresh positions ([W] "cold、
+        hot-update、hot-skip": a support that no longer covers the routing sends
+        the layer back to the full fresh path; [W] "Expert Atlas" defines the
+        coverage). For fresh position t: the dense selection D_t (the router's
+        rule with every expert eligible), R_t = the sum of its raw scores (dense
+        probabilities, or sigmoid scores), C_t = the part of that sum whose
+        experts are in t's support. t is under-covered when C_t < alpha R_t; the
+        support falls short when more than (1 - q) |F| fresh positions are.
+        Returns (under-covered count, shortfall)."""
+        alpha, q = self.coverage
+        everyone = np.ones(self.E, dtype=bool)
+        raw = Router(self.router.kind, self.router.n_group, self.router.topk_group, False)
+        n_under = 0
+        for t in fresh_pos:
+            sel, w = route_position(G[t], self.b_router, everyone, self.k, raw)
+            inside = self.eligible_for(int(t))[sel]
+            if np.sum(w[inside]) < alpha * np.sum(w):
+                n_under += 1
+        return n_under, n_under > (1.0 - q) * len(fresh_pos)
+
     def iterate(self, x: np.ndarray, live: np.ndarray, decoded: np.ndarray, i: int,
                 adopt: Optional[Callable[[int, np.ndarray, np.ndarray, np.ndarray],
                                          Optional[np.ndarray]]] = None,
@@ -578,12 +631,13 @@ class LayerOracle:
         stays restricted to the support and nothing else changes."""
         N = x.shape[0]
         host_fallback = (not self.planned) or (i != self.last_iter + 1) or (N != self.n_pos)
+        short_prev = self.shortfall and not host_fallback
         if hot_update:
             self.hot_update(x)
         G = self.logits(x)
         R = 0 if refresh else self.R
-        cl = classify_positions(live, decoded, self.prev_decoded, self.stamp, i, R, host_fallback)
-        fallback = host_fallback or cl.anomaly
+        cl = classify_positions(live, decoded, self.prev_decoded, self.stamp, i, R, host_fallback or short_prev)
+        fallback = host_fallback or short_prev or cl.anomaly
         everyone = np.ones(self.E, dtype=bool)
 
         fresh_pos = np.nonzero(cl.fresh)[0]
@@ -640,10 +694,15 @@ class LayerOracle:
         if self.residual:
             y = y + x
 
+        n_under = 0
+        if self.coverage is not None:
+            n_under, self.shortfall = self.coverage_shortfall(G, fresh_pos)
+        else:
+            self.shortfall = False
         self.prev_decoded[:N] = ~cl.is_live
         self.last_iter = i
         return IterResult(y, G, fresh_pos, sel, w, wl_expert, wl_pos, wl_j, offsets, routed,
-                          fallback, host_fallback, cl, slot)
+                          fallback, host_fallback, cl, slot, short_prev, n_under)
 
 
 def dense_moe(x: np.ndarray, w_router: np.ndarray, b_router: np.ndarray,

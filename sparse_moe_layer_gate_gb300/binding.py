@@ -25,7 +25,9 @@ class epoch_layer_config(C.Structure):
                 ("top_k", C.c_int32), ("n_shared", C.c_int32), ("shared_inter", C.c_int32),
                 ("max_positions", C.c_int32), ("dtype", C.c_int32), ("tau", C.c_double),
                 ("refresh_R", C.c_int32), ("residual", C.c_int32), ("router", C.c_int32),
-                ("n_group", C.c_int32), ("topk_group", C.c_int32)]
+                ("n_group", C.c_int32), ("topk_group", C.c_int32), ("raw_weights", C.c_int32),
+                ("coverage_check", C.c_int32), ("coverage_alpha", C.c_double), ("coverage_q", C.c_double),
+                ("request_size", C.c_int32)]
 
 
 class epoch_layer_weights(C.Structure):
@@ -36,7 +38,7 @@ class epoch_layer_weights(C.Structure):
 
 STATS_FIELDS = ("iteration", "n_pos", "n_live", "n_new", "n_miss", "n_stale", "n_forced", "n_reuse",
                 "n_fresh", "n_edges", "n_hit_experts", "support_len", "fallback", "bad_flags",
-                "tiles_up", "tiles_down")
+                "tiles_up", "tiles_down", "n_under")
 
 
 class epoch_iter_stats(C.Structure):
@@ -53,7 +55,8 @@ class epoch_debug_view(C.Structure):
                 ("sel", C.c_void_p), ("sel_w", C.c_void_p), ("offsets", C.c_void_p),
                 ("wl_pos", C.c_void_p), ("slot", C.c_void_p), ("stamp", C.c_void_p),
                 ("cache", C.c_void_p), ("stats", C.c_void_p), ("error_word", C.c_void_p),
-                ("trace", C.c_void_p), ("timeline", C.c_void_p)]
+                ("trace", C.c_void_p), ("timeline", C.c_void_p), ("support_masks", C.c_void_p),
+                ("request_ids", C.c_void_p), ("request_len", C.c_void_p)]
 
 
 class epoch_profile(C.Structure):

@@ -69,6 +69,11 @@ bool valid_config(const epoch_layer_config *c) {
   if (c->dtype == EPOCH_BF16 && c->hidden % kBmDn) return false;  // down tiles cover 256 rows of H
   if (c->n_shared > 0 && c->shared_inter % q) return false;
   if (c->router != EPOCH_ROUTER_SOFTMAX && c->router != EPOCH_ROUTER_SIGMOID_GROUP) return false;
+  if (c->raw_weights != 0 && c->raw_weights != 1) return false;
+  if (c->request_size < 0 || c->request_size > c->max_positions) return false;
+  if (c->coverage_check && !(c->coverage_alpha >= 0.0 && c->coverage_alpha <= 1.0 && c->coverage_q >= 0.0 &&
+                             c->coverage_q <= 1.0))
+    return false;
   if (c->router == EPOCH_ROUTER_SIGMOID_GROUP &&
       (c->n_group < 1 || c->n_group > 32 || c->n_experts % c->n_group || c->topk_group < 1 ||
        c->topk_group > c->n_group))
@@ -92,9 +97,12 @@ size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   Work t;
   t.stamp = static_cast<int32_t *>(take(2 * N * 4));
   t.prev_dec = static_cast<uint8_t *>(take(2 * N));
-  t.support_mask = static_cast<uint8_t *>(take(E));
+  const size_t R = c.request_size > 0 ? (N + c.request_size - 1) / c.request_size : 1;
+  t.support_mask = static_cast<uint8_t *>(take(R * E));
   t.support_ids = static_cast<int32_t *>(take(E * 4));
-  t.plan_counts = static_cast<int32_t *>(take(E * 4));
+  t.plan_counts = static_cast<int32_t *>(take(R * E * 4));
+  t.req_ids = static_cast<int32_t *>(take(R * E * 4));
+  t.req_len = static_cast<int32_t *>(take(R * 4));
   t.cache = take(N * H * act);
   t.logits = static_cast<float *>(take(N * E * 4));
   t.cat = static_cast<uint8_t *>(take(N));
@@ -103,10 +111,10 @@ size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   t.sel = static_cast<int32_t *>(take(N * k * 4));
   t.selw = static_cast<float *>(take(N * k * 4));
   t.sel_words = static_cast<uint32_t *>(take(2 * chunks * E * 4));
-  t.pre = static_cast<int32_t *>(take(chunks * E * 4));
   t.offsets = static_cast<int32_t *>(take((E + 1) * 4));
   t.grp_list = static_cast<int32_t *>(take((E + nsh + 1) * 4));
   t.done_up = static_cast<int32_t *>(take((E + nsh) * 4));
+  t.cov_under = static_cast<int32_t *>(take(8));
   t.tile_ctr = static_cast<int32_t *>(take(16));
   t.sh_ctr = static_cast<int32_t *>(take(2 * (1 + nsh * ((N + kTnUp - 1) / kTnUp)) * 4));
   t.wl_pos = static_cast<int32_t *>(take(N * k * 4));
@@ -170,6 +178,11 @@ epoch_status run(epoch_layer *L, Kind kind, cudaStream_t s, F &&launch) {
     const epoch_status st_ = (expr);          \
     if (st_ != EPOCH_OK) return st_;          \
   } while (0)
+
+// Support rows of the plan: one per request with per-request supports, else one.
+size_t plan_rows(const epoch_layer_config &c, int32_t n_pos) {
+  return c.request_size > 0 ? static_cast<size_t>((n_pos + c.request_size - 1) / c.request_size) : 1;
+}
 
 Dims call_dims(const epoch_layer *L, int32_t n_pos, int32_t iter, int host_fallback) {
   Dims d = L->dims;
@@ -235,6 +248,11 @@ epoch_status epoch_layer_create(const epoch_layer_config *cfg, const epoch_layer
   d.router = cfg->router;
   d.n_group = cfg->router ? cfg->n_group : 1;
   d.topk_group = cfg->router ? cfg->topk_group : 1;
+  d.raw_weights = cfg->raw_weights;
+  d.req_size = cfg->request_size;
+  d.cov_check = cfg->coverage_check ? 1 : 0;
+  d.cov_alpha = static_cast<float>(cfg->coverage_alpha);
+  d.cov_q = static_cast<float>(cfg->coverage_q);
   d.tn = L->bf16 ? kTnUp : 0;
   d.cmax = (cfg->max_positions + 31) / 32;
   d.timeout_ns = 2000000000ll;
@@ -260,7 +278,7 @@ epoch_status epoch_layer_create(const epoch_layer_config *cfg, const epoch_layer
   // empty cache, no plan: zero the workspace, stamps = -1, support = every expert
   if (cudaMemset(workspace, 0, bytes) != cudaSuccess ||
       cudaMemset(L->ws.stamp, 0xFF, 2 * sizeof(int32_t) * d.Nmax) != cudaSuccess ||
-      cudaMemset(L->ws.support_mask, 1, d.E) != cudaSuccess) {
+      cudaMemset(L->ws.support_mask, 1, plan_rows(*cfg, d.Nmax) * d.E) != cudaSuccess) {
     delete L;
     return EPOCH_ECUDA;
   }
@@ -311,13 +329,14 @@ epoch_status epoch_plan_block(epoch_layer *L, const void *x, int32_t n_pos, epoc
   d.plan_mode = 1;
   CUtensorMap x_map_up;
   EPOCH_TRY(run_gate(L, d, x, nullptr, nullptr, &x_map_up, s));
-  if (cudaMemsetAsync(L->ws.plan_counts, 0, sizeof(int32_t) * d.E, s) != cudaSuccess) return EPOCH_ECUDA;
+  if (cudaMemsetAsync(L->ws.plan_counts, 0, sizeof(int32_t) * d.E * plan_rows(L->cfg, n_pos), s) != cudaSuccess)
+    return EPOCH_ECUDA;
   EPOCH_TRY(run(L, K_PLAN_TOPK, s, [&] { return launch_plan_topk(d, L->w, L->ws, s); }));
   const double tau = L->cfg.tau;
   const int all = tau >= 1.0;
   const int32_t T = static_cast<int32_t>(std::ceil(tau * static_cast<double>(n_pos * L->cfg.top_k)));
   EPOCH_TRY(run(L, K_PLAN_SUPPORT, s,
-                [&] { return launch_plan_support(d, L->ws, T, all, 1, support_ids_dev, support_len_dev, s); }));
+                [&] { return launch_plan_support(d, L->ws, T, all, 1, support_ids_dev, support_len_dev, tau, s); }));
   L->planned = true;
   L->n_pos_plan = n_pos;
   L->last_iter = -1;
@@ -349,13 +368,14 @@ epoch_status epoch_moe_iter_path(epoch_layer *L, const void *x, const uint8_t *l
     // (block-plan rule, state kept), then classification and top-k over it
     d.plan_mode = 1;
     EPOCH_TRY(run_gate(L, d, x, live, decoded, &x_map_up, s));
-    if (cudaMemsetAsync(L->ws.plan_counts, 0, sizeof(int32_t) * d.E, s) != cudaSuccess) return EPOCH_ECUDA;
+    if (cudaMemsetAsync(L->ws.plan_counts, 0, sizeof(int32_t) * d.E * plan_rows(L->cfg, n_pos), s) != cudaSuccess)
+      return EPOCH_ECUDA;
     EPOCH_TRY(run(L, K_PLAN_TOPK, s, [&] { return launch_plan_topk(d, L->w, L->ws, s); }));
     const double tau = L->cfg.tau;
     const int all = tau >= 1.0;
     const int32_t T = static_cast<int32_t>(std::ceil(tau * static_cast<double>(n_pos * L->cfg.top_k)));
     EPOCH_TRY(run(L, K_PLAN_SUPPORT, s,
-                  [&] { return launch_plan_support(d, L->ws, T, all, 0, nullptr, nullptr, s); }));
+                  [&] { return launch_plan_support(d, L->ws, T, all, 0, nullptr, nullptr, tau, s); }));
     d.plan_mode = 0;
     EPOCH_TRY(run(L, K_SELECT, s, [&] { return launch_select(d, L->ws, live, decoded, L->w.b_router, s); }));
     ++L->n_hot_update;
@@ -363,15 +383,15 @@ epoch_status epoch_moe_iter_path(epoch_layer *L, const void *x, const uint8_t *l
     EPOCH_TRY(run_gate(L, d, x, live, decoded, &x_map_up, s));
   }
   if (path & EPOCH_PATH_REFRESH) ++L->n_refresh;
-  EPOCH_TRY(run(L, K_ROUTING, s, [&] { return launch_route(d, L->ws, s); }));
-  L->state_rd ^= 1;  // this iteration wrote the new state into the other half
   if (L->bf16) {
-    EPOCH_TRY(run(L, K_PERMUTE, s, [&] { return launch_permute(d, L->ws, x, s); }));
+    // the expert kernel builds the worklist itself (worklist.cuh)
     EPOCH_TRY(run(L, K_UP, s, [&] { return launch_experts_tc(d, L->maps, L->ws, x_map_up, x, s); }));
   } else {
+    EPOCH_TRY(run(L, K_ROUTING, s, [&] { return launch_route(d, L->ws, s); }));
     EPOCH_TRY(run(L, K_UP, s, [&] { return launch_up_simt(d, L->w, L->ws, x, s); }));
     EPOCH_TRY(run(L, K_DOWN, s, [&] { return launch_down_simt(d, L->w, L->ws, s); }));
   }
+  L->state_rd ^= 1;  // this iteration wrote the new state into the other half
   EPOCH_TRY(run(L, K_COMBINE, s, [&] { return launch_combine(d, L->ws, x, y, L->bf16, s); }));
   L->last_iter = iteration;
   if (host_fallback) ++L->n_fallback;
@@ -433,6 +453,9 @@ epoch_status epoch_debug_pointers(epoch_layer *L, epoch_debug_view *v) {
   v->timeline = reinterpret_cast<const int64_t *>(L->ws.timeline);
   v->stats = L->ws.stats;
   v->error_word = L->ws.err;
+  v->support_masks = L->ws.support_mask;
+  v->request_ids = L->ws.req_ids;
+  v->request_len = L->ws.req_len;
   return EPOCH_OK;
 }
 

@@ -29,6 +29,7 @@
 #include "common.cuh"
 #include "layer.h"
 #include "select.cuh"
+#include "worklist.cuh"
 
 namespace epoch {
 
@@ -97,6 +98,24 @@ struct __align__(128) GateParams {
 // done), the reduced rows [TN / CS][E_pad], the support mask [1024], barriers.
 __host__ __device__ inline int gate_e_pad(int E) { return ((E + 127) / 128) * 128; }
 __host__ __device__ inline int gate_stage_bytes(int E, int TN) { return (gate_e_pad(E) / 128) * kTileBytes + TN * 64 * 2; }
+
+// One position of the gate's epilogue: records its classification and, if it
+// is fresh, takes its top-k (one warp; row = its reduced logits).
+template <int EPL>
+__device__ __forceinline__ void gate_position(const Dims &d, const Work &ws, int t, int code, int32_t stamp,
+                                              const float *row, int E_pad, const uint8_t *support, bool force,
+                                              uint32_t *words, uint2 *scratch, const float *bias) {
+  const bool fresh = force || (code & 15) != C_REUSE;
+  if (lane_id() == 0) record_position(d, ws, t, code, fresh ? d.iter : stamp);
+  if (!fresh) return;
+  float v[EPL];
+#pragma unroll
+  for (int c = 0; c < EPL; ++c) {
+    const int e = lane_id() * EPL + c;
+    v[c] = e < E_pad ? row[e] : -INFINITY;
+  }
+  select_position<EPL>(d, ws, t, v, support, force, words, scratch, bias);
+}
 
 // 12 warps: 0 issues the TMA loads, 1 the MMAs, 4-7 read TMEM; all of them
 // reduce, and each takes the top-k of one of the CTA's positions (up to 12).
@@ -251,6 +270,7 @@ __global__ void __maxnreg__(104) k_tc_gate(const __grid_constant__ GateParams p)
       if (any_anomaly(d, p.live, p.decoded, ws.prev_dec + static_cast<size_t>(rd) * d.Nmax, tid - 64,
                       kGateThreads - 64))
         atomicOr(s_anom, 1);
+      if (tid == 64 && shortfall_flag(d, ws)) atomicOr(s_anom, 2);
     }
   }
   if (wid >= 4 && wid < 8) {
@@ -276,6 +296,7 @@ __global__ void __maxnreg__(104) k_tc_gate(const __grid_constant__ GateParams p)
   tc_fence_before();
   __syncthreads();
   if (trace2 && tid == 0) trace2[0] = static_cast<int64_t>(globaltimer_ns());
+  if (!d.plan_mode && blockIdx.x == 0) reset_iteration_state(d, ws, *s_anom);
   if (wid == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, tcols);
@@ -346,17 +367,10 @@ __global__ void __maxnreg__(104) k_tc_gate(const __grid_constant__ GateParams p)
     for (int j = wid; j < TPC; j += kGateThreads / 32) {
       const int t = t_own + j;
       if (t >= d.n_pos) continue;
-      const int code = s_code[j];
-      const bool fresh = force || (code & 15) != C_REUSE;
-      if (lane == 0) record_position(d, ws, t, code, fresh ? d.iter : s_stamp[j]);
-      if (!fresh) continue;
-      float v[EPL];
-#pragma unroll
-      for (int c = 0; c < EPL; ++c) {
-        const int e = lane * EPL + c;
-        v[c] = e < E_pad ? rows[j * E_pad + e] : -INFINITY;
-      }
-      select_position<EPL>(d, ws, t, v, s_support, force, words, s_scr + 32 * wid, s_bias);
+      // per-request supports: the position's request's mask (read from global memory)
+      const uint8_t *mask = d.req_size > 0 ? ws.support_mask + static_cast<size_t>(t / d.req_size) * d.E : s_support;
+      gate_position<EPL>(d, ws, t, s_code[j], s_stamp[j], rows + j * E_pad, E_pad, mask, force, words,
+                         s_scr + 32 * wid, s_bias);
     }
   }
   if (trace && tid == 0) {
@@ -396,13 +410,7 @@ constexpr int kExpOffOffs = kExpOffPref + 4 * kExpGroups;         // int32 [kExp
 constexpr int kExpSmem = 1024 + kExpOffOffs + 4 * kExpGroups;
 static_assert(kExpSmem <= 227 * 1024, "shared memory");
 static_assert(kTnUp == kTnDn, "up and down tiles share the token tiling");
-
-// The shared experts' up tiles need no routing: with kSharedUpEarly the expert
-// kernel runs them while the gate and worklist kernels still run (phase A);
-// otherwise they lead the tile list that follows the worklist (measured
-// slightly faster on the LLaDA2.0-mini-shaped layer: CTAs that took shared
-// tiles early were late for the routed ones).
-constexpr bool kSharedUpEarly = false;
+static_assert(sizeof(WlSmem) <= 4 * kExpStg, "the worklist scratch fits in the epilogue staging area");
 
 // Decoded tile as handed through the ring: x = group | kDownBit for a down
 // tile (-1 ends the stream), y = row block, z = first token row, w = valid rows.
@@ -586,33 +594,35 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   if (trace && threadIdx.x == 0) trace[1] = static_cast<int64_t>(globaltimer_ns());
-  // The prologue above may overlap the gate and worklist kernels (programmatic
-  // dependent launch). Shared-expert tiles need no routing and start at once;
-  // the routed tiles wait until the worklist kernel has published this call's
-  // worklist (route_done = this call's sequence number, acquire).
+  // The prologue above may overlap the gate (programmatic dependent launch).
+  // Once the gate has finished, every CTA builds the worklist's offsets and
+  // group list itself (all 192 threads, from the gate's selection words) and
+  // copies its share of the worklist rows into xp. The producer streams no
+  // tile until every CTA has copied its rows (tile_ctr[2]): these steps are
+  // chains of dependent memory accesses, and weight streams running beside
+  // them make every access wait behind them. The epilogue warps meanwhile do
+  // this CTA's share of the bookkeeping before their first epilogue. The
+  // scratch of the worklist build lives in the epilogue staging area.
   const int par = static_cast<int>(d.seq & 1u);
   int32_t *shc = ws.sh_ctr + static_cast<size_t>(par) * sh_stride(d);  // [0] tile counter, then done counts
   const int nt_max = (d.Nmax + kTnUp - 1) / kTnUp;
   const int nt_sh = (d.n_pos + kTnUp - 1) / kTnUp;
   const int n_sh_up = d.tn > 0 ? d.n_sh * nt_sh * (d.I_s / BM) : 0;
   const int n_sh_dn = d.tn > 0 ? d.n_sh * nt_sh * (d.H / kBmDn) : 0;
-  auto wait_worklist = [&]() -> bool {
-    const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-      unsigned int v;
-      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ws.route_done) : "memory");
-      if (v == d.seq) return true;
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > tmo) {
-        set_error(ws.err, EPOCH_DEVERR_TIMEOUT);
-        *abort_flag = 1;
-        return false;
-      }
-      __nanosleep(32);
-    }
-  };
+  WlSmem &wsm = *reinterpret_cast<WlSmem *>(stage_out);
+  int64_t *trace_wl = (d.trace && blockIdx.x == 0) ? ws.trace + 3ull * kTraceCtas * kTraceFields : nullptr;
+  const Group all{static_cast<int>(threadIdx.x), 192, 0};
+  const Group epi{static_cast<int>(threadIdx.x) - 64, 128, 2};
+  if (trace_wl && threadIdx.x == 0) trace_wl[0] = static_cast<int64_t>(globaltimer_ns());
+  wl_prepare(d, ws, wsm, s_offs, all);
+  pdl_wait();  // the gate has finished: selection words, selections, codes, anomaly flag
+  if (trace_wl && threadIdx.x == 0) trace_wl[1] = static_cast<int64_t>(globaltimer_ns());
+  const WlPlan wl = wl_phase_a(d, ws, wsm, s_offs, s_list, blockIdx.x == 0, all);
+  if (trace_wl && threadIdx.x == 0) trace_wl[2] = static_cast<int64_t>(globaltimer_ns());
+  // this CTA's worklist rows (positions, and x rows into xp) before any tile streams
+  wl_rows(d, ws, wsm, s_offs, wl, p.x, p.vec_per_row, blockIdx.x, gridDim.x, all);
+  if (trace_wl && threadIdx.x == 0) trace_wl[4] = static_cast<int64_t>(globaltimer_ns());
 
-  int64_t *trace7 = trace ? ws.trace + (6ull * kTraceCtas + blockIdx.x) * kTraceFields : nullptr;
   if (wid == 0) {
     // ---------------- producer warp (lane 0 issues): per K block, a 32 KB run of
     // packed weights (bulk copy) and the tile's token rows (tiled TMA load: x
@@ -695,43 +705,34 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
       return true;
     };
     if (lane == 0) {
+      if (trace) trace[2] = static_cast<int64_t>(globaltimer_ns());
       tma_prefetch_desc(&p.bs);
       tma_prefetch_desc(&p.bs2);
-      // phase A: the shared experts' up tiles (they read x; no routing needed)
-      while (ok && kSharedUpEarly) {
-        const int q = atomicAdd(shc, 1);
-        if (q >= n_sh_up) break;
-        int need, tt;
-        const int4 td = shared_tile(d, q, &need, &tt);
-        ok = post(td) && issue(td, nullptr, 0, 0);
-      }
-      if (trace) trace7[3] = static_cast<int64_t>(globaltimer_ns());
-      if (ok) ok = wait_worklist();
-      if (trace) trace7[4] = static_cast<int64_t>(globaltimer_ns());
-    }
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    // phase B: the routed experts' tiles
-    if (ok) {
-      for (int i = lane; i <= d.E; i += 32) {
-        s_list[i] = ws.grp_list[i];
-        s_offs[i] = ws.offsets[i];
-      }
-    }
-    __syncwarp();
-    if (lane == 0) {
-      if (trace) trace[2] = static_cast<int64_t>(globaltimer_ns());
       tma_prefetch_desc(&p.b[0]);
       tma_prefetch_desc(&p.b2[0]);
-      // tile list of this phase, in segments: [the shared experts' up tiles,
-      // unless phase A ran them], routed up tiles, the shared experts' down
-      // tiles, routed down tiles
-      const int n_up = ok ? ws.ctrl->tiles_up : 0;
-      const int sh_up_here = kSharedUpEarly ? 0 : n_sh_up;
-      const int seg_end[4] = {sh_up_here, sh_up_here + n_up, sh_up_here + n_up + n_sh_dn,
-                              sh_up_here + n_up + n_sh_dn + (ok ? ws.ctrl->tiles_dn : 0)};
+      // tile list, in segments: the shared experts' up tiles, routed up tiles,
+      // the shared experts' down tiles, routed down tiles
+      const int n_up = d.tn > 0 ? (d.I / BM) * wl.n_tiles : 0;
+      const int seg_end[4] = {n_sh_up, n_sh_up + n_up, n_sh_up + n_up + n_sh_dn,
+                              n_sh_up + n_up + n_sh_dn + (d.tn > 0 ? (d.H / kBmDn) * wl.n_tiles : 0)};
       const int total = ok ? seg_end[3] : 0;
-      const int L = s_offs[d.E];
-      const int copied = L * p.vec_per_row;  // vectors the permute kernel copies into xp
+      const int copied = wl.n_edges * p.vec_per_row;  // vectors the CTAs copy into xp
+      {  // no weight stream before every CTA's worklist steps are done
+        const uint64_t t0 = globaltimer_ns();
+        for (;;) {
+          int done;
+          asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(done) : "l"(ws.tile_ctr + 2) : "memory");
+          if (done >= copied) break;
+          if (globaltimer_ns() - t0 > tmo) {
+            set_error(ws.err, EPOCH_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          __nanosleep(200);  // 152 pollers of one line: keep its traffic low
+        }
+        if (trace) trace[2] = static_cast<int64_t>(globaltimer_ns());
+      }
       while (ok) {
         const int tile = atomicAdd(ws.tile_ctr, 1);
         if (tile >= total) break;
@@ -770,6 +771,7 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
           if (armed & (1u << s)) mbar_drain(full_bar(s), (armed_par >> s) & 1u, 50000000ull);
       }
       if (trace) {
+        int64_t *trace7 = ws.trace + (6ull * kTraceCtas + blockIdx.x) * kTraceFields;
         trace[6] = static_cast<int64_t>(waited);
         trace7[0] = waited_by[0];
         trace7[1] = waited_by[1];
@@ -839,6 +841,9 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
     }
     __syncwarp();
   } else if (wid >= 2) {
+    // ---------------- worklist bookkeeping of this CTA (for the combine)
+    wl_bookkeeping(d, ws, wsm, s_offs, wl, blockIdx.x, gridDim.x, epi, trace_wl);
+    if (trace_wl && threadIdx.x == 64) trace_wl[3] = static_cast<int64_t>(globaltimer_ns());
     // ---------------- epilogue (warps 2..5; warp w reads TMEM lanes 32*(w%4)..)
     const int q = wid & 3;
     uint8_t *stg = stage_out + (wid - 2) * kExpStg;
@@ -961,10 +966,6 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
       tr2[7] = trace[7];
     }
   }
-  // The worklist kernel finishes its bookkeeping (fresh list, slots, statistics)
-  // after publishing the worklist; this grid completes only after it, so the
-  // combine kernel, which waits for this grid, sees those writes.
-  if (threadIdx.x == 0) pdl_wait();
   tc_fence_before();
   __syncthreads();
   if (wid == 0) {

@@ -20,7 +20,9 @@ struct Ctrl {
   int32_t tiles_up;     // grouped-GEMM tiles (routed + shared)
   int32_t tiles_dn;
   int32_t support_len;  // |S| of the current plan
-  int32_t pad;
+  int32_t anom;         // full fresh from the device, set by the classifying kernel: bit 0 a decoded ->
+                        // live transition, bit 1 the previous iteration's coverage shortfall
+  int32_t short_next;   // the support coverage fell short: the next iteration runs full fresh
 };
 
 // Device pointers carved from the caller's workspace.
@@ -29,9 +31,11 @@ struct Work {
   int32_t *stamp;         // [2][Nmax] iteration of the row's last fresh compute, -1 none
   uint8_t *prev_dec;      // [2][Nmax] decoded at the previous iteration
                           // (both double-buffered: an iteration reads half state_rd, writes the other)
-  uint8_t *support_mask;  // [E]
-  int32_t *support_ids;   // [E] ranked experts
-  int32_t *plan_counts;   // [E] block-start hit counts
+  uint8_t *support_mask;  // [R][E] the block's support (R = 1), or one per request (R = requests)
+  int32_t *support_ids;   // [E] ranked experts (per-request supports: their union, ascending)
+  int32_t *plan_counts;   // [R][E] block-start hit counts (per request)
+  int32_t *req_ids;       // [R][E] per-request supports: ranked experts of each request
+  int32_t *req_len;       // [R] and each request's |S|
   void *cache;            // [Nmax][H] routed-output cache, layer dtype
   // one iteration
   float *logits;          // [Nmax][E] G = x W_r^T + b (gate kernel)
@@ -42,13 +46,14 @@ struct Work {
   float *selw;            // [Nmax][k] their routing weights
   uint32_t *sel_words;    // [2][E][cmax] bit t%32 of word (e, t/32): fresh position t selected expert e;
                           // the iteration writes half state_rd ^ 1 and clears half state_rd
-  int32_t *pre;           // [E][cmax] selected positions of expert e in words before word c
   int32_t *offsets;       // [E+1]
   int32_t *grp_list;      // [E + n_sh + 1] expert-kernel groups in list order: token tiles of the
                           // groups before << kGrpIdBits | group (shared experts E..E+n_sh-1)
   int32_t *done_up;       // [E + n_sh] up tiles of each group finished this iteration (by group id)
+  int32_t *cov_under;     // [2 (call parity)] fresh positions under the coverage floor
   int32_t *tile_ctr;      // routed tiles: [0] next tile of the expert kernel (dynamic scheduling),
-                          // [2] 16-byte vectors of worklist rows copied into xp
+                          // [2] 16-byte vectors of worklist rows copied into xp (both reset by the
+                          // classifying kernel of the iteration)
   int32_t *sh_ctr;        // shared-expert tiles, [2 (call parity)][sh_stride]: [0] next tile, then the
                           // finished up tiles of each (shared expert, token tile)
   int32_t *wl_pos;        // [Nmax*k] expert-sorted worklist positions
@@ -65,7 +70,7 @@ struct Work {
   uint8_t *pk_d;          // routed W_down: [E*H/256][I/64] x (two 128-row tiles) = 32 KB
   uint8_t *pk_sgu;        // shared W_gate/W_up: [n_sh*I_s/128][H/64] x 32 KB
   uint8_t *pk_sd;         // shared W_down: [n_sh*H/256][I_s/64] x 32 KB
-  unsigned int *route_done;  // sequence number of the last call whose worklist is complete
+  unsigned int *route_done;  // sequence number of the last call whose expert offsets and group list are out
   int64_t *trace;         // [kTraceRows][kTraceCtas][8] per-CTA timeline (when tracing)
   unsigned long long *timeline;  // [2][K_NUM]: first CTA entry, last CTA exit per kernel kind (ns)
   Ctrl *ctrl;
@@ -81,7 +86,7 @@ constexpr int kTraceFields = 8;
 constexpr int kTraceRows = 9;
 
 constexpr int kTileBytes = 128 * 64 * 2;  // one packed 128 x 64 bf16 tile
-constexpr int kRouteThreads = 512;        // the one CTA of the worklist kernel
+constexpr int kRouteThreads = 256;        // threads per CTA of the worklist kernel
 
 // Shapes and per-call values handed to every kernel by value.
 struct Dims {
@@ -98,6 +103,11 @@ struct Dims {
   int32_t plan_mode;     // gate kernels: 1 = block plan (logits only), 0 = iteration
   int32_t router;        // 0: softmax over the selected logits (bias in G); 1: group-limited sigmoid
   int32_t n_group, topk_group;  // group rule of router 1
+  int32_t raw_weights;   // 1: weights are the router's own scores (no renormalisation over the selection)
+  int32_t req_size;      // > 0: positions per request, each request with its own support
+  int32_t cov_check;     // support-coverage check: fresh positions with less than cov_alpha of their
+  float cov_alpha, cov_q;  // dense selection's mass on the support; more than (1 - cov_q) |F| of them
+                           // make the next iteration full fresh
   uint32_t seq;          // sequence number of this call (route_done handshake)
   int64_t timeout_ns;
   epoch_iter_stats *stats_out;  // caller's copy of this iteration's statistics (nullable)
@@ -124,7 +134,7 @@ constexpr int kBoxRows[4] = {32, 64, 128, 256};
 
 // Kernel kinds, for profiling and launch counting.
 enum Kind {
-  K_GATE = 0, K_PLAN_TOPK, K_PLAN_SUPPORT, K_ROUTING, K_UP, K_DOWN, K_COMBINE, K_TEST, K_SELECT, K_PERMUTE, K_NUM
+  K_GATE = 0, K_PLAN_TOPK, K_PLAN_SUPPORT, K_ROUTING, K_UP, K_DOWN, K_COMBINE, K_TEST, K_SELECT, K_NUM
 };
 extern const char *const kKindName[K_NUM];
 
@@ -161,11 +171,16 @@ cudaError_t launch_select(const Dims &d, const Work &ws, const uint8_t *live, co
                           cudaStream_t s);
 cudaError_t launch_plan_topk(const Dims &d, const Weights &w, const Work &ws, cudaStream_t s);
 // clear_state: also reset every stamp and decoded flag (a block plan; not a hot update).
-// ids_out / len_out: the caller's copies of the ranked experts and |S| (nullable).
+// ids_out / len_out: the caller's copies of the ranked experts and |S| (nullable;
+// per-request supports: of their union). threshold: the block's (one support);
+// per-request thresholds come from tau on the device.
 cudaError_t launch_plan_support(const Dims &d, const Work &ws, int32_t threshold, int all_experts,
-                                int clear_state, int32_t *ids_out, int32_t *len_out, cudaStream_t s);
+                                int clear_state, int32_t *ids_out, int32_t *len_out, double tau, cudaStream_t s);
+// The worklist kernel of fp32 layers (bf16 layers build it in the expert kernel).
 cudaError_t launch_route(const Dims &d, const Work &ws, cudaStream_t s);
-cudaError_t launch_permute(const Dims &d, const Work &ws, const void *x, cudaStream_t s);
+// CTAs that build the worklist: the worklist kernel's grid (fp32 layers) and
+// the expert kernel's (bf16 layers) are both one CTA per SM.
+int route_ctas();
 cudaError_t launch_combine(const Dims &d, const Work &ws, const void *x, void *y, int bf16, cudaStream_t s);
 cudaError_t launch_wait_test(uint32_t *err, int64_t timeout_ns, cudaStream_t s);
 

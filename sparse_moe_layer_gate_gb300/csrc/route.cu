@@ -18,76 +18,14 @@
 #include "layer.h"
 #include "select.cuh"
 #include "topk.cuh"
+#include "worklist.cuh"
 
 namespace epoch {
 
-const char *const kKindName[K_NUM] = {"gate",    "plan_topk",   "plan_support", "routing", "experts",
-                                      "expert_down", "combine", "wait_test", "select", "permute"};
+const char *const kKindName[K_NUM] = {"gate",        "plan_topk", "plan_support", "routing", "experts",
+                                      "expert_down", "combine",   "wait_test",    "select"};
 
 // ---------------------------------------------------------------- helpers
-
-// Exclusive scan over a CTA of up to 1024 threads; *total gets the sum.
-__device__ __forceinline__ int block_excl_scan(int v, int *warp_tmp, int *total) {
-  const int lane = lane_id(), wid = warp_id(), nw = (blockDim.x + 31) >> 5;
-  int incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int u = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += u;
-  }
-  if (lane == 31) warp_tmp[wid] = incl;
-  __syncthreads();
-  if (wid == 0) {
-    const int x = lane < nw ? warp_tmp[lane] : 0;
-    int xi = x;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, xi, o);
-      if (lane >= o) xi += u;
-    }
-    warp_tmp[lane] = xi - x;
-    if (lane == 31) warp_tmp[32] = xi;
-  }
-  __syncthreads();
-  const int r = warp_tmp[wid] + incl - v;
-  *total = warp_tmp[32];
-  __syncthreads();
-  return r;
-}
-
-// Exclusive scan of four values at once over a CTA of up to 1024 threads
-// (independent components, one pass); *total gets the sums.
-__device__ __forceinline__ int4 block_excl_scan4(int4 v, int4 *warp_tmp, int4 *total) {
-  const int lane = lane_id(), wid = warp_id(), nw = (blockDim.x + 31) >> 5;
-  auto scan = [&](int4 a) {
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int ux = __shfl_up_sync(0xffffffffu, a.x, o), uy = __shfl_up_sync(0xffffffffu, a.y, o);
-      const int uz = __shfl_up_sync(0xffffffffu, a.z, o), uw = __shfl_up_sync(0xffffffffu, a.w, o);
-      if (lane >= o) {
-        a.x += ux;
-        a.y += uy;
-        a.z += uz;
-        a.w += uw;
-      }
-    }
-    return a;
-  };
-  const int4 incl = scan(v);
-  if (lane == 31) warp_tmp[wid] = incl;
-  __syncthreads();
-  if (wid == 0) {
-    const int4 x = lane < nw ? warp_tmp[lane] : make_int4(0, 0, 0, 0);
-    const int4 xi = scan(x);
-    warp_tmp[lane] = make_int4(xi.x - x.x, xi.y - x.y, xi.z - x.z, xi.w - x.w);
-    if (lane == 31) warp_tmp[32] = xi;
-  }
-  __syncthreads();
-  const int4 b = warp_tmp[wid];
-  *total = warp_tmp[32];
-  __syncthreads();
-  return make_int4(b.x + incl.x - v.x, b.y + incl.y - v.y, b.z + incl.z - v.z, b.w + incl.w - v.w);
-}
 
 // ---------------------------------------------------------------- gate (SIMT)
 // G = x W_r^T + b for fp32 layers: one warp per (position, expert), lanes
@@ -135,23 +73,35 @@ __global__ void k_plan_topk(Dims d, const float *__restrict__ logits, const floa
       warp_group_limit<EPL>(v, ok, d.E, d.n_group, d.topk_group, d.k);
     }
     warp_topk<EPL>(v, ok, d.k, &sel, &val, s_scr[warp_id()]);
-    if (lane < d.k && sel >= 0) atomicAdd(&counts[sel], 1);
+    const size_t row = d.req_size > 0 ? static_cast<size_t>(t / d.req_size) * d.E : 0;
+    if (lane < d.k && sel >= 0) atomicAdd(&counts[row + sel], 1);
   }
 }
 
-// One CTA: rank experts by (count desc, id asc), take the smallest prefix whose
-// counts reach `threshold` (at least k; every expert when all_experts), and,
-// for a block plan (cold path), clear the block's stamps and previous-decoded
-// flags; a hot update keeps them.
+// One CTA per support (the block's, or request r's with per-request
+// supports): rank experts by (count desc, id asc), take the smallest prefix
+// whose counts reach the threshold (at least k; every expert when
+// all_experts) -- for a request, ceil(tau * n_r * k) over its own n_r
+// positions, formed on the device exactly as the host forms the block's --
+// and, for a block plan (cold path), clear the block's stamps, previous-decoded
+// flags and coverage state; a hot update keeps them.
 __global__ void __launch_bounds__(1024) k_plan_support(Dims d, Work ws, int32_t threshold, int all_experts,
-                                                       int clear_state, int32_t *ids_out, int32_t *len_out) {
+                                                       int clear_state, int32_t *ids_out, int32_t *len_out,
+                                                       double tau) {
   const KernelMark mark_(d, ws, K_PLAN_SUPPORT);
   __shared__ int32_t cnt[1024];
   __shared__ int32_t sorted_cnt[1024];
   __shared__ int32_t len_s;
   const int tid = threadIdx.x;
-  const int E = d.E;
-  if (tid < E) cnt[tid] = ws.plan_counts[tid];
+  const int E = d.E, r = blockIdx.x;
+  const bool per_req = d.req_size > 0;
+  if (per_req) {
+    const int n_r = min(d.req_size, d.n_pos - r * d.req_size);
+    threshold = static_cast<int32_t>(ceil(tau * static_cast<double>(n_r * d.k)));
+  }
+  int32_t *ranked = per_req ? ws.req_ids + static_cast<size_t>(r) * E : ws.support_ids;
+  uint8_t *mask = ws.support_mask + static_cast<size_t>(r) * E;
+  if (tid < E) cnt[tid] = ws.plan_counts[static_cast<size_t>(r) * E + tid];
   if (tid == 0) len_s = E;
   __syncthreads();
   if (tid < E) {
@@ -161,8 +111,8 @@ __global__ void __launch_bounds__(1024) k_plan_support(Dims d, Work ws, int32_t 
       const int ce = cnt[e];
       rank += (ce > c) || (ce == c && e < tid);
     }
-    ws.support_ids[rank] = tid;
-    if (ids_out) ids_out[rank] = tid;
+    ranked[rank] = tid;
+    if (ids_out && !per_req) ids_out[rank] = tid;
     sorted_cnt[rank] = c;
   }
   __syncthreads();
@@ -190,17 +140,66 @@ __global__ void __launch_bounds__(1024) k_plan_support(Dims d, Work ws, int32_t 
       const int ce = cnt[e];
       rank += (ce > c) || (ce == c && e < tid);
     }
-    ws.support_mask[tid] = rank < len ? 1 : 0;
+    mask[tid] = rank < len ? 1 : 0;
   }
   if (tid == 0) {
-    ws.ctrl->support_len = len;
-    if (len_out) *len_out = len;
+    if (per_req) {
+      ws.req_len[r] = len;
+    } else {
+      ws.ctrl->support_len = len;
+      if (len_out) *len_out = len;
+    }
+    if (clear_state && r == 0) ws.ctrl->short_next = 0;  // a new block starts without a coverage shortfall
   }
-  if (clear_state) {
+  if (clear_state && r == 0) {
     for (int t = tid; t < 2 * d.Nmax; t += blockDim.x) {  // both halves of the iteration state
       ws.stamp[t] = -1;
       ws.prev_dec[t] = 0;
     }
+  }
+}
+
+// Per-request supports: the union of the requests' supports (their masks,
+// rows [0, n_req)) is the layer's candidate set, in ascending expert order;
+// one CTA.
+__global__ void __launch_bounds__(1024) k_plan_union(Dims d, Work ws, int32_t *ids_out, int32_t *len_out) {
+  __shared__ int32_t tmp[33];
+  const int tid = threadIdx.x, E = d.E;
+  const int n_req = (d.n_pos + d.req_size - 1) / d.req_size;
+  int in = 0;
+  if (tid < E)
+    for (int r = 0; r < n_req && !in; ++r) in = ws.support_mask[static_cast<size_t>(r) * E + tid];
+  // exclusive scan of the membership flags over the expert ids
+  const int lane = lane_id(), wid = warp_id();
+  int incl = in;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) tmp[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int x = lane < static_cast<int>(blockDim.x >> 5) ? tmp[lane] : 0;
+    int xi = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, xi, o);
+      if (lane >= o) xi += u;
+    }
+    tmp[lane] = xi - x;
+    if (lane == 31) tmp[32] = xi;
+  }
+  __syncthreads();
+  const int pos = tmp[wid] + incl - in, total = tmp[32];
+  if (tid < E && in) {
+    ws.support_ids[pos] = tid;
+    if (ids_out) ids_out[pos] = tid;
+  }
+  if (tid < E && tid >= total) ws.support_ids[tid] = -1;  // beyond the union
+  if (tid == 0) {
+    ws.ctrl->support_len = total;
+    if (len_out) *len_out = total;
   }
 }
 
@@ -219,7 +218,9 @@ __global__ void __launch_bounds__(256) k_select(Dims d, Work ws, const uint8_t *
   const int rd = d.state_rd & 1;
   const bool anom = __syncthreads_or(
       any_anomaly(d, live, decoded, ws.prev_dec + static_cast<size_t>(rd) * d.Nmax, threadIdx.x, blockDim.x) ? 1 : 0);
-  const bool force = d.host_fallback != 0 || anom;
+  const int flags = (anom ? 1 : 0) | shortfall_flag(d, ws);
+  const bool force = d.host_fallback != 0 || flags != 0;
+  if (blockIdx.x == 0) reset_iteration_state(d, ws, flags);
   uint32_t *words = words_written(d, ws);
   const int lane = lane_id(), warps = gridDim.x * (blockDim.x >> 5);
   for (int t = blockIdx.x * (blockDim.x >> 5) + warp_id(); t < d.n_pos; t += warps) {
@@ -229,441 +230,26 @@ __global__ void __launch_bounds__(256) k_select(Dims d, Work ws, const uint8_t *
     if (!fresh) continue;
     float v[EPL];
     lane_logits<EPL>(ws.logits + static_cast<size_t>(t) * d.E, d.E, v);
-    select_position<EPL>(d, ws, t, v, ws.support_mask, force, words, s_scr[warp_id()], bias);
+    const uint8_t *mask = ws.support_mask + (d.req_size > 0 ? static_cast<size_t>(t / d.req_size) * d.E : 0);
+    select_position<EPL>(d, ws, t, v, mask, force, words, s_scr[warp_id()], bias);
   }
 }
 
 // ---------------------------------------------------------------- worklist
-// One CTA builds the iteration's worklist from the selection words the gate
-// (or select) kernel set ([W] section "FreshLane Dispatch": pack, count
-// exchange -> offsets, compact dispatch -- here the count exchange is a
-// popcount over per-expert bitmasks on one chip). Only experts that can hold a
-// selection are visited: the support, or every expert on a fallback. Every
-// step before the worklist is published reads shared memory only, after one
-// batched load of the candidates' words (global memory round trips, not
-// arithmetic, bound this kernel):
-//  1 rows of each candidate expert and per-word prefixes (one warp per expert);
-//  2 expert offsets (scan), the expert kernel's group list and tile counts;
-//  3 worklist positions, expert-major, positions ascending: the row of fresh
-//    position t for expert e is offset(e) + rows of e before t;
-//  4 publish (route_done = this call's sequence number, release), so the
-//    expert kernel, already running, starts on the routed tiles;
-//  5 then, off the critical path: the ascending fresh list, the worklist row of
-//    every selection (for the combine), statistics, the state of positions
-//    beyond n_pos, the cleared selection words and shared-expert counters of
-//    the next iteration.
-constexpr int kRouteSmemWords = 12 * 1024;  // candidate words (and prefixes) kept in shared memory
-
-__global__ void __launch_bounds__(kRouteThreads, 1) k_route(Dims d, Work ws) {
+// The worklist kernel of fp32 layers (bf16 layers build the worklist inside
+// the tcgen05 expert kernel): every CTA runs both phases of worklist.cuh with
+// all its threads. No row copy: the FFMA experts read x through wl_pos.
+__global__ void __launch_bounds__(kRouteThreads) k_route(Dims d, Work ws) {
   const KernelMark mark_(d, ws, K_ROUTING);
-  pdl_trigger();  // the expert kernel may start its launch; it waits on route_done for routed tiles
-  extern __shared__ uint32_t s_dyn[];
-  __shared__ int32_t tmp[33];
-  __shared__ int4 tmp4[33];
-  __shared__ int32_t s_off[1025];
-  __shared__ int16_t s_cand[1024];  // candidate experts (support ranking, or every expert)
-  __shared__ int16_t s_cidx[1024];  // candidate index of an expert, -1 if none
-  __shared__ int32_t s_cat[8];
-  __shared__ int s_force, s_anom, s_supp;
-  const int tid = threadIdx.x, lane = lane_id(), wid = warp_id(), nw = kRouteThreads / 32;
-  const int n = d.n_pos, E = d.E, k = d.k, cmax = d.cmax;
-  const int nch = (n + 31) >> 5;
-  const int rd = d.state_rd & 1, wr = rd ^ 1;
-  int64_t *trace = (d.trace && blockIdx.x < kTraceCtas) ? ws.trace + (3ull * kTraceCtas + blockIdx.x) * kTraceFields
-                                                         : nullptr;
-  if (trace && tid == 0) {
-    trace[0] = static_cast<int64_t>(globaltimer_ns());
-    uint32_t smid;
-    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-    trace[7] = smid;
-  }
-  // the block plan (written before this iteration began) can be read at once
-  if (tid < 8) s_cat[tid] = 0;
-  if (tid == 0) s_supp = min(E, ws.ctrl->support_len);
-  for (int e = tid; e < E; e += kRouteThreads) s_cand[e] = static_cast<int16_t>(ws.support_ids[e]);
-  for (int e = tid; e <= E; e += kRouteThreads) s_off[e] = 0;
-  pdl_wait();  // the gate / select kernel has finished: selection words, selections, codes
-  if (trace && tid == 0) trace[1] = static_cast<int64_t>(globaltimer_ns());
-  const uint32_t *words = ws.sel_words + static_cast<size_t>(wr) * E * cmax;
-
-  // Candidates: the support, or every expert on a host-detected fallback.
-  // Their words are requested together with the decoded -> live scan of the
-  // codes the gate wrote (one round trip); an anomaly found there turns the
-  // iteration into a fallback and the words of every expert are loaded.
-  uint32_t *sw = s_dyn;
-  int32_t *sp = reinterpret_cast<int32_t *>(s_dyn + kRouteSmemWords);
-  auto load_words = [&](int n_c) {
-    for (int q0 = tid; q0 < n_c * nch; q0 += kRouteThreads * 8) {
-      uint32_t v[8];
-#pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        const int q = q0 + b * kRouteThreads;
-        v[b] = q < n_c * nch ? words[static_cast<size_t>(s_cand[q / nch]) * cmax + q % nch] : 0u;
-      }
-#pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        const int q = q0 + b * kRouteThreads;
-        if (q < n_c * nch) sw[q] = v[b];
-      }
-    }
-  };
-  if (d.host_fallback)
-    for (int e = tid; e < E; e += kRouteThreads) s_cand[e] = static_cast<int16_t>(e);
-  __syncthreads();
-  int n_cand = d.host_fallback ? E : s_supp;
-  bool in_smem = n_cand * nch <= kRouteSmemWords;
-  {
-    int anom = 0;
-    for (int t = tid; t < n; t += kRouteThreads) anom |= ws.cat[t] & kCodeAnom;
-    if (in_smem) load_words(n_cand);
-    const int any = __syncthreads_or(anom);
-    if (tid == 0) {
-      s_anom = any != 0;
-      s_force = (d.host_fallback != 0 || any != 0) ? 1 : 0;
-    }
-    __syncthreads();
-  }
-  const bool force = s_force != 0;
-  if (force && !d.host_fallback) {  // anomaly: every expert is a candidate
-    for (int e = tid; e < E; e += kRouteThreads) s_cand[e] = static_cast<int16_t>(e);
-    __syncthreads();
-    n_cand = E;
-    in_smem = n_cand * nch <= kRouteSmemWords;
-    if (in_smem) load_words(n_cand);
-  }
-  for (int e = tid; e < E; e += kRouteThreads) s_cidx[e] = -1;
-  __syncthreads();
-  for (int i = tid; i < n_cand; i += kRouteThreads) s_cidx[s_cand[i]] = static_cast<int16_t>(i);
-  int64_t *trace2 = trace ? ws.trace + (5ull * kTraceCtas + blockIdx.x) * kTraceFields : nullptr;
-  if (trace2 && tid == 0) trace2[0] = static_cast<int64_t>(globaltimer_ns());
-  __syncthreads();
-  auto word = [&](int ci, int c) -> uint32_t {
-    return in_smem ? sw[ci * nch + c] : words[static_cast<size_t>(s_cand[ci]) * cmax + c];
-  };
-  auto pre = [&](int ci, int c) -> int32_t & {
-    return in_smem ? sp[ci * nch + c] : ws.pre[static_cast<size_t>(s_cand[ci]) * cmax + c];
-  };
-
-  // ---- 1: rows of each candidate expert and the per-word prefixes
-  {
-    const int cpl = (nch + 31) / 32;
-    for (int ci = wid; ci < n_cand; ci += nw) {
-      const int c0 = min(nch, lane * cpl), c1 = min(nch, c0 + cpl);
-      int sum = 0;
-      for (int c = c0; c < c1; ++c) sum += __popc(word(ci, c));
-      int incl = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += u;
-      }
-      int run = incl - sum;
-      for (int c = c0; c < c1; ++c) {
-        pre(ci, c) = run;
-        run += __popc(word(ci, c));
-      }
-      if (lane == 31) s_off[s_cand[ci]] = incl;  // count, scanned below
-    }
-  }
-  __syncthreads();
-  if (trace && tid == 0) trace[2] = static_cast<int64_t>(globaltimer_ns());
-
-  // ---- 2: one scan over the experts in id order (thread tid owns [tid * gpt,
-  // tid * gpt + gpt)) gives the expert offsets and, per row-count class of the
-  // group list (2: >= 96 rows, 1: >= 32, 0: fewer; listed in that order, by id
-  // within a class), the list positions and token-tile prefixes: .x rows,
-  // .y experts of class 0 | class 1 << 16, .z experts of class 2 | its tiles
-  // << 16, .w tiles of class 0 | class 1 << 16.
-  int n_edges, n_tiles;
-  {
-    const int gpt = (E + kRouteThreads - 1) / kRouteThreads;
-    const int g0 = tid * gpt;
-    auto cls_of = [](int r) { return r >= 96 ? 2 : r >= 32 ? 1 : 0; };
-    int c[4] = {0, 0, 0, 0};
-    int4 v = make_int4(0, 0, 0, 0);
-#pragma unroll
-    for (int h = 0; h < 4; ++h)
-      if (h < gpt && g0 + h < E) {
-        const int r = s_off[g0 + h], k2 = cls_of(r), nt = d.tn > 0 ? (r + d.tn - 1) / d.tn : 0;
-        c[h] = r;
-        v.x += r;
-        if (k2 == 0) {
-          v.y += 1;
-          v.w += nt;
-        } else if (k2 == 1) {
-          v.y += 1 << 16;
-          v.w += nt << 16;
-        } else {
-          v.z += 1 | (nt << 16);
-        }
-      }
-    int4 tot;
-    const int4 ex = block_excl_scan4(v, reinterpret_cast<int4 *>(tmp4), &tot);
-    const int n2 = tot.z & 0xffff, n1 = tot.y >> 16;
-    const int t2 = tot.z >> 16, t1 = tot.w >> 16, t0 = tot.w & 0xffff;
-    const int pos_base[3] = {n2 + n1, n2, 0};
-    const int tile_base[3] = {t2 + t1, t2, 0};
-    int rank[3] = {ex.y & 0xffff, ex.y >> 16, ex.z & 0xffff};
-    int tb[3] = {ex.w & 0xffff, ex.w >> 16, ex.z >> 16};
-    int before = ex.x;
-    n_edges = tot.x;
-    n_tiles = t0 + t1 + t2;
-#pragma unroll
-    for (int h = 0; h < 4; ++h)
-      if (h < gpt && g0 + h < E) {
-        const int e = g0 + h, r = c[h], k2 = cls_of(r), nt = d.tn > 0 ? (r + d.tn - 1) / d.tn : 0;
-        s_off[e] = before;
-        ws.offsets[e] = before;
-        before += r;
-        ws.grp_list[pos_base[k2] + rank[k2]++] = ((tile_base[k2] + tb[k2]) << kGrpIdBits) | e;
-        tb[k2] += nt;
-      }
-    if (tid == 0) {
-      s_off[E] = n_edges;
-      ws.offsets[E] = n_edges;
-      ws.grp_list[E] = n_tiles << kGrpIdBits;
-      ws.ctrl->tiles_up = d.tn > 0 ? (d.I / 128) * n_tiles : 0;
-      ws.ctrl->tiles_dn = d.tn > 0 ? (d.H / kBmDn) * n_tiles : 0;
-    }
-  }
-  __syncthreads();
-  if (trace2 && tid == 0) trace2[1] = static_cast<int64_t>(globaltimer_ns());
-  for (int g = tid; g < E; g += kRouteThreads) ws.done_up[g] = 0;
-  if (tid == 0) {
-    ws.tile_ctr[0] = 0;  // routed tiles drawn
-    ws.tile_ctr[2] = 0;  // 16-byte vectors of worklist rows copied into xp
-    ws.ctrl->n_edges = n_edges;
-  }
-  if (trace && tid == 0) trace[3] = static_cast<int64_t>(globaltimer_ns());
-
-  // ---- 3: worklist positions, one thread per candidate word
-  for (int q = tid; q < n_cand * nch; q += kRouteThreads) {
-    const int ci = q / nch, c = q - ci * nch;
-    uint32_t w = word(ci, c);
-    if (w == 0u) continue;
-    int dst = s_off[s_cand[ci]] + pre(ci, c);
-    while (w) {
-      const int b = __ffs(w) - 1;
-      w &= w - 1u;
-      if (dst < 0 || dst >= d.Nmax * k) {
-        set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-        break;
-      }
-      ws.wl_pos[dst++] = 32 * c + b;
-    }
-  }
-  // ---- 4: publish the worklist (every thread's writes, then one release)
-  if (trace2 && tid == 0) trace2[2] = static_cast<int64_t>(globaltimer_ns());
-  __syncthreads();
-  if (tid == 0) {
-    if (trace2) trace2[3] = static_cast<int64_t>(globaltimer_ns());
-    __threadfence();
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ws.route_done), "r"(d.seq) : "memory");
-  }
-  if (trace && tid == 0) trace[4] = static_cast<int64_t>(globaltimer_ns());
-
-  // ---- 5: fresh list, selection slots, statistics; thread tid owns a
-  // contiguous range of positions so the fresh list comes out ascending
-  const int ppt = (n + kRouteThreads - 1) / kRouteThreads;
-  const int p0 = min(n, tid * ppt), p1 = min(n, p0 + ppt);
-  int cnt[5] = {0, 0, 0, 0, 0}, bad = 0;
-  for (int t = p0; t < p1; ++t) {
-    const int code = ws.cat[t];
-    const int c = code & 15;
-#pragma unroll
-    for (int q = 0; q < 5; ++q) cnt[q] += c == q;
-    bad += (code & kCodeBad) ? 1 : 0;
-  }
-  int n_fresh;
-  int f = block_excl_scan((p1 - p0) - (force ? 0 : cnt[C_REUSE]), tmp, &n_fresh);
-  for (int t = p0; t < p1; ++t) {
-    const bool fresh = force || (ws.cat[t] & 15) != C_REUSE;
-    if (!fresh) {
-      ws.fidx[t] = -1;
-      continue;
-    }
-    ws.fresh_pos[f] = t;
-    ws.fidx[t] = f++;
-    const int c = t >> 5;
-    const uint32_t below = (1u << (t & 31)) - 1u;
-    for (int j = 0; j < k; ++j) {
-      const int e = ws.sel[static_cast<size_t>(t) * k + j];
-      if (e < 0 || e >= E) {
-        set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-        ws.slot[static_cast<size_t>(t) * k + j] = 0;
-        continue;
-      }
-      const int ci = s_cidx[e];
-      if (ci < 0) {
-        set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-        ws.slot[static_cast<size_t>(t) * k + j] = 0;
-        continue;
-      }
-      ws.slot[static_cast<size_t>(t) * k + j] = s_off[e] + pre(ci, c) + __popc(word(ci, c) & below);
-    }
-  }
-#pragma unroll
-  for (int q = 0; q < 5; ++q) cnt[q] = __reduce_add_sync(0xffffffffu, cnt[q]);
-  bad = __reduce_add_sync(0xffffffffu, bad);
-  if (lane == 0) {
-#pragma unroll
-    for (int q = 0; q < 5; ++q) atomicAdd(&s_cat[q], cnt[q]);
-    atomicAdd(&s_cat[5], bad);
-  }
-  // experts with at least one row (statistics)
-  int hit = 0;
-  for (int e = tid; e < E; e += kRouteThreads) hit += s_off[e + 1] > s_off[e];
-  hit = __reduce_add_sync(0xffffffffu, hit);
-  if (lane == 0) atomicAdd(&s_cat[6], hit);
-  __syncthreads();
-  if (tid == 0) {
-    const int nt_sh = d.tn > 0 ? d.n_sh * ((n + d.tn - 1) / d.tn) : 0;
-    ws.ctrl->n_hit = s_cat[6];
-    ws.stats->n_hit_experts = s_cat[6];
-    ws.stats->tiles_up = (d.tn > 0 ? (d.I / 128) * n_tiles : 0) + (d.I_s / 128) * nt_sh;
-    ws.stats->tiles_down = (d.tn > 0 ? (d.H / kBmDn) * n_tiles : 0) + (d.H / kBmDn) * nt_sh;
-    const int fb = (d.host_fallback ? 1 : 0) | (s_anom ? 2 : 0);
-    if (n_fresh * k != n_edges) set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-    ws.ctrl->n_fresh = n_fresh;
-    ws.ctrl->fallback = fb;
-    epoch_iter_stats *st = ws.stats;
-    st->iteration = d.iter;
-    st->n_pos = n;
-    st->n_live = s_cat[C_LIVE];
-    st->n_new = s_cat[C_NEW];
-    st->n_miss = s_cat[C_MISS];
-    st->n_stale = s_cat[C_STALE];
-    st->n_forced = force ? s_cat[C_REUSE] : 0;
-    st->n_reuse = force ? 0 : s_cat[C_REUSE];
-    st->n_fresh = n_fresh;
-    st->n_edges = n_edges;
-    st->support_len = fb ? E : ws.ctrl->support_len;
-    st->fallback = fb;
-    st->bad_flags = s_cat[5];
-    if (s_cat[5]) set_error(ws.err, EPOCH_DEVERR_FLAGS);
-    if (d.stats_out) *d.stats_out = *st;
-  }
-  // positions beyond this call's n_pos keep their state
-  for (int t = n + tid; t < d.Nmax; t += kRouteThreads) {
-    ws.stamp[static_cast<size_t>(wr) * d.Nmax + t] = ws.stamp[static_cast<size_t>(rd) * d.Nmax + t];
-    ws.prev_dec[static_cast<size_t>(wr) * d.Nmax + t] = ws.prev_dec[static_cast<size_t>(rd) * d.Nmax + t];
-  }
-  // the words and the shared-expert tile counters of the next iteration start at zero
-  uint32_t *next = ws.sel_words + static_cast<size_t>(rd) * E * cmax;
-  for (int q = tid; q < E * cmax; q += kRouteThreads) next[q] = 0u;
-  const int nxt = static_cast<int>((d.seq + 1u) & 1u);
-  int32_t *sh = ws.sh_ctr + static_cast<size_t>(nxt) * sh_stride(d);
-  for (int q = tid; q < sh_stride(d); q += kRouteThreads) sh[q] = 0;
-  // ---- 6: publish the bookkeeping (route_done[1] = this call's sequence
-  // number, release) for the combine kernel, which reads the fresh index,
-  // slots and weights before the expert outputs exist
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ws.route_done + 1), "r"(d.seq) : "memory");
-  }
-  if (trace && tid == 0) trace[5] = static_cast<int64_t>(globaltimer_ns());
-}
-
-// ---------------------------------------------------------------- permute
-// Copies the token rows of the worklist into the compact buffer xp (row l = x
-// at wl_pos[l], [W] section "FreshLane Dispatch": compact dispatch), so the
-// expert kernel loads each expert's rows as one tiled TMA box. Launched right
-// behind the worklist kernel, it waits for the worklist to be published
-// (route_done = this call's sequence number), copies its share of the 16-byte
-// vectors and adds their count to tile_ctr[2]; the expert kernel's routed up
-// tiles start once that count reaches L * (vectors per row). It exits as soon
-// as its copies are counted (it does not wait for the worklist kernel to
-// finish: its CTAs would hold SMs the expert kernel needs); the combine kernel
-// waits for the worklist kernel's bookkeeping through route_done[1].
-// One CTA per SM (the block scheduler spreads a grid of one CTA per SM over
-// every SM before it stacks any; a larger grid stacked several CTAs on the SMs
-// the gate leaves free, and an expert CTA could not start there until they
-// left). 384 threads, at most 64 registers: a CTA fits beside a gate CTA or an
-// expert CTA. (With fewer registers the scheduler stacked two or three on the
-// SMs the gate leaves free, and an SM sub-partition's registers then no longer
-// held an expert CTA's warps beside them.)
-constexpr int kPermuteThreads = 384;
-constexpr int kPermuteVec = 8;  // 16-byte vectors per thread per round
-constexpr int kTraceRowPermute = 8;
-__global__ void __maxnreg__(64) k_permute(Dims d, Work ws, const uint4 *__restrict__ x, int vpr) {
   pdl_trigger();
-  __shared__ int s_ok, s_L;
-  const int tid = threadIdx.x;
-  int64_t *trace = (d.trace && blockIdx.x < kTraceCtas && tid == 0)
-                       ? ws.trace + (static_cast<size_t>(kTraceRowPermute) * kTraceCtas + blockIdx.x) * kTraceFields
-                       : nullptr;
-  if (trace) {
-    trace[0] = static_cast<int64_t>(globaltimer_ns());
-    uint32_t smid;
-    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-    trace[7] = smid;
-  }
-  if (tid == 0) {
-    int ok = 1;
-    const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-      unsigned int v;
-      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ws.route_done) : "memory");
-      if (v == d.seq) break;
-      if (globaltimer_ns() - t0 > static_cast<uint64_t>(d.timeout_ns)) {
-        set_error(ws.err, EPOCH_DEVERR_TIMEOUT);
-        ok = 0;
-        break;
-      }
-      __nanosleep(32);
-    }
-    s_ok = ok;
-    s_L = ok ? ws.ctrl->n_edges : 0;
-    if (trace) trace[1] = static_cast<int64_t>(globaltimer_ns());
-  }
-  __syncthreads();
-  // rows [r0, r1) of the worklist; warp w copies rows r0 + w, r0 + w + 12, ...,
-  // lane l the vectors l, l + 32, ... of a row. The warp's row positions are
-  // loaded first, one per lane, so the row copies do not wait on them one by one.
-  const int L = s_L, lane = lane_id(), wid = warp_id(), nw = kPermuteThreads / 32;
-  const int r0 = static_cast<int>(static_cast<long long>(L) * blockIdx.x / gridDim.x);
-  const int r1 = static_cast<int>(static_cast<long long>(L) * (blockIdx.x + 1) / gridDim.x);
-  uint4 *xp = static_cast<uint4 *>(ws.xp);
-  for (int rb = r0 + wid; rb < r1; rb += 32 * nw) {
-    int my_pos = 0;
-    const int rl = rb + lane * nw;  // this lane's row of the batch
-    if (rl < r1) {
-      my_pos = ws.wl_pos[rl];
-      if (my_pos < 0 || my_pos >= d.n_pos) {
-        set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-        my_pos = 0;
-      }
-    }
-    const int nb = min(32, (r1 - rb + nw - 1) / nw);  // rows of this batch
-#pragma unroll 1
-    for (int b = 0; b < nb; ++b) {
-      const int row = rb + b * nw;
-      const int pos = __shfl_sync(0xffffffffu, my_pos, b);
-      const uint4 *src = x + static_cast<size_t>(pos) * vpr;
-      uint4 *dst = xp + static_cast<size_t>(row) * vpr;
-#pragma unroll 1
-      for (int v0 = 0; v0 < vpr; v0 += 32 * kPermuteVec) {
-        uint4 buf[kPermuteVec];
-#pragma unroll
-        for (int q = 0; q < kPermuteVec; ++q) {
-          const int v = v0 + lane + 32 * q;
-          if (v < vpr) buf[q] = __ldg(src + v);
-        }
-#pragma unroll
-        for (int q = 0; q < kPermuteVec; ++q) {
-          const int v = v0 + lane + 32 * q;
-          if (v < vpr) dst[v] = buf[q];
-        }
-      }
-    }
-  }
-  __syncthreads();
-  if (tid == 0 && s_ok && r1 > r0) {
-    __threadfence();
-    atomicAdd(ws.tile_ctr + 2, (r1 - r0) * vpr);
-  }
-  if (trace) trace[2] = static_cast<int64_t>(globaltimer_ns());
+  __shared__ WlSmem sm;
+  __shared__ int32_t s_off[1025];
+  const Group g{static_cast<int>(threadIdx.x), kRouteThreads, 0};
+  wl_prepare(d, ws, sm, s_off, g);
+  pdl_wait();  // the select kernel has finished: selection words, selections, codes, anomaly flag
+  const WlPlan pl = wl_phase_a(d, ws, sm, s_off, nullptr, blockIdx.x == 0, g);
+  wl_rows(d, ws, sm, s_off, pl, nullptr, 0, blockIdx.x, gridDim.x, g);
+  wl_bookkeeping(d, ws, sm, s_off, pl, blockIdx.x, gridDim.x, g, nullptr);
 }
 
 // ---------------------------------------------------------------- combine + cache
@@ -715,11 +301,9 @@ template <> struct Row8<float> {
 // ([W] section "Liveness-Shard Parallelism": Y[F_i] = Y_F); reused t: r = the
 // cached row (Y[not F_i] = C_l[not F_i]). Then y = r + shared outputs (+ x when
 // residual), rounded once: the dense shard is restored at the layer boundary.
-// The fresh index, slots and weights come from the worklist kernel's
-// bookkeeping and are read while the experts still run (route_done[1] = this
-// call's sequence number); once the expert grid has finished, each pass
-// requests every row it needs (the k expert-output rows or the cached row,
-// the shared outputs, x) before using any of them.
+// The fresh index, slots and weights come from the worklist bookkeeping; each
+// pass requests every row it needs (the k expert-output rows or the cached
+// row, the shared outputs, x) before using any of them.
 template <typename T>
 __global__ void __launch_bounds__(128, 7) k_combine(Dims d, Work ws, const T *__restrict__ x, T *__restrict__ y) {
   const KernelMark mark_(d, ws, K_COMBINE);
@@ -737,29 +321,18 @@ __global__ void __launch_bounds__(128, 7) k_combine(Dims d, Work ws, const T *__
   __shared__ int32_t slot_s[16];
   __shared__ float w_s[16];
   __shared__ int f_s;
-  if (threadIdx.x == 0) {
-    const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-      unsigned int v;
-      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ws.route_done + 1) : "memory");
-      if (v == d.seq) break;
-      if (globaltimer_ns() - t0 > static_cast<uint64_t>(d.timeout_ns)) {
-        set_error(ws.err, EPOCH_DEVERR_TIMEOUT);
-        break;
-      }
-      __nanosleep(64);
-    }
-  }
-  __syncthreads();
+  // Every kernel of the iteration before this one has completed: the expert
+  // outputs, and the worklist bookkeeping (built inside the tcgen05 expert
+  // kernel, or by the worklist kernel before the FFMA experts). A hardware
+  // wait: no thread of this grid polls memory while the experts stream.
+  pdl_wait();
   if (t < d.n_pos) {
     if (threadIdx.x < k) {
-      int sl = ws.slot[static_cast<size_t>(t) * k + threadIdx.x];
-      slot_s[threadIdx.x] = sl;
+      slot_s[threadIdx.x] = ws.slot[static_cast<size_t>(t) * k + threadIdx.x];
       w_s[threadIdx.x] = ws.selw[static_cast<size_t>(t) * k + threadIdx.x];
     }
     if (threadIdx.x == 0) f_s = ws.fidx[t];
   }
-  pdl_wait();  // the expert outputs of this call are complete
   if (trace) trace[1] = static_cast<int64_t>(globaltimer_ns());
   if (t >= d.n_pos) return;
   __syncthreads();
@@ -964,10 +537,16 @@ cudaError_t launch_plan_topk(const Dims &d, const Weights &w, const Work &ws, cu
 }
 
 cudaError_t launch_plan_support(const Dims &d, const Work &ws, int32_t threshold, int all_experts,
-                                int clear_state, int32_t *ids_out, int32_t *len_out, cudaStream_t s) {
-  static bool carve_ = (prefer_max_shared(k_plan_support) == cudaSuccess);
+                                int clear_state, int32_t *ids_out, int32_t *len_out, double tau, cudaStream_t s) {
+  static bool carve_ = (prefer_max_shared(k_plan_support) == cudaSuccess && prefer_max_shared(k_plan_union) == cudaSuccess);
   (void)carve_;
-  k_plan_support<<<1, 1024, 0, s>>>(d, ws, threshold, all_experts, clear_state, ids_out, len_out);
+  const int n_req = d.req_size > 0 ? (d.n_pos + d.req_size - 1) / d.req_size : 1;
+  k_plan_support<<<n_req, 1024, 0, s>>>(d, ws, threshold, all_experts, clear_state, ids_out, len_out, tau);
+  if (d.req_size > 0) {
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    k_plan_union<<<1, 1024, 0, s>>>(d, ws, ids_out, len_out);
+  }
   return cudaGetLastError();
 }
 
@@ -989,30 +568,19 @@ cudaError_t launch_select(const Dims &d, const Work &ws, const uint8_t *live, co
   return cudaGetLastError();
 }
 
-cudaError_t launch_permute(const Dims &d, const Work &ws, const void *x, cudaStream_t s) {
-  static bool c_ = (prefer_max_shared(k_permute) == cudaSuccess);
-  (void)c_;
-  Dims dd = d;
-  Work ww = ws;
-  const uint4 *xv = static_cast<const uint4 *>(x);
-  int vpr = d.H * 2 / 16;
-  void *args[] = {&dd, &ww, &xv, &vpr};
-  return launch_kernel(reinterpret_cast<void *>(k_permute), dim3(num_sms()), dim3(kPermuteThreads), 0, s, args,
-                       true);
-}
+int route_ctas() { return num_sms(); }
 
-// One CTA, launched programmatically: it starts while the gate kernel runs and
-// waits for it (pdl_wait) before reading its outputs.
+// One CTA per SM, launched programmatically: the CTAs become resident while
+// the select kernel runs and wait for it (pdl_wait) before reading.
 cudaError_t launch_route(const Dims &d, const Work &ws, cudaStream_t s) {
-  if (d.E > 4 * kRouteThreads) return cudaErrorInvalidConfiguration;
-  constexpr size_t kDyn = (2 * kRouteSmemWords + 1024) * 4;  // words, prefixes, group list
-  static bool c_ = (prefer_max_shared(k_route) == cudaSuccess &&
-                    cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn) == cudaSuccess);
+  if (d.E > 8 * kRouteThreads) return cudaErrorInvalidConfiguration;
+  static bool c_ = (prefer_max_shared(k_route) == cudaSuccess);
   if (!c_) return cudaErrorInvalidConfiguration;
   Dims dd = d;
   Work ww = ws;
   void *args[] = {&dd, &ww};
-  return launch_kernel(reinterpret_cast<void *>(k_route), dim3(1), dim3(kRouteThreads), kDyn, s, args, true);
+  return launch_kernel(reinterpret_cast<void *>(k_route), dim3(route_ctas()), dim3(kRouteThreads), 0, s, args,
+                       true);
 }
 
 cudaError_t launch_combine(const Dims &d, const Work &ws, const void *x, void *y, int bf16, cudaStream_t s) {

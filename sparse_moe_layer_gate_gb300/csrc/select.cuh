@@ -94,6 +94,12 @@ __device__ __forceinline__ bool classify_and_update(const Dims &d, const Work &w
   return fresh;
 }
 
+// The previous iteration's coverage shortfall makes this one full fresh
+// (unless a host fallback already does): 2, else 0.
+__device__ __forceinline__ int shortfall_flag(const Dims &d, const Work &ws) {
+  return (d.cov_check && !d.host_fallback && !d.plan_mode && ws.ctrl->short_next) ? 2 : 0;
+}
+
 // Top-k of fresh position t by one warp over the eligible experts (every
 // expert when `force`, else the support mask), ordered by logit desc, lower id
 // first; weights = softmax over the k selected logits, summed in selection
@@ -104,7 +110,12 @@ __device__ __forceinline__ bool classify_and_update(const Dims &d, const Work &w
 // Group-limited sigmoid router (d.router == 1; v holds x W_r^T without the
 // bias): scores s = sigmoid(v), selection scores c = s + bias, the group rule
 // of warp_group_limit, the top-k of c, weights = the selected s divided by
-// their sum in selection order.
+// their sum in selection order. With d.raw_weights the weights are not
+// renormalised: the selected s, or (softmax router) the dense router
+// probabilities -- the softmax of v over every expert, eligible or not.
+// With d.cov_check the position's support coverage is checked as well (see
+// the coverage fields of epoch_layer_config) against support_mask, the block
+// support, and an under-covered position is counted in cov_under.
 template <int EPL>
 __device__ __forceinline__ void select_position(const Dims &d, const Work &ws, int t, const float (&v)[EPL],
                                                 const uint8_t *support_mask, bool force, uint32_t *words,
@@ -120,11 +131,25 @@ __device__ __forceinline__ void select_position(const Dims &d, const Work &ws, i
   float val, wgt;
   if (d.router == 0) {
     warp_topk<EPL>(v, ok, k, &sel, &val, scratch);
-    const float top = __shfl_sync(0xffffffffu, val, 0);
-    const float ex = lane < k ? expf(val - top) : 0.f;
-    float denom = 0.f;
-    for (int j = 0; j < k; ++j) denom += __shfl_sync(0xffffffffu, ex, j);
-    wgt = ex / denom;
+    if (d.raw_weights) {  // dense router probability: softmax of the row over every expert
+      float m = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < EPL; ++c) m = fmaxf(m, v[c]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < EPL; ++c) sum += e0 + c < d.E ? expf(v[c] - m) : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      wgt = lane < k ? expf(val - m) / sum : 0.f;
+    } else {
+      const float top = __shfl_sync(0xffffffffu, val, 0);
+      const float ex = lane < k ? expf(val - top) : 0.f;
+      float denom = 0.f;
+      for (int j = 0; j < k; ++j) denom += __shfl_sync(0xffffffffu, ex, j);
+      wgt = ex / denom;
+    }
   } else {
     float cs[EPL];
 #pragma unroll
@@ -145,7 +170,7 @@ __device__ __forceinline__ void select_position(const Dims &d, const Work &ws, i
     const float sg = lane < k ? 1.f / (1.f + expf(-z)) : 0.f;
     float denom = 0.f;
     for (int j = 0; j < k; ++j) denom += __shfl_sync(0xffffffffu, sg, j);
-    wgt = sg / denom;
+    wgt = d.raw_weights ? sg : sg / denom;
   }
   if (lane < k) {
     if (sel < 0 || sel >= d.E) {
@@ -155,6 +180,67 @@ __device__ __forceinline__ void select_position(const Dims &d, const Work &ws, i
       ws.selw[static_cast<size_t>(t) * k + lane] = wgt;
       atomicOr(&words[static_cast<size_t>(sel) * d.cmax + (t >> 5)], 1u << (t & 31));
     }
+  }
+  if (d.cov_check) {
+    // support coverage of t: its dense selection (every expert eligible) and
+    // the share of that selection's raw score mass on support experts
+    bool all[EPL];
+#pragma unroll
+    for (int c = 0; c < EPL; ++c) all[c] = e0 + c < d.E;
+    int dsel;
+    float dval, score;
+    if (d.router == 0) {
+      warp_topk<EPL>(v, all, k, &dsel, &dval, scratch);
+      float m = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < EPL; ++c) m = fmaxf(m, v[c]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < EPL; ++c) sum += e0 + c < d.E ? expf(v[c] - m) : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      score = lane < k ? expf(dval - m) / sum : 0.f;
+    } else {
+      float cs[EPL];
+#pragma unroll
+      for (int c = 0; c < EPL; ++c) cs[c] = e0 + c < d.E ? 1.f / (1.f + expf(-v[c])) + bias[e0 + c] : -INFINITY;
+      warp_group_limit<EPL>(cs, all, d.E, d.n_group, d.topk_group, k);
+      warp_topk<EPL>(cs, all, k, &dsel, &dval, scratch);
+      const int owner = dsel >= 0 ? dsel / EPL : 0, idx = dsel >= 0 ? dsel - owner * EPL : 0;
+      float z = 0.f;
+#pragma unroll
+      for (int c = 0; c < EPL; ++c) {
+        const float o = __shfl_sync(0xffffffffu, v[c], owner);
+        if (c == idx) z = o;
+      }
+      score = lane < k ? 1.f / (1.f + expf(-z)) : 0.f;
+    }
+    float mass = 0.f, covered = 0.f;
+    for (int j = 0; j < k; ++j) {  // in selection order
+      const float sj = __shfl_sync(0xffffffffu, score, j);
+      const int ej = __shfl_sync(0xffffffffu, dsel, j);
+      mass += sj;
+      if (ej >= 0 && support_mask[ej]) covered += sj;
+    }
+    if (lane == 0 && covered < d.cov_alpha * mass) atomicAdd(&ws.cov_under[d.seq & 1], 1);
+  }
+}
+
+// Per-iteration handshake state, set by block 0 of the kernel that classifies
+// the positions (the gate, or the select kernel) while no later kernel of the
+// iteration reads it yet: the anomaly flag, and the counters the worklist and
+// expert kernels advance (routed tiles drawn, xp vectors copied, up tiles
+// done per group). Their readers wait for this call's worklist first.
+// flags: bit 0 a decoded -> live anomaly, bit 1 the previous iteration's
+// coverage shortfall (both make the iteration full fresh).
+__device__ __forceinline__ void reset_iteration_state(const Dims &d, const Work &ws, int flags) {
+  for (int g = threadIdx.x; g < d.E + d.n_sh; g += blockDim.x) ws.done_up[g] = 0;
+  if (threadIdx.x == 0) {
+    ws.ctrl->anom = flags;
+    ws.tile_ctr[0] = 0;
+    ws.tile_ctr[2] = 0;
   }
 }
 

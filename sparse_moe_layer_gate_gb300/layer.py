@@ -31,6 +31,9 @@ def _stream(stream) -> int:
 class EpochLayer:
     """One routed-expert MoE layer with its block plan and routed-output cache.
 
+    coverage: (alpha, q) turns on the per-iteration support-coverage check
+    (see epoch_layer_config); None leaves it off.
+
     weights: dict of CUDA tensors -- w_router [E,H], b_router [E] float32,
     w_gate/w_up [E,I,H], w_down [E,H,I], and when n_shared > 0 ws_gate/ws_up
     [n_sh,I_s,H], ws_down [n_sh,H,I_s]; all contiguous, in the layer dtype.
@@ -39,18 +42,22 @@ class EpochLayer:
     def __init__(self, *, hidden: int, n_experts: int, inter: int, top_k: int, max_positions: int,
                  dtype: str, tau: float, refresh_R: Optional[int], weights: Dict[str, torch.Tensor],
                  n_shared: int = 0, shared_inter: Optional[int] = None, residual: bool = False,
-                 router: str = "softmax", n_group: int = 1, topk_group: int = 1):
+                 router: str = "softmax", n_group: int = 1, topk_group: int = 1, raw_weights: bool = False,
+                 coverage: Optional[tuple] = None, request_size: int = 0):
         self.dtype = dtype
         self.hidden, self.n_experts, self.inter, self.top_k = hidden, n_experts, inter, top_k
         self.n_shared = n_shared
         self.max_positions = max_positions
+        self.request_size = int(request_size)
         self.cfg = B.epoch_layer_config(
             hidden=hidden, n_experts=n_experts, inter=inter, top_k=top_k, n_shared=n_shared,
             shared_inter=(shared_inter or inter) if n_shared else 0, max_positions=max_positions,
             dtype=_ABI_DT[dtype], tau=float(tau),
             refresh_R=B.EPOCH_REFRESH_NEVER if refresh_R is None else int(refresh_R),
             residual=1 if residual else 0, router=_ROUTER[router], n_group=int(n_group),
-            topk_group=int(topk_group))
+            topk_group=int(topk_group), raw_weights=1 if raw_weights else 0,
+            coverage_check=1 if coverage else 0, coverage_alpha=float(coverage[0]) if coverage else 0.0,
+            coverage_q=float(coverage[1]) if coverage else 0.0, request_size=int(request_size))
         tdt = _TORCH_DT[dtype]
         for name, t in weights.items():
             if not (t.is_cuda and t.is_contiguous()):
@@ -215,7 +222,14 @@ class EpochLayer:
         if "plan" in parts:
             d["support_len"] = int(self._copy(v.support_len, 1, np.int32, stream)[0])
             d["support_ids"] = self._copy(v.support_ids, E, np.int32, stream)
-            d["plan_counts"] = self._copy(v.plan_counts, E, np.int32, stream)
+            if self.request_size > 0:
+                R = (n_pos + self.request_size - 1) // self.request_size
+                d["plan_counts"] = self._copy(v.plan_counts, R * E, np.int32, stream).reshape(R, E)
+                d["request_ids"] = self._copy(v.request_ids, R * E, np.int32, stream).reshape(R, E)
+                d["request_len"] = self._copy(v.request_len, R, np.int32, stream)
+                d["support_masks"] = self._copy(v.support_masks, R * E, np.uint8, stream).reshape(R, E)
+            else:
+                d["plan_counts"] = self._copy(v.plan_counts, E, np.int32, stream)
         if "iter" in parts:
             # selections, weights and slots are stored per position; rows of the
             # fresh positions, in fresh-list order

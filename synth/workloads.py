@@ -58,6 +58,9 @@ class Workload:
     router: str = "softmax"  # or "sigmoid_group" (group-limited sigmoid router)
     n_group: int = 1
     topk_group: int = 1
+    raw_weights: bool = False  # weights not renormalised over the selection
+    coverage: Optional[tuple] = None  # (alpha, q) of the per-iteration support-coverage check
+    request_size: int = 0  # > 0: positions per request, each request with its own block plan
     description: str = ""
 
     @property

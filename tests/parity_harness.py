@@ -62,7 +62,8 @@ def layer_for_workload(wl, layer_index: int = 0, device="cuda", threads: Optiona
     return EpochLayer(hidden=wl.hidden, n_experts=wl.n_experts, inter=wl.inter, top_k=wl.top_k,
                       max_positions=max_positions or wl.n_pos, dtype=wl.dtype, tau=wl.tau, refresh_R=wl.refresh_R,
                       weights=weights, n_shared=wl.n_shared, shared_inter=wl.shared_inter,
-                      residual=wl.residual, router=wl.router, n_group=wl.n_group, topk_group=wl.topk_group)
+                      residual=wl.residual, router=wl.router, n_group=wl.n_group, topk_group=wl.topk_group,
+                      raw_weights=wl.raw_weights, coverage=wl.coverage, request_size=wl.request_size)
 
 
 def tol_for(dtype: str) -> float:
@@ -85,7 +86,8 @@ def oracle_layer(wl, layer_index: int = 0, max_positions: Optional[int] = None) 
                               w_router=synth.to_f64(wr, wl.dtype), b_router=b.astype(np.float64),
                               expert=expert, shared=shared, residual=wl.residual,
                               max_positions=max_positions or wl.n_pos,
-                              router=oracle.Router(wl.router, wl.n_group, wl.topk_group))
+                              router=oracle.Router(wl.router, wl.n_group, wl.topk_group, not wl.raw_weights),
+                              coverage=wl.coverage, request_size=wl.request_size or None)
 
 
 def tensor_to_f64(t: torch.Tensor) -> np.ndarray:
@@ -234,7 +236,7 @@ def counts_explained(orc, G: np.ndarray, oracle_counts: np.ndarray, gpu_counts: 
     return int(np.maximum(D, 0).sum()) <= moves
 
 
-def _check_support(orc, op, gplan: dict, n_pos: int, rep: Report, what: str) -> None:
+def _check_support(orc, op, gplan: dict, n_pos: int, rep: Report, what: str, adopt=None) -> None:
     glen = int(gplan["support_len"])
     gids = np.asarray(gplan["support_ids"])
     gcnt = np.asarray(gplan["plan_counts"])
@@ -251,12 +253,36 @@ def _check_support(orc, op, gplan: dict, n_pos: int, rep: Report, what: str) -> 
         return
     moved = int(np.abs(gcnt - op.counts).sum()) // 2
     rep.near_ties.append(f"{what}: {moved} edge(s) moved at near-tied positions; adopting GPU support")
-    orc.adopt_support(gids, glen)
+    (adopt or orc.adopt_support)(gids, glen)
+
+
+def _check_supports(orc, op, gplan: dict, n_pos: int, rep: Report, what: str) -> None:
+    """The block's support, or with per-request supports each request's (its
+    own counts, threshold and prefix) and their union, ascending."""
+    if not orc.request_size:
+        _check_support(orc, op, gplan, n_pos, rep, what)
+        return
+    rs = orc.request_size
+    for r, rp in enumerate(orc.request_plans):
+        def adopt(ids, ln, r=r):
+            orc.request_masks[r] = False
+            orc.request_masks[r, np.asarray(ids[:ln], dtype=np.int64)] = True
+        g = dict(support_len=gplan["request_len"][r], support_ids=gplan["request_ids"][r],
+                 plan_counts=gplan["plan_counts"][r])
+        _check_support(orc, rp, g, min(rs, n_pos - r * rs), rep, f"{what} request {r}", adopt)
+        want_mask = orc.request_masks[r]
+        if not np.array_equal(np.asarray(gplan["support_masks"][r], dtype=bool), want_mask):
+            rep.mismatches.append(f"{what} request {r}: support mask differs")
+    orc.support_mask = orc.request_masks.any(axis=0)
+    union = np.nonzero(orc.support_mask)[0]
+    glen = int(gplan["support_len"])
+    if glen != union.size or not np.array_equal(np.asarray(gplan["support_ids"])[:glen], union):
+        rep.mismatches.append(f"{what}: union of the request supports differs")
 
 
 def check_plan(orc: oracle.LayerOracle, gplan: dict, x0: np.ndarray, wl, rep: Report, tag: str):
     op = orc.plan_block(x0)
-    _check_support(orc, op, gplan, x0.shape[0], rep, f"{tag} plan")
+    _check_supports(orc, op, gplan, x0.shape[0], rep, f"{tag} plan")
     return op
 
 
@@ -264,7 +290,7 @@ def check_hot_update(orc: oracle.LayerOracle, gplan: dict, x0: np.ndarray, wl, r
     """The support a hot-update iteration rebuilt (oracle.hot_update on the same
     input; near-ties as for the block plan)."""
     op = orc.hot_update(x0)
-    _check_support(orc, op, gplan, x0.shape[0], rep, f"{tag} hot update")
+    _check_supports(orc, op, gplan, x0.shape[0], rep, f"{tag} hot update")
     return op
 
 
@@ -289,7 +315,8 @@ def check_iteration(orc, step: GpuStep, live, dec, i: int, wl, rep: Report, tag:
     cl = res.classified
     exp = dict(n_live=cl.n_live, n_new=cl.n_new, n_miss=cl.n_miss, n_stale=cl.n_stale, n_forced=cl.n_forced,
                n_reuse=cl.n_reuse, n_fresh=len(res.fresh_pos), n_edges=res.n_edges,
-               fallback=(1 if res.host_fallback else 0) | (2 if cl.anomaly else 0), bad_flags=cl.bad_flags)
+               fallback=(1 if res.host_fallback else 0) | (2 if cl.anomaly else 0) | (4 if res.shortfall_prev else 0),
+               bad_flags=cl.bad_flags, n_under=res.n_under)
     for key, v in exp.items():
         if st[key] != v:
             rep.mismatches.append(f"{tag} i={i}: stats {key} gpu {st[key]} oracle {v}")

@@ -33,7 +33,8 @@ def _record(orc, wl, x, live, dec, i, force=None):
     cl = res.classified
     stats = dict(n_live=cl.n_live, n_new=cl.n_new, n_miss=cl.n_miss, n_stale=cl.n_stale, n_forced=cl.n_forced,
                  n_reuse=cl.n_reuse, n_fresh=len(res.fresh_pos), n_edges=res.n_edges,
-                 fallback=(1 if res.host_fallback else 0) | (2 if cl.anomaly else 0), bad_flags=cl.bad_flags)
+                 fallback=(1 if res.host_fallback else 0) | (2 if cl.anomaly else 0) | (4 if res.shortfall_prev else 0),
+                 bad_flags=cl.bad_flags, n_under=res.n_under)
     dbg = dict(stats=stats, fresh_pos=res.fresh_pos.copy(), sel=res.sel.copy(), sel_w=res.w.astype(np.float32),
                offsets=res.offsets.copy(), wl_pos=res.wl_pos.copy(), slot=res.slot.copy())
     return GpuStep(x, res.y.copy(), dbg)

@@ -113,7 +113,8 @@ def test_boundary_outputs_support_and_stats():
     ids = torch.full((E,), -1, dtype=torch.int32, device="cuda")
     slen = torch.zeros(1, dtype=torch.int32, device="cuda")
     lay.plan_block(payload_to_torch(xs[0], wl.dtype, lay.device), support_ids=ids, support_len=slen)
-    stats = [torch.full((16,), -7, dtype=torch.int32, device="cuda") for _ in range(4)]
+    from sparse_moe_layer_gate_gb300 import binding as B
+    stats = [torch.full((len(B.STATS_FIELDS),), -7, dtype=torch.int32, device="cuda") for _ in range(4)]
     for i in range(4):
         lay.moe_iter(payload_to_torch(xs[i], wl.dtype, lay.device), torch.from_numpy(live[i]).cuda(),
                      torch.from_numpy(dec[i]).cuda(), i, stats=stats[i])
@@ -208,6 +209,68 @@ def test_group_limited_sigmoid_router(name):
     rep = block_parity(wl)
     assert_clean(rep)
     assert rep.iterations == 6
+
+
+@pytest.mark.parametrize("name", ["tiny_bf16_raw", "tiny_bf16_grouped_raw", "tiny_fp32_raw", "e256_bf16_raw"])
+def test_weights_without_renormalisation(name):
+    """Routing weights kept as the router's own scores: the dense router
+    probabilities of the selected experts (softmax router) or their sigmoid
+    scores (group-limited router), against the oracle."""
+    wl = {
+        "tiny_bf16_raw": TINY_BF16.replace(name=name, raw_weights=True, iters=6),
+        "tiny_bf16_grouped_raw": TINY_BF16.replace(name=name, wid=9, router="sigmoid_group", n_group=4,
+                                                   topk_group=2, raw_weights=True, iters=6),
+        "tiny_fp32_raw": synth.WORKLOADS["tiny_fp32"].replace(name=name, raw_weights=True, iters=6),
+        "e256_bf16_raw": TINY_BF16.replace(name=name, wid=10, n_experts=256, top_k=8, tau=0.95,
+                                           raw_weights=True, iters=6),
+    }[name]
+    rep = block_parity(wl)
+    assert_clean(rep)
+    assert rep.iterations == 6
+
+
+@pytest.mark.parametrize("name", ["tiny_bf16_cov", "tiny_fp32_cov", "e256_bf16_grouped_cov"])
+def test_support_coverage_shortfall(name):
+    """The per-iteration support-coverage check: a support planned small
+    (tau 0.5) under-covers many fresh positions, so some iterations fall back
+    to full fresh with every expert eligible; counts, fallbacks and outputs
+    against the oracle."""
+    wl = {
+        "tiny_bf16_cov": TINY_BF16.replace(name=name, tau=0.5, coverage=(0.6, 0.7), iters=8),
+        "tiny_fp32_cov": synth.WORKLOADS["tiny_fp32"].replace(name=name, tau=0.5, coverage=(0.6, 0.7)),
+        "e256_bf16_grouped_cov": TINY_BF16.replace(name=name, wid=10, n_experts=256, top_k=8, tau=0.6,
+                                                   router="sigmoid_group", n_group=8, topk_group=4,
+                                                   coverage=(0.7, 0.6), iters=8),
+    }[name]
+    layers = [layer_for_workload(wl)]
+    rep = block_parity(wl, layers=layers)
+    assert_clean(rep)
+    assert rep.iterations == wl.iters
+    layers[0].close()
+
+
+@pytest.mark.parametrize("name", ["tiny_bf16_req", "e256_bf16_req", "tiny_fp32_req", "req_grouped_hot"])
+def test_per_request_supports(name):
+    """One block plan per request (32 positions): each request's hit counts,
+    threshold and support, their union as the worklist candidates, and every
+    position selecting within its own request's support; with a hot update
+    for the last case."""
+    if name == "req_grouped_hot":
+        wl = TINY_BF16.replace(name=name, wid=9, router="sigmoid_group", n_group=4, topk_group=2, tau=0.6,
+                               request_size=32)
+        xs, live, dec = _steps_from(wl, 6)
+        steps = [dict(op="plan", x=xs[0])]
+        steps += [dict(op="iter", x=xs[i], live=live[i], dec=dec[i], i=i, hot_update=(i == 3)) for i in range(6)]
+        assert_clean(scenario_parity(wl, steps))
+        return
+    wl = {
+        "tiny_bf16_req": TINY_BF16.replace(name=name, tau=0.6, request_size=32, iters=6),
+        "e256_bf16_req": TINY_BF16.replace(name=name, wid=10, n_experts=256, top_k=8, tau=0.9, request_size=32,
+                                           iters=6),
+        "tiny_fp32_req": synth.WORKLOADS["tiny_fp32"].replace(name=name, batch=3, tau=0.6, request_size=32),
+    }[name]
+    rep = block_parity(wl)
+    assert_clean(rep)
 
 
 def test_tau1_R1_is_dense_moe():

@@ -634,6 +634,110 @@ def test_one_request_is_the_single_support():
     np.testing.assert_allclose(lay.iterate(x, live, dec, 0).y, one.iterate(x, live, dec, 0).y, rtol=1e-14)
 
 
+# ------------------------------------------------------------------ weights without renormalisation
+
+def test_raw_weights_hand_worked():
+    """Weights kept as the router's own scores (renormalize=False), worked by hand:
+    softmax router, logits log(.5, .3, .15, .05), k = 2: the selection is
+    experts 0, 1 with weights .5, .3 (renormalised: .625, .375); sigmoid router
+    with no bias, one group, logits 0, ln 3, -ln 3, 0, k = 2: scores .5, .75,
+    .25, .5, selection 1 then 0 (the tie with 3 goes to the lower id), weights
+    .75, .5 (renormalised: .6, .4)."""
+    g = np.log(np.array([.5, .3, .15, .05]))
+    every = np.ones(4, dtype=bool)
+    sel, w = oracle.route_position(g, np.zeros(4), every, 2, oracle.Router(renormalize=False))
+    assert sel.tolist() == [0, 1]
+    np.testing.assert_allclose(w, [.5, .3], rtol=1e-12)
+    _, w = oracle.route_position(g, np.zeros(4), every, 2, oracle.Router())
+    np.testing.assert_allclose(w, [.625, .375], rtol=1e-12)
+    g = np.array([0.0, np.log(3.0), -np.log(3.0), 0.0])
+    sel, w = oracle.route_position(g, np.zeros(4), every, 2, oracle.Router("sigmoid_group", 1, 1, False))
+    assert sel.tolist() == [1, 0]
+    np.testing.assert_allclose(w, [.75, .5], rtol=1e-12)
+    _, w = oracle.route_position(g, np.zeros(4), every, 2, oracle.Router("sigmoid_group", 1, 1, True))
+    np.testing.assert_allclose(w, [.6, .4], rtol=1e-12)
+
+
+def test_raw_softmax_weights_are_the_topk_routing_mass():
+    """Softmax router without renormalisation: the k weights add up to the k
+    largest dense router probabilities (sorted independently here), all
+    experts selected gives the renormalised weights, and a restricted
+    selection keeps each expert's dense probability."""
+    rng = np.random.default_rng(131)
+    raw = oracle.Router(renormalize=False)
+    for _ in range(50):
+        E, k = int(rng.integers(2, 12)), 0
+        k = int(rng.integers(1, E + 1))
+        g = rng.normal(size=E) * 2
+        every = np.ones(E, dtype=bool)
+        p = np.exp(g) / np.sum(np.exp(g))
+        _, w = oracle.route_position(g, np.zeros(E), every, k, raw)
+        assert abs(np.sum(w) - np.sum(np.sort(p)[::-1][:k])) < 1e-12
+        _, wk = oracle.route_position(g, np.zeros(E), every, E, raw)
+        _, wn = oracle.route_position(g, np.zeros(E), every, E, oracle.Router())
+        np.testing.assert_allclose(wk, wn, rtol=1e-12)
+        mask = rng.random(E) < 0.6
+        if mask.sum() >= k:
+            sel, w = oracle.route_position(g, np.zeros(E), mask, k, raw)
+            np.testing.assert_allclose(w, p[sel], rtol=1e-12)
+
+
+# ------------------------------------------------------------------ support-coverage shortfall
+
+def _coverage_layer(alpha, q, support, experts=4):
+    """G = x (identity router, no bias), SwiGLU experts of a fixed seed, the
+    support set by hand."""
+    rng = np.random.default_rng(141)
+    ex = [(rng.normal(size=(3, experts)), rng.normal(size=(3, experts)), rng.normal(size=(experts, 3)))
+          for _ in range(experts)]
+    lay = oracle.LayerOracle(n_experts=experts, top_k=1, tau=1.0, refresh_R=None, w_router=np.eye(experts),
+                             b_router=np.zeros(experts), expert=lambda e: ex[e], max_positions=2,
+                             coverage=(alpha, q))
+    x = np.log(np.array([[.1, .2, .6, .1], [.7, .1, .1, .1]]))
+    lay.plan_block(x)
+    lay.adopt_support(np.array(support), len(support))
+    return lay, x
+
+
+def test_coverage_shortfall_hand_worked():
+    """Support {0, 1}, top-1, two fresh positions with router probabilities
+    (.1, .2, .6, .1) and (.7, .1, .1, .1): the first one's dense choice (expert
+    2, mass .6) lies outside the support (covered 0 < alpha * .6), the second's
+    inside. One of two under-covered: with q = .6 more than (1 - q) * 2 = .8
+    positions are, so the support falls short and the next iteration is full
+    fresh with every expert eligible (the first position then takes expert 2);
+    with q = .4 the bound is 1.2 and nothing changes. Worked by hand from the
+    definitions of the "Expert Atlas" and lifecycle sections."""
+    live, dec = np.ones(2, np.uint8), np.zeros(2, np.uint8)
+    lay, x = _coverage_layer(0.5, 0.6, [0, 1])
+    r0 = lay.iterate(x, live, dec, 0)
+    assert r0.n_under == 1 and lay.shortfall and not r0.fallback
+    assert r0.sel[:, 0].tolist() == [1, 0]          # restricted to the support
+    r1 = lay.iterate(x, live, dec, 1)
+    assert r1.shortfall_prev and r1.fallback and not r1.host_fallback
+    assert r1.sel[:, 0].tolist() == [2, 0]          # every expert eligible
+    lay, x = _coverage_layer(0.5, 0.4, [0, 1])
+    lay.iterate(x, live, dec, 0)
+    assert not lay.shortfall
+    assert not lay.iterate(x, live, dec, 1).fallback
+
+
+def test_coverage_shortfall_special_cases():
+    """alpha = 0 never falls short; a support of every expert covers every
+    position; a new block plan clears a pending shortfall."""
+    live, dec = np.ones(2, np.uint8), np.zeros(2, np.uint8)
+    lay, x = _coverage_layer(0.0, 1.0, [0])
+    lay.iterate(x, live, dec, 0)
+    assert not lay.shortfall
+    lay, x = _coverage_layer(1.0, 1.0, [0, 1, 2, 3])
+    assert lay.iterate(x, live, dec, 0).n_under == 0 and not lay.shortfall
+    lay, x = _coverage_layer(0.5, 1.0, [0])
+    lay.iterate(x, live, dec, 0)
+    assert lay.shortfall
+    lay.plan_block(x)
+    assert not lay.shortfall
+
+
 # ------------------------------------------------------------------ Expert Atlas planner
 
 def test_atlas_hand_worked_example():
@@ -710,7 +814,9 @@ def _pins_pass():
               test_refresh_path_recomputes_every_position_over_the_support,
               test_hot_update_rebuilds_the_support_from_current_logits,
               test_atlas_hand_worked_example, test_atlas_special_cases_and_invariants,
-              test_per_request_supports_equal_independent_layers, test_one_request_is_the_single_support]
+              test_per_request_supports_equal_independent_layers, test_one_request_is_the_single_support,
+              test_raw_weights_hand_worked, test_raw_softmax_weights_are_the_topk_routing_mass,
+              test_coverage_shortfall_hand_worked, test_coverage_shortfall_special_cases]
     for c in checks:
         try:
             c()
@@ -777,6 +883,29 @@ def _mut_groups_ignore_k(scores, n_elig, topk_group, k):
 CHOSEN_ORIG = om.chosen_groups
 
 
+def _mut_weights_always_renormalised(g_row, sel, router):
+    return SELW_ORIG(g_row, sel, oracle.Router(router.kind, router.n_group, router.topk_group, True))
+
+
+SELW_ORIG = om.selection_weights
+
+
+def _mut_raw_over_selection(g_row):
+    return np.ones_like(g_row) / g_row.shape[0]
+
+
+def _mut_shortfall_q_swapped(self, G, fresh_pos):
+    alpha, q = self.coverage
+    self.coverage = (alpha, 1.0 - q)
+    try:
+        return SHORT_ORIG(self, G, fresh_pos)
+    finally:
+        self.coverage = (alpha, q)
+
+
+SHORT_ORIG = om.LayerOracle.coverage_shortfall
+
+
 def _mut_sigmoid_neg(z):
     return 1.0 / (1.0 + np.exp(z))
 
@@ -792,9 +921,18 @@ def _mut_sigmoid_neg(z):
     ("group score from the best expert only", "group_scores", _mut_group_top1),
     ("groups not extended to k eligible experts", "chosen_groups", _mut_groups_ignore_k),
     ("sigmoid of -G", "sigmoid", _mut_sigmoid_neg),
+    ("raw weights renormalised anyway", "selection_weights", _mut_weights_always_renormalised),
+    ("dense probabilities replaced by a uniform", "dense_probabilities", _mut_raw_over_selection),
 ])
 def test_planted_mistakes_are_caught(monkeypatch, name, attr, mutant):
     assert _pins_pass()
     monkeypatch.setattr(om, attr, mutant)
     monkeypatch.setattr(oracle, attr, mutant)
     assert not _pins_pass(), f"no pin caught: {name}"
+
+
+def test_planted_shortfall_mistake_is_caught(monkeypatch):
+    """The coverage bound taken as q |F| instead of (1 - q) |F|."""
+    assert _pins_pass()
+    monkeypatch.setattr(om.LayerOracle, "coverage_shortfall", _mut_shortfall_q_swapped)
+    assert not _pins_pass(), "no pin caught: shortfall bound with q and 1 - q swapped"
