@@ -36,6 +36,17 @@ METRIC = "MoE-layer µs/refinement iter; fresh token-expert edges/s; % of HBM/TC
 WORKLOAD = "llada2_mini"
 L2_FLUSH_BYTES = 256 << 20
 
+
+class L2Flush:
+    """Evicts L2 between timed iterations by writing a buffer larger than L2."""
+
+    def __init__(self, device):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def __call__(self, i=0):
+        self.w.fill_(i & 0xFF)
+
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one expert-kernel
 # launch: the ncu capture at iteration 20 of the accounting block (231.9 MB read,
 # 3.0 MB written; every iteration of this workload hits the same 34 routed
@@ -104,7 +115,8 @@ def device_layer(wl, layer_index=0, device="cuda", weights=None, max_positions=N
                       max_positions=max_positions or wl.n_pos, dtype=wl.dtype, tau=wl.tau, refresh_R=wl.refresh_R,
                       weights=w, n_shared=wl.n_shared, shared_inter=wl.shared_inter, residual=wl.residual,
                       router=wl.router, n_group=wl.n_group, topk_group=wl.topk_group,
-                      raw_weights=wl.raw_weights, coverage=wl.coverage, request_size=wl.request_size)
+                      raw_weights=wl.raw_weights, coverage=wl.coverage, request_size=wl.request_size,
+                      atlas=dict(zip(("m", "B", "alpha", "q", "beta", "c"), wl.atlas)) if wl.atlas else None)
 
 
 # ---------------------------------------------------------------- data parallelism (replicas only)
@@ -288,7 +300,7 @@ def run_epoch(args, rank, world):
     lv = [torch.from_numpy(live_h[i]).to(dev) for i in range(wl.iters)]
     dc = [torch.from_numpy(dec_h[i]).to(dev) for i in range(wl.iters)]
     ys = [torch.empty_like(xs[0]) for _ in range(wl.iters)]
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
 
     # per-iteration work accounting (inputs are identical every block)
@@ -308,7 +320,7 @@ def run_epoch(args, rank, world):
         lay.plan_block(xs[0])
         ev_plan[1].record(stream)
         for i in range(wl.iters):
-            flush.fill_(i & 0xFF)
+            flush(i)
             ev_iters[i][0].record(stream)
             lay.moe_iter(xs[i], lv[i], dc[i], i, ys[i])
             ev_iters[i][1].record(stream)
@@ -350,6 +362,8 @@ def run_epoch(args, rank, world):
     prof = lay.read_profile()
     clk = clocks.stop()
 
+    pipelined = traced_breakdown(lay, wl, xs, lv, dc, ys, flush)
+    graph = graph_replay_timing(lay, wl, xs, lv, dc, ys, flush, args.steps, edges_per_block)
     plan_ms = [r[0][0].elapsed_time(r[0][1]) for r in records]
     iter_ms = np.array([[r[1][i][0].elapsed_time(r[1][i][1]) for i in range(wl.iters)] for r in records])
     step_ms = np.array(plan_ms) + iter_ms.sum(axis=1)
@@ -399,12 +413,109 @@ def run_epoch(args, rank, world):
                      "peak_source": f"of {src} (STREAM copy, burst)"},
         "kernels": kernels,
         "gpu_launches": gpu_launches,
-        "kernel_timing": "per-kernel CUDA events in a second timed pass of the same steps",
+        "kernel_timing": "per-kernel CUDA events in a second timed pass of the same steps (an event pair "
+                         "around every launch serialises the kernels; see pipelined for the overlapped phases)",
+        "pipelined": pipelined,
+        "graph_replay": graph,
         "clocks": clk,
     }
     if e2e:
         out["e2e"] = e2e
     return out, wl, payload
+
+
+def traced_breakdown(lay, wl, xs, lv, dc, ys, flush):
+    """Phases of the pipelined iteration from the kernels' own per-CTA traces
+    (globaltimer), one traced block, synchronised after every iteration:
+    gate (its first CTA entry until its CTAs have all selected: the grid
+    barrier of its worklist tail, or its last exit when a separate worklist
+    kernel follows), worklist (from there to the expert kernel's first tile:
+    offsets, group list and row copies), expert phase (first tile to the last
+    epilogue), combine tail (last expert epilogue to the combine's last exit),
+    and the whole span. Means over the iterations, in us."""
+    import numpy as np
+    import torch
+    lay.plan_block(xs[0])
+    lay.set_tracing(True)
+    rows = []
+    for i in range(wl.iters):
+        flush(i)
+        lay.moe_iter(xs[i], lv[i], dc[i], i, ys[i])
+        torch.cuda.synchronize()
+        tl = lay.read_timeline()
+        tr = lay.read_trace().astype(np.float64)
+        if not all(k in tl for k in ("gate", "experts", "combine")):
+            continue
+        t0, g1 = tl["gate"]
+        if "routing" not in tl and tr[3, 0, 1] > t0:
+            g1 = tr[3, 0, 1]  # the gate's grid barrier, passed by CTA 0
+        e = tr[1]
+        em = (e[:, 2] > 0) & (e[:, 4] > 0)
+        first_tile, last_epi = float(e[em, 2].min()), float(e[em, 4].max())
+        rows.append([(g1 - t0) / 1e3, (first_tile - g1) / 1e3, (last_epi - first_tile) / 1e3,
+                     (tl["combine"][1] - last_epi) / 1e3, (tl["combine"][1] - t0) / 1e3])
+    lay.set_tracing(False)
+    lay.block_end()
+    if not rows:
+        return None
+    m = np.array(rows).mean(axis=0)
+    return {"gate_us": round(float(m[0]), 2), "worklist_us": round(float(m[1]), 2),
+            "expert_phase_us": round(float(m[2]), 2), "combine_tail_us": round(float(m[3]), 2),
+            "span_us": round(float(m[4]), 2),
+            "how": "per-CTA globaltimer traces of one block, synchronised after every iteration"}
+
+
+def graph_replay_timing(lay, wl, xs, lv, dc, ys, flush, steps, edges_per_block):
+    """The same block (plan, then per iteration an L2 flush and the call)
+    captured once into a CUDA graph and replayed `steps` times, with timing
+    events captured as event-record nodes around the plan and every call
+    (the flushes stay outside them). Returns the edges/s and us per iteration
+    of the replays, or the reason it could not run."""
+    import numpy as np
+    import torch
+    try:
+        mk = lambda: torch.cuda.Event(enable_timing=True, external=True)  # noqa: E731
+        evp = (mk(), mk())
+    except TypeError:
+        return {"unavailable": "this PyTorch cannot capture timing events into a graph"}
+    evi = [(mk(), mk()) for _ in range(wl.iters)]
+
+    def block():
+        s = torch.cuda.current_stream()
+        evp[0].record(s)
+        lay.plan_block(xs[0])
+        evp[1].record(s)
+        for i in range(wl.iters):
+            flush(i)
+            evi[i][0].record(s)
+            lay.moe_iter(xs[i], lv[i], dc[i], i, ys[i])
+            evi[i][1].record(s)
+        lay.block_end()
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        block()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        block()
+    graph.replay()  # warm-up replay
+    torch.cuda.synchronize()
+    plan_ms, iter_ms = [], []
+    for _ in range(steps):
+        graph.replay()
+        torch.cuda.synchronize()
+        plan_ms.append(evp[0].elapsed_time(evp[1]))
+        iter_ms.append([a.elapsed_time(b) for a, b in evi])
+    iter_ms = np.array(iter_ms)
+    block_s = (float(np.sum(plan_ms)) + float(iter_ms.sum())) / 1e3
+    del graph
+    return {"value": edges_per_block * steps / block_s, "unit": "edges/s",
+            "us_per_iter": 1e3 * float(iter_ms.mean()), "plan_us_per_block": 1e3 * float(np.mean(plan_ms)),
+            "steps": steps,
+            "how": "one block captured into a CUDA graph, replayed; event-record nodes around the plan and each call"}
 
 
 # ---------------------------------------------------------------- other workload shapes
@@ -450,7 +561,7 @@ def time_stack(layers, wl, xs, lv, dc, flush, steps, warmup):
                 lay.plan_block(plan_in[l])
             evp[1].record(stream)
         for i in range(wl.iters):
-            flush.fill_(i & 0xFF)
+            flush(i)
             evi[i][0].record(stream)
             x = xs[i]
             for l, lay in enumerate(layers):
@@ -499,7 +610,7 @@ def run_per_config(steps, warmup, dev):
     import synth
     from sparse_moe_layer_gate_gb300.layer import payload_to_torch
     out = {}
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     def inputs(wl):
         xs_h = synth.hidden_states(wl)
@@ -567,7 +678,7 @@ def run_e2e(lay, wl, xs_host, live_h, dec_h, edges_per_block, steps, flush, dev,
     for step in range(steps + 1):
         evs = []
         for i in range(wl.iters):
-            flush.fill_(i & 0xFF)
+            flush(i)
             a, b = mk(), mk()
             a.record(stream)
             xd.copy_(xs_pin[i], non_blocking=True)

@@ -108,12 +108,28 @@ typedef enum { EPOCH_F32 = 0, EPOCH_BF16 = 1 } epoch_dtype;
  *    hot-update、hot-skip": a block plan belongs to one diffusion block). The
  *    layer's support (epoch_plan_block's outputs, the statistics) is then the
  *    union of the requests' supports, in ascending expert order.
+ *  planner: EPOCH_PLANNER_PREFIX (0) is the hit-count prefix rule of tau.
+ *    EPOCH_PLANNER_ATLAS (1) is the planner of [W] section "Expert Atlas"
+ *    (softmax router, one support per call; tau unused): every position's
+ *    K = min(k + atlas_m, E) best experts by logit are its candidate edges,
+ *    weighted by the dense router probabilities W; the coverage floor of a
+ *    position is r = atlas_alpha * (mass of its first k candidates); the initial
+ *    support is the max(atlas_B, k) experts of largest popularity (sum of W
+ *    over their candidate edges); then, while more than (1 - atlas_q) of the
+ *    positions have a support coverage C < r, the at most atlas_c experts of
+ *    largest positive H_e + atlas_beta * G_e join (G_e: the uncovered mass e
+ *    would add, min(W, r - C) summed over under-covered positions; H_e: the
+ *    under-covered positions it would lift to r). The support is listed in
+ *    the order experts joined.
  * Constraints (else EPOCH_EINVAL): 1 <= top_k <= n_experts <= 1024, top_k <= 16;
  *  bf16: H a multiple of 256, I and shared_inter multiples of 128; f32: multiples of 4;
  *  1 <= max_positions <= 16384; router 1: 1 <= n_group <= 32, n_experts a
  *  multiple of n_group, 1 <= topk_group <= n_group (router 0 ignores both);
  *  raw_weights 0 or 1; with coverage_check, 0 <= coverage_alpha <= 1 and
- *  0 <= coverage_q <= 1; 0 <= request_size <= max_positions. */
+ *  0 <= coverage_q <= 1; 0 <= request_size <= max_positions; planner 0 or 1; the
+ *  Atlas planner needs router 0, request_size 0, atlas_m >= 0, k + atlas_m <= 32,
+ *  atlas_B >= 1, atlas_c >= 1, 0 <= atlas_alpha <= 1, 0 <= atlas_q <= 1,
+ *  atlas_beta >= 0. */
 typedef struct {
   int32_t hidden;
   int32_t n_experts;
@@ -134,7 +150,16 @@ typedef struct {
   double coverage_alpha;
   double coverage_q;
   int32_t request_size;
+  int32_t planner;
+  int32_t atlas_m;
+  int32_t atlas_B;
+  int32_t atlas_c;
+  double atlas_alpha;
+  double atlas_q;
+  double atlas_beta;
 } epoch_layer_config;
+
+enum { EPOCH_PLANNER_PREFIX = 0, EPOCH_PLANNER_ATLAS = 1 };
 
 enum { EPOCH_ROUTER_SOFTMAX = 0, EPOCH_ROUTER_SIGMOID_GROUP = 1 };
 
@@ -226,6 +251,9 @@ typedef struct {
   const uint8_t *support_masks;
   const int32_t *request_ids;
   const int32_t *request_len;
+  /* Expert Atlas planner: [0] coverage bound met (1) or not, [1] positions
+   * left under-covered, [2] repair rounds. */
+  const int32_t *atlas_result;
 } epoch_debug_view;
 
 /* Per-kernel timing, accumulated while profiling is on. */

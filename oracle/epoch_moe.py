@@ -294,6 +294,11 @@ class AtlasResult:
     n_under: int             # |U|, tokens below their coverage floor
     rounds: int              # repair rounds run
     popularity: np.ndarray   # p_e
+    # the smallest gap at any decision of the run (popularity at the cut of
+    # the initial support, |C_t - r_t| of every coverage test, the score at the
+    # cut of every repair round and its distance from zero): a GPU run in
+    # float32 may decide differently only where this is tiny
+    min_margin: float = float("inf")
 
 
 def softmax_rows(G: np.ndarray) -> np.ndarray:
@@ -334,7 +339,9 @@ def atlas_support(G: np.ndarray, k: int, m: int, B: int, alpha: float, q: float,
         for j in range(K):
             pop[cand[t, j]] += W[t, j]
     by_pop = sorted(range(E), key=lambda e: (-pop[e], e))
-    support = list(by_pop[:min(max(B, k), E)])
+    n_init = min(max(B, k), E)
+    support = list(by_pop[:n_init])
+    margin = [abs(pop[by_pop[n_init - 1]] - pop[by_pop[n_init]])] if n_init < E else []
     in_s = np.zeros(E, dtype=bool)
     in_s[support] = True
 
@@ -343,6 +350,7 @@ def atlas_support(G: np.ndarray, k: int, m: int, B: int, alpha: float, q: float,
 
     rounds = 0
     C = coverage()
+    margin.append(float(np.min(np.abs(C - r))))
     under = [t for t in range(N) if C[t] < r[t]]
     while len(under) > (1.0 - q) * N:
         Gs = np.zeros(E)
@@ -356,20 +364,27 @@ def atlas_support(G: np.ndarray, k: int, m: int, B: int, alpha: float, q: float,
                 Gs[e] += min(W[t, j], r[t] - C[t])
                 mass[e] = mass.get(e, 0.0) + W[t, j]
             for e, w in mass.items():
+                margin.append(abs(C[t] + w - r[t]))
                 if C[t] + w >= r[t]:
                     Hs[e] += 1
         score = Hs + beta * Gs
         pos = [e for e in range(E) if not in_s[e] and score[e] > 0]
         if not pos:
             break
-        add = sorted(pos, key=lambda e: (-score[e], e))[:c]
+        ranked = sorted(pos, key=lambda e: (-score[e], e))
+        add = ranked[:c]
+        margin.append(min(score[e] for e in pos))
+        if len(ranked) > c:
+            margin.append(score[ranked[c - 1]] - score[ranked[c]])
         for e in add:
             in_s[e] = True
             support.append(e)
         rounds += 1
         C = coverage()
+        margin.append(float(np.min(np.abs(C - r))))
         under = [t for t in range(N) if C[t] < r[t]]
-    return AtlasResult(np.array(support, dtype=np.int64), len(under) <= (1.0 - q) * N, len(under), rounds, pop)
+    return AtlasResult(np.array(support, dtype=np.int64), len(under) <= (1.0 - q) * N, len(under), rounds, pop,
+                       float(min(margin)) if margin else float("inf"))
 
 
 # ------------------------------------------------------------------ liveness
@@ -477,7 +492,7 @@ class LayerOracle:
                  expert: Callable[[int], ExpertWeights],
                  shared: Sequence[ExpertWeights] = (), residual: bool = False,
                  max_positions: int, router: Router = Router(), request_size: Optional[int] = None,
-                 coverage: Optional[Tuple[float, float]] = None):
+                 coverage: Optional[Tuple[float, float]] = None, atlas: Optional[dict] = None):
         self.E = n_experts
         self.k = top_k
         self.tau = tau
@@ -506,6 +521,12 @@ class LayerOracle:
         # support-coverage check (alpha, q) or None: see coverage_shortfall
         self.coverage = coverage
         self.shortfall = False
+        # Expert Atlas planner instead of the hit-count prefix: dict of m, B,
+        # alpha, q, beta, c (atlas_support), or None
+        self.atlas = atlas
+        self.atlas_result: Optional[AtlasResult] = None
+        if atlas is not None and (request_size is not None or router.kind != "softmax"):
+            raise ValueError("the Expert Atlas planner is built for one support per call and the softmax router")
 
     def logits(self, x: np.ndarray) -> np.ndarray:
         """Router logits G (the bias is part of G only for the softmax router)."""
@@ -539,6 +560,12 @@ class LayerOracle:
         """The plan rule on G: one support, or one per request (each request's
         own positions, counts and threshold); support_mask is then their union."""
         N = G.shape[0]
+        if self.atlas is not None:
+            res = atlas_support(G, self.k, **self.atlas)
+            self.atlas_result = res
+            self.support_mask = np.zeros(self.E, dtype=bool)
+            self.support_mask[res.support] = True
+            return PlanResult(G, res.popularity, res.support, int(res.support.size), 0)
         cnt = self.counts(G)
         if self.request_size is None:
             ranked, slen = plan_support(cnt, self.k, self.tau, N)

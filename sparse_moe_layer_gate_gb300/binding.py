@@ -27,7 +27,9 @@ class epoch_layer_config(C.Structure):
                 ("refresh_R", C.c_int32), ("residual", C.c_int32), ("router", C.c_int32),
                 ("n_group", C.c_int32), ("topk_group", C.c_int32), ("raw_weights", C.c_int32),
                 ("coverage_check", C.c_int32), ("coverage_alpha", C.c_double), ("coverage_q", C.c_double),
-                ("request_size", C.c_int32)]
+                ("request_size", C.c_int32), ("planner", C.c_int32), ("atlas_m", C.c_int32),
+                ("atlas_B", C.c_int32), ("atlas_c", C.c_int32), ("atlas_alpha", C.c_double),
+                ("atlas_q", C.c_double), ("atlas_beta", C.c_double)]
 
 
 class epoch_layer_weights(C.Structure):
@@ -56,7 +58,7 @@ class epoch_debug_view(C.Structure):
                 ("wl_pos", C.c_void_p), ("slot", C.c_void_p), ("stamp", C.c_void_p),
                 ("cache", C.c_void_p), ("stats", C.c_void_p), ("error_word", C.c_void_p),
                 ("trace", C.c_void_p), ("timeline", C.c_void_p), ("support_masks", C.c_void_p),
-                ("request_ids", C.c_void_p), ("request_len", C.c_void_p)]
+                ("request_ids", C.c_void_p), ("request_len", C.c_void_p), ("atlas_result", C.c_void_p)]
 
 
 class epoch_profile(C.Structure):

@@ -32,7 +32,6 @@ struct epoch_layer {
   int32_t n_pos_plan;
   int32_t last_iter;
   int32_t state_rd;  // half of the double-buffered iteration state the next iteration reads
-  uint32_t seq;      // sequence number of the last iteration call
   int64_t n_cold, n_hot, n_fallback, n_launch;
   int64_t n_hot_update, n_refresh;
   // profiling
@@ -71,6 +70,12 @@ bool valid_config(const epoch_layer_config *c) {
   if (c->router != EPOCH_ROUTER_SOFTMAX && c->router != EPOCH_ROUTER_SIGMOID_GROUP) return false;
   if (c->raw_weights != 0 && c->raw_weights != 1) return false;
   if (c->request_size < 0 || c->request_size > c->max_positions) return false;
+  if (c->planner != EPOCH_PLANNER_PREFIX && c->planner != EPOCH_PLANNER_ATLAS) return false;
+  if (c->planner == EPOCH_PLANNER_ATLAS &&
+      (c->router != EPOCH_ROUTER_SOFTMAX || c->request_size != 0 || c->atlas_m < 0 || c->top_k + c->atlas_m > 32 ||
+       c->atlas_B < 1 || c->atlas_c < 1 || !(c->atlas_alpha >= 0.0 && c->atlas_alpha <= 1.0) ||
+       !(c->atlas_q >= 0.0 && c->atlas_q <= 1.0) || !(c->atlas_beta >= 0.0)))
+    return false;
   if (c->coverage_check && !(c->coverage_alpha >= 0.0 && c->coverage_alpha <= 1.0 && c->coverage_q >= 0.0 &&
                              c->coverage_q <= 1.0))
     return false;
@@ -103,6 +108,12 @@ size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   t.plan_counts = static_cast<int32_t *>(take(R * E * 4));
   t.req_ids = static_cast<int32_t *>(take(R * E * 4));
   t.req_len = static_cast<int32_t *>(take(R * 4));
+  const bool atlas = c.planner == EPOCH_PLANNER_ATLAS;
+  t.atlas_cand = static_cast<int32_t *>(take(atlas ? N * 32 * 4 : 16));
+  t.atlas_w = static_cast<float *>(take(atlas ? N * 32 * 4 : 16));
+  t.atlas_r = static_cast<float *>(take(atlas ? N * 4 : 16));
+  t.atlas_pop = static_cast<unsigned long long *>(take(E * 8));
+  t.atlas_out = static_cast<int32_t *>(take(16));
   t.cache = take(N * H * act);
   t.logits = static_cast<float *>(take(N * E * 4));
   t.cat = static_cast<uint8_t *>(take(N));
@@ -116,7 +127,9 @@ size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   t.done_up = static_cast<int32_t *>(take((E + nsh) * 4));
   t.cov_under = static_cast<int32_t *>(take(8));
   t.tile_ctr = static_cast<int32_t *>(take(16));
-  t.sh_ctr = static_cast<int32_t *>(take(2 * (1 + nsh * ((N + kTnUp - 1) / kTnUp)) * 4));
+  t.tally = static_cast<int32_t *>(take(32));
+  t.gate_arrive = static_cast<int32_t *>(take(8));
+  t.sh_ctr = static_cast<int32_t *>(take((1 + nsh * ((N + kTnUp - 1) / kTnUp)) * 4));
   t.wl_pos = static_cast<int32_t *>(take(N * k * 4));
   t.slot = static_cast<int32_t *>(take(N * k * 4));
   t.xp = take(N * k * H * act);
@@ -132,7 +145,6 @@ size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   } else {
     t.pk_gu = t.pk_d = t.pk_sgu = t.pk_sd = nullptr;
   }
-  t.route_done = static_cast<unsigned int *>(take(16));
   t.trace = static_cast<int64_t *>(take(static_cast<size_t>(kTraceRows) * kTraceCtas * kTraceFields * 8));
   t.timeline = static_cast<unsigned long long *>(take(2ull * K_NUM * 8));
   t.ctrl = static_cast<Ctrl *>(take(sizeof(Ctrl)));
@@ -190,6 +202,7 @@ Dims call_dims(const epoch_layer *L, int32_t n_pos, int32_t iter, int host_fallb
   d.iter = iter;
   d.host_fallback = host_fallback;
   d.state_rd = L->state_rd;
+  d.wl_in_gate = 0;
   return d;
 }
 
@@ -207,6 +220,27 @@ epoch_status run_gate(epoch_layer *L, Dims &d, const void *x, const uint8_t *liv
   EPOCH_TRY(run(L, K_GATE, s, [&] { return launch_gate_simt(d, L->w, L->ws, x, 0, s); }));
   if (d.plan_mode) return EPOCH_OK;
   return run(L, K_SELECT, s, [&] { return launch_select(d, L->ws, live, decoded, L->w.b_router, s); });
+}
+
+// The support from the logits of the plan-mode gate: the hit-count prefix
+// rule (one support, or one per request), or the Expert Atlas planner.
+// clear_state: a block plan (resets the block's cache state); else a hot update.
+epoch_status run_planner(epoch_layer *L, const Dims &d, int clear_state, int32_t *ids_out, int32_t *len_out,
+                         cudaStream_t s) {
+  if (L->cfg.planner == EPOCH_PLANNER_ATLAS) {
+    const AtlasParams a{L->cfg.atlas_m, L->cfg.atlas_B, L->cfg.atlas_c, L->cfg.atlas_alpha, L->cfg.atlas_q,
+                        L->cfg.atlas_beta};
+    return run(L, K_PLAN_SUPPORT, s, [&] { return launch_atlas(d, L->ws, a, clear_state, ids_out, len_out, s); });
+  }
+  const int32_t n_pos = d.n_pos;
+  if (cudaMemsetAsync(L->ws.plan_counts, 0, sizeof(int32_t) * d.E * plan_rows(L->cfg, n_pos), s) != cudaSuccess)
+    return EPOCH_ECUDA;
+  EPOCH_TRY(run(L, K_PLAN_TOPK, s, [&] { return launch_plan_topk(d, L->w, L->ws, s); }));
+  const double tau = L->cfg.tau;
+  const int all = tau >= 1.0;
+  const int32_t T = static_cast<int32_t>(std::ceil(tau * static_cast<double>(n_pos * L->cfg.top_k)));
+  return run(L, K_PLAN_SUPPORT, s,
+             [&] { return launch_plan_support(d, L->ws, T, all, clear_state, ids_out, len_out, tau, s); });
 }
 
 }  // namespace
@@ -310,7 +344,6 @@ epoch_status epoch_layer_create(const epoch_layer_config *cfg, const epoch_layer
   L->n_pos_plan = 0;
   L->last_iter = -1;
   L->state_rd = 0;
-  L->seq = 0;
   L->prof = false;
   for (int i = 0; i < K_NUM; ++i) {
     L->total_ms[i] = 0.0;
@@ -329,14 +362,7 @@ epoch_status epoch_plan_block(epoch_layer *L, const void *x, int32_t n_pos, epoc
   d.plan_mode = 1;
   CUtensorMap x_map_up;
   EPOCH_TRY(run_gate(L, d, x, nullptr, nullptr, &x_map_up, s));
-  if (cudaMemsetAsync(L->ws.plan_counts, 0, sizeof(int32_t) * d.E * plan_rows(L->cfg, n_pos), s) != cudaSuccess)
-    return EPOCH_ECUDA;
-  EPOCH_TRY(run(L, K_PLAN_TOPK, s, [&] { return launch_plan_topk(d, L->w, L->ws, s); }));
-  const double tau = L->cfg.tau;
-  const int all = tau >= 1.0;
-  const int32_t T = static_cast<int32_t>(std::ceil(tau * static_cast<double>(n_pos * L->cfg.top_k)));
-  EPOCH_TRY(run(L, K_PLAN_SUPPORT, s,
-                [&] { return launch_plan_support(d, L->ws, T, all, 1, support_ids_dev, support_len_dev, tau, s); }));
+  EPOCH_TRY(run_planner(L, d, 1, support_ids_dev, support_len_dev, s));
   L->planned = true;
   L->n_pos_plan = n_pos;
   L->last_iter = -1;
@@ -361,33 +387,28 @@ epoch_status epoch_moe_iter_path(epoch_layer *L, const void *x, const uint8_t *l
         cudaMemsetAsync(L->ws.timeline + K_NUM, 0, K_NUM * 8, s) != cudaSuccess)
       return EPOCH_ECUDA;
   }
-  d.seq = ++L->seq;
   CUtensorMap x_map_up;
   if (path & EPOCH_PATH_HOT_UPDATE) {
     // hot-update path: logits of this iteration, the support rebuilt from them
     // (block-plan rule, state kept), then classification and top-k over it
     d.plan_mode = 1;
     EPOCH_TRY(run_gate(L, d, x, live, decoded, &x_map_up, s));
-    if (cudaMemsetAsync(L->ws.plan_counts, 0, sizeof(int32_t) * d.E * plan_rows(L->cfg, n_pos), s) != cudaSuccess)
-      return EPOCH_ECUDA;
-    EPOCH_TRY(run(L, K_PLAN_TOPK, s, [&] { return launch_plan_topk(d, L->w, L->ws, s); }));
-    const double tau = L->cfg.tau;
-    const int all = tau >= 1.0;
-    const int32_t T = static_cast<int32_t>(std::ceil(tau * static_cast<double>(n_pos * L->cfg.top_k)));
-    EPOCH_TRY(run(L, K_PLAN_SUPPORT, s,
-                  [&] { return launch_plan_support(d, L->ws, T, all, 0, nullptr, nullptr, tau, s); }));
+    EPOCH_TRY(run_planner(L, d, 0, nullptr, nullptr, s));
     d.plan_mode = 0;
     EPOCH_TRY(run(L, K_SELECT, s, [&] { return launch_select(d, L->ws, live, decoded, L->w.b_router, s); }));
     ++L->n_hot_update;
   } else {
+    // bf16 gates of one wave build the worklist in their tail
+    d.wl_in_gate = L->bf16 && gate_builds_worklist(d) ? 1 : 0;
     EPOCH_TRY(run_gate(L, d, x, live, decoded, &x_map_up, s));
   }
   if (path & EPOCH_PATH_REFRESH) ++L->n_refresh;
   if (L->bf16) {
-    // the expert kernel builds the worklist itself (worklist.cuh)
-    EPOCH_TRY(run(L, K_UP, s, [&] { return launch_experts_tc(d, L->maps, L->ws, x_map_up, x, s); }));
+    if (!d.wl_in_gate)
+      EPOCH_TRY(run(L, K_ROUTING, s, [&] { return launch_route(d, L->ws, x, s); }));
+    EPOCH_TRY(run(L, K_UP, s, [&] { return launch_experts_tc(d, L->maps, L->ws, x_map_up, s); }));
   } else {
-    EPOCH_TRY(run(L, K_ROUTING, s, [&] { return launch_route(d, L->ws, s); }));
+    EPOCH_TRY(run(L, K_ROUTING, s, [&] { return launch_route(d, L->ws, nullptr, s); }));
     EPOCH_TRY(run(L, K_UP, s, [&] { return launch_up_simt(d, L->w, L->ws, x, s); }));
     EPOCH_TRY(run(L, K_DOWN, s, [&] { return launch_down_simt(d, L->w, L->ws, s); }));
   }
@@ -456,6 +477,7 @@ epoch_status epoch_debug_pointers(epoch_layer *L, epoch_debug_view *v) {
   v->support_masks = L->ws.support_mask;
   v->request_ids = L->ws.req_ids;
   v->request_len = L->ws.req_len;
+  v->atlas_result = L->ws.atlas_out;
   return EPOCH_OK;
 }
 

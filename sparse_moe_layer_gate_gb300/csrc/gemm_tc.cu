@@ -29,7 +29,7 @@
 #include "common.cuh"
 #include "layer.h"
 #include "select.cuh"
-#include "worklist.cuh"
+#include "gate_tail.cuh"
 
 namespace epoch {
 
@@ -49,8 +49,6 @@ struct __align__(128) TcParams {
   CUtensorMap bs2;   // experts: A (shared down tiles), box of kTnUp rows
   Dims d;
   Work ws;
-  const uint4 *x;    // x rows, copied into xp at the worklist positions
-  int32_t vec_per_row;  // 16-byte vectors per row of x
 };
 
 // Waits for a phase without the abort check (teardown after an abort: lets
@@ -86,6 +84,7 @@ struct __align__(128) GateParams {
   Work ws;
   const float *bias;
   const uint8_t *live, *decoded;
+  const uint4 *xv;  // x as 16-byte vectors (rows copied into xp by the worklist tail)
   int32_t cs;      // CTAs per cluster (H slices)
   int32_t tn;      // positions per cluster tile (multiple of 16, <= 256, multiple of cs)
   int32_t tcols;   // TMEM columns allocated
@@ -104,9 +103,13 @@ __host__ __device__ inline int gate_stage_bytes(int E, int TN) { return (gate_e_
 template <int EPL>
 __device__ __forceinline__ void gate_position(const Dims &d, const Work &ws, int t, int code, int32_t stamp,
                                               const float *row, int E_pad, const uint8_t *support, bool force,
-                                              uint32_t *words, uint2 *scratch, const float *bias) {
+                                              uint32_t *words, uint2 *scratch, const float *bias, uint8_t *fr_out,
+                                              int16_t *sel_out) {
   const bool fresh = force || (code & 15) != C_REUSE;
-  if (lane_id() == 0) record_position(d, ws, t, code, fresh ? d.iter : stamp);
+  if (lane_id() == 0) {
+    record_position(d, ws, t, code, fresh ? d.iter : stamp);
+    *fr_out = fresh ? 1 : 0;
+  }
   if (!fresh) return;
   float v[EPL];
 #pragma unroll
@@ -114,15 +117,16 @@ __device__ __forceinline__ void gate_position(const Dims &d, const Work &ws, int
     const int e = lane_id() * EPL + c;
     v[c] = e < E_pad ? row[e] : -INFINITY;
   }
-  select_position<EPL>(d, ws, t, v, support, force, words, scratch, bias);
+  select_position<EPL>(d, ws, t, v, support, force, words, scratch, bias, sel_out);
 }
+
+constexpr int kGateThreads = 384;
 
 // 12 warps: 0 issues the TMA loads, 1 the MMAs, 4-7 read TMEM; all of them
 // reduce, and each takes the top-k of one of the CTA's positions (up to 12).
-constexpr int kGateThreads = 384;
 
-// At most 104 registers a thread, so that a CTA of the row-permute kernel
-// (launched while the gate runs) still fits beside a gate CTA.
+// At most 104 registers a thread: the CTA's 384 threads take 40 K of the SM's
+// 64 K registers.
 template <int EPL>
 __global__ void __maxnreg__(104) k_tc_gate(const __grid_constant__ GateParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -150,6 +154,14 @@ __global__ void __maxnreg__(104) k_tc_gate(const __grid_constant__ GateParams p)
   int *s_code = reinterpret_cast<int *>(tmem_slot + 4);  // [TPC] classification codes of the own positions
   int *s_stamp = s_code + 64;                             // [TPC] their previous stamps
   uint2 *s_scr = reinterpret_cast<uint2 *>(s_stamp + 64);  // [warps][32] top-k scratch
+  // for the worklist tail (gate_tail.cuh)
+  uint64_t *x_barp = reinterpret_cast<uint64_t *>(s_scr + 32 * (kGateThreads / 32));  // staged x rows
+  int *s_ncand = reinterpret_cast<int *>(x_barp + 1);
+  uint8_t *s_fr = reinterpret_cast<uint8_t *>(s_ncand + 2);  // [64] own position fresh
+  int16_t *s_sel = reinterpret_cast<int16_t *>(s_fr + 64);   // [64][16] its selected experts
+  int16_t *s_cand = s_sel + 64 * 16;                         // [1024] candidate experts
+  int16_t *s_cidx = s_cand + 1024;                           // [1024] candidate index of an expert
+  const uint32_t x_bar = smem_u32(x_barp);
 
   const KernelMark mark_(d, ws, K_GATE);
   pdl_wait();
@@ -175,6 +187,7 @@ __global__ void __maxnreg__(104) k_tc_gate(const __grid_constant__ GateParams p)
       mbar_init(empty_bar(s), 1);
     }
     mbar_init(done_bar, 1);
+    mbar_init(x_bar, 1);
     *abort_flag = 0;
     *s_anom = 0;
     mbar_fence_init();
@@ -271,6 +284,16 @@ __global__ void __maxnreg__(104) k_tc_gate(const __grid_constant__ GateParams p)
                       kGateThreads - 64))
         atomicOr(s_anom, 1);
       if (tid == 64 && shortfall_flag(d, ws)) atomicOr(s_anom, 2);
+      if (d.wl_in_gate) {  // the plan's candidate experts, for the worklist tail
+        const int nc = ws.ctrl->support_len;
+        if (tid == 64) *s_ncand = nc;
+        for (int i = tid - 64; i < d.E; i += kGateThreads - 64) {
+          const int e = ws.support_ids[i];
+          const bool valid = e >= 0 && e < d.E;
+          s_cand[i] = static_cast<int16_t>(valid ? e : 0);
+          if (i < nc && valid) s_cidx[e] = static_cast<int16_t>(i);
+        }
+      }
     }
   }
   if (wid >= 4 && wid < 8) {
@@ -296,7 +319,9 @@ __global__ void __maxnreg__(104) k_tc_gate(const __grid_constant__ GateParams p)
   tc_fence_before();
   __syncthreads();
   if (trace2 && tid == 0) trace2[0] = static_cast<int64_t>(globaltimer_ns());
-  if (!d.plan_mode && blockIdx.x == 0) reset_iteration_state(d, ws, *s_anom);
+  if (!d.plan_mode && blockIdx.x == 0) {
+    reset_iteration_state(d, ws, *s_anom);
+  }
   if (wid == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, tcols);
@@ -370,7 +395,7 @@ __global__ void __maxnreg__(104) k_tc_gate(const __grid_constant__ GateParams p)
       // per-request supports: the position's request's mask (read from global memory)
       const uint8_t *mask = d.req_size > 0 ? ws.support_mask + static_cast<size_t>(t / d.req_size) * d.E : s_support;
       gate_position<EPL>(d, ws, t, s_code[j], s_stamp[j], rows + j * E_pad, E_pad, mask, force, words,
-                         s_scr + 32 * wid, s_bias);
+                         s_scr + 32 * wid, s_bias, s_fr + j, s_sel + j * 16);
     }
   }
   if (trace && tid == 0) {
@@ -380,6 +405,12 @@ __global__ void __maxnreg__(104) k_tc_gate(const __grid_constant__ GateParams p)
   }
   cluster_wait();  // no CTA leaves while another may still read its partials
   if (trace2 && tid == 0) trace2[3] = static_cast<int64_t>(globaltimer_ns());
+  if (!d.plan_mode && d.wl_in_gate) {
+    const GateTail gt{s_sel, s_fr, s_code, s_cand, s_cidx, *s_ncand, x_bar};
+    int64_t *trace_wl = (d.trace && blockIdx.x == 0) ? ws.trace + 3ull * kTraceCtas * kTraceFields : nullptr;
+    gate_tail(d, ws, reinterpret_cast<const uint8_t *>(p.xv), smem, gt, tile * TN + rank * TPC, TPC,
+              d.host_fallback != 0 || *s_anom != 0, *s_anom, trace_wl);
+  }
 }
 
 // ---------------------------------------------------------------- fused expert kernel
@@ -410,7 +441,6 @@ constexpr int kExpOffOffs = kExpOffPref + 4 * kExpGroups;         // int32 [kExp
 constexpr int kExpSmem = 1024 + kExpOffOffs + 4 * kExpGroups;
 static_assert(kExpSmem <= 227 * 1024, "shared memory");
 static_assert(kTnUp == kTnDn, "up and down tiles share the token tiling");
-static_assert(sizeof(WlSmem) <= 4 * kExpStg, "the worklist scratch fits in the epilogue staging area");
 
 // Decoded tile as handed through the ring: x = group | kDownBit for a down
 // tile (-1 ends the stream), y = row block, z = first token row, w = valid rows.
@@ -594,34 +624,17 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   if (trace && threadIdx.x == 0) trace[1] = static_cast<int64_t>(globaltimer_ns());
-  // The prologue above may overlap the gate (programmatic dependent launch).
-  // Once the gate has finished, every CTA builds the worklist's offsets and
-  // group list itself (all 192 threads, from the gate's selection words) and
-  // copies its share of the worklist rows into xp. The producer streams no
-  // tile until every CTA has copied its rows (tile_ctr[2]): these steps are
-  // chains of dependent memory accesses, and weight streams running beside
-  // them make every access wait behind them. The epilogue warps meanwhile do
-  // this CTA's share of the bookkeeping before their first epilogue. The
-  // scratch of the worklist build lives in the epilogue staging area.
-  const int par = static_cast<int>(d.seq & 1u);
-  int32_t *shc = ws.sh_ctr + static_cast<size_t>(par) * sh_stride(d);  // [0] tile counter, then done counts
+  // This launch overlaps the kernel before it (programmatic dependent
+  // launch): the gate, which builds the iteration's worklist in its tail, or
+  // the worklist kernel. The shared experts need only the layer input, so the
+  // CTAs start on their tiles at once (on the SMs the gate leaves free, while
+  // it runs); the producer waits for the kernel before to complete only when
+  // the shared tiles are all taken, then reads the worklist.
+  int32_t *shc = ws.sh_ctr;  // [0] shared tile counter, then done counts (zeroed by the previous combine)
   const int nt_max = (d.Nmax + kTnUp - 1) / kTnUp;
   const int nt_sh = (d.n_pos + kTnUp - 1) / kTnUp;
   const int n_sh_up = d.tn > 0 ? d.n_sh * nt_sh * (d.I_s / BM) : 0;
   const int n_sh_dn = d.tn > 0 ? d.n_sh * nt_sh * (d.H / kBmDn) : 0;
-  WlSmem &wsm = *reinterpret_cast<WlSmem *>(stage_out);
-  int64_t *trace_wl = (d.trace && blockIdx.x == 0) ? ws.trace + 3ull * kTraceCtas * kTraceFields : nullptr;
-  const Group all{static_cast<int>(threadIdx.x), 192, 0};
-  const Group epi{static_cast<int>(threadIdx.x) - 64, 128, 2};
-  if (trace_wl && threadIdx.x == 0) trace_wl[0] = static_cast<int64_t>(globaltimer_ns());
-  wl_prepare(d, ws, wsm, s_offs, all);
-  pdl_wait();  // the gate has finished: selection words, selections, codes, anomaly flag
-  if (trace_wl && threadIdx.x == 0) trace_wl[1] = static_cast<int64_t>(globaltimer_ns());
-  const WlPlan wl = wl_phase_a(d, ws, wsm, s_offs, s_list, blockIdx.x == 0, all);
-  if (trace_wl && threadIdx.x == 0) trace_wl[2] = static_cast<int64_t>(globaltimer_ns());
-  // this CTA's worklist rows (positions, and x rows into xp) before any tile streams
-  wl_rows(d, ws, wsm, s_offs, wl, p.x, p.vec_per_row, blockIdx.x, gridDim.x, all);
-  if (trace_wl && threadIdx.x == 0) trace_wl[4] = static_cast<int64_t>(globaltimer_ns());
 
   if (wid == 0) {
     // ---------------- producer warp (lane 0 issues): per K block, a 32 KB run of
@@ -710,60 +723,44 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
       tma_prefetch_desc(&p.bs2);
       tma_prefetch_desc(&p.b[0]);
       tma_prefetch_desc(&p.b2[0]);
-      // tile list, in segments: the shared experts' up tiles, routed up tiles,
-      // the shared experts' down tiles, routed down tiles
-      const int n_up = d.tn > 0 ? (d.I / BM) * wl.n_tiles : 0;
-      const int seg_end[4] = {n_sh_up, n_sh_up + n_up, n_sh_up + n_up + n_sh_dn,
-                              n_sh_up + n_up + n_sh_dn + (d.tn > 0 ? (d.H / kBmDn) * wl.n_tiles : 0)};
-      const int total = ok ? seg_end[3] : 0;
-      const int copied = wl.n_edges * p.vec_per_row;  // vectors the CTAs copy into xp
-      {  // no weight stream before every CTA's worklist steps are done
-        const uint64_t t0 = globaltimer_ns();
-        for (;;) {
-          int done;
-          asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(done) : "l"(ws.tile_ctr + 2) : "memory");
-          if (done >= copied) break;
-          if (globaltimer_ns() - t0 > tmo) {
-            set_error(ws.err, EPOCH_DEVERR_TIMEOUT);
-            *abort_flag = 1;
-            ok = false;
-            break;
-          }
-          __nanosleep(200);  // 152 pollers of one line: keep its traffic low
-        }
-        if (trace) trace[2] = static_cast<int64_t>(globaltimer_ns());
-      }
+      // 1. the shared experts' tiles (up tiles, then down tiles), from launch
       while (ok) {
-        const int tile = atomicAdd(ws.tile_ctr, 1);
-        if (tile >= total) break;
-        const int seg = tile < seg_end[0] ? 0 : tile < seg_end[1] ? 1 : tile < seg_end[2] ? 2 : 3;
+        const int q = atomicAdd(shc, 1);
+        if (q >= n_sh_up + n_sh_dn) break;
+        int need = 0, tt;
+        const int4 td = shared_tile(d, q, &need, &tt);
+        const int32_t *flag = q >= n_sh_up ? shc + 1 + ((td.x & (kDownBit - 1)) - d.E) * nt_max + tt : nullptr;
+        ok = post(td) && issue(td, flag, need, 2);
+      }
+    }
+    __syncwarp();
+    // 2. the routed experts' tiles, from one counter: up tiles, then down
+    // tiles, once the worklist of this call is complete (offsets, group list,
+    // xp rows)
+    pdl_wait();
+    for (int i = lane; i <= d.E; i += 32) {
+      s_list[i] = ws.grp_list[i];
+      s_offs[i] = ws.offsets[i];
+    }
+    __syncwarp();
+    if (lane == 0) {
+      const int n_tiles = s_list[d.E] >> kGrpIdBits;
+      const int n_up = d.tn > 0 ? (d.I / BM) * n_tiles : 0;
+      const int total = ok ? n_up + (d.tn > 0 ? (d.H / kBmDn) * n_tiles : 0) : 0;
+      while (ok) {
+        const int q = atomicAdd(ws.tile_ctr, 1);
+        if (q >= total) break;
         int4 td;
-        int need = 0, kind = 0;
-        const int32_t *flag = nullptr;
-        if (seg == 0 || seg == 2) {  // shared experts: up tiles first, then down tiles
-          int tt;
-          td = shared_tile(d, seg == 0 ? tile : n_sh_up + tile - seg_end[1], &need, &tt);
-          if (seg == 2) {
-            flag = shc + 1 + ((td.x & (kDownBit - 1)) - d.E) * nt_max + tt;
-            kind = 2;
-          }
-        } else {
-          const int q = seg == 1 ? tile - seg_end[0] : n_up + tile - seg_end[2];
-          if (!locate(d, s_list, s_offs, q, n_up, &td, &need)) {
-            set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-            *abort_flag = 1;
-            ok = false;
-            break;
-          }
-          if (seg == 1) {
-            flag = ws.tile_ctr + 2;
-            need = copied;
-          } else {
-            flag = ws.done_up + (td.x & (kDownBit - 1));
-            kind = 1;
-          }
+        int need = 0;
+        if (!locate(d, s_list, s_offs, q, n_up, &td, &need)) {
+          set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+          *abort_flag = 1;
+          ok = false;
+          break;
         }
-        ok = post(td) && issue(td, flag, need, kind);
+        // routed up tiles: the rows are in xp; down tiles: wait for their group's up tiles
+        const int32_t *flag = q < n_up ? nullptr : ws.done_up + (td.x & (kDownBit - 1));
+        ok = post(td) && issue(td, flag, need, 1);
       }
       if (ok) ok = post(make_int4(-1, 0, 0, 0));  // end of the stream
       if (!ok) {
@@ -841,9 +838,6 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
     }
     __syncwarp();
   } else if (wid >= 2) {
-    // ---------------- worklist bookkeeping of this CTA (for the combine)
-    wl_bookkeeping(d, ws, wsm, s_offs, wl, blockIdx.x, gridDim.x, epi, trace_wl);
-    if (trace_wl && threadIdx.x == 64) trace_wl[3] = static_cast<int64_t>(globaltimer_ns());
     // ---------------- epilogue (warps 2..5; warp w reads TMEM lanes 32*(w%4)..)
     const int q = wid & 3;
     uint8_t *stg = stage_out + (wid - 2) * kExpStg;
@@ -1066,7 +1060,7 @@ static GateGeom gate_geom_for(const Dims &d, int tn) {
   g.region0 = g.stages * stage > partial ? g.stages * stage : partial;
   const int rows = (tn / g.cs) * e_pad * 4;
   g.smem = 1024 + g.region0 + rows + e_pad * 4 + 1024 + (2 * g.stages + 1) * 8 + 16 + 2 * 64 * 4 +
-           (kGateThreads / 32) * 32 * 8;
+           (kGateThreads / 32) * 32 * 8 + 8 + 8 + 64 + 64 * 16 * 2 + 2 * 1024 * 2;
   const int cols = (e_pad / BM - 1) * tn + ((tn + 31) / 32) * 32;
   g.tcols = cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512;
   if (cols > 512) g.smem = kGateSmemCap + 1;  // does not fit: rejected by the caller
@@ -1142,6 +1136,13 @@ static GateGeom gate_geom(const Dims &d) {
   return g;
 }
 
+bool gate_builds_worklist(const Dims &d) {
+  const GateGeom g = gate_geom(d);
+  const int tiles = (d.n_pos + g.tn - 1) / g.tn, tpc = g.tn / g.cs;
+  return g.smem <= kGateSmemCap && g.region0 >= gate_tail_bytes(d, tpc) && tpc <= 64 && d.k <= 16 &&
+         d.E <= 1024 && tiles <= gate_max_clusters(d, g.cs);
+}
+
 bool gate_tc_supported(const Dims &d) {
   Dims dd = d;
   dd.n_pos = d.Nmax;
@@ -1162,6 +1163,7 @@ cudaError_t launch_gate_tc(const Dims &d, const Maps &m, const Work &ws, const v
   p.bias = bias;
   p.live = live;
   p.decoded = decoded;
+  p.xv = static_cast<const uint4 *>(x);
   p.cs = g.cs;
   p.tn = g.tn;
   p.tcols = g.tcols;
@@ -1174,7 +1176,7 @@ cudaError_t launch_gate_tc(const Dims &d, const Maps &m, const Work &ws, const v
 }
 
 cudaError_t launch_experts_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map_up,
-                              const void *x, cudaStream_t s) {
+                              cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k_tc_experts, cudaFuncAttributeMaxDynamicSharedMemorySize, kExpSmem);
@@ -1190,8 +1192,6 @@ cudaError_t launch_experts_tc(const Dims &d, const Maps &m, const Work &ws, cons
     p.b[i] = m.xp[i];
     p.b2[i] = m.a_int[i];
   }
-  p.x = static_cast<const uint4 *>(x);
-  p.vec_per_row = d.H * 2 / 16;
   p.bs = x_map_up;
   p.bs2 = m.a_sh;
   // Down tiles wait for up tiles of other CTAs, but never for a CTA that has

@@ -36,6 +36,12 @@ struct Work {
   int32_t *plan_counts;   // [R][E] block-start hit counts (per request)
   int32_t *req_ids;       // [R][E] per-request supports: ranked experts of each request
   int32_t *req_len;       // [R] and each request's |S|
+  // Expert Atlas planner
+  int32_t *atlas_cand;    // [Nmax][32] candidate experts of each token
+  float *atlas_w;         // [Nmax][32] their dense router probabilities
+  float *atlas_r;         // [Nmax] coverage floors
+  unsigned long long *atlas_pop;  // [E] popularity, fixed point
+  int32_t *atlas_out;     // [4] covered_ok, under-covered tokens, repair rounds
   void *cache;            // [Nmax][H] routed-output cache, layer dtype
   // one iteration
   float *logits;          // [Nmax][E] G = x W_r^T + b (gate kernel)
@@ -50,12 +56,17 @@ struct Work {
   int32_t *grp_list;      // [E + n_sh + 1] expert-kernel groups in list order: token tiles of the
                           // groups before << kGrpIdBits | group (shared experts E..E+n_sh-1)
   int32_t *done_up;       // [E + n_sh] up tiles of each group finished this iteration (by group id)
-  int32_t *cov_under;     // [2 (call parity)] fresh positions under the coverage floor
-  int32_t *tile_ctr;      // routed tiles: [0] next tile of the expert kernel (dynamic scheduling),
-                          // [2] 16-byte vectors of worklist rows copied into xp (both reset by the
+  int32_t *cov_under;     // [1] fresh positions of this call under the coverage floor (zeroed by the
+                          // worklist bookkeeping once read)
+  int32_t *tile_ctr;      // [0] next tile of the expert kernel (dynamic scheduling; reset by the
                           // classifying kernel of the iteration)
-  int32_t *sh_ctr;        // shared-expert tiles, [2 (call parity)][sh_stride]: [0] next tile, then the
-                          // finished up tiles of each (shared expert, token tile)
+  int32_t *tally;         // [8] the gate tail's per-iteration counts (categories, bad flags, fresh),
+                          // added by every gate CTA, read and zeroed by CTA 0
+  int32_t *gate_arrive;   // grid barrier of the gate before the worklist: [0] CTAs arrived (zeroed by
+                          // CTA 0 once it has passed), [1] generation (advanced by the last to arrive)
+  int32_t *sh_ctr;        // shared-expert tiles, [sh_stride]: [0] next tile, then the finished up
+                          // tiles of each (shared expert, token tile); zeroed by each call's combine
+                          // for the next call
   int32_t *wl_pos;        // [Nmax*k] expert-sorted worklist positions
   int32_t *slot;          // [Nmax][k] worklist row of selection (t, j)
   void *xp;               // [Nmax*k][H] token rows of the worklist (x at wl_pos), expert-sorted
@@ -70,7 +81,6 @@ struct Work {
   uint8_t *pk_d;          // routed W_down: [E*H/256][I/64] x (two 128-row tiles) = 32 KB
   uint8_t *pk_sgu;        // shared W_gate/W_up: [n_sh*I_s/128][H/64] x 32 KB
   uint8_t *pk_sd;         // shared W_down: [n_sh*H/256][I_s/64] x 32 KB
-  unsigned int *route_done;  // sequence number of the last call whose expert offsets and group list are out
   int64_t *trace;         // [kTraceRows][kTraceCtas][8] per-CTA timeline (when tracing)
   unsigned long long *timeline;  // [2][K_NUM]: first CTA entry, last CTA exit per kernel kind (ns)
   Ctrl *ctrl;
@@ -108,7 +118,8 @@ struct Dims {
   int32_t cov_check;     // support-coverage check: fresh positions with less than cov_alpha of their
   float cov_alpha, cov_q;  // dense selection's mass on the support; more than (1 - cov_q) |F| of them
                            // make the next iteration full fresh
-  uint32_t seq;          // sequence number of this call (route_done handshake)
+  int32_t wl_in_gate;    // 1: the gate kernel builds the worklist in its tail (bf16 layers whose gate
+                         // grid is one wave); 0: the worklist kernel builds it
   int64_t timeout_ns;
   epoch_iter_stats *stats_out;  // caller's copy of this iteration's statistics (nullable)
 };
@@ -131,6 +142,12 @@ struct Maps {
 // Token-box heights of the routed B operands; a tile loads the smallest box
 // that holds its valid rows.
 constexpr int kBoxRows[4] = {32, 64, 128, 256};
+
+// Parameters of the Expert Atlas planner (see epoch_layer_config).
+struct AtlasParams {
+  int32_t m, B, c;
+  double alpha, q, beta;
+};
 
 // Kernel kinds, for profiling and launch counting.
 enum Kind {
@@ -176,10 +193,14 @@ cudaError_t launch_plan_topk(const Dims &d, const Weights &w, const Work &ws, cu
 // per-request thresholds come from tau on the device.
 cudaError_t launch_plan_support(const Dims &d, const Work &ws, int32_t threshold, int all_experts,
                                 int clear_state, int32_t *ids_out, int32_t *len_out, double tau, cudaStream_t s);
-// The worklist kernel of fp32 layers (bf16 layers build it in the expert kernel).
-cudaError_t launch_route(const Dims &d, const Work &ws, cudaStream_t s);
-// CTAs that build the worklist: the worklist kernel's grid (fp32 layers) and
-// the expert kernel's (bf16 layers) are both one CTA per SM.
+// The worklist kernel: expert offsets, group list, bookkeeping for the combine
+// and, for bf16 layers (x non-null), the token rows of the worklist copied into
+// xp. Used where the gate does not build the worklist itself.
+cudaError_t launch_route(const Dims &d, const Work &ws, const void *x, cudaStream_t s);
+// Expert Atlas planner over ws.logits (candidates, then the one-CTA planner).
+cudaError_t launch_atlas(const Dims &d, const Work &ws, const AtlasParams &a, int clear_state, int32_t *ids_out,
+                         int32_t *len_out, cudaStream_t s);
+// CTAs of the worklist kernel: one per SM.
 int route_ctas();
 cudaError_t launch_combine(const Dims &d, const Work &ws, const void *x, void *y, int bf16, cudaStream_t s);
 cudaError_t launch_wait_test(uint32_t *err, int64_t timeout_ns, cudaStream_t s);
@@ -197,18 +218,23 @@ bool tma_encode_init();
 bool encode_kmajor_bf16(CUtensorMap *map, const void *base, uint64_t k_elems, uint64_t rows, uint32_t box_rows);
 constexpr int kTnUp = 128;    // expert-kernel token tiles (up and down)
 constexpr int kTnDn = 128;
-// Entries per call parity of Work::sh_ctr.
+// Entries of Work::sh_ctr.
 __host__ __device__ inline int sh_stride(const Dims &d) { return 1 + d.n_sh * ((d.Nmax + kTnUp - 1) / kTnUp); }
 constexpr int kBmDn = 256;    // rows of H per down tile (two 128-row MMAs)
 constexpr int kGrpIdBits = 11;  // group id field of a grp_list entry (E + n_sh <= 1024 < 2^11)
+
 cudaError_t launch_gate_tc(const Dims &d, const Maps &m, const Work &ws, const void *x, const float *bias,
                            const uint8_t *live, const uint8_t *decoded, cudaStream_t s);
-// x_map_up: x with boxes of kTnUp rows (shared-expert up tiles); x: the same
-// rows, which the kernel copies into the compact worklist rows xp.
+// x_map_up: x with boxes of kTnUp rows (shared-expert up tiles). The worklist
+// (offsets, group list, xp rows) is complete when the kernel before it in the
+// stream has completed.
 cudaError_t launch_experts_tc(const Dims &d, const Maps &m, const Work &ws, const CUtensorMap &x_map_up,
-                              const void *x, cudaStream_t s);
+                              cudaStream_t s);
 // Checks that the gate's thread-block clusters can be scheduled on this device.
 bool gate_tc_supported(const Dims &d);
+// True when the gate grid of d.n_pos positions is resident all at once (one
+// wave of clusters), which its in-kernel grid barrier before the worklist needs.
+bool gate_builds_worklist(const Dims &d);
 
 int num_sms();
 

@@ -1,6 +1,7 @@
-// Routing side of the Epoch MoE-layer iteration (sm_103a): block plan,
-// liveness classification and compaction, support-restricted top-k, the
-// expert-sorted worklist, the permute into compact rows, and the weighted
+// Routing side of the Epoch MoE-layer iteration (sm_103a): block plan (hit-
+// count prefix and Expert Atlas planners), liveness classification and
+// compaction, support-restricted top-k (fp32 layers; bf16 layers take it in
+// the gate's epilogue), the worklist kernel (worklist.cuh), and the weighted
 // combine with the routed-output cache.
 //
 // Source: walk-through page "Epoch 完全拆解:把扩散块编译成稀疏 MoE 服务单元" ([W]):
@@ -26,6 +27,26 @@ const char *const kKindName[K_NUM] = {"gate",        "plan_topk", "plan_support"
                                       "expert_down", "combine",   "wait_test",    "select"};
 
 // ---------------------------------------------------------------- helpers
+
+// A block plan's reset of the iteration state (all threads of one CTA): both
+// halves of the stamps, decoded flags and selection words, and the arrival
+// count of the gate's grid barrier, the gate tail's tallies and the shared-
+// expert tile counters (left over only by a timed-out call). Every iteration
+// of the block that follows starts from this state, whatever calls ran before
+// it.
+__device__ void clear_block_state(const Dims &d, const Work &ws) {
+  for (int t = threadIdx.x; t < 2 * d.Nmax; t += blockDim.x) {
+    ws.stamp[t] = -1;
+    ws.prev_dec[t] = 0;
+  }
+  for (int q = threadIdx.x; q < 2 * d.E * d.cmax; q += blockDim.x) ws.sel_words[q] = 0u;
+  if (threadIdx.x == 0) {
+    ws.gate_arrive[0] = 0;
+    *ws.cov_under = 0;
+  }
+  if (threadIdx.x < 8) ws.tally[threadIdx.x] = 0;
+  for (int q = threadIdx.x; q < sh_stride(d); q += blockDim.x) ws.sh_ctr[q] = 0;
+}
 
 // ---------------------------------------------------------------- gate (SIMT)
 // G = x W_r^T + b for fp32 layers: one warp per (position, expert), lanes
@@ -151,12 +172,7 @@ __global__ void __launch_bounds__(1024) k_plan_support(Dims d, Work ws, int32_t 
     }
     if (clear_state && r == 0) ws.ctrl->short_next = 0;  // a new block starts without a coverage shortfall
   }
-  if (clear_state && r == 0) {
-    for (int t = tid; t < 2 * d.Nmax; t += blockDim.x) {  // both halves of the iteration state
-      ws.stamp[t] = -1;
-      ws.prev_dec[t] = 0;
-    }
-  }
+  if (clear_state && r == 0) clear_block_state(d, ws);
 }
 
 // Per-request supports: the union of the requests' supports (their masks,
@@ -203,6 +219,185 @@ __global__ void __launch_bounds__(1024) k_plan_union(Dims d, Work ws, int32_t *i
   }
 }
 
+// ---------------------------------------------------------------- Expert Atlas planner
+// The planner of [W] section "Expert Atlas" (softmax router, one support per
+// call): extended candidates, popularity, greedy repair of under-covered
+// tokens. Float sums that decide an ordering (popularity, the repair gain G_e)
+// are accumulated as 64-bit fixed point (2^40 per unit of routing mass), so
+// that the order of the atomic additions cannot change them; per-token sums
+// run in candidate order in float.
+constexpr int kAtlasK = 32;  // candidates per token at most (k + m)
+constexpr double kAtlasFix = 1099511627776.0;  // 2^40
+
+// One warp per position: its K = min(k + m, E) best experts by logit (lower id
+// first), their dense router probabilities W (softmax over all experts), the
+// coverage floor r = alpha * (mass of the first k), and the popularity sums
+// p_e += W over the candidate edges.
+template <int EPL>
+__global__ void k_atlas_cand(Dims d, Work ws, int K, float alpha) {
+  __shared__ uint2 s_scr[8][32];
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int lane = lane_id();
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < d.n_pos; t += warps) {
+    float v[EPL];
+    bool ok[EPL];
+    lane_logits<EPL>(ws.logits + static_cast<size_t>(t) * d.E, d.E, v);
+#pragma unroll
+    for (int c = 0; c < EPL; ++c) ok[c] = lane * EPL + c < d.E;
+    int sel;
+    float val;
+    warp_topk<EPL>(v, ok, K, &sel, &val, s_scr[warp_id()]);
+    float m = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < EPL; ++c) m = fmaxf(m, v[c]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float sum = 0.f;
+#pragma unroll
+    for (int c = 0; c < EPL; ++c) sum += lane * EPL + c < d.E ? expf(v[c] - m) : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float w = (lane < K && sel >= 0) ? expf(val - m) / sum : 0.f;
+    float topk = 0.f;
+    for (int j = 0; j < d.k; ++j) topk += __shfl_sync(0xffffffffu, w, j);
+    if (lane < K) {
+      ws.atlas_cand[static_cast<size_t>(t) * kAtlasK + lane] = sel;
+      ws.atlas_w[static_cast<size_t>(t) * kAtlasK + lane] = w;
+      if (sel >= 0) atomicAdd(ws.atlas_pop + sel, static_cast<unsigned long long>(llrint(static_cast<double>(w) * kAtlasFix)));
+    }
+    if (lane == 0) ws.atlas_r[t] = alpha * topk;
+  }
+}
+
+// One CTA: the initial support (the max(B, k) most popular experts, lower id
+// first on equal popularity), then repair rounds while more than (1 - q) N
+// tokens are under-covered (C_t < r_t): for every expert outside the support,
+// G_e = sum over under-covered t and their candidate edges to e of
+// min(W, r_t - C_t) and H_e = the under-covered t with C_t + W >= r_t; the at
+// most c experts of largest positive H_e + beta G_e (lower id first) join; a
+// round with no positive score ends the search. support_ids gets the support
+// in entry order, then the other experts in id order.
+__global__ void __launch_bounds__(1024) k_atlas_plan(Dims d, Work ws, int K, int B, int c, double q, double beta,
+                                                     int clear_state, int32_t *ids_out, int32_t *len_out) {
+  const KernelMark mark_(d, ws, K_PLAN_SUPPORT);
+  __shared__ unsigned long long s_fix[1024];  // popularity, then G_e of a round
+  __shared__ int32_t s_h[1024];
+  __shared__ uint8_t s_in[1024];
+  __shared__ double s_score[1024];            // repair scores of a round (-1: not a candidate)
+  __shared__ int32_t s_len, s_rounds;
+  const int tid = threadIdx.x, E = d.E, N = d.n_pos;
+  if (tid < E) s_fix[tid] = ws.atlas_pop[tid];
+  if (tid == 0) {
+    s_len = min(max(B, d.k), E);
+    s_rounds = 0;
+  }
+  __syncthreads();
+  const int n_init = s_len;
+  if (tid < E) {
+    const unsigned long long p = s_fix[tid];
+    int rank = 0;
+    for (int e = 0; e < E; ++e) rank += (s_fix[e] > p) || (s_fix[e] == p && e < tid);
+    s_in[tid] = rank < n_init ? 1 : 0;
+    if (rank < n_init) ws.support_ids[rank] = tid;
+  }
+  __syncthreads();
+  __shared__ int32_t s_warp[32];
+  // per-block sum of one int per thread
+  auto block_sum = [&](int v) {
+    v = __reduce_add_sync(0xffffffffu, v);
+    if (lane_id() == 0) s_warp[warp_id()] = v;
+    __syncthreads();
+    int tot = 0;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) tot += s_warp[w];
+    __syncthreads();
+    return tot;
+  };
+  auto coverage = [&](int t) {
+    const int32_t *ct = ws.atlas_cand + static_cast<size_t>(t) * kAtlasK;
+    const float *wt = ws.atlas_w + static_cast<size_t>(t) * kAtlasK;
+    float cov = 0.f;
+    for (int j = 0; j < K; ++j) {  // candidate order
+      const int e = ct[j];
+      if (e >= 0 && e < E && s_in[e]) cov += wt[j];
+    }
+    return cov;
+  };
+  int n_under = 0;
+  for (int round = 0; round <= E; ++round) {
+    int under = 0;
+    for (int t = tid; t < N; t += blockDim.x) under += coverage(t) < ws.atlas_r[t] ? 1 : 0;
+    n_under = block_sum(under);
+    if (!(static_cast<double>(n_under) > (1.0 - q) * N)) break;
+    // gains of the experts outside the support over the under-covered tokens
+    if (tid < E) {
+      s_fix[tid] = 0ull;
+      s_h[tid] = 0;
+    }
+    __syncthreads();
+    for (int t = tid; t < N; t += blockDim.x) {
+      const float cov = coverage(t), r = ws.atlas_r[t];
+      if (!(cov < r)) continue;
+      const int32_t *ct = ws.atlas_cand + static_cast<size_t>(t) * kAtlasK;
+      const float *wt = ws.atlas_w + static_cast<size_t>(t) * kAtlasK;
+      for (int j = 0; j < K; ++j) {
+        const int e = ct[j];
+        if (e < 0 || e >= E || s_in[e]) continue;
+        const float w = wt[j];
+        atomicAdd(s_fix + e, static_cast<unsigned long long>(llrint(static_cast<double>(fminf(w, r - cov)) * kAtlasFix)));
+        if (cov + w >= r) atomicAdd(s_h + e, 1);
+      }
+    }
+    __syncthreads();
+    // the at most c experts of largest positive score join (lower id first on equal scores)
+    double score = 0.0;
+    bool posv = false;
+    if (tid < E && !s_in[tid]) {
+      score = static_cast<double>(s_h[tid]) + beta * (static_cast<double>(s_fix[tid]) / kAtlasFix);
+      posv = score > 0.0;
+    }
+    const int n_pos_scores = block_sum(posv ? 1 : 0);
+    if (n_pos_scores == 0) break;
+    if (tid < E) s_score[tid] = posv ? score : -1.0;
+    __syncthreads();
+    const int base = s_len;
+    if (posv) {
+      int rank = 0;
+      for (int e = 0; e < E; ++e) rank += (s_score[e] > score) || (s_score[e] == score && e < tid);
+      if (rank < c) ws.support_ids[base + rank] = tid;
+    }
+    __syncthreads();
+    const int n_add = min(c, n_pos_scores);
+    if (tid < n_add) s_in[ws.support_ids[base + tid]] = 1;
+    if (tid == 0) {
+      s_len = base + n_add;
+      s_rounds = round + 1;
+    }
+    __syncthreads();
+  }
+  // support in entry order, then the other experts in id order; the mask
+  const int len = s_len;
+  if (tid < E) {
+    ws.support_mask[tid] = s_in[tid];
+    if (!s_in[tid]) {
+      int before = 0;
+      for (int e = 0; e < tid; ++e) before += s_in[e] ? 0 : 1;
+      ws.support_ids[len + before] = tid;
+    }
+  }
+  __syncthreads();
+  if (ids_out)
+    for (int e = tid; e < E; e += blockDim.x) ids_out[e] = ws.support_ids[e];
+  if (tid == 0) {
+    ws.ctrl->support_len = len;
+    if (len_out) *len_out = len;
+    ws.atlas_out[0] = static_cast<double>(n_under) > (1.0 - q) * N ? 0 : 1;  // covered_ok
+    ws.atlas_out[1] = n_under;
+    ws.atlas_out[2] = s_rounds;
+    if (clear_state) ws.ctrl->short_next = 0;
+  }
+  if (clear_state) clear_block_state(d, ws);
+}
+
 // ---------------------------------------------------------------- select (fp32 layers)
 // Classification and support-restricted top-k of every position from the
 // logits of the FFMA gate (the tcgen05 gate of bf16 layers does the same in its
@@ -236,19 +431,22 @@ __global__ void __launch_bounds__(256) k_select(Dims d, Work ws, const uint8_t *
 }
 
 // ---------------------------------------------------------------- worklist
-// The worklist kernel of fp32 layers (bf16 layers build the worklist inside
-// the tcgen05 expert kernel): every CTA runs both phases of worklist.cuh with
-// all its threads. No row copy: the FFMA experts read x through wl_pos.
-__global__ void __launch_bounds__(kRouteThreads) k_route(Dims d, Work ws) {
+// The worklist kernel, where the gate does not build the worklist in its own
+// tail (fp32 layers, gates of more than one wave, the hot-update path): every
+// CTA runs the phases of worklist.cuh with all its threads. xv: x as 16-byte
+// vectors, whose worklist rows the CTAs copy into xp for the tcgen05 expert
+// kernel (bf16 layers); null for fp32 layers, whose FFMA experts read x
+// through wl_pos.
+__global__ void __launch_bounds__(kRouteThreads) k_route(Dims d, Work ws, const uint4 *xv) {
   const KernelMark mark_(d, ws, K_ROUTING);
   pdl_trigger();
   __shared__ WlSmem sm;
   __shared__ int32_t s_off[1025];
   const Group g{static_cast<int>(threadIdx.x), kRouteThreads, 0};
   wl_prepare(d, ws, sm, s_off, g);
-  pdl_wait();  // the select kernel has finished: selection words, selections, codes, anomaly flag
+  pdl_wait();  // the kernel before has finished: selection words, selections, codes, anomaly flag
   const WlPlan pl = wl_phase_a(d, ws, sm, s_off, nullptr, blockIdx.x == 0, g);
-  wl_rows(d, ws, sm, s_off, pl, nullptr, 0, blockIdx.x, gridDim.x, g);
+  wl_rows(d, ws, sm, s_off, pl, xv, xv ? d.H * 2 / 16 : 0, blockIdx.x, gridDim.x, g);
   wl_bookkeeping(d, ws, sm, s_off, pl, blockIdx.x, gridDim.x, g, nullptr);
 }
 
@@ -322,10 +520,12 @@ __global__ void __launch_bounds__(128, 7) k_combine(Dims d, Work ws, const T *__
   __shared__ float w_s[16];
   __shared__ int f_s;
   // Every kernel of the iteration before this one has completed: the expert
-  // outputs, and the worklist bookkeeping (built inside the tcgen05 expert
-  // kernel, or by the worklist kernel before the FFMA experts). A hardware
-  // wait: no thread of this grid polls memory while the experts stream.
+  // outputs, and the worklist bookkeeping (the gate's tail or the worklist
+  // kernel, both before the experts). A hardware wait: no thread of this grid
+  // polls memory while the experts stream.
   pdl_wait();
+  if (blockIdx.x == 0)  // the next call's expert kernel takes shared-expert tiles from its launch
+    for (int q = threadIdx.x; q < sh_stride(d); q += blockDim.x) ws.sh_ctr[q] = 0;
   if (t < d.n_pos) {
     if (threadIdx.x < k) {
       slot_s[threadIdx.x] = ws.slot[static_cast<size_t>(t) * k + threadIdx.x];
@@ -550,6 +750,30 @@ cudaError_t launch_plan_support(const Dims &d, const Work &ws, int32_t threshold
   return cudaGetLastError();
 }
 
+cudaError_t launch_atlas(const Dims &d, const Work &ws, const AtlasParams &a, int clear_state, int32_t *ids_out,
+                         int32_t *len_out, cudaStream_t s) {
+  const int K = min(d.k + a.m, d.E);
+  if (K > kAtlasK) return cudaErrorInvalidValue;
+  cudaError_t e = cudaMemsetAsync(ws.atlas_pop, 0, sizeof(unsigned long long) * d.E, s);
+  if (e != cudaSuccess) return e;
+  const int blocks = (d.n_pos + 7) / 8;
+  const float alpha = static_cast<float>(a.alpha);
+  switch (epl_for(d.E)) {
+#define EPOCH_CASE(N)                                                   \
+  case N:                                                               \
+    k_atlas_cand<N><<<blocks, 256, 0, s>>>(d, ws, K, alpha);            \
+    break;
+    EPOCH_CASE(1) EPOCH_CASE(2) EPOCH_CASE(4) EPOCH_CASE(8) EPOCH_CASE(16) EPOCH_CASE(32)
+#undef EPOCH_CASE
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  static bool carve_ = (prefer_max_shared(k_atlas_plan) == cudaSuccess);
+  (void)carve_;
+  k_atlas_plan<<<1, 1024, 0, s>>>(d, ws, K, a.B, a.c, a.q, a.beta, clear_state, ids_out, len_out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_select(const Dims &d, const Work &ws, const uint8_t *live, const uint8_t *decoded,
                           const float *bias, cudaStream_t s) {
   int blocks = (d.n_pos + 7) / 8;
@@ -571,14 +795,15 @@ cudaError_t launch_select(const Dims &d, const Work &ws, const uint8_t *live, co
 int route_ctas() { return num_sms(); }
 
 // One CTA per SM, launched programmatically: the CTAs become resident while
-// the select kernel runs and wait for it (pdl_wait) before reading.
-cudaError_t launch_route(const Dims &d, const Work &ws, cudaStream_t s) {
+// the kernel before runs and wait for it (pdl_wait) before reading.
+cudaError_t launch_route(const Dims &d, const Work &ws, const void *x, cudaStream_t s) {
   if (d.E > 8 * kRouteThreads) return cudaErrorInvalidConfiguration;
   static bool c_ = (prefer_max_shared(k_route) == cudaSuccess);
   if (!c_) return cudaErrorInvalidConfiguration;
   Dims dd = d;
   Work ww = ws;
-  void *args[] = {&dd, &ww};
+  const uint4 *xv = static_cast<const uint4 *>(x);
+  void *args[] = {&dd, &ww, &xv};
   return launch_kernel(reinterpret_cast<void *>(k_route), dim3(route_ctas()), dim3(kRouteThreads), 0, s, args,
                        true);
 }

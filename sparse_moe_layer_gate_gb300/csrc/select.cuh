@@ -105,7 +105,8 @@ __device__ __forceinline__ int shortfall_flag(const Dims &d, const Work &ws) {
 // first; weights = softmax over the k selected logits, summed in selection
 // order. Lane l holds the logits v of experts [l*EPL, l*EPL + EPL); `scratch`
 // is the warp's 32 entries of shared memory for the top-k. Writes sel/selw of
-// t and sets bit t of the selected experts' words in `words`.
+// t and sets bit t of the selected experts' words in `words`; sel_out
+// (nullable, shared memory) gets the k selected experts as well.
 //
 // Group-limited sigmoid router (d.router == 1; v holds x W_r^T without the
 // bias): scores s = sigmoid(v), selection scores c = s + bias, the group rule
@@ -119,7 +120,7 @@ __device__ __forceinline__ int shortfall_flag(const Dims &d, const Work &ws) {
 template <int EPL>
 __device__ __forceinline__ void select_position(const Dims &d, const Work &ws, int t, const float (&v)[EPL],
                                                 const uint8_t *support_mask, bool force, uint32_t *words,
-                                                uint2 *scratch, const float *bias) {
+                                                uint2 *scratch, const float *bias, int16_t *sel_out = nullptr) {
   const int lane = lane_id(), e0 = lane * EPL, k = d.k;
   bool ok[EPL];
 #pragma unroll
@@ -178,6 +179,7 @@ __device__ __forceinline__ void select_position(const Dims &d, const Work &ws, i
     } else {
       ws.sel[static_cast<size_t>(t) * k + lane] = sel;
       ws.selw[static_cast<size_t>(t) * k + lane] = wgt;
+      if (sel_out) sel_out[lane] = static_cast<int16_t>(sel);
       atomicOr(&words[static_cast<size_t>(sel) * d.cmax + (t >> 5)], 1u << (t & 31));
     }
   }
@@ -224,15 +226,17 @@ __device__ __forceinline__ void select_position(const Dims &d, const Work &ws, i
       mass += sj;
       if (ej >= 0 && support_mask[ej]) covered += sj;
     }
-    if (lane == 0 && covered < d.cov_alpha * mass) atomicAdd(&ws.cov_under[d.seq & 1], 1);
+    if (lane == 0 && covered < d.cov_alpha * mass) atomicAdd(ws.cov_under, 1);
   }
 }
 
 // Per-iteration handshake state, set by block 0 of the kernel that classifies
 // the positions (the gate, or the select kernel) while no later kernel of the
-// iteration reads it yet: the anomaly flag, and the counters the worklist and
-// expert kernels advance (routed tiles drawn, xp vectors copied, up tiles
-// done per group). Their readers wait for this call's worklist first.
+// iteration reads it yet: the anomaly flag, and the counters the expert kernel
+// advances on the routed tiles (tiles drawn, up tiles done per group); it
+// reads them only once this call's worklist is complete. (The shared-expert
+// tile counters, which the expert kernel uses from its launch, are zeroed by
+// the combine kernel of the call before, and by a block plan.)
 // flags: bit 0 a decoded -> live anomaly, bit 1 the previous iteration's
 // coverage shortfall (both make the iteration full fresh).
 __device__ __forceinline__ void reset_iteration_state(const Dims &d, const Work &ws, int flags) {
@@ -240,7 +244,6 @@ __device__ __forceinline__ void reset_iteration_state(const Dims &d, const Work 
   if (threadIdx.x == 0) {
     ws.ctrl->anom = flags;
     ws.tile_ctr[0] = 0;
-    ws.tile_ctr[2] = 0;
   }
 }
 

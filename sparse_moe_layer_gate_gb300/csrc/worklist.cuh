@@ -1,5 +1,8 @@
-// The expert-sorted worklist of one iteration, built by every CTA of a grid
-// from the selection words of the classifying kernel (gate or select).
+// The expert-sorted worklist of one iteration, built by every CTA of the
+// worklist kernel from the selection words of the classifying kernel (gate or
+// select kernel), where the gate does not build it in its own tail
+// (gate_tail.cuh): fp32 layers, gates of more than one wave, the hot-update
+// path.
 //
 // Walk-through page "Epoch 完全拆解:把扩散块编译成稀疏 MoE 服务单元", section
 // "FreshLane Dispatch": pack the fresh token-expert pairs, exchange per-expert
@@ -10,21 +13,21 @@
 // into the compact buffer xp.
 //
 // Every CTA derives the same expert offsets on its own (one round of loads,
-// then shared-memory work), so no CTA waits for another before it can decode
-// its expert tiles. The work comes in two phases, each run by a group of the
-// CTA's threads:
+// then shared-memory work), so no CTA waits for another. The work comes in two
+// phases:
 //  A rows per candidate expert (the support, or every expert on a fallback),
 //    the expert offsets (a scan over expert ids) and the group list of the
 //    expert kernel (experts by row-count class, with token-tile prefixes); CTA
-//    0 also writes them to global memory (for the combine and the statistics);
-//  B the CTA's share of the worklist rows (position of each row, its row of x
-//    copied into xp, counted in tile_ctr[2] for the expert kernel's routed up
-//    tiles); then, off the critical path, its share of the positions' fresh
-//    index, fresh list and selection slots, the statistics (CTA 0), the state
-//    of positions beyond n_pos and the cleared words of the next iteration.
-// The counters advanced here and by the expert kernel (tile_ctr, done_up) were
-// reset, and the anomaly flag set, by block 0 of the classifying kernel, which
-// has completed before phase A reads anything.
+//    0 writes them to global memory;
+//  B the CTA's share of the worklist rows (position of each row and, for bf16
+//    layers, its row of x copied into xp); then its share of the positions'
+//    fresh index, fresh list and selection slots, the statistics (CTA 0), the
+//    state of positions beyond n_pos and the cleared words of the next
+//    iteration.
+// The tcgen05 expert kernel reads the finished worklist once this grid has
+// completed. The counters it advances (tile_ctr, done_up) were reset, and the
+// anomaly flag set, by block 0 of the classifying kernel before phase A reads
+// anything.
 #pragma once
 
 #include "common.cuh"
@@ -164,26 +167,34 @@ __device__ __forceinline__ WlPlan wl_phase_a(const Dims &d, const Work &ws, WlSm
   pl.staged = pl.n_cand * nch <= kWlStageWords;
   g.sync();
   for (int i = g.gtid; i < pl.n_cand; i += g.n) sm.cidx[sm.cand[i]] = static_cast<int16_t>(i);
-  // the candidates' words in one round of loads; rows per expert (the lanes
-  // of a warp that hold words of one candidate add their popcounts together)
-  const int total = pl.n_cand * nch;
+  // the candidates' words in one round of loads; rows per expert. Items are
+  // (candidate, block of 32 words); warp w takes items w, w + warps, ..., up to
+  // eight at a time, lane l loading word l of each, and adds the block's
+  // popcount to its candidate's row count.
   const int lane = lane_id();
-  for (int q0 = g.gtid - lane; q0 < total; q0 += g.n * 8) {  // the same trip count for every lane of a warp
+  const int nwb = (nch + 31) >> 5;
+  const int items = pl.n_cand * nwb;
+  const int wid = g.warp(), nw = g.warps();
+  for (int i0 = wid; i0 < items; i0 += nw * 8) {
     uint32_t v[8];
-    int ci[8];
 #pragma unroll
     for (int bb = 0; bb < 8; ++bb) {
-      const int q = q0 + bb * g.n + lane;
-      ci[bb] = q < total ? q / nch : -1;
-      v[bb] = ci[bb] >= 0 ? words[static_cast<size_t>(sm.cand[ci[bb]]) * cmax + (q - ci[bb] * nch)] : 0u;
+      const int it = i0 + bb * nw;
+      v[bb] = 0u;
+      if (it < items) {
+        const int ci = it / nwb, w = (it - ci * nwb) * 32 + lane;
+        if (w < nch) v[bb] = words[static_cast<size_t>(sm.cand[ci]) * cmax + w];
+      }
     }
 #pragma unroll
     for (int bb = 0; bb < 8; ++bb) {
-      const int q = q0 + bb * g.n + lane;
-      if (pl.staged && ci[bb] >= 0) sm.words[q] = v[bb];
-      const unsigned same = __match_any_sync(0xffffffffu, ci[bb]);
-      const int sum = __reduce_add_sync(same, __popc(v[bb]));
-      if (ci[bb] >= 0 && lane == __ffs(same) - 1 && sum) atomicAdd(&s_off[sm.cand[ci[bb]]], sum);
+      const int it = i0 + bb * nw;
+      if (it < items) {  // the same for every lane of the warp
+        const int ci = it / nwb, w = (it - ci * nwb) * 32 + lane;
+        if (pl.staged && w < nch) sm.words[ci * nch + w] = v[bb];
+        const int sum = __reduce_add_sync(0xffffffffu, __popc(v[bb]));
+        if (lane == 0 && sum) atomicAdd(&s_off[sm.cand[ci]], sum);
+      }
     }
   }
   g.sync();
@@ -265,9 +276,9 @@ __device__ __forceinline__ WlPlan wl_phase_a(const Dims &d, const Work &ws, WlSm
 }
 
 // Phase B, rows: CTA b of G's share of the worklist rows: the position of
-// each row (wl_pos) and, for bf16 layers, its row of x copied into xp, counted
-// in tile_ctr[2]. x: the layer input, vpr its 16-byte vectors per row (0: no
-// copy, as for the FFMA experts, which read x through wl_pos).
+// each row (wl_pos) and, for bf16 layers, its row of x copied into xp. x: the
+// layer input, vpr its 16-byte vectors per row (0: no copy, as for the FFMA
+// experts, which read x through wl_pos).
 __device__ __forceinline__ void wl_rows(const Dims &d, const Work &ws, WlSmem &sm, const int32_t *s_off,
                                      const WlPlan &pl, const uint4 *__restrict__ x, int vpr, int b, int G,
                                      const Group &g) {
@@ -322,10 +333,15 @@ __device__ __forceinline__ void wl_rows(const Dims &d, const Work &ws, WlSmem &s
           const int u = __shfl_up_sync(0xffffffffu, incl, o);
           if (lane >= o) incl += u;
         }
-        // j = words of this round whose running total is at or below the lane's rank
+        // j = words of this round whose running total is at or below the lane's
+        // rank (the totals ascend with the lane: a binary search over them)
         int j = 0;
-#pragma unroll 8
-        for (int q = 0; q < 32; ++q) j += (base + __shfl_sync(0xffffffffu, incl, q)) <= my_rank ? 1 : 0;
+#pragma unroll
+        for (int step = 16; step >= 1; step >>= 1) {
+          const int probe = __shfl_sync(0xffffffffu, incl, j + step - 1);
+          if (base + probe <= my_rank) j += step;
+        }
+        if (base + __shfl_sync(0xffffffffu, incl, 31) <= my_rank) j = 32;
         const int jj = j < 32 ? j : 31;
         const uint32_t vj = __shfl_sync(0xffffffffu, v, jj);
         const int exj = __shfl_sync(0xffffffffu, incl - cnt, jj);
@@ -343,26 +359,23 @@ __device__ __forceinline__ void wl_rows(const Dims &d, const Work &ws, WlSmem &s
     }
     if (vpr > 0) {
       g.sync();
+      // the chunk's rows, one per warp at a time, eight 16-byte vectors per lane in flight
       const int nrows = min(kWlChunk, r1 - c0);
-      for (int q0 = g.gtid; q0 < nrows * vpr; q0 += g.n * 8) {
-        uint4 buf[8];
+      for (int rr = g.warp(); rr < nrows; rr += g.warps()) {
+        const uint4 *src = x + static_cast<size_t>(sm.pos[rr]) * vpr;
+        uint4 *dst = xp + static_cast<size_t>(c0 + rr) * vpr;
+        for (int v0 = lane; v0 < vpr; v0 += 32 * 8) {
+          uint4 buf[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int q = q0 + u * g.n;
-          if (q < nrows * vpr) buf[u] = __ldg(x + static_cast<size_t>(sm.pos[q / vpr]) * vpr + q % vpr);
-        }
+          for (int u = 0; u < 8; ++u)
+            if (v0 + 32 * u < vpr) buf[u] = __ldg(src + v0 + 32 * u);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int q = q0 + u * g.n;
-          if (q < nrows * vpr) xp[static_cast<size_t>(c0 + q / vpr) * vpr + q % vpr] = buf[u];
+          for (int u = 0; u < 8; ++u)
+            if (v0 + 32 * u < vpr) dst[v0 + 32 * u] = buf[u];
         }
       }
       g.sync();
     }
-  }
-  if (g.gtid == 0 && vpr > 0 && r1 > r0) {
-    __threadfence();
-    atomicAdd(ws.tile_ctr + 2, (r1 - r0) * vpr);
   }
 }
 
@@ -477,18 +490,15 @@ __device__ __forceinline__ void wl_bookkeeping(const Dims &d, const Work &ws, Wl
       st->tiles_up = (d.tn > 0 ? (d.I / 128) * pl.n_tiles : 0) + (d.I_s / 128) * nt_sh;
       st->tiles_down = (d.tn > 0 ? (d.H / kBmDn) * pl.n_tiles : 0) + (d.H / kBmDn) * nt_sh;
       // support coverage of this iteration's fresh positions -> the next iteration
-      const int under = d.cov_check ? ws.cov_under[d.seq & 1] : 0;
-      ws.cov_under[(d.seq + 1u) & 1u] = 0;
+      // (every selection of the call has counted itself; the count restarts for the next call)
+      const int under = d.cov_check ? *ws.cov_under : 0;
+      *ws.cov_under = 0;
       ws.ctrl->short_next = (d.cov_check && static_cast<float>(under) > (1.f - d.cov_q) * static_cast<float>(n_fresh))
                                 ? 1 : 0;
       st->n_under = under;
       if (sm.cat[5]) set_error(ws.err, EPOCH_DEVERR_FLAGS);
       if (d.stats_out) *d.stats_out = *st;
     }
-    // the shared-expert tile counters of the next iteration start at zero
-    const int nxt = static_cast<int>((d.seq + 1u) & 1u);
-    int32_t *sh = ws.sh_ctr + static_cast<size_t>(nxt) * sh_stride(d);
-    for (int q = g.gtid; q < sh_stride(d); q += g.n) sh[q] = 0;
     if (trace) trace[7] = static_cast<int64_t>(globaltimer_ns());
   }
   // positions beyond this call's n_pos keep their state; the words of the next

@@ -32,7 +32,8 @@ class EpochLayer:
     """One routed-expert MoE layer with its block plan and routed-output cache.
 
     coverage: (alpha, q) turns on the per-iteration support-coverage check
-    (see epoch_layer_config); None leaves it off.
+    (see epoch_layer_config); None leaves it off. atlas: dict of m, B, alpha,
+    q, beta, c selects the Expert Atlas planner; None the hit-count prefix.
 
     weights: dict of CUDA tensors -- w_router [E,H], b_router [E] float32,
     w_gate/w_up [E,I,H], w_down [E,H,I], and when n_shared > 0 ws_gate/ws_up
@@ -43,7 +44,7 @@ class EpochLayer:
                  dtype: str, tau: float, refresh_R: Optional[int], weights: Dict[str, torch.Tensor],
                  n_shared: int = 0, shared_inter: Optional[int] = None, residual: bool = False,
                  router: str = "softmax", n_group: int = 1, topk_group: int = 1, raw_weights: bool = False,
-                 coverage: Optional[tuple] = None, request_size: int = 0):
+                 coverage: Optional[tuple] = None, request_size: int = 0, atlas: Optional[dict] = None):
         self.dtype = dtype
         self.hidden, self.n_experts, self.inter, self.top_k = hidden, n_experts, inter, top_k
         self.n_shared = n_shared
@@ -57,7 +58,11 @@ class EpochLayer:
             residual=1 if residual else 0, router=_ROUTER[router], n_group=int(n_group),
             topk_group=int(topk_group), raw_weights=1 if raw_weights else 0,
             coverage_check=1 if coverage else 0, coverage_alpha=float(coverage[0]) if coverage else 0.0,
-            coverage_q=float(coverage[1]) if coverage else 0.0, request_size=int(request_size))
+            coverage_q=float(coverage[1]) if coverage else 0.0, request_size=int(request_size),
+            planner=1 if atlas else 0, atlas_m=int(atlas["m"]) if atlas else 0,
+            atlas_B=int(atlas["B"]) if atlas else 0, atlas_c=int(atlas["c"]) if atlas else 0,
+            atlas_alpha=float(atlas["alpha"]) if atlas else 0.0, atlas_q=float(atlas["q"]) if atlas else 0.0,
+            atlas_beta=float(atlas["beta"]) if atlas else 0.0)
         tdt = _TORCH_DT[dtype]
         for name, t in weights.items():
             if not (t.is_cuda and t.is_contiguous()):
@@ -168,8 +173,10 @@ class EpochLayer:
 
     def read_trace(self, stream=None) -> np.ndarray:
         """[9, 1024, 8] int64 per-CTA trace rows: gate, experts, expert epilogue,
-        worklist kernel, gate epilogue steps, worklist kernel steps, expert waits,
-        combine, permute."""
+        the gate's worklist tail (CTA 0: [1] grid barrier passed, [2] words read,
+        [4] offsets scanned, [5] slots, [6] rows issued, [0] before the final
+        wait, [3] done), gate epilogue steps, worklist kernel steps, expert
+        waits, combine, the gate tail's end per CTA ([3])."""
         v = B.epoch_debug_view()
         B.check(B.lib().epoch_debug_pointers(self.handle, C.byref(v)), "epoch_debug_pointers")
         return self._copy(v.trace, 9 * 1024 * 8, np.int64, stream).reshape(9, 1024, 8)
@@ -230,6 +237,9 @@ class EpochLayer:
                 d["support_masks"] = self._copy(v.support_masks, R * E, np.uint8, stream).reshape(R, E)
             else:
                 d["plan_counts"] = self._copy(v.plan_counts, E, np.int32, stream)
+            if self.cfg.planner == 1:
+                res = self._copy(v.atlas_result, 3, np.int32, stream)
+                d["atlas"] = dict(covered_ok=bool(res[0]), n_under=int(res[1]), rounds=int(res[2]))
         if "iter" in parts:
             # selections, weights and slots are stored per position; rows of the
             # fresh positions, in fresh-list order

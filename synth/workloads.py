@@ -61,6 +61,7 @@ class Workload:
     raw_weights: bool = False  # weights not renormalised over the selection
     coverage: Optional[tuple] = None  # (alpha, q) of the per-iteration support-coverage check
     request_size: int = 0  # > 0: positions per request, each request with its own block plan
+    atlas: Optional[tuple] = None  # Expert Atlas planner (m, B, alpha, q, beta, c) instead of the prefix rule
     description: str = ""
 
     @property

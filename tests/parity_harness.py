@@ -63,7 +63,15 @@ def layer_for_workload(wl, layer_index: int = 0, device="cuda", threads: Optiona
                       max_positions=max_positions or wl.n_pos, dtype=wl.dtype, tau=wl.tau, refresh_R=wl.refresh_R,
                       weights=weights, n_shared=wl.n_shared, shared_inter=wl.shared_inter,
                       residual=wl.residual, router=wl.router, n_group=wl.n_group, topk_group=wl.topk_group,
-                      raw_weights=wl.raw_weights, coverage=wl.coverage, request_size=wl.request_size)
+                      raw_weights=wl.raw_weights, coverage=wl.coverage, request_size=wl.request_size,
+                      atlas=atlas_dict(wl))
+
+
+def atlas_dict(wl) -> Optional[dict]:
+    """The workload's Expert Atlas parameters by name (None: the prefix rule)."""
+    if wl.atlas is None:
+        return None
+    return dict(zip(("m", "B", "alpha", "q", "beta", "c"), wl.atlas))
 
 
 def tol_for(dtype: str) -> float:
@@ -87,7 +95,8 @@ def oracle_layer(wl, layer_index: int = 0, max_positions: Optional[int] = None) 
                               expert=expert, shared=shared, residual=wl.residual,
                               max_positions=max_positions or wl.n_pos,
                               router=oracle.Router(wl.router, wl.n_group, wl.topk_group, not wl.raw_weights),
-                              coverage=wl.coverage, request_size=wl.request_size or None)
+                              coverage=wl.coverage, request_size=wl.request_size or None,
+                              atlas=atlas_dict(wl))
 
 
 def tensor_to_f64(t: torch.Tensor) -> np.ndarray:
@@ -256,9 +265,35 @@ def _check_support(orc, op, gplan: dict, n_pos: int, rep: Report, what: str, ado
     (adopt or orc.adopt_support)(gids, glen)
 
 
+def _check_atlas(orc, gplan: dict, rep: Report, what: str) -> None:
+    """The Expert Atlas support: the same experts in the same entry order, and
+    the same coverage outcome; a difference is accepted only when the oracle's
+    run took a decision within NEAR_TIE (its smallest decision margin), and the
+    GPU's support is then adopted."""
+    res = orc.atlas_result
+    glen = int(gplan["support_len"])
+    gids = np.asarray(gplan["support_ids"])[:glen]
+    ga = gplan["atlas"]
+    same = (np.array_equal(gids, res.support) and ga["covered_ok"] == res.covered_ok and
+            ga["n_under"] == res.n_under and ga["rounds"] == res.rounds)
+    if same:
+        return
+    if res.min_margin <= NEAR_TIE:
+        rep.near_ties.append(f"{what}: Atlas support differs at a decision margin of {res.min_margin:.2g}; "
+                             "adopting GPU support")
+        orc.adopt_support(gids, glen)
+        return
+    rep.mismatches.append(f"{what}: Atlas support gpu {gids.tolist()} oracle {res.support.tolist()} "
+                          f"(covered {ga['covered_ok']}/{res.covered_ok}, under {ga['n_under']}/{res.n_under}, "
+                          f"rounds {ga['rounds']}/{res.rounds})")
+
+
 def _check_supports(orc, op, gplan: dict, n_pos: int, rep: Report, what: str) -> None:
     """The block's support, or with per-request supports each request's (its
     own counts, threshold and prefix) and their union, ascending."""
+    if orc.atlas is not None:
+        _check_atlas(orc, gplan, rep, what)
+        return
     if not orc.request_size:
         _check_support(orc, op, gplan, n_pos, rep, what)
         return

@@ -273,6 +273,30 @@ def test_per_request_supports(name):
     assert_clean(rep)
 
 
+@pytest.mark.parametrize("name", ["tiny_bf16_atlas", "tiny_fp32_atlas", "e256_bf16_atlas", "mini_atlas_hot"])
+def test_expert_atlas_planner(name):
+    """The Expert Atlas planner on the GPU: candidates, popularity, greedy
+    repair rounds; the support (in entry order), coverage outcome and rounds
+    against the oracle, then iterations over that support; the last case
+    plans the LLaDA2.0-mini-shaped layer and rebuilds its support with a hot
+    update."""
+    if name == "mini_atlas_hot":
+        wl = synth.WORKLOADS["llada2_mini"].replace(name=name, atlas=(4, 16, 0.9, 0.95, 0.1, 4), iters=4)
+        xs, live, dec = _steps_from(wl, 4)
+        steps = [dict(op="plan", x=xs[0])]
+        steps += [dict(op="iter", x=xs[i], live=live[i], dec=dec[i], i=i, hot_update=(i == 2)) for i in range(4)]
+        assert_clean(scenario_parity(wl, steps))
+        return
+    wl = {
+        "tiny_bf16_atlas": TINY_BF16.replace(name=name, atlas=(2, 3, 0.8, 0.9, 0.5, 2), iters=6),
+        "tiny_fp32_atlas": synth.WORKLOADS["tiny_fp32"].replace(name=name, atlas=(2, 3, 0.8, 0.9, 0.5, 2)),
+        "e256_bf16_atlas": TINY_BF16.replace(name=name, wid=10, n_experts=256, top_k=8, atlas=(4, 16, 0.9, 0.95,
+                                                                                               0.1, 4), iters=6),
+    }[name]
+    rep = block_parity(wl)
+    assert_clean(rep)
+
+
 def test_tau1_R1_is_dense_moe():
     """tau = 1 and R = 1: every position fresh with every expert eligible, so the
     layer equals the dense MoE formula at every iteration."""
@@ -397,6 +421,58 @@ def test_determinism_bitwise():
         assert np.array_equal(a, b)
     for a, b in zip(outs[0][1], outs[1][1]):
         assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("n_iters,hot_at", [(4, None), (5, 2)])
+def test_cuda_graph_replay_matches_eager(n_iters, hot_at):
+    """A block (plan + iterations) captured into a CUDA graph and replayed
+    three times gives, bit for bit, the outputs of the same block run eagerly;
+    an eager block after the replays still does. An odd iteration count and a
+    hot-update iteration (worklist kernel instead of the gate's tail) are
+    included: no per-iteration state may depend on how many calls ran before."""
+    wl = synth.WORKLOADS["llada2_mini"]
+    xs = synth.hidden_states(wl, n_iters)
+    live, dec = synth.block_masks(wl, n_iters)
+    lay = layer_for_workload(wl)
+    dev = lay.device
+    X = [payload_to_torch(xs[i], wl.dtype, dev) for i in range(n_iters)]
+    LV = [torch.from_numpy(live[i]).to(dev) for i in range(n_iters)]
+    DC = [torch.from_numpy(dec[i]).to(dev) for i in range(n_iters)]
+    Y = [torch.empty_like(X[0]) for _ in range(n_iters)]
+
+    def block():
+        lay.plan_block(X[0])
+        for i in range(n_iters):
+            lay.moe_iter(X[i], LV[i], DC[i], i, Y[i], hot_update=(i == hot_at))
+        lay.block_end()
+
+    def outputs():
+        torch.cuda.synchronize()
+        return [y.view(torch.int16).cpu().numpy() for y in Y]
+
+    block()
+    eager = outputs()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        block()
+    torch.cuda.current_stream().wait_stream(side)
+    assert all(np.array_equal(a, b) for a, b in zip(eager, outputs()))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        block()
+    for _ in range(3):
+        for y in Y:
+            y.zero_()
+        graph.replay()
+        got = outputs()
+        for i, (a, b) in enumerate(zip(eager, got)):
+            assert np.array_equal(a, b), f"iteration {i} differs after a replay"
+    code, word = lay.status()
+    assert code == 0, word
+    block()
+    assert all(np.array_equal(a, b) for a, b in zip(eager, outputs()))
+    lay.close()
 
 
 def test_bounded_wait_times_out_and_reports():
