@@ -626,10 +626,10 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
   if (trace && threadIdx.x == 0) trace[1] = static_cast<int64_t>(globaltimer_ns());
   // This launch overlaps the kernel before it (programmatic dependent
   // launch): the gate, which builds the iteration's worklist in its tail, or
-  // the worklist kernel. The shared experts need only the layer input, so the
-  // CTAs start on their tiles at once (on the SMs the gate leaves free, while
-  // it runs); the producer waits for the kernel before to complete only when
-  // the shared tiles are all taken, then reads the worklist.
+  // the worklist kernel. The shared experts' up tiles need only the layer
+  // input, so the CTAs start on them at once (on the SMs the gate leaves free,
+  // while it runs); the producer waits for the kernel before to complete only
+  // when they are all taken, then reads the worklist.
   int32_t *shc = ws.sh_ctr;  // [0] shared tile counter, then done counts (zeroed by the previous combine)
   const int nt_max = (d.Nmax + kTnUp - 1) / kTnUp;
   const int nt_sh = (d.n_pos + kTnUp - 1) / kTnUp;
@@ -723,20 +723,19 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
       tma_prefetch_desc(&p.bs2);
       tma_prefetch_desc(&p.b[0]);
       tma_prefetch_desc(&p.b2[0]);
-      // 1. the shared experts' tiles (up tiles, then down tiles), from launch
+      // 1. the shared experts' up tiles, from launch (their inputs are the layer input)
       while (ok) {
         const int q = atomicAdd(shc, 1);
-        if (q >= n_sh_up + n_sh_dn) break;
+        if (q >= n_sh_up) break;
         int need = 0, tt;
         const int4 td = shared_tile(d, q, &need, &tt);
-        const int32_t *flag = q >= n_sh_up ? shc + 1 + ((td.x & (kDownBit - 1)) - d.E) * nt_max + tt : nullptr;
-        ok = post(td) && issue(td, flag, need, 2);
+        ok = post(td) && issue(td, nullptr, need, 2);
       }
     }
     __syncwarp();
-    // 2. the routed experts' tiles, from one counter: up tiles, then down
-    // tiles, once the worklist of this call is complete (offsets, group list,
-    // xp rows)
+    // 2. once the worklist of this call is complete (offsets, group list, xp
+    // rows), from one counter: the routed up tiles, the shared experts' down
+    // tiles, the routed down tiles (down tiles wait for their group's up tiles)
     pdl_wait();
     for (int i = lane; i <= d.E; i += 32) {
       s_list[i] = ws.grp_list[i];
@@ -746,21 +745,30 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
     if (lane == 0) {
       const int n_tiles = s_list[d.E] >> kGrpIdBits;
       const int n_up = d.tn > 0 ? (d.I / BM) * n_tiles : 0;
-      const int total = ok ? n_up + (d.tn > 0 ? (d.H / kBmDn) * n_tiles : 0) : 0;
+      const int total = ok ? n_up + n_sh_dn + (d.tn > 0 ? (d.H / kBmDn) * n_tiles : 0) : 0;
       while (ok) {
         const int q = atomicAdd(ws.tile_ctr, 1);
         if (q >= total) break;
         int4 td;
-        int need = 0;
-        if (!locate(d, s_list, s_offs, q, n_up, &td, &need)) {
-          set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-          *abort_flag = 1;
-          ok = false;
-          break;
+        int need = 0, kind = 1;
+        const int32_t *flag = nullptr;
+        if (q >= n_up && q < n_up + n_sh_dn) {
+          int tt;
+          td = shared_tile(d, n_sh_up + q - n_up, &need, &tt);
+          flag = shc + 1 + ((td.x & (kDownBit - 1)) - d.E) * nt_max + tt;
+          kind = 2;
+        } else {
+          const int qr = q < n_up ? q : q - n_sh_dn;
+          if (!locate(d, s_list, s_offs, qr, n_up, &td, &need)) {
+            set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          // routed up tiles: the rows are in xp; down tiles: their group's up tiles
+          if (q >= n_up) flag = ws.done_up + (td.x & (kDownBit - 1));
         }
-        // routed up tiles: the rows are in xp; down tiles: wait for their group's up tiles
-        const int32_t *flag = q < n_up ? nullptr : ws.done_up + (td.x & (kDownBit - 1));
-        ok = post(td) && issue(td, flag, need, 1);
+        ok = post(td) && issue(td, flag, need, kind);
       }
       if (ok) ok = post(make_int4(-1, 0, 0, 0));  // end of the stream
       if (!ok) {
