@@ -140,10 +140,11 @@ __device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t byt
                "r"(src), "r"(bytes)
                : "memory");
 }
-// Waits until every bulk store this thread issued has completed.
-__device__ __forceinline__ void bulk_store_wait_all() {
+// Waits until every bulk store this thread issued has read its shared-memory
+// source (the writes complete with the grid: kernels launched after it see them).
+__device__ __forceinline__ void bulk_store_wait_read() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 // Orders this CTA's earlier generic-proxy accesses to shared memory before
 // later async-proxy (bulk copy) accesses to it.

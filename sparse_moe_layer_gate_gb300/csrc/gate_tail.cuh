@@ -20,8 +20,9 @@
 // e in [p0, t). The CTA then bulk-copies each staged x row to its k worklist
 // rows and writes the slots, the fresh index and the fresh list of its
 // positions. CTA 0 also publishes the offsets and the expert kernel's group
-// list, CTA 1 the statistics. One round of global loads after the barrier, no
-// other global read on the way to the expert kernel's inputs.
+// list; the combine kernel finishes the statistics. One round of global loads
+// after the barrier, no other global read on the way to the expert kernel's
+// inputs.
 //
 // Worklist order: expert-major, positions ascending within an expert (the
 // order the oracle defines), reached without any sort.
@@ -44,6 +45,7 @@ struct GateTail {
   const int16_t *cidx;  // [E] candidate index of an expert (valid where cand[cidx[e]] == e)
   int ncand;            // candidates of the plan
   uint32_t x_bar;       // mbarrier of the staged x rows (phase 0)
+  int gen0;             // the grid barrier's generation word, read at the kernel's start
 };
 
 // Shared-memory bytes of the tail's scratch in the operand ring: staged x
@@ -119,9 +121,11 @@ __device__ __forceinline__ void gate_tail(const Dims &d, const Work &ws, const u
   // last CTA to arrive advances the generation word the others wait on, and
   // CTA 0 zeroes the arrival count once it has passed. Bounded.
   if (tid == 0) {
+    // (the generation read at the kernel's start cannot have moved: the barrier
+    // is released only after this CTA has arrived)
     int32_t *count = ws.gate_arrive, *gen = ws.gate_arrive + 1;
-    int g0, arrived;
-    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(g0) : "l"(gen) : "memory");
+    const int g0 = gt.gen0;
+    int arrived;
     // release: this CTA's selections, words and tallies; acquire (the last
     // CTA): every other CTA's, before it releases the rest
     asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(arrived) : "l"(count) : "memory");
@@ -319,53 +323,15 @@ __device__ __forceinline__ void gate_tail(const Dims &d, const Work &ws, const u
   }
 
   if (trace && tid == 0) trace[6] = static_cast<int64_t>(globaltimer_ns());
-  // ---- 6. control words and statistics (CTA 1, beside CTA 0's publication)
-  if (blockIdx.x == (gridDim.x > 1 ? 1 : 0) && ok && tid == 0) {
-    // the tallies every CTA added before the barrier (they restart for the
-    // next call), the coverage count, the plan's support size: loaded together
-    int tl[kTallies];
-#pragma unroll
-    for (int q = 0; q < kTallies; ++q) tl[q] = __ldcg(ws.tally + q);
-    const int under = d.cov_check ? __ldcg(ws.cov_under) : 0;
-    const int slen = __ldcg(&ws.ctrl->support_len);
-#pragma unroll
-    for (int q = 0; q < kTallies; ++q) ws.tally[q] = 0;
-    *ws.cov_under = 0;
-    const int n_fresh = tl[6];
-    const int nt_sh = d.tn > 0 ? d.n_sh * ((n + d.tn - 1) / d.tn) : 0;
-    const int fb = (d.host_fallback ? 1 : 0) | ((anom & 1) ? 2 : 0) | ((anom & 2) ? 4 : 0);
-    if (n_fresh * k != n_edges) set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-    if (tl[5]) set_error(ws.err, EPOCH_DEVERR_FLAGS);
+  // ---- 6. the control words the statistics need (CTA 0); the statistics
+  // themselves are finished by the combine kernel (gate_tail_stats), off the
+  // path to the expert kernel
+  if (blockIdx.x == 0 && ok && tid == 0) {
     Ctrl *c = ws.ctrl;
     c->tiles_up = d.tn > 0 ? (d.I / 128) * n_tiles : 0;
     c->tiles_dn = d.tn > 0 ? (d.H / kBmDn) * n_tiles : 0;
     c->n_edges = n_edges;
     c->n_hit = n_hit;
-    c->n_fresh = n_fresh;
-    c->fallback = fb;
-    // support coverage of this iteration's fresh positions -> the next iteration
-    c->short_next =
-        (d.cov_check && static_cast<float>(under) > (1.f - d.cov_q) * static_cast<float>(n_fresh)) ? 1 : 0;
-    epoch_iter_stats st;
-    st.iteration = d.iter;
-    st.n_pos = n;
-    st.n_live = tl[C_LIVE];
-    st.n_new = tl[C_NEW];
-    st.n_miss = tl[C_MISS];
-    st.n_stale = tl[C_STALE];
-    st.n_forced = force ? tl[C_REUSE] : 0;
-    st.n_reuse = force ? 0 : tl[C_REUSE];
-    st.n_fresh = n_fresh;
-    st.n_edges = n_edges;
-    st.n_hit_experts = n_hit;
-    st.support_len = fb ? E : slen;
-    st.fallback = fb;
-    st.bad_flags = tl[5];
-    st.tiles_up = (d.tn > 0 ? (d.I / 128) * n_tiles : 0) + (d.I_s / 128) * nt_sh;
-    st.tiles_down = (d.tn > 0 ? (d.H / kBmDn) * n_tiles : 0) + (d.H / kBmDn) * nt_sh;
-    st.n_under = under;
-    *ws.stats = st;
-    if (d.stats_out) *d.stats_out = st;
   }
 
   // ---- 7. positions beyond n_pos keep their state; the words of the next
@@ -381,9 +347,59 @@ __device__ __forceinline__ void gate_tail(const Dims &d, const Work &ws, const u
     for (int q = gi; q < E * cmax; q += gs) next[q] = 0u;
   }
   if (trace && tid == 0) trace[0] = static_cast<int64_t>(globaltimer_ns());
-  bulk_store_wait_all();  // the worklist rows are written before the CTA exits
+  bulk_store_wait_read();  // the staged rows are read out before the CTA exits
   if (trace && tid == 0) trace[3] = static_cast<int64_t>(globaltimer_ns());
   if (d.trace && tid == 0 && blockIdx.x < kTraceCtas) ws.trace[(8ull * kTraceCtas + blockIdx.x) * kTraceFields + 3] = static_cast<int64_t>(globaltimer_ns());
+}
+
+// The iteration's statistics and control words after a gate-tail worklist,
+// by one thread of the combine kernel (which runs once the expert kernel, and
+// so the gate, has completed): the tallies every gate CTA added (they restart
+// for the next call), the coverage count, and the values gate CTA 0 left in
+// the control block.
+__device__ __forceinline__ void gate_tail_stats(const Dims &d, const Work &ws) {
+  const int n = d.n_pos, E = d.E, k = d.k;
+  int tl[kTallies];
+#pragma unroll
+  for (int q = 0; q < kTallies; ++q) tl[q] = __ldcg(ws.tally + q);
+  const int under = d.cov_check ? __ldcg(ws.cov_under) : 0;
+  Ctrl *c = ws.ctrl;
+  const int anom = c->anom, slen = c->support_len, n_edges = c->n_edges, n_hit = c->n_hit;
+  const int tiles_up = c->tiles_up, tiles_dn = c->tiles_dn;
+#pragma unroll
+  for (int q = 0; q < kTallies; ++q) ws.tally[q] = 0;
+  *ws.cov_under = 0;
+  const bool force = d.host_fallback != 0 || anom != 0;
+  const int n_fresh = tl[6];
+  const int nt_sh = d.tn > 0 ? d.n_sh * ((n + d.tn - 1) / d.tn) : 0;
+  const int fb = (d.host_fallback ? 1 : 0) | ((anom & 1) ? 2 : 0) | ((anom & 2) ? 4 : 0);
+  if (n_fresh * k != n_edges) set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+  if (tl[5]) set_error(ws.err, EPOCH_DEVERR_FLAGS);
+  c->n_fresh = n_fresh;
+  c->fallback = fb;
+  // support coverage of this iteration's fresh positions -> the next iteration
+  c->short_next =
+      (d.cov_check && static_cast<float>(under) > (1.f - d.cov_q) * static_cast<float>(n_fresh)) ? 1 : 0;
+  epoch_iter_stats st;
+  st.iteration = d.iter;
+  st.n_pos = n;
+  st.n_live = tl[C_LIVE];
+  st.n_new = tl[C_NEW];
+  st.n_miss = tl[C_MISS];
+  st.n_stale = tl[C_STALE];
+  st.n_forced = force ? tl[C_REUSE] : 0;
+  st.n_reuse = force ? 0 : tl[C_REUSE];
+  st.n_fresh = n_fresh;
+  st.n_edges = n_edges;
+  st.n_hit_experts = n_hit;
+  st.support_len = fb ? E : slen;
+  st.fallback = fb;
+  st.bad_flags = tl[5];
+  st.tiles_up = tiles_up + (d.I_s / 128) * nt_sh;
+  st.tiles_down = tiles_dn + (d.H / kBmDn) * nt_sh;
+  st.n_under = under;
+  *ws.stats = st;
+  if (d.stats_out) *d.stats_out = st;
 }
 
 }  // namespace epoch

@@ -156,7 +156,7 @@ __global__ void __maxnreg__(104) k_tc_gate(const __grid_constant__ GateParams p)
   uint2 *s_scr = reinterpret_cast<uint2 *>(s_stamp + 64);  // [warps][32] top-k scratch
   // for the worklist tail (gate_tail.cuh)
   uint64_t *x_barp = reinterpret_cast<uint64_t *>(s_scr + 32 * (kGateThreads / 32));  // staged x rows
-  int *s_ncand = reinterpret_cast<int *>(x_barp + 1);
+  int *s_ncand = reinterpret_cast<int *>(x_barp + 1);      // [0] candidates, [1] barrier generation
   uint8_t *s_fr = reinterpret_cast<uint8_t *>(s_ncand + 2);  // [64] own position fresh
   int16_t *s_sel = reinterpret_cast<int16_t *>(s_fr + 64);   // [64][16] its selected experts
   int16_t *s_cand = s_sel + 64 * 16;                         // [1024] candidate experts
@@ -286,7 +286,10 @@ __global__ void __maxnreg__(104) k_tc_gate(const __grid_constant__ GateParams p)
       if (tid == 64 && shortfall_flag(d, ws)) atomicOr(s_anom, 2);
       if (d.wl_in_gate) {  // the plan's candidate experts, for the worklist tail
         const int nc = ws.ctrl->support_len;
-        if (tid == 64) *s_ncand = nc;
+        if (tid == 64) {
+          s_ncand[0] = nc;
+          s_ncand[1] = *reinterpret_cast<volatile const int32_t *>(ws.gate_arrive + 1);  // barrier generation
+        }
         for (int i = tid - 64; i < d.E; i += kGateThreads - 64) {
           const int e = ws.support_ids[i];
           const bool valid = e >= 0 && e < d.E;
@@ -406,7 +409,7 @@ __global__ void __maxnreg__(104) k_tc_gate(const __grid_constant__ GateParams p)
   cluster_wait();  // no CTA leaves while another may still read its partials
   if (trace2 && tid == 0) trace2[3] = static_cast<int64_t>(globaltimer_ns());
   if (!d.plan_mode && d.wl_in_gate) {
-    const GateTail gt{s_sel, s_fr, s_code, s_cand, s_cidx, *s_ncand, x_bar};
+    const GateTail gt{s_sel, s_fr, s_code, s_cand, s_cidx, s_ncand[0], x_bar, s_ncand[1]};
     int64_t *trace_wl = (d.trace && blockIdx.x == 0) ? ws.trace + 3ull * kTraceCtas * kTraceFields : nullptr;
     gate_tail(d, ws, reinterpret_cast<const uint8_t *>(p.xv), smem, gt, tile * TN + rank * TPC, TPC,
               d.host_fallback != 0 || *s_anom != 0, *s_anom, trace_wl);

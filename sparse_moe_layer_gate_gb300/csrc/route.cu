@@ -20,6 +20,7 @@
 #include "select.cuh"
 #include "topk.cuh"
 #include "worklist.cuh"
+#include "gate_tail.cuh"
 
 namespace epoch {
 
@@ -524,8 +525,11 @@ __global__ void __launch_bounds__(128, 7) k_combine(Dims d, Work ws, const T *__
   // kernel, both before the experts). A hardware wait: no thread of this grid
   // polls memory while the experts stream.
   pdl_wait();
-  if (blockIdx.x == 0)  // the next call's expert kernel takes shared-expert tiles from its launch
+  if (blockIdx.x == 0) {
+    // the next call's expert kernel takes shared-expert tiles from its launch
     for (int q = threadIdx.x; q < sh_stride(d); q += blockDim.x) ws.sh_ctr[q] = 0;
+    if (d.wl_in_gate && threadIdx.x == 0) gate_tail_stats(d, ws);
+  }
   if (t < d.n_pos) {
     if (threadIdx.x < k) {
       slot_s[threadIdx.x] = ws.slot[static_cast<size_t>(t) * k + threadIdx.x];
