@@ -124,7 +124,7 @@ size_t carve(const epoch_layer_config &c, char *base, Work *w) {
   t.sel_words = static_cast<uint32_t *>(take(2 * chunks * E * 4));
   t.offsets = static_cast<int32_t *>(take((E + 1) * 4));
   t.grp_list = static_cast<int32_t *>(take((E + nsh + 1) * 4));
-  t.done_up = static_cast<int32_t *>(take((E + nsh) * 4));
+  t.done_up = static_cast<int32_t *>(take(E * ((I + 127) / 128) * 4));
   t.cov_under = static_cast<int32_t *>(take(8));
   t.tile_ctr = static_cast<int32_t *>(take(16));
   t.tally = static_cast<int32_t *>(take(32));

@@ -481,7 +481,7 @@ __device__ __forceinline__ bool locate(const Dims &d, const int32_t *list, const
   const int n_valid = min(kTnUp, rows - tt * kTnUp);
   if (n_valid <= 0) return false;
   *td = make_int4(g | (up ? 0 : kDownBit), m, r0, n_valid);
-  *need = nt * (d.I / BM);
+  *need = nt;  // down tiles: every token tile of the group, per row block of I
   return true;
 }
 
@@ -650,16 +650,18 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
     uint32_t phase = 0, armed = 0, armed_par = 0;
     bool ok = true;
     uint64_t waited = 0;
+    int64_t waited_by[3] = {0, 0, 0};  // ns waiting for: (unused), routed up tiles, shared up tiles
     // Issues the operand copies of one tile. Token rows that this launch
-    // produces -- routed up tiles: xp rows (copy warps); down tiles: the
-    // activations of the group's up tiles -- are awaited (flag >= target)
-    // after the weight copies of the first stages have gone out.
-    int64_t waited_by[3] = {0, 0, 0};  // ns waiting for: xp rows, routed up tiles, shared up tiles
-    auto issue = [&](const int4 &td, const int32_t *flag, int target, int wait_kind) -> bool {
+    // produces -- the activations of down tiles -- are awaited (counter >=
+    // target) after the weight copies of the first stages have gone out. flag:
+    // nullptr (no dependency) or the first readiness counter; fstep > 0: K
+    // block kb waits for flag[kb / fstep] (the group's up tiles of one row
+    // block), 0: every K block waits for flag[0].
+    auto issue = [&](const int4 &td, const int32_t *flag, int target, int wait_kind, int fstep) -> bool {
       const XTile t = xdecode(p, td);
       const uint32_t tx = t.a_bytes + t.b_bytes;
       const bool dep = flag != nullptr;
-      const int pre = dep ? min(t.nk, t.up ? kExpStages : 2) : 0;
+      const int pre = dep ? min(t.nk, kExpStages) : 0;
       int pre_stage[kExpStages] = {0, 0, 0, 0};
       for (int kb = 0; kb < pre; ++kb) {
         if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, ws.err, tmo)) return false;
@@ -674,36 +676,45 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
           phase ^= 1u;
         }
       }
-      if (dep) {
-        const uint64_t t0 = globaltimer_ns();
-        for (;;) {
-          int done;
-          asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(done) : "l"(flag) : "memory");
-          if (done >= target) break;
-          if (*abort_flag) return false;
-          if (globaltimer_ns() - t0 > tmo) {
-            set_error(ws.err, EPOCH_DEVERR_TIMEOUT);
-            *abort_flag = 1;
-            return false;
+      int ready = -1;  // the counter last seen at its target
+      auto tokens = [&](int kb, int st) -> bool {
+        if (dep) {
+          const int fi = fstep > 0 ? kb / fstep : 0;
+          if (fi != ready) {
+            const int32_t *f = flag + fi;
+            const uint64_t t0 = globaltimer_ns();
+            for (;;) {
+              int done;
+              asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(done) : "l"(f) : "memory");
+              if (done >= target) break;
+              if (*abort_flag) return false;
+              if (globaltimer_ns() - t0 > tmo) {
+                set_error(ws.err, EPOCH_DEVERR_TIMEOUT);
+                *abort_flag = 1;
+                return false;
+              }
+              __nanosleep(32);
+            }
+            const int64_t w_ns = static_cast<int64_t>(globaltimer_ns() - t0);
+            waited += w_ns;
+            waited_by[wait_kind] += w_ns;
+            asm volatile("fence.proxy.async.global;" ::: "memory");  // generic writes -> TMA reads
+            ready = fi;
           }
-          __nanosleep(32);
         }
-        const int64_t w_ns = static_cast<int64_t>(globaltimer_ns() - t0);
-        waited += w_ns;
-        waited_by[wait_kind] += w_ns;
-        asm volatile("fence.proxy.async.global;" ::: "memory");  // generic writes -> TMA reads
-        for (int kb = 0; kb < pre; ++kb)
-          tma_load_2d(sbase + pre_stage[kb] * kExpStage + 2 * kTileBytes, t.mb, kb * BK, t.b_row,
-                      full_bar(pre_stage[kb]), pol_b);
-      }
+        tma_load_2d(sbase + st * kExpStage + 2 * kTileBytes, t.mb, kb * BK, t.b_row, full_bar(st), pol_b);
+        return true;
+      };
+      for (int kb = 0; kb < pre; ++kb)
+        if (!tokens(kb, pre_stage[kb])) return false;
       for (int kb = pre; kb < t.nk; ++kb) {
         if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, ws.err, tmo)) return false;
         mbar_arrive_expect_tx(full_bar(stage), tx);
         const uint32_t st = sbase + stage * kExpStage;
         bulk_load(st, t.a_src + static_cast<size_t>(kb) * t.a_bytes, t.a_bytes, full_bar(stage), pol_w);
-        tma_load_2d(st + 2 * kTileBytes, t.mb, kb * BK, t.b_row, full_bar(stage), pol_b);
         armed |= 1u << stage;
         armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+        if (!tokens(kb, stage)) return false;
         if (++stage == kExpStages) {
           stage = 0;
           phase ^= 1u;
@@ -732,7 +743,7 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
         if (q >= n_sh_up) break;
         int need = 0, tt;
         const int4 td = shared_tile(d, q, &need, &tt);
-        ok = post(td) && issue(td, nullptr, need, 2);
+        ok = post(td) && issue(td, nullptr, need, 2, 0);
       }
     }
     __syncwarp();
@@ -753,13 +764,14 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
         const int q = atomicAdd(ws.tile_ctr, 1);
         if (q >= total) break;
         int4 td;
-        int need = 0, kind = 1;
+        int need = 0, kind = 1, fstep = BM / BK;
         const int32_t *flag = nullptr;
         if (q >= n_up && q < n_up + n_sh_dn) {
           int tt;
           td = shared_tile(d, n_sh_up + q - n_up, &need, &tt);
           flag = shc + 1 + ((td.x & (kDownBit - 1)) - d.E) * nt_max + tt;
           kind = 2;
+          fstep = 0;
         } else {
           const int qr = q < n_up ? q : q - n_sh_dn;
           if (!locate(d, s_list, s_offs, qr, n_up, &td, &need)) {
@@ -768,10 +780,11 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
             ok = false;
             break;
           }
-          // routed up tiles: the rows are in xp; down tiles: their group's up tiles
-          if (q >= n_up) flag = ws.done_up + (td.x & (kDownBit - 1));
+          // routed up tiles: the rows are in xp; down tiles: their group's up
+          // tiles, one row block of I (two K blocks) at a time
+          if (q >= n_up) flag = ws.done_up + static_cast<size_t>(td.x & (kDownBit - 1)) * (d.I / BM);
         }
-        ok = post(td) && issue(td, flag, need, kind);
+        ok = post(td) && issue(td, flag, need, kind, fstep);
       }
       if (ok) ok = post(make_int4(-1, 0, 0, 0));  // end of the stream
       if (!ok) {
@@ -938,7 +951,9 @@ __global__ void __launch_bounds__(192, 1) k_tc_experts(const __grid_constant__ T
         if (wid == 2 && lane == 0) {
           __threadfence();
           asm volatile("fence.proxy.async.global;" ::: "memory");
-          atomicAdd(t.g >= d.E ? shc + 1 + (t.g - d.E) * nt_max + t.b_row / kTnUp : ws.done_up + t.g, 1);
+          atomicAdd(t.g >= d.E ? shc + 1 + (t.g - d.E) * nt_max + t.b_row / kTnUp
+                               : ws.done_up + static_cast<size_t>(t.g) * (d.I / BM) + t.col0 / BM,
+                    1);
         }
       }
       if (etr) {

@@ -55,7 +55,8 @@ struct Work {
   int32_t *offsets;       // [E+1]
   int32_t *grp_list;      // [E + n_sh + 1] expert-kernel groups in list order: token tiles of the
                           // groups before << kGrpIdBits | group (shared experts E..E+n_sh-1)
-  int32_t *done_up;       // [E + n_sh] up tiles of each group finished this iteration (by group id)
+  int32_t *done_up;       // [E][I/128] routed up tiles finished this iteration, per expert and row block
+                          // of I (counting token tiles)
   int32_t *cov_under;     // [1] fresh positions of this call under the coverage floor (zeroed by the
                           // worklist bookkeeping once read)
   int32_t *tile_ctr;      // [0] next tile of the expert kernel (dynamic scheduling; reset by the

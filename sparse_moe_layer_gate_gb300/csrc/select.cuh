@@ -240,7 +240,7 @@ __device__ __forceinline__ void select_position(const Dims &d, const Work &ws, i
 // flags: bit 0 a decoded -> live anomaly, bit 1 the previous iteration's
 // coverage shortfall (both make the iteration full fresh).
 __device__ __forceinline__ void reset_iteration_state(const Dims &d, const Work &ws, int flags) {
-  for (int g = threadIdx.x; g < d.E + d.n_sh; g += blockDim.x) ws.done_up[g] = 0;
+  for (int g = threadIdx.x; g < d.E * (d.I / 128); g += blockDim.x) ws.done_up[g] = 0;
   if (threadIdx.x == 0) {
     ws.ctrl->anom = flags;
     ws.tile_ctr[0] = 0;

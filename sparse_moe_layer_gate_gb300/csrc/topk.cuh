@@ -82,7 +82,10 @@ __device__ __forceinline__ void warp_topk(const float (&v)[EPL], const bool (&ok
   *my_val = -INFINITY;
   if (k <= 16) {
     int r = 0;  // rank of this lane's best among the lane bests
-#pragma unroll
+    // (a partly rolled loop: this code runs once per position and iteration,
+    // usually from a cold instruction cache, where its size costs more than
+    // the loop overhead)
+#pragma unroll 4
     for (int i = 0; i < 32; ++i) {
       const unsigned o = __shfl_sync(kAll, bk, i);
       r += (o > bk) || (o == bk && i < lane);
