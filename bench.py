@@ -48,12 +48,11 @@ class L2Flush:
         self.w.fill_(i & 0xFF)
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one expert-kernel
-# launch: the ncu capture at iteration 20 of the accounting block (231.9 MB read,
-# 3.0 MB written; every iteration of this workload hits the same 34 routed
-# experts), tied to the kernel source it was measured on (null once that
-# source changes; the hash covers the whole file: it was moved on from the
-# captured source only by edits outside k_tc_experts, to the gate's router).
-TRAFFIC = {"experts": {"bytes_per_launch": 234.92e6, "source_sha": "6ff4dc48f09af719"}}
+# launch: the ncu capture of iteration 20 of the accounting block
+# (profiles/experts_llada2_mini.md: 232.0 MB read, 3.3 MB written; every
+# iteration of this workload hits the same 34 routed experts), tied to the
+# source it was measured on (reported as null once that source changes).
+TRAFFIC = {"experts": {"bytes_per_launch": 235.27e6, "source_sha": "61a8b53b7730cb99"}}
 
 
 def parse():
@@ -161,9 +160,12 @@ def experts_kernel_bytes(wl, st):
 
 
 def source_sha():
+    """Hash of the expert kernel's source files (the kernel, its helpers and the
+    shared layout header)."""
     h = hashlib.sha256()
-    with open(os.path.join(ROOT, "sparse_moe_layer_gate_gb300", "csrc", "gemm_tc.cu"), "rb") as fh:
-        h.update(fh.read())
+    for f in ("gemm_tc.cu", "common.cuh", "layer.h"):
+        with open(os.path.join(ROOT, "sparse_moe_layer_gate_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
@@ -427,12 +429,13 @@ def run_epoch(args, rank, world):
 def traced_breakdown(lay, wl, xs, lv, dc, ys, flush):
     """Phases of the pipelined iteration from the kernels' own per-CTA traces
     (globaltimer), one traced block, synchronised after every iteration:
-    gate (its first CTA entry until its CTAs have all selected: the grid
-    barrier of its worklist tail, or its last exit when a separate worklist
-    kernel follows), worklist (from there to the expert kernel's first tile:
-    offsets, group list and row copies), expert phase (first tile to the last
-    epilogue), combine tail (last expert epilogue to the combine's last exit),
-    and the whole span. Means over the iterations, in us."""
+    selection (the gate's first CTA entry until its CTAs have all classified
+    and routed their positions: the grid barrier of its worklist tail),
+    worklist (from there to the gate's last exit; with a separate worklist
+    kernel, to that kernel's last exit), expert phase (from there to the expert
+    kernel's last epilogue: the routed tiles; the shared experts' up tiles ran
+    earlier, beside the gate), combine tail (to the combine's last exit), and
+    the whole span. Means over the iterations, in us."""
     import numpy as np
     import torch
     lay.plan_block(xs[0])
@@ -447,19 +450,21 @@ def traced_breakdown(lay, wl, xs, lv, dc, ys, flush):
         if not all(k in tl for k in ("gate", "experts", "combine")):
             continue
         t0, g1 = tl["gate"]
-        if "routing" not in tl and tr[3, 0, 1] > t0:
-            g1 = tr[3, 0, 1]  # the gate's grid barrier, passed by CTA 0
+        if "routing" in tl:
+            sel_end, wl_end = g1, tl["routing"][1]
+        else:
+            sel_end, wl_end = (tr[3, 0, 1] if tr[3, 0, 1] > t0 else g1), g1
         e = tr[1]
-        em = (e[:, 2] > 0) & (e[:, 4] > 0)
-        first_tile, last_epi = float(e[em, 2].min()), float(e[em, 4].max())
-        rows.append([(g1 - t0) / 1e3, (first_tile - g1) / 1e3, (last_epi - first_tile) / 1e3,
+        em = e[:, 4] > 0
+        last_epi = float(e[em, 4].max())
+        rows.append([(sel_end - t0) / 1e3, (wl_end - sel_end) / 1e3, (last_epi - wl_end) / 1e3,
                      (tl["combine"][1] - last_epi) / 1e3, (tl["combine"][1] - t0) / 1e3])
     lay.set_tracing(False)
     lay.block_end()
     if not rows:
         return None
     m = np.array(rows).mean(axis=0)
-    return {"gate_us": round(float(m[0]), 2), "worklist_us": round(float(m[1]), 2),
+    return {"selection_us": round(float(m[0]), 2), "worklist_us": round(float(m[1]), 2),
             "expert_phase_us": round(float(m[2]), 2), "combine_tail_us": round(float(m[3]), 2),
             "span_us": round(float(m[4]), 2),
             "how": "per-CTA globaltimer traces of one block, synchronised after every iteration"}

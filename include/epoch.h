@@ -225,21 +225,19 @@ typedef struct {
    * on (globaltimer ns; unused fields keep older values). Row 0, gate (bf16
    * layers): entry, setup done, first operand stage landed, last MMA issued,
    * epilogue done, position tile, H slice (cluster rank), SM id. Row 1,
-   * experts: entry, setup done, worklist received, last MMA complete, epilogue
+   * experts: entry, setup done, producer start, last MMA complete, epilogue
    * done, tiles, ns the producer waited for up tiles, SM id. Row 2, expert
    * epilogue: ns busy, ns waiting for accumulators, longest tile epilogue in
    * ns, that tile's group (bit 30 set: down tile) and valid rows, start and end
-   * of the last tile's epilogue, SM id. Row 3, worklist kernel (one CTA):
-   * entry, gate finished, expert counts done, offsets and tile list done,
-   * worklist published, end, -, SM id. Row 4, gate epilogue: partial sums in
-   * shared memory, cluster barrier passed, own rows reduced, exit. Row 5,
-   * worklist kernel steps: candidates' words loaded, offsets scanned, worklist
-   * positions written, publish. Row 6, experts: ns the producer waited for
-   * compact token rows, for routed up tiles, for shared-expert up tiles; time
-   * the shared-expert phase ended, time the worklist was seen. Row 7, combine
-   * (one CTA per position): entry, expert outputs complete, slots checked,
-   * end, -, -, -, SM id. Row 8, permute: entry, worklist seen, copies
-   * counted, -, -, -, -, SM id. */
+   * of the last tile's epilogue, SM id. Row 3, the gate's worklist tail (CTA 0;
+   * bf16 layers whose gate grid is one wave): before the final wait, grid
+   * barrier passed, candidates' words read, done, offsets scanned, slots
+   * written, worklist rows issued. Row 4, gate epilogue: partial sums in shared
+   * memory, cluster barrier passed, own rows reduced, exit. Row 5: unused. Row
+   * 6, experts: -, ns the producer waited for routed up tiles, for shared-expert
+   * up tiles. Row 7, combine (one CTA per position): entry, expert outputs
+   * complete, slots checked, end, -, -, -, SM id. Row 8, the gate's worklist
+   * tail: field 3, the CTA's end. */
   const int64_t *trace;
   /* [2][EPOCH_PROF_KINDS] while tracing: first CTA entry and last CTA exit
    * (globaltimer ns) of each kernel kind in the last iteration, in the order

@@ -172,11 +172,10 @@ class EpochLayer:
         B.check(B.lib().epoch_set_tracing(self.handle, 1 if on else 0), "epoch_set_tracing")
 
     def read_trace(self, stream=None) -> np.ndarray:
-        """[9, 1024, 8] int64 per-CTA trace rows: gate, experts, expert epilogue,
-        the gate's worklist tail (CTA 0: [1] grid barrier passed, [2] words read,
-        [4] offsets scanned, [5] slots, [6] rows issued, [0] before the final
-        wait, [3] done), gate epilogue steps, worklist kernel steps, expert
-        waits, combine, the gate tail's end per CTA ([3])."""
+        """[9, 1024, 8] int64 per-CTA trace rows (see epoch_debug_view.trace):
+        gate, experts, expert epilogue, the gate's worklist tail (CTA 0), gate
+        epilogue steps, unused, expert waits, combine, the gate tail's end per
+        CTA."""
         v = B.epoch_debug_view()
         B.check(B.lib().epoch_debug_pointers(self.handle, C.byref(v)), "epoch_debug_pointers")
         return self._copy(v.trace, 9 * 1024 * 8, np.int64, stream).reshape(9, 1024, 8)

@@ -137,9 +137,8 @@ def test_boundary_outputs_support_and_stats():
 
 
 def test_every_expert_eligible_at_2048_positions():
-    """tau = 1 keeps all 256 experts: the candidates' selection words (256 x 64)
-    exceed the worklist kernel's shared-memory staging, which then reads them
-    from global memory."""
+    """tau = 1 keeps all 256 experts over 2048 positions: every expert is a
+    candidate and each candidate's selection words span two 32-word blocks."""
     assert_clean(block_parity(synth.sweep_workload(64, 1.0, 4), n_iters=2))
 
 
