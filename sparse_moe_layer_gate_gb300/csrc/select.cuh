@@ -117,6 +117,97 @@ __device__ __forceinline__ int shortfall_flag(const Dims &d, const Work &ws) {
 // With d.cov_check the position's support coverage is checked as well (see
 // the coverage fields of epoch_layer_config) against support_mask, the block
 // support, and an under-covered position is counted in cov_under.
+// Top-k of the group-limited sigmoid router (see select_position), out of
+// line so that the default router's path stays short: lane l passes its EPL
+// logits v (without the bias) and eligibility; *sel and *wgt get lane l's
+// selection (l < k).
+template <int EPL>
+__device__ __noinline__ void select_sigmoid_group(const Dims &d, const float *v_in, const bool *ok_in,
+                                                  const float *bias, uint2 *scratch, int *sel_out, float *wgt_out) {
+  const int lane = lane_id(), e0 = lane * EPL, k = d.k;
+  float v[EPL], cs[EPL];
+  bool ok[EPL];
+#pragma unroll
+  for (int c = 0; c < EPL; ++c) {
+    v[c] = v_in[c];
+    ok[c] = ok_in[c];
+    const int e = e0 + c;
+    cs[c] = e < d.E ? 1.f / (1.f + expf(-v[c])) + bias[e] : -INFINITY;
+  }
+  warp_group_limit<EPL>(cs, ok, d.E, d.n_group, d.topk_group, k);
+  int sel;
+  float val;
+  warp_topk<EPL>(cs, ok, k, &sel, &val, scratch);
+  // the selected expert's logit, from the lane that owns it
+  const int owner = sel >= 0 ? sel / EPL : 0, idx = sel >= 0 ? sel - owner * EPL : 0;
+  float z = 0.f;
+#pragma unroll
+  for (int c = 0; c < EPL; ++c) {
+    const float o = __shfl_sync(0xffffffffu, v[c], owner);
+    if (c == idx) z = o;
+  }
+  const float sg = lane < k ? 1.f / (1.f + expf(-z)) : 0.f;
+  float denom = 0.f;
+  for (int j = 0; j < k; ++j) denom += __shfl_sync(0xffffffffu, sg, j);
+  *sel_out = sel;
+  *wgt_out = d.raw_weights ? sg : sg / denom;
+}
+
+// Support coverage of one fresh position (see select_position), out of line:
+// its dense selection (every expert eligible) and the share of that
+// selection's raw score mass on the experts of support_mask. Returns whether
+// the position is under the coverage floor (on every lane).
+template <int EPL>
+__device__ __noinline__ bool coverage_under(const Dims &d, const float *v_in, const uint8_t *support_mask,
+                                            const float *bias, uint2 *scratch) {
+  const int lane = lane_id(), e0 = lane * EPL, k = d.k;
+  float v[EPL];
+  bool all[EPL];
+#pragma unroll
+  for (int c = 0; c < EPL; ++c) {
+    v[c] = v_in[c];
+    all[c] = e0 + c < d.E;
+  }
+  int dsel;
+  float dval, score;
+  if (d.router == 0) {
+    warp_topk<EPL>(v, all, k, &dsel, &dval, scratch);
+    float m = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < EPL; ++c) m = fmaxf(m, v[c]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float sum = 0.f;
+#pragma unroll
+    for (int c = 0; c < EPL; ++c) sum += e0 + c < d.E ? expf(v[c] - m) : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    score = lane < k ? expf(dval - m) / sum : 0.f;
+  } else {
+    float cs[EPL];
+#pragma unroll
+    for (int c = 0; c < EPL; ++c) cs[c] = e0 + c < d.E ? 1.f / (1.f + expf(-v[c])) + bias[e0 + c] : -INFINITY;
+    warp_group_limit<EPL>(cs, all, d.E, d.n_group, d.topk_group, k);
+    warp_topk<EPL>(cs, all, k, &dsel, &dval, scratch);
+    const int owner = dsel >= 0 ? dsel / EPL : 0, idx = dsel >= 0 ? dsel - owner * EPL : 0;
+    float z = 0.f;
+#pragma unroll
+    for (int c = 0; c < EPL; ++c) {
+      const float o = __shfl_sync(0xffffffffu, v[c], owner);
+      if (c == idx) z = o;
+    }
+    score = lane < k ? 1.f / (1.f + expf(-z)) : 0.f;
+  }
+  float mass = 0.f, covered = 0.f;
+  for (int j = 0; j < k; ++j) {  // in selection order
+    const float sj = __shfl_sync(0xffffffffu, score, j);
+    const int ej = __shfl_sync(0xffffffffu, dsel, j);
+    mass += sj;
+    if (ej >= 0 && support_mask[ej]) covered += sj;
+  }
+  return covered < d.cov_alpha * mass;
+}
+
 template <int EPL>
 __device__ __forceinline__ void select_position(const Dims &d, const Work &ws, int t, const float (&v)[EPL],
                                                 const uint8_t *support_mask, bool force, uint32_t *words,
@@ -152,26 +243,7 @@ __device__ __forceinline__ void select_position(const Dims &d, const Work &ws, i
       wgt = ex / denom;
     }
   } else {
-    float cs[EPL];
-#pragma unroll
-    for (int c = 0; c < EPL; ++c) {
-      const int e = e0 + c;
-      cs[c] = e < d.E ? 1.f / (1.f + expf(-v[c])) + bias[e] : -INFINITY;
-    }
-    warp_group_limit<EPL>(cs, ok, d.E, d.n_group, d.topk_group, k);
-    warp_topk<EPL>(cs, ok, k, &sel, &val, scratch);
-    // the selected expert's logit, from the lane that owns it
-    const int owner = sel >= 0 ? sel / EPL : 0, idx = sel >= 0 ? sel - owner * EPL : 0;
-    float z = 0.f;
-#pragma unroll
-    for (int c = 0; c < EPL; ++c) {
-      const float o = __shfl_sync(0xffffffffu, v[c], owner);
-      if (c == idx) z = o;
-    }
-    const float sg = lane < k ? 1.f / (1.f + expf(-z)) : 0.f;
-    float denom = 0.f;
-    for (int j = 0; j < k; ++j) denom += __shfl_sync(0xffffffffu, sg, j);
-    wgt = d.raw_weights ? sg : sg / denom;
+    select_sigmoid_group<EPL>(d, v, ok, bias, scratch, &sel, &wgt);
   }
   if (lane < k) {
     if (sel < 0 || sel >= d.E) {
@@ -183,51 +255,8 @@ __device__ __forceinline__ void select_position(const Dims &d, const Work &ws, i
       atomicOr(&words[static_cast<size_t>(sel) * d.cmax + (t >> 5)], 1u << (t & 31));
     }
   }
-  if (d.cov_check) {
-    // support coverage of t: its dense selection (every expert eligible) and
-    // the share of that selection's raw score mass on support experts
-    bool all[EPL];
-#pragma unroll
-    for (int c = 0; c < EPL; ++c) all[c] = e0 + c < d.E;
-    int dsel;
-    float dval, score;
-    if (d.router == 0) {
-      warp_topk<EPL>(v, all, k, &dsel, &dval, scratch);
-      float m = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < EPL; ++c) m = fmaxf(m, v[c]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      float sum = 0.f;
-#pragma unroll
-      for (int c = 0; c < EPL; ++c) sum += e0 + c < d.E ? expf(v[c] - m) : 0.f;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      score = lane < k ? expf(dval - m) / sum : 0.f;
-    } else {
-      float cs[EPL];
-#pragma unroll
-      for (int c = 0; c < EPL; ++c) cs[c] = e0 + c < d.E ? 1.f / (1.f + expf(-v[c])) + bias[e0 + c] : -INFINITY;
-      warp_group_limit<EPL>(cs, all, d.E, d.n_group, d.topk_group, k);
-      warp_topk<EPL>(cs, all, k, &dsel, &dval, scratch);
-      const int owner = dsel >= 0 ? dsel / EPL : 0, idx = dsel >= 0 ? dsel - owner * EPL : 0;
-      float z = 0.f;
-#pragma unroll
-      for (int c = 0; c < EPL; ++c) {
-        const float o = __shfl_sync(0xffffffffu, v[c], owner);
-        if (c == idx) z = o;
-      }
-      score = lane < k ? 1.f / (1.f + expf(-z)) : 0.f;
-    }
-    float mass = 0.f, covered = 0.f;
-    for (int j = 0; j < k; ++j) {  // in selection order
-      const float sj = __shfl_sync(0xffffffffu, score, j);
-      const int ej = __shfl_sync(0xffffffffu, dsel, j);
-      mass += sj;
-      if (ej >= 0 && support_mask[ej]) covered += sj;
-    }
-    if (lane == 0 && covered < d.cov_alpha * mass) atomicAdd(ws.cov_under, 1);
-  }
+  if (d.cov_check && coverage_under<EPL>(d, v, support_mask, bias, scratch) && lane == 0)
+    atomicAdd(ws.cov_under, 1);
 }
 
 // Per-iteration handshake state, set by block 0 of the kernel that classifies
