@@ -208,6 +208,25 @@ __device__ __noinline__ bool coverage_under(const Dims &d, const float *v_in, co
   return covered < d.cov_alpha * mass;
 }
 
+// Weight without renormalisation for the softmax router, out of line: the
+// dense router probability of the lane's selected logit val (softmax of the
+// row over every expert, eligible or not; lanes >= k get 0).
+template <int EPL>
+__device__ __noinline__ float dense_probability(const Dims &d, const float *v_in, float val) {
+  const int lane = lane_id(), e0 = lane * EPL;
+  float m = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < EPL; ++c) m = fmaxf(m, v_in[c]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float sum = 0.f;
+#pragma unroll
+  for (int c = 0; c < EPL; ++c) sum += e0 + c < d.E ? expf(v_in[c] - m) : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  return lane < d.k ? expf(val - m) / sum : 0.f;
+}
+
 template <int EPL>
 __device__ __forceinline__ void select_position(const Dims &d, const Work &ws, int t, const float (&v)[EPL],
                                                 const uint8_t *support_mask, bool force, uint32_t *words,
@@ -223,18 +242,8 @@ __device__ __forceinline__ void select_position(const Dims &d, const Work &ws, i
   float val, wgt;
   if (d.router == 0) {
     warp_topk<EPL>(v, ok, k, &sel, &val, scratch);
-    if (d.raw_weights) {  // dense router probability: softmax of the row over every expert
-      float m = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < EPL; ++c) m = fmaxf(m, v[c]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      float sum = 0.f;
-#pragma unroll
-      for (int c = 0; c < EPL; ++c) sum += e0 + c < d.E ? expf(v[c] - m) : 0.f;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      wgt = lane < k ? expf(val - m) / sum : 0.f;
+    if (d.raw_weights) {
+      wgt = dense_probability<EPL>(d, v, val);
     } else {
       const float top = __shfl_sync(0xffffffffu, val, 0);
       const float ex = lane < k ? expf(val - top) : 0.f;

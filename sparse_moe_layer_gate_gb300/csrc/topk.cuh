@@ -46,6 +46,51 @@ __device__ __forceinline__ void lane_logits(const float *__restrict__ row, int E
   for (int c = 0; c < EPL; ++c) v[c] = e0 + c < E ? __ldg(row + e0 + c) : -INFINITY;
 }
 
+// The general case of warp_topk, out of line (rare: more than 32 entries at or
+// above the threshold, or k > 16): k rounds, each taking the best remaining
+// lane best (a warp max, then the lowest lane holding it: lanes own ascending
+// id ranges, so that is the lowest id). key: this lane's EPL keys (0:
+// ineligible).
+template <int EPL>
+__device__ __noinline__ void warp_topk_rounds(const unsigned *key_in, int k, int *my_sel, float *my_val) {
+  constexpr unsigned kAll = 0xffffffffu;
+  const int lane = lane_id();
+  unsigned key[EPL];
+#pragma unroll
+  for (int c = 0; c < EPL; ++c) key[c] = key_in[c];
+  unsigned bk = key[0];
+  int bc = 0;
+#pragma unroll
+  for (int c = 1; c < EPL; ++c)
+    if (key[c] > bk) {
+      bk = key[c];
+      bc = c;
+    }
+  for (int j = 0; j < k; ++j) {
+    const unsigned best = __reduce_max_sync(kAll, bk);
+    const unsigned hold = __ballot_sync(kAll, bk == best && bk != 0u);
+    const int win = __ffs(hold) - 1;  // -1: nothing eligible is left
+    const int wsel = __shfl_sync(kAll, lane * EPL + bc, win < 0 ? 0 : win);
+    if (lane == j && win >= 0) {
+      *my_sel = wsel;
+      *my_val = key_value(best);
+    }
+    if (lane == win) {  // take the entry, then this lane's next best
+#pragma unroll
+      for (int c = 0; c < EPL; ++c)
+        if (c == bc) key[c] = 0u;
+      bk = key[0];
+      bc = 0;
+#pragma unroll
+      for (int c = 1; c < EPL; ++c)
+        if (key[c] > bk) {
+          bk = key[c];
+          bc = c;
+        }
+    }
+  }
+}
+
 // Top-k of one position by one warp. Lane l owns the EPL experts
 // [l*EPL, l*EPL + EPL) with logits v; entries with ok false never win. Every
 // comparison is on (order key desc, id asc). `scratch` is 32 entries of
@@ -134,29 +179,7 @@ __device__ __forceinline__ void warp_topk(const float (&v)[EPL], const bool (&ok
       return;
     }
   }
-  for (int j = 0; j < k; ++j) {
-    const unsigned best = __reduce_max_sync(kAll, bk);
-    const unsigned hold = __ballot_sync(kAll, bk == best && bk != 0u);
-    const int win = __ffs(hold) - 1;  // -1: nothing eligible is left
-    const int wsel = __shfl_sync(kAll, lane * EPL + bc, win < 0 ? 0 : win);
-    if (lane == j && win >= 0) {
-      *my_sel = wsel;
-      *my_val = key_value(best);
-    }
-    if (lane == win) {  // take the entry, then this lane's next best
-#pragma unroll
-      for (int c = 0; c < EPL; ++c)
-        if (c == bc) key[c] = 0u;
-      bk = key[0];
-      bc = 0;
-#pragma unroll
-      for (int c = 1; c < EPL; ++c)
-        if (key[c] > bk) {
-          bk = key[c];
-          bc = c;
-        }
-    }
-  }
+  warp_topk_rounds<EPL>(key, k, my_sel, my_val);
 }
 
 // Group-limited eligibility (the group rule of sigmoid routers): the E experts
