@@ -356,8 +356,8 @@ __device__ __forceinline__ void gate_tail(const Dims &d, const Work &ws, const u
 // by one thread of the combine kernel (which runs once the expert kernel, and
 // so the gate, has completed): the tallies every gate CTA added (they restart
 // for the next call), the coverage count, and the values gate CTA 0 left in
-// the control block.
-__device__ __forceinline__ void gate_tail_stats(const Dims &d, const Work &ws) {
+// the control block. Out of line: one CTA of the combine runs it.
+static __device__ __noinline__ void gate_tail_stats(const Dims &d, const Work &ws) {
   const int n = d.n_pos, E = d.E, k = d.k;
   int tl[kTallies];
 #pragma unroll
