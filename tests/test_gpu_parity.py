@@ -142,6 +142,21 @@ def test_every_expert_eligible_at_2048_positions():
     assert_clean(block_parity(synth.sweep_workload(64, 1.0, 4), n_iters=2))
 
 
+def test_multi_wave_gate_uses_the_worklist_kernel():
+    """4096 positions: the gate's clusters no longer fit in one wave, so the
+    gate cannot build the worklist behind its grid barrier; the worklist
+    kernel builds it (copying the rows for the tensor-core experts) on the
+    normal iteration path."""
+    wl = synth.sweep_workload(128, 0.95, 4).replace(name="mini_4096_positions", iters=3)
+    lay = layer_for_workload(wl)
+    lay.set_profiling(True)
+    assert_clean(block_parity(wl, n_iters=3, layers=[lay]))
+    prof = lay.read_profile()
+    lay.set_profiling(False)
+    assert prof.get("routing", {}).get("launches", 0) == 3, prof
+    lay.close()
+
+
 def test_wide_router_320_experts():
     """E = 320 > 256: the gate's wider per-lane top-k and larger partial-sum
     tiles (three 128-expert MMA blocks per tile)."""
