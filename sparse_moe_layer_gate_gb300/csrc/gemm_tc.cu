@@ -1,27 +1,31 @@
 // tcgen05 + TMA GEMMs of the Epoch MoE layer (bf16 in, fp32 accumulate).
 //
-// Two persistent, warp-specialised kernels:
-//   k_tc_gate     G = x W_r^T + b for every position, one CTA per (128
-//                 experts, 32 tokens) tile over all of H ([W] section "Expert
-//                 Atlas": G in R^{N x E}, recomputed every iteration);
-//   k_tc_experts  per group g, UP: A_g = silu(X_g W_gate,g^T) * (X_g W_up,g^T)
-//                 and DOWN: O_g = A_g W_down,g^T, both stored as bf16, in one
-//                 launch with per-group dependencies.
+// Two warp-specialised kernels:
+//   k_tc_gate     G = x W_r^T + b for every position: clusters of CTAs split
+//                 H, each CTA an (E, position tile) MMA over its slice, the
+//                 partials summed over distributed shared memory ([W] section
+//                 "Expert Atlas": G in R^{N x E}, recomputed every iteration);
+//                 then the classification and top-k of every position, and
+//                 the iteration's worklist in the kernel's own tail
+//                 (gate_tail.cuh);
+//   k_tc_experts  persistent, per group g, UP: A_g = silu(X_g W_gate,g^T) *
+//                 (X_g W_up,g^T) and DOWN: O_g = A_g W_down,g^T, both stored as
+//                 bf16, in one launch with per-group dependencies.
 // Groups are the routed experts with at least one worklist row and the shared
 // experts over every position; each routed expert runs once over its compact
 // rows (the "light-traffic expert kernel" of [W] section "FreshLane
 // Dispatch"); experts with no row produce no tile, so their weights are never
-// read ("invalid slots load no expert weights", same section).
+// read (no weight loads for empty slots, same section).
 // [W] = walk-through page "Epoch 完全拆解:把扩散块编译成稀疏 MoE 服务单元".
 //
 // Swap-AB: weight rows are the MMA M dimension (128) and tokens the N
 // dimension (16..128, rounded up to 16 per tile), because an expert may hold
-// from one to a thousand rows. Roles per CTA (192 threads): warp 0 issues the
-// operand copies into a shared-memory ring (128-byte swizzle, K-major), warp 1
-// issues tcgen05.mma into TMEM accumulators (double-buffered, so the epilogue
-// of one tile overlaps the next tile's main loop), warps 2-5 read TMEM with
-// tcgen05.ld and store. One CTA per SM, persistent over a device-resident tile
-// count: no host synchronisation.
+// from one to a thousand rows. Roles per expert CTA (192 threads): warp 0
+// issues the operand copies into a shared-memory ring (128-byte swizzle,
+// K-major), warp 1 issues tcgen05.mma into TMEM accumulators (double-buffered,
+// so the epilogue of one tile overlaps the next tile's main loop), warps 2-5
+// read TMEM with tcgen05.ld and store. One CTA per SM, persistent over
+// device-resident tile counters: no host synchronisation.
 #include <cudaTypedefs.h>
 
 #include <cstring>
@@ -36,7 +40,7 @@ namespace epoch {
 constexpr int BM = 128;
 constexpr int BK = 64;
 
-// Rows of the per-CTA trace: 0 gate, 1 experts, 2 expert epilogue (the worklist kernel uses row 3).
+// Rows of the per-CTA trace: 0 gate, 1 experts, 2 expert epilogue (the gate's worklist tail uses rows 3 and 8).
 constexpr int kTraceRowGate = 0;
 constexpr int kTraceRowExperts = 1;
 constexpr int kTraceRowEpilogue = 2;  // expert-kernel epilogue summary
@@ -417,18 +421,21 @@ __global__ void __maxnreg__(104) k_tc_gate(const __grid_constant__ GateParams p)
 }
 
 // ---------------------------------------------------------------- fused expert kernel
-// Up and down projections of every group in one persistent cooperative launch
-// (one CTA per SM). Tiles of the list [all up tiles, then all down tiles] are
-// handed out one at a time from a global counter, so a CTA that drew short
-// tiles draws more. Both kinds are two 128-row MMAs sharing one token tile of
-// <= 128 tokens: an up tile (group g, 128 rows of I) multiplies the gate and up
-// rows and writes silu(gate) * up as bf16, then counts itself done for g; a
-// down tile (g, 256 rows of H) waits until every up tile of g is done before
-// loading its activations (its weight copies go out first), so the down work of
-// lightly loaded experts runs while heavy up tiles are still streaming, with no
-// launch in between. Every tile uses one 256-column TMEM accumulator buffer,
-// double-buffered; a 48 KB stage holds 32 KB of packed weights (one contiguous
-// run) and a 16 KB token tile.
+// Up and down projections of every group in one persistent launch (one CTA
+// per SM). The shared experts' up tiles are drawn from their own counter from
+// the launch on (they need only the layer input); once the worklist is
+// complete, one counter hands out [routed up tiles, shared down tiles, routed
+// down tiles] one at a time, so a CTA that drew short tiles draws more. Both
+// kinds are two 128-row MMAs sharing one token tile of <= 128 tokens: an up
+// tile (group g, 128 rows of I) multiplies the gate and up rows and writes
+// silu(gate) * up as bf16, then counts itself done for (g, its row block of
+// I); a down tile (g, 256 rows of H) issues its first weight copies, then
+// loads its activations one row block of I at a time as the group's up tiles
+// of that row block complete, so the down work of lightly loaded experts runs
+// while heavy up tiles are still streaming, with no launch in between. Every
+// tile uses one 256-column TMEM accumulator buffer, double-buffered; a 48 KB
+// stage holds 32 KB of packed weights (one contiguous run) and a 16 KB token
+// tile.
 constexpr int kExpStages = 4;
 constexpr int kExpStage = 48 * 1024;
 constexpr int kExpStg = 32 * 80;  // epilogue staging per warp: 32 tokens x 32 bf16 rows, padded
