@@ -6,6 +6,7 @@ or a special case that reduces to the plain dense MoE formula computed in a
 different arrangement. The mutation tests at the end plant plausible mistakes
 in the oracle and check that some pin catches each one.
 """
+import dataclasses
 import itertools
 import math
 import os
@@ -43,7 +44,8 @@ def load_schedules():
             else:
                 kv = dict(zip(tok[0::2], tok[1::2]))
                 cur["steps"].append(dict(i=int(kv["i"]), decoded=[int(c) for c in kv["decoded"]],
-                                         fresh=_ints(kv["fresh"]), fallback=int(kv["fallback"])))
+                                         fresh=_ints(kv["fresh"]), fallback=int(kv["fallback"]),
+                                         cats=[int(c) for c in kv["cats"].split("/")]))
     return scheds
 
 
@@ -240,6 +242,8 @@ def test_fresh_schedules_golden(sched):
         res = lay.iterate(x + 0.01 * st["i"], 1 - dec, dec, st["i"])
         assert list(res.fresh_pos) == st["fresh"], (sched["name"], st)
         assert int(res.fallback) == st["fallback"], (sched["name"], st)
+        cl = res.classified
+        assert [cl.n_live, cl.n_new, cl.n_miss, cl.n_stale, cl.n_forced, cl.n_reuse] == st["cats"], (sched["name"], st)
 
 
 # ------------------------------------------------------------------ dense special case
@@ -865,6 +869,12 @@ def _mut_stale_strict(live, decoded, prev, stamp, i, R, force):
 CLASSIFY_ORIG = om.classify_positions
 
 
+def _mut_forced_counted_as_reuse(live, decoded, prev, stamp, i, R, force):
+    """Same fresh set, but positions a fallback made fresh are tallied as reused."""
+    cl = CLASSIFY_ORIG(live, decoded, prev, stamp, i, R, force)
+    return dataclasses.replace(cl, n_forced=0, n_reuse=cl.n_reuse + cl.n_forced)
+
+
 def _mut_group_top1(c, eligible, n_group):
     E = c.shape[0]
     gs = E // n_group
@@ -918,6 +928,7 @@ def _mut_sigmoid_neg(z):
     ("weights not renormalised", "renorm_softmax", _mut_softmax_unnormalised),
     ("support one too long", "plan_support", _mut_plan_off_by_one),
     ("refresh one iteration late", "classify_positions", _mut_stale_strict),
+    ("fallback positions tallied as reused", "classify_positions", _mut_forced_counted_as_reuse),
     ("group score from the best expert only", "group_scores", _mut_group_top1),
     ("groups not extended to k eligible experts", "chosen_groups", _mut_groups_ignore_k),
     ("sigmoid of -G", "sigmoid", _mut_sigmoid_neg),
