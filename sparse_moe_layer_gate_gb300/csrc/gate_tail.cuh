@@ -123,185 +123,214 @@ __device__ __forceinline__ void gate_tail(const Dims &d, const Work &ws, const u
   if (tid == 0) {
     // (the generation read at the kernel's start cannot have moved: the barrier
     // is released only after this CTA has arrived)
-    int32_t *count = ws.gate_arrive, *gen = ws.gate_arrive + 1;
-    const int g0 = gt.gen0;
     int arrived;
     // release: this CTA's selections, words and tallies; acquire (the last
     // CTA): every other CTA's, before it releases the rest
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(arrived) : "l"(count) : "memory");
-    int ok = 1;
-    if (arrived == static_cast<int>(gridDim.x) - 1) {
-      asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(gen), "r"(g0 + 1) : "memory");
-    } else {
-      const uint64_t t0 = globaltimer_ns();
-      for (;;) {
-        int v;
-        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(gen) : "memory");
-        if (v != g0) break;
-        if (globaltimer_ns() - t0 > static_cast<uint64_t>(d.timeout_ns)) {
-          set_error(ws.err, EPOCH_DEVERR_TIMEOUT);
-          ok = 0;
-          break;
-        }
-        __nanosleep(64);
-      }
-    }
-    if (ok && blockIdx.x == 0) *count = 0;
-    s_misc[40] = ok;
-    if (trace) trace[1] = static_cast<int64_t>(globaltimer_ns());
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(arrived) : "l"(ws.gate_arrive) : "memory");
+    if (arrived == static_cast<int>(gridDim.x) - 1)
+      asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(ws.gate_arrive + 1), "r"(gt.gen0 + 1) : "memory");
+    s_misc[41] = arrived;
   }
   __syncthreads();
-  const bool ok = s_misc[40] != 0;
-
-  // ---- 2. the candidates' words, one round of loads: rows per expert, bits
-  // before p0 and the words covering the own positions, per candidate. Items
-  // are (candidate, block of 32 words); lane l loads word l of an item.
-  const uint32_t *words = ws.sel_words + static_cast<size_t>((d.state_rd & 1) ^ 1) * E * cmax;
-  const int nch = (n + 31) >> 5, nwb = (nch + 31) >> 5, wa = p0 >> 5;
-  const uint32_t m0 = (1u << (p0 & 31)) - 1u;
-  const int items = ok ? n_cand * nwb : 0;
-  for (int i0 = wid; i0 < items; i0 += nw * 4) {
-    uint32_t v[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int it = i0 + u * nw;
-      v[u] = 0u;
-      if (it < items) {
-        const int ci = it / nwb, w = (it - ci * nwb) * 32 + lane;
-        if (w < nch) v[u] = __ldcg(words + static_cast<size_t>(cand_of(ci)) * cmax + w);
+  const int arrived = s_misc[41];
+  const bool last = arrived == static_cast<int>(gridDim.x) - 1;
+  // Steps 2-4 run once after the barrier. The first CTA to arrive also runs
+  // them before it, on the words as they stand, with every global write and
+  // error check off and its scratch zeroed again afterwards: the other CTAs
+  // then find these instructions in L2 (the input flush between iterations
+  // evicts code too), not in HBM, when they run the steps for real.
+  bool ok = true;
+  int n_tiles = 0, n_hit = 0;
+#pragma unroll 1
+  for (int pass = arrived == 0 && !last ? 0 : 1; pass < 2; ++pass) {
+    const bool dry = pass == 0;
+    if (!dry) {
+      if (tid == 0) {
+        int pass_ok = 1;
+        if (!last) {
+          const uint64_t t0 = globaltimer_ns();
+          for (;;) {
+            int v;
+            asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ws.gate_arrive + 1) : "memory");
+            if (v != gt.gen0) break;
+            if (globaltimer_ns() - t0 > static_cast<uint64_t>(d.timeout_ns)) {
+              set_error(ws.err, EPOCH_DEVERR_TIMEOUT);
+              pass_ok = 0;
+              break;
+            }
+            __nanosleep(64);
+          }
+        }
+        if (pass_ok && blockIdx.x == 0) ws.gate_arrive[0] = 0;
+        s_misc[40] = pass_ok;
+        if (trace) trace[1] = static_cast<int64_t>(globaltimer_ns());
       }
+      __syncthreads();
+      ok = s_misc[40] != 0;
     }
+
+    // ---- 2. the candidates' words, one round of loads: rows per expert, bits
+    // before p0 and the words covering the own positions, per candidate. Items
+    // are (candidate, block of 32 words); lane l loads word l of an item.
+    const uint32_t *words = ws.sel_words + static_cast<size_t>((d.state_rd & 1) ^ 1) * E * cmax;
+    const int nch = (n + 31) >> 5, nwb = (nch + 31) >> 5, wa = p0 >> 5;
+    const uint32_t m0 = (1u << (p0 & 31)) - 1u;
+    const int items = ok ? n_cand * nwb : 0;
+    for (int i0 = wid; i0 < items; i0 += nw * 4) {
+      uint32_t v[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int it = i0 + u * nw;
-      if (it < items) {  // the same for every lane of the warp
-        const int ci = it / nwb, w = (it - ci * nwb) * 32 + lane;
-        const int tot = __reduce_add_sync(0xffffffffu, __popc(v[u]));
-        const int bef = __reduce_add_sync(0xffffffffu, __popc(w < wa ? v[u] : (w == wa ? v[u] & m0 : 0u)));
-        if (w >= wa && w < wa + 3) s_own[3 * ci + (w - wa)] = v[u];
-        if (lane == 0) {
-          if (tot) atomicAdd(&s_off[cand_of(ci)], tot);
-          if (bef) atomicAdd(&s_bef[ci], bef);
+      for (int u = 0; u < 4; ++u) {
+        const int it = i0 + u * nw;
+        v[u] = 0u;
+        if (it < items) {
+          const int ci = it / nwb, w = (it - ci * nwb) * 32 + lane;
+          if (w < nch) v[u] = __ldcg(words + static_cast<size_t>(cand_of(ci)) * cmax + w);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int it = i0 + u * nw;
+        if (it < items) {  // the same for every lane of the warp
+          const int ci = it / nwb, w = (it - ci * nwb) * 32 + lane;
+          const int tot = __reduce_add_sync(0xffffffffu, __popc(v[u]));
+          const int bef = __reduce_add_sync(0xffffffffu, __popc(w < wa ? v[u] : (w == wa ? v[u] & m0 : 0u)));
+          if (w >= wa && w < wa + 3) s_own[3 * ci + (w - wa)] = v[u];
+          if (lane == 0) {
+            if (tot) atomicAdd(&s_off[cand_of(ci)], tot);
+            if (bef) atomicAdd(&s_bef[ci], bef);
+          }
         }
       }
     }
-  }
-  __syncthreads();
-  if (trace && tid == 0) trace[2] = static_cast<int64_t>(globaltimer_ns());
+    __syncthreads();
+    if (trace && tid == 0) trace[2] = static_cast<int64_t>(globaltimer_ns());
 
-  // ---- 3. one scan over the experts in id order: the expert offsets and,
-  // per row-count class of the expert kernel's group list (2: >= 96 rows, 1:
-  // >= 32, 0: fewer; listed in that order, by id within a class), each
-  // expert's list position and the token tiles of the entries before it
-  // (scan components: .x rows, .y experts of class 0 | class 1 << 16, .z
-  // experts of class 2 | its tiles << 16, .w tiles of class 0 | class 1 << 16).
-  // CTA 0 publishes the offsets and the list.
-  auto cls_of = [](int r) { return r >= 96 ? 2 : r >= 32 ? 1 : 0; };
-  const int tn = d.tn > 0 ? d.tn : 1;
-  int n_tiles, n_hit = 0;
-  {
-    int b = 0;
-    for (int c = tid; c < n_cand; c += nthr) b += s_bef[c];
-    b = __reduce_add_sync(0xffffffffu, b);
-    if (lane == 0 && b) atomicAdd(&s_misc[36], b);
-    const int gpt = (E + nthr - 1) / nthr, e0 = tid * gpt;
-    int4 v = make_int4(0, 0, 0, 0);
-    int hm = 0;  // bit h: expert e0 + h has rows
-    for (int h = 0; h < gpt && e0 + h < E; ++h) {
-      const int r = s_off[e0 + h], c2 = cls_of(r), nt = (r + tn - 1) / tn;
-      hm |= (r > 0 ? 1 : 0) << h;
-      v.x += r;
-      if (c2 == 0) {
-        v.y += 1;
-        v.w += nt;
-      } else if (c2 == 1) {
-        v.y += 1 << 16;
-        v.w += nt << 16;
-      } else {
-        v.z += 1 | (nt << 16);
+    // ---- 3. one scan over the experts in id order: the expert offsets and,
+    // per row-count class of the expert kernel's group list (2: >= 96 rows, 1:
+    // >= 32, 0: fewer; listed in that order, by id within a class), each
+    // expert's list position and the token tiles of the entries before it
+    // (scan components: .x rows, .y experts of class 0 | class 1 << 16, .z
+    // experts of class 2 | its tiles << 16, .w tiles of class 0 | class 1 << 16).
+    // CTA 0 publishes the offsets and the list.
+    auto cls_of = [](int r) { return r >= 96 ? 2 : r >= 32 ? 1 : 0; };
+    const int tn = d.tn > 0 ? d.tn : 1;
+    n_hit = 0;
+    {
+      int b = 0;
+      for (int c = tid; c < n_cand; c += nthr) b += s_bef[c];
+      b = __reduce_add_sync(0xffffffffu, b);
+      if (lane == 0 && b) atomicAdd(&s_misc[36], b);
+      const int gpt = (E + nthr - 1) / nthr, e0 = tid * gpt;
+      int4 v = make_int4(0, 0, 0, 0);
+      int hm = 0;  // bit h: expert e0 + h has rows
+      for (int h = 0; h < gpt && e0 + h < E; ++h) {
+        const int r = s_off[e0 + h], c2 = cls_of(r), nt = (r + tn - 1) / tn;
+        hm |= (r > 0 ? 1 : 0) << h;
+        v.x += r;
+        if (c2 == 0) {
+          v.y += 1;
+          v.w += nt;
+        } else if (c2 == 1) {
+          v.y += 1 << 16;
+          v.w += nt << 16;
+        } else {
+          v.z += 1 | (nt << 16);
+        }
+      }
+      int4 tot;
+      const Group g{tid, nthr, 0};
+      const int4 ex = group_excl_scan4(g, v, s_scan, &tot);
+      const int n2 = tot.z & 0xffff, n1 = tot.y >> 16;
+      const int t2 = tot.z >> 16, t1 = tot.w >> 16;
+      n_tiles = t2 + t1 + (tot.w & 0xffff);
+      int rank0 = ex.y & 0xffff, rank1 = ex.y >> 16, rank2 = ex.z & 0xffff;
+      int tb0 = ex.w & 0xffff, tb1 = ex.w >> 16, tb2 = ex.z >> 16;
+      int run = ex.x;
+      const bool publish = blockIdx.x == 0 && ok && !dry;
+      for (int h = 0; h < gpt && e0 + h < E; ++h) {
+        const int e = e0 + h, r = s_off[e], c2 = cls_of(r), nt = (r + tn - 1) / tn;
+        s_off[e] = run;
+        if (publish) {
+          ws.offsets[e] = run;
+          if (c2 == 2) ws.grp_list[rank2++] = (tb2 << kGrpIdBits) | e;
+          else if (c2 == 1) ws.grp_list[n2 + rank1++] = ((t2 + tb1) << kGrpIdBits) | e;
+          else ws.grp_list[n2 + n1 + rank0++] = ((t2 + t1 + tb0) << kGrpIdBits) | e;
+        }
+        tb2 += c2 == 2 ? nt : 0;
+        tb1 += c2 == 1 ? nt : 0;
+        tb0 += c2 == 0 ? nt : 0;
+        run += r;
+      }
+      if (tid == 0) {
+        s_off[E] = tot.x;
+        if (publish) {
+          ws.offsets[E] = tot.x;
+          ws.grp_list[E] = n_tiles << kGrpIdBits;
+        }
+      }
+      for (int h = 0; h < gpt; ++h) n_hit += __syncthreads_count((hm >> h) & 1);  // (also a barrier)
+    }
+    if (trace && tid == 0) trace[4] = static_cast<int64_t>(globaltimer_ns());
+    const bool real = ok && !dry;  // global writes and error checks
+    if (real && s_off[E] > d.Nmax * k && tid == 0) set_error(ws.err, EPOCH_DEVERR_BOUNDS);  // inconsistent words
+
+    // ---- 4. the own positions: fresh index and list, slots
+    if (real && wid == 0) {
+      int f = s_misc[36] / k;  // fresh positions before p0 (each sets k bits)
+      for (int j0 = 0; j0 < np; j0 += 32) {
+        const int j = j0 + lane;
+        const bool fr = j < np && gt.fr[j];
+        const unsigned m = __ballot_sync(0xffffffffu, fr);
+        if (j < np) {
+          const int mine = f + __popc(m & ((1u << lane) - 1u));
+          ws.fidx[p0 + j] = fr ? mine : -1;
+          if (fr && mine < d.Nmax) ws.fresh_pos[mine] = p0 + j;
+        }
+        f += __popc(m);
       }
     }
-    int4 tot;
-    const Group g{tid, nthr, 0};
-    const int4 ex = group_excl_scan4(g, v, s_scan, &tot);
-    const int n2 = tot.z & 0xffff, n1 = tot.y >> 16;
-    const int t2 = tot.z >> 16, t1 = tot.w >> 16;
-    n_tiles = t2 + t1 + (tot.w & 0xffff);
-    int rank0 = ex.y & 0xffff, rank1 = ex.y >> 16, rank2 = ex.z & 0xffff;
-    int tb0 = ex.w & 0xffff, tb1 = ex.w >> 16, tb2 = ex.z >> 16;
-    int run = ex.x;
-    const bool publish = blockIdx.x == 0 && ok;
-    for (int h = 0; h < gpt && e0 + h < E; ++h) {
-      const int e = e0 + h, r = s_off[e], c2 = cls_of(r), nt = (r + tn - 1) / tn;
-      s_off[e] = run;
-      if (publish) {
-        ws.offsets[e] = run;
-        if (c2 == 2) ws.grp_list[rank2++] = (tb2 << kGrpIdBits) | e;
-        else if (c2 == 1) ws.grp_list[n2 + rank1++] = ((t2 + tb1) << kGrpIdBits) | e;
-        else ws.grp_list[n2 + n1 + rank0++] = ((t2 + t1 + tb0) << kGrpIdBits) | e;
+    const int r0 = p0 & 31;
+    for (int q = tid; q < np * k; q += nthr) {
+      const int j = q / k, jj = q - j * k, t = p0 + j;
+      int slot = -1;
+      if (ok && gt.fr[j]) {
+        const int e = gt.sel[j * 16 + jj];
+        const int ci = (e >= 0 && e < E) ? (force ? e : gt.cidx[e]) : -1;
+        if (ci < 0 || ci >= n_cand || cand_of(ci) != e) {
+          if (real) set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+        } else {
+          const int rt = t - (wa << 5);  // bit of t counted from word wa (< 96)
+          int rank = s_bef[ci];
+#pragma unroll
+          for (int w = 0; w < 3; ++w) {
+            const int lo = max(r0 - 32 * w, 0), hi = min(rt - 32 * w, 32);
+            if (hi > lo) rank += __popc(s_own[3 * ci + w] & bit_range(lo, hi));
+          }
+          slot = s_off[e] + rank;
+          if (slot >= s_off[e + 1] || slot >= d.Nmax * k) {
+            if (real) set_error(ws.err, EPOCH_DEVERR_BOUNDS);
+            slot = -1;
+          }
+        }
+        if (real) {
+          ws.slot[static_cast<size_t>(t) * k + jj] = slot >= 0 ? slot : 0;
+          if (slot >= 0) ws.wl_pos[slot] = t;
+        }
       }
-      tb2 += c2 == 2 ? nt : 0;
-      tb1 += c2 == 1 ? nt : 0;
-      tb0 += c2 == 0 ? nt : 0;
-      run += r;
+      s_slot[q] = slot;
     }
-    if (tid == 0) {
-      s_off[E] = tot.x;
-      if (publish) {
-        ws.offsets[E] = tot.x;
-        ws.grp_list[E] = n_tiles << kGrpIdBits;
+    __syncthreads();
+    if (dry) {  // the scratch the real pass accumulates into starts at zero again
+      for (int e = tid; e <= E; e += nthr) s_off[e] = 0;
+      for (int c = tid; c < n_cand; c += nthr) {
+        s_bef[c] = 0;
+        s_own[3 * c] = s_own[3 * c + 1] = s_own[3 * c + 2] = 0u;
       }
+      if (tid == 0) s_misc[36] = 0;
+      __syncthreads();
     }
-    for (int h = 0; h < gpt; ++h) n_hit += __syncthreads_count((hm >> h) & 1);  // (also a barrier)
   }
-  if (trace && tid == 0) trace[4] = static_cast<int64_t>(globaltimer_ns());
   const int n_edges = s_off[E];
-  if (ok && n_edges > d.Nmax * k && tid == 0) set_error(ws.err, EPOCH_DEVERR_BOUNDS);  // inconsistent words
-
-  // ---- 4. the own positions: fresh index and list, slots
-  if (ok && wid == 0) {
-    int f = s_misc[36] / k;  // fresh positions before p0 (each sets k bits)
-    for (int j0 = 0; j0 < np; j0 += 32) {
-      const int j = j0 + lane;
-      const bool fr = j < np && gt.fr[j];
-      const unsigned m = __ballot_sync(0xffffffffu, fr);
-      if (j < np) {
-        const int mine = f + __popc(m & ((1u << lane) - 1u));
-        ws.fidx[p0 + j] = fr ? mine : -1;
-        if (fr && mine < d.Nmax) ws.fresh_pos[mine] = p0 + j;
-      }
-      f += __popc(m);
-    }
-  }
-  const int r0 = p0 & 31;
-  for (int q = tid; q < np * k; q += nthr) {
-    const int j = q / k, jj = q - j * k, t = p0 + j;
-    int slot = -1;
-    if (ok && gt.fr[j]) {
-      const int e = gt.sel[j * 16 + jj];
-      const int ci = (e >= 0 && e < E) ? (force ? e : gt.cidx[e]) : -1;
-      if (ci < 0 || ci >= n_cand || cand_of(ci) != e) {
-        set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-      } else {
-        const int rt = t - (wa << 5);  // bit of t counted from word wa (< 96)
-        int rank = s_bef[ci];
-#pragma unroll
-        for (int w = 0; w < 3; ++w) {
-          const int lo = max(r0 - 32 * w, 0), hi = min(rt - 32 * w, 32);
-          if (hi > lo) rank += __popc(s_own[3 * ci + w] & bit_range(lo, hi));
-        }
-        slot = s_off[e] + rank;
-        if (slot >= s_off[e + 1] || slot >= d.Nmax * k) {
-          set_error(ws.err, EPOCH_DEVERR_BOUNDS);
-          slot = -1;
-        }
-      }
-      ws.slot[static_cast<size_t>(t) * k + jj] = slot >= 0 ? slot : 0;
-      if (slot >= 0) ws.wl_pos[slot] = t;
-    }
-    s_slot[q] = slot;
-  }
-  __syncthreads();
   if (trace && tid == 0) trace[5] = static_cast<int64_t>(globaltimer_ns());
 
   // ---- 5. the worklist rows: each staged row to its k rows of xp (the
