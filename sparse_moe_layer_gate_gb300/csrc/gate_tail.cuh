@@ -134,15 +134,21 @@ __device__ __forceinline__ void gate_tail(const Dims &d, const Work &ws, const u
   __syncthreads();
   const int arrived = s_misc[41];
   const bool last = arrived == static_cast<int>(gridDim.x) - 1;
-  // Steps 2-4 run once after the barrier. The first CTA to arrive also runs
-  // them before it, on the words as they stand, with every global write and
-  // error check off and its scratch zeroed again afterwards: the other CTAs
-  // then find these instructions in L2 (the input flush between iterations
-  // evicts code too), not in HBM, when they run the steps for real.
+  // Steps 2-4 run once after the barrier. The first three CTAs to arrive
+  // (not the last) also run one of them each before it -- step 2, 3 or 4 by
+  // arrival -- on the data as it stands, with every global write and error
+  // check off and their scratch zeroed again afterwards: the other CTAs then
+  // find these instructions in L2 (the input flush between iterations evicts
+  // code too), not in HBM, when they run the steps for real. One step each
+  // keeps every warm-up short enough to end before the barrier opens.
+  const int dmask = last || arrived > 2 ? 0 : 1 << arrived;
   bool ok = true;
   int n_tiles = 0, n_hit = 0;
+  const uint32_t *words = ws.sel_words + static_cast<size_t>((d.state_rd & 1) ^ 1) * E * cmax;
+  const int nch = (n + 31) >> 5, nwb = (nch + 31) >> 5, wa = p0 >> 5;
+  const uint32_t m0 = (1u << (p0 & 31)) - 1u;
 #pragma unroll 1
-  for (int pass = arrived == 0 && !last ? 0 : 1; pass < 2; ++pass) {
+  for (int pass = dmask ? 0 : 1; pass < 2; ++pass) {
     const bool dry = pass == 0;
     if (!dry) {
       if (tid == 0) {
@@ -172,10 +178,7 @@ __device__ __forceinline__ void gate_tail(const Dims &d, const Work &ws, const u
     // ---- 2. the candidates' words, one round of loads: rows per expert, bits
     // before p0 and the words covering the own positions, per candidate. Items
     // are (candidate, block of 32 words); lane l loads word l of an item.
-    const uint32_t *words = ws.sel_words + static_cast<size_t>((d.state_rd & 1) ^ 1) * E * cmax;
-    const int nch = (n + 31) >> 5, nwb = (nch + 31) >> 5, wa = p0 >> 5;
-    const uint32_t m0 = (1u << (p0 & 31)) - 1u;
-    const int items = ok ? n_cand * nwb : 0;
+    const int items = ok && (!dry || (dmask & 1)) ? n_cand * nwb : 0;
     for (int i0 = wid; i0 < items; i0 += nw * 4) {
       uint32_t v[4];
 #pragma unroll
@@ -215,7 +218,7 @@ __device__ __forceinline__ void gate_tail(const Dims &d, const Work &ws, const u
     auto cls_of = [](int r) { return r >= 96 ? 2 : r >= 32 ? 1 : 0; };
     const int tn = d.tn > 0 ? d.tn : 1;
     n_hit = 0;
-    {
+    if (!dry || (dmask & 2)) {
       int b = 0;
       for (int c = tid; c < n_cand; c += nthr) b += s_bef[c];
       b = __reduce_add_sync(0xffffffffu, b);
@@ -274,14 +277,16 @@ __device__ __forceinline__ void gate_tail(const Dims &d, const Work &ws, const u
     const bool real = ok && !dry;  // global writes and error checks
     if (real && s_off[E] > d.Nmax * k && tid == 0) set_error(ws.err, EPOCH_DEVERR_BOUNDS);  // inconsistent words
 
-    // ---- 4. the own positions: fresh index and list, slots
-    if (real && wid == 0) {
+    // ---- 4. the own positions: fresh index and list, slots (a warm-up runs
+    // the slot arithmetic for every own position, fresh or not)
+    const bool step4 = ok && (!dry || (dmask & 4));
+    if (step4 && wid == 0) {
       int f = s_misc[36] / k;  // fresh positions before p0 (each sets k bits)
       for (int j0 = 0; j0 < np; j0 += 32) {
         const int j = j0 + lane;
         const bool fr = j < np && gt.fr[j];
         const unsigned m = __ballot_sync(0xffffffffu, fr);
-        if (j < np) {
+        if (j < np && real) {
           const int mine = f + __popc(m & ((1u << lane) - 1u));
           ws.fidx[p0 + j] = fr ? mine : -1;
           if (fr && mine < d.Nmax) ws.fresh_pos[mine] = p0 + j;
@@ -290,10 +295,10 @@ __device__ __forceinline__ void gate_tail(const Dims &d, const Work &ws, const u
       }
     }
     const int r0 = p0 & 31;
-    for (int q = tid; q < np * k; q += nthr) {
+    for (int q = tid; q < (step4 ? np * k : 0); q += nthr) {
       const int j = q / k, jj = q - j * k, t = p0 + j;
       int slot = -1;
-      if (ok && gt.fr[j]) {
+      if (gt.fr[j] || dry) {
         const int e = gt.sel[j * 16 + jj];
         const int ci = (e >= 0 && e < E) ? (force ? e : gt.cidx[e]) : -1;
         if (ci < 0 || ci >= n_cand || cand_of(ci) != e) {
