@@ -331,7 +331,9 @@ epoch_status epoch_block_end(epoch_layer *layer);
  * EPOCH_OK when clear, EPOCH_ETIMEOUT if the timeout bit is set, else EPOCH_EDEVICE. */
 epoch_status epoch_get_status(epoch_layer *layer, epoch_stream stream, uint32_t *word_out);
 
-/* Clears the device error word (enqueued on the stream). */
+/* Clears the device error word and resets the gate's grid-barrier counter
+ * (enqueued on the stream). After a timeout, clear the status before the next
+ * call: a call that timed out may leave the barrier part-way. */
 epoch_status epoch_clear_status(epoch_layer *layer, epoch_stream stream);
 
 /* Copies the last iteration's statistics to host memory (synchronises the

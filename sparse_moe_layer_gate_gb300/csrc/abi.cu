@@ -445,7 +445,11 @@ epoch_status epoch_get_status(epoch_layer *L, epoch_stream stream, uint32_t *wor
 
 epoch_status epoch_clear_status(epoch_layer *L, epoch_stream stream) {
   if (L == nullptr) return EPOCH_EINVAL;
-  return cudaMemsetAsync(L->ws.err, 0, sizeof(uint32_t), S(stream)) == cudaSuccess ? EPOCH_OK : EPOCH_ECUDA;
+  // the gate's grid barrier too: a call that timed out may leave it part-way
+  return cudaMemsetAsync(L->ws.err, 0, sizeof(uint32_t), S(stream)) == cudaSuccess &&
+                 cudaMemsetAsync(L->ws.gate_arrive, 0, 2 * sizeof(int32_t), S(stream)) == cudaSuccess
+             ? EPOCH_OK
+             : EPOCH_ECUDA;
 }
 
 epoch_status epoch_read_stats(epoch_layer *L, epoch_iter_stats *out, epoch_stream stream) {

@@ -9,10 +9,10 @@
 // expert e's words: fresh position t selected e), and the dispatch copies each
 // fresh position's row of x into its k worklist rows.
 //
-// Every CTA owns a run of positions [p0, p0 + TPC). Before the grid barrier it
-// starts bulk copies of its fresh positions' x rows into shared memory and
-// adds its positions' category counts to the iteration tallies. After the
-// barrier it reads the candidate experts' words once (the block support, or
+// Every CTA owns a run of positions [p0, p0 + TPC). Once it has arrived at
+// the grid barrier it starts bulk copies of its fresh positions' x rows into
+// shared memory and adds its positions' category counts to the iteration
+// tallies. After the barrier it reads the candidate experts' words once (the block support, or
 // every expert on a fallback) and gets, per candidate, its rows in the whole
 // iteration and its set bits before p0, plus the words that cover its own
 // positions. The expert offsets follow from one scan over expert ids; the row
@@ -45,7 +45,7 @@ struct GateTail {
   const int16_t *cidx;  // [E] candidate index of an expert (valid where cand[cidx[e]] == e)
   int ncand;            // candidates of the plan
   uint32_t x_bar;       // mbarrier of the staged x rows (phase 0)
-  int gen0;             // the grid barrier's generation word, read at the kernel's start
+  int gen0;             // the grid barrier's arrival count when the call began (read at the kernel's start)
 };
 
 // Shared-memory bytes of the tail's scratch in the operand ring: staged x
@@ -84,13 +84,28 @@ __device__ __forceinline__ void gate_tail(const Dims &d, const Work &ws, const u
   int32_t *s_misc = s_slot + tpc * k;  // 36 bits before p0, 40 barrier passed
   auto cand_of = [&](int ci) { return force ? ci : static_cast<int>(gt.cand[ci]); };
 
-  // ---- 1. before the grid barrier
+  // ---- 1. arrive at the grid barrier over the gate's CTAs, then, while it
+  // fills: zero the scratch, add the own positions' category counts to the
+  // iteration tallies and start bulk copies of the own fresh positions' x rows
+  // into the ring. All gate CTAs are resident (one wave of clusters, and no
+  // later kernel starts before every gate CTA has). The arrival counter only
+  // grows: this call's CTAs wait until it has grown by the grid size from the
+  // value it had when the call began (gt.gen0, set by the previous call's CTA 0
+  // once its barrier had passed, so it cannot move before every CTA of this
+  // call has arrived). Bounded.
+  __syncthreads();  // every warp's selections and words are written
+  unsigned arrived_raw = 0;
+  if (tid == 0) {
+    // release: this CTA's selections and words; acquire (the last CTA, which
+    // does not wait): every other CTA's
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(arrived_raw) : "l"(ws.gate_arrive) : "memory");
+  }
   for (int e = tid; e <= E; e += nthr) s_off[e] = 0;
   for (int c = tid; c < n_cand; c += nthr) {
     s_bef[c] = 0;
     s_own[3 * c] = s_own[3 * c + 1] = s_own[3 * c + 2] = 0u;
   }
-  if (tid < 48) s_misc[tid] = 0;
+  if (tid < 48 && tid != 41) s_misc[tid] = 0;
   if (wid == 0) {  // the own positions' categories, for the statistics
     int cnt[kTallies] = {0, 0, 0, 0, 0, 0, 0, 0};
     for (int j = lane; j < np; j += 32) {
@@ -115,22 +130,7 @@ __device__ __forceinline__ void gate_tail(const Dims &d, const Work &ws, const u
     for (int j = 0; j < np; ++j)
       if (gt.fr[j]) bulk_load(smem_u32(xs + j * rowb), x + static_cast<size_t>(p0 + j) * rowb, rowb, gt.x_bar, pol);
   }
-  __syncthreads();
-  // Grid barrier over the gate's CTAs (all resident: one wave of clusters, and
-  // no later kernel starts before every gate CTA has). Self-resetting: the
-  // last CTA to arrive advances the generation word the others wait on, and
-  // CTA 0 zeroes the arrival count once it has passed. Bounded.
-  if (tid == 0) {
-    // (the generation read at the kernel's start cannot have moved: the barrier
-    // is released only after this CTA has arrived)
-    int arrived;
-    // release: this CTA's selections, words and tallies; acquire (the last
-    // CTA): every other CTA's, before it releases the rest
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(arrived) : "l"(ws.gate_arrive) : "memory");
-    if (arrived == static_cast<int>(gridDim.x) - 1)
-      asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(ws.gate_arrive + 1), "r"(gt.gen0 + 1) : "memory");
-    s_misc[41] = arrived;
-  }
+  if (tid == 0) s_misc[41] = static_cast<int>(arrived_raw - static_cast<unsigned>(gt.gen0));  // arrival order
   __syncthreads();
   const int arrived = s_misc[41];
   const bool last = arrived == static_cast<int>(gridDim.x) - 1;
@@ -156,9 +156,9 @@ __device__ __forceinline__ void gate_tail(const Dims &d, const Work &ws, const u
         if (!last) {
           const uint64_t t0 = globaltimer_ns();
           for (;;) {
-            int v;
-            asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ws.gate_arrive + 1) : "memory");
-            if (v != gt.gen0) break;
+            unsigned v;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ws.gate_arrive) : "memory");
+            if (static_cast<int>(v - static_cast<unsigned>(gt.gen0)) >= static_cast<int>(gridDim.x)) break;
             if (globaltimer_ns() - t0 > static_cast<uint64_t>(d.timeout_ns)) {
               set_error(ws.err, EPOCH_DEVERR_TIMEOUT);
               pass_ok = 0;
@@ -167,7 +167,8 @@ __device__ __forceinline__ void gate_tail(const Dims &d, const Work &ws, const u
             __nanosleep(64);
           }
         }
-        if (pass_ok && blockIdx.x == 0) ws.gate_arrive[0] = 0;
+        if (pass_ok && blockIdx.x == 0)  // the next call's starting count (modulo 2^32)
+          ws.gate_arrive[1] = static_cast<int32_t>(static_cast<unsigned>(gt.gen0) + gridDim.x);
         s_misc[40] = pass_ok;
         if (trace) trace[1] = static_cast<int64_t>(globaltimer_ns());
       }

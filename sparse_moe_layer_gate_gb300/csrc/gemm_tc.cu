@@ -160,7 +160,7 @@ __global__ void __maxnreg__(104) k_tc_gate(const __grid_constant__ GateParams p)
   uint2 *s_scr = reinterpret_cast<uint2 *>(s_stamp + 64);  // [warps][32] top-k scratch
   // for the worklist tail (gate_tail.cuh)
   uint64_t *x_barp = reinterpret_cast<uint64_t *>(s_scr + 32 * (kGateThreads / 32));  // staged x rows
-  int *s_ncand = reinterpret_cast<int *>(x_barp + 1);      // [0] candidates, [1] barrier generation
+  int *s_ncand = reinterpret_cast<int *>(x_barp + 1);      // [0] candidates, [1] barrier count at the start
   uint8_t *s_fr = reinterpret_cast<uint8_t *>(s_ncand + 2);  // [64] own position fresh
   int16_t *s_sel = reinterpret_cast<int16_t *>(s_fr + 64);   // [64][16] its selected experts
   int16_t *s_cand = s_sel + 64 * 16;                         // [1024] candidate experts
@@ -292,7 +292,7 @@ __global__ void __maxnreg__(104) k_tc_gate(const __grid_constant__ GateParams p)
         const int nc = ws.ctrl->support_len;
         if (tid == 64) {
           s_ncand[0] = nc;
-          s_ncand[1] = *reinterpret_cast<volatile const int32_t *>(ws.gate_arrive + 1);  // barrier generation
+          s_ncand[1] = *reinterpret_cast<volatile const int32_t *>(ws.gate_arrive + 1);  // barrier count at the start
         }
         for (int i = tid - 64; i < d.E; i += kGateThreads - 64) {
           const int e = ws.support_ids[i];

@@ -63,8 +63,9 @@ struct Work {
                           // classifying kernel of the iteration)
   int32_t *tally;         // [8] the gate tail's per-iteration counts (categories, bad flags, fresh),
                           // added by every gate CTA, read and zeroed by CTA 0
-  int32_t *gate_arrive;   // grid barrier of the gate before the worklist: [0] CTAs arrived (zeroed by
-                          // CTA 0 once it has passed), [1] generation (advanced by the last to arrive)
+  int32_t *gate_arrive;   // grid barrier of the gate before the worklist: [0] arrivals (only grows,
+                          // modulo 2^32), [1] its value when the next call begins (set by CTA 0 once
+                          // the barrier has passed); both zeroed by the plan and by clearing the status
   int32_t *sh_ctr;        // shared-expert tiles, [sh_stride]: [0] next tile, then the finished up
                           // tiles of each (shared expert, token tile); zeroed by each call's combine
                           // for the next call

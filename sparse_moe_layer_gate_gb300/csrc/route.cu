@@ -43,6 +43,7 @@ __device__ void clear_block_state(const Dims &d, const Work &ws) {
   for (int q = threadIdx.x; q < 2 * d.E * d.cmax; q += blockDim.x) ws.sel_words[q] = 0u;
   if (threadIdx.x == 0) {
     ws.gate_arrive[0] = 0;
+    ws.gate_arrive[1] = 0;
     *ws.cov_under = 0;
   }
   if (threadIdx.x < 8) ws.tally[threadIdx.x] = 0;
