@@ -344,8 +344,9 @@ __global__ void __maxnreg__(104) k_tc_gate(const __grid_constant__ GateParams p)
   const bool vec_out = (d.E & 3) == 0;
   // units of 4 experts x 1 position, kGateBatch per thread at a time: every
   // rank's partials of a batch are requested before any is summed (one round
-  // trip over the cluster per batch)
-  constexpr int kGateBatch = 2;
+  // trip over the cluster per batch). One unit a time: the loop runs once per
+  // iteration, cold, so short code beats the second unit's overlap.
+  constexpr int kGateBatch = 1;
   const int n_units = TPC * e4n;
   for (int u0 = tid; u0 < n_units; u0 += kGateBatch * blockDim.x) {
     float4 v[kGateBatch][8];
