@@ -49,10 +49,10 @@ class L2Flush:
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one expert-kernel
 # launch: the ncu capture of iteration 20 of the accounting block
-# (profiles/experts_llada2_mini.md: 231.9 MB read, 3.6 MB written; every
+# (profiles/experts_llada2_mini.md: 231.9 MB read, 3.5 MB written; every
 # iteration of this workload hits the same 34 routed experts), tied to the
 # source it was measured on (reported as null once that source changes).
-TRAFFIC = {"experts": {"bytes_per_launch": 235.55e6, "source_sha": "4e06f643634539bd"}}
+TRAFFIC = {"experts": {"bytes_per_launch": 235.48e6, "source_sha": "b0d7c7cf299aa28d"}}
 
 
 def parse():
