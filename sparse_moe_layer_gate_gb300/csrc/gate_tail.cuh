@@ -81,7 +81,7 @@ __device__ __forceinline__ void gate_tail(const Dims &d, const Work &ws, const u
   int32_t *s_bef = s_off + ((E + 4) & ~3);                                      // [E] by candidate
   uint32_t *s_own = reinterpret_cast<uint32_t *>(s_bef + E);                    // [E][3] by candidate
   int32_t *s_slot = reinterpret_cast<int32_t *>(s_own + 3 * E);                 // [tpc * k]
-  int32_t *s_misc = s_slot + tpc * k;  // 36 bits before p0, 40 barrier passed
+  int32_t *s_misc = s_slot + tpc * k;  // 36 bits before p0, 40 barrier passed, 41 arrival order
   auto cand_of = [&](int ci) { return force ? ci : static_cast<int>(gt.cand[ci]); };
 
   // ---- 1. arrive at the grid barrier over the gate's CTAs, then, while it
