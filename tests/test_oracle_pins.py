@@ -342,6 +342,30 @@ def test_iteration_invariants():
         prev_dec = dec
 
 
+def test_block_outputs_equal_restricted_moe_at_each_rows_last_refresh():
+    """Every output of a block, reused rows included: y_i[t] is the restricted
+    MoE of the support evaluated on x at the iteration t was last fresh, plus
+    the shared expert on x_i ([W] "Liveness-Shard Parallelism", merge
+    equations), with both sides written out independently of the oracle by
+    masked_dense."""
+    k, R = 2, 3
+    lay, plan, hist, (wr, b, experts, shared) = run_random_block(k=k, R=R)
+    elig = lay.support_mask  # the block's support (no hot update in this block)
+    routed_at = {}
+    n_reused = 0
+    for i, dec, x, res, stamp in hist:
+        routed_now = masked_dense(x, wr, b, experts, k, (), eligible=elig)
+        shared_now = masked_dense(x, wr, b, experts, k, shared, eligible=elig) - routed_now
+        fresh = set(res.fresh_pos.tolist())
+        for t in range(x.shape[0]):
+            if t in fresh:
+                routed_at[t] = routed_now[t]
+            else:
+                n_reused += 1
+            np.testing.assert_allclose(res.y[t], routed_at[t] + shared_now[t], rtol=1e-11, atol=1e-11)
+    assert n_reused > 0
+
+
 def test_support_equal_k_selects_whole_support():
     lay, wr, b, experts, shared = tiny_layer(E=9, H=5, I=4, k=3, tau=0.05, R=2, seed=21,
                                              max_positions=10)
